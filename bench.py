@@ -1,0 +1,435 @@
+#!/usr/bin/env python3
+"""Benchmark: fused GEMM + ReduceScatter throughput on one GB300.
+
+One step is one fcc_gemm_rs call on the row-parallel MLP down-projection
+workload (8 ranks, A_r 8192x3584, B_r 3584x8192, bf16 shards of 1024x8192),
+inputs resident in HBM.  The inputs (940 MB) are larger than L2, so no flush is
+needed between steps.  Prints ONE JSON line on rank 0.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl fcc|reference]
+
+Under torchrun (N > 1) every rank runs an independent replica of the same
+workload on its own GPU (the path has no exchange between GPUs), with a barrier
+and synchronisation around the timed region and the max time over ranks.
+
+--impl reference times the fp64 CPU oracle on the host cores on a bounded
+sample of the same workload (the reference arm).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = ("fused GEMM+RS TFLOP/s and % roofline at 1 GB300 vs unfused baseline and CPU "
+          "oracle")
+WORKLOAD = "gemm_rs_r8_8192x8192x3584"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="fcc", choices=["fcc", "reference"])
+    ap.add_argument("--headline-only", action="store_true",
+                    help="skip the unfused baselines and the other operators")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0,
+                    help="target CPU time of the oracle sample (cpu_baseline)")
+    ap.add_argument("--ref-seconds", type=float, default=90.0,
+                    help="target CPU time of the whole --impl reference run")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ helpers
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 100 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t_start = self.t_stop = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self._t = threading.Thread(target=self._read, daemon=True)
+        self._t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark_start(self):
+        self.t_start = time.time()
+
+    def mark_stop(self):
+        self.t_stop = time.time()
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        rows = [l for (t, l) in self.lines
+                if self.t_start is not None and self.t_start <= t <= (self.t_stop or t)]
+        if not rows:
+            rows = [l for (_, l) in self.lines]
+        sm, smax, reasons = [], [], set()
+        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        for r in rows:
+            parts = [p.strip() for p in r.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names[1:], parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def kernel_traffic(kernel: str, src_files):
+    """Per-launch DRAM bytes from a committed ncu summary, if the kernel source is unchanged."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}.traffic.txt")
+    if not os.path.exists(path):
+        return None
+    vals = {}
+    with open(path) as f:
+        for line in f:
+            if "=" in line and not line.startswith("#"):
+                k, v = line.split("=", 1)
+                vals[k.strip()] = v.strip()
+    h = hashlib.sha256()
+    for s in src_files:
+        with open(os.path.join(ROOT, s), "rb") as f:
+            h.update(f.read())
+    if vals.get("source_sha256") != h.hexdigest():
+        return None
+    try:
+        return float(vals["bytes_per_launch_full"])
+    except (KeyError, ValueError):
+        return None
+
+
+# ------------------------------------------------------------- distributed
+def dist_setup(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if _cuda_ok() else "gloo"
+        dist.init_process_group(backend=backend)
+        pg = dist
+    return world, rank, local, pg
+
+
+def _cuda_ok():
+    try:
+        import torch
+        return torch.cuda.is_available()
+    except Exception:
+        return False
+
+
+def max_over_ranks(x: float, pg) -> float:
+    if pg is None:
+        return x
+    import torch
+    dev = "cuda" if _cuda_ok() else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(pg):
+    if pg is not None:
+        pg.barrier()
+
+
+# --------------------------------------------------------------- oracle leg
+def oracle_seconds_per_row(A, B):
+    """Calibrate: oracle seconds per output row (one row per thread, all threads)."""
+    import numpy as np
+    import oracle
+    oracle.build()
+    threads = oracle.num_threads()
+    t0 = time.perf_counter()
+    oracle.rank_sum(A, B, np.arange(threads, dtype=np.int64))
+    return (time.perf_counter() - t0) / threads, threads
+
+
+def oracle_sample(A, B, R, M, rows_per_shard: int, seed: int = 1234, gpu_shards=None):
+    """Time the fp64 oracle on `rows_per_shard` seeded rows of every shard.
+
+    The oracle's reduce-scatter output row i of shard j is row j*M/R + i of the
+    rank sum; all sampled rows go to one (thread-parallel) oracle call.
+    Returns (tflops, seconds, rows, check); check is the worst relative
+    Frobenius error of the GPU rows against the oracle rows (if given)."""
+    import numpy as np
+    import oracle
+    K = A[0].shape[1]
+    N = B[0].shape[1]
+    Ms = M // R
+    rng = np.random.Generator(np.random.PCG64(seed))
+    sel = [np.sort(rng.choice(Ms, size=rows_per_shard, replace=False)).astype(np.int64)
+           for _ in range(R)]
+    rows = np.concatenate([j * Ms + s for j, s in enumerate(sel)])
+    t0 = time.perf_counter()
+    ref = oracle.rank_sum(A, B, rows)
+    secs = time.perf_counter() - t0
+    flops = 2.0 * rows.size * N * K * R
+    check = None
+    if gpu_shards is not None:
+        worst = 0.0
+        for j in range(R):
+            got = gpu_shards[j][sel[j]]
+            r = ref[j * rows_per_shard:(j + 1) * rows_per_shard]
+            worst = max(worst, float(np.linalg.norm(got - r) / np.linalg.norm(r)))
+        check = worst
+    return flops / secs / 1e12, secs, int(rows.size), check
+
+
+# -------------------------------------------------------------------- arms
+def run_reference(args, world, rank, pg):
+    if rank != 0:
+        return
+    import synth
+    w = synth.WORKLOADS[WORKLOAD]
+    A, B = synth.gemm_inputs(w.R, w.M, w.N, w.K, w.std_a, w.std_b, seed=0)
+    # The whole run gets about args.ref_seconds of CPU time, spread over all steps.
+    per_row, threads = oracle_seconds_per_row(A, B)
+    per_step = args.ref_seconds / max(1, args.steps + args.warmup)
+    rows_per_shard = int(max(1, min(w.M // w.R, per_step / max(per_row * w.R, 1e-9))))
+    vals = []
+    rows = 0
+    for i in range(args.warmup + args.steps):
+        v, secs, rows, _ = oracle_sample(A, B, w.R, w.M, rows_per_shard, seed=i)
+        if i >= args.warmup:
+            vals.append((v, secs))
+    total_flops = sum(v * s for v, s in vals) * 1e12
+    total_s = sum(s for _, s in vals)
+    value = total_flops / total_s / 1e12
+    sample = (f"{rows} output rows per step ({rows_per_shard} per shard, seeded choice) of "
+              f"the {WORKLOAD} workload; each row is the full R*K-term sum over 8192 columns")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total_s / len(vals), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "R": w.R, "M": w.M, "N": w.N, "K": w.K,
+                   "out": "f64", "parallelism": f"replicas{args.gpus}"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def time_calls(fn, steps, warmup, stream):
+    import torch
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    s = torch.cuda.Event(enable_timing=True)
+    e = torch.cuda.Event(enable_timing=True)
+    s.record(stream)
+    for _ in range(steps):
+        fn()
+    e.record(stream)
+    torch.cuda.synchronize()
+    return s.elapsed_time(e) / steps  # ms
+
+
+def run_fcc(args, world, rank, local, pg):
+    import numpy as np
+    import torch
+    import gemm_collective_gb300 as fcc
+    import synth
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+    pk, pk_src = peaks()
+    w = synth.WORKLOADS[WORKLOAD]
+    R, M, N, K = w.R, w.M, w.N, w.K
+    flops = w.flops()
+    A, B = synth.gemm_inputs(R, M, N, K, w.std_a, w.std_b, seed=0)
+
+    def up(a):
+        return torch.from_numpy(a.view(np.int16)).to(dev)
+
+    dA = [up(a) for a in A]
+    dB = [up(b) for b in B]
+    outs = [torch.empty((M // R, N), dtype=torch.bfloat16, device=dev) for _ in range(R)]
+
+    def step():
+        fcc.fcc_gemm_rs(R, dA, dB, outs, M, N, K, fcc.FCC_BF16, fcc.FCC_BF16, None, stream)
+
+    # ---- headline: device-resident inputs
+    clocks = ClockSampler(local)
+    clocks.start()
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    time.sleep(0.3)  # let the sampler come up
+    barrier(pg)
+    torch.cuda.synchronize()
+    l0 = fcc.fcc_launch_count()
+    s_ev = torch.cuda.Event(enable_timing=True)
+    e_ev = torch.cuda.Event(enable_timing=True)
+    clocks.mark_start()
+    s_ev.record(stream)
+    for _ in range(args.steps):
+        step()
+    e_ev.record(stream)
+    torch.cuda.synchronize()
+    clocks.mark_stop()
+    barrier(pg)
+    launches = fcc.fcc_launch_count() - l0
+    ms_local = s_ev.elapsed_time(e_ev) / args.steps
+    clocks.stop()
+    st = fcc.fcc_stream_status(stream)
+    if st != fcc.FCC_OK:
+        raise RuntimeError(f"device status after the timed region: {fcc.fcc_status_string(st)}")
+    ms = max_over_ranks(ms_local, pg)
+    value = world * flops / (ms * 1e-3) / 1e12
+
+    # ---- roofline of the (only) kernel of the step
+    timed_s = ms_local * args.steps * 1e-3
+    sustained = timed_s >= 0.5
+    peak = pk["bf16_tflops_sustained"] if sustained else pk["bf16_tflops"]
+    achieved = flops / (ms_local * 1e-3) / 1e12
+    traffic = kernel_traffic("gemm_rs_fused", ["gemm_collective_gb300/csrc/fcc_gemm.cu",
+                                                "gemm_collective_gb300/csrc/fcc_ptx.cuh"])
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": traffic,
+                "peak_source": f"{pk_src} {'sustained' if sustained else 'burst'} bf16",
+                "kernel": "gemm_kernel<MODE_RS>",
+                "algorithmic_bytes_per_launch": float(R * (M * K + K * N) * 2 + M * N * 2)}
+
+    # ---- e2e: host buffers, copies inside the timed region
+    hA = [torch.from_numpy(a.view(np.int16)).pin_memory() for a in A]
+    hB = [torch.from_numpy(b.view(np.int16)).pin_memory() for b in B]
+    hO = [torch.empty((M // R, N), dtype=torch.bfloat16).pin_memory() for _ in range(R)]
+    h2d = sum(t.numel() * 2 for t in hA + hB)
+    d2h = sum(t.numel() * 2 for t in hO)
+
+    def e2e_step():
+        for d, h in zip(dA + dB, hA + hB):
+            d.copy_(h, non_blocking=True)
+        step()
+        for h, d in zip(hO, outs):
+            h.copy_(d, non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 20))
+    barrier(pg)
+    e2e_ms = max_over_ranks(time_calls(e2e_step, e2e_steps, 3, stream), pg)
+    e2e = {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded PCG64 normals rounded to bf16)",
+        "config": {"workload": WORKLOAD, "R": R, "M": M, "N": N, "K": K, "out": "bf16",
+                   "algo": "fused, ordered tile-owner accumulation",
+                   "l2": "inputs (940 MB) larger than L2; no flush",
+                   "parallelism": f"replicas{world}"},
+        "roofline": roofline, "e2e": e2e, "gpu_launches": launches,
+        "clocks": clocks.summary(),
+    }
+
+    # ---- unfused baselines and cuBLAS on the same workload
+    if not args.headline_only:
+        base = {}
+        for name, o in [("unfused", fcc.make_opts(algo=fcc.FCC_ALGO_UNFUSED)),
+                        ("interdecom", fcc.make_opts(algo=fcc.FCC_ALGO_INTERDECOM)),
+                        ("copy_engine", fcc.make_opts(algo=fcc.FCC_ALGO_CE)),
+                        ("fused_push", fcc.make_opts(algo=fcc.FCC_ALGO_FUSED, deterministic=0))]:
+            f = (lambda o=o: fcc.fcc_gemm_rs(R, dA, dB, outs, M, N, K, 0, 0, o, stream))
+            t = time_calls(f, 20, 3, stream)
+            base[name] = {"ms": t, "TFLOP/s": flops / (t * 1e-3) / 1e12}
+        Acat = torch.cat([a.view(torch.bfloat16) for a in dA], dim=1)
+        Bcat = torch.cat([b.view(torch.bfloat16) for b in dB], dim=0)
+        t = time_calls(lambda: torch.matmul(Acat, Bcat), 20, 3, stream)
+        base["cublas_stacked_gemm"] = {"ms": t, "TFLOP/s": flops / (t * 1e-3) / 1e12,
+                                       "note": "one library GEMM of the same FLOPs, no collective"}
+        del Acat, Bcat
+        line["baselines"] = base
+
+    # ---- CPU oracle on a bounded sample (rank 0 only)
+    if rank == 0:
+        got = [o.float().cpu().numpy().astype(np.float64) for o in outs]
+        per_row, threads = oracle_seconds_per_row(A, B)
+        rps = int(max(1, min(M // R, args.cpu_seconds / max(per_row * R, 1e-9))))
+        v, secs, rows, chk = oracle_sample(A, B, R, M, rps, gpu_shards=got)
+        line["cpu_baseline"] = {
+            "value": v, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": f"{rows} output rows ({rows // R} per shard, seeded choice), "
+                      f"{secs:.1f} s of fp64 CPU work",
+            "gpu_rows_rel_fro_err": chk}
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    world, rank, local, pg = dist_setup(args.gpus)
+    try:
+        if args.impl == "reference":
+            run_reference(args, world, rank, pg)
+        else:
+            run_fcc(args, world, rank, local, pg)
+    finally:
+        if pg is not None:
+            pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,205 @@
+"""Python binding of libfcc (fused GEMM + collective on one GB300).
+
+A thin ctypes layer over the C ABI declared in ``include/fcc.h``: every
+function has the C name and argument order, and only marshals arguments
+(lists of device pointers or CUDA tensors, a stream, an options struct).
+All computation runs in the library's CUDA kernels.  Importing this module
+loads ``libfcc.so``; if the library has not been built the import fails
+loudly -- there is no fallback path.
+
+Pointer-array arguments accept a sequence of ``int`` device addresses or of
+objects with ``data_ptr()`` (torch tensors).  ``stream`` accepts ``None``
+(the legacy default stream), an ``int`` handle or an object with a
+``cuda_stream`` attribute (``torch.cuda.Stream``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libfcc.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"libfcc.so is not built ({LIB_PATH}); run gemm_collective_gb300/build.py "
+        "or __graft_entry__.build() first")
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+# ----------------------------------------------------------------- constants
+FCC_BF16, FCC_F16, FCC_F32 = 0, 1, 2
+(FCC_OK, FCC_ERR_INVALID, FCC_ERR_UNSUPPORTED, FCC_ERR_CUDA, FCC_ERR_CAPACITY,
+ FCC_ERR_TIMEOUT, FCC_ERR_WORKSPACE) = range(7)
+(FCC_ALGO_AUTO, FCC_ALGO_FUSED, FCC_ALGO_UNFUSED, FCC_ALGO_INTERDECOM,
+ FCC_ALGO_CE) = range(5)
+FCC_OP_GEMM_RS, FCC_OP_GEMM_AR, FCC_OP_GEMV_AR, FCC_OP_AG_GEMM = range(4)
+FCC_MAX_RANKS = 8
+FCC_MAX_EXPERTS = 64
+
+
+class fcc_opts(ctypes.Structure):
+    _fields_ = [
+        ("algo", ctypes.c_int),
+        ("deterministic", ctypes.c_int),
+        ("chunks", ctypes.c_int),
+        ("max_ctas", ctypes.c_int),
+        ("timeout_ns", ctypes.c_int64),
+        ("workspace", ctypes.c_void_p),
+        ("workspace_bytes", ctypes.c_size_t),
+    ]
+
+
+def make_opts(algo=FCC_ALGO_AUTO, deterministic=1, chunks=0, max_ctas=0, timeout_ns=0,
+              workspace=None, workspace_bytes=0) -> fcc_opts:
+    ws = workspace.data_ptr() if hasattr(workspace, "data_ptr") else workspace
+    return fcc_opts(algo, deterministic, chunks, max_ctas, timeout_ns, ws, workspace_bytes)
+
+
+class FccError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {fcc_status_string(status)} ({status})")
+
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_I64 = ctypes.c_int64
+_OPTS = ctypes.POINTER(fcc_opts)
+
+
+def _sig(name, res, args):
+    f = getattr(_lib, name)
+    f.restype = res
+    f.argtypes = args
+    return f
+
+
+_gemm_rs = _sig("fcc_gemm_rs", _I, [_I, _P, _P, _P, _I64, _I64, _I64, _I, _I, _OPTS, _P])
+_gemm_ar = _sig("fcc_gemm_ar", _I, [_I, _P, _P, _P, _I64, _I64, _I64, _I, _I, _OPTS, _P])
+_gemv_ar = _sig("fcc_gemv_ar", _I, [_I, _P, _P, _P, _I64, _I64, _I64, _I, _I, _OPTS, _P])
+_ag_gemm = _sig("fcc_ag_gemm", _I, [_I, _P, _P, _P, _P, _I64, _I64, _I64, _I, _I, _OPTS, _P])
+_moe = _sig("fcc_moe_dispatch_gemm", _I,
+            [_I, _P, _P, _P, _I64, _I64, _I64, _I, _I, _P, _P, _I64, _P, _P, _P, _P, _P, _I, _I,
+             _OPTS, _P])
+_ws = _sig("fcc_workspace_size", ctypes.c_size_t, [_I, _I, _I64, _I64, _I64, _OPTS])
+_moe_ws = _sig("fcc_moe_workspace_size", ctypes.c_size_t,
+               [_I, _I64, _I64, _I64, _I, _I, _I64, _OPTS])
+_stream_status = _sig("fcc_stream_status", _I, [_P])
+_status_string = _sig("fcc_status_string", ctypes.c_char_p, [_I])
+_chunks = _sig("fcc_interdecom_chunks", _I, [ctypes.c_double, ctypes.c_double,
+                                              ctypes.c_double, _I])
+_itime = _sig("fcc_interdecom_time", ctypes.c_double, [ctypes.c_double, ctypes.c_double,
+                                                       ctypes.c_double, _I])
+_launches = _sig("fcc_launch_count", ctypes.c_uint64, [])
+_version = _sig("fcc_version", ctypes.c_char_p, [])
+_wait_timeout = _sig("fcc_test_wait_timeout", _I, [_I64, _P])
+
+
+# ---------------------------------------------------------------- marshalling
+def _addr(x) -> int:
+    if x is None:
+        return 0
+    if hasattr(x, "data_ptr"):
+        return int(x.data_ptr())
+    return int(x)
+
+
+def _ptrs(seq):
+    if seq is None:
+        return None
+    vals = [_addr(x) for x in seq]
+    return (ctypes.c_void_p * len(vals))(*vals)
+
+
+def _stream(s) -> int:
+    if s is None:
+        return 0
+    if hasattr(s, "cuda_stream"):
+        return int(s.cuda_stream)
+    return int(s)
+
+
+def _opts(o):
+    return ctypes.byref(o) if o is not None else None
+
+
+def _check(st: int, where: str):
+    if st != FCC_OK:
+        raise FccError(st, where)
+
+
+# ------------------------------------------------------------------ the calls
+def fcc_gemm_rs(R, A, B, out_shard, M, N, K, in_dtype=FCC_BF16, out_dtype=FCC_BF16, opts=None,
+                stream=None):
+    _check(_gemm_rs(R, _ptrs(A), _ptrs(B), _ptrs(out_shard), M, N, K, in_dtype, out_dtype,
+                    _opts(opts), _stream(stream)), "fcc_gemm_rs")
+
+
+def fcc_gemm_ar(R, A, B, out, M, N, K, in_dtype=FCC_BF16, out_dtype=FCC_BF16, opts=None,
+                stream=None):
+    _check(_gemm_ar(R, _ptrs(A), _ptrs(B), _ptrs(out), M, N, K, in_dtype, out_dtype,
+                    _opts(opts), _stream(stream)), "fcc_gemm_ar")
+
+
+def fcc_gemv_ar(R, A, B, out, M, N, K, in_dtype=FCC_BF16, out_dtype=FCC_F32, opts=None,
+                stream=None):
+    _check(_gemv_ar(R, _ptrs(A), _ptrs(B), _ptrs(out), M, N, K, in_dtype, out_dtype,
+                    _opts(opts), _stream(stream)), "fcc_gemv_ar")
+
+
+def fcc_ag_gemm(R, X_shard, B, out, gathered, M, N, K, in_dtype=FCC_BF16, out_dtype=FCC_BF16,
+                opts=None, stream=None):
+    _check(_ag_gemm(R, _ptrs(X_shard), _ptrs(B), _ptrs(out), _ptrs(gathered), M, N, K,
+                    in_dtype, out_dtype, _opts(opts), _stream(stream)), "fcc_ag_gemm")
+
+
+def fcc_moe_dispatch_gemm(R, X, logits, W, T, H, F, E, topk, recv_x, recv_y, cap, topk_idx,
+                          topk_gate, expert_counts, send_counts, recv_src, in_dtype=FCC_BF16,
+                          out_dtype=FCC_BF16, opts=None, stream=None):
+    _check(_moe(R, _ptrs(X), _ptrs(logits), _ptrs(W), T, H, F, E, topk, _ptrs(recv_x),
+                _ptrs(recv_y), cap, _ptrs(topk_idx), _ptrs(topk_gate), _addr(expert_counts),
+                _addr(send_counts), _ptrs(recv_src), in_dtype, out_dtype, _opts(opts),
+                _stream(stream)), "fcc_moe_dispatch_gemm")
+
+
+def fcc_workspace_size(op, R, M, N, K, opts=None) -> int:
+    return int(_ws(op, R, M, N, K, _opts(opts)))
+
+
+def fcc_moe_workspace_size(R, T, H, F, E, topk, cap, opts=None) -> int:
+    return int(_moe_ws(R, T, H, F, E, topk, cap, _opts(opts)))
+
+
+def fcc_stream_status(stream=None) -> int:
+    """Synchronise the stream; return (and clear) the device status word."""
+    return int(_stream_status(_stream(stream)))
+
+
+def fcc_status_string(status: int) -> str:
+    return _status_string(status).decode()
+
+
+def fcc_interdecom_chunks(G: float, X: float, alpha: float, max_chunks: int) -> int:
+    return int(_chunks(G, X, alpha, max_chunks))
+
+
+def fcc_interdecom_time(G: float, X: float, alpha: float, chunks: int) -> float:
+    return float(_itime(G, X, alpha, chunks))
+
+
+def fcc_launch_count() -> int:
+    return int(_launches())
+
+
+def fcc_version() -> str:
+    return _version().decode()
+
+
+def fcc_test_wait_timeout(timeout_ns: int, stream=None):
+    _check(_wait_timeout(timeout_ns, _stream(stream)), "fcc_test_wait_timeout")
+
+
+def raw_status(fn_name: str, *args) -> int:
+    """Call a C entry point with already-marshalled ctypes arguments; return its status."""
+    return int(getattr(_lib, fn_name)(*args))

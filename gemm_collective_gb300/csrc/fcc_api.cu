@@ -1,0 +1,691 @@
+// fcc_api.cu -- the C ABI of libfcc: argument checks, tensor maps, workspace,
+// algorithm selection (fused / unfused / InterDecom / copy engine) and the
+// device status word.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "fcc.h"
+#include "fcc_internal.h"
+
+namespace fcc {
+
+// Device status word: kernels record the first device-side error here.
+__device__ int g_status_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr unsigned long long kDefaultTimeoutNs = 1000ull * 1000 * 1000;  // 1 s
+constexpr int kGemmBN = 256;
+constexpr int kMaxChunks = 64;
+constexpr int kSideStreams = 4;
+
+std::atomic<uint64_t> g_launches{0};
+std::mutex g_mu;
+
+struct DeviceState {
+  bool init = false;
+  int sms = 0;
+  int* status = nullptr;
+  void* pool = nullptr;
+  size_t pool_bytes = 0;
+  cudaStream_t side[kSideStreams] = {};
+  cudaEvent_t ev[kMaxChunks + kSideStreams + 2] = {};
+};
+DeviceState g_dev[kMaxDevices];
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+fcc_status cuda_fail(cudaError_t e) { return e == cudaSuccess ? FCC_OK : FCC_ERR_CUDA; }
+
+fcc_status device_state(DeviceState** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FCC_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceState& d = g_dev[dev];
+  if (!d.init) {
+    if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return FCC_ERR_CUDA;
+    if (cudaGetSymbolAddress(reinterpret_cast<void**>(&d.status), g_status_word) != cudaSuccess)
+      return FCC_ERR_CUDA;
+    for (int i = 0; i < kSideStreams; ++i)
+      if (cudaStreamCreateWithFlags(&d.side[i], cudaStreamNonBlocking) != cudaSuccess)
+        return FCC_ERR_CUDA;
+    for (auto& e : d.ev)
+      if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return FCC_ERR_CUDA;
+    if (g_encode == nullptr) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                           &q) != cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || fn == nullptr)
+        return FCC_ERR_CUDA;
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+    d.init = true;
+  }
+  *out = &d;
+  return FCC_OK;
+}
+
+// 2-D bf16 tensor map over a row-major [rows, cols] matrix, box [box_rows, 64],
+// 128-byte swizzle, zero fill out of bounds.
+fcc_status make_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols,
+                    uint32_t box_rows) {
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FCC_OK : FCC_ERR_CUDA;
+}
+
+bool aligned16(const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool ptrs_ok(const void* const* arr, int n) {
+  if (arr == nullptr) return false;
+  for (int i = 0; i < n; ++i)
+    if (!aligned16(arr[i])) return false;
+  return true;
+}
+
+unsigned long long timeout_of(const fcc_opts* o) {
+  return (o != nullptr && o->timeout_ns > 0) ? static_cast<unsigned long long>(o->timeout_ns)
+                                              : kDefaultTimeoutNs;
+}
+
+fcc_algo algo_of(const fcc_opts* o) {
+  if (o == nullptr || o->algo == FCC_ALGO_AUTO) return FCC_ALGO_FUSED;
+  return o->algo;
+}
+
+bool deterministic_of(const fcc_opts* o) { return o == nullptr || o->deterministic != 0; }
+
+int grid_for(const DeviceState* d, const fcc_opts* o, int64_t units) {
+  int g = d->sms;
+  if (o != nullptr && o->max_ctas > 0) g = std::min(g, o->max_ctas);
+  if (units < g) g = static_cast<int>(std::max<int64_t>(units, 1));
+  return g;
+}
+
+size_t align_up(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+// Workspace: the caller's, else the internal pool (grown with cudaMalloc).
+fcc_status get_workspace(DeviceState* d, const fcc_opts* o, size_t bytes, void** out) {
+  *out = nullptr;
+  if (bytes == 0) return FCC_OK;
+  if (o != nullptr && o->workspace != nullptr) {
+    if (o->workspace_bytes < bytes || !aligned16(o->workspace)) return FCC_ERR_WORKSPACE;
+    *out = o->workspace;
+    return FCC_OK;
+  }
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (d->pool_bytes < bytes) {
+    if (d->pool != nullptr) {
+      if (cudaFree(d->pool) != cudaSuccess) return FCC_ERR_CUDA;
+      d->pool = nullptr;
+      d->pool_bytes = 0;
+    }
+    if (cudaMalloc(&d->pool, bytes) != cudaSuccess) return FCC_ERR_CUDA;
+    d->pool_bytes = bytes;
+  }
+  *out = d->pool;
+  return FCC_OK;
+}
+
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Common GEMM problem checks.  K and N must keep TMA row strides 16-byte aligned.
+fcc_status check_gemm(int R, const void* const* A, const void* const* B, int64_t M, int64_t N,
+                      int64_t K, fcc_dtype in) {
+  if (R < 1 || R > FCC_MAX_RANKS) return FCC_ERR_INVALID;
+  if (M <= 0 || N <= 0 || K <= 0) return FCC_ERR_INVALID;
+  if (K % 8 != 0 || N % 8 != 0) return FCC_ERR_INVALID;
+  if (M > (1ll << 31) - 1 || N > (1ll << 31) - 1 || K > (1ll << 31) - 1) return FCC_ERR_INVALID;
+  if (!ptrs_ok(A, R) || !ptrs_ok(B, R)) return FCC_ERR_INVALID;
+  if (in != FCC_BF16 && in != FCC_F16 && in != FCC_F32) return FCC_ERR_INVALID;
+  if (in != FCC_BF16) return FCC_ERR_UNSUPPORTED;
+  return FCC_OK;
+}
+
+fcc_status check_out_dtype(fcc_dtype out) {
+  if (out == FCC_BF16 || out == FCC_F32) return FCC_OK;
+  if (out == FCC_F16) return FCC_ERR_UNSUPPORTED;
+  return FCC_ERR_INVALID;
+}
+
+// Fills the GEMM parameters shared by all modes.
+fcc_status gemm_params(GemmParams& p, DeviceState* d, int mode, int R, const void* const* A,
+                       const void* const* B, void* const* out, int nout, int64_t M, int64_t N,
+                       int64_t K, int64_t Ms, int64_t m_begin, int64_t m_end, int out_f32,
+                       const fcc_opts* o) {
+  std::memset(&p, 0, sizeof(p));
+  const int64_t a_rows = (mode == MODE_AG) ? Ms : M;
+  for (int r = 0; r < R; ++r) {
+    fcc_status s = make_map(&p.mapA[r], A[r], a_rows, K, kBM);
+    if (s != FCC_OK) return s;
+    s = make_map(&p.mapB[r], B[r], K, N, kBK);
+    if (s != FCC_OK) return s;
+  }
+  for (int i = 0; i < nout; ++i) p.out[i] = out[i];
+  p.R = R;
+  p.M = static_cast<int>(M);
+  p.N = static_cast<int>(N);
+  p.K = static_cast<int>(K);
+  p.Ms = static_cast<int>(Ms);
+  p.m_begin = static_cast<int>(m_begin);
+  p.m_end = static_cast<int>(m_end);
+  p.kb_per_rank = static_cast<int>(cdiv(K, kBK));
+  p.out_f32 = out_f32;
+  p.group_m = 16;
+  p.status = d->status;
+  p.timeout_ns = timeout_of(o);
+  const int tn = static_cast<int>(cdiv(N, kGemmBN));
+  switch (mode) {
+    case MODE_RS:
+    case MODE_AR:
+      p.tiles_m = static_cast<int>(cdiv(M, kBM));
+      p.tiles_n = tn;
+      p.num_tiles = p.tiles_m * p.tiles_n;
+      p.k_iters = R * p.kb_per_rank;
+      break;
+    case MODE_RS_PUSH:
+    case MODE_AR_PUSH:
+      p.tiles_m = static_cast<int>(cdiv(M, kBM));
+      p.tiles_n = tn;
+      p.num_tiles = R * p.tiles_m * p.tiles_n;
+      p.k_iters = p.kb_per_rank;
+      break;
+    case MODE_PARTIAL:
+      p.tiles_m = static_cast<int>(cdiv(m_end - m_begin, kBM));
+      p.tiles_n = tn;
+      p.num_tiles = R * p.tiles_m * p.tiles_n;
+      p.k_iters = p.kb_per_rank;
+      break;
+    case MODE_AG:
+      p.tiles_m = R * static_cast<int>(cdiv(Ms, kBM));
+      p.tiles_n = R * tn;
+      p.num_tiles = p.tiles_m * p.tiles_n;
+      p.k_iters = p.kb_per_rank;
+      p.group_m = 8;
+      break;
+    default:
+      return FCC_ERR_INVALID;
+  }
+  return FCC_OK;
+}
+
+fcc_status run_gemm(const GemmParams& p, int mode, DeviceState* d, const fcc_opts* o,
+                    cudaStream_t st) {
+  if (p.num_tiles <= 0) return FCC_OK;
+  const int grid = grid_for(d, o, p.num_tiles);
+  cudaError_t e = launch_gemm(p, mode, grid, st);
+  if (e != cudaSuccess) return FCC_ERR_CUDA;
+  g_launches.fetch_add(1);
+  return FCC_OK;
+}
+
+// ------------------------------------------------------------ layouts
+struct RankSumPlan {
+  size_t partial_bytes = 0;  // R x M x N f32
+  size_t recv_bytes = 0;     // CE: R x M x N f32
+  size_t acc_bytes = 0;      // push: M x N f32
+  size_t ticket_bytes = 0;
+  size_t total() const {
+    return align_up(partial_bytes) + align_up(recv_bytes) + align_up(acc_bytes) +
+           align_up(ticket_bytes);
+  }
+};
+
+RankSumPlan rank_sum_plan(int R, int64_t M, int64_t N, bool out_f32, const fcc_opts* o) {
+  RankSumPlan pl;
+  const fcc_algo a = algo_of(o);
+  const size_t mn = static_cast<size_t>(M) * static_cast<size_t>(N);
+  if (a == FCC_ALGO_FUSED) {
+    if (!deterministic_of(o) && !out_f32) {
+      pl.acc_bytes = mn * 4;
+      pl.ticket_bytes = static_cast<size_t>(cdiv(M, kBM) * cdiv(N, kGemmBN)) * 4;
+    }
+  } else {
+    pl.partial_bytes = static_cast<size_t>(R) * mn * 4;
+    if (a == FCC_ALGO_CE) pl.recv_bytes = static_cast<size_t>(R) * mn * 4;
+  }
+  return pl;
+}
+
+// Rows per InterDecom chunk, a multiple of the tile height.
+int64_t chunk_rows(int64_t M, int chunks) {
+  int64_t rows = cdiv(M, chunks);
+  return cdiv(rows, kBM) * kBM;
+}
+
+// Default model constants for the chunk count when the caller gives none:
+// sustained tensor rate, copy bandwidth and per-chunk overhead on a GB300.
+constexpr double kModelTcFlops = 1.6e15;
+constexpr double kModelBytesPerS = 6.0e12;
+constexpr double kModelAlphaS = 6.0e-6;
+
+int model_chunks(int R, int64_t M, int64_t N, int64_t K, int out_bytes) {
+  const double G = 2.0 * R * static_cast<double>(M) * N * K / kModelTcFlops;
+  const double X = (static_cast<double>(R) * M * N * 4 + static_cast<double>(M) * N * out_bytes) /
+                   kModelBytesPerS;
+  const int maxc = static_cast<int>(std::min<int64_t>(kMaxChunks, cdiv(M, kBM)));
+  return fcc_interdecom_chunks(G, X, kModelAlphaS, maxc);
+}
+
+// Sum over ranks (RS or AR) through partial GEMM + reduce: UNFUSED, INTERDECOM, CE.
+fcc_status rank_sum_unfused(int R, const void* const* A, const void* const* B, void* const* out,
+                            int nout, bool per_shard, int64_t M, int64_t N, int64_t K,
+                            int out_f32, const fcc_opts* o, DeviceState* d, void* ws,
+                            const RankSumPlan& pl, cudaStream_t st) {
+  const fcc_algo algo = algo_of(o);
+  float* P[FCC_MAX_RANKS];
+  char* base = static_cast<char*>(ws);
+  for (int r = 0; r < R; ++r) P[r] = reinterpret_cast<float*>(base) + static_cast<size_t>(r) * M * N;
+  float* recv[FCC_MAX_RANKS];
+  char* recv_base = base + align_up(pl.partial_bytes);
+  for (int r = 0; r < R; ++r)
+    recv[r] = reinterpret_cast<float*>(recv_base) + static_cast<size_t>(r) * M * N;
+  const int64_t Ms = per_shard ? M / R : M;
+  void* Pv[FCC_MAX_RANKS];
+  for (int r = 0; r < R; ++r) Pv[r] = P[r];
+
+  if (algo == FCC_ALGO_UNFUSED || algo == FCC_ALGO_CE) {
+    GemmParams p;
+    fcc_status s = gemm_params(p, d, MODE_PARTIAL, R, A, B, Pv, R, M, N, K, Ms, 0, M, 1, o);
+    if (s != FCC_OK) return s;
+    s = run_gemm(p, MODE_PARTIAL, d, o, st);
+    if (s != FCC_OK) return s;
+    const float* const* src = P;
+    if (algo == FCC_ALGO_CE) {
+      // Copy-engine movement of every partial shard to its owner (R x R copies),
+      // spread over side streams; the reduction itself still needs SMs.
+      cudaEvent_t fork = d->ev[kMaxChunks];
+      if (cudaEventRecord(fork, st) != cudaSuccess) return FCC_ERR_CUDA;
+      for (int i = 0; i < kSideStreams; ++i)
+        if (cudaStreamWaitEvent(d->side[i], fork, 0) != cudaSuccess) return FCC_ERR_CUDA;
+      const int64_t rows = per_shard ? Ms : M;
+      const int nshards = per_shard ? R : 1;
+      int q = 0;
+      for (int j = 0; j < nshards; ++j) {
+        for (int r = 0; r < R; ++r) {
+          const size_t off = static_cast<size_t>(j) * rows * N;
+          const size_t bytes = static_cast<size_t>(rows) * N * 4;
+          if (cudaMemcpyAsync(recv[r] + off, P[r] + off, bytes, cudaMemcpyDeviceToDevice,
+                              d->side[q % kSideStreams]) != cudaSuccess)
+            return FCC_ERR_CUDA;
+          ++q;
+        }
+      }
+      for (int i = 0; i < kSideStreams; ++i) {
+        if (cudaEventRecord(d->ev[kMaxChunks + 1 + i], d->side[i]) != cudaSuccess) return FCC_ERR_CUDA;
+        if (cudaStreamWaitEvent(st, d->ev[kMaxChunks + 1 + i], 0) != cudaSuccess) return FCC_ERR_CUDA;
+      }
+      src = recv;
+    }
+    if (cuda_fail(launch_reduce_shards(src, R, out, nout, per_shard ? 1 : 0, M, N, Ms, 0, M,
+                                       out_f32, st)) != FCC_OK)
+      return FCC_ERR_CUDA;
+    return FCC_OK;
+  }
+
+  // INTERDECOM: GEMM of row chunk i on the caller stream overlaps the reduce
+  // of chunk i-1 on a side stream.
+  int chunks = (o != nullptr && o->chunks > 0) ? o->chunks
+                                               : model_chunks(R, M, N, K, out_f32 ? 4 : 2);
+  chunks = std::max(1, std::min(chunks, kMaxChunks));
+  const int64_t rows = chunk_rows(M, chunks);
+  cudaStream_t side = d->side[0];
+  int i = 0;
+  for (int64_t m0 = 0; m0 < M; m0 += rows, ++i) {
+    const int64_t m1 = std::min(M, m0 + rows);
+    GemmParams p;
+    fcc_status s = gemm_params(p, d, MODE_PARTIAL, R, A, B, Pv, R, M, N, K, Ms, m0, m1, 1, o);
+    if (s != FCC_OK) return s;
+    s = run_gemm(p, MODE_PARTIAL, d, o, st);
+    if (s != FCC_OK) return s;
+    if (cudaEventRecord(d->ev[i], st) != cudaSuccess) return FCC_ERR_CUDA;
+    if (cudaStreamWaitEvent(side, d->ev[i], 0) != cudaSuccess) return FCC_ERR_CUDA;
+    if (cuda_fail(launch_reduce_shards(P, R, out, nout, per_shard ? 1 : 0, M, N, Ms, m0, m1,
+                                       out_f32, side)) != FCC_OK)
+      return FCC_ERR_CUDA;
+  }
+  cudaEvent_t join = d->ev[kMaxChunks + kSideStreams + 1];
+  if (cudaEventRecord(join, side) != cudaSuccess) return FCC_ERR_CUDA;
+  if (cudaStreamWaitEvent(st, join, 0) != cudaSuccess) return FCC_ERR_CUDA;
+  return FCC_OK;
+}
+
+fcc_status rank_sum_call(int R, const void* const* A, const void* const* B, void* const* out,
+                         bool per_shard, int64_t M, int64_t N, int64_t K, fcc_dtype in,
+                         fcc_dtype out_dtype, const fcc_opts* o, cudaStream_t st) {
+  fcc_status s = check_gemm(R, A, B, M, N, K, in);
+  if (s != FCC_OK) return s;
+  if (per_shard && M % R != 0) return FCC_ERR_INVALID;
+  if ((s = check_out_dtype(out_dtype)) != FCC_OK) return s;
+  if (!ptrs_ok(out, R)) return FCC_ERR_INVALID;
+  const fcc_algo algo = algo_of(o);
+  if (algo != FCC_ALGO_FUSED && algo != FCC_ALGO_UNFUSED && algo != FCC_ALGO_INTERDECOM &&
+      algo != FCC_ALGO_CE)
+    return FCC_ERR_INVALID;
+  DeviceState* d = nullptr;
+  if ((s = device_state(&d)) != FCC_OK) return s;
+  const int out_f32 = out_dtype == FCC_F32 ? 1 : 0;
+  const RankSumPlan pl = rank_sum_plan(R, M, N, out_f32, o);
+  void* ws = nullptr;
+  if ((s = get_workspace(d, o, pl.total(), &ws)) != FCC_OK) return s;
+  const int64_t Ms = per_shard ? M / R : M;
+
+  if (algo != FCC_ALGO_FUSED)
+    return rank_sum_unfused(R, A, B, out, R, per_shard, M, N, K, out_f32, o, d, ws, pl, st);
+
+  if (deterministic_of(o)) {
+    const int mode = per_shard ? MODE_RS : MODE_AR;
+    GemmParams p;
+    if ((s = gemm_params(p, d, mode, R, A, B, out, R, M, N, K, Ms, 0, M, out_f32, o)) != FCC_OK)
+      return s;
+    return run_gemm(p, mode, d, o, st);
+  }
+
+  // Push mode: every (rank, tile) adds its f32 result into the owner's buffer.
+  const int mode = per_shard ? MODE_RS_PUSH : MODE_AR_PUSH;
+  GemmParams p;
+  if ((s = gemm_params(p, d, mode, R, A, B, out, R, M, N, K, Ms, 0, M, out_f32, o)) != FCC_OK)
+    return s;
+  if (out_f32) {
+    // Accumulate in place: zero the destinations first.
+    if (per_shard) {
+      for (int j = 0; j < R; ++j)
+        if (cudaMemsetAsync(out[j], 0, static_cast<size_t>(Ms) * N * 4, st) != cudaSuccess)
+          return FCC_ERR_CUDA;
+    } else if (cudaMemsetAsync(out[0], 0, static_cast<size_t>(M) * N * 4, st) != cudaSuccess) {
+      return FCC_ERR_CUDA;
+    }
+  } else {
+    char* base = static_cast<char*>(ws);
+    p.acc_ws = reinterpret_cast<float*>(base);
+    p.tickets = reinterpret_cast<int*>(base + align_up(pl.acc_bytes));
+    if (cudaMemsetAsync(ws, 0, pl.total(), st) != cudaSuccess) return FCC_ERR_CUDA;
+  }
+  if ((s = run_gemm(p, mode, d, o, st)) != FCC_OK) return s;
+  if (!per_shard && out_f32) {
+    for (int r = 1; r < R; ++r)
+      if (cudaMemcpyAsync(out[r], out[0], static_cast<size_t>(M) * N * 4, cudaMemcpyDeviceToDevice,
+                          st) != cudaSuccess)
+        return FCC_ERR_CUDA;
+  }
+  return FCC_OK;
+}
+
+// ---------------------------------------------------------------- GEMV
+struct GemvPlan {
+  int slabs = 0;
+  size_t partial_bytes = 0;
+  size_t ticket_bytes = 0;
+  size_t total() const { return align_up(partial_bytes) + align_up(ticket_bytes); }
+};
+
+GemvPlan gemv_plan(int64_t N, int sms) {
+  GemvPlan g;
+  g.slabs = static_cast<int>(cdiv(N, 128));
+  g.partial_bytes = static_cast<size_t>(g.slabs + sms) * 16 * 128 * 4;
+  g.ticket_bytes = static_cast<size_t>(g.slabs) * 4;
+  return g;
+}
+
+}  // namespace
+
+int* device_status_ptr() {
+  DeviceState* d = nullptr;
+  return device_state(&d) == FCC_OK ? d->status : nullptr;
+}
+
+int device_sm_count() {
+  DeviceState* d = nullptr;
+  return device_state(&d) == FCC_OK ? d->sms : 1;
+}
+
+uint64_t bump_launch_count(uint64_t n) { return g_launches.fetch_add(n) + n; }
+
+}  // namespace fcc
+
+using namespace fcc;
+
+extern "C" {
+
+fcc_status fcc_gemm_rs(int R, const void* const* A, const void* const* B, void* const* out_shard,
+                       int64_t M, int64_t N, int64_t K, fcc_dtype in, fcc_dtype out,
+                       const fcc_opts* opts, fcc_stream_t stream) {
+  return rank_sum_call(R, A, B, out_shard, true, M, N, K, in, out, opts,
+                       reinterpret_cast<cudaStream_t>(stream));
+}
+
+fcc_status fcc_gemm_ar(int R, const void* const* A, const void* const* B, void* const* out,
+                       int64_t M, int64_t N, int64_t K, fcc_dtype in, fcc_dtype out_dtype,
+                       const fcc_opts* opts, fcc_stream_t stream) {
+  return rank_sum_call(R, A, B, out, false, M, N, K, in, out_dtype, opts,
+                       reinterpret_cast<cudaStream_t>(stream));
+}
+
+fcc_status fcc_gemv_ar(int R, const void* const* A, const void* const* B, void* const* out,
+                       int64_t M, int64_t N, int64_t K, fcc_dtype in, fcc_dtype out_dtype,
+                       const fcc_opts* opts, fcc_stream_t stream) {
+  fcc_status s = check_gemm(R, A, B, M, N, K, in);
+  if (s != FCC_OK) return s;
+  if (M > 16) return FCC_ERR_INVALID;
+  if ((s = check_out_dtype(out_dtype)) != FCC_OK) return s;
+  if (!ptrs_ok(out, R)) return FCC_ERR_INVALID;
+  const fcc_algo algo = algo_of(opts);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const int out_f32 = out_dtype == FCC_F32 ? 1 : 0;
+  if (algo != FCC_ALGO_FUSED) {
+    if (algo == FCC_ALGO_INTERDECOM) return FCC_ERR_UNSUPPORTED;  // one 8-row chunk: nothing to split
+    if (algo != FCC_ALGO_UNFUSED && algo != FCC_ALGO_CE) return FCC_ERR_INVALID;
+    DeviceState* d = nullptr;
+    if ((s = device_state(&d)) != FCC_OK) return s;
+    const RankSumPlan pl = rank_sum_plan(R, M, N, out_f32, opts);
+    void* ws = nullptr;
+    if ((s = get_workspace(d, opts, pl.total(), &ws)) != FCC_OK) return s;
+    return rank_sum_unfused(R, A, B, out, R, false, M, N, K, out_f32, opts, d, ws, pl, st);
+  }
+  DeviceState* d = nullptr;
+  if ((s = device_state(&d)) != FCC_OK) return s;
+  const GemvPlan g = gemv_plan(N, d->sms);
+  void* ws = nullptr;
+  if ((s = get_workspace(d, opts, g.total(), &ws)) != FCC_OK) return s;
+  GemvParams p;
+  std::memset(&p, 0, sizeof(p));
+  for (int r = 0; r < R; ++r) {
+    if ((s = make_map(&p.mapA[r], A[r], M, K, 16)) != FCC_OK) return s;
+    if ((s = make_map(&p.mapB[r], B[r], K, N, kBK)) != FCC_OK) return s;
+    p.out[r] = out[r];
+  }
+  p.R = R;
+  p.M = static_cast<int>(M);
+  p.N = static_cast<int>(N);
+  p.K = static_cast<int>(K);
+  p.kb_per_rank = static_cast<int>(cdiv(K, kBK));
+  p.slabs = g.slabs;
+  p.units = static_cast<long long>(g.slabs) * R * p.kb_per_rank;
+  p.out_f32 = out_f32;
+  p.partials = static_cast<float*>(ws);
+  p.tickets = reinterpret_cast<int*>(static_cast<char*>(ws) + align_up(g.partial_bytes));
+  p.status = d->status;
+  p.timeout_ns = timeout_of(opts);
+  if (cudaMemsetAsync(p.tickets, 0, g.ticket_bytes, st) != cudaSuccess) return FCC_ERR_CUDA;
+  const int grid = grid_for(d, opts, p.units);
+  if (launch_gemv(p, grid, st) != cudaSuccess) return FCC_ERR_CUDA;
+  g_launches.fetch_add(1);
+  return FCC_OK;
+}
+
+fcc_status fcc_ag_gemm(int R, const void* const* X_shard, const void* const* B, void* const* out,
+                       void* const* gathered, int64_t M, int64_t N, int64_t K, fcc_dtype in,
+                       fcc_dtype out_dtype, const fcc_opts* opts, fcc_stream_t stream) {
+  fcc_status s = check_gemm(R, X_shard, B, M, N, K, in);
+  if (s != FCC_OK) return s;
+  if (M % R != 0) return FCC_ERR_INVALID;
+  if ((s = check_out_dtype(out_dtype)) != FCC_OK) return s;
+  if (!ptrs_ok(out, R)) return FCC_ERR_INVALID;
+  if (gathered != nullptr)
+    for (int r = 0; r < R; ++r)
+      if (gathered[r] != nullptr && !aligned16(gathered[r])) return FCC_ERR_INVALID;
+  const fcc_algo algo = algo_of(opts);
+  if (algo == FCC_ALGO_INTERDECOM) return FCC_ERR_UNSUPPORTED;
+  if (algo != FCC_ALGO_FUSED && algo != FCC_ALGO_UNFUSED && algo != FCC_ALGO_CE)
+    return FCC_ERR_INVALID;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  DeviceState* d = nullptr;
+  if ((s = device_state(&d)) != FCC_OK) return s;
+  const int64_t Ms = M / R;
+  const int out_f32 = out_dtype == FCC_F32 ? 1 : 0;
+
+  if (algo == FCC_ALGO_FUSED) {
+    GemmParams p;
+    if ((s = gemm_params(p, d, MODE_AG, R, X_shard, B, out, R, M, N, K, Ms, 0, M, out_f32,
+                         opts)) != FCC_OK)
+      return s;
+    if ((s = run_gemm(p, MODE_AG, d, opts, st)) != FCC_OK) return s;
+    // The gathered copies are an optional output: materialise them after the GEMM
+    // has read the shards in place.
+    if (gathered != nullptr) {
+      for (int r = 0; r < R; ++r)
+        if (gathered[r] != nullptr &&
+            cuda_fail(launch_gather_rows(X_shard, R, Ms, K, gathered[r], st)) != FCC_OK)
+          return FCC_ERR_CUDA;
+    }
+    return FCC_OK;
+  }
+
+  // Unfused: gather X (SM copy kernel or copy engines), then one GEMM per rank.
+  const void* src = nullptr;
+  void* ws = nullptr;
+  const bool have_g = gathered != nullptr && gathered[0] != nullptr;
+  const size_t xbytes = static_cast<size_t>(M) * K * 2;
+  if (!have_g) {
+    if ((s = get_workspace(d, opts, xbytes, &ws)) != FCC_OK) return s;
+  }
+  void* g0 = have_g ? gathered[0] : ws;
+  if (algo == FCC_ALGO_CE) {
+    for (int sh = 0; sh < R; ++sh)
+      if (cudaMemcpyAsync(static_cast<char*>(g0) + static_cast<size_t>(sh) * Ms * K * 2, X_shard[sh],
+                          static_cast<size_t>(Ms) * K * 2, cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+        return FCC_ERR_CUDA;
+  } else if (cuda_fail(launch_gather_rows(X_shard, R, Ms, K, g0, st)) != FCC_OK) {
+    return FCC_ERR_CUDA;
+  }
+  src = g0;
+  const void* Ag[FCC_MAX_RANKS];
+  for (int r = 0; r < R; ++r) Ag[r] = src;
+  GemmParams p;
+  if ((s = gemm_params(p, d, MODE_PARTIAL, R, Ag, B, out, R, M, N, K, M, 0, M, out_f32, opts)) !=
+      FCC_OK)
+    return s;
+  if ((s = run_gemm(p, MODE_PARTIAL, d, opts, st)) != FCC_OK) return s;
+  if (have_g) {
+    for (int r = 1; r < R; ++r)
+      if (gathered[r] != nullptr &&
+          cudaMemcpyAsync(gathered[r], g0, xbytes, cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+        return FCC_ERR_CUDA;
+  }
+  return FCC_OK;
+}
+
+size_t fcc_workspace_size(fcc_op op, int R, int64_t M, int64_t N, int64_t K,
+                          const fcc_opts* opts) {
+  (void)K;
+  if (R < 1 || R > FCC_MAX_RANKS || M <= 0 || N <= 0) return 0;
+  switch (op) {
+    case FCC_OP_GEMM_RS:
+    case FCC_OP_GEMM_AR:
+      // bf16 vs f32 output only matters for the push mode; report the larger.
+      return rank_sum_plan(R, M, N, false, opts).total();
+    case FCC_OP_GEMV_AR: {
+      if (algo_of(opts) != FCC_ALGO_FUSED) return rank_sum_plan(R, M, N, false, opts).total();
+      int sms = 0, dev = 0;
+      if (cudaGetDevice(&dev) != cudaSuccess ||
+          cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        sms = 256;
+      return gemv_plan(N, sms).total();
+    }
+    case FCC_OP_AG_GEMM:
+      return algo_of(opts) == FCC_ALGO_FUSED ? 0 : static_cast<size_t>(M) * K * 2;
+  }
+  return 0;
+}
+
+fcc_status fcc_stream_status(fcc_stream_t stream) {
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return FCC_ERR_CUDA;
+  DeviceState* d = nullptr;
+  fcc_status s = device_state(&d);
+  if (s != FCC_OK) return s;
+  int v = 0;
+  if (cudaMemcpy(&v, d->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return FCC_ERR_CUDA;
+  if (v != 0) {
+    const int zero = 0;
+    if (cudaMemcpy(d->status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+      return FCC_ERR_CUDA;
+  }
+  return static_cast<fcc_status>(v);
+}
+
+const char* fcc_status_string(fcc_status s) {
+  switch (s) {
+    case FCC_OK: return "ok";
+    case FCC_ERR_INVALID: return "invalid argument";
+    case FCC_ERR_UNSUPPORTED: return "unsupported";
+    case FCC_ERR_CUDA: return "CUDA error";
+    case FCC_ERR_CAPACITY: return "receive capacity exceeded";
+    case FCC_ERR_TIMEOUT: return "device wait timed out";
+    case FCC_ERR_WORKSPACE: return "workspace too small";
+  }
+  return "unknown status";
+}
+
+double fcc_interdecom_time(double G, double X, double alpha, int chunks) {
+  if (chunks < 1) chunks = 1;
+  return std::max(G, X) + std::min(G, X) / chunks + chunks * alpha;
+}
+
+int fcc_interdecom_chunks(double G, double X, double alpha, int max_chunks) {
+  if (max_chunks < 1) max_chunks = 1;
+  if (!(G > 0) || !(X > 0)) return 1;
+  if (!(alpha > 0)) return max_chunks;
+  const double c = std::sqrt(std::min(G, X) / alpha);
+  int lo = static_cast<int>(std::floor(c));
+  int hi = lo + 1;
+  lo = std::max(1, std::min(lo, max_chunks));
+  hi = std::max(1, std::min(hi, max_chunks));
+  return fcc_interdecom_time(G, X, alpha, hi) < fcc_interdecom_time(G, X, alpha, lo) ? hi : lo;
+}
+
+uint64_t fcc_launch_count(void) { return g_launches.load(); }
+
+const char* fcc_version(void) { return "0.1.0"; }
+
+fcc_status fcc_test_wait_timeout(int64_t timeout_ns, fcc_stream_t stream) {
+  if (timeout_ns <= 0) return FCC_ERR_INVALID;
+  DeviceState* d = nullptr;
+  fcc_status s = device_state(&d);
+  if (s != FCC_OK) return s;
+  return cuda_fail(launch_wait_probe(d->status, static_cast<unsigned long long>(timeout_ns),
+                                     reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,430 @@
+// fcc_gemm.cu -- persistent tcgen05 GEMM with collective epilogues (sm_103a).
+//
+// One CTA per SM loops over output tiles (128 x 256).  Warp 0 streams A and B
+// tiles with TMA into a 4-stage shared-memory ring; warp 1 issues
+// tcgen05.mma (bf16 x bf16 -> f32) into one of two TMEM accumulators; warps
+// 2-5 drain the other accumulator with tcgen05.ld and perform the collective
+// step in the epilogue, so the stores of tile i overlap the MMAs of tile i+1.
+//
+// The collective step per mode (the fused operators of the mKernel article's
+// kernel list and of the SC24 paper's abstract, where each workgroup ships
+// its result to the owner as soon as its tile is done):
+//   MODE_RS       the tile's K loop runs over (rank 0..R-1) x K, so the one
+//                 accumulator holds sum_r A_r B_r for the tile in a fixed
+//                 rank order; the owner shard receives one store per element.
+//   MODE_AR       the same sum, stored into every rank's buffer.
+//   MODE_RS_PUSH  each (rank, tile) is its own work item; its f32 result is
+//   MODE_AR_PUSH  added into the owner's f32 buffer with red.global.add.v4.f32;
+//                 for bf16 outputs the last arriving rank (ticket) converts.
+//   MODE_AG       the A tile is read straight from the shard that owns its rows
+//                 (the gather), the B tile and output from the column's rank.
+//   MODE_PARTIAL  plain per-rank GEMM over a row window (unfused baselines).
+//
+// Shared memory operand layouts (128-byte swizzle, as written by TMA):
+//   A stage  [128 rows][64 k]   K-major: row m at m*128 B, 8-row groups 1 KiB apart
+//   B stage  4 boxes of [64 k][64 n] MN-major: box i at i*8 KiB, k-row at k*128 B
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "fcc_internal.h"
+#include "fcc_ptx.cuh"
+
+namespace fcc {
+namespace {
+
+constexpr int kBN = 256;
+constexpr int kStages = 4;
+constexpr uint32_t kABytes = kBM * kBK * 2;         // 16 KiB
+constexpr uint32_t kBBoxBytes = kBK * 64 * 2;       // 8 KiB: [64 k][64 n]
+constexpr uint32_t kBBytes = kBK * kBN * 2;         // 32 KiB
+constexpr uint32_t kStageBytes = kABytes + kBBytes;
+constexpr uint32_t kTmemCols = 2 * kBN;             // double-buffered accumulator
+constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(kBM, kBN, /*a_mn=*/false, /*b_mn=*/true);
+constexpr uint64_t kDrainNs = 50ull * 1000 * 1000;  // unwinding limit after an abort
+
+constexpr int kSmemBytes = 1024 /*alignment slack*/ + kStages * kStageBytes +
+                           (2 * kStages + 5) * 8 + 16;
+
+struct Tile {
+  int rank;    // rank whose A/B feed the tile (PARTIAL/PUSH/AG-B), -1 = all ranks
+  int shard;   // AG: shard that owns the A rows
+  int mt, nt;  // tile indices within one rank's output
+};
+
+__device__ __forceinline__ void raster(int t, int tiles_m, int tiles_n, int group, int& mt,
+                                       int& nt) {
+  const int per_group = group * tiles_n;
+  const int g = t / per_group;
+  const int first = g * group;
+  const int gm = min(group, tiles_m - first);
+  const int local = t - g * per_group;
+  mt = first + local % gm;
+  nt = local / gm;
+}
+
+template <int MODE>
+__device__ __forceinline__ Tile tile_of(const GemmParams& p, int t) {
+  Tile tl;
+  tl.rank = -1;
+  tl.shard = 0;
+  if constexpr (MODE == MODE_RS || MODE == MODE_AR) {
+    raster(t, p.tiles_m, p.tiles_n, p.group_m, tl.mt, tl.nt);
+  } else if constexpr (MODE == MODE_AG) {
+    // tiles_m = R * (tiles per shard), tiles_n = R * (tiles per rank)
+    int gm, gn;
+    raster(t, p.tiles_m, p.tiles_n, p.group_m, gm, gn);
+    const int mt_per_shard = p.tiles_m / p.R;
+    const int nt_per_rank = p.tiles_n / p.R;
+    tl.shard = gm / mt_per_shard;
+    tl.mt = gm - tl.shard * mt_per_shard;
+    tl.rank = gn / nt_per_rank;
+    tl.nt = gn - tl.rank * nt_per_rank;
+  } else {
+    const int per_rank = p.tiles_m * p.tiles_n;
+    tl.rank = t / per_rank;
+    raster(t - tl.rank * per_rank, p.tiles_m, p.tiles_n, p.group_m, tl.mt, tl.nt);
+  }
+  return tl;
+}
+
+// ----------------------------------------------------------------- epilogue
+// Stores 32 consecutive f32 accumulator columns of one row.
+__device__ __forceinline__ void store_row_chunk(void* row_ptr, int col, int N, int out_f32,
+                                                const uint32_t (&v)[32]) {
+  if (out_f32) {
+    float* dst = reinterpret_cast<float*>(row_ptr) + col;
+#pragma unroll
+    for (int g = 0; g < 8; ++g) {
+      if (col + 4 * g + 4 <= N)
+        ptx::st_global_v4(dst + 4 * g, v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
+    }
+  } else {
+    uint16_t* dst = reinterpret_cast<uint16_t*>(row_ptr) + col;
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      if (col + 8 * g + 8 <= N) {
+        uint32_t w[4];
+#pragma unroll
+        for (int h = 0; h < 4; ++h)
+          w[h] = ptx::pack_bf16x2(__uint_as_float(v[8 * g + 2 * h]),
+                                  __uint_as_float(v[8 * g + 2 * h + 1]));
+        ptx::st_global_v4(dst + 8 * g, w[0], w[1], w[2], w[3]);
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void red_row_chunk(float* row_ptr, int col, int N,
+                                              const uint32_t (&v)[32]) {
+  float* dst = row_ptr + col;
+#pragma unroll
+  for (int g = 0; g < 8; ++g) {
+    if (col + 4 * g + 4 <= N)
+      ptx::red_add_v4_f32(dst + 4 * g, __uint_as_float(v[4 * g]), __uint_as_float(v[4 * g + 1]),
+                          __uint_as_float(v[4 * g + 2]), __uint_as_float(v[4 * g + 3]));
+  }
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_constant__ GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + kStages * kABytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + kStages * kBBytes);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + kStages;
+  uint64_t* tfull = bars + 2 * kStages;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* mma_done = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* bcast = reinterpret_cast<volatile int*>(tmem_slot + 2);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      ptx::mbar_init(&full[s], 1);
+      ptx::mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(&tfull[b], 1);
+      ptx::mbar_init(&tempty[b], 4);
+    }
+    ptx::mbar_init(mma_done, 1);
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    for (int r = 0; r < p.R; ++r) {
+      ptx::tma_prefetch_desc(&p.mapA[r]);
+      ptx::tma_prefetch_desc(&p.mapB[r]);
+    }
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(tmem_slot, kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const ptx::Waiter W{abort_flag, p.status, p.timeout_ns};
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0;
+      uint32_t issued = 0, last_parity = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+        const Tile tl = tile_of<MODE>(p, t);
+        int a_row;
+        if constexpr (MODE == MODE_AG) {
+          a_row = tl.mt * kBM;
+        } else if constexpr (MODE == MODE_PARTIAL) {
+          a_row = p.m_begin + tl.mt * kBM;
+        } else {
+          a_row = tl.mt * kBM;
+        }
+        const int b_col = tl.nt * kBN;
+        int r = (tl.rank >= 0) ? tl.rank : 0;
+        int kb = 0;
+        for (int it = 0; it < p.k_iters; ++it) {
+          if (!W.wait(&empty[stage], phase ^ 1u)) {
+            ok = false;
+            break;
+          }
+          ptx::mbar_arrive_expect_tx(&full[stage], kStageBytes);
+          const CUtensorMap* ma = (MODE == MODE_AG) ? &p.mapA[tl.shard] : &p.mapA[r];
+          const CUtensorMap* mb = &p.mapB[r];
+          uint8_t* a_dst = sA + stage * kABytes;
+          uint8_t* b_dst = sB + stage * kBBytes;
+          ptx::tma_load_2d(a_dst, ma, &full[stage], kb * kBK, a_row);
+#pragma unroll
+          for (int i = 0; i < kBN / 64; ++i)
+            ptx::tma_load_2d(b_dst + i * kBBoxBytes, mb, &full[stage], b_col + 64 * i, kb * kBK);
+          issued |= 1u << stage;
+          last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+          if (++kb == p.kb_per_rank) {
+            kb = 0;
+            ++r;  // only MODE_RS / MODE_AR iterate past one rank
+          }
+        }
+      }
+      if (*abort_flag) {
+        // Loads still in flight write into this CTA's shared memory: let them land.
+        for (int s = 0; s < kStages; ++s)
+          if (issued & (1u << s)) W.drain(&full[s], (last_parity >> s) & 1u, kDrainNs);
+      }
+    }
+  } else if (warp == 1) {
+    // ----------------------------------------------------------- MMA issue
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0;
+      uint32_t acc = 0, acc_phase = 0;
+      bool any = false, ok = true;
+      for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+        if (!W.wait(&tempty[acc], acc_phase ^ 1u)) break;
+        ptx::tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * kBN;
+        for (int it = 0; it < p.k_iters; ++it) {
+          if (!W.wait(&full[stage], phase)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t a_addr = ptx::smem_addr(sA + stage * kABytes);
+          const uint32_t b_addr = ptx::smem_addr(sB + stage * kBBytes);
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            // A: K-major, advance 16 elements (32 B) inside the swizzled row.
+            const uint64_t ad = ptx::smem_desc_sw128(a_addr + kk * 32, 16, 1024);
+            // B: MN-major, advance 16 k-rows (2 KiB); 64-wide n atoms 8 KiB apart.
+            const uint64_t bd = ptx::smem_desc_sw128(b_addr + kk * 2048, kBBoxBytes, 1024);
+            ptx::mma_f16(d_tmem, ad, bd, kIdesc, (it > 0 || kk > 0) ? 1u : 0u);
+          }
+          ptx::mma_commit(&empty[stage]);
+          any = true;
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        ptx::mma_commit(&tfull[acc]);
+        acc ^= 1u;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      if (any) {
+        ptx::mma_commit(mma_done);
+        W.drain(mma_done, 0, kDrainNs);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------- epilogue
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int row_in_tile = q * 32 + lane;
+    uint32_t acc = 0, acc_phase = 0;
+    for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
+      const Tile tl = tile_of<MODE>(p, t);
+      const bool failed = !W.wait(&tfull[acc], acc_phase);
+      if constexpr (MODE == MODE_RS_PUSH || MODE == MODE_AR_PUSH) {
+        // The four epilogue warps meet at named barriers below: stop together.
+        if (ptx::named_barrier_or(1, 128, failed)) break;
+      } else {
+        if (failed) break;
+      }
+      ptx::tc_fence_after();
+
+      // Destination row(s) for this thread.
+      bool row_ok;
+      void* rowp = nullptr;
+      int64_t grow = 0;  // global row (RS/AR/PUSH)
+      const int esz = p.out_f32 ? 4 : 2;
+      if constexpr (MODE == MODE_RS || MODE == MODE_RS_PUSH) {
+        grow = static_cast<int64_t>(tl.mt) * kBM + row_in_tile;
+        row_ok = grow < p.M;
+        if (row_ok) {
+          const int j = static_cast<int>(grow / p.Ms);
+          rowp = static_cast<char*>(p.out[j]) + (grow - static_cast<int64_t>(j) * p.Ms) * p.N * esz;
+        }
+      } else if constexpr (MODE == MODE_AR || MODE == MODE_AR_PUSH) {
+        grow = static_cast<int64_t>(tl.mt) * kBM + row_in_tile;
+        row_ok = grow < p.M;
+      } else if constexpr (MODE == MODE_AG) {
+        const int64_t local = static_cast<int64_t>(tl.mt) * kBM + row_in_tile;
+        row_ok = local < p.Ms;
+        grow = static_cast<int64_t>(tl.shard) * p.Ms + local;
+        if (row_ok) rowp = static_cast<char*>(p.out[tl.rank]) + grow * p.N * esz;
+      } else {  // MODE_PARTIAL
+        grow = static_cast<int64_t>(p.m_begin) + static_cast<int64_t>(tl.mt) * kBM + row_in_tile;
+        row_ok = grow < p.m_end;
+        if (row_ok) rowp = static_cast<char*>(p.out[tl.rank]) + grow * p.N * esz;
+      }
+
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kBN;
+      const int col0 = tl.nt * kBN;
+#pragma unroll 1
+      for (int c = 0; c < kBN; c += 32) {
+        uint32_t v[32];
+        ptx::tmem_ld_32x32b_x32(taddr + c, v);
+        ptx::tmem_ld_wait();
+        if (c == kBN - 32) {
+          // Accumulator fully read: hand it back to the MMA warp early.
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(&tempty[acc]);
+        }
+        const int col = col0 + c;
+        if (!row_ok || col >= p.N) continue;
+        if constexpr (MODE == MODE_AR) {
+          for (int r = 0; r < p.R; ++r)
+            store_row_chunk(static_cast<char*>(p.out[r]) + grow * p.N * esz, col, p.N, p.out_f32, v);
+        } else if constexpr (MODE == MODE_RS_PUSH || MODE == MODE_AR_PUSH) {
+          float* dst;
+          if (p.out_f32) {
+            if constexpr (MODE == MODE_RS_PUSH)
+              dst = reinterpret_cast<float*>(rowp);
+            else
+              dst = reinterpret_cast<float*>(p.out[0]) + grow * p.N;  // copied to others later
+          } else {
+            dst = p.acc_ws + grow * p.N;
+          }
+          red_row_chunk(dst, col, p.N, v);
+        } else {
+          store_row_chunk(rowp, col, p.N, p.out_f32, v);
+        }
+      }
+
+      if constexpr (MODE == MODE_RS_PUSH || MODE == MODE_AR_PUSH) {
+        if (!p.out_f32) {
+          // Last of the R contributions to this output tile converts it to bf16.
+          __threadfence();
+          ptx::named_barrier_sync(1, 128);
+          if (threadIdx.x == 64) {
+            const int tid = tl.mt * p.tiles_n + tl.nt;
+            const int prev = atomicAdd(&p.tickets[tid], 1);
+            *bcast = (prev == p.R - 1) ? 1 : 0;
+            if (prev == p.R - 1) p.tickets[tid] = 0;
+          }
+          ptx::named_barrier_sync(1, 128);
+          if (*bcast) {
+            __threadfence();
+            if (row_ok) {
+              const float* src = p.acc_ws + grow * p.N;
+#pragma unroll 1
+              for (int c = 0; c < kBN; c += 32) {
+                const int col = col0 + c;
+                if (col >= p.N) break;
+                uint32_t v[32];
+#pragma unroll
+                for (int i = 0; i < 32; i += 4) {
+                  if (col + i + 4 <= p.N) {
+                    const float4 f = __ldcg(reinterpret_cast<const float4*>(src + col + i));
+                    v[i] = __float_as_uint(f.x);
+                    v[i + 1] = __float_as_uint(f.y);
+                    v[i + 2] = __float_as_uint(f.z);
+                    v[i + 3] = __float_as_uint(f.w);
+                  }
+                }
+                if constexpr (MODE == MODE_RS_PUSH) {
+                  store_row_chunk(rowp, col, p.N, 0, v);
+                } else {
+                  for (int r = 0; r < p.R; ++r)
+                    store_row_chunk(static_cast<char*>(p.out[r]) + grow * p.N * 2, col, p.N, 0, v);
+                }
+              }
+            }
+          }
+          ptx::named_barrier_sync(1, 128);
+        }
+      }
+      acc ^= 1u;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  }
+
+  __syncwarp();
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+template <int MODE>
+cudaError_t launch_mode(const GemmParams& p, int grid, cudaStream_t st) {
+  auto kern = gemm_kernel<MODE>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       kSmemBytes);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, kGemmThreads, kSmemBytes, st>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int gemm_smem_bytes() { return kSmemBytes; }
+
+cudaError_t launch_gemm(const GemmParams& p, int mode, int grid, cudaStream_t st) {
+  switch (mode) {
+    case MODE_RS: return launch_mode<MODE_RS>(p, grid, st);
+    case MODE_AR: return launch_mode<MODE_AR>(p, grid, st);
+    case MODE_PARTIAL: return launch_mode<MODE_PARTIAL>(p, grid, st);
+    case MODE_AG: return launch_mode<MODE_AG>(p, grid, st);
+    case MODE_RS_PUSH: return launch_mode<MODE_RS_PUSH>(p, grid, st);
+    case MODE_AR_PUSH: return launch_mode<MODE_AR_PUSH>(p, grid, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace fcc

@@ -1,0 +1,84 @@
+// fcc_internal.h -- declarations shared by the libfcc translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+#include "fcc.h"
+
+namespace fcc {
+
+constexpr int kBM = 128;       // output tile rows (one TMEM lane per row)
+constexpr int kBK = 64;        // K per pipeline stage (128 bytes of bf16: one swizzle row)
+constexpr int kGemmThreads = 192;  // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
+
+enum GemmMode : int {
+  MODE_RS = 0,         // reduce-scatter, ordered tile-owner accumulation over ranks
+  MODE_AR = 1,         // all-reduce: the same, stored to every rank's buffer
+  MODE_PARTIAL = 2,    // plain per-rank GEMM: out[r] = A_r @ B_r over a row window
+  MODE_AG = 3,         // all-gather + GEMM: A tile from the owning shard
+  MODE_RS_PUSH = 4,    // reduce-scatter, push: red.add of each rank's tile into the owner
+  MODE_AR_PUSH = 5,    // all-reduce, push
+};
+
+struct GemmParams {
+  CUtensorMap mapA[FCC_MAX_RANKS];
+  CUtensorMap mapB[FCC_MAX_RANKS];
+  void* out[FCC_MAX_RANKS];
+  int R;
+  int M, N, K;          // GEMM extents (RS/AR: all rows; AG: gathered rows; PARTIAL: rows of A_r)
+  int Ms;               // rows per shard (RS, AG)
+  int m_begin, m_end;   // row window (PARTIAL; others 0..M)
+  int tiles_m, tiles_n; // tile grid of one rank's output
+  int num_tiles;
+  int k_iters;          // pipeline stages per tile
+  int kb_per_rank;      // ceil(K / kBK)
+  int out_f32;          // output storage: 1 = f32, 0 = bf16
+  int group_m;          // raster group height (tiles)
+  int* status;
+  unsigned long long timeout_ns;
+  float* acc_ws;        // push mode with bf16 output: f32 accumulation rows (M x N)
+  int* tickets;         // push mode with bf16 output: per output tile arrival counters
+};
+
+struct GemvParams {
+  CUtensorMap mapA[FCC_MAX_RANKS];  // [M, K] rows padded to 16 by out-of-bounds fill
+  CUtensorMap mapB[FCC_MAX_RANKS];  // [K, N]
+  void* out[FCC_MAX_RANKS];
+  int R, M, N, K;
+  int kb_per_rank;
+  int slabs;            // ceil(N / 128)
+  long long units;      // slabs * R * kb_per_rank
+  int out_f32;
+  float* partials;      // [(slabs + grid) slots][16][128]
+  int* tickets;         // [slabs]
+  int* status;
+  unsigned long long timeout_ns;
+};
+
+// Launchers (return cudaSuccess or the launch error).
+cudaError_t launch_gemm(const GemmParams& p, int mode, int grid, cudaStream_t st);
+int gemm_smem_bytes();
+cudaError_t launch_gemv(const GemvParams& p, int grid, cudaStream_t st);
+int gemv_smem_bytes();
+
+// Elementwise helpers (fcc_aux.cu).
+// out_j rows [row_begin,row_end) of shard j = sum_r P[r] rows, P[r] is [M, N] f32.
+cudaError_t launch_reduce_shards(const float* const* P, int R, void* const* out, int nout,
+                                 int per_shard, int64_t M, int64_t N, int64_t Ms,
+                                 int64_t row_begin, int64_t row_end, int out_f32,
+                                 cudaStream_t st);
+// out bf16 = convert(acc f32), rows [row_begin, row_end) of an [M,N] matrix into shards.
+cudaError_t launch_gather_rows(const void* const* X, int R, int64_t Ms, int64_t K, void* dst,
+                               cudaStream_t st);
+cudaError_t launch_wait_probe(int* status, unsigned long long timeout_ns, cudaStream_t st);
+
+// Shared host helpers (fcc_api.cu).
+int* device_status_ptr();
+int device_sm_count();
+uint64_t bump_launch_count(uint64_t n);
+
+}  // namespace fcc

@@ -1,0 +1,214 @@
+/*
+ * fcc.h -- libfcc: GEMMs fused with the collective that consumes their output,
+ * for one GB300 (sm_103a), across R tensor-parallel ranks whose buffers are
+ * disjoint allocations in the one GPU's HBM.
+ *
+ * "Communication" between ranks is a kernel storing into (or loading from)
+ * another rank's buffer.  The operators are the fused kernels named in
+ * "GPU-vezerelt kommunikacioval gyorsitjak az AI-betanitast a kutatok"
+ * (mKernel article, section on the five fused kernels: AllGather + GEMM,
+ * GEMM + AllReduce, MoE Dispatch + GEMM, GEMM + ReduceScatter) and in
+ * "Optimizing Distributed ML Communication with Fused Computation-Collective
+ * Operations" (SC24, abstract: GEMV + AllReduce, GEMM + All-to-All, with
+ * workgroups that ship their results as soon as they finish).
+ *
+ * Conventions for every call
+ *  - Matrices are row-major and contiguous.  A_r is [M,K], B_r is [K,N]; the
+ *    product is A_r @ B_r as in torch.  Shard j of an M-row result is the
+ *    contiguous row block [j*M/R, (j+1)*M/R).
+ *  - Pointer arrays (A, B, out, ...) are HOST arrays of DEVICE pointers, one
+ *    per rank; they are read during the call and not retained.  Device
+ *    pointers must be 16-byte aligned.  The caller owns every buffer.
+ *  - Inputs are bf16; accumulation is f32; f32 results are stored as f32 and
+ *    bf16 results are rounded to nearest even.
+ *  - Calls are asynchronous on `stream` and return after enqueueing.
+ *    Argument errors are reported synchronously and nothing is launched.
+ *    Errors found on the device (a wait that timed out, a receive buffer too
+ *    small) are recorded in a per-device status word that fcc_stream_status()
+ *    reads and clears.
+ *  - opts may be NULL for the defaults (fused, deterministic, library-owned
+ *    workspace, 1 s wait limit).
+ *  - Workspace: calls that need scratch memory take it from opts->workspace
+ *    (size from fcc_workspace_size / fcc_moe_workspace_size); with no
+ *    workspace given, the library keeps an internal per-device pool that it
+ *    grows with cudaMalloc on first use (and when a larger call comes), which
+ *    synchronises the device at that moment.
+ *  - Not thread-safe for concurrent calls on the same stream; calls on
+ *    different streams share the internal pool and must not overlap unless
+ *    each passes its own workspace.
+ */
+#ifndef FCC_H_
+#define FCC_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* cudaStream_t without pulling in the CUDA headers. */
+typedef struct CUstream_st *fcc_stream_t;
+
+#define FCC_MAX_RANKS 8
+#define FCC_MAX_EXPERTS 64
+
+typedef enum { FCC_BF16 = 0, FCC_F16 = 1, FCC_F32 = 2 } fcc_dtype;
+
+typedef enum {
+  FCC_OK = 0,
+  FCC_ERR_INVALID = 1,     /* bad argument: null or misaligned pointer, bad size */
+  FCC_ERR_UNSUPPORTED = 2, /* valid but not implemented (dtype, algorithm) */
+  FCC_ERR_CUDA = 3,        /* a CUDA runtime call failed */
+  FCC_ERR_CAPACITY = 4,    /* a receive buffer is too small (MoE cap) */
+  FCC_ERR_TIMEOUT = 5,     /* a device-side wait ran out of time */
+  FCC_ERR_WORKSPACE = 6    /* caller workspace too small */
+} fcc_status;
+
+typedef enum {
+  FCC_ALGO_AUTO = 0,       /* the fused kernel */
+  FCC_ALGO_FUSED = 1,      /* fused GEMM + collective in one persistent kernel */
+  FCC_ALGO_UNFUSED = 2,    /* per-rank GEMM to f32 partials, then a reduce/copy kernel */
+  FCC_ALGO_INTERDECOM = 3, /* row chunks: GEMM of chunk i overlaps the collective of i-1 */
+  FCC_ALGO_CE = 4          /* partials moved by copy engines (cudaMemcpyAsync), no SMs */
+} fcc_algo;
+
+typedef struct {
+  fcc_algo algo;
+  /* Fused GEMM+ReduceScatter/AllReduce: 1 = ordered tile-owner accumulation
+   * (each output tile sums ranks 0..R-1 in order in one accumulator; bitwise
+   * repeatable), 0 = push mode (each rank's tile is added into the owner's f32
+   * shard with red.global.add.v4.f32; order-free). */
+  int deterministic;
+  int chunks;              /* InterDecom chunk count; 0 = the cost model */
+  int max_ctas;            /* persistent grid size cap; 0 = one CTA per SM */
+  int64_t timeout_ns;      /* device wait limit; 0 = 1 s */
+  void *workspace;         /* device scratch, or NULL for the internal pool */
+  size_t workspace_bytes;
+} fcc_opts;
+
+/* Operator identifiers for fcc_workspace_size. */
+typedef enum {
+  FCC_OP_GEMM_RS = 0,
+  FCC_OP_GEMM_AR = 1,
+  FCC_OP_GEMV_AR = 2,
+  FCC_OP_AG_GEMM = 3
+} fcc_op;
+
+/*
+ * GEMM + ReduceScatter (mKernel article, fused kernel list; SC24 abstract).
+ *   out_shard[j][i][n] = sum_{r<R} sum_{k<K} A[r][j*M/R + i][k] * B[r][k][n]
+ * R in 1..8; A[r]: [M,K] bf16; B[r]: [K,N] bf16; out_shard[j]: [M/R, N] of
+ * dtype `out` (FCC_BF16 or FCC_F32).  M % R == 0, K % 8 == 0, N % 8 == 0.
+ */
+fcc_status fcc_gemm_rs(int R, const void *const *A, const void *const *B,
+                       void *const *out_shard, int64_t M, int64_t N, int64_t K,
+                       fcc_dtype in, fcc_dtype out, const fcc_opts *opts,
+                       fcc_stream_t stream);
+
+/*
+ * GEMM + AllReduce (mKernel article, fused kernel list).
+ *   out[r'] = sum_{r<R} A[r] @ B[r]  for every rank r' (M x N each).
+ * Shapes as fcc_gemm_rs (no divisibility of M needed).
+ */
+fcc_status fcc_gemm_ar(int R, const void *const *A, const void *const *B, void *const *out,
+                       int64_t M, int64_t N, int64_t K, fcc_dtype in, fcc_dtype out_dtype,
+                       const fcc_opts *opts, fcc_stream_t stream);
+
+/*
+ * GEMV + AllReduce, the decode shape (SC24 abstract, Transformer operator).
+ *   out[r'] = sum_{r<R} A[r] @ B[r] for every rank r'; A[r]: [M,K] with
+ *   1 <= M <= 16 tokens; B[r]: [K,N]; out[r']: [M,N] f32 (or bf16).
+ * The cross-rank sum is deterministic (fixed order).  Uses workspace.
+ */
+fcc_status fcc_gemv_ar(int R, const void *const *A, const void *const *B, void *const *out,
+                       int64_t M, int64_t N, int64_t K, fcc_dtype in, fcc_dtype out_dtype,
+                       const fcc_opts *opts, fcc_stream_t stream);
+
+/*
+ * AllGather + GEMM (mKernel article, fused kernel list).
+ *   X = [X_shard[0]; ...; X_shard[R-1]]   (each [M/R, K], X is [M, K])
+ *   out[r] = X @ B[r]                      ([M, N] per rank, dtype `out_dtype`)
+ *   gathered[r] (nullable array, or NULL entries): receives X ([M, K] bf16).
+ */
+fcc_status fcc_ag_gemm(int R, const void *const *X_shard, const void *const *B,
+                       void *const *out, void *const *gathered, int64_t M, int64_t N,
+                       int64_t K, fcc_dtype in, fcc_dtype out_dtype, const fcc_opts *opts,
+                       fcc_stream_t stream);
+
+/*
+ * MoE Dispatch + GEMM (mKernel article, fused kernel list; SC24 abstract,
+ * GEMM + All-to-All for MoE).  R source ranks with T tokens each; E experts,
+ * E/R per rank, expert e on rank e/(E/R).
+ *   route:    topk_idx[s][t][0..topk) = experts with the largest logits
+ *             (ties: lower index first); topk_gate = their softmax probability
+ *             over all E experts (not renormalised, not applied below).
+ *   dispatch: assignments (s, t, slot) sorted stably by expert; rank d
+ *             receives its experts' rows in (expert, s, t, slot) order:
+ *             recv_src[d][row] = s*T + t, recv_x[d][row] = X[s][t] (if
+ *             recv_x is non-NULL), expert_counts[e], send_counts[s*R + d].
+ *   GEMM:     recv_y[d][row] = X[s][t] @ W[e]  ([F] per row, dtype out_dtype).
+ * X[s]: [T,H] bf16; logits[s]: [T,E] f32; W[e]: [H,F] bf16 (E pointers);
+ * recv_x[d]: [cap,H]; recv_y[d]: [cap,F]; recv_src[d]: [cap] int32;
+ * topk_idx[s]: [T,topk] int32; topk_gate[s]: [T,topk] f32; expert_counts:
+ * [E] int32 device; send_counts: [R*R] int32 device.  Rows of a receive
+ * buffer past the received count are left untouched.  topk in {1, 2};
+ * E <= 64; H % 64 == 0; F % 8 == 0.  A rank receiving more than cap rows sets
+ * FCC_ERR_CAPACITY in the status word and its rows past cap are dropped.
+ */
+fcc_status fcc_moe_dispatch_gemm(int R, const void *const *X, const float *const *logits,
+                                 const void *const *W, int64_t T, int64_t H, int64_t F, int E,
+                                 int topk, void *const *recv_x, void *const *recv_y,
+                                 int64_t cap, int32_t *const *topk_idx,
+                                 float *const *topk_gate, int32_t *expert_counts,
+                                 int32_t *send_counts, int32_t *const *recv_src, fcc_dtype in,
+                                 fcc_dtype out_dtype, const fcc_opts *opts,
+                                 fcc_stream_t stream);
+
+/* Scratch bytes a call needs (for opts->workspace); 0 if none. */
+size_t fcc_workspace_size(fcc_op op, int R, int64_t M, int64_t N, int64_t K,
+                          const fcc_opts *opts);
+size_t fcc_moe_workspace_size(int R, int64_t T, int64_t H, int64_t F, int E, int topk,
+                              int64_t cap, const fcc_opts *opts);
+
+/*
+ * Synchronises `stream`, then returns and clears the device status word of
+ * the current device (FCC_OK if no device-side error was recorded).
+ */
+fcc_status fcc_stream_status(fcc_stream_t stream);
+
+/* Static description of a status code. */
+const char *fcc_status_string(fcc_status s);
+
+/*
+ * InterDecom chunk-count model ("Compass: Dissecting Communication and
+ * Computation Operators for Efficient LLM Training", abstract: a model that
+ * derives the optimal decomposition degree; its formula is not given there).
+ * Two-stage pipeline, c chunks, per-chunk overhead alpha:
+ *   T(c) = max(G, X) + min(G, X) / c + c * alpha
+ * minimised at c* = sqrt(min(G, X) / alpha), rounded to the better integer
+ * neighbour and clamped to [1, max_chunks].  G = one-shot GEMM time, X =
+ * one-shot collective time (any consistent unit).
+ */
+int fcc_interdecom_chunks(double G, double X, double alpha, int max_chunks);
+double fcc_interdecom_time(double G, double X, double alpha, int chunks);
+
+/*
+ * Test support: launches one kernel whose bounded wait on a barrier that
+ * nothing completes runs out after timeout_ns; the kernel then records
+ * FCC_ERR_TIMEOUT in the status word and returns, leaving the context usable.
+ * fcc_stream_status() afterwards returns FCC_ERR_TIMEOUT.
+ */
+fcc_status fcc_test_wait_timeout(int64_t timeout_ns, fcc_stream_t stream);
+
+/* Number of kernels this library has launched in this process (all devices). */
+uint64_t fcc_launch_count(void);
+
+/* Library version, "major.minor.patch". */
+const char *fcc_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FCC_H_ */

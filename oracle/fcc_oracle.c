@@ -30,6 +30,7 @@
  */
 #include <math.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 
 #ifdef _OPENMP
@@ -100,13 +101,18 @@ int orc_gemm_rs_rows(int R, const uint16_t *const *A, const uint16_t *const *B,
     if (R < 1 || M % R != 0 || j < 0 || j >= R || nrows < 0)
         return 1;
     const int64_t Ms = M / R;
-    int rc = 0;
-    for (int64_t i = 0; i < nrows && rc == 0; ++i) {
-        if (local_rows[i] < 0 || local_rows[i] >= Ms)
+    int64_t *rows = (int64_t *)malloc(sizeof(int64_t) * (size_t)(nrows > 0 ? nrows : 1));
+    if (rows == NULL)
+        return 1;
+    for (int64_t i = 0; i < nrows; ++i) {
+        if (local_rows[i] < 0 || local_rows[i] >= Ms) {
+            free(rows);
             return 1;
-        const int64_t row = (int64_t)j * Ms + local_rows[i];
-        rc = orc_rank_sum_rows(R, A, B, M, N, K, &row, 1, out + i * N);
+        }
+        rows[i] = (int64_t)j * Ms + local_rows[i];
     }
+    const int rc = orc_rank_sum_rows(R, A, B, M, N, K, rows, nrows, out);
+    free(rows);
     return rc;
 }
 

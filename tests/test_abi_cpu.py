@@ -1,0 +1,105 @@
+"""CPU checks of the C ABI: the library loads without a GPU, exports every
+symbol include/fcc.h declares, rejects bad arguments before touching CUDA,
+and the InterDecom chunk model behaves as stated."""
+import ctypes
+import math
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fcc.h")
+
+
+@pytest.fixture(scope="module")
+def fcc():
+    import __graft_entry__
+    __graft_entry__.build()
+    import gemm_collective_gb300 as m
+    return m
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fcc_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(fcc):
+    names = _declared()
+    assert "fcc_gemm_rs" in names and "fcc_moe_dispatch_gemm" in names
+    lib = ctypes.CDLL(fcc.LIB_PATH)
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_library_needs_no_driver_to_load(fcc):
+    # Loaded above in a process that has no GPU: the CUDA runtime is static and
+    # the driver is resolved lazily.
+    assert fcc.fcc_version().count(".") == 2
+
+
+def test_status_strings(fcc):
+    assert fcc.fcc_status_string(fcc.FCC_OK) == "ok"
+    assert "timed out" in fcc.fcc_status_string(fcc.FCC_ERR_TIMEOUT)
+    assert fcc.fcc_status_string(99) == "unknown status"
+
+
+def test_invalid_arguments_rejected_without_cuda(fcc):
+    P = ctypes.c_void_p
+    two = (P * 2)(16, 32)
+    bad = (P * 2)(16, 33)
+    null = (P * 2)(16, 0)
+    cases = [
+        (0, two, two, two, 256, 256, 128, 0, 0),     # R = 0
+        (9, two, two, two, 256, 256, 128, 0, 0),     # R > 8
+        (2, two, two, two, 255, 256, 128, 0, 0),     # M % R
+        (2, two, two, two, 256, 250, 128, 0, 0),     # N % 8
+        (2, two, two, two, 256, 256, 100, 0, 0),     # K % 8
+        (2, bad, two, two, 256, 256, 128, 0, 0),     # misaligned A
+        (2, two, null, two, 256, 256, 128, 0, 0),    # null B
+        (2, two, two, bad, 256, 256, 128, 0, 0),     # misaligned output
+        (2, two, two, two, 0, 256, 128, 0, 0),       # empty M
+        (2, two, two, two, 256, 256, 128, 5, 0),     # bad input dtype
+        (2, two, two, two, 256, 256, 128, 0, 7),     # bad output dtype
+    ]
+    for c in cases:
+        st = fcc.raw_status("fcc_gemm_rs", *c, None, None)
+        assert st == fcc.FCC_ERR_INVALID, c
+    # unsupported input dtype (f16 inputs are not implemented)
+    assert fcc.raw_status("fcc_gemm_rs", 2, two, two, two, 256, 256, 128, 1, 0, None,
+                          None) == fcc.FCC_ERR_UNSUPPORTED
+    # GEMV: more than 16 tokens
+    assert fcc.raw_status("fcc_gemv_ar", 2, two, two, two, 17, 256, 128, 0, 2, None,
+                          None) == fcc.FCC_ERR_INVALID
+    # AG: M % R
+    assert fcc.raw_status("fcc_ag_gemm", 2, two, two, two, None, 255, 256, 128, 0, 0, None,
+                          None) == fcc.FCC_ERR_INVALID
+    assert fcc.fcc_launch_count() == 0
+
+
+def test_interdecom_model(fcc):
+    # T(c) = max(G,X) + min(G,X)/c + c*alpha, minimised near sqrt(min/alpha)
+    G, X, a = 1000.0, 400.0, 4.0
+    c = fcc.fcc_interdecom_chunks(G, X, a, 64)
+    assert c == 10  # sqrt(400/4) = 10
+    t = [fcc.fcc_interdecom_time(G, X, a, k) for k in range(1, 65)]
+    assert t.index(min(t)) + 1 == c
+    assert math.isclose(fcc.fcc_interdecom_time(G, X, a, 1), G + X + a)
+    assert fcc.fcc_interdecom_chunks(G, X, a, 4) == 4      # clamped
+    assert fcc.fcc_interdecom_chunks(G, X, 1e9, 64) == 1   # overhead dominates
+    assert fcc.fcc_interdecom_chunks(G, X, 0.0, 16) == 16  # free chunks: as many as allowed
+    for G, X, a in [(10.0, 90.0, 0.3), (5.0, 5.0, 0.01), (300.0, 1.0, 0.02)]:
+        c = fcc.fcc_interdecom_chunks(G, X, a, 128)
+        t = [fcc.fcc_interdecom_time(G, X, a, k) for k in range(1, 129)]
+        assert math.isclose(t[c - 1], min(t)), (G, X, a, c)
+
+
+def test_workspace_sizes(fcc):
+    o = fcc.make_opts(algo=fcc.FCC_ALGO_UNFUSED)
+    assert fcc.fcc_workspace_size(fcc.FCC_OP_GEMM_RS, 8, 8192, 8192, 3584, o) >= 8 * 8192 * 8192 * 4
+    assert fcc.fcc_workspace_size(fcc.FCC_OP_GEMM_RS, 8, 8192, 8192, 3584, None) == 0
+    o = fcc.make_opts(algo=fcc.FCC_ALGO_CE)
+    assert fcc.fcc_workspace_size(fcc.FCC_OP_GEMM_RS, 2, 256, 256, 128, o) >= 2 * 2 * 256 * 256 * 4
+    assert fcc.fcc_workspace_size(fcc.FCC_OP_AG_GEMM, 8, 8192, 3584, 8192, None) == 0

@@ -1,0 +1,285 @@
+"""GPU parity: fused GEMM + ReduceScatter / AllReduce / AllGather against the oracle.
+
+Every case calls the library through its C ABI (the ctypes binding) and
+compares element by element with the fp64 CPU oracle on the same seeded
+inputs.  Small shapes cover several tiles and ragged tails in M, N and K;
+the full-size row-parallel MLP shape (8 ranks, 8192 x 8192 x 3584) is checked
+on sampled rows the oracle computes one by one.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from tests.gpu_util import assert_close, bits, dev_bf16, empty, to_f64
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():  # pragma: no cover - CPU container
+    pytest.skip("needs a GPU", allow_module_level=True)
+
+import gemm_collective_gb300 as fcc  # noqa: E402
+
+
+def _upload(A, B):
+    return [dev_bf16(a) for a in A], [dev_bf16(b) for b in B]
+
+
+def _rs(R, dA, dB, M, N, K, out_dtype, opts=None):
+    tdt = torch.float32 if out_dtype == fcc.FCC_F32 else torch.bfloat16
+    outs = [empty((M // R, N), tdt, fill=float("nan")) for _ in range(R)]
+    fcc.fcc_gemm_rs(R, dA, dB, outs, M, N, K, fcc.FCC_BF16, out_dtype, opts)
+    assert fcc.fcc_stream_status() == fcc.FCC_OK
+    return outs
+
+
+def _ar(R, dA, dB, M, N, K, out_dtype, opts=None):
+    tdt = torch.float32 if out_dtype == fcc.FCC_F32 else torch.bfloat16
+    outs = [empty((M, N), tdt, fill=float("nan")) for _ in range(R)]
+    fcc.fcc_gemm_ar(R, dA, dB, outs, M, N, K, fcc.FCC_BF16, out_dtype, opts)
+    assert fcc.fcc_stream_status() == fcc.FCC_OK
+    return outs
+
+
+# ------------------------------------------------------------ exactness first
+
+def test_rs_integer_inputs_bit_exact():
+    """Small integers: every f32 partial sum is exact, so GPU == oracle exactly."""
+    R, M, N, K = 2, 256, 256, 128
+    A, B = synth.integer_gemm_inputs(R, M, N, K, -4, 4, seed=1)
+    dA, dB = _upload(A, B)
+    outs = _rs(R, dA, dB, M, N, K, fcc.FCC_F32)
+    for j in range(R):
+        assert np.array_equal(to_f64(outs[j]), oracle.gemm_rs(A, B, j)), f"shard {j}"
+
+
+def test_rs_one_hot_selects_b_rows():
+    """A_r one-hot: the output is a sum of exact B rows (catches layout/descriptor errors)."""
+    R, M, N, K = 2, 128, 512, 256
+    rng = np.random.Generator(np.random.PCG64(2))
+    A, B = [], []
+    for r in range(R):
+        a = np.zeros((M, K), np.float32)
+        a[np.arange(M), rng.integers(0, K, M)] = 1.0
+        A.append(synth.f32_to_bf16_bits(a))
+        B.append(synth.integer_bf16(rng, (K, N), -8, 8))
+    dA, dB = _upload(A, B)
+    outs = _rs(R, dA, dB, M, N, K, fcc.FCC_F32)
+    for j in range(R):
+        assert np.array_equal(to_f64(outs[j]), oracle.gemm_rs(A, B, j))
+
+
+# ------------------------------------------------------ the 2-rank workload
+
+def test_rs_two_rank_workload_f32():
+    w = synth.WORKLOADS["gemm_rs_r2_256x256x128"]
+    A, B = synth.gemm_inputs(w.R, w.M, w.N, w.K, w.std_a, w.std_b, seed=0)
+    dA, dB = _upload(A, B)
+    outs = _rs(w.R, dA, dB, w.M, w.N, w.K, fcc.FCC_F32)
+    for j in range(w.R):
+        fro, mx = assert_close(to_f64(outs[j]), oracle.gemm_rs(A, B, j), f"shard {j}")
+        assert fro < 1e-5  # f32 output: only f32 accumulation rounding
+    again = _rs(w.R, dA, dB, w.M, w.N, w.K, fcc.FCC_F32)
+    for j in range(w.R):
+        assert np.array_equal(bits(outs[j]), bits(again[j])), "not bitwise repeatable"
+
+
+# ------------------------------------------------------------ ragged shapes
+
+RAGGED = [
+    (3, 360, 200, 72),     # shard rows 120, N and K not tile multiples
+    (1, 136, 264, 8),      # one rank, K = 8
+    (4, 512, 1032, 200),   # several tiles in M and N, ragged N
+    (8, 1024, 520, 136),
+]
+
+
+@pytest.mark.parametrize("R,M,N,K", RAGGED)
+@pytest.mark.parametrize("out_dtype", [0, 2])
+def test_rs_ragged(R, M, N, K, out_dtype):
+    A, B = synth.gemm_inputs(R, M, N, K, 1.0, 1.0, seed=R * 7 + K)
+    dA, dB = _upload(A, B)
+    outs = _rs(R, dA, dB, M, N, K, out_dtype)
+    for j in range(R):
+        assert_close(to_f64(outs[j]), oracle.gemm_rs(A, B, j), f"shard {j}")
+
+
+@pytest.mark.parametrize("R,M,N,K", [(4, 200, 264, 136), (2, 130, 16, 64), (8, 256, 256, 64)])
+def test_ar_all_buffers_identical_and_equal_rs(R, M, N, K):
+    A, B = synth.gemm_inputs(R, M, N, K, 1.0, 1.0, seed=3)
+    dA, dB = _upload(A, B)
+    outs = _ar(R, dA, dB, M, N, K, fcc.FCC_BF16)
+    ref = oracle.gemm_ar(A, B)
+    assert_close(to_f64(outs[0]), ref, "ar")
+    for r in range(1, R):
+        assert np.array_equal(bits(outs[r]), bits(outs[0])), f"rank {r} differs"
+    if M % R == 0:
+        shards = _rs(R, dA, dB, M, N, K, fcc.FCC_BF16)
+        cat = np.concatenate([bits(s) for s in shards])
+        assert np.array_equal(cat, bits(outs[0])), "RS shards != AR rows (deterministic mode)"
+
+
+def test_rank_permutation_within_tolerance():
+    R, M, N, K = 4, 256, 512, 128
+    A, B = synth.gemm_inputs(R, M, N, K, 1.0, 1.0, seed=5)
+    perm = [2, 0, 3, 1]
+    dA, dB = _upload(A, B)
+    a = _ar(R, dA, dB, M, N, K, fcc.FCC_F32)[0]
+    b = _ar(R, [dA[p] for p in perm], [dB[p] for p in perm], M, N, K, fcc.FCC_F32)[0]
+    assert_close(to_f64(b), to_f64(a), "permuted")
+
+
+# ------------------------------------------------------- other algorithms
+
+ALGOS = [
+    ("push", dict(algo=1, deterministic=0)),
+    ("unfused", dict(algo=2)),
+    ("interdecom4", dict(algo=3, chunks=4)),
+    ("interdecom_model", dict(algo=3, chunks=0)),
+    ("ce", dict(algo=4)),
+]
+
+
+@pytest.mark.parametrize("name,kw", ALGOS)
+@pytest.mark.parametrize("out_dtype", [0, 2])
+def test_rs_algorithms(name, kw, out_dtype):
+    R, M, N, K = 4, 640, 520, 192
+    A, B = synth.gemm_inputs(R, M, N, K, 1.0, 1.0, seed=11)
+    dA, dB = _upload(A, B)
+    outs = _rs(R, dA, dB, M, N, K, out_dtype, fcc.make_opts(**kw))
+    for j in range(R):
+        assert_close(to_f64(outs[j]), oracle.gemm_rs(A, B, j), f"{name} shard {j}")
+
+
+@pytest.mark.parametrize("name,kw", ALGOS)
+def test_ar_algorithms(name, kw):
+    R, M, N, K = 3, 264, 256, 128
+    A, B = synth.gemm_inputs(R, M, N, K, 1.0, 1.0, seed=12)
+    dA, dB = _upload(A, B)
+    ref = oracle.gemm_ar(A, B)
+    for out_dtype in (0, 2):
+        outs = _ar(R, dA, dB, M, N, K, out_dtype, fcc.make_opts(**kw))
+        for r in range(R):
+            assert_close(to_f64(outs[r]), ref, f"{name} rank {r}")
+
+
+def test_caller_workspace_and_too_small():
+    R, M, N, K = 2, 256, 256, 64
+    A, B = synth.gemm_inputs(R, M, N, K, 1.0, 1.0, seed=13)
+    dA, dB = _upload(A, B)
+    o = fcc.make_opts(algo=fcc.FCC_ALGO_UNFUSED)
+    need = fcc.fcc_workspace_size(fcc.FCC_OP_GEMM_RS, R, M, N, K, o)
+    assert need >= R * M * N * 4
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    o = fcc.make_opts(algo=fcc.FCC_ALGO_UNFUSED, workspace=ws, workspace_bytes=need)
+    outs = _rs(R, dA, dB, M, N, K, fcc.FCC_F32, o)
+    for j in range(R):
+        assert_close(to_f64(outs[j]), oracle.gemm_rs(A, B, j))
+    small = fcc.make_opts(algo=fcc.FCC_ALGO_UNFUSED, workspace=ws, workspace_bytes=need - 256)
+    with pytest.raises(fcc.FccError) as e:
+        _rs(R, dA, dB, M, N, K, fcc.FCC_F32, small)
+    assert e.value.status == fcc.FCC_ERR_WORKSPACE
+
+
+# ----------------------------------------------------------------- AG + GEMM
+
+@pytest.mark.parametrize("R,Ms,N,K", [(4, 136, 200, 96), (2, 128, 512, 64), (8, 64, 264, 136)])
+@pytest.mark.parametrize("algo", [1, 2, 4])
+def test_ag_gemm(R, Ms, N, K, algo):
+    X, B = synth.gemm_inputs(R, Ms, N, K, 1.0, 1.0, seed=17 + R)
+    dX, dB = _upload(X, B)
+    M = R * Ms
+    outs = [empty((M, N), torch.bfloat16, fill=float("nan")) for _ in range(R)]
+    gath = [empty((M, K), torch.bfloat16, fill=0.0) for _ in range(R)]
+    fcc.fcc_ag_gemm(R, dX, dB, outs, gath, M, N, K, fcc.FCC_BF16, fcc.FCC_BF16,
+                    fcc.make_opts(algo=algo))
+    assert fcc.fcc_stream_status() == fcc.FCC_OK
+    full = np.concatenate(X)
+    for r in range(R):
+        assert_close(to_f64(outs[r]), oracle.ag_gemm(X, B, r), f"rank {r}")
+        assert np.array_equal(bits(gath[r]).view(np.uint16), full), f"gathered copy {r}"
+
+
+def test_ag_gemm_without_gathered_output():
+    R, Ms, N, K = 2, 200, 256, 128
+    X, B = synth.gemm_inputs(R, Ms, N, K, 1.0, 1.0, seed=23)
+    dX, dB = _upload(X, B)
+    M = R * Ms
+    outs = [empty((M, N), torch.float32) for _ in range(R)]
+    fcc.fcc_ag_gemm(R, dX, dB, outs, None, M, N, K, fcc.FCC_BF16, fcc.FCC_F32)
+    assert fcc.fcc_stream_status() == fcc.FCC_OK
+    for r in range(R):
+        assert_close(to_f64(outs[r]), oracle.ag_gemm(X, B, r))
+
+
+# ------------------------------------------------------------- full sizes
+
+def _sample_rows(n, k, seed):
+    rng = np.random.Generator(np.random.PCG64(seed))
+    rows = set(rng.choice(n, size=k - 3, replace=False).tolist())
+    rows |= {0, n - 1, n // 2}
+    return np.array(sorted(rows), dtype=np.int64)
+
+
+def test_rs_full_size_sampled_rows():
+    """The 8-rank 8192x8192x3584 workload, bf16 shards, in the benchmark's launch shape."""
+    w = synth.WORKLOADS["gemm_rs_r8_8192x8192x3584"]
+    A, B = synth.gemm_inputs(w.R, w.M, w.N, w.K, w.std_a, w.std_b, seed=0)
+    dA, dB = _upload(A, B)
+    outs = _rs(w.R, dA, dB, w.M, w.N, w.K, fcc.FCC_BF16)
+    Ms = w.M // w.R
+    for j in range(w.R):
+        rows = _sample_rows(Ms, 8, seed=j)
+        got = to_f64(outs[j][torch.from_numpy(rows).cuda()])
+        assert_close(got, oracle.gemm_rs(A, B, j, rows), f"shard {j}")
+    # every element finite and the shards bitwise repeatable
+    again = _rs(w.R, dA, dB, w.M, w.N, w.K, fcc.FCC_BF16)
+    for j in range(w.R):
+        assert torch.isfinite(outs[j].float()).all()
+        assert torch.equal(outs[j].view(torch.int16), again[j].view(torch.int16))
+
+
+def test_ag_full_size_sampled_rows():
+    w = synth.WORKLOADS["ag_gemm_r8_8192x3584x8192"]
+    Ms = w.M // w.R
+    X, B = synth.gemm_inputs(w.R, Ms, w.N, w.K, w.std_a, w.std_b, seed=0)
+    dX, dB = _upload(X, B)
+    outs = [empty((w.M, w.N), torch.bfloat16, fill=float("nan")) for _ in range(w.R)]
+    fcc.fcc_ag_gemm(w.R, dX, dB, outs, None, w.M, w.N, w.K, fcc.FCC_BF16, fcc.FCC_BF16)
+    assert fcc.fcc_stream_status() == fcc.FCC_OK
+    for r in range(w.R):
+        rows = _sample_rows(w.M, 12, seed=100 + r)
+        got = to_f64(outs[r][torch.from_numpy(rows).cuda()])
+        assert_close(got, oracle.ag_gemm(X, B, r, rows), f"rank {r}")
+        assert torch.isfinite(outs[r].float()).all()
+
+
+# --------------------------------------------------------- error reporting
+
+def test_bounded_wait_reports_timeout_and_context_survives():
+    fcc.fcc_test_wait_timeout(2_000_000)  # 2 ms on a barrier nothing completes
+    assert fcc.fcc_stream_status() == fcc.FCC_ERR_TIMEOUT
+    assert fcc.fcc_stream_status() == fcc.FCC_OK  # cleared
+    R, M, N, K = 2, 256, 256, 128
+    A, B = synth.integer_gemm_inputs(R, M, N, K, -2, 2, seed=4)
+    dA, dB = _upload(A, B)
+    outs = _rs(R, dA, dB, M, N, K, fcc.FCC_F32)
+    assert np.array_equal(to_f64(outs[1]), oracle.gemm_rs(A, B, 1))
+
+
+def test_invalid_arguments_rejected_before_launch():
+    R, M, N, K = 2, 256, 256, 128
+    A, B = synth.gemm_inputs(R, M, N, K, 1.0, 1.0)
+    dA, dB = _upload(A, B)
+    outs = [empty((M // R, N)) for _ in range(R)]
+    before = fcc.fcc_launch_count()
+    for args in [(0, dA, dB, outs, M, N, K), (2, dA, dB, outs, 255, N, K),
+                 (2, dA, dB, outs, M, N, 100), (2, dA, dB, outs, M, 250, K)]:
+        with pytest.raises(fcc.FccError) as e:
+            fcc.fcc_gemm_rs(*args)
+        assert e.value.status == fcc.FCC_ERR_INVALID
+    with pytest.raises(fcc.FccError) as e:
+        fcc.fcc_gemm_rs(R, [dA[0], dA[1].data_ptr() + 2], dB, outs, M, N, K)
+    assert e.value.status == fcc.FCC_ERR_INVALID
+    assert fcc.fcc_launch_count() == before
