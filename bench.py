@@ -48,6 +48,7 @@ def parse():
                     help="target CPU time of the oracle sample (cpu_baseline)")
     ap.add_argument("--ref-seconds", type=float, default=90.0,
                     help="target CPU time of the whole --impl reference run")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg")
     return ap.parse_args()
 
 
@@ -286,6 +287,70 @@ def time_calls(fn, steps, warmup, stream):
     return s.elapsed_time(e) / steps  # ms
 
 
+def other_ops(fcc, torch, np, synth, dev, stream, dA_rs, dB_rs, pk):
+    """The other fused operators at their workload sizes, each with its baselines."""
+    ops = {}
+    hbm = pk["hbm_gbs"]
+    tc = pk["bf16_tflops"]
+
+    def up(a):
+        return torch.from_numpy(a.view(np.int16)).to(dev)
+
+    # GEMM + AllReduce on the same 8-rank 8192x8192x3584 inputs
+    w = synth.WORKLOADS["gemm_ar_r8_8192x8192x3584"]
+    R, M, N, K = w.R, w.M, w.N, w.K
+    dA = dA_rs  # the same A_r and B_r as the reduce-scatter leg
+    outs = [torch.empty((M, N), dtype=torch.bfloat16, device=dev) for _ in range(R)]
+    res = {}
+    for name, o in [("fused", None), ("unfused", fcc.make_opts(algo=fcc.FCC_ALGO_UNFUSED)),
+                    ("copy_engine", fcc.make_opts(algo=fcc.FCC_ALGO_CE))]:
+        t = time_calls(lambda o=o: fcc.fcc_gemm_ar(R, dA, dB_rs, outs, M, N, K, 0, 0, o, stream),
+                       10, 3, stream)
+        res[name] = {"ms": t, "TFLOP/s": w.flops() / (t * 1e-3) / 1e12}
+    res["roofline_frac"] = res["fused"]["TFLOP/s"] / tc
+    ops[w.name] = res
+    del outs, dA
+
+    # GEMV + AllReduce (decode); B_r reuses the RS leg's 3584x8192 N(0, 0.02) weights
+    w = synth.WORKLOADS["gemv_ar_r8_8x8192x3584"]
+    R, M, N, K = w.R, w.M, w.N, w.K
+    rng = np.random.Generator(np.random.PCG64(7))
+    dA = [up(synth.normal_bf16(rng, (M, K), 1.0)) for _ in range(R)]
+    outs = [torch.empty((M, N), dtype=torch.float32, device=dev) for _ in range(R)]
+    byts = R * (K * N * 2 + M * K * 2 + M * N * 4)
+    res = {}
+    for name, o in [("fused", None), ("unfused", fcc.make_opts(algo=fcc.FCC_ALGO_UNFUSED)),
+                    ("copy_engine", fcc.make_opts(algo=fcc.FCC_ALGO_CE))]:
+        t = time_calls(lambda o=o: fcc.fcc_gemv_ar(R, dA, dB_rs, outs, M, N, K, 0, 2, o, stream),
+                       50, 5, stream)
+        res[name] = {"us": t * 1e3, "GB/s": byts / (t * 1e-3) / 1e9}
+    res["roofline_frac"] = res["fused"]["GB/s"] / hbm
+    res["algorithmic_bytes"] = byts
+    ops[w.name] = res
+    del outs, dA
+
+    # AllGather + GEMM
+    w = synth.WORKLOADS["ag_gemm_r8_8192x3584x8192"]
+    R, M, N, K = w.R, w.M, w.N, w.K
+    X, Bx = synth.gemm_inputs(R, M // R, N, K, w.std_a, w.std_b, seed=0)
+    dX = [up(x) for x in X]
+    dBx = [up(b) for b in Bx]
+    outs = [torch.empty((M, N), dtype=torch.bfloat16, device=dev) for _ in range(R)]
+    res = {}
+    for name, o in [("fused", None), ("unfused", fcc.make_opts(algo=fcc.FCC_ALGO_UNFUSED)),
+                    ("copy_engine", fcc.make_opts(algo=fcc.FCC_ALGO_CE))]:
+        t = time_calls(lambda o=o: fcc.fcc_ag_gemm(R, dX, dBx, outs, None, M, N, K, 0, 0, o,
+                                                   stream), 10, 3, stream)
+        res[name] = {"ms": t, "TFLOP/s": w.flops() / (t * 1e-3) / 1e12}
+    res["roofline_frac"] = res["fused"]["TFLOP/s"] / tc
+    ops[w.name] = res
+    del outs, dX, dBx
+    st = fcc.fcc_stream_status(stream)
+    if st != fcc.FCC_OK:
+        raise RuntimeError(f"device status after the operator legs: {fcc.fcc_status_string(st)}")
+    return ops
+
+
 def run_fcc(args, world, rank, local, pg):
     import numpy as np
     import torch
@@ -367,11 +432,14 @@ def run_fcc(args, world, rank, local, pg):
         for h, d in zip(hO, outs):
             h.copy_(d, non_blocking=True)
 
-    e2e_steps = max(3, min(args.steps, 20))
-    barrier(pg)
-    e2e_ms = max_over_ranks(time_calls(e2e_step, e2e_steps, 3, stream), pg)
-    e2e = {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
-           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+    e2e = None
+    if not args.no_e2e:
+        e2e_steps = max(3, min(args.steps, 20))
+        barrier(pg)
+        e2e_ms = max_over_ranks(time_calls(e2e_step, e2e_steps, 3, stream), pg)
+        e2e = {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+    del hA, hB, hO
 
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
@@ -403,9 +471,12 @@ def run_fcc(args, world, rank, local, pg):
                                        "note": "one library GEMM of the same FLOPs, no collective"}
         del Acat, Bcat
         line["baselines"] = base
+        line["ops"] = other_ops(fcc, torch, np, synth, dev, stream, dA, dB, pk)
 
     # ---- CPU oracle on a bounded sample (rank 0 only)
-    if rank == 0:
+    if rank == 0 and args.cpu_seconds <= 0:
+        print(json.dumps(line), flush=True)
+    elif rank == 0:
         got = [o.float().cpu().numpy().astype(np.float64) for o in outs]
         per_row, threads = oracle_seconds_per_row(A, B)
         rps = int(max(1, min(M // R, args.cpu_seconds / max(per_row * R, 1e-9))))
