@@ -82,6 +82,8 @@ def test_gemv_full_decode_workload():
     outs = _run(w.R, A, B, w.M, w.N, w.K)
     ref = oracle.gemv_ar(A, B)
     fro, mx = assert_close(to_f64(outs[0]), ref, "decode workload")
-    assert fro < 1e-5  # f32 output
+    # f32 output: only f32 accumulation rounding over K' = R*K = 28672 terms,
+    # typically ~sqrt(K') * 2^-24 = 1e-5 relative; 1e-4 leaves a 10x margin.
+    assert fro < 1e-4
     for r in range(1, w.R):
         assert np.array_equal(bits(outs[r]), bits(outs[0]))
