@@ -78,6 +78,8 @@ def _sig(name, res, args):
 _gemm_rs = _sig("fcc_gemm_rs", _I, [_I, _P, _P, _P, _I64, _I64, _I64, _I, _I, _OPTS, _P])
 _gemm_ar = _sig("fcc_gemm_ar", _I, [_I, _P, _P, _P, _I64, _I64, _I64, _I, _I, _OPTS, _P])
 _gemv_ar = _sig("fcc_gemv_ar", _I, [_I, _P, _P, _P, _I64, _I64, _I64, _I, _I, _OPTS, _P])
+_gemv_ar_static = _sig("fcc_gemv_ar_static", _I,
+                       [_I, _P, _P, _P, _I64, _I64, _I64, _I, _I, _OPTS, _P])
 _ag_gemm = _sig("fcc_ag_gemm", _I, [_I, _P, _P, _P, _P, _I64, _I64, _I64, _I, _I, _OPTS, _P])
 _moe = _sig("fcc_moe_dispatch_gemm", _I,
             [_I, _P, _P, _P, _I64, _I64, _I64, _I, _I, _P, _P, _I64, _P, _P, _P, _P, _P, _I, _I,
@@ -146,6 +148,13 @@ def fcc_gemv_ar(R, A, B, out, M, N, K, in_dtype=FCC_BF16, out_dtype=FCC_F32, opt
                 stream=None):
     _check(_gemv_ar(R, _ptrs(A), _ptrs(B), _ptrs(out), M, N, K, in_dtype, out_dtype,
                     _opts(opts), _stream(stream)), "fcc_gemv_ar")
+
+
+def fcc_gemv_ar_static(R, A, B, out, M, N, K, in_dtype=FCC_BF16, out_dtype=FCC_F32, opts=None,
+                       stream=None):
+    """fcc_gemv_ar with its scratch in the library's static device array (no allocation)."""
+    _check(_gemv_ar_static(R, _ptrs(A), _ptrs(B), _ptrs(out), M, N, K, in_dtype, out_dtype,
+                           _opts(opts), _stream(stream)), "fcc_gemv_ar_static")
 
 
 def fcc_ag_gemm(R, X_shard, B, out, gathered, M, N, K, in_dtype=FCC_BF16, out_dtype=FCC_BF16,

@@ -689,3 +689,50 @@ fcc_status fcc_test_wait_timeout(int64_t timeout_ns, fcc_stream_t stream) {
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------------
+// Helpers for entry points that must not create streams, events or pools:
+// they only look up what already exists (driver entry point, symbol addresses).
+namespace fcc {
+
+fcc_status light_encoder_ready() {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_encode != nullptr) return FCC_OK;
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                       &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || fn == nullptr)
+    return FCC_ERR_CUDA;
+  g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  return FCC_OK;
+}
+
+fcc_status light_make_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols,
+                          uint32_t box_rows) {
+  fcc_status s = light_encoder_ready();
+  if (s != FCC_OK) return s;
+  return make_map(m, ptr, rows, cols, box_rows);
+}
+
+fcc_status light_status_word(int** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FCC_ERR_CUDA;
+  static int* cached[kMaxDevices] = {};
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (cached[dev] == nullptr) {
+    if (cudaGetSymbolAddress(reinterpret_cast<void**>(&cached[dev]), g_status_word) != cudaSuccess)
+      return FCC_ERR_CUDA;
+  }
+  *out = cached[dev];
+  return FCC_OK;
+}
+
+fcc_status light_check_gemm(int R, const void* const* A, const void* const* B, int64_t M,
+                            int64_t N, int64_t K, fcc_dtype in) {
+  return check_gemm(R, A, B, M, N, K, in);
+}
+
+void count_launch() { g_launches.fetch_add(1); }
+
+}  // namespace fcc

@@ -19,6 +19,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <cstring>
+
 #include "fcc_internal.h"
 #include "fcc_ptx.cuh"
 
@@ -258,3 +260,119 @@ cudaError_t launch_gemv(const GemvParams& p, int grid, cudaStream_t st) {
 }
 
 }  // namespace fcc
+
+// ---------------------------------------------------------------------------
+// fcc_gemv_ar_static: the same GEMV + AllReduce kernel with its scratch (the
+// per-CTA partial sums and the per-slab arrival tickets) in a fixed device
+// array of this file instead of caller or pool memory, for callers that cannot
+// allocate device memory.  The array lives on every GPU that loads the library
+// until the process exits.
+#include <mutex>
+
+namespace fcc {
+namespace {
+
+constexpr size_t kStaticScratchBytes = size_t(4) << 20;  // 4 MiB in total
+constexpr size_t kStaticTicketBytes = 4096;              // tickets: up to 1024 slabs
+constexpr size_t kSlotBytes = size_t(kTok) * kSlab * 4;  // one partial: 16 x 128 f32
+
+__device__ __align__(256) unsigned char g_gemv_static_scratch[kStaticScratchBytes];
+
+struct StaticScratchDev {
+  bool ready = false;
+  unsigned char* ptr = nullptr;  // device address of g_gemv_static_scratch
+  int sms = 0;
+};
+StaticScratchDev g_static_dev[64];
+std::mutex g_static_mu;
+
+// Once per device, with that device current: look up the array's device
+// address (host code cannot use the symbol itself as a pointer) and the SM count.
+fcc_status static_scratch_for_current_device(unsigned char** ptr, int* sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return FCC_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_static_mu);
+  StaticScratchDev& s = g_static_dev[dev];
+  if (!s.ready) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_gemv_static_scratch) != cudaSuccess || p == nullptr)
+      return FCC_ERR_CUDA;
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return FCC_ERR_CUDA;
+    s.ptr = static_cast<unsigned char*>(p);
+    s.sms = n;
+    s.ready = true;
+  }
+  *ptr = s.ptr;
+  *sms = s.sms;
+  return FCC_OK;
+}
+
+}  // namespace
+}  // namespace fcc
+
+extern "C" fcc_status fcc_gemv_ar_static(int R, const void* const* A, const void* const* B,
+                                         void* const* out, int64_t M, int64_t N, int64_t K,
+                                         fcc_dtype in, fcc_dtype out_dtype, const fcc_opts* opts,
+                                         fcc_stream_t stream) {
+  using namespace fcc;
+  fcc_status s = light_check_gemm(R, A, B, M, N, K, in);
+  if (s != FCC_OK) return s;
+  if (M > kTok) return FCC_ERR_INVALID;
+  if (out_dtype != FCC_BF16 && out_dtype != FCC_F32)
+    return out_dtype == FCC_F16 ? FCC_ERR_UNSUPPORTED : FCC_ERR_INVALID;
+  if (out == nullptr) return FCC_ERR_INVALID;
+  for (int r = 0; r < R; ++r)
+    if (out[r] == nullptr || (reinterpret_cast<uintptr_t>(out[r]) & 15u) != 0)
+      return FCC_ERR_INVALID;
+  if (opts != nullptr && opts->algo != FCC_ALGO_AUTO && opts->algo != FCC_ALGO_FUSED)
+    return FCC_ERR_UNSUPPORTED;
+
+  unsigned char* scratch = nullptr;
+  int sms = 0;
+  if ((s = static_scratch_for_current_device(&scratch, &sms)) != FCC_OK) return s;
+  int* status = nullptr;
+  if ((s = light_status_word(&status)) != FCC_OK) return s;
+
+  const int slabs = static_cast<int>((N + kSlab - 1) / kSlab);
+  const int kb = static_cast<int>((K + kBK - 1) / kBK);
+  const long long units = static_cast<long long>(slabs) * R * kb;
+  int grid = sms;
+  if (opts != nullptr && opts->max_ctas > 0 && opts->max_ctas < grid) grid = opts->max_ctas;
+  if (units < grid) grid = static_cast<int>(units);
+  // Size limit of the static array: tickets for every slab, one partial slot
+  // per (slab, contributing CTA) pair, of which there are at most slabs + grid.
+  if (static_cast<size_t>(slabs) * 4 > kStaticTicketBytes ||
+      static_cast<size_t>(slabs + grid) * kSlotBytes > kStaticScratchBytes - kStaticTicketBytes)
+    return FCC_ERR_WORKSPACE;
+
+  GemvParams p;
+  std::memset(&p, 0, sizeof(p));
+  for (int r = 0; r < R; ++r) {
+    if ((s = light_make_map(&p.mapA[r], A[r], M, K, kTok)) != FCC_OK) return s;
+    if ((s = light_make_map(&p.mapB[r], B[r], K, N, kBK)) != FCC_OK) return s;
+    p.out[r] = out[r];
+  }
+  p.R = R;
+  p.M = static_cast<int>(M);
+  p.N = static_cast<int>(N);
+  p.K = static_cast<int>(K);
+  p.kb_per_rank = kb;
+  p.slabs = slabs;
+  p.units = units;
+  p.out_f32 = out_dtype == FCC_F32 ? 1 : 0;
+  p.tickets = reinterpret_cast<int*>(scratch);
+  p.partials = reinterpret_cast<float*>(scratch + kStaticTicketBytes);
+  p.status = status;
+  p.timeout_ns = (opts != nullptr && opts->timeout_ns > 0)
+                     ? static_cast<unsigned long long>(opts->timeout_ns)
+                     : 1000ull * 1000 * 1000;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  // The array keeps the previous call's contents: the tickets must start at zero.
+  if (cudaMemsetAsync(p.tickets, 0, static_cast<size_t>(slabs) * 4, st) != cudaSuccess)
+    return FCC_ERR_CUDA;
+  if (launch_gemv(p, grid, st) != cudaSuccess) return FCC_ERR_CUDA;
+  count_launch();
+  return FCC_OK;
+}

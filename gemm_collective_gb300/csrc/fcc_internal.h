@@ -82,3 +82,14 @@ int device_sm_count();
 uint64_t bump_launch_count(uint64_t n);
 
 }  // namespace fcc
+
+namespace fcc {
+// Look-up-only helpers (no streams, events or device memory are created).
+fcc_status light_encoder_ready();
+fcc_status light_make_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols,
+                          uint32_t box_rows);
+fcc_status light_status_word(int** out);
+fcc_status light_check_gemm(int R, const void* const* A, const void* const* B, int64_t M,
+                            int64_t N, int64_t K, fcc_dtype in);
+void count_launch();
+}  // namespace fcc

@@ -126,6 +126,30 @@ fcc_status fcc_gemv_ar(int R, const void *const *A, const void *const *B, void *
                        const fcc_opts *opts, fcc_stream_t stream);
 
 /*
+ * GEMV + AllReduce that allocates nothing.  The pages have no counterpart:
+ * this is an addition for callers that cannot call cudaMalloc -- a process
+ * whose device memory is already reserved by its own allocator, or a
+ * latency-critical path that cannot take cudaMalloc/cudaFree's implicit
+ * device synchronisation.  Same arguments and results as fcc_gemv_ar; the
+ * caller passes inputs and outputs, and the kernel's scratch (partial sums
+ * and arrival tickets) is a 4 MiB static device array inside the library,
+ * held on every GPU that loads the library until the process exits.
+ *  - Limit: (ceil(N/128) + CTAs) * 8 KiB <= 4 MiB - 4 KiB, i.e. N <= 45,952
+ *    with one CTA per SM on a 152-SM GB300 (fewer CTAs via opts->max_ctas
+ *    allow more); beyond it the call returns FCC_ERR_WORKSPACE and launches
+ *    nothing.  opts->workspace is ignored; algo must be AUTO or FUSED.
+ *  - The first call on a device looks up the array's device address and the
+ *    SM count (cudaGetSymbolAddress, cudaDeviceGetAttribute) with that device
+ *    current; make that first call before any stream capture.
+ *  - Every call uses the same array and clears its tickets (cudaMemsetAsync)
+ *    first.  Calls that overlap on the GPU (other streams, other threads)
+ *    race on the array: serialise them.
+ */
+fcc_status fcc_gemv_ar_static(int R, const void *const *A, const void *const *B,
+                              void *const *out, int64_t M, int64_t N, int64_t K, fcc_dtype in,
+                              fcc_dtype out_dtype, const fcc_opts *opts, fcc_stream_t stream);
+
+/*
  * AllGather + GEMM (mKernel article, fused kernel list).
  *   X = [X_shard[0]; ...; X_shard[R-1]]   (each [M/R, K], X is [M, K])
  *   out[r] = X @ B[r]                      ([M, N] per rank, dtype `out_dtype`)
