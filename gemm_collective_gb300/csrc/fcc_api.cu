@@ -736,3 +736,26 @@ fcc_status light_check_gemm(int R, const void* const* A, const void* const* B, i
 void count_launch() { g_launches.fetch_add(1); }
 
 }  // namespace fcc
+
+// ------------------------------------------------------------------------
+// Host helpers shared with the other translation units (MoE entry point).
+namespace fcc {
+
+fcc_status internal_prepare(const fcc_opts* o, size_t ws_bytes, void** ws, int** status,
+                            int* sms, unsigned long long* timeout_ns) {
+  DeviceState* d = nullptr;
+  fcc_status s = device_state(&d);
+  if (s != FCC_OK) return s;
+  if ((s = get_workspace(d, o, ws_bytes, ws)) != FCC_OK) return s;
+  *status = d->status;
+  *sms = (o != nullptr && o->max_ctas > 0) ? std::min(d->sms, o->max_ctas) : d->sms;
+  *timeout_ns = timeout_of(o);
+  return FCC_OK;
+}
+
+fcc_status internal_make_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols,
+                             uint32_t box_rows) {
+  return make_map(m, ptr, rows, cols, box_rows);
+}
+
+}  // namespace fcc

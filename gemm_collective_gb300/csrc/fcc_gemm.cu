@@ -47,8 +47,11 @@ constexpr int kSmemBytes = 1024 /*alignment slack*/ + kStages * kStageBytes +
 
 struct Tile {
   int rank;    // rank whose A/B feed the tile (PARTIAL/PUSH/AG-B), -1 = all ranks
-  int shard;   // AG: shard that owns the A rows
-  int mt, nt;  // tile indices within one rank's output
+  int shard;   // AG: shard that owns the A rows; GROUPED: receiving rank
+  int mt, nt;  // tile indices within one rank's output (GROUPED: within the expert)
+  int expert;  // GROUPED: expert of the tile
+  int row0;    // GROUPED: first receive-buffer row of the tile
+  int rows;    // GROUPED: valid rows of the tile
 };
 
 __device__ __forceinline__ void raster(int t, int tiles_m, int tiles_n, int group, int& mt,
@@ -62,12 +65,54 @@ __device__ __forceinline__ void raster(int t, int tiles_m, int tiles_n, int grou
   nt = local / gm;
 }
 
-template <int MODE>
-__device__ __forceinline__ Tile tile_of(const GemmParams& p, int t) {
+template <int MODE, class P>
+__device__ __forceinline__ int num_tiles_of(const P& p) {
+  if constexpr (MODE == MODE_GROUPED) {
+    return __ldcg(p.tile_start + p.E);  // written on the device by the dispatch kernels
+  } else {
+    return p.num_tiles;
+  }
+}
+
+template <int MODE, class P>
+__device__ __forceinline__ int k_iters_of(const P& p) {
+  if constexpr (MODE == MODE_GROUPED) {
+    return p.kb_per_rank;
+  } else {
+    return p.k_iters;
+  }
+}
+
+template <int MODE, class P>
+__device__ __forceinline__ Tile tile_of(const P& p, int t) {
   Tile tl;
   tl.rank = -1;
   tl.shard = 0;
-  if constexpr (MODE == MODE_RS || MODE == MODE_AR) {
+  tl.expert = 0;
+  tl.row0 = 0;
+  tl.rows = 0;
+  if constexpr (MODE == MODE_GROUPED) {
+    // Expert of tile t: the last e with tile_start[e] <= t (binary search).
+    int lo = 0, hi = p.E - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (__ldcg(p.tile_start + mid) <= t)
+        lo = mid;
+      else
+        hi = mid - 1;
+    }
+    const int e = lo;
+    const int rows_e = __ldcg(p.expert_rows + e);
+    const int tm = (rows_e + kBM - 1) / kBM;
+    const int lt = t - __ldcg(p.tile_start + e);
+    // m fastest: CTAs running at the same time share the expert's weight slab.
+    tl.mt = lt % tm;
+    tl.nt = lt / tm;
+    tl.expert = e;
+    tl.shard = e / p.Eloc;
+    tl.row0 = __ldcg(p.expert_base + e) + tl.mt * kBM;
+    tl.rows = min(kBM, rows_e - tl.mt * kBM);
+  } else if constexpr (MODE == MODE_RS || MODE == MODE_AR) {
     raster(t, p.tiles_m, p.tiles_n, p.group_m, tl.mt, tl.nt);
   } else if constexpr (MODE == MODE_AG) {
     // tiles_m = R * (tiles per shard), tiles_n = R * (tiles per rank)
@@ -125,8 +170,8 @@ __device__ __forceinline__ void red_row_chunk(float* row_ptr, int col, int N,
   }
 }
 
-template <int MODE>
-__global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_constant__ GemmParams p) {
+template <int MODE, class P>
+__global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_constant__ P p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -161,9 +206,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
   if (warp == 0 && lane == 0) {
     for (int r = 0; r < p.R; ++r) {
       ptx::tma_prefetch_desc(&p.mapA[r]);
-      ptx::tma_prefetch_desc(&p.mapB[r]);
+      if constexpr (MODE != MODE_GROUPED) ptx::tma_prefetch_desc(&p.mapB[r]);
     }
   }
+  const int num_tiles = num_tiles_of<MODE>(p);
+  const int k_iters = k_iters_of<MODE>(p);
   if (warp == 1) {
     ptx::tmem_alloc(tmem_slot, kTmemCols);
     ptx::tmem_relinquish();
@@ -180,10 +227,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
       uint32_t stage = 0, phase = 0;
       uint32_t issued = 0, last_parity = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
         const Tile tl = tile_of<MODE>(p, t);
         int a_row;
-        if constexpr (MODE == MODE_AG) {
+        if constexpr (MODE == MODE_GROUPED) {
+          a_row = tl.row0;
+        } else if constexpr (MODE == MODE_AG) {
           a_row = tl.mt * kBM;
         } else if constexpr (MODE == MODE_PARTIAL) {
           a_row = p.m_begin + tl.mt * kBM;
@@ -193,14 +242,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         const int b_col = tl.nt * kBN;
         int r = (tl.rank >= 0) ? tl.rank : 0;
         int kb = 0;
-        for (int it = 0; it < p.k_iters; ++it) {
+        for (int it = 0; it < k_iters; ++it) {
           if (!W.wait(&empty[stage], phase ^ 1u)) {
             ok = false;
             break;
           }
           ptx::mbar_arrive_expect_tx(&full[stage], kStageBytes);
-          const CUtensorMap* ma = (MODE == MODE_AG) ? &p.mapA[tl.shard] : &p.mapA[r];
-          const CUtensorMap* mb = &p.mapB[r];
+          const CUtensorMap* ma =
+              (MODE == MODE_AG || MODE == MODE_GROUPED) ? &p.mapA[tl.shard] : &p.mapA[r];
+          const CUtensorMap* mb = (MODE == MODE_GROUPED) ? &p.mapB[tl.expert] : &p.mapB[r];
           uint8_t* a_dst = sA + stage * kABytes;
           uint8_t* b_dst = sB + stage * kBBytes;
           ptx::tma_load_2d(a_dst, ma, &full[stage], kb * kBK, a_row);
@@ -231,11 +281,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
       uint32_t stage = 0, phase = 0;
       uint32_t acc = 0, acc_phase = 0;
       bool any = false, ok = true;
-      for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
         if (!W.wait(&tempty[acc], acc_phase ^ 1u)) break;
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * kBN;
-        for (int it = 0; it < p.k_iters; ++it) {
+        for (int it = 0; it < k_iters; ++it) {
           if (!W.wait(&full[stage], phase)) {
             ok = false;
             break;
@@ -273,7 +323,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int row_in_tile = q * 32 + lane;
     uint32_t acc = 0, acc_phase = 0;
-    for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
+    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
       const Tile tl = tile_of<MODE>(p, t);
       const bool failed = !W.wait(&tfull[acc], acc_phase);
       if constexpr (MODE == MODE_RS_PUSH || MODE == MODE_AR_PUSH) {
@@ -304,6 +354,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         row_ok = local < p.Ms;
         grow = static_cast<int64_t>(tl.shard) * p.Ms + local;
         if (row_ok) rowp = static_cast<char*>(p.out[tl.rank]) + grow * p.N * esz;
+      } else if constexpr (MODE == MODE_GROUPED) {
+        row_ok = row_in_tile < tl.rows;
+        grow = static_cast<int64_t>(tl.row0) + row_in_tile;
+        if (row_ok) rowp = static_cast<char*>(p.out[tl.shard]) + grow * p.N * esz;
       } else {  // MODE_PARTIAL
         grow = static_cast<int64_t>(p.m_begin) + static_cast<int64_t>(tl.mt) * kBM + row_in_tile;
         row_ok = grow < p.m_end;
@@ -401,9 +455,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
   }
 }
 
-template <int MODE>
-cudaError_t launch_mode(const GemmParams& p, int grid, cudaStream_t st) {
-  auto kern = gemm_kernel<MODE>;
+template <int MODE, class P>
+cudaError_t launch_mode(const P& p, int grid, cudaStream_t st) {
+  auto kern = gemm_kernel<MODE, P>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        kSmemBytes);
   if (e != cudaSuccess) return e;
@@ -417,14 +471,18 @@ int gemm_smem_bytes() { return kSmemBytes; }
 
 cudaError_t launch_gemm(const GemmParams& p, int mode, int grid, cudaStream_t st) {
   switch (mode) {
-    case MODE_RS: return launch_mode<MODE_RS>(p, grid, st);
-    case MODE_AR: return launch_mode<MODE_AR>(p, grid, st);
-    case MODE_PARTIAL: return launch_mode<MODE_PARTIAL>(p, grid, st);
-    case MODE_AG: return launch_mode<MODE_AG>(p, grid, st);
-    case MODE_RS_PUSH: return launch_mode<MODE_RS_PUSH>(p, grid, st);
-    case MODE_AR_PUSH: return launch_mode<MODE_AR_PUSH>(p, grid, st);
+    case MODE_RS: return launch_mode<MODE_RS, GemmParams>(p, grid, st);
+    case MODE_AR: return launch_mode<MODE_AR, GemmParams>(p, grid, st);
+    case MODE_PARTIAL: return launch_mode<MODE_PARTIAL, GemmParams>(p, grid, st);
+    case MODE_AG: return launch_mode<MODE_AG, GemmParams>(p, grid, st);
+    case MODE_RS_PUSH: return launch_mode<MODE_RS_PUSH, GemmParams>(p, grid, st);
+    case MODE_AR_PUSH: return launch_mode<MODE_AR_PUSH, GemmParams>(p, grid, st);
     default: return cudaErrorInvalidValue;
   }
+}
+
+cudaError_t launch_grouped_gemm(const GroupedParams& p, int grid, cudaStream_t st) {
+  return launch_mode<MODE_GROUPED, GroupedParams>(p, grid, st);
 }
 
 }  // namespace fcc

@@ -22,6 +22,7 @@ enum GemmMode : int {
   MODE_AG = 3,         // all-gather + GEMM: A tile from the owning shard
   MODE_RS_PUSH = 4,    // reduce-scatter, push: red.add of each rank's tile into the owner
   MODE_AR_PUSH = 5,    // all-reduce, push
+  MODE_GROUPED = 6,    // MoE grouped expert GEMM over a device-built tile table
 };
 
 struct GemmParams {
@@ -60,7 +61,28 @@ struct GemvParams {
 };
 
 // Launchers (return cudaSuccess or the launch error).
+// Grouped expert GEMM (MoE): tile t belongs to expert e with
+// tile_start[e] <= t < tile_start[e+1]; the expert's rows are
+// [expert_base[e], expert_base[e] + expert_rows[e]) of rank e/Eloc's receive
+// buffers.  The tile table is written on the device by the dispatch kernels.
+struct GroupedParams {
+  CUtensorMap mapA[FCC_MAX_RANKS];     // recv_x[d]: [cap, H]
+  CUtensorMap mapB[FCC_MAX_EXPERTS];   // W_e: [H, F]
+  void* out[FCC_MAX_RANKS];            // recv_y[d]: [cap, F]
+  int R, E, Eloc;
+  int N, K;                            // F, H
+  int tiles_n;                         // ceil(F / 256)
+  int kb_per_rank;                     // ceil(H / 64)
+  int out_f32;
+  const int* tile_start;               // [E + 1]
+  const int* expert_base;              // [E]
+  const int* expert_rows;              // [E] (clamped to the receive capacity)
+  int* status;
+  unsigned long long timeout_ns;
+};
+
 cudaError_t launch_gemm(const GemmParams& p, int mode, int grid, cudaStream_t st);
+cudaError_t launch_grouped_gemm(const GroupedParams& p, int grid, cudaStream_t st);
 int gemm_smem_bytes();
 cudaError_t launch_gemv(const GemvParams& p, int grid, cudaStream_t st);
 int gemv_smem_bytes();
@@ -92,4 +114,14 @@ fcc_status light_status_word(int** out);
 fcc_status light_check_gemm(int R, const void* const* A, const void* const* B, int64_t M,
                             int64_t N, int64_t K, fcc_dtype in);
 void count_launch();
+}  // namespace fcc
+
+namespace fcc {
+// Device state, workspace (caller's or the pool), status word, usable SM count
+// and the wait limit for a call; the tensor-map encoder is ready afterwards.
+fcc_status internal_prepare(const fcc_opts* o, size_t ws_bytes, void** ws, int** status,
+                            int* sms, unsigned long long* timeout_ns);
+// 2-D bf16 tensor map, box [box_rows, 64], 128-byte swizzle (after internal_prepare).
+fcc_status internal_make_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols,
+                             uint32_t box_rows);
 }  // namespace fcc

@@ -1,21 +1,429 @@
-// fcc_moe.cu -- MoE route, dispatch (all-to-all) and grouped expert GEMM.
+// fcc_moe.cu -- MoE route, dispatch (all-to-all) and grouped expert GEMM (sm_103a).
+//
+// The MoE Dispatch + GEMM kernel of the mKernel article's fused-kernel list
+// (and the GEMM + All-to-All operator for MoE in the SC24 paper's abstract),
+// over R virtual ranks in one GPU:
+//   1. route_kernel   one warp per token: top-k experts by logit (ties to the
+//                     lower index, found with warp shuffles), softmax gates,
+//                     and a per-chunk expert histogram (chunk = 128 tokens of
+//                     one source rank).
+//   2. scan_kernel    one CTA: exclusive prefix of the histograms over chunks
+//                     (a fixed order), expert counts, send counts, each
+//                     expert's first row in its receiving rank's buffer, and
+//                     the grouped GEMM's tile table.
+//   3. rank_kernel    one CTA per chunk: the stable rank of every assignment
+//                     within its expert (warp match + popc, then a prefix over
+//                     the CTA's warps), i.e. its receive row; writes recv_src.
+//   4. copy_kernel    one warp per token: reads the token row once and writes
+//                     it to each of its receive rows (the all-to-all).
+//   5. the persistent tcgen05 GEMM in grouped mode: tiles over
+//                     (expert, m tile, n tile) from the device tile table.
+// No atomics decide any position, so every index output is bit-exact and
+// repeatable; the host never waits for the counts.
 #include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstring>
 
 #include "fcc.h"
 #include "fcc_internal.h"
+#include "fcc_ptx.cuh"
+
+namespace fcc {
+namespace {
+
+constexpr int kChunkTok = 128;   // tokens per chunk (one source rank per chunk)
+constexpr int kMoeBN = 256;      // grouped GEMM tile width (the GEMM's BN)
+
+struct MoeArgs {
+  const void* X[FCC_MAX_RANKS];       // [T, H] bf16 per source rank
+  const float* logits[FCC_MAX_RANKS]; // [T, E]
+  int32_t* idx[FCC_MAX_RANKS];        // [T, topk]
+  float* gate[FCC_MAX_RANKS];         // [T, topk]
+  void* recv_x[FCC_MAX_RANKS];        // [cap, H] per receiving rank
+  int32_t* recv_src[FCC_MAX_RANKS];   // [cap]
+  int R, E, Eloc, topk;
+  int T, H;
+  int cap;
+  int chunks_per_rank;
+  int tiles_n;
+  int32_t* chunk_counts;  // [nchunks][E]
+  int32_t* chunk_off;     // [nchunks][E]
+  int32_t* expert_counts; // [E] (caller's output)
+  int32_t* send_counts;   // [R][R] (caller's output)
+  int32_t* expert_base;   // [E]
+  int32_t* expert_rows;   // [E], clamped to cap
+  int32_t* tile_start;    // [E + 1]
+  int32_t* row_of;        // [R*T*topk]: receive row of each assignment, -1 if dropped
+  int* status;
+};
+
+struct Cand {
+  float v;
+  int i;
+};
+
+// a ranks before b: larger logit, or equal logit and lower expert index.
+__device__ __forceinline__ bool better(const Cand& a, const Cand& b) {
+  return a.v > b.v || (a.v == b.v && a.i < b.i);
+}
+
+__device__ __forceinline__ Cand warp_best(Cand c) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    Cand o;
+    o.v = __shfl_xor_sync(0xffffffffu, c.v, off);
+    o.i = __shfl_xor_sync(0xffffffffu, c.i, off);
+    if (better(o, c)) c = o;
+  }
+  return c;
+}
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+  return x;
+}
+
+// Grid: one CTA per chunk, 256 threads (8 warps, one token at a time each).
+__global__ void __launch_bounds__(256) route_kernel(const MoeArgs a) {
+  __shared__ int hist[FCC_MAX_EXPERTS];
+  const int chunk = blockIdx.x;
+  const int s = chunk / a.chunks_per_rank;
+  const int t0 = (chunk - s * a.chunks_per_rank) * kChunkTok;
+  const int t1 = min(a.T, t0 + kChunkTok);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x < FCC_MAX_EXPERTS) hist[threadIdx.x] = 0;
+  __syncthreads();
+  const float neg_inf = __int_as_float(0xff800000);
+  for (int t = t0 + warp; t < t1; t += 8) {
+    const float* lg = a.logits[s] + static_cast<long long>(t) * a.E;
+    const float l0 = lane < a.E ? lg[lane] : neg_inf;
+    const float l1 = lane + 32 < a.E ? lg[lane + 32] : neg_inf;
+    // candidates this lane holds; experts past E carry index E (never chosen)
+    Cand c0{l0, lane < a.E ? lane : a.E};
+    Cand c1{l1, lane + 32 < a.E ? lane + 32 : a.E};
+    Cand best = better(c1, c0) ? c1 : c0;
+    const Cand first = warp_best(best);
+    // softmax denominator over all E experts, relative to the largest logit
+    float ex = 0.f;
+    if (lane < a.E) ex += expf(l0 - first.v);
+    if (lane + 32 < a.E) ex += expf(l1 - first.v);
+    const float den = warp_sum(ex);
+    Cand picked[2] = {first, first};
+    if (a.topk > 1) {
+      if (c0.i == first.i) c0.v = neg_inf, c0.i = a.E;
+      if (c1.i == first.i) c1.v = neg_inf, c1.i = a.E;
+      best = better(c1, c0) ? c1 : c0;
+      picked[1] = warp_best(best);
+    }
+    if (lane < a.topk) {
+      const Cand c = picked[lane];
+      a.idx[s][static_cast<long long>(t) * a.topk + lane] = c.i;
+      a.gate[s][static_cast<long long>(t) * a.topk + lane] = expf(c.v - first.v) / den;
+      atomicAdd(&hist[c.i], 1);  // a count: order does not matter
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x < a.E)
+    a.chunk_counts[static_cast<long long>(chunk) * a.E + threadIdx.x] = hist[threadIdx.x];
+}
+
+// One CTA of 64 threads.  Thread e scans expert e's histogram over the chunks
+// in chunk order (source rank, then token), so chunk_off[c][e] is the number of
+// assignments to e that precede chunk c in (s, t, slot) order.
+__global__ void __launch_bounds__(64) scan_kernel(const MoeArgs a) {
+  __shared__ int counts[FCC_MAX_EXPERTS];
+  __shared__ int rows[FCC_MAX_EXPERTS];
+  const int e = threadIdx.x;
+  const int nchunks = a.R * a.chunks_per_rank;
+  if (e < a.E) {
+    int run = 0;
+    for (int c = 0; c < nchunks; ++c) {
+      a.chunk_off[static_cast<long long>(c) * a.E + e] = run;
+      run += a.chunk_counts[static_cast<long long>(c) * a.E + e];
+    }
+    counts[e] = run;
+    a.expert_counts[e] = run;
+  }
+  __syncthreads();
+  if (e < a.E) {
+    const int d = e / a.Eloc;
+    long long base = 0;
+    for (int f = d * a.Eloc; f < e; ++f) base += counts[f];
+    const long long room = static_cast<long long>(a.cap) - base;
+    const int kept = static_cast<int>(max(0ll, min(static_cast<long long>(counts[e]), room)));
+    a.expert_base[e] = static_cast<int>(min(base, static_cast<long long>(a.cap)));
+    a.expert_rows[e] = kept;
+    rows[e] = kept;
+    if (e == (d + 1) * a.Eloc - 1 && base + counts[e] > a.cap && a.status != nullptr)
+      atomicCAS(a.status, 0, FCC_ERR_CAPACITY);
+  }
+  // send_counts[s][d]: assignments from source rank s to the experts of rank d
+  if (e < a.R * a.R) {
+    const int s = e / a.R, d = e - (e / a.R) * a.R;
+    int sum = 0;
+    for (int c = s * a.chunks_per_rank; c < (s + 1) * a.chunks_per_rank; ++c)
+      for (int f = d * a.Eloc; f < (d + 1) * a.Eloc; ++f)
+        sum += a.chunk_counts[static_cast<long long>(c) * a.E + f];
+    a.send_counts[e] = sum;
+  }
+  __syncthreads();
+  if (e == 0) {
+    int acc = 0;
+    for (int f = 0; f < a.E; ++f) {
+      a.tile_start[f] = acc;
+      acc += ((rows[f] + kBM - 1) / kBM) * a.tiles_n;
+    }
+    a.tile_start[a.E] = acc;
+  }
+}
+
+// One CTA of 256 threads per chunk; thread i holds assignment i of the chunk
+// (token t0 + i/topk, slot i%topk), so the 8 warps hold consecutive runs of
+// assignments in (t, slot) order.
+__global__ void __launch_bounds__(256) rank_kernel(const MoeArgs a) {
+  __shared__ int cnt[8][FCC_MAX_EXPERTS];
+  const int chunk = blockIdx.x;
+  const int s = chunk / a.chunks_per_rank;
+  const int t0 = (chunk - s * a.chunks_per_rank) * kChunkTok;
+  const int t1 = min(a.T, t0 + kChunkTok);
+  const int n_assign = (t1 - t0) * a.topk;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = threadIdx.x; i < 8 * FCC_MAX_EXPERTS; i += blockDim.x) (&cnt[0][0])[i] = 0;
+  __syncthreads();
+  const int i = threadIdx.x;
+  const bool valid = i < n_assign;
+  const int t = t0 + i / a.topk;
+  const int e = valid ? a.idx[s][static_cast<long long>(t0) * a.topk + i] : -1;
+  const unsigned peers = __match_any_sync(0xffffffffu, e);
+  const unsigned lower = (1u << lane) - 1u;
+  const int rank_in_warp = __popc(peers & lower);
+  if (valid && rank_in_warp == 0) cnt[warp][e] = __popc(peers);
+  __syncthreads();
+  // exclusive prefix over the warps, per expert
+  if (threadIdx.x < a.E) {
+    int run = 0;
+    for (int w = 0; w < 8; ++w) {
+      const int c = cnt[w][threadIdx.x];
+      cnt[w][threadIdx.x] = run;
+      run += c;
+    }
+  }
+  __syncthreads();
+  if (valid) {
+    const int pos = a.chunk_off[static_cast<long long>(chunk) * a.E + e] + cnt[warp][e] +
+                    rank_in_warp;
+    const int d = e / a.Eloc;
+    const int row = a.expert_base[e] + pos;
+    const bool kept = pos < a.expert_rows[e];
+    const long long gidx = (static_cast<long long>(s) * a.T + t0) * a.topk + i;
+    a.row_of[gidx] = kept ? row : -1;
+    if (kept) a.recv_src[d][row] = s * a.T + t;
+  }
+}
+
+// One warp per token: read the token's row once (16-byte loads) and write it to
+// each of its receive rows.
+__global__ void __launch_bounds__(256) copy_kernel(const MoeArgs a) {
+  const int lane = threadIdx.x & 31;
+  const long long warps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
+  const long long ntok = static_cast<long long>(a.R) * a.T;
+  const int vec = a.H / 8;  // uint4 per row
+  for (long long g = blockIdx.x * static_cast<long long>(blockDim.x >> 5) + (threadIdx.x >> 5);
+       g < ntok; g += warps) {
+    const int s = static_cast<int>(g / a.T);
+    const int t = static_cast<int>(g - static_cast<long long>(s) * a.T);
+    int row = -1, d = 0;
+    if (lane < a.topk) {
+      row = a.row_of[g * a.topk + lane];
+      d = a.idx[s][static_cast<long long>(t) * a.topk + lane] / a.Eloc;
+    }
+    const int row0 = __shfl_sync(0xffffffffu, row, 0);
+    const int d0 = __shfl_sync(0xffffffffu, d, 0);
+    const int row1 = __shfl_sync(0xffffffffu, row, 1);
+    const int d1 = __shfl_sync(0xffffffffu, d, 1);
+    const uint4* src = reinterpret_cast<const uint4*>(a.X[s]) + static_cast<long long>(t) * vec;
+    uint4* dst0 = row0 >= 0 ? reinterpret_cast<uint4*>(a.recv_x[d0]) +
+                                  static_cast<long long>(row0) * vec
+                            : nullptr;
+    uint4* dst1 = (a.topk > 1 && row1 >= 0) ? reinterpret_cast<uint4*>(a.recv_x[d1]) +
+                                                  static_cast<long long>(row1) * vec
+                                            : nullptr;
+    for (int v = lane; v < vec; v += 32) {
+      const uint4 x = __ldcs(src + v);
+      if (dst0 != nullptr) dst0[v] = x;
+      if (dst1 != nullptr) dst1[v] = x;
+    }
+  }
+}
+
+struct MoePlan {
+  int chunks_per_rank = 0;
+  int nchunks = 0;
+  size_t off_chunk_counts = 0, off_chunk_off = 0, off_base = 0, off_rows = 0, off_tiles = 0,
+         off_row_of = 0, total = 0;
+};
+
+size_t up256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+MoePlan moe_plan(int R, int64_t T, int E, int topk) {
+  MoePlan p;
+  p.chunks_per_rank = static_cast<int>((T + kChunkTok - 1) / kChunkTok);
+  p.nchunks = R * p.chunks_per_rank;
+  size_t off = 0;
+  p.off_chunk_counts = off;
+  off += up256(static_cast<size_t>(p.nchunks) * E * 4);
+  p.off_chunk_off = off;
+  off += up256(static_cast<size_t>(p.nchunks) * E * 4);
+  p.off_base = off;
+  off += up256(static_cast<size_t>(E) * 4);
+  p.off_rows = off;
+  off += up256(static_cast<size_t>(E) * 4);
+  p.off_tiles = off;
+  off += up256(static_cast<size_t>(E + 1) * 4);
+  p.off_row_of = off;
+  off += up256(static_cast<size_t>(R) * T * topk * 4);
+  p.total = off;
+  return p;
+}
+
+bool al(const void* p, uintptr_t a) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+fcc_status check_moe(int R, const void* const* X, const float* const* logits,
+                     const void* const* W, int64_t T, int64_t H, int64_t F, int E, int topk,
+                     void* const* recv_x, void* const* recv_y, int64_t cap,
+                     int32_t* const* topk_idx, float* const* topk_gate, int32_t* expert_counts,
+                     int32_t* send_counts, int32_t* const* recv_src, fcc_dtype in,
+                     fcc_dtype out_dtype, const fcc_opts* opts) {
+  if (R < 1 || R > FCC_MAX_RANKS || E < R || E > FCC_MAX_EXPERTS || E % R != 0)
+    return FCC_ERR_INVALID;
+  if (topk < 1 || topk > 2 || topk > E) return FCC_ERR_INVALID;
+  if (T < 1 || H < 8 || F < 8 || H % 8 != 0 || F % 8 != 0 || cap < 1) return FCC_ERR_INVALID;
+  if (T > (1ll << 28) || H > (1ll << 30) || F > (1ll << 30) || cap > (1ll << 30) ||
+      static_cast<int64_t>(R) * T * topk > (1ll << 30))
+    return FCC_ERR_INVALID;
+  if (X == nullptr || logits == nullptr || W == nullptr || recv_y == nullptr ||
+      topk_idx == nullptr || topk_gate == nullptr || recv_src == nullptr ||
+      !al(expert_counts, 4) || !al(send_counts, 4))
+    return FCC_ERR_INVALID;
+  for (int r = 0; r < R; ++r) {
+    if (!al(X[r], 16) || !al(logits[r], 4) || !al(recv_y[r], 16) || !al(topk_idx[r], 4) ||
+        !al(topk_gate[r], 4) || !al(recv_src[r], 4))
+      return FCC_ERR_INVALID;
+    if (recv_x != nullptr && !al(recv_x[r], 16)) return FCC_ERR_INVALID;
+  }
+  for (int e = 0; e < E; ++e)
+    if (!al(W[e], 16)) return FCC_ERR_INVALID;
+  if (in != FCC_BF16 && in != FCC_F16 && in != FCC_F32) return FCC_ERR_INVALID;
+  if (in != FCC_BF16) return FCC_ERR_UNSUPPORTED;
+  if (out_dtype != FCC_BF16 && out_dtype != FCC_F32)
+    return out_dtype == FCC_F16 ? FCC_ERR_UNSUPPORTED : FCC_ERR_INVALID;
+  if (recv_x == nullptr) return FCC_ERR_UNSUPPORTED;  // the rows are staged in recv_x
+  if (opts != nullptr && opts->algo != FCC_ALGO_AUTO && opts->algo != FCC_ALGO_FUSED &&
+      opts->algo != FCC_ALGO_UNFUSED)
+    return FCC_ERR_UNSUPPORTED;
+  return FCC_OK;
+}
+
+}  // namespace
+}  // namespace fcc
+
+using namespace fcc;
 
 extern "C" {
 
-fcc_status fcc_moe_dispatch_gemm(int, const void* const*, const float* const*, const void* const*,
-                                 int64_t, int64_t, int64_t, int, int, void* const*, void* const*,
-                                 int64_t, int32_t* const*, float* const*, int32_t*, int32_t*,
-                                 int32_t* const*, fcc_dtype, fcc_dtype, const fcc_opts*,
-                                 fcc_stream_t) {
-  return FCC_ERR_UNSUPPORTED;
+size_t fcc_moe_workspace_size(int R, int64_t T, int64_t H, int64_t F, int E, int topk,
+                              int64_t cap, const fcc_opts* opts) {
+  (void)H;
+  (void)F;
+  (void)cap;
+  (void)opts;
+  if (R < 1 || R > FCC_MAX_RANKS || T < 1 || E < 1 || E > FCC_MAX_EXPERTS || topk < 1)
+    return 0;
+  return moe_plan(R, T, E, topk).total;
 }
 
-size_t fcc_moe_workspace_size(int, int64_t, int64_t, int64_t, int, int, int64_t, const fcc_opts*) {
-  return 0;
+fcc_status fcc_moe_dispatch_gemm(int R, const void* const* X, const float* const* logits,
+                                 const void* const* W, int64_t T, int64_t H, int64_t F, int E,
+                                 int topk, void* const* recv_x, void* const* recv_y,
+                                 int64_t cap, int32_t* const* topk_idx,
+                                 float* const* topk_gate, int32_t* expert_counts,
+                                 int32_t* send_counts, int32_t* const* recv_src, fcc_dtype in,
+                                 fcc_dtype out_dtype, const fcc_opts* opts,
+                                 fcc_stream_t stream) {
+  fcc_status s = check_moe(R, X, logits, W, T, H, F, E, topk, recv_x, recv_y, cap, topk_idx,
+                           topk_gate, expert_counts, send_counts, recv_src, in, out_dtype, opts);
+  if (s != FCC_OK) return s;
+  const MoePlan plan = moe_plan(R, T, E, topk);
+  void* ws = nullptr;
+  int* status = nullptr;
+  int sms = 0;
+  unsigned long long timeout_ns = 0;
+  if ((s = internal_prepare(opts, plan.total, &ws, &status, &sms, &timeout_ns)) != FCC_OK)
+    return s;
+  char* base = static_cast<char*>(ws);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+
+  MoeArgs a;
+  std::memset(&a, 0, sizeof(a));
+  for (int r = 0; r < R; ++r) {
+    a.X[r] = X[r];
+    a.logits[r] = logits[r];
+    a.idx[r] = topk_idx[r];
+    a.gate[r] = topk_gate[r];
+    a.recv_x[r] = recv_x[r];
+    a.recv_src[r] = recv_src[r];
+  }
+  a.R = R;
+  a.E = E;
+  a.Eloc = E / R;
+  a.topk = topk;
+  a.T = static_cast<int>(T);
+  a.H = static_cast<int>(H);
+  a.cap = static_cast<int>(cap);
+  a.chunks_per_rank = plan.chunks_per_rank;
+  a.tiles_n = static_cast<int>((F + kMoeBN - 1) / kMoeBN);
+  a.chunk_counts = reinterpret_cast<int32_t*>(base + plan.off_chunk_counts);
+  a.chunk_off = reinterpret_cast<int32_t*>(base + plan.off_chunk_off);
+  a.expert_counts = expert_counts;
+  a.send_counts = send_counts;
+  a.expert_base = reinterpret_cast<int32_t*>(base + plan.off_base);
+  a.expert_rows = reinterpret_cast<int32_t*>(base + plan.off_rows);
+  a.tile_start = reinterpret_cast<int32_t*>(base + plan.off_tiles);
+  a.row_of = reinterpret_cast<int32_t*>(base + plan.off_row_of);
+  a.status = status;
+
+  GroupedParams g;
+  std::memset(&g, 0, sizeof(g));
+  for (int d = 0; d < R; ++d) {
+    if ((s = internal_make_map(&g.mapA[d], recv_x[d], cap, H, kBM)) != FCC_OK) return s;
+    g.out[d] = recv_y[d];
+  }
+  for (int e = 0; e < E; ++e)
+    if ((s = internal_make_map(&g.mapB[e], W[e], H, F, kBK)) != FCC_OK) return s;
+  g.R = R;
+  g.E = E;
+  g.Eloc = E / R;
+  g.N = static_cast<int>(F);
+  g.K = static_cast<int>(H);
+  g.tiles_n = a.tiles_n;
+  g.kb_per_rank = static_cast<int>((H + kBK - 1) / kBK);
+  g.out_f32 = out_dtype == FCC_F32 ? 1 : 0;
+  g.tile_start = a.tile_start;
+  g.expert_base = a.expert_base;
+  g.expert_rows = a.expert_rows;
+  g.status = status;
+  g.timeout_ns = timeout_ns;
+
+  route_kernel<<<plan.nchunks, 256, 0, st>>>(a);
+  scan_kernel<<<1, 64, 0, st>>>(a);
+  rank_kernel<<<plan.nchunks, 256, 0, st>>>(a);
+  copy_kernel<<<std::max(1, sms) * 4, 256, 0, st>>>(a);
+  if (cudaGetLastError() != cudaSuccess) return FCC_ERR_CUDA;
+  if (launch_grouped_gemm(g, std::max(1, sms), st) != cudaSuccess) return FCC_ERR_CUDA;
+  bump_launch_count(5);
+  return FCC_OK;
 }
 
 }  // extern "C"

@@ -169,16 +169,20 @@ fcc_status fcc_ag_gemm(int R, const void *const *X_shard, const void *const *B,
  *             over all E experts (not renormalised, not applied below).
  *   dispatch: assignments (s, t, slot) sorted stably by expert; rank d
  *             receives its experts' rows in (expert, s, t, slot) order:
- *             recv_src[d][row] = s*T + t, recv_x[d][row] = X[s][t] (if
- *             recv_x is non-NULL), expert_counts[e], send_counts[s*R + d].
+ *             recv_src[d][row] = s*T + t, recv_x[d][row] = X[s][t],
+ *             expert_counts[e], send_counts[s*R + d].
  *   GEMM:     recv_y[d][row] = X[s][t] @ W[e]  ([F] per row, dtype out_dtype).
- * X[s]: [T,H] bf16; logits[s]: [T,E] f32; W[e]: [H,F] bf16 (E pointers);
- * recv_x[d]: [cap,H]; recv_y[d]: [cap,F]; recv_src[d]: [cap] int32;
- * topk_idx[s]: [T,topk] int32; topk_gate[s]: [T,topk] f32; expert_counts:
- * [E] int32 device; send_counts: [R*R] int32 device.  Rows of a receive
- * buffer past the received count are left untouched.  topk in {1, 2};
- * E <= 64; H % 64 == 0; F % 8 == 0.  A rank receiving more than cap rows sets
- * FCC_ERR_CAPACITY in the status word and its rows past cap are dropped.
+ * X[s]: [T,H] bf16; logits[s]: [T,E] f32, finite; W[e]: [H,F] bf16 (E
+ * pointers); recv_x[d]: [cap,H] bf16 (required: the dispatched rows are
+ * staged there; NULL returns FCC_ERR_UNSUPPORTED); recv_y[d]: [cap,F];
+ * recv_src[d]: [cap] int32; topk_idx[s]: [T,topk] int32; topk_gate[s]:
+ * [T,topk] f32; expert_counts: [E] int32 device; send_counts: [R*R] int32
+ * device.  Rows of a receive buffer past the received count are left
+ * untouched.  topk in {1, 2}; R <= E <= 64, E % R == 0; H % 8 == 0;
+ * F % 8 == 0.  A rank receiving more than cap rows sets FCC_ERR_CAPACITY in
+ * the status word; its rows past cap are dropped (not copied, not multiplied).
+ * Index outputs are bit-exact and repeatable (no atomics decide a position).
+ * Uses workspace (fcc_moe_workspace_size).
  */
 fcc_status fcc_moe_dispatch_gemm(int R, const void *const *X, const float *const *logits,
                                  const void *const *W, int64_t T, int64_t H, int64_t F, int E,

@@ -1,0 +1,148 @@
+"""GPU parity: MoE route + dispatch (all-to-all) + grouped expert GEMM.
+
+Indices, counts and receive positions must equal the oracle bit for bit; the
+staged rows must be the source rows bit for bit; gates match the fp64 softmax
+to f32 rounding; expert outputs match the oracle within the float tolerance.
+The full workload (8 ranks x 4096 tokens, hidden 4096, 64 experts, top-2,
+F = 1408) is checked on all index outputs and on sampled output rows.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from tests.gpu_util import assert_close, dev_bf16, dev_f32, empty, to_f64
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():  # pragma: no cover - CPU container
+    pytest.skip("needs a GPU", allow_module_level=True)
+
+import gemm_collective_gb300 as fcc  # noqa: E402
+
+# f32 softmax: E exp() values (a few ulp each) summed in f32 and one division;
+# |rel err| <= (E + 3) * 2^-24 ~ 4e-6 for E = 64.
+GATE_RTOL = 5e-6
+
+
+def _run(X, logits, W, R, T, H, F, E, topk, cap, out_dtype=fcc.FCC_BF16):
+    dX = [dev_bf16(x) for x in X]
+    dL = [dev_f32(l) for l in logits]
+    dW = [dev_bf16(w) for w in W]
+    tdt = torch.float32 if out_dtype == fcc.FCC_F32 else torch.bfloat16
+    recv_x = [empty((cap, H), torch.bfloat16, fill=0.0) for _ in range(R)]
+    recv_y = [empty((cap, F), tdt, fill=float("nan")) for _ in range(R)]
+    idx = [torch.full((T, topk), -7, dtype=torch.int32, device="cuda") for _ in range(R)]
+    gate = [empty((T, topk), torch.float32) for _ in range(R)]
+    counts = torch.full((E,), -7, dtype=torch.int32, device="cuda")
+    send = torch.full((R * R,), -7, dtype=torch.int32, device="cuda")
+    src = [torch.full((cap,), -1, dtype=torch.int32, device="cuda") for _ in range(R)]
+    fcc.fcc_moe_dispatch_gemm(R, dX, dL, dW, T, H, F, E, topk, recv_x, recv_y, cap, idx, gate,
+                              counts, send, src, fcc.FCC_BF16, out_dtype)
+    st = fcc.fcc_stream_status()
+    return dict(recv_x=recv_x, recv_y=recv_y, idx=idx, gate=gate, counts=counts, send=send,
+                src=src, status=st)
+
+
+def _check(X, logits, W, R, T, H, F, E, topk, cap, out, sample=None, seed=0):
+    assert out["status"] == fcc.FCC_OK
+    lg = np.stack(logits)
+    ref_idx, ref_gate = oracle.moe_route(lg, topk)
+    got_idx = np.stack([i.cpu().numpy() for i in out["idx"]])
+    assert np.array_equal(got_idx, ref_idx), "top-k indices differ"
+    got_gate = np.stack([g.cpu().numpy() for g in out["gate"]]).astype(np.float64)
+    assert np.allclose(got_gate, ref_gate, rtol=GATE_RTOL, atol=0), \
+        f"gates: max rel {np.max(np.abs(got_gate / ref_gate - 1)):.2e}"
+    d = oracle.moe_dispatch(ref_idx, R, E, cap)
+    assert np.array_equal(out["counts"].cpu().numpy(), d.counts)
+    assert np.array_equal(out["send"].cpu().numpy().reshape(R, R), d.send_counts)
+    rng = np.random.Generator(np.random.PCG64(seed))
+    for dst in range(R):
+        n = int(d.recv_counts[dst])
+        src = out["src"][dst].cpu().numpy()
+        assert np.array_equal(src[:n], d.recv_src[dst, :n]), f"recv_src of rank {dst}"
+        assert np.all(src[n:] == -1), "rows past the count were written"
+        rows = np.arange(n) if sample is None else np.sort(
+            rng.choice(n, size=min(n, sample), replace=False))
+        s_rank = d.recv_src[dst, rows] // T
+        s_tok = d.recv_src[dst, rows] % T
+        # staged rows are the source rows, bit for bit
+        rx = out["recv_x"][dst][torch.from_numpy(rows).cuda()].view(torch.int16).cpu().numpy()
+        want = np.stack([X[s][t] for s, t in zip(s_rank, s_tok)]).view(np.int16)
+        assert np.array_equal(rx, want), f"recv_x of rank {dst}"
+        ref = oracle.moe_expert_rows(X, W, s_rank, s_tok, d.recv_expert[dst, rows])
+        got = to_f64(out["recv_y"][dst][torch.from_numpy(rows).cuda()])
+        assert_close(got, ref, f"recv_y of rank {dst}")
+
+
+@pytest.mark.parametrize("R,T,H,F,E,topk", [
+    (2, 300, 128, 136, 8, 2),     # ragged chunk, ragged F tile
+    (4, 257, 256, 264, 16, 2),
+    (8, 64, 64, 64, 64, 2),       # more experts than tokens per expert
+    (2, 200, 192, 128, 4, 1),     # top-1
+    (4, 130, 128, 72, 4, 2),      # one expert per rank: plain all-to-all
+    (1, 500, 128, 256, 8, 2),     # one rank
+])
+def test_moe_small(R, T, H, F, E, topk):
+    X, logits, W = synth.moe_inputs(R, T, H, E, F, seed=R * 100 + T)
+    cap = R * T * topk
+    out = _run(X, logits, W, R, T, H, F, E, topk, cap)
+    _check(X, logits, W, R, T, H, F, E, topk, cap, out)
+
+
+def test_moe_ties_and_f32_output():
+    R, T, H, F, E, topk = 2, 128, 64, 64, 8, 2
+    X, logits, W = synth.moe_inputs(R, T, H, E, F, seed=5)
+    logits[0][0, :] = 1.0                  # all tied: experts 0, 1
+    logits[0][1, [2, 6]] = 9.0             # tie for first: 2 then 6
+    logits[1][5, [7, 3, 5]] = [4.0, 4.0, 4.0]
+    cap = R * T * topk
+    out = _run(X, logits, W, R, T, H, F, E, topk, cap, fcc.FCC_F32)
+    _check(X, logits, W, R, T, H, F, E, topk, cap, out)
+    idx0 = out["idx"][0].cpu().numpy()
+    assert list(idx0[0]) == [0, 1] and list(idx0[1]) == [2, 6]
+
+
+def test_moe_repeatable():
+    R, T, H, F, E, topk = 4, 256, 128, 128, 16, 2
+    X, logits, W = synth.moe_inputs(R, T, H, E, F, seed=6)
+    cap = R * T * topk
+    a = _run(X, logits, W, R, T, H, F, E, topk, cap)
+    b = _run(X, logits, W, R, T, H, F, E, topk, cap)
+    for d in range(R):
+        assert torch.equal(a["src"][d], b["src"][d])
+        assert torch.equal(a["recv_y"][d].view(torch.int16), b["recv_y"][d].view(torch.int16))
+
+
+def test_moe_capacity_overflow_reported():
+    R, T, H, F, E, topk = 2, 256, 64, 64, 4, 2
+    X, logits, W = synth.moe_inputs(R, T, H, E, F, seed=7)
+    out = _run(X, logits, W, R, T, H, F, E, topk, cap=100)
+    assert out["status"] == fcc.FCC_ERR_CAPACITY
+    assert fcc.fcc_stream_status() == fcc.FCC_OK
+    # the kept rows are the first cap rows of the full dispatch
+    d = oracle.moe_dispatch(oracle.moe_route(np.stack(logits), topk)[0], R, E, R * T * topk)
+    for dst in range(R):
+        n = min(100, int(d.recv_counts[dst]))
+        assert np.array_equal(out["src"][dst].cpu().numpy()[:n], d.recv_src[dst, :n])
+
+
+def test_moe_invalid_arguments():
+    R, T, H, F, E, topk = 2, 16, 64, 64, 4, 2
+    X, logits, W = synth.moe_inputs(R, T, H, E, F, seed=8)
+    with pytest.raises(fcc.FccError) as e:
+        _run(X, logits, W, R, T, H, F, 3, topk, 64)        # E % R != 0
+    assert e.value.status == fcc.FCC_ERR_INVALID
+    with pytest.raises(fcc.FccError) as e:
+        _run(X, logits, W, R, T, H, F, E, 3, 64)           # topk = 3
+    assert e.value.status == fcc.FCC_ERR_INVALID
+
+
+def test_moe_full_workload_sampled():
+    w = synth.WORKLOADS["moe_r8_t4096_h4096_e64_f1408"]
+    X, logits, W = synth.moe_inputs(w.R, w.T, w.H, w.E, w.F, std_x=w.std_a, std_w=w.std_b,
+                                    seed=0)
+    cap = 2 * w.T * w.topk  # twice the mean load per rank
+    out = _run(X, logits, W, w.R, w.T, w.H, w.F, w.E, w.topk, cap)
+    _check(X, logits, W, w.R, w.T, w.H, w.F, w.E, w.topk, cap, out, sample=48)
