@@ -47,13 +47,15 @@ class fcc_opts(ctypes.Structure):
         ("timeout_ns", ctypes.c_int64),
         ("workspace", ctypes.c_void_p),
         ("workspace_bytes", ctypes.c_size_t),
+        ("cta_pair", ctypes.c_int),
     ]
 
 
 def make_opts(algo=FCC_ALGO_AUTO, deterministic=1, chunks=0, max_ctas=0, timeout_ns=0,
-              workspace=None, workspace_bytes=0) -> fcc_opts:
+              workspace=None, workspace_bytes=0, cta_pair=0) -> fcc_opts:
     ws = workspace.data_ptr() if hasattr(workspace, "data_ptr") else workspace
-    return fcc_opts(algo, deterministic, chunks, max_ctas, timeout_ns, ws, workspace_bytes)
+    return fcc_opts(algo, deterministic, chunks, max_ctas, timeout_ns, ws, workspace_bytes,
+                    cta_pair)
 
 
 class FccError(RuntimeError):

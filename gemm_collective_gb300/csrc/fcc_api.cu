@@ -115,6 +115,13 @@ fcc_algo algo_of(const fcc_opts* o) {
 
 bool deterministic_of(const fcc_opts* o) { return o == nullptr || o->deterministic != 0; }
 
+// Tensor-core tile shape: a CTA pair per 256-row tile unless the rows are few
+// (or the caller forces a shape).
+int choose_cg(const fcc_opts* o, int64_t rows) {
+  if (o != nullptr && (o->cta_pair == 1 || o->cta_pair == 2)) return o->cta_pair;
+  return rows > kBM ? 2 : 1;
+}
+
 int grid_for(const DeviceState* d, const fcc_opts* o, int64_t units) {
   int g = d->sms;
   if (o != nullptr && o->max_ctas > 0) g = std::min(g, o->max_ctas);
@@ -195,29 +202,32 @@ fcc_status gemm_params(GemmParams& p, DeviceState* d, int mode, int R, const voi
   p.status = d->status;
   p.timeout_ns = timeout_of(o);
   const int tn = static_cast<int>(cdiv(N, kGemmBN));
+  const int64_t rows = (mode == MODE_AG) ? Ms : (mode == MODE_PARTIAL ? m_end - m_begin : M);
+  p.cg = choose_cg(o, rows);
+  const int64_t tm = static_cast<int64_t>(kBM) * p.cg;
   switch (mode) {
     case MODE_RS:
     case MODE_AR:
-      p.tiles_m = static_cast<int>(cdiv(M, kBM));
+      p.tiles_m = static_cast<int>(cdiv(M, tm));
       p.tiles_n = tn;
       p.num_tiles = p.tiles_m * p.tiles_n;
       p.k_iters = R * p.kb_per_rank;
       break;
     case MODE_RS_PUSH:
     case MODE_AR_PUSH:
-      p.tiles_m = static_cast<int>(cdiv(M, kBM));
+      p.tiles_m = static_cast<int>(cdiv(M, tm));
       p.tiles_n = tn;
       p.num_tiles = R * p.tiles_m * p.tiles_n;
       p.k_iters = p.kb_per_rank;
       break;
     case MODE_PARTIAL:
-      p.tiles_m = static_cast<int>(cdiv(m_end - m_begin, kBM));
+      p.tiles_m = static_cast<int>(cdiv(m_end - m_begin, tm));
       p.tiles_n = tn;
       p.num_tiles = R * p.tiles_m * p.tiles_n;
       p.k_iters = p.kb_per_rank;
       break;
     case MODE_AG:
-      p.tiles_m = R * static_cast<int>(cdiv(Ms, kBM));
+      p.tiles_m = R * static_cast<int>(cdiv(Ms, tm));
       p.tiles_n = R * tn;
       p.num_tiles = p.tiles_m * p.tiles_n;
       p.k_iters = p.kb_per_rank;
@@ -232,8 +242,10 @@ fcc_status gemm_params(GemmParams& p, DeviceState* d, int mode, int R, const voi
 fcc_status run_gemm(const GemmParams& p, int mode, DeviceState* d, const fcc_opts* o,
                     cudaStream_t st) {
   if (p.num_tiles <= 0) return FCC_OK;
-  const int grid = grid_for(d, o, p.num_tiles);
-  cudaError_t e = launch_gemm(p, mode, grid, st);
+  // Grid in CTAs: one CTA (or CTA pair) per SM (pair of SMs), at most one per tile.
+  int grid = grid_for(d, o, static_cast<int64_t>(p.num_tiles) * p.cg);
+  grid = std::max(p.cg, (grid / p.cg) * p.cg);
+  cudaError_t e = launch_gemm(p, mode, p.cg, grid, st);
   if (e != cudaSuccess) return FCC_ERR_CUDA;
   g_launches.fetch_add(1);
   return FCC_OK;
@@ -258,7 +270,8 @@ RankSumPlan rank_sum_plan(int R, int64_t M, int64_t N, bool out_f32, const fcc_o
   if (a == FCC_ALGO_FUSED) {
     if (!deterministic_of(o) && !out_f32) {
       pl.acc_bytes = mn * 4;
-      pl.ticket_bytes = static_cast<size_t>(cdiv(M, kBM) * cdiv(N, kGemmBN)) * 4;
+      // one counter per (tile, CTA): enough for either tile shape
+      pl.ticket_bytes = static_cast<size_t>((cdiv(M, kBM) + 1) * cdiv(N, kGemmBN)) * 4;
     }
   } else {
     pl.partial_bytes = static_cast<size_t>(R) * mn * 4;

@@ -1,10 +1,20 @@
 // fcc_gemm.cu -- persistent tcgen05 GEMM with collective epilogues (sm_103a).
 //
-// One CTA per SM loops over output tiles (128 x 256).  Warp 0 streams A and B
-// tiles with TMA into a 4-stage shared-memory ring; warp 1 issues
-// tcgen05.mma (bf16 x bf16 -> f32) into one of two TMEM accumulators; warps
-// 2-5 drain the other accumulator with tcgen05.ld and perform the collective
-// step in the epilogue, so the stores of tile i overlap the MMAs of tile i+1.
+// Persistent kernel: every SM runs one CTA that loops over output tiles.
+// Warp 0 streams A and B tiles with TMA into a shared-memory ring; warp 1
+// issues tcgen05.mma (bf16 x bf16 -> f32) into one of two TMEM accumulators;
+// warps 2-5 drain the other accumulator with tcgen05.ld and perform the
+// collective step in the epilogue, so the stores of tile i overlap the MMAs of
+// tile i+1.
+//
+// Two shapes (template parameter CG):
+//   CG = 1  one CTA per 128 x 256 tile, tcgen05.mma.cta_group::1 (M = 128),
+//           4-stage ring of 48 KiB (A 128x64 + B 64x256).
+//   CG = 2  a CTA pair (cluster of 2 on neighbouring SMs) per 256 x 256 tile,
+//           tcgen05.mma.cta_group::2 (M = 256) issued by the pair's leader;
+//           each CTA loads its 128 rows of A and its 128 columns of B (no
+//           multicast), so each SM keeps a 6-stage ring of 32 KiB and reads
+//           half the B bytes per MMA.  Each CTA's TMEM holds its 128 rows.
 //
 // The collective step per mode (the fused operators of the mKernel article's
 // kernel list and of the SC24 paper's abstract, where each workgroup ships
@@ -19,10 +29,11 @@
 //   MODE_AG       the A tile is read straight from the shard that owns its rows
 //                 (the gather), the B tile and output from the column's rank.
 //   MODE_PARTIAL  plain per-rank GEMM over a row window (unfused baselines).
+//   MODE_GROUPED  MoE expert GEMM over a tile table built on the device.
 //
 // Shared memory operand layouts (128-byte swizzle, as written by TMA):
 //   A stage  [128 rows][64 k]   K-major: row m at m*128 B, 8-row groups 1 KiB apart
-//   B stage  4 boxes of [64 k][64 n] MN-major: box i at i*8 KiB, k-row at k*128 B
+//   B stage  boxes of [64 k][64 n] MN-major: box i at i*8 KiB, k-row at k*128 B
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -32,18 +43,23 @@
 namespace fcc {
 namespace {
 
-constexpr int kBN = 256;
-constexpr int kStages = 4;
-constexpr uint32_t kABytes = kBM * kBK * 2;         // 16 KiB
+constexpr int kBN = 256;                            // tile columns
+constexpr uint32_t kABytes = kBM * kBK * 2;         // 16 KiB per CTA and stage
 constexpr uint32_t kBBoxBytes = kBK * 64 * 2;       // 8 KiB: [64 k][64 n]
-constexpr uint32_t kBBytes = kBK * kBN * 2;         // 32 KiB
-constexpr uint32_t kStageBytes = kABytes + kBBytes;
 constexpr uint32_t kTmemCols = 2 * kBN;             // double-buffered accumulator
-constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(kBM, kBN, /*a_mn=*/false, /*b_mn=*/true);
 constexpr uint64_t kDrainNs = 50ull * 1000 * 1000;  // unwinding limit after an abort
 
-constexpr int kSmemBytes = 1024 /*alignment slack*/ + kStages * kStageBytes +
-                           (2 * kStages + 5) * 8 + 16;
+template <int CG>
+struct Cfg {
+  static constexpr int kTileM = kBM * CG;                   // rows of one (pair) tile
+  static constexpr int kBNcta = kBN / CG;                   // B columns this CTA loads
+  static constexpr int kStages = CG == 2 ? 6 : 4;
+  static constexpr uint32_t kBBytes = kBK * kBNcta * 2;     // 32 or 16 KiB
+  static constexpr uint32_t kStageBytes = kABytes + kBBytes;
+  static constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(kTileM, kBN, false, true);
+  static constexpr int kSmem = 1024 + kStages * static_cast<int>(kStageBytes) +
+                               (2 * kStages + 5) * 8 + 16;
+};
 
 struct Tile {
   int rank;    // rank whose A/B feed the tile (PARTIAL/PUSH/AG-B), -1 = all ranks
@@ -83,7 +99,7 @@ __device__ __forceinline__ int k_iters_of(const P& p) {
   }
 }
 
-template <int MODE, class P>
+template <int MODE, int TM, class P>
 __device__ __forceinline__ Tile tile_of(const P& p, int t) {
   Tile tl;
   tl.rank = -1;
@@ -103,15 +119,15 @@ __device__ __forceinline__ Tile tile_of(const P& p, int t) {
     }
     const int e = lo;
     const int rows_e = __ldcg(p.expert_rows + e);
-    const int tm = (rows_e + kBM - 1) / kBM;
+    const int tm = (rows_e + TM - 1) / TM;
     const int lt = t - __ldcg(p.tile_start + e);
     // m fastest: CTAs running at the same time share the expert's weight slab.
     tl.mt = lt % tm;
     tl.nt = lt / tm;
     tl.expert = e;
     tl.shard = e / p.Eloc;
-    tl.row0 = __ldcg(p.expert_base + e) + tl.mt * kBM;
-    tl.rows = min(kBM, rows_e - tl.mt * kBM);
+    tl.row0 = __ldcg(p.expert_base + e) + tl.mt * TM;
+    tl.rows = min(TM, rows_e - tl.mt * TM);
   } else if constexpr (MODE == MODE_RS || MODE == MODE_AR) {
     raster(t, p.tiles_m, p.tiles_n, p.group_m, tl.mt, tl.nt);
   } else if constexpr (MODE == MODE_AG) {
@@ -170,14 +186,17 @@ __device__ __forceinline__ void red_row_chunk(float* row_ptr, int col, int N,
   }
 }
 
-template <int MODE, class P>
+template <int MODE, int CG, class P>
 __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_constant__ P p) {
+  using C = Cfg<CG>;
+  constexpr int kStages = C::kStages;
+  constexpr int TM = C::kTileM;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + kStages * kABytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + kStages * kBBytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + kStages * C::kBBytes);
   uint64_t* full = bars;
   uint64_t* empty = bars + kStages;
   uint64_t* tfull = bars + 2 * kStages;
@@ -189,6 +208,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // Rank of this CTA in its pair (0 = leader, which issues the MMAs).
+  const uint32_t cta = (CG == 2) ? ptx::cluster_ctarank() : 0u;
+  const int pair = blockIdx.x / CG;
+  const int npairs = gridDim.x / CG;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -197,7 +220,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(&tfull[b], 1);
-      ptx::mbar_init(&tempty[b], 4);
+      ptx::mbar_init(&tempty[b], 4 * CG);  // every epilogue warp of the pair
     }
     ptx::mbar_init(mma_done, 1);
     *abort_flag = 0;
@@ -212,11 +235,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
   const int num_tiles = num_tiles_of<MODE>(p);
   const int k_iters = k_iters_of<MODE>(p);
   if (warp == 1) {
-    ptx::tmem_alloc(tmem_slot, kTmemCols);
-    ptx::tmem_relinquish();
+    if constexpr (CG == 2) {
+      ptx::tmem_alloc_pair(tmem_slot, kTmemCols);
+      ptx::tmem_relinquish_pair();
+    } else {
+      ptx::tmem_alloc(tmem_slot, kTmemCols);
+      ptx::tmem_relinquish();
+    }
   }
   ptx::tc_fence_before();
-  __syncthreads();
+  if constexpr (CG == 2) {
+    ptx::cluster_sync_all();  // the peer's barriers exist before anyone signals them
+  } else {
+    __syncthreads();
+  }
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const ptx::Waiter W{abort_flag, p.status, p.timeout_ns};
@@ -227,19 +259,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
       uint32_t stage = 0, phase = 0;
       uint32_t issued = 0, last_parity = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-        const Tile tl = tile_of<MODE>(p, t);
+      for (int t = pair; t < num_tiles && ok; t += npairs) {
+        const Tile tl = tile_of<MODE, TM>(p, t);
         int a_row;
         if constexpr (MODE == MODE_GROUPED) {
           a_row = tl.row0;
-        } else if constexpr (MODE == MODE_AG) {
-          a_row = tl.mt * kBM;
         } else if constexpr (MODE == MODE_PARTIAL) {
-          a_row = p.m_begin + tl.mt * kBM;
+          a_row = p.m_begin + tl.mt * TM;
         } else {
-          a_row = tl.mt * kBM;
+          a_row = tl.mt * TM;
         }
-        const int b_col = tl.nt * kBN;
+        a_row += static_cast<int>(cta) * kBM;                 // this CTA's half of the rows
+        const int b_col = tl.nt * kBN + static_cast<int>(cta) * C::kBNcta;
         int r = (tl.rank >= 0) ? tl.rank : 0;
         int kb = 0;
         for (int it = 0; it < k_iters; ++it) {
@@ -247,16 +278,27 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
             ok = false;
             break;
           }
-          ptx::mbar_arrive_expect_tx(&full[stage], kStageBytes);
           const CUtensorMap* ma =
               (MODE == MODE_AG || MODE == MODE_GROUPED) ? &p.mapA[tl.shard] : &p.mapA[r];
           const CUtensorMap* mb = (MODE == MODE_GROUPED) ? &p.mapB[tl.expert] : &p.mapB[r];
           uint8_t* a_dst = sA + stage * kABytes;
-          uint8_t* b_dst = sB + stage * kBBytes;
-          ptx::tma_load_2d(a_dst, ma, &full[stage], kb * kBK, a_row);
+          uint8_t* b_dst = sB + stage * C::kBBytes;
+          if constexpr (CG == 2) {
+            // Both CTAs' bytes are counted on the leader's full barrier.
+            const uint32_t bar = ptx::mapa(ptx::smem_addr(&full[stage]), 0);
+            if (cta == 0) ptx::mbar_arrive_expect_tx(&full[stage], 2 * C::kStageBytes);
+            ptx::tma_load_2d_pair(a_dst, ma, bar, kb * kBK, a_row);
 #pragma unroll
-          for (int i = 0; i < kBN / 64; ++i)
-            ptx::tma_load_2d(b_dst + i * kBBoxBytes, mb, &full[stage], b_col + 64 * i, kb * kBK);
+            for (int i = 0; i < C::kBNcta / 64; ++i)
+              ptx::tma_load_2d_pair(b_dst + i * kBBoxBytes, mb, bar, b_col + 64 * i, kb * kBK);
+          } else {
+            ptx::mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
+            ptx::tma_load_2d(a_dst, ma, &full[stage], kb * kBK, a_row);
+#pragma unroll
+            for (int i = 0; i < C::kBNcta / 64; ++i)
+              ptx::tma_load_2d(b_dst + i * kBBoxBytes, mb, &full[stage], b_col + 64 * i,
+                               kb * kBK);
+          }
           issued |= 1u << stage;
           last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
           if (++stage == kStages) {
@@ -269,19 +311,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
           }
         }
       }
-      if (*abort_flag) {
-        // Loads still in flight write into this CTA's shared memory: let them land.
+      if (*abort_flag && cta == 0) {
+        // Loads still in flight write into shared memory: let them land.  (In a
+        // pair every load is counted on the leader's barriers, so the leader
+        // drains them before the final pair barrier releases its peer.)
         for (int s = 0; s < kStages; ++s)
           if (issued & (1u << s)) W.drain(&full[s], (last_parity >> s) & 1u, kDrainNs);
       }
     }
   } else if (warp == 1) {
     // ----------------------------------------------------------- MMA issue
-    if (lane == 0) {
+    if (lane == 0 && cta == 0) {
       uint32_t stage = 0, phase = 0;
       uint32_t acc = 0, acc_phase = 0;
       bool any = false, ok = true;
-      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+      for (int t = pair; t < num_tiles && ok; t += npairs) {
         if (!W.wait(&tempty[acc], acc_phase ^ 1u)) break;
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * kBN;
@@ -292,16 +336,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
           }
           ptx::tc_fence_after();
           const uint32_t a_addr = ptx::smem_addr(sA + stage * kABytes);
-          const uint32_t b_addr = ptx::smem_addr(sB + stage * kBBytes);
+          const uint32_t b_addr = ptx::smem_addr(sB + stage * C::kBBytes);
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk) {
             // A: K-major, advance 16 elements (32 B) inside the swizzled row.
             const uint64_t ad = ptx::smem_desc_sw128(a_addr + kk * 32, 16, 1024);
             // B: MN-major, advance 16 k-rows (2 KiB); 64-wide n atoms 8 KiB apart.
             const uint64_t bd = ptx::smem_desc_sw128(b_addr + kk * 2048, kBBoxBytes, 1024);
-            ptx::mma_f16(d_tmem, ad, bd, kIdesc, (it > 0 || kk > 0) ? 1u : 0u);
+            if constexpr (CG == 2)
+              ptx::mma_f16_pair(d_tmem, ad, bd, C::kIdesc, (it > 0 || kk > 0) ? 1u : 0u);
+            else
+              ptx::mma_f16(d_tmem, ad, bd, C::kIdesc, (it > 0 || kk > 0) ? 1u : 0u);
           }
-          ptx::mma_commit(&empty[stage]);
+          if constexpr (CG == 2)
+            ptx::mma_commit_pair_multicast(&empty[stage], 0x3);  // frees the stage in both CTAs
+          else
+            ptx::mma_commit(&empty[stage]);
           any = true;
           if (++stage == kStages) {
             stage = 0;
@@ -309,22 +359,29 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
           }
         }
         if (!ok) break;
-        ptx::mma_commit(&tfull[acc]);
+        if constexpr (CG == 2)
+          ptx::mma_commit_pair_multicast(&tfull[acc], 0x3);
+        else
+          ptx::mma_commit(&tfull[acc]);
         acc ^= 1u;
         if (acc == 0) acc_phase ^= 1u;
       }
       if (any) {
-        ptx::mma_commit(mma_done);
+        if constexpr (CG == 2)
+          ptx::mma_commit_pair(mma_done);
+        else
+          ptx::mma_commit(mma_done);
         W.drain(mma_done, 0, kDrainNs);
       }
     }
   } else {
     // ------------------------------------------------------------- epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may access
-    const int row_in_tile = q * 32 + lane;
+    const int row_in_tile = static_cast<int>(cta) * kBM + q * 32 + lane;  // row of the pair tile
+    const uint32_t tempty_leader0 = (CG == 2) ? ptx::mapa(ptx::smem_addr(&tempty[0]), 0) : 0u;
     uint32_t acc = 0, acc_phase = 0;
-    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
-      const Tile tl = tile_of<MODE>(p, t);
+    for (int t = pair; t < num_tiles; t += npairs) {
+      const Tile tl = tile_of<MODE, TM>(p, t);
       const bool failed = !W.wait(&tfull[acc], acc_phase);
       if constexpr (MODE == MODE_RS_PUSH || MODE == MODE_AR_PUSH) {
         // The four epilogue warps meet at named barriers below: stop together.
@@ -340,17 +397,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
       int64_t grow = 0;  // global row (RS/AR/PUSH)
       const int esz = p.out_f32 ? 4 : 2;
       if constexpr (MODE == MODE_RS || MODE == MODE_RS_PUSH) {
-        grow = static_cast<int64_t>(tl.mt) * kBM + row_in_tile;
+        grow = static_cast<int64_t>(tl.mt) * TM + row_in_tile;
         row_ok = grow < p.M;
         if (row_ok) {
           const int j = static_cast<int>(grow / p.Ms);
           rowp = static_cast<char*>(p.out[j]) + (grow - static_cast<int64_t>(j) * p.Ms) * p.N * esz;
         }
       } else if constexpr (MODE == MODE_AR || MODE == MODE_AR_PUSH) {
-        grow = static_cast<int64_t>(tl.mt) * kBM + row_in_tile;
+        grow = static_cast<int64_t>(tl.mt) * TM + row_in_tile;
         row_ok = grow < p.M;
       } else if constexpr (MODE == MODE_AG) {
-        const int64_t local = static_cast<int64_t>(tl.mt) * kBM + row_in_tile;
+        const int64_t local = static_cast<int64_t>(tl.mt) * TM + row_in_tile;
         row_ok = local < p.Ms;
         grow = static_cast<int64_t>(tl.shard) * p.Ms + local;
         if (row_ok) rowp = static_cast<char*>(p.out[tl.rank]) + grow * p.N * esz;
@@ -359,7 +416,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         grow = static_cast<int64_t>(tl.row0) + row_in_tile;
         if (row_ok) rowp = static_cast<char*>(p.out[tl.shard]) + grow * p.N * esz;
       } else {  // MODE_PARTIAL
-        grow = static_cast<int64_t>(p.m_begin) + static_cast<int64_t>(tl.mt) * kBM + row_in_tile;
+        grow = static_cast<int64_t>(p.m_begin) + static_cast<int64_t>(tl.mt) * TM + row_in_tile;
         row_ok = grow < p.m_end;
         if (row_ok) rowp = static_cast<char*>(p.out[tl.rank]) + grow * p.N * esz;
       }
@@ -375,7 +432,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
           // Accumulator fully read: hand it back to the MMA warp early.
           ptx::tc_fence_before();
           __syncwarp();
-          if (lane == 0) ptx::mbar_arrive(&tempty[acc]);
+          if (lane == 0) {
+            if constexpr (CG == 2)
+              ptx::mbar_arrive_cluster(tempty_leader0 + acc * 8);
+            else
+              ptx::mbar_arrive(&tempty[acc]);
+          }
         }
         const int col = col0 + c;
         if (!row_ok || col >= p.N) continue;
@@ -400,11 +462,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
 
       if constexpr (MODE == MODE_RS_PUSH || MODE == MODE_AR_PUSH) {
         if (!p.out_f32) {
-          // Last of the R contributions to this output tile converts it to bf16.
+          // Last of the R contributions to this CTA's rows of the output tile
+          // converts them to bf16 (one ticket per tile and CTA of the pair).
           __threadfence();
           ptx::named_barrier_sync(1, 128);
           if (threadIdx.x == 64) {
-            const int tid = tl.mt * p.tiles_n + tl.nt;
+            const int tid = (tl.mt * p.tiles_n + tl.nt) * CG + static_cast<int>(cta);
             const int prev = atomicAdd(&p.tickets[tid], 1);
             *bcast = (prev == p.R - 1) ? 1 : 0;
             if (prev == p.R - 1) p.tickets[tid] = 0;
@@ -448,41 +511,72 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
 
   __syncwarp();
   ptx::tc_fence_before();
-  __syncthreads();
+  if constexpr (CG == 2) {
+    // The leader's MMAs read the peer's shared memory and write the peer's TMEM:
+    // neither CTA frees anything before both are done.
+    ptx::cluster_sync_all();
+  } else {
+    __syncthreads();
+  }
   if (warp == 1) {
     ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem_base, kTmemCols);
+    if constexpr (CG == 2)
+      ptx::tmem_dealloc_pair(tmem_base, kTmemCols);
+    else
+      ptx::tmem_dealloc(tmem_base, kTmemCols);
   }
 }
 
-template <int MODE, class P>
+template <int MODE, int CG, class P>
 cudaError_t launch_mode(const P& p, int grid, cudaStream_t st) {
-  auto kern = gemm_kernel<MODE, P>;
+  auto kern = gemm_kernel<MODE, CG, P>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       kSmemBytes);
+                                       Cfg<CG>::kSmem);
   if (e != cudaSuccess) return e;
-  kern<<<grid, kGemmThreads, kSmemBytes, st>>>(p);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(kGemmThreads, 1, 1);
+  cfg.dynamicSmemBytes = Cfg<CG>::kSmem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CG;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kern, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
-}  // namespace
-
-int gemm_smem_bytes() { return kSmemBytes; }
-
-cudaError_t launch_gemm(const GemmParams& p, int mode, int grid, cudaStream_t st) {
+template <int CG>
+cudaError_t launch_cg(const GemmParams& p, int mode, int grid, cudaStream_t st) {
   switch (mode) {
-    case MODE_RS: return launch_mode<MODE_RS, GemmParams>(p, grid, st);
-    case MODE_AR: return launch_mode<MODE_AR, GemmParams>(p, grid, st);
-    case MODE_PARTIAL: return launch_mode<MODE_PARTIAL, GemmParams>(p, grid, st);
-    case MODE_AG: return launch_mode<MODE_AG, GemmParams>(p, grid, st);
-    case MODE_RS_PUSH: return launch_mode<MODE_RS_PUSH, GemmParams>(p, grid, st);
-    case MODE_AR_PUSH: return launch_mode<MODE_AR_PUSH, GemmParams>(p, grid, st);
+    case MODE_RS: return launch_mode<MODE_RS, CG, GemmParams>(p, grid, st);
+    case MODE_AR: return launch_mode<MODE_AR, CG, GemmParams>(p, grid, st);
+    case MODE_PARTIAL: return launch_mode<MODE_PARTIAL, CG, GemmParams>(p, grid, st);
+    case MODE_AG: return launch_mode<MODE_AG, CG, GemmParams>(p, grid, st);
+    case MODE_RS_PUSH: return launch_mode<MODE_RS_PUSH, CG, GemmParams>(p, grid, st);
+    case MODE_AR_PUSH: return launch_mode<MODE_AR_PUSH, CG, GemmParams>(p, grid, st);
     default: return cudaErrorInvalidValue;
   }
 }
 
-cudaError_t launch_grouped_gemm(const GroupedParams& p, int grid, cudaStream_t st) {
-  return launch_mode<MODE_GROUPED, GroupedParams>(p, grid, st);
+}  // namespace
+
+int gemm_smem_bytes(int cg) { return cg == 2 ? Cfg<2>::kSmem : Cfg<1>::kSmem; }
+
+cudaError_t launch_gemm(const GemmParams& p, int mode, int cg, int grid, cudaStream_t st) {
+  if (cg == 2) return launch_cg<2>(p, mode, grid, st);
+  if (cg == 1) return launch_cg<1>(p, mode, grid, st);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_grouped_gemm(const GroupedParams& p, int cg, int grid, cudaStream_t st) {
+  if (cg == 2) return launch_mode<MODE_GROUPED, 2, GroupedParams>(p, grid, st);
+  if (cg == 1) return launch_mode<MODE_GROUPED, 1, GroupedParams>(p, grid, st);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace fcc

@@ -42,7 +42,8 @@ struct GemmParams {
   int* status;
   unsigned long long timeout_ns;
   float* acc_ws;        // push mode with bf16 output: f32 accumulation rows (M x N)
-  int* tickets;         // push mode with bf16 output: per output tile arrival counters
+  int* tickets;         // push mode with bf16 output: per (tile, CTA of the pair) counters
+  int cg;               // host side: tile shape of the launch (1 or 2 CTAs per tile)
 };
 
 struct GemvParams {
@@ -81,9 +82,11 @@ struct GroupedParams {
   unsigned long long timeout_ns;
 };
 
-cudaError_t launch_gemm(const GemmParams& p, int mode, int grid, cudaStream_t st);
-cudaError_t launch_grouped_gemm(const GroupedParams& p, int grid, cudaStream_t st);
-int gemm_smem_bytes();
+// cg = 1: one CTA per 128 x 256 tile; cg = 2: a CTA pair (cluster of 2) per
+// 256 x 256 tile.  grid is in CTAs (a multiple of cg).
+cudaError_t launch_gemm(const GemmParams& p, int mode, int cg, int grid, cudaStream_t st);
+cudaError_t launch_grouped_gemm(const GroupedParams& p, int cg, int grid, cudaStream_t st);
+int gemm_smem_bytes(int cg);
 cudaError_t launch_gemv(const GemvParams& p, int grid, cudaStream_t st);
 int gemv_smem_bytes();
 

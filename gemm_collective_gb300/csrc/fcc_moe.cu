@@ -7,10 +7,10 @@
 //                     lower index, found with warp shuffles), softmax gates,
 //                     and a per-chunk expert histogram (chunk = 128 tokens of
 //                     one source rank).
-//   2. scan_kernel    one CTA: exclusive prefix of the histograms over chunks
-//                     (a fixed order), expert counts, send counts, each
-//                     expert's first row in its receiving rank's buffer, and
-//                     the grouped GEMM's tile table.
+//   2. scan_kernel    one CTA per expert: exclusive prefix of its histogram
+//                     over the chunks (a fixed order) and its count;
+//      finalize_kernel  send counts, each expert's first row in its receiving
+//                     rank's buffer, and the grouped GEMM's tile table.
 //   3. rank_kernel    one CTA per chunk: the stable rank of every assignment
 //                     within its expert (warp match + popc, then a prefix over
 //                     the CTA's warps), i.e. its receive row; writes recv_src.
@@ -47,6 +47,7 @@ struct MoeArgs {
   int cap;
   int chunks_per_rank;
   int tiles_n;
+  int tile_m;             // rows per grouped-GEMM tile
   int32_t* chunk_counts;  // [nchunks][E]
   int32_t* chunk_off;     // [nchunks][E]
   int32_t* expert_counts; // [E] (caller's output)
@@ -129,23 +130,49 @@ __global__ void __launch_bounds__(256) route_kernel(const MoeArgs a) {
     a.chunk_counts[static_cast<long long>(chunk) * a.E + threadIdx.x] = hist[threadIdx.x];
 }
 
-// One CTA of 64 threads.  Thread e scans expert e's histogram over the chunks
-// in chunk order (source rank, then token), so chunk_off[c][e] is the number of
-// assignments to e that precede chunk c in (s, t, slot) order.
-__global__ void __launch_bounds__(64) scan_kernel(const MoeArgs a) {
+// One CTA per expert e (256 threads): exclusive prefix of expert e's histogram
+// over the chunks, in chunk order (source rank, then token), so chunk_off[c][e]
+// is the number of assignments to e that precede chunk c in (s, t, slot)
+// order.  Integer sums in a fixed tree of warp shuffles: the result does not
+// depend on any scheduling.
+__global__ void __launch_bounds__(256) scan_kernel(const MoeArgs a) {
+  __shared__ int warp_tot[8];
+  __shared__ int carry_s;
+  const int e = blockIdx.x;
+  const int nchunks = a.R * a.chunks_per_rank;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) carry_s = 0;
+  __syncthreads();
+  for (int c0 = 0; c0 < nchunks; c0 += 256) {
+    const int c = c0 + threadIdx.x;
+    const int v = c < nchunks ? a.chunk_counts[static_cast<long long>(c) * a.E + e] : 0;
+    int incl = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += y;
+    }
+    if (lane == 31) warp_tot[warp] = incl;
+    __syncthreads();
+    int before = carry_s;
+    for (int w = 0; w < warp; ++w) before += warp_tot[w];
+    if (c < nchunks) a.chunk_off[static_cast<long long>(c) * a.E + e] = before + incl - v;
+    __syncthreads();
+    if (threadIdx.x == 255) carry_s = before + incl;
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) a.expert_counts[e] = carry_s;
+}
+
+// One CTA of 64 threads after the scan: each expert's first row in its
+// receiving rank's buffer and its kept rows (capacity), the send counts and the
+// grouped GEMM's tile table.
+__global__ void __launch_bounds__(64) finalize_kernel(const MoeArgs a) {
   __shared__ int counts[FCC_MAX_EXPERTS];
   __shared__ int rows[FCC_MAX_EXPERTS];
   const int e = threadIdx.x;
   const int nchunks = a.R * a.chunks_per_rank;
-  if (e < a.E) {
-    int run = 0;
-    for (int c = 0; c < nchunks; ++c) {
-      a.chunk_off[static_cast<long long>(c) * a.E + e] = run;
-      run += a.chunk_counts[static_cast<long long>(c) * a.E + e];
-    }
-    counts[e] = run;
-    a.expert_counts[e] = run;
-  }
+  if (e < a.E) counts[e] = a.expert_counts[e];
   __syncthreads();
   if (e < a.E) {
     const int d = e / a.Eloc;
@@ -159,13 +186,17 @@ __global__ void __launch_bounds__(64) scan_kernel(const MoeArgs a) {
     if (e == (d + 1) * a.Eloc - 1 && base + counts[e] > a.cap && a.status != nullptr)
       atomicCAS(a.status, 0, FCC_ERR_CAPACITY);
   }
-  // send_counts[s][d]: assignments from source rank s to the experts of rank d
+  // send_counts[s][d]: assignments from source rank s to the experts of rank d,
+  // read off the prefix at the boundaries of s's chunks.
   if (e < a.R * a.R) {
     const int s = e / a.R, d = e - (e / a.R) * a.R;
+    const int c_lo = s * a.chunks_per_rank, c_hi = (s + 1) * a.chunks_per_rank;
     int sum = 0;
-    for (int c = s * a.chunks_per_rank; c < (s + 1) * a.chunks_per_rank; ++c)
-      for (int f = d * a.Eloc; f < (d + 1) * a.Eloc; ++f)
-        sum += a.chunk_counts[static_cast<long long>(c) * a.E + f];
+    for (int f = d * a.Eloc; f < (d + 1) * a.Eloc; ++f) {
+      const int hi = c_hi < nchunks ? a.chunk_off[static_cast<long long>(c_hi) * a.E + f]
+                                    : counts[f];
+      sum += hi - a.chunk_off[static_cast<long long>(c_lo) * a.E + f];
+    }
     a.send_counts[e] = sum;
   }
   __syncthreads();
@@ -173,7 +204,7 @@ __global__ void __launch_bounds__(64) scan_kernel(const MoeArgs a) {
     int acc = 0;
     for (int f = 0; f < a.E; ++f) {
       a.tile_start[f] = acc;
-      acc += ((rows[f] + kBM - 1) / kBM) * a.tiles_n;
+      acc += ((rows[f] + a.tile_m - 1) / a.tile_m) * a.tiles_n;
     }
     a.tile_start[a.E] = acc;
   }
@@ -384,6 +415,8 @@ fcc_status fcc_moe_dispatch_gemm(int R, const void* const* X, const float* const
   a.cap = static_cast<int>(cap);
   a.chunks_per_rank = plan.chunks_per_rank;
   a.tiles_n = static_cast<int>((F + kMoeBN - 1) / kMoeBN);
+  const int cg = (opts != nullptr && opts->cta_pair == 1) ? 1 : 2;
+  a.tile_m = kBM * cg;
   a.chunk_counts = reinterpret_cast<int32_t*>(base + plan.off_chunk_counts);
   a.chunk_off = reinterpret_cast<int32_t*>(base + plan.off_chunk_off);
   a.expert_counts = expert_counts;
@@ -417,12 +450,14 @@ fcc_status fcc_moe_dispatch_gemm(int R, const void* const* X, const float* const
   g.timeout_ns = timeout_ns;
 
   route_kernel<<<plan.nchunks, 256, 0, st>>>(a);
-  scan_kernel<<<1, 64, 0, st>>>(a);
+  scan_kernel<<<E, 256, 0, st>>>(a);
+  finalize_kernel<<<1, 64, 0, st>>>(a);
   rank_kernel<<<plan.nchunks, 256, 0, st>>>(a);
   copy_kernel<<<std::max(1, sms) * 4, 256, 0, st>>>(a);
   if (cudaGetLastError() != cudaSuccess) return FCC_ERR_CUDA;
-  if (launch_grouped_gemm(g, std::max(1, sms), st) != cudaSuccess) return FCC_ERR_CUDA;
-  bump_launch_count(5);
+  const int grid = std::max(cg, (sms / cg) * cg);
+  if (launch_grouped_gemm(g, cg, grid, st) != cudaSuccess) return FCC_ERR_CUDA;
+  bump_launch_count(6);
   return FCC_OK;
 }
 

@@ -85,6 +85,10 @@ typedef struct {
   int64_t timeout_ns;      /* device wait limit; 0 = 1 s */
   void *workspace;         /* device scratch, or NULL for the internal pool */
   size_t workspace_bytes;
+  /* Tensor-core tile shape of the GEMMs: 0 = automatic (a CTA pair per
+   * 256 x 256 tile when the rows exceed 128), 1 = one CTA per 128 x 256 tile,
+   * 2 = a CTA pair (cluster of 2, tcgen05 cta_group::2) per 256 x 256 tile. */
+  int cta_pair;
 } fcc_opts;
 
 /* Operator identifiers for fcc_workspace_size. */

@@ -44,12 +44,13 @@ def _ar(R, dA, dB, M, N, K, out_dtype, opts=None):
 
 # ------------------------------------------------------------ exactness first
 
-def test_rs_integer_inputs_bit_exact():
+@pytest.mark.parametrize("pair", [1, 2])
+def test_rs_integer_inputs_bit_exact(pair):
     """Small integers: every f32 partial sum is exact, so GPU == oracle exactly."""
-    R, M, N, K = 2, 256, 256, 128
+    R, M, N, K = 2, 512, 512, 128
     A, B = synth.integer_gemm_inputs(R, M, N, K, -4, 4, seed=1)
     dA, dB = _upload(A, B)
-    outs = _rs(R, dA, dB, M, N, K, fcc.FCC_F32)
+    outs = _rs(R, dA, dB, M, N, K, fcc.FCC_F32, fcc.make_opts(cta_pair=pair))
     for j in range(R):
         assert np.array_equal(to_f64(outs[j]), oracle.gemm_rs(A, B, j)), f"shard {j}"
 
@@ -97,25 +98,29 @@ RAGGED = [
 
 @pytest.mark.parametrize("R,M,N,K", RAGGED)
 @pytest.mark.parametrize("out_dtype", [0, 2])
-def test_rs_ragged(R, M, N, K, out_dtype):
+@pytest.mark.parametrize("pair", [1, 2])
+def test_rs_ragged(R, M, N, K, out_dtype, pair):
     A, B = synth.gemm_inputs(R, M, N, K, 1.0, 1.0, seed=R * 7 + K)
     dA, dB = _upload(A, B)
-    outs = _rs(R, dA, dB, M, N, K, out_dtype)
+    outs = _rs(R, dA, dB, M, N, K, out_dtype, fcc.make_opts(cta_pair=pair))
     for j in range(R):
         assert_close(to_f64(outs[j]), oracle.gemm_rs(A, B, j), f"shard {j}")
 
 
-@pytest.mark.parametrize("R,M,N,K", [(4, 200, 264, 136), (2, 130, 16, 64), (8, 256, 256, 64)])
-def test_ar_all_buffers_identical_and_equal_rs(R, M, N, K):
+@pytest.mark.parametrize("R,M,N,K", [(4, 200, 264, 136), (2, 130, 16, 64), (8, 256, 256, 64),
+                                     (4, 1032, 264, 128)])
+@pytest.mark.parametrize("pair", [0, 1])
+def test_ar_all_buffers_identical_and_equal_rs(R, M, N, K, pair):
     A, B = synth.gemm_inputs(R, M, N, K, 1.0, 1.0, seed=3)
     dA, dB = _upload(A, B)
-    outs = _ar(R, dA, dB, M, N, K, fcc.FCC_BF16)
+    o = fcc.make_opts(cta_pair=pair)
+    outs = _ar(R, dA, dB, M, N, K, fcc.FCC_BF16, o)
     ref = oracle.gemm_ar(A, B)
     assert_close(to_f64(outs[0]), ref, "ar")
     for r in range(1, R):
         assert np.array_equal(bits(outs[r]), bits(outs[0])), f"rank {r} differs"
     if M % R == 0:
-        shards = _rs(R, dA, dB, M, N, K, fcc.FCC_BF16)
+        shards = _rs(R, dA, dB, M, N, K, fcc.FCC_BF16, o)
         cat = np.concatenate([bits(s) for s in shards])
         assert np.array_equal(cat, bits(outs[0])), "RS shards != AR rows (deterministic mode)"
 
@@ -143,11 +148,12 @@ ALGOS = [
 
 @pytest.mark.parametrize("name,kw", ALGOS)
 @pytest.mark.parametrize("out_dtype", [0, 2])
-def test_rs_algorithms(name, kw, out_dtype):
+@pytest.mark.parametrize("pair", [1, 2])
+def test_rs_algorithms(name, kw, out_dtype, pair):
     R, M, N, K = 4, 640, 520, 192
     A, B = synth.gemm_inputs(R, M, N, K, 1.0, 1.0, seed=11)
     dA, dB = _upload(A, B)
-    outs = _rs(R, dA, dB, M, N, K, out_dtype, fcc.make_opts(**kw))
+    outs = _rs(R, dA, dB, M, N, K, out_dtype, fcc.make_opts(cta_pair=pair, **kw))
     for j in range(R):
         assert_close(to_f64(outs[j]), oracle.gemm_rs(A, B, j), f"{name} shard {j}")
 
@@ -184,7 +190,8 @@ def test_caller_workspace_and_too_small():
 
 # ----------------------------------------------------------------- AG + GEMM
 
-@pytest.mark.parametrize("R,Ms,N,K", [(4, 136, 200, 96), (2, 128, 512, 64), (8, 64, 264, 136)])
+@pytest.mark.parametrize("R,Ms,N,K", [(4, 136, 200, 96), (2, 128, 512, 64), (8, 64, 264, 136),
+                                      (2, 520, 264, 64)])
 @pytest.mark.parametrize("algo", [1, 2, 4])
 def test_ag_gemm(R, Ms, N, K, algo):
     X, B = synth.gemm_inputs(R, Ms, N, K, 1.0, 1.0, seed=17 + R)

@@ -26,7 +26,7 @@ import gemm_collective_gb300 as fcc  # noqa: E402
 GATE_RTOL = 5e-6
 
 
-def _run(X, logits, W, R, T, H, F, E, topk, cap, out_dtype=fcc.FCC_BF16):
+def _run(X, logits, W, R, T, H, F, E, topk, cap, out_dtype=fcc.FCC_BF16, opts=None):
     dX = [dev_bf16(x) for x in X]
     dL = [dev_f32(l) for l in logits]
     dW = [dev_bf16(w) for w in W]
@@ -39,7 +39,7 @@ def _run(X, logits, W, R, T, H, F, E, topk, cap, out_dtype=fcc.FCC_BF16):
     send = torch.full((R * R,), -7, dtype=torch.int32, device="cuda")
     src = [torch.full((cap,), -1, dtype=torch.int32, device="cuda") for _ in range(R)]
     fcc.fcc_moe_dispatch_gemm(R, dX, dL, dW, T, H, F, E, topk, recv_x, recv_y, cap, idx, gate,
-                              counts, send, src, fcc.FCC_BF16, out_dtype)
+                              counts, send, src, fcc.FCC_BF16, out_dtype, opts)
     st = fcc.fcc_stream_status()
     return dict(recv_x=recv_x, recv_y=recv_y, idx=idx, gate=gate, counts=counts, send=send,
                 src=src, status=st)
@@ -84,10 +84,11 @@ def _check(X, logits, W, R, T, H, F, E, topk, cap, out, sample=None, seed=0):
     (4, 130, 128, 72, 4, 2),      # one expert per rank: plain all-to-all
     (1, 500, 128, 256, 8, 2),     # one rank
 ])
-def test_moe_small(R, T, H, F, E, topk):
+@pytest.mark.parametrize("pair", [1, 2])
+def test_moe_small(R, T, H, F, E, topk, pair):
     X, logits, W = synth.moe_inputs(R, T, H, E, F, seed=R * 100 + T)
     cap = R * T * topk
-    out = _run(X, logits, W, R, T, H, F, E, topk, cap)
+    out = _run(X, logits, W, R, T, H, F, E, topk, cap, opts=fcc.make_opts(cta_pair=pair))
     _check(X, logits, W, R, T, H, F, E, topk, cap, out)
 
 
