@@ -86,8 +86,8 @@ __device__ __forceinline__ float warp_sum(float x) {
   return x;
 }
 
-// Grid: one CTA per chunk, 256 threads (8 warps, one token at a time each).
-__global__ void __launch_bounds__(256) route_kernel(const MoeArgs a) {
+// Grid: one CTA per chunk, 1024 threads (32 warps, one token at a time each).
+__global__ void __launch_bounds__(1024) route_kernel(const MoeArgs a) {
   __shared__ int hist[FCC_MAX_EXPERTS];
   const int chunk = blockIdx.x;
   const int s = chunk / a.chunks_per_rank;
@@ -97,7 +97,7 @@ __global__ void __launch_bounds__(256) route_kernel(const MoeArgs a) {
   if (threadIdx.x < FCC_MAX_EXPERTS) hist[threadIdx.x] = 0;
   __syncthreads();
   const float neg_inf = __int_as_float(0xff800000);
-  for (int t = t0 + warp; t < t1; t += 8) {
+  for (int t = t0 + warp; t < t1; t += 32) {
     const float* lg = a.logits[s] + static_cast<long long>(t) * a.E;
     const float l0 = lane < a.E ? lg[lane] : neg_inf;
     const float l1 = lane + 32 < a.E ? lg[lane + 32] : neg_inf;
@@ -449,7 +449,7 @@ fcc_status fcc_moe_dispatch_gemm(int R, const void* const* X, const float* const
   g.status = status;
   g.timeout_ns = timeout_ns;
 
-  route_kernel<<<plan.nchunks, 256, 0, st>>>(a);
+  route_kernel<<<plan.nchunks, 1024, 0, st>>>(a);
   scan_kernel<<<E, 256, 0, st>>>(a);
   finalize_kernel<<<1, 64, 0, st>>>(a);
   rank_kernel<<<plan.nchunks, 256, 0, st>>>(a);
