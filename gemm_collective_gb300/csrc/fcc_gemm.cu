@@ -213,9 +213,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
   const int pair = blockIdx.x / CG;
   const int npairs = gridDim.x / CG;
 
+  // Gather mode (MoE without a staged copy): the producer warp copies A rows
+  // with cp.async and signals each stage once its copies have landed, so the
+  // full barrier also counts one A-ready arrival per CTA of the pair.
+  bool gather = false;
+  if constexpr (MODE == MODE_GROUPED) gather = p.gather != 0;
+  const uint32_t full_count = gather ? 1u + CG : 1u;
+
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      ptx::mbar_init(&full[s], 1);
+      ptx::mbar_init(&full[s], full_count);
       ptx::mbar_init(&empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -253,7 +260,113 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
   const uint32_t tmem_base = *tmem_slot;
   const ptx::Waiter W{abort_flag, p.status, p.timeout_ns};
 
-  if (warp == 0) {
+  if (warp == 0 && gather) {
+    // ----------------------------------------------- producer, gather mode
+    // The whole warp: lane l copies rows l, l+32, l+64, l+96 of this CTA's 128
+    // A rows, 16 bytes at a time, straight from the source token rows, into
+    // the 128-byte-swizzled K-major layout the MMA descriptor expects (chunk c
+    // of row r lands at r*128 + ((c ^ (r % 8)) * 16)).  Each stage's copies are
+    // a cp.async group; a stage is signalled ready kLag stages later, after
+    // its group has landed and a proxy fence has made it visible to the tensor
+    // core.  Lane 0 also loads the B tile with TMA.
+    if constexpr (MODE == MODE_GROUPED) {
+      constexpr int kLag = 3;
+      const uint32_t full0_leader = (CG == 2) ? ptx::mapa(ptx::smem_addr(&full[0]), 0) : 0u;
+      auto signal = [&](uint32_t s) {
+        if (lane == 0) {
+          if constexpr (CG == 2)
+            ptx::mbar_arrive_cluster(full0_leader + s * 8);
+          else
+            ptx::mbar_arrive(&full[s]);
+        }
+      };
+      uint32_t stage = 0, phase = 0, sig = 0;
+      int pending = 0;
+      uint32_t issued = 0, last_parity = 0;
+      bool ok = true;
+      const uint16_t* X0 = static_cast<const uint16_t*>(p.X[0]);
+      for (int t = pair; t < num_tiles && ok; t += npairs) {
+        const Tile tl = tile_of<MODE, TM>(p, t);
+        const int b_col = tl.nt * kBN + static_cast<int>(cta) * C::kBNcta;
+        const uint16_t* rowp[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int local = static_cast<int>(cta) * kBM + lane + 32 * j;
+          rowp[j] = X0;  // padding rows read a valid row; their results are not stored
+          if (local < tl.rows) {
+            const int src = __ldcg(p.recv_src[tl.shard] + tl.row0 + local);
+            const int s = src / p.T;
+            rowp[j] = static_cast<const uint16_t*>(p.X[s]) +
+                      static_cast<long long>(src - s * p.T) * p.K;
+          }
+        }
+        for (int it = 0; it < k_iters; ++it) {
+          if (!W.wait(&empty[stage], phase ^ 1u)) {
+            ok = false;
+            break;
+          }
+          if (lane == 0) {
+            const CUtensorMap* mb = &p.mapB[tl.expert];
+            uint8_t* b_dst = sB + stage * C::kBBytes;
+            if constexpr (CG == 2) {
+              const uint32_t bar = ptx::mapa(ptx::smem_addr(&full[stage]), 0);
+              if (cta == 0) ptx::mbar_arrive_expect_tx(&full[stage], 2 * C::kBBytes);
+#pragma unroll
+              for (int i = 0; i < C::kBNcta / 64; ++i)
+                ptx::tma_load_2d_pair(b_dst + i * kBBoxBytes, mb, bar, b_col + 64 * i, it * kBK);
+            } else {
+              ptx::mbar_arrive_expect_tx(&full[stage], C::kBBytes);
+#pragma unroll
+              for (int i = 0; i < C::kBNcta / 64; ++i)
+                ptx::tma_load_2d(b_dst + i * kBBoxBytes, mb, &full[stage], b_col + 64 * i,
+                                 it * kBK);
+            }
+            issued |= 1u << stage;
+            last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
+          }
+          const uint32_t a_base = ptx::smem_addr(sA + stage * kABytes);
+          const int k0 = it * kBK;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int r = lane + 32 * j;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              const int k = k0 + c * 8;
+              const bool in = k < p.K;
+              ptx::cp_async_16(a_base + r * 128 + ((c ^ (r & 7)) << 4), rowp[j] + (in ? k : 0),
+                               in ? 16u : 0u);
+            }
+          }
+          ptx::cp_async_commit();
+          if (++pending > kLag) {
+            ptx::cp_async_wait<kLag>();
+            ptx::fence_proxy_async_smem();
+            __syncwarp();
+            signal(sig);
+            if (++sig == static_cast<uint32_t>(kStages)) sig = 0;
+            --pending;
+          }
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // Flush: every issued stage is signalled once its copies have landed.
+      ptx::cp_async_wait<0>();
+      ptx::fence_proxy_async_smem();
+      __syncwarp();
+      while (pending > 0) {
+        signal(sig);
+        if (++sig == static_cast<uint32_t>(kStages)) sig = 0;
+        --pending;
+      }
+      if (*abort_flag && cta == 0 && lane == 0) {
+        for (int s = 0; s < kStages; ++s)
+          if (issued & (1u << s)) W.drain(&full[s], (last_parity >> s) & 1u, kDrainNs);
+      }
+    }
+  } else if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       uint32_t stage = 0, phase = 0;
@@ -330,7 +443,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * kBN;
         for (int it = 0; it < k_iters; ++it) {
-          if (!W.wait(&full[stage], phase)) {
+          // In a pair, the peer's A-ready arrival is released at cluster scope.
+          if (!W.template wait<CG == 2>(&full[stage], phase)) {
             ok = false;
             break;
           }

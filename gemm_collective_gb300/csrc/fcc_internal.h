@@ -80,6 +80,13 @@ struct GroupedParams {
   const int* expert_rows;              // [E] (clamped to the receive capacity)
   int* status;
   unsigned long long timeout_ns;
+  // Gather mode (gather = 1): the A rows are read straight from the source
+  // tokens, row i of rank d's receive order being X[s][t] with
+  // recv_src[d][i] = s*T + t, instead of from a staged copy (mapA unused).
+  const void* X[FCC_MAX_RANKS];        // [T, H] bf16 per source rank
+  const int* recv_src[FCC_MAX_RANKS];  // [cap] per receiving rank
+  int T;
+  int gather;
 };
 
 // cg = 1: one CTA per 128 x 256 tile; cg = 2: a CTA pair (cluster of 2) per

@@ -15,9 +15,13 @@
 //                     within its expert (warp match + popc, then a prefix over
 //                     the CTA's warps), i.e. its receive row; writes recv_src.
 //   4. copy_kernel    one warp per token: reads the token row once and writes
-//                     it to each of its receive rows (the all-to-all).
+//                     it to each of its receive rows (the all-to-all), when
+//                     the caller asks for the staged rows (recv_x given).
 //   5. the persistent tcgen05 GEMM in grouped mode: tiles over
 //                     (expert, m tile, n tile) from the device tile table.
+//                     Without recv_x the GEMM's producer warp gathers each A
+//                     row straight from the source token (recv_src gives it),
+//                     so the dispatched rows never make a round trip to HBM.
 // No atomics decide any position, so every index output is bit-exact and
 // repeatable; the host never waits for the counts.
 #include <cuda_runtime.h>
@@ -350,7 +354,6 @@ fcc_status check_moe(int R, const void* const* X, const float* const* logits,
   if (in != FCC_BF16) return FCC_ERR_UNSUPPORTED;
   if (out_dtype != FCC_BF16 && out_dtype != FCC_F32)
     return out_dtype == FCC_F16 ? FCC_ERR_UNSUPPORTED : FCC_ERR_INVALID;
-  if (recv_x == nullptr) return FCC_ERR_UNSUPPORTED;  // the rows are staged in recv_x
   if (opts != nullptr && opts->algo != FCC_ALGO_AUTO && opts->algo != FCC_ALGO_FUSED &&
       opts->algo != FCC_ALGO_UNFUSED)
     return FCC_ERR_UNSUPPORTED;
@@ -403,7 +406,7 @@ fcc_status fcc_moe_dispatch_gemm(int R, const void* const* X, const float* const
     a.logits[r] = logits[r];
     a.idx[r] = topk_idx[r];
     a.gate[r] = topk_gate[r];
-    a.recv_x[r] = recv_x[r];
+    a.recv_x[r] = recv_x != nullptr ? recv_x[r] : nullptr;
     a.recv_src[r] = recv_src[r];
   }
   a.R = R;
@@ -429,8 +432,12 @@ fcc_status fcc_moe_dispatch_gemm(int R, const void* const* X, const float* const
 
   GroupedParams g;
   std::memset(&g, 0, sizeof(g));
+  const bool gather = (recv_x == nullptr);
   for (int d = 0; d < R; ++d) {
-    if ((s = internal_make_map(&g.mapA[d], recv_x[d], cap, H, kBM)) != FCC_OK) return s;
+    if (!gather && (s = internal_make_map(&g.mapA[d], recv_x[d], cap, H, kBM)) != FCC_OK)
+      return s;
+    g.X[d] = X[d];
+    g.recv_src[d] = recv_src[d];
     g.out[d] = recv_y[d];
   }
   for (int e = 0; e < E; ++e)
@@ -448,16 +455,18 @@ fcc_status fcc_moe_dispatch_gemm(int R, const void* const* X, const float* const
   g.expert_rows = a.expert_rows;
   g.status = status;
   g.timeout_ns = timeout_ns;
+  g.T = static_cast<int>(T);
+  g.gather = gather ? 1 : 0;
 
   route_kernel<<<plan.nchunks, 1024, 0, st>>>(a);
   scan_kernel<<<E, 256, 0, st>>>(a);
   finalize_kernel<<<1, 64, 0, st>>>(a);
   rank_kernel<<<plan.nchunks, 256, 0, st>>>(a);
-  copy_kernel<<<std::max(1, sms) * 4, 256, 0, st>>>(a);
+  if (!gather) copy_kernel<<<std::max(1, sms) * 4, 256, 0, st>>>(a);
   if (cudaGetLastError() != cudaSuccess) return FCC_ERR_CUDA;
   const int grid = std::max(cg, (sms / cg) * cg);
   if (launch_grouped_gemm(g, cg, grid, st) != cudaSuccess) return FCC_ERR_CUDA;
-  bump_launch_count(6);
+  bump_launch_count(gather ? 5 : 6);
   return FCC_OK;
 }
 

@@ -26,12 +26,13 @@ import gemm_collective_gb300 as fcc  # noqa: E402
 GATE_RTOL = 5e-6
 
 
-def _run(X, logits, W, R, T, H, F, E, topk, cap, out_dtype=fcc.FCC_BF16, opts=None):
+def _run(X, logits, W, R, T, H, F, E, topk, cap, out_dtype=fcc.FCC_BF16, opts=None,
+         staged=True):
     dX = [dev_bf16(x) for x in X]
     dL = [dev_f32(l) for l in logits]
     dW = [dev_bf16(w) for w in W]
     tdt = torch.float32 if out_dtype == fcc.FCC_F32 else torch.bfloat16
-    recv_x = [empty((cap, H), torch.bfloat16, fill=0.0) for _ in range(R)]
+    recv_x = [empty((cap, H), torch.bfloat16, fill=0.0) for _ in range(R)] if staged else None
     recv_y = [empty((cap, F), tdt, fill=float("nan")) for _ in range(R)]
     idx = [torch.full((T, topk), -7, dtype=torch.int32, device="cuda") for _ in range(R)]
     gate = [empty((T, topk), torch.float32) for _ in range(R)]
@@ -67,10 +68,11 @@ def _check(X, logits, W, R, T, H, F, E, topk, cap, out, sample=None, seed=0):
             rng.choice(n, size=min(n, sample), replace=False))
         s_rank = d.recv_src[dst, rows] // T
         s_tok = d.recv_src[dst, rows] % T
-        # staged rows are the source rows, bit for bit
-        rx = out["recv_x"][dst][torch.from_numpy(rows).cuda()].view(torch.int16).cpu().numpy()
-        want = np.stack([X[s][t] for s, t in zip(s_rank, s_tok)]).view(np.int16)
-        assert np.array_equal(rx, want), f"recv_x of rank {dst}"
+        if out["recv_x"] is not None:
+            # staged rows are the source rows, bit for bit
+            rx = out["recv_x"][dst][torch.from_numpy(rows).cuda()].view(torch.int16).cpu().numpy()
+            want = np.stack([X[s][t] for s, t in zip(s_rank, s_tok)]).view(np.int16)
+            assert np.array_equal(rx, want), f"recv_x of rank {dst}"
         ref = oracle.moe_expert_rows(X, W, s_rank, s_tok, d.recv_expert[dst, rows])
         got = to_f64(out["recv_y"][dst][torch.from_numpy(rows).cuda()])
         assert_close(got, ref, f"recv_y of rank {dst}")
@@ -85,10 +87,12 @@ def _check(X, logits, W, R, T, H, F, E, topk, cap, out, sample=None, seed=0):
     (1, 500, 128, 256, 8, 2),     # one rank
 ])
 @pytest.mark.parametrize("pair", [1, 2])
-def test_moe_small(R, T, H, F, E, topk, pair):
+@pytest.mark.parametrize("staged", [True, False])
+def test_moe_small(R, T, H, F, E, topk, pair, staged):
     X, logits, W = synth.moe_inputs(R, T, H, E, F, seed=R * 100 + T)
     cap = R * T * topk
-    out = _run(X, logits, W, R, T, H, F, E, topk, cap, opts=fcc.make_opts(cta_pair=pair))
+    out = _run(X, logits, W, R, T, H, F, E, topk, cap, opts=fcc.make_opts(cta_pair=pair),
+               staged=staged)
     _check(X, logits, W, R, T, H, F, E, topk, cap, out)
 
 
@@ -99,7 +103,7 @@ def test_moe_ties_and_f32_output():
     logits[0][1, [2, 6]] = 9.0             # tie for first: 2 then 6
     logits[1][5, [7, 3, 5]] = [4.0, 4.0, 4.0]
     cap = R * T * topk
-    out = _run(X, logits, W, R, T, H, F, E, topk, cap, fcc.FCC_F32)
+    out = _run(X, logits, W, R, T, H, F, E, topk, cap, fcc.FCC_F32, staged=False)
     _check(X, logits, W, R, T, H, F, E, topk, cap, out)
     idx0 = out["idx"][0].cpu().numpy()
     assert list(idx0[0]) == [0, 1] and list(idx0[1]) == [2, 6]
@@ -109,8 +113,8 @@ def test_moe_repeatable():
     R, T, H, F, E, topk = 4, 256, 128, 128, 16, 2
     X, logits, W = synth.moe_inputs(R, T, H, E, F, seed=6)
     cap = R * T * topk
-    a = _run(X, logits, W, R, T, H, F, E, topk, cap)
-    b = _run(X, logits, W, R, T, H, F, E, topk, cap)
+    a = _run(X, logits, W, R, T, H, F, E, topk, cap, staged=False)
+    b = _run(X, logits, W, R, T, H, F, E, topk, cap, staged=False)
     for d in range(R):
         assert torch.equal(a["src"][d], b["src"][d])
         assert torch.equal(a["recv_y"][d].view(torch.int16), b["recv_y"][d].view(torch.int16))
@@ -140,10 +144,12 @@ def test_moe_invalid_arguments():
     assert e.value.status == fcc.FCC_ERR_INVALID
 
 
-def test_moe_full_workload_sampled():
+@pytest.mark.parametrize("staged", [True, False])
+def test_moe_full_workload_sampled(staged):
+    """The benchmark's launch: rows gathered from the source tokens (staged=False)."""
     w = synth.WORKLOADS["moe_r8_t4096_h4096_e64_f1408"]
     X, logits, W = synth.moe_inputs(w.R, w.T, w.H, w.E, w.F, std_x=w.std_a, std_w=w.std_b,
                                     seed=0)
     cap = 2 * w.T * w.topk  # twice the mean load per rank
-    out = _run(X, logits, W, w.R, w.T, w.H, w.F, w.E, w.topk, cap)
+    out = _run(X, logits, W, w.R, w.T, w.H, w.F, w.E, w.topk, cap, staged=staged)
     _check(X, logits, W, w.R, w.T, w.H, w.F, w.E, w.topk, cap, out, sample=48)
