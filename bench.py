@@ -366,12 +366,18 @@ def other_ops(fcc, torch, np, synth, dev, stream, dA_rs, dB_rs, pk):
                                   gate, counts, send, src, 0, 0, None, stream)
 
     t = time_calls(moe, 10, 3, stream)
+    og = fcc.make_opts(algo=fcc.FCC_ALGO_FUSED)
+    tg = time_calls(lambda: fcc.fcc_moe_dispatch_gemm(R, dX, dL, dW, T, H, F, E, topk, None,
+                                                      recv_y, cap, idx, gate, counts, send,
+                                                      src, 0, 0, og, stream), 5, 2, stream)
     # algorithmic bytes: X once, logits once, W once, Y once (indices negligible)
     byts = R * T * H * 2 + R * T * E * 4 + E * H * F * 2 + R * T * topk * F * 2
-    res = {"fused": {"ms": t, "TFLOP/s": w.flops() / (t * 1e-3) / 1e12},
+    res = {"fused": {"ms": t, "TFLOP/s": w.flops() / (t * 1e-3) / 1e12,
+                     "path": "route, dispatch copy into workspace, grouped GEMM"},
+           "gather_in_gemm": {"ms": tg, "TFLOP/s": w.flops() / (tg * 1e-3) / 1e12,
+                              "path": "no staged rows: cp.async gather in the GEMM producer"},
            "roofline_frac": (w.flops() / (t * 1e-3) / 1e12) / tc,
-           "algorithmic_bytes": byts,
-           "note": "rows gathered from the source tokens by the grouped GEMM (no staged copy)"}
+           "algorithmic_bytes": byts}
     ops[w.name] = res
     del dX, dL, dW, recv_y
     st = fcc.fcc_stream_status(stream)

@@ -296,13 +296,19 @@ __global__ void __launch_bounds__(256) copy_kernel(const MoeArgs a) {
 struct MoePlan {
   int chunks_per_rank = 0;
   int nchunks = 0;
+  size_t off_stage = 0;  // staged rows when the caller passes no recv_x ([R][cap][H] bf16)
   size_t off_chunk_counts = 0, off_chunk_off = 0, off_base = 0, off_rows = 0, off_tiles = 0,
          off_row_of = 0, total = 0;
 };
 
 size_t up256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
-MoePlan moe_plan(int R, int64_t T, int E, int topk) {
+// Gather inside the expert GEMM (no staged rows) only when asked for with
+// FCC_ALGO_FUSED; otherwise the rows are staged (in recv_x, or in workspace).
+bool moe_gathers(const fcc_opts* o) { return o != nullptr && o->algo == FCC_ALGO_FUSED; }
+
+MoePlan moe_plan(int R, int64_t T, int E, int topk, int64_t H = 0, int64_t cap = 0,
+                 bool stage_in_workspace = false) {
   MoePlan p;
   p.chunks_per_rank = static_cast<int>((T + kChunkTok - 1) / kChunkTok);
   p.nchunks = R * p.chunks_per_rank;
@@ -319,6 +325,8 @@ MoePlan moe_plan(int R, int64_t T, int E, int topk) {
   off += up256(static_cast<size_t>(E + 1) * 4);
   p.off_row_of = off;
   off += up256(static_cast<size_t>(R) * T * topk * 4);
+  p.off_stage = off;
+  if (stage_in_workspace) off += up256(static_cast<size_t>(R) * cap * H * 2);
   p.total = off;
   return p;
 }
@@ -375,7 +383,8 @@ size_t fcc_moe_workspace_size(int R, int64_t T, int64_t H, int64_t F, int E, int
   (void)opts;
   if (R < 1 || R > FCC_MAX_RANKS || T < 1 || E < 1 || E > FCC_MAX_EXPERTS || topk < 1)
     return 0;
-  return moe_plan(R, T, E, topk).total;
+  // Upper bound: includes room to stage the rows in case recv_x is NULL.
+  return moe_plan(R, T, E, topk, H, cap, !moe_gathers(opts)).total;
 }
 
 fcc_status fcc_moe_dispatch_gemm(int R, const void* const* X, const float* const* logits,
@@ -389,7 +398,9 @@ fcc_status fcc_moe_dispatch_gemm(int R, const void* const* X, const float* const
   fcc_status s = check_moe(R, X, logits, W, T, H, F, E, topk, recv_x, recv_y, cap, topk_idx,
                            topk_gate, expert_counts, send_counts, recv_src, in, out_dtype, opts);
   if (s != FCC_OK) return s;
-  const MoePlan plan = moe_plan(R, T, E, topk);
+  const bool gather = moe_gathers(opts);
+  const bool stage_ws = !gather && recv_x == nullptr;
+  const MoePlan plan = moe_plan(R, T, E, topk, H, cap, stage_ws);
   void* ws = nullptr;
   int* status = nullptr;
   int sms = 0;
@@ -406,7 +417,11 @@ fcc_status fcc_moe_dispatch_gemm(int R, const void* const* X, const float* const
     a.logits[r] = logits[r];
     a.idx[r] = topk_idx[r];
     a.gate[r] = topk_gate[r];
-    a.recv_x[r] = recv_x != nullptr ? recv_x[r] : nullptr;
+    a.recv_x[r] = recv_x != nullptr
+                      ? recv_x[r]
+                      : (stage_ws ? static_cast<char*>(ws) + plan.off_stage +
+                                        static_cast<size_t>(r) * cap * H * 2
+                                  : nullptr);
     a.recv_src[r] = recv_src[r];
   }
   a.R = R;
@@ -432,9 +447,8 @@ fcc_status fcc_moe_dispatch_gemm(int R, const void* const* X, const float* const
 
   GroupedParams g;
   std::memset(&g, 0, sizeof(g));
-  const bool gather = (recv_x == nullptr);
   for (int d = 0; d < R; ++d) {
-    if (!gather && (s = internal_make_map(&g.mapA[d], recv_x[d], cap, H, kBM)) != FCC_OK)
+    if (!gather && (s = internal_make_map(&g.mapA[d], a.recv_x[d], cap, H, kBM)) != FCC_OK)
       return s;
     g.X[d] = X[d];
     g.recv_src[d] = recv_src[d];

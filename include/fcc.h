@@ -178,8 +178,9 @@ fcc_status fcc_ag_gemm(int R, const void *const *X_shard, const void *const *B,
  *   GEMM:     recv_y[d][row] = X[s][t] @ W[e]  ([F] per row, dtype out_dtype).
  * X[s]: [T,H] bf16; logits[s]: [T,E] f32, finite; W[e]: [H,F] bf16 (E
  * pointers); recv_x: NULL, or per rank [cap,H] bf16 to receive the
- * dispatched rows (with NULL the expert GEMM reads each row straight from its
- * source token and no staged copy is written); recv_y[d]: [cap,F];
+ * dispatched rows (with NULL they are staged in workspace, or, with
+ * opts->algo == FCC_ALGO_FUSED, not staged at all: the expert GEMM then reads
+ * each row straight from its source token); recv_y[d]: [cap,F];
  * recv_src[d]: [cap] int32; topk_idx[s]: [T,topk] int32; topk_gate[s]:
  * [T,topk] f32; expert_counts: [E] int32 device; send_counts: [R*R] int32
  * device.  Rows of a receive buffer past the received count are left

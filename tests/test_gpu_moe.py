@@ -28,6 +28,8 @@ GATE_RTOL = 5e-6
 
 def _run(X, logits, W, R, T, H, F, E, topk, cap, out_dtype=fcc.FCC_BF16, opts=None,
          staged=True):
+    """staged: rows into caller buffers; False: recv_x NULL (library workspace, or
+    no staged copy at all with opts.algo = FCC_ALGO_FUSED)."""
     dX = [dev_bf16(x) for x in X]
     dL = [dev_f32(l) for l in logits]
     dW = [dev_bf16(w) for w in W]
@@ -87,12 +89,13 @@ def _check(X, logits, W, R, T, H, F, E, topk, cap, out, sample=None, seed=0):
     (1, 500, 128, 256, 8, 2),     # one rank
 ])
 @pytest.mark.parametrize("pair", [1, 2])
-@pytest.mark.parametrize("staged", [True, False])
-def test_moe_small(R, T, H, F, E, topk, pair, staged):
+@pytest.mark.parametrize("path", ["staged", "workspace", "gather"])
+def test_moe_small(R, T, H, F, E, topk, pair, path):
     X, logits, W = synth.moe_inputs(R, T, H, E, F, seed=R * 100 + T)
     cap = R * T * topk
-    out = _run(X, logits, W, R, T, H, F, E, topk, cap, opts=fcc.make_opts(cta_pair=pair),
-               staged=staged)
+    algo = fcc.FCC_ALGO_FUSED if path == "gather" else fcc.FCC_ALGO_AUTO
+    out = _run(X, logits, W, R, T, H, F, E, topk, cap,
+               opts=fcc.make_opts(cta_pair=pair, algo=algo), staged=(path == "staged"))
     _check(X, logits, W, R, T, H, F, E, topk, cap, out)
 
 
@@ -103,7 +106,8 @@ def test_moe_ties_and_f32_output():
     logits[0][1, [2, 6]] = 9.0             # tie for first: 2 then 6
     logits[1][5, [7, 3, 5]] = [4.0, 4.0, 4.0]
     cap = R * T * topk
-    out = _run(X, logits, W, R, T, H, F, E, topk, cap, fcc.FCC_F32, staged=False)
+    out = _run(X, logits, W, R, T, H, F, E, topk, cap, fcc.FCC_F32, staged=False,
+               opts=fcc.make_opts(algo=fcc.FCC_ALGO_FUSED))
     _check(X, logits, W, R, T, H, F, E, topk, cap, out)
     idx0 = out["idx"][0].cpu().numpy()
     assert list(idx0[0]) == [0, 1] and list(idx0[1]) == [2, 6]
@@ -113,8 +117,9 @@ def test_moe_repeatable():
     R, T, H, F, E, topk = 4, 256, 128, 128, 16, 2
     X, logits, W = synth.moe_inputs(R, T, H, E, F, seed=6)
     cap = R * T * topk
-    a = _run(X, logits, W, R, T, H, F, E, topk, cap, staged=False)
-    b = _run(X, logits, W, R, T, H, F, E, topk, cap, staged=False)
+    o = fcc.make_opts(algo=fcc.FCC_ALGO_FUSED)
+    a = _run(X, logits, W, R, T, H, F, E, topk, cap, staged=False, opts=o)
+    b = _run(X, logits, W, R, T, H, F, E, topk, cap, staged=False, opts=o)
     for d in range(R):
         assert torch.equal(a["src"][d], b["src"][d])
         assert torch.equal(a["recv_y"][d].view(torch.int16), b["recv_y"][d].view(torch.int16))
@@ -144,12 +149,14 @@ def test_moe_invalid_arguments():
     assert e.value.status == fcc.FCC_ERR_INVALID
 
 
-@pytest.mark.parametrize("staged", [True, False])
-def test_moe_full_workload_sampled(staged):
-    """The benchmark's launch: rows gathered from the source tokens (staged=False)."""
+@pytest.mark.parametrize("path", ["workspace", "gather"])
+def test_moe_full_workload_sampled(path):
+    """The benchmark's launches: rows staged in library workspace, and gathered."""
     w = synth.WORKLOADS["moe_r8_t4096_h4096_e64_f1408"]
     X, logits, W = synth.moe_inputs(w.R, w.T, w.H, w.E, w.F, std_x=w.std_a, std_w=w.std_b,
                                     seed=0)
     cap = 2 * w.T * w.topk  # twice the mean load per rank
-    out = _run(X, logits, W, w.R, w.T, w.H, w.F, w.E, w.topk, cap, staged=staged)
+    algo = fcc.FCC_ALGO_FUSED if path == "gather" else fcc.FCC_ALGO_AUTO
+    out = _run(X, logits, W, w.R, w.T, w.H, w.F, w.E, w.topk, cap, staged=False,
+               opts=fcc.make_opts(algo=algo))
     _check(X, logits, W, w.R, w.T, w.H, w.F, w.E, w.topk, cap, out, sample=48)
