@@ -446,17 +446,17 @@ fcc_status rank_sum_call(int R, const void* const* A, const void* const* B, void
 
 // ---------------------------------------------------------------- GEMV
 struct GemvPlan {
-  int slabs = 0;
+  int groups = 0, splits = 0;
   size_t partial_bytes = 0;
   size_t ticket_bytes = 0;
   size_t total() const { return align_up(partial_bytes) + align_up(ticket_bytes); }
 };
 
-GemvPlan gemv_plan(int64_t N, int sms) {
+GemvPlan gemv_plan(int R, int64_t M, int64_t N, int64_t K, int sms, const fcc_opts* o) {
   GemvPlan g;
-  g.slabs = static_cast<int>(cdiv(N, 128));
-  g.partial_bytes = static_cast<size_t>(g.slabs + sms) * 16 * 128 * 4;
-  g.ticket_bytes = static_cast<size_t>(g.slabs) * 4;
+  gemv_shape(N, R, K, sms, o != nullptr ? o->max_ctas : 0, &g.groups, &g.splits);
+  g.partial_bytes = gemv_partial_bytes(g.groups, g.splits, M);
+  g.ticket_bytes = static_cast<size_t>(g.groups) * 4;
   return g;
 }
 
@@ -517,7 +517,7 @@ fcc_status fcc_gemv_ar(int R, const void* const* A, const void* const* B, void* 
   }
   DeviceState* d = nullptr;
   if ((s = device_state(&d)) != FCC_OK) return s;
-  const GemvPlan g = gemv_plan(N, d->sms);
+  const GemvPlan g = gemv_plan(R, M, N, K, d->sms, opts);
   void* ws = nullptr;
   if ((s = get_workspace(d, opts, g.total(), &ws)) != FCC_OK) return s;
   GemvParams p;
@@ -532,16 +532,15 @@ fcc_status fcc_gemv_ar(int R, const void* const* A, const void* const* B, void* 
   p.N = static_cast<int>(N);
   p.K = static_cast<int>(K);
   p.kb_per_rank = static_cast<int>(cdiv(K, kBK));
-  p.slabs = g.slabs;
-  p.units = static_cast<long long>(g.slabs) * R * p.kb_per_rank;
+  p.groups = g.groups;
+  p.splits = g.splits;
   p.out_f32 = out_f32;
   p.partials = static_cast<float*>(ws);
   p.tickets = reinterpret_cast<int*>(static_cast<char*>(ws) + align_up(g.partial_bytes));
   p.status = d->status;
   p.timeout_ns = timeout_of(opts);
   if (cudaMemsetAsync(p.tickets, 0, g.ticket_bytes, st) != cudaSuccess) return FCC_ERR_CUDA;
-  const int grid = grid_for(d, opts, p.units);
-  if (launch_gemv(p, grid, st) != cudaSuccess) return FCC_ERR_CUDA;
+  if (launch_gemv(p, g.groups * g.splits, st) != cudaSuccess) return FCC_ERR_CUDA;
   g_launches.fetch_add(1);
   return FCC_OK;
 }
@@ -633,7 +632,7 @@ size_t fcc_workspace_size(fcc_op op, int R, int64_t M, int64_t N, int64_t K,
       if (cudaGetDevice(&dev) != cudaSuccess ||
           cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         sms = 256;
-      return gemv_plan(N, sms).total();
+      return gemv_plan(R, M, N, K, sms, opts).total();
     }
     case FCC_OP_AG_GEMM:
       return algo_of(opts) == FCC_ALGO_FUSED ? 0 : static_cast<size_t>(M) * K * 2;

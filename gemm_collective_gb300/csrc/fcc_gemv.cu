@@ -3,19 +3,23 @@
 // Y = sum_r A_r @ B_r with A_r [M <= 16, K] (tokens) and B_r [K, N]; Y is
 // written to every rank's buffer (SC24 paper, abstract: the GEMV + AllReduce
 // operator for Transformers).  The work is a stream of B bytes from HBM, so
-// the kernel is built to keep HBM busy: every SM runs one persistent CTA that
-// streams its contiguous share of (column slab, rank, k block) units through a
-// 10-stage TMA ring.  The multiply runs on the tensor cores with the roles
-// swapped (D^T = B^T A^T): the 128-column B slab is the M=128 operand
-// (MN-major in shared memory), the tokens padded to 16 rows by TMA's
-// out-of-bounds zero fill are the N=16 operand, and the f32 accumulator sits
-// in TMEM, one lane per output column.
+// the kernel is shaped for HBM: the grid is (column groups of 1024) x (splits
+// of the rank-and-K range K' = R*K), one persistent CTA per SM.  A CTA walks
+// its K' range in 64-row blocks and, for each, reads the block's 1024 columns
+// as four 32 KiB stages of 64 rows x 256 columns, so each row is read as 2 KiB
+// contiguous and the CTAs of a group read neighbouring rows at the same time.
 //
-// Cross-CTA sum: a slab's K' = R*K range is split over consecutive CTAs
-// (stream-K).  Each CTA writes its f32 partial for the slab to its own
-// workspace slot and takes a ticket; the last to arrive adds the partials in
-// CTA order (a fixed order, so the result is repeatable) and stores the sum to
-// all R output buffers.  Nothing waits on another CTA.
+// The multiply runs on the tensor cores with the roles swapped (D^T = B^T
+// A^T): each 128-column half of a stage is an M=128 operand (MN-major in
+// shared memory), the tokens padded to 16 rows by TMA's out-of-bounds zero
+// fill are the N=16 operand, and the group's eight f32 accumulators (one per
+// 128 columns) stay in TMEM for the whole range, one lane per column.
+//
+// Cross-CTA sum: each CTA writes its f32 partial for the group to its own
+// workspace slot and takes the group's ticket; the last to arrive adds the
+// group's partials in split order (a fixed order, so the result is
+// repeatable) and stores the sum to all R output buffers.  No CTA waits on
+// another.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -27,57 +31,53 @@
 namespace fcc {
 namespace {
 
-constexpr int kSlab = 128;                      // output columns per slab (UMMA M)
+constexpr int kGroupCols = 1024;                // columns per CTA group
+constexpr int kHalf = 128;                      // columns per UMMA (M = 128)
+constexpr int kStageCols = 256;                 // columns per pipeline stage
 constexpr int kTok = 16;                        // padded tokens (UMMA N)
-constexpr int kStages = 10;
+constexpr int kStages = 6;
 constexpr uint32_t kBBox = kBK * 64 * 2;        // [64 k][64 n] bf16 = 8 KiB
-constexpr uint32_t kBStage = 2 * kBBox;         // 16 KiB: [64 k][128 n]
+constexpr uint32_t kBStage = 4 * kBBox;         // 32 KiB: [64 k][256 n]
 constexpr uint32_t kAStage = kTok * kBK * 2;    // 2 KiB: [16 tokens][64 k]
 constexpr uint32_t kStageBytes = kBStage + kAStage;
-constexpr uint32_t kTmemCols = 32;              // 2 accumulators x 16 columns
-constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(kSlab, kTok, /*a_mn=*/true, /*b_mn=*/false);
+constexpr uint32_t kTmemCols = 128;             // 8 accumulators x 16 columns
+constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(kHalf, kTok, /*a_mn=*/true, /*b_mn=*/false);
 constexpr uint64_t kDrainNs = 50ull * 1000 * 1000;
-constexpr int kSmemBytes = 1024 + kStages * kStageBytes + (2 * kStages + 5) * 8 + 16;
-
-__device__ __forceinline__ int owner_of(long long u, long long U, int G) {
-  // CTA b covers units [floor(b*U/G), floor((b+1)*U/G)); the owner of u is the
-  // largest b whose range starts at or before u.
-  return static_cast<int>(((u + 1) * G - 1) / U);
-}
+constexpr int kSmemBytes = 1024 + kStages * kStageBytes + (2 * kStages + 4) * 8 + 16;
 
 __global__ void __launch_bounds__(kGemmThreads, 1) gemv_ar_kernel(const __grid_constant__ GemvParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  uint8_t* sB = smem;                          // kStages x 16 KiB
+  uint8_t* sB = smem;                          // kStages x 32 KiB
   uint8_t* sA = smem + kStages * kBStage;      // kStages x 2 KiB
   uint64_t* bars = reinterpret_cast<uint64_t*>(sA + kStages * kAStage);
   uint64_t* full = bars;
   uint64_t* empty = bars + kStages;
   uint64_t* tfull = bars + 2 * kStages;
-  uint64_t* tempty = tfull + 2;
-  uint64_t* mma_done = tempty + 2;
+  uint64_t* mma_done = tfull + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* bcast = reinterpret_cast<volatile int*>(tmem_slot + 2);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int G = gridDim.x;
-  const long long U = p.units;
-  const long long u0 = U * blockIdx.x / G;
-  const long long u1 = U * (blockIdx.x + 1) / G;
-  const int per_slab = p.R * p.kb_per_rank;
+  const int g = blockIdx.x / p.splits;              // column group
+  const int split = blockIdx.x - g * p.splits;      // part of the K' range
+  const int kbt = p.R * p.kb_per_rank;              // 64-row blocks of K'
+  const int kb0 = static_cast<int>(static_cast<long long>(kbt) * split / p.splits);
+  const int kb1 = static_cast<int>(static_cast<long long>(kbt) * (split + 1) / p.splits);
+  const int col0 = g * kGroupCols;
+  const int ncols = min(kGroupCols, p.N - col0);
+  const int nstage_cols = (ncols + kStageCols - 1) / kStageCols;  // stages per 64-row block
+  const int nslabs = (ncols + kHalf - 1) / kHalf;                 // accumulators in use
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(&full[s], 1);
       ptx::mbar_init(&empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      ptx::mbar_init(&tfull[b], 1);
-      ptx::mbar_init(&tempty[b], 4);
-    }
+    ptx::mbar_init(tfull, 1);
     ptx::mbar_init(mma_done, 1);
     *abort_flag = 0;
     ptx::fence_mbar_init();
@@ -100,26 +100,32 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemv_ar_kernel(const __grid_c
 
   if (warp == 0) {
     if (lane == 0) {
-      const uint64_t keep = ptx::policy_evict_last();    // A rows are re-read by every slab
+      const uint64_t keep = ptx::policy_evict_last();    // A rows are re-read by every group
       const uint64_t stream = ptx::policy_evict_first(); // B is read exactly once
       uint32_t stage = 0, phase = 0, issued = 0, last_parity = 0;
-      for (long long u = u0; u < u1; ++u) {
-        const int slab = static_cast<int>(u / per_slab);
-        const int rem = static_cast<int>(u - static_cast<long long>(slab) * per_slab);
-        const int r = rem / p.kb_per_rank;
-        const int kb = rem - r * p.kb_per_rank;
-        if (!W.wait(&empty[stage], phase ^ 1u)) break;
-        ptx::mbar_arrive_expect_tx(&full[stage], kStageBytes);
-        uint8_t* b_dst = sB + stage * kBStage;
-        ptx::tma_load_2d_hint(b_dst, &p.mapB[r], &full[stage], slab * kSlab, kb * kBK, stream);
-        ptx::tma_load_2d_hint(b_dst + kBBox, &p.mapB[r], &full[stage], slab * kSlab + 64,
-                              kb * kBK, stream);
-        ptx::tma_load_2d_hint(sA + stage * kAStage, &p.mapA[r], &full[stage], kb * kBK, 0, keep);
-        issued |= 1u << stage;
-        last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
-        if (++stage == kStages) {
-          stage = 0;
-          phase ^= 1u;
+      bool ok = true;
+      for (int kbi = kb0; kbi < kb1 && ok; ++kbi) {
+        const int r = kbi / p.kb_per_rank;
+        const int kb = kbi - r * p.kb_per_rank;
+        for (int sc = 0; sc < nstage_cols; ++sc) {
+          if (!W.wait(&empty[stage], phase ^ 1u)) {
+            ok = false;
+            break;
+          }
+          ptx::mbar_arrive_expect_tx(&full[stage], kStageBytes);
+          uint8_t* b_dst = sB + stage * kBStage;
+#pragma unroll
+          for (int i = 0; i < kStageCols / 64; ++i)
+            ptx::tma_load_2d_hint(b_dst + i * kBBox, &p.mapB[r], &full[stage],
+                                  col0 + sc * kStageCols + 64 * i, kb * kBK, stream);
+          ptx::tma_load_2d_hint(sA + stage * kAStage, &p.mapA[r], &full[stage], kb * kBK, 0,
+                                keep);
+          issued |= 1u << stage;
+          last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
         }
       }
       if (*abort_flag) {
@@ -129,16 +135,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemv_ar_kernel(const __grid_c
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+      uint32_t stage = 0, phase = 0;
       bool any = false, ok = true;
-      long long u = u0;
-      while (u < u1 && ok) {
-        const int slab = static_cast<int>(u / per_slab);
-        const long long seg_end = min(u1, static_cast<long long>(slab + 1) * per_slab);
-        if (!W.wait(&tempty[acc], acc_phase ^ 1u)) break;
-        ptx::tc_fence_after();
-        const uint32_t d_tmem = tmem_base + acc * kTok;
-        for (long long v = u; v < seg_end; ++v) {
+      for (int kbi = kb0; kbi < kb1 && ok; ++kbi) {
+        for (int sc = 0; sc < nstage_cols; ++sc) {
           if (!W.wait(&full[stage], phase)) {
             ok = false;
             break;
@@ -148,11 +148,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemv_ar_kernel(const __grid_c
           const uint32_t a_addr = ptx::smem_addr(sA + stage * kAStage);
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk) {
-            // UMMA A = B^T slab: MN-major, 16 k-rows per step (2 KiB); n atoms 8 KiB apart.
-            const uint64_t ad = ptx::smem_desc_sw128(b_addr + kk * 2048, kBBox, 1024);
             // UMMA B = tokens: K-major rows of 128 B, advance 32 B per 16 k.
             const uint64_t bd = ptx::smem_desc_sw128(a_addr + kk * 32, 16, 1024);
-            ptx::mma_f16(d_tmem, ad, bd, kIdesc, (v > u || kk > 0) ? 1u : 0u);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              // UMMA A = half h of the stage's B^T columns: MN-major, 16 k-rows
+              // per step (2 KiB), its two 64-column atoms 8 KiB apart.
+              const uint64_t ad =
+                  ptx::smem_desc_sw128(b_addr + h * 2 * kBBox + kk * 2048, kBBox, 1024);
+              const uint32_t d = tmem_base + (sc * 2 + h) * kTok;
+              ptx::mma_f16(d, ad, bd, kIdesc, (kbi > kb0 || kk > 0) ? 1u : 0u);
+            }
           }
           ptx::mma_commit(&empty[stage]);
           any = true;
@@ -161,80 +167,74 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemv_ar_kernel(const __grid_c
             phase ^= 1u;
           }
         }
-        if (!ok) break;
-        ptx::mma_commit(&tfull[acc]);
-        acc ^= 1u;
-        if (acc == 0) acc_phase ^= 1u;
-        u = seg_end;
       }
+      if (ok && any) ptx::mma_commit(tfull);
       if (any) {
         ptx::mma_commit(mma_done);
         W.drain(mma_done, 0, kDrainNs);
       }
     }
   } else {
-    // Epilogue: one thread per output column of the slab.
+    // Epilogue: one thread per column of each 128-column slab of the group.
     const int q = warp & 3;
     const int n_local = q * 32 + lane;
     const int ep_tid = threadIdx.x - 64;
-    uint32_t acc = 0, acc_phase = 0;
-    long long u = u0;
-    while (u < u1) {
-      const int slab = static_cast<int>(u / per_slab);
-      const long long seg_end = min(u1, static_cast<long long>(slab + 1) * per_slab);
-      const bool failed = !W.wait(&tfull[acc], acc_phase);
-      if (ptx::named_barrier_or(1, 128, failed)) break;  // the epilogue warps stop together
+    const bool failed = (kb1 <= kb0) || !W.wait(tfull, 0);
+    if (!ptx::named_barrier_or(1, 128, failed)) {  // the epilogue warps stop together
       ptx::tc_fence_after();
-      uint32_t v[8], w[8];
-      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kTok;
-      ptx::tmem_ld_32x32b_x8(taddr, v);
-      ptx::tmem_ld_32x32b_x8(taddr + 8, w);
-      ptx::tmem_ld_wait();
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&tempty[acc]);
-
-      const int slot = blockIdx.x + slab;
-      float* part = p.partials + static_cast<long long>(slot) * kTok * kSlab;
+      float* part = p.partials + static_cast<long long>(blockIdx.x) * p.M * kGroupCols;
+      for (int s = 0; s < nslabs; ++s) {
+        uint32_t v[16];
+        ptx::tmem_ld_32x32b_x16(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + s * kTok, v);
+        ptx::tmem_ld_wait();
 #pragma unroll
-      for (int t = 0; t < 8; ++t)
-        if (t < p.M) part[t * kSlab + n_local] = __uint_as_float(v[t]);
-#pragma unroll
-      for (int t = 0; t < 8; ++t)
-        if (t + 8 < p.M) part[(t + 8) * kSlab + n_local] = __uint_as_float(w[t]);
+        for (int t = 0; t < kTok; ++t)
+          if (t < p.M) part[t * kGroupCols + s * kHalf + n_local] = __uint_as_float(v[t]);
+      }
       __threadfence();
       ptx::named_barrier_sync(1, 128);
-      const int first = owner_of(static_cast<long long>(slab) * per_slab, U, G);
-      const int last = owner_of(static_cast<long long>(slab + 1) * per_slab - 1, U, G);
       if (ep_tid == 0) {
-        const int prev = atomicAdd(&p.tickets[slab], 1);
-        const int is_last = (prev == last - first) ? 1 : 0;
-        if (is_last) p.tickets[slab] = 0;
+        const int prev = atomicAdd(&p.tickets[g], 1);
+        const int is_last = (prev == p.splits - 1) ? 1 : 0;
+        if (is_last) p.tickets[g] = 0;
         *bcast = is_last;
       }
       ptx::named_barrier_sync(1, 128);
       if (*bcast) {
+        // Last of the group: sum the splits' partials in split order; each
+        // thread handles 8 consecutive columns (two 16-byte loads per partial).
         __threadfence();
-        const int col = slab * kSlab + n_local;
-        if (col < p.N) {
+        const int c = ep_tid * 8;
+        if (c < ncols) {
+          const float* base = p.partials + static_cast<long long>(g) * p.splits * p.M * kGroupCols;
           for (int t = 0; t < p.M; ++t) {
-            float s = 0.f;
-            for (int c = first; c <= last; ++c)
-              s += __ldcg(p.partials + (static_cast<long long>(c + slab) * kTok + t) * kSlab + n_local);
+            float s8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            for (int sp = 0; sp < p.splits; ++sp) {
+              const float4* src = reinterpret_cast<const float4*>(
+                  base + (static_cast<long long>(sp) * p.M + t) * kGroupCols + c);
+              const float4 x = __ldcg(src);
+              const float4 y = __ldcg(src + 1);
+              s8[0] += x.x; s8[1] += x.y; s8[2] += x.z; s8[3] += x.w;
+              s8[4] += y.x; s8[5] += y.y; s8[6] += y.z; s8[7] += y.w;
+            }
+            const long long o = static_cast<long long>(t) * p.N + col0 + c;
             for (int r = 0; r < p.R; ++r) {
               if (p.out_f32) {
-                reinterpret_cast<float*>(p.out[r])[static_cast<long long>(t) * p.N + col] = s;
+                float4* d = reinterpret_cast<float4*>(static_cast<float*>(p.out[r]) + o);
+                d[0] = make_float4(s8[0], s8[1], s8[2], s8[3]);
+                d[1] = make_float4(s8[4], s8[5], s8[6], s8[7]);
               } else {
-                reinterpret_cast<uint16_t*>(p.out[r])[static_cast<long long>(t) * p.N + col] =
-                    static_cast<uint16_t>(ptx::pack_bf16x2(s, 0.f) & 0xFFFFu);
+                uint4 w;
+                w.x = ptx::pack_bf16x2(s8[0], s8[1]);
+                w.y = ptx::pack_bf16x2(s8[2], s8[3]);
+                w.z = ptx::pack_bf16x2(s8[4], s8[5]);
+                w.w = ptx::pack_bf16x2(s8[6], s8[7]);
+                *reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out[r]) + o) = w;
               }
             }
           }
         }
       }
-      acc ^= 1u;
-      if (acc == 0) acc_phase ^= 1u;
-      u = seg_end;
     }
   }
 
@@ -259,11 +259,29 @@ cudaError_t launch_gemv(const GemvParams& p, int grid, cudaStream_t st) {
   return cudaGetLastError();
 }
 
+// Grid shape: groups = ceil(N / 1024) column groups, `splits` CTAs per group
+// (about one CTA per SM in total, at most one per 64-row block of K').
+void gemv_shape(int64_t N, int R, int64_t K, int sms, int max_ctas, int* groups, int* splits) {
+  const int g = static_cast<int>((N + kGroupCols - 1) / kGroupCols);
+  const long long kbt = static_cast<long long>(R) * ((K + kBK - 1) / kBK);
+  int ctas = sms;
+  if (max_ctas > 0 && max_ctas < ctas) ctas = max_ctas;
+  long long s = ctas / g;
+  if (s < 1) s = 1;
+  if (s > kbt) s = kbt;
+  *groups = g;
+  *splits = static_cast<int>(s);
+}
+
+size_t gemv_partial_bytes(int groups, int splits, int64_t M) {
+  return static_cast<size_t>(groups) * splits * M * kGroupCols * 4;
+}
+
 }  // namespace fcc
 
 // ---------------------------------------------------------------------------
 // fcc_gemv_ar_static: the same GEMV + AllReduce kernel with its scratch (the
-// per-CTA partial sums and the per-slab arrival tickets) in a fixed device
+// per-CTA partial sums and the per-group arrival tickets) in a fixed device
 // array of this file instead of caller or pool memory, for callers that cannot
 // allocate device memory.  The array lives on every GPU that loads the library
 // until the process exits.
@@ -273,8 +291,7 @@ namespace fcc {
 namespace {
 
 constexpr size_t kStaticScratchBytes = size_t(4) << 20;  // 4 MiB in total
-constexpr size_t kStaticTicketBytes = 4096;              // tickets: up to 1024 slabs
-constexpr size_t kSlotBytes = size_t(kTok) * kSlab * 4;  // one partial: 16 x 128 f32
+constexpr size_t kStaticTicketBytes = 4096;              // tickets: up to 1024 groups
 
 __device__ __align__(256) unsigned char g_gemv_static_scratch[kStaticScratchBytes];
 
@@ -335,17 +352,16 @@ extern "C" fcc_status fcc_gemv_ar_static(int R, const void* const* A, const void
   int* status = nullptr;
   if ((s = light_status_word(&status)) != FCC_OK) return s;
 
-  const int slabs = static_cast<int>((N + kSlab - 1) / kSlab);
-  const int kb = static_cast<int>((K + kBK - 1) / kBK);
-  const long long units = static_cast<long long>(slabs) * R * kb;
-  int grid = sms;
-  if (opts != nullptr && opts->max_ctas > 0 && opts->max_ctas < grid) grid = opts->max_ctas;
-  if (units < grid) grid = static_cast<int>(units);
-  // Size limit of the static array: tickets for every slab, one partial slot
-  // per (slab, contributing CTA) pair, of which there are at most slabs + grid.
-  if (static_cast<size_t>(slabs) * 4 > kStaticTicketBytes ||
-      static_cast<size_t>(slabs + grid) * kSlotBytes > kStaticScratchBytes - kStaticTicketBytes)
+  int groups = 0, splits = 0;
+  gemv_shape(N, R, K, sms, opts != nullptr ? opts->max_ctas : 0, &groups, &splits);
+  // Size limit of the static array: one ticket per column group, and one
+  // partial (M x 1024 f32 = M x 4 KiB) per CTA; fewer CTAs per group are used
+  // when the default number does not fit.
+  const size_t room = kStaticScratchBytes - kStaticTicketBytes;
+  const size_t per_split = gemv_partial_bytes(groups, 1, M);
+  if (static_cast<size_t>(groups) * 4 > kStaticTicketBytes || per_split > room)
     return FCC_ERR_WORKSPACE;
+  if (static_cast<size_t>(splits) * per_split > room) splits = static_cast<int>(room / per_split);
 
   GemvParams p;
   std::memset(&p, 0, sizeof(p));
@@ -358,9 +374,9 @@ extern "C" fcc_status fcc_gemv_ar_static(int R, const void* const* A, const void
   p.M = static_cast<int>(M);
   p.N = static_cast<int>(N);
   p.K = static_cast<int>(K);
-  p.kb_per_rank = kb;
-  p.slabs = slabs;
-  p.units = units;
+  p.kb_per_rank = static_cast<int>((K + kBK - 1) / kBK);
+  p.groups = groups;
+  p.splits = splits;
   p.out_f32 = out_dtype == FCC_F32 ? 1 : 0;
   p.tickets = reinterpret_cast<int*>(scratch);
   p.partials = reinterpret_cast<float*>(scratch + kStaticTicketBytes);
@@ -370,9 +386,9 @@ extern "C" fcc_status fcc_gemv_ar_static(int R, const void* const* A, const void
                      : 1000ull * 1000 * 1000;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   // The array keeps the previous call's contents: the tickets must start at zero.
-  if (cudaMemsetAsync(p.tickets, 0, static_cast<size_t>(slabs) * 4, st) != cudaSuccess)
+  if (cudaMemsetAsync(p.tickets, 0, static_cast<size_t>(groups) * 4, st) != cudaSuccess)
     return FCC_ERR_CUDA;
-  if (launch_gemv(p, grid, st) != cudaSuccess) return FCC_ERR_CUDA;
+  if (launch_gemv(p, groups * splits, st) != cudaSuccess) return FCC_ERR_CUDA;
   count_launch();
   return FCC_OK;
 }

@@ -52,11 +52,11 @@ struct GemvParams {
   void* out[FCC_MAX_RANKS];
   int R, M, N, K;
   int kb_per_rank;
-  int slabs;            // ceil(N / 128)
-  long long units;      // slabs * R * kb_per_rank
+  int groups;           // column groups of 1024 columns: ceil(N / 1024)
+  int splits;           // CTAs per group (parts of the R*K range); grid = groups * splits
   int out_f32;
-  float* partials;      // [(slabs + grid) slots][16][128]
-  int* tickets;         // [slabs]
+  float* partials;      // [groups * splits][M][1024]
+  int* tickets;         // [groups]
   int* status;
   unsigned long long timeout_ns;
 };
@@ -96,6 +96,9 @@ cudaError_t launch_grouped_gemm(const GroupedParams& p, int cg, int grid, cudaSt
 int gemm_smem_bytes(int cg);
 cudaError_t launch_gemv(const GemvParams& p, int grid, cudaStream_t st);
 int gemv_smem_bytes();
+// GEMV grid shape for N columns and R*K rows over `sms` SMs (max_ctas 0 = no cap).
+void gemv_shape(int64_t N, int R, int64_t K, int sms, int max_ctas, int* groups, int* splits);
+size_t gemv_partial_bytes(int groups, int splits, int64_t M);
 
 // Elementwise helpers (fcc_aux.cu).
 // out_j rows [row_begin,row_end) of shard j = sum_r P[r] rows, P[r] is [M, N] f32.
