@@ -534,12 +534,18 @@ fcc_status fcc_gemv_ar(int R, const void* const* A, const void* const* B, void* 
   p.kb_per_rank = static_cast<int>(cdiv(K, kBK));
   p.groups = g.groups;
   p.splits = g.splits;
+  p.gen = next_gemv_gen();
   p.out_f32 = out_f32;
   p.partials = static_cast<float*>(ws);
   p.tickets = reinterpret_cast<int*>(static_cast<char*>(ws) + align_up(g.partial_bytes));
   p.status = d->status;
   p.timeout_ns = timeout_of(opts);
-  if (cudaMemsetAsync(p.tickets, 0, g.ticket_bytes, st) != cudaSuccess) return FCC_ERR_CUDA;
+  if ((opts == nullptr || opts->workspace == nullptr) && g.groups <= kMaxGemvGroups) {
+    // Library-held tickets: consistent across calls without clearing.
+    if ((s = gemv_internal_tickets(&p.tickets)) != FCC_OK) return s;
+  } else if (cudaMemsetAsync(p.tickets, 0, g.ticket_bytes, st) != cudaSuccess) {
+    return FCC_ERR_CUDA;  // caller workspace may hold anything: start the tickets at zero
+  }
   if (launch_gemv(p, g.groups * g.splits, st) != cudaSuccess) return FCC_ERR_CUDA;
   g_launches.fetch_add(1);
   return FCC_OK;

@@ -23,7 +23,9 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstring>
+#include <mutex>
 
 #include "fcc_internal.h"
 #include "fcc_ptx.cuh"
@@ -194,10 +196,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemv_ar_kernel(const __grid_c
       __threadfence();
       ptx::named_barrier_sync(1, 128);
       if (ep_tid == 0) {
-        const int prev = atomicAdd(&p.tickets[g], 1);
-        const int is_last = (prev == p.splits - 1) ? 1 : 0;
-        if (is_last) p.tickets[g] = 0;
-        *bcast = is_last;
+        // Ticket = (call generation << 8) | arrivals.  A value left by an
+        // earlier call has another generation and counts as zero, so the
+        // tickets need no clearing between calls.  Each CAS that fails means
+        // another CTA of the group got in: at most `splits` retries.
+        unsigned* tk = reinterpret_cast<unsigned*>(p.tickets + g);
+        const unsigned gen = p.gen & 0xFFFFFFu;
+        unsigned cur = *reinterpret_cast<volatile unsigned*>(tk), nv;
+        while (true) {
+          const unsigned cnt = ((cur >> 8) == gen) ? (cur & 0xFFu) : 0u;
+          nv = (gen << 8) | (cnt + 1u);
+          const unsigned prev = atomicCAS(tk, cur, nv);
+          if (prev == cur) break;
+          cur = prev;
+        }
+        *bcast = ((nv & 0xFFu) == static_cast<unsigned>(p.splits)) ? 1 : 0;
       }
       ptx::named_barrier_sync(1, 128);
       if (*bcast) {
@@ -259,6 +272,30 @@ cudaError_t launch_gemv(const GemvParams& p, int grid, cudaStream_t st) {
   return cudaGetLastError();
 }
 
+// Arrival tickets of the default path (no caller workspace): a library array,
+// zero at load, that the generation-stamped tickets keep consistent without
+// clearing (one entry per column group).
+__device__ unsigned g_gemv_tickets[kMaxGemvGroups];
+
+std::atomic<unsigned> g_gemv_gen{0};
+
+unsigned next_gemv_gen() {
+  return (g_gemv_gen.fetch_add(1) % 0xFFFFFEu) + 1u;  // 1 .. 2^24 - 2, never 0
+}
+
+fcc_status gemv_internal_tickets(int** out) {
+  static int* cached[64] = {};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return FCC_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(mu);
+  if (cached[dev] == nullptr &&
+      cudaGetSymbolAddress(reinterpret_cast<void**>(&cached[dev]), g_gemv_tickets) != cudaSuccess)
+    return FCC_ERR_CUDA;
+  *out = cached[dev];
+  return FCC_OK;
+}
+
 // Grid shape: groups = ceil(N / 1024) column groups, `splits` CTAs per group
 // (about one CTA per SM in total, at most one per 64-row block of K').
 void gemv_shape(int64_t N, int R, int64_t K, int sms, int max_ctas, int* groups, int* splits) {
@@ -269,6 +306,7 @@ void gemv_shape(int64_t N, int R, int64_t K, int sms, int max_ctas, int* groups,
   long long s = ctas / g;
   if (s < 1) s = 1;
   if (s > kbt) s = kbt;
+  if (s > 255) s = 255;  // ticket arrivals are counted in 8 bits
   *groups = g;
   *splits = static_cast<int>(s);
 }
@@ -377,6 +415,7 @@ extern "C" fcc_status fcc_gemv_ar_static(int R, const void* const* A, const void
   p.kb_per_rank = static_cast<int>((K + kBK - 1) / kBK);
   p.groups = groups;
   p.splits = splits;
+  p.gen = next_gemv_gen();
   p.out_f32 = out_dtype == FCC_F32 ? 1 : 0;
   p.tickets = reinterpret_cast<int*>(scratch);
   p.partials = reinterpret_cast<float*>(scratch + kStaticTicketBytes);

@@ -56,7 +56,8 @@ struct GemvParams {
   int splits;           // CTAs per group (parts of the R*K range); grid = groups * splits
   int out_f32;
   float* partials;      // [groups * splits][M][1024]
-  int* tickets;         // [groups]
+  int* tickets;         // [groups]: (generation << 8) | arrivals
+  unsigned gen;         // call generation, 1..2^24-1 (never 0: zeroed tickets are "old")
   int* status;
   unsigned long long timeout_ns;
 };
@@ -99,6 +100,10 @@ int gemv_smem_bytes();
 // GEMV grid shape for N columns and R*K rows over `sms` SMs (max_ctas 0 = no cap).
 void gemv_shape(int64_t N, int R, int64_t K, int sms, int max_ctas, int* groups, int* splits);
 size_t gemv_partial_bytes(int groups, int splits, int64_t M);
+constexpr int kMaxGemvGroups = 1024;  // column groups with library-held tickets
+unsigned next_gemv_gen();
+// Device address of the library's GEMV ticket array on the current device.
+fcc_status gemv_internal_tickets(int** out);
 
 // Elementwise helpers (fcc_aux.cu).
 // out_j rows [row_begin,row_end) of shard j = sum_r P[r] rows, P[r] is [M, N] f32.
