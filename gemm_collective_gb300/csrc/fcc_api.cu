@@ -523,7 +523,7 @@ fcc_status fcc_gemv_ar(int R, const void* const* A, const void* const* B, void* 
   GemvParams p;
   std::memset(&p, 0, sizeof(p));
   for (int r = 0; r < R; ++r) {
-    if ((s = make_map(&p.mapA[r], A[r], M, K, 16)) != FCC_OK) return s;
+    if ((s = make_map(&p.mapA[r], A[r], M, K, kBM)) != FCC_OK) return s;
     if ((s = make_map(&p.mapB[r], B[r], K, N, kBK)) != FCC_OK) return s;
     p.out[r] = out[r];
   }

@@ -2,21 +2,20 @@
 //
 // Y = sum_r A_r @ B_r with A_r [M <= 16, K] (tokens) and B_r [K, N]; Y is
 // written to every rank's buffer (SC24 paper, abstract: the GEMV + AllReduce
-// operator for Transformers).  The work is a stream of B bytes from HBM, so
-// the kernel is shaped for HBM: the grid is (column groups of 1024) x (splits
-// of the rank-and-K range K' = R*K), one persistent CTA per SM.  A CTA walks
-// its K' range in 64-row blocks and, for each, reads the block's 1024 columns
-// as four 32 KiB stages of 64 rows x 256 columns, so each row is read as 2 KiB
-// contiguous and the CTAs of a group read neighbouring rows at the same time.
+// operator for Transformers).  The work is a stream of B bytes from HBM.  The
+// grid is (column groups of 512) x (splits of the rank-and-K range K' = R*K),
+// about one persistent CTA per SM; the CTAs of one split read the same rows of
+// B across all groups at the same time, so B is read in whole rows.
 //
-// The multiply runs on the tensor cores with the roles swapped (D^T = B^T
-// A^T): each 128-column half of a stage is an M=128 operand (MN-major in
-// shared memory), the tokens padded to 16 rows by TMA's out-of-bounds zero
-// fill are the N=16 operand, and the group's eight f32 accumulators (one per
-// 128 columns) stay in TMEM for the whole range, one lane per column.
+// Each stage is one 64-row block of 256 columns (32 KiB, four TMA boxes) plus
+// the token rows of that block, loaded as a 128-row TMA box whose rows past M
+// are filled with zeros.  One tcgen05.mma per 16 k (M = 128 token rows, N =
+// 256 columns) accumulates into one of the group's two TMEM accumulators, so
+// the tensor core does little work per byte and keeps up with HBM; TMEM lane t
+// holds token t's row.
 //
-// Cross-CTA sum: each CTA writes its f32 partial for the group to its own
-// workspace slot and takes the group's ticket; the last to arrive adds the
+// Cross-CTA sum: each CTA writes its f32 partial rows for the group to its
+// own workspace slot and takes the group's ticket; the last to arrive adds the
 // group's partials in split order (a fixed order, so the result is
 // repeatable) and stores the sum to all R output buffers.  No CTA waits on
 // another.
@@ -33,17 +32,16 @@
 namespace fcc {
 namespace {
 
-constexpr int kGroupCols = 1024;                // columns per CTA group
-constexpr int kHalf = 128;                      // columns per UMMA (M = 128)
-constexpr int kStageCols = 256;                 // columns per pipeline stage
-constexpr int kTok = 16;                        // padded tokens (UMMA N)
-constexpr int kStages = 6;
+constexpr int kGroupCols = 512;                 // columns per CTA group (two accumulators)
+constexpr int kStageCols = 256;                 // columns per pipeline stage (UMMA N)
+constexpr int kTok = 16;                        // tokens handled (M <= 16)
+constexpr int kStages = 4;
 constexpr uint32_t kBBox = kBK * 64 * 2;        // [64 k][64 n] bf16 = 8 KiB
 constexpr uint32_t kBStage = 4 * kBBox;         // 32 KiB: [64 k][256 n]
-constexpr uint32_t kAStage = kTok * kBK * 2;    // 2 KiB: [16 tokens][64 k]
+constexpr uint32_t kAStage = kBM * kBK * 2;     // 16 KiB: [128 rows][64 k], rows >= M zero
 constexpr uint32_t kStageBytes = kBStage + kAStage;
-constexpr uint32_t kTmemCols = 128;             // 8 accumulators x 16 columns
-constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(kHalf, kTok, /*a_mn=*/true, /*b_mn=*/false);
+constexpr uint32_t kTmemCols = 512;             // 2 accumulators x 256 columns
+constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(kBM, kStageCols, /*a_mn=*/false, /*b_mn=*/true);
 constexpr uint64_t kDrainNs = 50ull * 1000 * 1000;
 constexpr int kSmemBytes = 1024 + kStages * kStageBytes + (2 * kStages + 4) * 8 + 16;
 
@@ -51,9 +49,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemv_ar_kernel(const __grid_c
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  uint8_t* sB = smem;                          // kStages x 32 KiB
-  uint8_t* sA = smem + kStages * kBStage;      // kStages x 2 KiB
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sA + kStages * kAStage);
+  uint8_t* sA = smem;                          // kStages x 16 KiB
+  uint8_t* sB = smem + kStages * kAStage;      // kStages x 32 KiB
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + kStages * kBStage);
   uint64_t* full = bars;
   uint64_t* empty = bars + kStages;
   uint64_t* tfull = bars + 2 * kStages;
@@ -71,8 +69,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemv_ar_kernel(const __grid_c
   const int kb1 = static_cast<int>(static_cast<long long>(kbt) * (split + 1) / p.splits);
   const int col0 = g * kGroupCols;
   const int ncols = min(kGroupCols, p.N - col0);
-  const int nstage_cols = (ncols + kStageCols - 1) / kStageCols;  // stages per 64-row block
-  const int nslabs = (ncols + kHalf - 1) / kHalf;                 // accumulators in use
+  const int nstage_cols = (ncols + kStageCols - 1) / kStageCols;  // accumulators in use
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -102,8 +99,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemv_ar_kernel(const __grid_c
 
   if (warp == 0) {
     if (lane == 0) {
-      const uint64_t keep = ptx::policy_evict_last();    // A rows are re-read by every group
-      const uint64_t stream = ptx::policy_evict_first(); // B is read exactly once
+      const uint64_t keep = ptx::policy_evict_last();    // token rows are re-read by every group
       uint32_t stage = 0, phase = 0, issued = 0, last_parity = 0;
       bool ok = true;
       for (int kbi = kb0; kbi < kb1 && ok; ++kbi) {
@@ -115,13 +111,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemv_ar_kernel(const __grid_c
             break;
           }
           ptx::mbar_arrive_expect_tx(&full[stage], kStageBytes);
+          ptx::tma_load_2d_hint(sA + stage * kAStage, &p.mapA[r], &full[stage], kb * kBK, 0,
+                                keep);
           uint8_t* b_dst = sB + stage * kBStage;
 #pragma unroll
           for (int i = 0; i < kStageCols / 64; ++i)
-            ptx::tma_load_2d_hint(b_dst + i * kBBox, &p.mapB[r], &full[stage],
-                                  col0 + sc * kStageCols + 64 * i, kb * kBK, stream);
-          ptx::tma_load_2d_hint(sA + stage * kAStage, &p.mapA[r], &full[stage], kb * kBK, 0,
-                                keep);
+            ptx::tma_load_2d(b_dst + i * kBBox, &p.mapB[r], &full[stage],
+                             col0 + sc * kStageCols + 64 * i, kb * kBK);
           issued |= 1u << stage;
           last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
           if (++stage == kStages) {
@@ -146,21 +142,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemv_ar_kernel(const __grid_c
             break;
           }
           ptx::tc_fence_after();
-          const uint32_t b_addr = ptx::smem_addr(sB + stage * kBStage);
           const uint32_t a_addr = ptx::smem_addr(sA + stage * kAStage);
+          const uint32_t b_addr = ptx::smem_addr(sB + stage * kBStage);
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk) {
-            // UMMA B = tokens: K-major rows of 128 B, advance 32 B per 16 k.
-            const uint64_t bd = ptx::smem_desc_sw128(a_addr + kk * 32, 16, 1024);
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              // UMMA A = half h of the stage's B^T columns: MN-major, 16 k-rows
-              // per step (2 KiB), its two 64-column atoms 8 KiB apart.
-              const uint64_t ad =
-                  ptx::smem_desc_sw128(b_addr + h * 2 * kBBox + kk * 2048, kBBox, 1024);
-              const uint32_t d = tmem_base + (sc * 2 + h) * kTok;
-              ptx::mma_f16(d, ad, bd, kIdesc, (kbi > kb0 || kk > 0) ? 1u : 0u);
-            }
+            // A = the token rows (zero past M): K-major, 32 B per 16 k.
+            const uint64_t ad = ptx::smem_desc_sw128(a_addr + kk * 32, 16, 1024);
+            // B = 256 columns: MN-major, 16 k-rows per step, 64-column atoms 8 KiB apart.
+            const uint64_t bd = ptx::smem_desc_sw128(b_addr + kk * 2048, kBBox, 1024);
+            ptx::mma_f16(tmem_base + sc * kStageCols, ad, bd, kIdesc,
+                         (kbi > kb0 || kk > 0) ? 1u : 0u);
           }
           ptx::mma_commit(&empty[stage]);
           any = true;
@@ -177,21 +168,31 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemv_ar_kernel(const __grid_c
       }
     }
   } else {
-    // Epilogue: one thread per column of each 128-column slab of the group.
+    // Epilogue.  TMEM lane t holds token t's row, so the warp reading lanes
+    // 0-31 (warp 4) copies the tokens' partial rows; all four warps then take
+    // the group's ticket together and, if last, sum the group.
     const int q = warp & 3;
-    const int n_local = q * 32 + lane;
     const int ep_tid = threadIdx.x - 64;
     const bool failed = (kb1 <= kb0) || !W.wait(tfull, 0);
     if (!ptx::named_barrier_or(1, 128, failed)) {  // the epilogue warps stop together
       ptx::tc_fence_after();
-      float* part = p.partials + static_cast<long long>(blockIdx.x) * p.M * kGroupCols;
-      for (int s = 0; s < nslabs; ++s) {
-        uint32_t v[16];
-        ptx::tmem_ld_32x32b_x16(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + s * kTok, v);
-        ptx::tmem_ld_wait();
+      if (q == 0) {
+        float* part = p.partials + (static_cast<long long>(blockIdx.x) * p.M + lane) * kGroupCols;
+        for (int sc = 0; sc < nstage_cols; ++sc) {
+#pragma unroll 1
+          for (int c = 0; c < kStageCols; c += 32) {
+            uint32_t v[32];
+            ptx::tmem_ld_32x32b_x32(tmem_base + sc * kStageCols + c, v);
+            ptx::tmem_ld_wait();
+            if (lane < p.M) {
+              float4* d = reinterpret_cast<float4*>(part + sc * kStageCols + c);
 #pragma unroll
-        for (int t = 0; t < kTok; ++t)
-          if (t < p.M) part[t * kGroupCols + s * kHalf + n_local] = __uint_as_float(v[t]);
+              for (int i = 0; i < 8; ++i)
+                d[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                   __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
+            }
+          }
+        }
       }
       __threadfence();
       ptx::named_barrier_sync(1, 128);
@@ -215,34 +216,27 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemv_ar_kernel(const __grid_c
       ptx::named_barrier_sync(1, 128);
       if (*bcast) {
         // Last of the group: sum the splits' partials in split order; each
-        // thread handles 8 consecutive columns (two 16-byte loads per partial).
+        // thread handles 4 consecutive columns (one 16-byte load per partial).
         __threadfence();
-        const int c = ep_tid * 8;
+        const int c = ep_tid * 4;
         if (c < ncols) {
           const float* base = p.partials + static_cast<long long>(g) * p.splits * p.M * kGroupCols;
           for (int t = 0; t < p.M; ++t) {
-            float s8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
             for (int sp = 0; sp < p.splits; ++sp) {
-              const float4* src = reinterpret_cast<const float4*>(
-                  base + (static_cast<long long>(sp) * p.M + t) * kGroupCols + c);
-              const float4 x = __ldcg(src);
-              const float4 y = __ldcg(src + 1);
-              s8[0] += x.x; s8[1] += x.y; s8[2] += x.z; s8[3] += x.w;
-              s8[4] += y.x; s8[5] += y.y; s8[6] += y.z; s8[7] += y.w;
+              const float4 x = __ldcg(reinterpret_cast<const float4*>(
+                  base + (static_cast<long long>(sp) * p.M + t) * kGroupCols + c));
+              acc.x += x.x; acc.y += x.y; acc.z += x.z; acc.w += x.w;
             }
             const long long o = static_cast<long long>(t) * p.N + col0 + c;
             for (int r = 0; r < p.R; ++r) {
               if (p.out_f32) {
-                float4* d = reinterpret_cast<float4*>(static_cast<float*>(p.out[r]) + o);
-                d[0] = make_float4(s8[0], s8[1], s8[2], s8[3]);
-                d[1] = make_float4(s8[4], s8[5], s8[6], s8[7]);
+                *reinterpret_cast<float4*>(static_cast<float*>(p.out[r]) + o) = acc;
               } else {
-                uint4 w;
-                w.x = ptx::pack_bf16x2(s8[0], s8[1]);
-                w.y = ptx::pack_bf16x2(s8[2], s8[3]);
-                w.z = ptx::pack_bf16x2(s8[4], s8[5]);
-                w.w = ptx::pack_bf16x2(s8[6], s8[7]);
-                *reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out[r]) + o) = w;
+                uint2 w;
+                w.x = ptx::pack_bf16x2(acc.x, acc.y);
+                w.y = ptx::pack_bf16x2(acc.z, acc.w);
+                *reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.out[r]) + o) = w;
               }
             }
           }
@@ -393,7 +387,7 @@ extern "C" fcc_status fcc_gemv_ar_static(int R, const void* const* A, const void
   int groups = 0, splits = 0;
   gemv_shape(N, R, K, sms, opts != nullptr ? opts->max_ctas : 0, &groups, &splits);
   // Size limit of the static array: one ticket per column group, and one
-  // partial (M x 1024 f32 = M x 4 KiB) per CTA; fewer CTAs per group are used
+  // partial (M x 512 f32 = M x 2 KiB) per CTA; fewer CTAs per group are used
   // when the default number does not fit.
   const size_t room = kStaticScratchBytes - kStaticTicketBytes;
   const size_t per_split = gemv_partial_bytes(groups, 1, M);
@@ -404,7 +398,7 @@ extern "C" fcc_status fcc_gemv_ar_static(int R, const void* const* A, const void
   GemvParams p;
   std::memset(&p, 0, sizeof(p));
   for (int r = 0; r < R; ++r) {
-    if ((s = light_make_map(&p.mapA[r], A[r], M, K, kTok)) != FCC_OK) return s;
+    if ((s = light_make_map(&p.mapA[r], A[r], M, K, kBM)) != FCC_OK) return s;
     if ((s = light_make_map(&p.mapB[r], B[r], K, N, kBK)) != FCC_OK) return s;
     p.out[r] = out[r];
   }

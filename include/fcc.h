@@ -138,9 +138,9 @@ fcc_status fcc_gemv_ar(int R, const void *const *A, const void *const *B, void *
  * caller passes inputs and outputs, and the kernel's scratch (partial sums
  * and arrival tickets) is a 4 MiB static device array inside the library,
  * held on every GPU that loads the library until the process exits.
- *  - Limit: each CTA keeps an M x 1024 f32 partial (M x 4 KiB) per group of
- *    1024 columns, so ceil(N/1024) * M <= 1023 (N <= 130,048 for 8 tokens,
- *    64,512 for 16); within that the call uses as many CTAs per column group
+ *  - Limit: each CTA keeps an M x 512 f32 partial (M x 2 KiB) per group of
+ *    512 columns, so ceil(N/512) * M <= 2047 (N <= 130,560 for 8 tokens,
+ *    65,024 for 16); within that the call uses as many CTAs per column group
  *    as fit in the array (possibly fewer than fcc_gemv_ar uses, which changes
  *    only the f32 summation order).  Beyond it the call returns
  *    FCC_ERR_WORKSPACE and launches nothing.  opts->workspace is ignored;

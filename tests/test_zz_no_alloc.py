@@ -46,7 +46,7 @@ def test_static_scratch_matches_allocating_entry_point(R, M, N, K):
 
 def test_static_scratch_size_limit_is_refused():
     R, M, K = 1, 16, 64
-    N = 1024 * 64  # 64 column groups x 16 tokens x 4 KiB per CTA: more than the array holds
+    N = 512 * 128  # 128 column groups x 16 tokens x 2 KiB per CTA: more than the array holds
     A, B = synth.gemm_inputs(R, M, N, K, 1.0, 0.02, seed=3)
     dA = [dev_bf16(a) for a in A]
     dB = [dev_bf16(b) for b in B]
