@@ -57,8 +57,9 @@ struct Cfg {
   static constexpr uint32_t kBBytes = kBK * kBNcta * 2;     // 32 or 16 KiB
   static constexpr uint32_t kStageBytes = kABytes + kBBytes;
   static constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(kTileM, kBN, false, true);
+  // ... + barriers + flags + the gather mode's table of 128 row addresses.
   static constexpr int kSmem = 1024 + kStages * static_cast<int>(kStageBytes) +
-                               (2 * kStages + 5) * 8 + 16;
+                               (2 * kStages + 5) * 8 + 16 + kBM * 8;
 };
 
 struct Tile {
@@ -205,6 +206,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* bcast = reinterpret_cast<volatile int*>(tmem_slot + 2);
+  uint64_t* rowtab = reinterpret_cast<uint64_t*>(tmem_slot + 4);  // gather mode: row addresses
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -288,18 +290,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
       for (int t = pair; t < num_tiles && ok; t += npairs) {
         const Tile tl = tile_of<MODE, TM>(p, t);
         const int b_col = tl.nt * kBN + static_cast<int>(cta) * C::kBNcta;
-        const uint16_t* rowp[4];
+        // Source address of each of this CTA's 128 rows, in shared memory
+        // (the previous tile's copies have all been issued: the warp is past them).
+        __syncwarp();
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const int local = static_cast<int>(cta) * kBM + lane + 32 * j;
-          rowp[j] = X0;  // padding rows read a valid row; their results are not stored
+          const uint16_t* rp = X0;  // padding rows read a valid row; their results are not stored
           if (local < tl.rows) {
             const int src = __ldcg(p.recv_src[tl.shard] + tl.row0 + local);
             const int s = src / p.T;
-            rowp[j] = static_cast<const uint16_t*>(p.X[s]) +
-                      static_cast<long long>(src - s * p.T) * p.K;
+            rp = static_cast<const uint16_t*>(p.X[s]) + static_cast<long long>(src - s * p.T) * p.K;
           }
+          rowtab[lane + 32 * j] = reinterpret_cast<uint64_t>(rp);
         }
+        __syncwarp();
         for (int it = 0; it < k_iters; ++it) {
           if (!W.wait(&empty[stage], phase ^ 1u)) {
             ok = false;
@@ -326,16 +331,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
           }
           const uint32_t a_base = ptx::smem_addr(sA + stage * kABytes);
           const int k0 = it * kBK;
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int r = lane + 32 * j;
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-              const int k = k0 + c * 8;
-              const bool in = k < p.K;
-              ptx::cp_async_16(a_base + r * 128 + ((c ^ (r & 7)) << 4), rowp[j] + (in ? k : 0),
-                               in ? 16u : 0u);
-            }
+          // Eight consecutive lanes copy one row's 128 bytes, so each warp-wide
+          // copy instruction touches four rows (four cache lines).
+          const int c = lane & 7;
+          const int k = k0 + c * 8;
+          const bool in = k < p.K;
+#pragma unroll 8
+          for (int j = 0; j < kBM / 4; ++j) {
+            const int r = (lane >> 3) + 4 * j;
+            const uint16_t* rp = reinterpret_cast<const uint16_t*>(rowtab[r]);
+            ptx::cp_async_16(a_base + r * 128 + ((c ^ (r & 7)) << 4), rp + (in ? k : 0),
+                             in ? 16u : 0u);
           }
           ptx::cp_async_commit();
           if (++pending > kLag) {
