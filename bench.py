@@ -287,6 +287,62 @@ def time_calls(fn, steps, warmup, stream):
     return s.elapsed_time(e) / steps  # ms
 
 
+def interdecom_check(fcc, R, M, N, K, dA, dB, outs, stream, unfused_ms, pk):
+    """The InterDecom chunk-count model against a sweep of chunk counts.
+
+    Model inputs from measurements of this run: X = the reduce of the R f32
+    partials into the shards at the measured copy bandwidth, G = the unfused
+    time minus X, alpha = what one chunk adds beyond G + X (T(1) - G - X)."""
+    sweep = {}
+    for c in (1, 2, 4, 8, 16, 32, 64):
+        o = fcc.make_opts(algo=fcc.FCC_ALGO_INTERDECOM, chunks=c)
+        sweep[c] = time_calls(lambda o=o: fcc.fcc_gemm_rs(R, dA, dB, outs, M, N, K, 0, 0, o,
+                                                          stream), 10, 2, stream)
+    X = (R * M * N * 4 + M * N * 2) / (pk["hbm_gbs"] * 1e9) * 1e3  # ms
+    G = max(unfused_ms - X, 1e-3)
+    alpha = max(sweep[1] - G - X, 1e-4)
+    c_star = fcc.fcc_interdecom_chunks(G, X, alpha, 64)
+    o = fcc.make_opts(algo=fcc.FCC_ALGO_INTERDECOM, chunks=c_star)
+    t_star = time_calls(lambda: fcc.fcc_gemm_rs(R, dA, dB, outs, M, N, K, 0, 0, o, stream),
+                        10, 2, stream)
+    best_c = min(sweep, key=sweep.get)
+    return {"sweep_ms": {str(c): t for c, t in sweep.items()}, "best_c": best_c,
+            "model": {"G_ms": G, "X_ms": X, "alpha_ms": alpha, "c_star": c_star,
+                      "T_cstar_ms": t_star,
+                      "T_model_ms": fcc.fcc_interdecom_time(G, X, alpha, c_star)},
+            "c_star_within_10pct_of_best": t_star <= 1.10 * sweep[best_c]}
+
+
+def small_rs_latency(fcc, torch, np, synth, dev, stream):
+    """The 2-rank 256x256x128 reduce-scatter: a latency case (launch-bound).
+
+    Reports back-to-back calls and, replayed from a CUDA graph, 1000 calls."""
+    w = synth.WORKLOADS["gemm_rs_r2_256x256x128"]
+    A, B = synth.gemm_inputs(w.R, w.M, w.N, w.K, w.std_a, w.std_b, seed=0)
+    dA = [torch.from_numpy(a.view(np.int16)).to(dev) for a in A]
+    dB = [torch.from_numpy(b.view(np.int16)).to(dev) for b in B]
+    outs = [torch.empty((w.M // w.R, w.N), dtype=torch.float32, device=dev) for _ in range(w.R)]
+
+    def call(s):
+        fcc.fcc_gemm_rs(w.R, dA, dB, outs, w.M, w.N, w.K, 0, 2, None, s)
+
+    res = {"plain_us": 1e3 * time_calls(lambda: call(stream), 200, 10, stream)}
+    try:
+        side = torch.cuda.Stream(device=dev)
+        with torch.cuda.stream(side):
+            call(side)  # one call outside capture: device set-up happens here
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=side):
+                for _ in range(100):
+                    call(torch.cuda.current_stream(dev))
+        res["graph_us"] = 1e3 * time_calls(g.replay, 10, 2, stream) / 100
+    except Exception as e:  # capture is optional information
+        res["graph_error"] = str(e)[:200]
+    res["TFLOP/s_plain"] = w.flops() / (res["plain_us"] * 1e-6) / 1e12
+    return res
+
+
 def other_ops(fcc, torch, np, synth, dev, stream, dA_rs, dB_rs, pk):
     """The other fused operators at their workload sizes, each with its baselines."""
     ops = {}
@@ -505,8 +561,12 @@ def run_fcc(args, world, rank, local, pg):
         base["cublas_stacked_gemm"] = {"ms": t, "TFLOP/s": flops / (t * 1e-3) / 1e12,
                                        "note": "one library GEMM of the same FLOPs, no collective"}
         del Acat, Bcat
+        base["interdecom_check"] = interdecom_check(fcc, R, M, N, K, dA, dB, outs, stream,
+                                                    base["unfused"]["ms"], pk)
         line["baselines"] = base
         line["ops"] = other_ops(fcc, torch, np, synth, dev, stream, dA, dB, pk)
+        line["ops"]["gemm_rs_r2_256x256x128"] = small_rs_latency(fcc, torch, np, synth, dev,
+                                                                 stream)
 
     # ---- CPU oracle on a bounded sample (rank 0 only)
     if rank == 0 and args.cpu_seconds <= 0:
