@@ -776,4 +776,14 @@ fcc_status internal_make_map(CUtensorMap* m, const void* ptr, int64_t rows, int6
   return make_map(m, ptr, rows, cols, box_rows);
 }
 
+fcc_status internal_side_stream(cudaStream_t* side, cudaEvent_t* ev, int n) {
+  DeviceState* d = nullptr;
+  fcc_status s = device_state(&d);
+  if (s != FCC_OK) return s;
+  if (n > 8) return FCC_ERR_INVALID;
+  *side = d->side[1];
+  for (int i = 0; i < n; ++i) ev[i] = d->ev[kMaxChunks - 8 + i];
+  return FCC_OK;
+}
+
 }  // namespace fcc

@@ -57,9 +57,11 @@ struct Cfg {
   static constexpr uint32_t kBBytes = kBK * kBNcta * 2;     // 32 or 16 KiB
   static constexpr uint32_t kStageBytes = kABytes + kBBytes;
   static constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(kTileM, kBN, false, true);
-  // ... + barriers + flags + the gather mode's table of 128 row addresses.
+  // A tile whose columns end in the first half of its 256 runs 128 wide.
+  static constexpr uint32_t kIdescNarrow = ptx::idesc_bf16_f32(kTileM, kBN / 2, false, true);
+  // ... + barriers + flags.
   static constexpr int kSmem = 1024 + kStages * static_cast<int>(kStageBytes) +
-                               (2 * kStages + 5) * 8 + 16 + kBM * 8;
+                               (2 * kStages + 5) * 8 + 16;
 };
 
 struct Tile {
@@ -85,7 +87,8 @@ __device__ __forceinline__ void raster(int t, int tiles_m, int tiles_n, int grou
 template <int MODE, class P>
 __device__ __forceinline__ int num_tiles_of(const P& p) {
   if constexpr (MODE == MODE_GROUPED) {
-    return __ldcg(p.tile_start + p.E);  // written on the device by the dispatch kernels
+    // Tiles of experts [e_lo, e_hi); the table is written by the dispatch kernels.
+    return __ldcg(p.tile_start + p.e_hi) - __ldcg(p.tile_start + p.e_lo);
   } else {
     return p.num_tiles;
   }
@@ -110,7 +113,8 @@ __device__ __forceinline__ Tile tile_of(const P& p, int t) {
   tl.rows = 0;
   if constexpr (MODE == MODE_GROUPED) {
     // Expert of tile t: the last e with tile_start[e] <= t (binary search).
-    int lo = 0, hi = p.E - 1;
+    t += __ldcg(p.tile_start + p.e_lo);
+    int lo = p.e_lo, hi = p.e_hi - 1;
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
       if (__ldcg(p.tile_start + mid) <= t)
@@ -206,7 +210,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* bcast = reinterpret_cast<volatile int*>(tmem_slot + 2);
-  uint64_t* rowtab = reinterpret_cast<uint64_t*>(tmem_slot + 4);  // gather mode: row addresses
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -215,16 +218,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
   const int pair = blockIdx.x / CG;
   const int npairs = gridDim.x / CG;
 
-  // Gather mode (MoE without a staged copy): the producer warp copies A rows
-  // with cp.async and signals each stage once its copies have landed, so the
-  // full barrier also counts one A-ready arrival per CTA of the pair.
+  // Gather mode (MoE without a staged copy): the producer warp fetches the A
+  // rows from the source tokens with TMA gather4.
   bool gather = false;
   if constexpr (MODE == MODE_GROUPED) gather = p.gather != 0;
-  const uint32_t full_count = gather ? 1u + CG : 1u;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      ptx::mbar_init(&full[s], full_count);
+      ptx::mbar_init(&full[s], 1);
       ptx::mbar_init(&empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -243,6 +244,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
   }
   const int num_tiles = num_tiles_of<MODE>(p);
   const int k_iters = k_iters_of<MODE>(p);
+  // Narrow tile: the output's last columns fit in the first half of the
+  // 256-wide tile, so the B loads, the MMA width and the epilogue are halved.
+  auto narrow = [&](int nt) { return p.N - nt * kBN <= kBN / 2; };
   if (warp == 1) {
     if constexpr (CG == 2) {
       ptx::tmem_alloc_pair(tmem_slot, kTmemCols);
@@ -264,108 +268,65 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
 
   if (warp == 0 && gather) {
     // ----------------------------------------------- producer, gather mode
-    // The whole warp: lane l copies rows l, l+32, l+64, l+96 of this CTA's 128
-    // A rows, 16 bytes at a time, straight from the source token rows, into
-    // the 128-byte-swizzled K-major layout the MMA descriptor expects (chunk c
-    // of row r lands at r*128 + ((c ^ (r % 8)) * 16)).  Each stage's copies are
-    // a cp.async group; a stage is signalled ready kLag stages later, after
-    // its group has landed and a proxy fence has made it visible to the tensor
-    // core.  Lane 0 also loads the B tile with TMA.
+    // The whole warp.  Row i of receiving rank d's order is row recv_src[d][i]
+    // of the sources' concatenated [R*T, H] token matrix (mapA, a box one row
+    // high), so lane q fetches rows 4q..4q+3 of this CTA's 128 A rows with one
+    // TMA gather4 per stage: four 128-byte row pieces, swizzled like a tiled
+    // box, counted on the same full barrier as the B tile that lane 0 loads.
     if constexpr (MODE == MODE_GROUPED) {
-      constexpr int kLag = 3;
-      const uint32_t full0_leader = (CG == 2) ? ptx::mapa(ptx::smem_addr(&full[0]), 0) : 0u;
-      auto signal = [&](uint32_t s) {
-        if (lane == 0) {
-          if constexpr (CG == 2)
-            ptx::mbar_arrive_cluster(full0_leader + s * 8);
-          else
-            ptx::mbar_arrive(&full[s]);
-        }
-      };
-      uint32_t stage = 0, phase = 0, sig = 0;
-      int pending = 0;
+      uint32_t stage = 0, phase = 0;
       uint32_t issued = 0, last_parity = 0;
       bool ok = true;
-      const uint16_t* X0 = static_cast<const uint16_t*>(p.X[0]);
+      const CUtensorMap* ma = &p.mapA[0];
       for (int t = pair; t < num_tiles && ok; t += npairs) {
         const Tile tl = tile_of<MODE, TM>(p, t);
-        const int b_col = tl.nt * kBN + static_cast<int>(cta) * C::kBNcta;
-        // Source address of each of this CTA's 128 rows, in shared memory
-        // (the previous tile's copies have all been issued: the warp is past them).
-        __syncwarp();
+        const int bn_cta = narrow(tl.nt) ? C::kBNcta / 2 : C::kBNcta;
+        const int b_col = tl.nt * kBN + static_cast<int>(cta) * bn_cta;
+        const uint32_t stage_bytes = kABytes + static_cast<uint32_t>(bn_cta) * kBK * 2;
+        // Source rows of this lane's four A rows; padding rows read row 0 (their
+        // results are never stored).
+        int y[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int local = static_cast<int>(cta) * kBM + lane + 32 * j;
-          const uint16_t* rp = X0;  // padding rows read a valid row; their results are not stored
-          if (local < tl.rows) {
-            const int src = __ldcg(p.recv_src[tl.shard] + tl.row0 + local);
-            const int s = src / p.T;
-            rp = static_cast<const uint16_t*>(p.X[s]) + static_cast<long long>(src - s * p.T) * p.K;
-          }
-          rowtab[lane + 32 * j] = reinterpret_cast<uint64_t>(rp);
+        for (int i = 0; i < 4; ++i) {
+          const int local = static_cast<int>(cta) * kBM + 4 * lane + i;
+          y[i] = local < tl.rows ? __ldcg(p.recv_src[tl.shard] + tl.row0 + local) : 0;
         }
-        __syncwarp();
         for (int it = 0; it < k_iters; ++it) {
-          if (!W.wait(&empty[stage], phase ^ 1u)) {
+          int good = 1;
+          if (lane == 0) good = W.wait(&empty[stage], phase ^ 1u) ? 1 : 0;
+          if (!__shfl_sync(0xffffffffu, good, 0)) {
             ok = false;
             break;
           }
-          if (lane == 0) {
-            const CUtensorMap* mb = &p.mapB[tl.expert];
-            uint8_t* b_dst = sB + stage * C::kBBytes;
-            if constexpr (CG == 2) {
-              const uint32_t bar = ptx::mapa(ptx::smem_addr(&full[stage]), 0);
-              if (cta == 0) ptx::mbar_arrive_expect_tx(&full[stage], 2 * C::kBBytes);
-#pragma unroll
-              for (int i = 0; i < C::kBNcta / 64; ++i)
+          const CUtensorMap* mb = &p.mapB[tl.expert];
+          uint8_t* a_dst = sA + stage * kABytes + lane * (4 * 128);
+          uint8_t* b_dst = sB + stage * C::kBBytes;
+          if constexpr (CG == 2) {
+            const uint32_t bar = ptx::mapa(ptx::smem_addr(&full[stage]), 0);
+            if (lane == 0) {
+              if (cta == 0) ptx::mbar_arrive_expect_tx(&full[stage], 2 * stage_bytes);
+              for (int i = 0; i < bn_cta / 64; ++i)
                 ptx::tma_load_2d_pair(b_dst + i * kBBoxBytes, mb, bar, b_col + 64 * i, it * kBK);
-            } else {
-              ptx::mbar_arrive_expect_tx(&full[stage], C::kBBytes);
-#pragma unroll
-              for (int i = 0; i < C::kBNcta / 64; ++i)
+            }
+            __syncwarp();
+            ptx::tma_gather4_pair(a_dst, ma, bar, it * kBK, y[0], y[1], y[2], y[3]);
+          } else {
+            if (lane == 0) {
+              ptx::mbar_arrive_expect_tx(&full[stage], stage_bytes);
+              for (int i = 0; i < bn_cta / 64; ++i)
                 ptx::tma_load_2d(b_dst + i * kBBoxBytes, mb, &full[stage], b_col + 64 * i,
                                  it * kBK);
             }
-            issued |= 1u << stage;
-            last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
-          }
-          const uint32_t a_base = ptx::smem_addr(sA + stage * kABytes);
-          const int k0 = it * kBK;
-          // Eight consecutive lanes copy one row's 128 bytes, so each warp-wide
-          // copy instruction touches four rows (four cache lines).
-          const int c = lane & 7;
-          const int k = k0 + c * 8;
-          const bool in = k < p.K;
-#pragma unroll 8
-          for (int j = 0; j < kBM / 4; ++j) {
-            const int r = (lane >> 3) + 4 * j;
-            const uint16_t* rp = reinterpret_cast<const uint16_t*>(rowtab[r]);
-            ptx::cp_async_16(a_base + r * 128 + ((c ^ (r & 7)) << 4), rp + (in ? k : 0),
-                             in ? 16u : 0u);
-          }
-          ptx::cp_async_commit();
-          if (++pending > kLag) {
-            ptx::cp_async_wait<kLag>();
-            ptx::fence_proxy_async_smem();
             __syncwarp();
-            signal(sig);
-            if (++sig == static_cast<uint32_t>(kStages)) sig = 0;
-            --pending;
+            ptx::tma_gather4(a_dst, ma, &full[stage], it * kBK, y[0], y[1], y[2], y[3]);
           }
+          issued |= 1u << stage;
+          last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
           if (++stage == kStages) {
             stage = 0;
             phase ^= 1u;
           }
         }
-      }
-      // Flush: every issued stage is signalled once its copies have landed.
-      ptx::cp_async_wait<0>();
-      ptx::fence_proxy_async_smem();
-      __syncwarp();
-      while (pending > 0) {
-        signal(sig);
-        if (++sig == static_cast<uint32_t>(kStages)) sig = 0;
-        --pending;
       }
       if (*abort_flag && cta == 0 && lane == 0) {
         for (int s = 0; s < kStages; ++s)
@@ -389,7 +350,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
           a_row = tl.mt * TM;
         }
         a_row += static_cast<int>(cta) * kBM;                 // this CTA's half of the rows
-        const int b_col = tl.nt * kBN + static_cast<int>(cta) * C::kBNcta;
+        const int bn_cta = narrow(tl.nt) ? C::kBNcta / 2 : C::kBNcta;  // B columns of this CTA
+        const int b_col = tl.nt * kBN + static_cast<int>(cta) * bn_cta;
+        const uint32_t stage_bytes = kABytes + static_cast<uint32_t>(bn_cta) * kBK * 2;
         int r = (tl.rank >= 0) ? tl.rank : 0;
         int kb = 0;
         for (int it = 0; it < k_iters; ++it) {
@@ -405,16 +368,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
           if constexpr (CG == 2) {
             // Both CTAs' bytes are counted on the leader's full barrier.
             const uint32_t bar = ptx::mapa(ptx::smem_addr(&full[stage]), 0);
-            if (cta == 0) ptx::mbar_arrive_expect_tx(&full[stage], 2 * C::kStageBytes);
+            if (cta == 0) ptx::mbar_arrive_expect_tx(&full[stage], 2 * stage_bytes);
             ptx::tma_load_2d_pair(a_dst, ma, bar, kb * kBK, a_row);
-#pragma unroll
-            for (int i = 0; i < C::kBNcta / 64; ++i)
+            for (int i = 0; i < bn_cta / 64; ++i)
               ptx::tma_load_2d_pair(b_dst + i * kBBoxBytes, mb, bar, b_col + 64 * i, kb * kBK);
           } else {
-            ptx::mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
+            ptx::mbar_arrive_expect_tx(&full[stage], stage_bytes);
             ptx::tma_load_2d(a_dst, ma, &full[stage], kb * kBK, a_row);
-#pragma unroll
-            for (int i = 0; i < C::kBNcta / 64; ++i)
+            for (int i = 0; i < bn_cta / 64; ++i)
               ptx::tma_load_2d(b_dst + i * kBBoxBytes, mb, &full[stage], b_col + 64 * i,
                                kb * kBK);
           }
@@ -445,12 +406,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
       uint32_t acc = 0, acc_phase = 0;
       bool any = false, ok = true;
       for (int t = pair; t < num_tiles && ok; t += npairs) {
+        const uint32_t idesc = narrow(tile_of<MODE, TM>(p, t).nt) ? C::kIdescNarrow : C::kIdesc;
         if (!W.wait(&tempty[acc], acc_phase ^ 1u)) break;
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * kBN;
         for (int it = 0; it < k_iters; ++it) {
-          // In a pair, the peer's A-ready arrival is released at cluster scope.
-          if (!W.template wait<CG == 2>(&full[stage], phase)) {
+          if (!W.wait(&full[stage], phase)) {
             ok = false;
             break;
           }
@@ -464,9 +425,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
             // B: MN-major, advance 16 k-rows (2 KiB); 64-wide n atoms 8 KiB apart.
             const uint64_t bd = ptx::smem_desc_sw128(b_addr + kk * 2048, kBBoxBytes, 1024);
             if constexpr (CG == 2)
-              ptx::mma_f16_pair(d_tmem, ad, bd, C::kIdesc, (it > 0 || kk > 0) ? 1u : 0u);
+              ptx::mma_f16_pair(d_tmem, ad, bd, idesc, (it > 0 || kk > 0) ? 1u : 0u);
             else
-              ptx::mma_f16(d_tmem, ad, bd, C::kIdesc, (it > 0 || kk > 0) ? 1u : 0u);
+              ptx::mma_f16(d_tmem, ad, bd, idesc, (it > 0 || kk > 0) ? 1u : 0u);
           }
           if constexpr (CG == 2)
             ptx::mma_commit_pair_multicast(&empty[stage], 0x3);  // frees the stage in both CTAs
@@ -543,12 +504,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
 
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kBN;
       const int col0 = tl.nt * kBN;
+      const int cend = narrow(tl.nt) ? kBN / 2 : kBN;  // accumulator columns written
 #pragma unroll 1
-      for (int c = 0; c < kBN; c += 32) {
+      for (int c = 0; c < cend; c += 32) {
         uint32_t v[32];
         ptx::tmem_ld_32x32b_x32(taddr + c, v);
         ptx::tmem_ld_wait();
-        if (c == kBN - 32) {
+        if (c == cend - 32) {
           // Accumulator fully read: hand it back to the MMA warp early.
           ptx::tc_fence_before();
           __syncwarp();

@@ -47,15 +47,15 @@ struct GemmParams {
 };
 
 struct GemvParams {
-  CUtensorMap mapA[FCC_MAX_RANKS];  // [M, K] rows padded to 16 by out-of-bounds fill
+  CUtensorMap mapA[FCC_MAX_RANKS];  // [M, K], rows padded to 128 by out-of-bounds fill
   CUtensorMap mapB[FCC_MAX_RANKS];  // [K, N]
   void* out[FCC_MAX_RANKS];
   int R, M, N, K;
   int kb_per_rank;
-  int groups;           // column groups of 1024 columns: ceil(N / 1024)
+  int groups;           // column groups of 512 columns: ceil(N / 512)
   int splits;           // CTAs per group (parts of the R*K range); grid = groups * splits
   int out_f32;
-  float* partials;      // [groups * splits][M][1024]
+  float* partials;      // [groups * splits][M][512]
   int* tickets;         // [groups]: (generation << 8) | arrivals
   unsigned gen;         // call generation, 1..2^24-1 (never 0: zeroed tickets are "old")
   int* status;
@@ -79,14 +79,14 @@ struct GroupedParams {
   const int* tile_start;               // [E + 1]
   const int* expert_base;              // [E]
   const int* expert_rows;              // [E] (clamped to the receive capacity)
+  int e_lo, e_hi;                      // this launch covers the tiles of experts [e_lo, e_hi)
   int* status;
   unsigned long long timeout_ns;
   // Gather mode (gather = 1): the A rows are read straight from the source
-  // tokens, row i of rank d's receive order being X[s][t] with
-  // recv_src[d][i] = s*T + t, instead of from a staged copy (mapA unused).
-  const void* X[FCC_MAX_RANKS];        // [T, H] bf16 per source rank
+  // tokens instead of from a staged copy.  Every mapA[d] is then the map of
+  // the sources' concatenated [R*T, H] matrix with a box one row high, and row
+  // i of rank d's receive order is its row recv_src[d][i] (= s*T + t).
   const int* recv_src[FCC_MAX_RANKS];  // [cap] per receiving rank
-  int T;
   int gather;
 };
 
@@ -142,4 +142,6 @@ fcc_status internal_prepare(const fcc_opts* o, size_t ws_bytes, void** ws, int**
 // 2-D bf16 tensor map, box [box_rows, 64], 128-byte swizzle (after internal_prepare).
 fcc_status internal_make_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols,
                              uint32_t box_rows);
+// A side stream and n <= 8 events of the current device (after internal_prepare).
+fcc_status internal_side_stream(cudaStream_t* side, cudaEvent_t* ev, int n);
 }  // namespace fcc

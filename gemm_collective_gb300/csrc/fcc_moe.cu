@@ -15,13 +15,17 @@
 //                     within its expert (warp match + popc, then a prefix over
 //                     the CTA's warps), i.e. its receive row; writes recv_src.
 //   4. copy_kernel    one warp per token: reads the token row once and writes
-//                     it to each of its receive rows (the all-to-all), when
-//                     the caller asks for the staged rows (recv_x given).
+//                     it to each of its receive rows (the all-to-all): into
+//                     the caller's recv_x, or into workspace when the GEMM
+//                     cannot gather.
 //   5. the persistent tcgen05 GEMM in grouped mode: tiles over
 //                     (expert, m tile, n tile) from the device tile table.
-//                     Without recv_x the GEMM's producer warp gathers each A
-//                     row straight from the source token (recv_src gives it),
-//                     so the dispatched rows never make a round trip to HBM.
+//                     With FCC_ALGO_FUSED and the sources one [R*T, H]
+//                     array, the GEMM's producer warp fetches each A row
+//                     straight from its source token with TMA gather4
+//                     (recv_src gives the row), so no staged copy precedes
+//                     it; a requested recv_x is then written by the copy on
+//                     a second stream, beside the GEMM.
 // No atomics decide any position, so every index output is bit-exact and
 // repeatable; the host never waits for the counts.
 #include <cuda_runtime.h>
@@ -303,9 +307,19 @@ struct MoePlan {
 
 size_t up256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
-// Gather inside the expert GEMM (no staged rows) only when asked for with
-// FCC_ALGO_FUSED; otherwise the rows are staged (in recv_x, or in workspace).
-bool moe_gathers(const fcc_opts* o) { return o != nullptr && o->algo == FCC_ALGO_FUSED; }
+// The expert GEMM gathers its rows from the sources (no staged copy on its
+// path) when FCC_ALGO_FUSED asks for it and the sources are one [R*T, H]
+// array (X[s] = X[0] + s*T*H elements).  TMA gather4 moves 4 rows of 128 bytes
+// per request, and on sm_103a its request rate, not memory, bounds that GEMM
+// (about 2.7x the staged form on the 8 x 4096-token, 64-expert workload), so
+// the default stages the rows with one streaming copy and loads whole tiles.
+bool moe_gathers(const fcc_opts* o, int R, const void* const* X, int64_t T, int64_t H) {
+  if (o == nullptr || o->algo != FCC_ALGO_FUSED) return false;
+  const char* x0 = static_cast<const char*>(X[0]);
+  for (int s = 1; s < R; ++s)
+    if (static_cast<const char*>(X[s]) != x0 + static_cast<int64_t>(s) * T * H * 2) return false;
+  return true;
+}
 
 MoePlan moe_plan(int R, int64_t T, int E, int topk, int64_t H = 0, int64_t cap = 0,
                  bool stage_in_workspace = false) {
@@ -383,8 +397,9 @@ size_t fcc_moe_workspace_size(int R, int64_t T, int64_t H, int64_t F, int E, int
   (void)opts;
   if (R < 1 || R > FCC_MAX_RANKS || T < 1 || E < 1 || E > FCC_MAX_EXPERTS || topk < 1)
     return 0;
-  // Upper bound: includes room to stage the rows in case recv_x is NULL.
-  return moe_plan(R, T, E, topk, H, cap, !moe_gathers(opts)).total;
+  // Upper bound: includes room to stage the rows (recv_x NULL, and the
+  // sources not one array or FCC_ALGO_UNFUSED asked for).
+  return moe_plan(R, T, E, topk, H, cap, true).total;
 }
 
 fcc_status fcc_moe_dispatch_gemm(int R, const void* const* X, const float* const* logits,
@@ -398,8 +413,9 @@ fcc_status fcc_moe_dispatch_gemm(int R, const void* const* X, const float* const
   fcc_status s = check_moe(R, X, logits, W, T, H, F, E, topk, recv_x, recv_y, cap, topk_idx,
                            topk_gate, expert_counts, send_counts, recv_src, in, out_dtype, opts);
   if (s != FCC_OK) return s;
-  const bool gather = moe_gathers(opts);
+  const bool gather = moe_gathers(opts, R, X, T, H);
   const bool stage_ws = !gather && recv_x == nullptr;
+  const bool copy = !gather || recv_x != nullptr;
   const MoePlan plan = moe_plan(R, T, E, topk, H, cap, stage_ws);
   void* ws = nullptr;
   int* status = nullptr;
@@ -448,9 +464,12 @@ fcc_status fcc_moe_dispatch_gemm(int R, const void* const* X, const float* const
   GroupedParams g;
   std::memset(&g, 0, sizeof(g));
   for (int d = 0; d < R; ++d) {
-    if (!gather && (s = internal_make_map(&g.mapA[d], a.recv_x[d], cap, H, kBM)) != FCC_OK)
-      return s;
-    g.X[d] = X[d];
+    if (gather)
+      s = d == 0 ? internal_make_map(&g.mapA[0], X[0], R * T, H, 1) : FCC_OK;
+    else
+      s = internal_make_map(&g.mapA[d], a.recv_x[d], cap, H, kBM);
+    if (s != FCC_OK) return s;
+    if (gather) g.mapA[d] = g.mapA[0];
     g.recv_src[d] = recv_src[d];
     g.out[d] = recv_y[d];
   }
@@ -467,20 +486,34 @@ fcc_status fcc_moe_dispatch_gemm(int R, const void* const* X, const float* const
   g.tile_start = a.tile_start;
   g.expert_base = a.expert_base;
   g.expert_rows = a.expert_rows;
+  g.e_lo = 0;
+  g.e_hi = E;
   g.status = status;
   g.timeout_ns = timeout_ns;
-  g.T = static_cast<int>(T);
   g.gather = gather ? 1 : 0;
 
   route_kernel<<<plan.nchunks, 1024, 0, st>>>(a);
   scan_kernel<<<E, 256, 0, st>>>(a);
   finalize_kernel<<<1, 64, 0, st>>>(a);
   rank_kernel<<<plan.nchunks, 256, 0, st>>>(a);
-  if (!gather) copy_kernel<<<std::max(1, sms) * 4, 256, 0, st>>>(a);
+  // With the gather the copy (only for a requested recv_x) runs beside the
+  // GEMM on a side stream: both only read what the dispatch kernels wrote.
+  const bool side_copy = copy && gather;
+  cudaStream_t side = nullptr;
+  cudaEvent_t ev[2] = {};
+  if (side_copy) {
+    if ((s = internal_side_stream(&side, ev, 2)) != FCC_OK) return s;
+    if (cudaEventRecord(ev[0], st) != cudaSuccess ||
+        cudaStreamWaitEvent(side, ev[0], 0) != cudaSuccess)
+      return FCC_ERR_CUDA;
+  }
+  if (copy) copy_kernel<<<std::max(1, sms) * 4, 256, 0, side_copy ? side : st>>>(a);
   if (cudaGetLastError() != cudaSuccess) return FCC_ERR_CUDA;
+  if (side_copy && cudaEventRecord(ev[1], side) != cudaSuccess) return FCC_ERR_CUDA;
   const int grid = std::max(cg, (sms / cg) * cg);
   if (launch_grouped_gemm(g, cg, grid, st) != cudaSuccess) return FCC_ERR_CUDA;
-  bump_launch_count(gather ? 5 : 6);
+  if (side_copy && cudaStreamWaitEvent(st, ev[1], 0) != cudaSuccess) return FCC_ERR_CUDA;
+  bump_launch_count(copy ? 6 : 5);
   return FCC_OK;
 }
 

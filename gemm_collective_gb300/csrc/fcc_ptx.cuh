@@ -60,8 +60,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return done != 0;
 }
 
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity);
-
 // Bounded waiting.  `abort_flag` lives in shared memory and is raised by the
 // first thread of the CTA that times out, so the other roles stop waiting too.
 struct Waiter {
@@ -76,22 +74,12 @@ struct Waiter {
 
   // Wait until the phase of `bar` with the given parity has completed.
   // Returns false (after raising the abort flag) on timeout or abort.
-  // kCluster: acquire at cluster scope (arrivals released by the peer CTA).
-  template <bool kCluster = false>
-  __device__ __forceinline__ bool try_once(uint64_t* bar, uint32_t parity) const {
-    if constexpr (kCluster)
-      return mbar_try_wait_cluster(bar, parity);
-    else
-      return mbar_try_wait(bar, parity);
-  }
-
-  template <bool kCluster = false>
   __device__ __forceinline__ bool wait(uint64_t* bar, uint32_t parity) const {
-    if (try_once<kCluster>(bar, parity)) return true;
+    if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
     uint32_t spins = 0;
     while (true) {
-      if (try_once<kCluster>(bar, parity)) return true;
+      if (mbar_try_wait(bar, parity)) return true;
       if ((++spins & 63u) == 0u) {
         if (*abort_flag) return false;
         if (globaltimer() - t0 > timeout_ns) {
@@ -267,36 +255,34 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn, b
          | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
 }
 
-// ------------------------------------------------------------- cp.async (16 B)
-// Copies 16 bytes global -> shared; `src_bytes` = 0 writes 16 zero bytes instead.
-__device__ __forceinline__ void cp_async_16(uint32_t dst_smem, const void* src,
-                                            uint32_t src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst_smem), "l"(src),
-               "r"(src_bytes)
-               : "memory");
-}
-
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;" ::: "memory");
-}
-
-// Wait until at most N of this thread's committed cp.async groups are pending.
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
-// try_wait with cluster-scope acquire: observes arrivals released by the peer CTA.
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
-  uint32_t done;
+// ------------------------------------------------------------- TMA gather4
+// Rows y0..y3 of a 2-D tensor map whose box is one row high, columns
+// [x, x + box width) of each, land as four consecutive rows at dst (with the
+// map's swizzle); the bytes are counted on `bar` like a tiled load.
+__device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                            int32_t x, int32_t y0, int32_t y1, int32_t y2,
+                                            int32_t y3) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(done)
-      : "r"(smem_addr(bar)), "r"(parity)
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_addr(bar)), "r"(x), "r"(y0), "r"(y1),
+      "r"(y2), "r"(y3)
       : "memory");
-  return done != 0;
+}
+
+// Same, for one CTA of a pair: the bytes are counted on the barrier at
+// `bar_cluster_addr` (the leader's, from mapa).
+__device__ __forceinline__ void tma_gather4_pair(void* dst, const CUtensorMap* map,
+                                                 uint32_t bar_cluster_addr, int32_t x,
+                                                 int32_t y0, int32_t y1, int32_t y2,
+                                                 int32_t y3) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile::gather4"
+      ".mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(
+          smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster_addr), "r"(x), "r"(y0), "r"(y1),
+      "r"(y2), "r"(y3)
+      : "memory");
 }
 
 // ------------------------------------------------------- CTA pairs (clusters)

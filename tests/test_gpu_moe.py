@@ -27,10 +27,16 @@ GATE_RTOL = 5e-6
 
 
 def _run(X, logits, W, R, T, H, F, E, topk, cap, out_dtype=fcc.FCC_BF16, opts=None,
-         staged=True):
-    """staged: rows into caller buffers; False: recv_x NULL (library workspace, or
-    no staged copy at all with opts.algo = FCC_ALGO_FUSED)."""
-    dX = [dev_bf16(x) for x in X]
+         staged=True, contiguous=False):
+    """staged: rows into caller buffers, else recv_x NULL.  contiguous: the
+    sources are views of one [R*T, H] tensor, so the expert GEMM gathers its
+    rows from them (unless opts asks for FCC_ALGO_UNFUSED); otherwise they are
+    separate tensors and the rows are staged (recv_x, or library workspace)."""
+    if contiguous:
+        whole = dev_bf16(np.concatenate(X))
+        dX = [whole[s * T:(s + 1) * T] for s in range(R)]
+    else:
+        dX = [dev_bf16(x) for x in X]
     dL = [dev_f32(l) for l in logits]
     dW = [dev_bf16(w) for w in W]
     tdt = torch.float32 if out_dtype == fcc.FCC_F32 else torch.bfloat16
@@ -80,6 +86,19 @@ def _check(X, logits, W, R, T, H, F, E, topk, cap, out, sample=None, seed=0):
         assert_close(got, ref, f"recv_y of rank {dst}")
 
 
+# (recv_x given, sources one array, algo) of each launch path:
+#   staged         copy into recv_x, GEMM on the copy (sources separate)
+#   workspace      copy into library workspace, GEMM on the copy (the default)
+#   gather         GEMM gathers from the sources, no copy
+#   gather_recv_x  GEMM gathers; recv_x written beside it on a side stream
+#   fused_separate FCC_ALGO_FUSED with separate sources: staged as by default
+PATHS = {"staged": (True, False, fcc.FCC_ALGO_AUTO),
+         "workspace": (False, True, fcc.FCC_ALGO_AUTO),
+         "gather": (False, True, fcc.FCC_ALGO_FUSED),
+         "gather_recv_x": (True, True, fcc.FCC_ALGO_FUSED),
+         "fused_separate": (False, False, fcc.FCC_ALGO_FUSED)}
+
+
 @pytest.mark.parametrize("R,T,H,F,E,topk", [
     (2, 300, 128, 136, 8, 2),     # ragged chunk, ragged F tile
     (4, 257, 256, 264, 16, 2),
@@ -89,13 +108,14 @@ def _check(X, logits, W, R, T, H, F, E, topk, cap, out, sample=None, seed=0):
     (1, 500, 128, 256, 8, 2),     # one rank
 ])
 @pytest.mark.parametrize("pair", [1, 2])
-@pytest.mark.parametrize("path", ["staged", "workspace", "gather"])
+@pytest.mark.parametrize("path", list(PATHS))
 def test_moe_small(R, T, H, F, E, topk, pair, path):
     X, logits, W = synth.moe_inputs(R, T, H, E, F, seed=R * 100 + T)
     cap = R * T * topk
-    algo = fcc.FCC_ALGO_FUSED if path == "gather" else fcc.FCC_ALGO_AUTO
+    staged, contiguous, algo = PATHS[path]
     out = _run(X, logits, W, R, T, H, F, E, topk, cap,
-               opts=fcc.make_opts(cta_pair=pair, algo=algo), staged=(path == "staged"))
+               opts=fcc.make_opts(cta_pair=pair, algo=algo), staged=staged,
+               contiguous=contiguous)
     _check(X, logits, W, R, T, H, F, E, topk, cap, out)
 
 
@@ -107,7 +127,7 @@ def test_moe_ties_and_f32_output():
     logits[1][5, [7, 3, 5]] = [4.0, 4.0, 4.0]
     cap = R * T * topk
     out = _run(X, logits, W, R, T, H, F, E, topk, cap, fcc.FCC_F32, staged=False,
-               opts=fcc.make_opts(algo=fcc.FCC_ALGO_FUSED))
+               contiguous=True, opts=fcc.make_opts(algo=fcc.FCC_ALGO_FUSED))
     _check(X, logits, W, R, T, H, F, E, topk, cap, out)
     idx0 = out["idx"][0].cpu().numpy()
     assert list(idx0[0]) == [0, 1] and list(idx0[1]) == [2, 6]
@@ -117,12 +137,17 @@ def test_moe_repeatable():
     R, T, H, F, E, topk = 4, 256, 128, 128, 16, 2
     X, logits, W = synth.moe_inputs(R, T, H, E, F, seed=6)
     cap = R * T * topk
-    o = fcc.make_opts(algo=fcc.FCC_ALGO_FUSED)
-    a = _run(X, logits, W, R, T, H, F, E, topk, cap, staged=False, opts=o)
-    b = _run(X, logits, W, R, T, H, F, E, topk, cap, staged=False, opts=o)
-    for d in range(R):
-        assert torch.equal(a["src"][d], b["src"][d])
-        assert torch.equal(a["recv_y"][d].view(torch.int16), b["recv_y"][d].view(torch.int16))
+    for path in ("workspace", "gather"):
+        staged, contiguous, algo = PATHS[path]
+        o = fcc.make_opts(algo=algo)
+        a = _run(X, logits, W, R, T, H, F, E, topk, cap, staged=staged, contiguous=contiguous,
+                 opts=o)
+        b = _run(X, logits, W, R, T, H, F, E, topk, cap, staged=staged, contiguous=contiguous,
+                 opts=o)
+        for d in range(R):
+            assert torch.equal(a["src"][d], b["src"][d])
+            assert torch.equal(a["recv_y"][d].view(torch.int16),
+                               b["recv_y"][d].view(torch.int16))
 
 
 def test_moe_capacity_overflow_reported():
@@ -149,14 +174,15 @@ def test_moe_invalid_arguments():
     assert e.value.status == fcc.FCC_ERR_INVALID
 
 
-@pytest.mark.parametrize("path", ["workspace", "gather"])
+@pytest.mark.parametrize("path", ["workspace", "gather", "gather_recv_x"])
 def test_moe_full_workload_sampled(path):
-    """The benchmark's launches: rows staged in library workspace, and gathered."""
+    """The benchmark's launches: rows staged in library workspace, gathered by
+    the GEMM, and gathered with recv_x written beside the GEMM."""
     w = synth.WORKLOADS["moe_r8_t4096_h4096_e64_f1408"]
     X, logits, W = synth.moe_inputs(w.R, w.T, w.H, w.E, w.F, std_x=w.std_a, std_w=w.std_b,
                                     seed=0)
     cap = 2 * w.T * w.topk  # twice the mean load per rank
-    algo = fcc.FCC_ALGO_FUSED if path == "gather" else fcc.FCC_ALGO_AUTO
-    out = _run(X, logits, W, w.R, w.T, w.H, w.F, w.E, w.topk, cap, staged=False,
-               opts=fcc.make_opts(algo=algo))
+    staged, contiguous, algo = PATHS[path]
+    out = _run(X, logits, W, w.R, w.T, w.H, w.F, w.E, w.topk, cap, staged=staged,
+               contiguous=contiguous, opts=fcc.make_opts(algo=algo))
     _check(X, logits, W, w.R, w.T, w.H, w.F, w.E, w.topk, cap, out, sample=48)
