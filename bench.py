@@ -49,6 +49,9 @@ def parse():
     ap.add_argument("--ref-seconds", type=float, default=90.0,
                     help="target CPU time of the whole --impl reference run")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg")
+    ap.add_argument("--op", default=None,
+                    help="run only this operator leg (a workload name of the ops table) "
+                         "and print its result; for profiling one kernel")
     return ap.parse_args()
 
 
@@ -343,104 +346,113 @@ def small_rs_latency(fcc, torch, np, synth, dev, stream):
     return res
 
 
-def other_ops(fcc, torch, np, synth, dev, stream, dA_rs, dB_rs, pk):
-    """The other fused operators at their workload sizes, each with its baselines."""
+def other_ops(fcc, torch, np, synth, dev, stream, dA_rs, dB_rs, pk, only=None):
+    """The other fused operators at their workload sizes, each with its baselines
+    (only: the one workload name to run)."""
     ops = {}
     hbm = pk["hbm_gbs"]
     tc = pk["bf16_tflops"]
+
+    def want(name):
+        return only is None or only == name
 
     def up(a):
         return torch.from_numpy(a.view(np.int16)).to(dev)
 
     # GEMM + AllReduce on the same 8-rank 8192x8192x3584 inputs
-    w = synth.WORKLOADS["gemm_ar_r8_8192x8192x3584"]
-    R, M, N, K = w.R, w.M, w.N, w.K
-    dA = dA_rs  # the same A_r and B_r as the reduce-scatter leg
-    outs = [torch.empty((M, N), dtype=torch.bfloat16, device=dev) for _ in range(R)]
-    res = {}
-    for name, o in [("fused", None), ("unfused", fcc.make_opts(algo=fcc.FCC_ALGO_UNFUSED)),
-                    ("copy_engine", fcc.make_opts(algo=fcc.FCC_ALGO_CE))]:
-        t = time_calls(lambda o=o: fcc.fcc_gemm_ar(R, dA, dB_rs, outs, M, N, K, 0, 0, o, stream),
-                       10, 3, stream)
-        res[name] = {"ms": t, "TFLOP/s": w.flops() / (t * 1e-3) / 1e12}
-    res["roofline_frac"] = res["fused"]["TFLOP/s"] / tc
-    ops[w.name] = res
-    del outs, dA
+    if want("gemm_ar_r8_8192x8192x3584"):
+        w = synth.WORKLOADS["gemm_ar_r8_8192x8192x3584"]
+        R, M, N, K = w.R, w.M, w.N, w.K
+        dA = dA_rs  # the same A_r and B_r as the reduce-scatter leg
+        outs = [torch.empty((M, N), dtype=torch.bfloat16, device=dev) for _ in range(R)]
+        res = {}
+        for name, o in [("fused", None), ("unfused", fcc.make_opts(algo=fcc.FCC_ALGO_UNFUSED)),
+                        ("copy_engine", fcc.make_opts(algo=fcc.FCC_ALGO_CE))]:
+            t = time_calls(lambda o=o: fcc.fcc_gemm_ar(R, dA, dB_rs, outs, M, N, K, 0, 0, o, stream),
+                           10, 3, stream)
+            res[name] = {"ms": t, "TFLOP/s": w.flops() / (t * 1e-3) / 1e12}
+        res["roofline_frac"] = res["fused"]["TFLOP/s"] / tc
+        ops[w.name] = res
+        del outs, dA
 
     # GEMV + AllReduce (decode); B_r reuses the RS leg's 3584x8192 N(0, 0.02) weights
-    w = synth.WORKLOADS["gemv_ar_r8_8x8192x3584"]
-    R, M, N, K = w.R, w.M, w.N, w.K
-    rng = np.random.Generator(np.random.PCG64(7))
-    dA = [up(synth.normal_bf16(rng, (M, K), 1.0)) for _ in range(R)]
-    outs = [torch.empty((M, N), dtype=torch.float32, device=dev) for _ in range(R)]
-    byts = R * (K * N * 2 + M * K * 2 + M * N * 4)
-    res = {}
-    for name, o in [("fused", None), ("unfused", fcc.make_opts(algo=fcc.FCC_ALGO_UNFUSED)),
-                    ("copy_engine", fcc.make_opts(algo=fcc.FCC_ALGO_CE))]:
-        t = time_calls(lambda o=o: fcc.fcc_gemv_ar(R, dA, dB_rs, outs, M, N, K, 0, 2, o, stream),
-                       50, 5, stream)
-        res[name] = {"us": t * 1e3, "GB/s": byts / (t * 1e-3) / 1e9}
-    res["roofline_frac"] = res["fused"]["GB/s"] / hbm
-    res["algorithmic_bytes"] = byts
-    ops[w.name] = res
-    del outs, dA
+    if want("gemv_ar_r8_8x8192x3584"):
+        w = synth.WORKLOADS["gemv_ar_r8_8x8192x3584"]
+        R, M, N, K = w.R, w.M, w.N, w.K
+        rng = np.random.Generator(np.random.PCG64(7))
+        dA = [up(synth.normal_bf16(rng, (M, K), 1.0)) for _ in range(R)]
+        outs = [torch.empty((M, N), dtype=torch.float32, device=dev) for _ in range(R)]
+        byts = R * (K * N * 2 + M * K * 2 + M * N * 4)
+        res = {}
+        for name, o in [("fused", None), ("unfused", fcc.make_opts(algo=fcc.FCC_ALGO_UNFUSED)),
+                        ("copy_engine", fcc.make_opts(algo=fcc.FCC_ALGO_CE))]:
+            t = time_calls(lambda o=o: fcc.fcc_gemv_ar(R, dA, dB_rs, outs, M, N, K, 0, 2, o, stream),
+                           50, 5, stream)
+            res[name] = {"us": t * 1e3, "GB/s": byts / (t * 1e-3) / 1e9}
+        res["roofline_frac"] = res["fused"]["GB/s"] / hbm
+        res["algorithmic_bytes"] = byts
+        ops[w.name] = res
+        del outs, dA
 
     # AllGather + GEMM
-    w = synth.WORKLOADS["ag_gemm_r8_8192x3584x8192"]
-    R, M, N, K = w.R, w.M, w.N, w.K
-    X, Bx = synth.gemm_inputs(R, M // R, N, K, w.std_a, w.std_b, seed=0)
-    dX = [up(x) for x in X]
-    dBx = [up(b) for b in Bx]
-    outs = [torch.empty((M, N), dtype=torch.bfloat16, device=dev) for _ in range(R)]
-    res = {}
-    for name, o in [("fused", None), ("unfused", fcc.make_opts(algo=fcc.FCC_ALGO_UNFUSED)),
-                    ("copy_engine", fcc.make_opts(algo=fcc.FCC_ALGO_CE))]:
-        t = time_calls(lambda o=o: fcc.fcc_ag_gemm(R, dX, dBx, outs, None, M, N, K, 0, 0, o,
-                                                   stream), 10, 3, stream)
-        res[name] = {"ms": t, "TFLOP/s": w.flops() / (t * 1e-3) / 1e12}
-    res["roofline_frac"] = res["fused"]["TFLOP/s"] / tc
-    ops[w.name] = res
-    del outs, dX, dBx
+    if want("ag_gemm_r8_8192x3584x8192"):
+        w = synth.WORKLOADS["ag_gemm_r8_8192x3584x8192"]
+        R, M, N, K = w.R, w.M, w.N, w.K
+        X, Bx = synth.gemm_inputs(R, M // R, N, K, w.std_a, w.std_b, seed=0)
+        dX = [up(x) for x in X]
+        dBx = [up(b) for b in Bx]
+        outs = [torch.empty((M, N), dtype=torch.bfloat16, device=dev) for _ in range(R)]
+        res = {}
+        for name, o in [("fused", None), ("unfused", fcc.make_opts(algo=fcc.FCC_ALGO_UNFUSED)),
+                        ("copy_engine", fcc.make_opts(algo=fcc.FCC_ALGO_CE))]:
+            t = time_calls(lambda o=o: fcc.fcc_ag_gemm(R, dX, dBx, outs, None, M, N, K, 0, 0, o,
+                                                       stream), 10, 3, stream)
+            res[name] = {"ms": t, "TFLOP/s": w.flops() / (t * 1e-3) / 1e12}
+        res["roofline_frac"] = res["fused"]["TFLOP/s"] / tc
+        ops[w.name] = res
+        del outs, dX, dBx
 
     # MoE route + dispatch + grouped expert GEMM
-    w = synth.WORKLOADS["moe_r8_t4096_h4096_e64_f1408"]
-    R, T, H, F, E, topk = w.R, w.T, w.H, w.F, w.E, w.topk
-    X, logits, Wt = synth.moe_inputs(R, T, H, E, F, std_x=w.std_a, std_w=w.std_b, seed=0)
-    Xall = up(np.concatenate(X))           # the sources as one [R*T, H] array
-    dX = [Xall[s * T:(s + 1) * T] for s in range(R)]
-    dL = [torch.from_numpy(l).to(dev) for l in logits]
-    dW = [up(x) for x in Wt]
-    cap = 2 * T * topk
-    recv_y = [torch.empty((cap, F), dtype=torch.bfloat16, device=dev) for _ in range(R)]
-    recv_x = [torch.empty((cap, H), dtype=torch.bfloat16, device=dev) for _ in range(R)]
-    idx = [torch.empty((T, topk), dtype=torch.int32, device=dev) for _ in range(R)]
-    gate = [torch.empty((T, topk), dtype=torch.float32, device=dev) for _ in range(R)]
-    counts = torch.empty((E,), dtype=torch.int32, device=dev)
-    send = torch.empty((R * R,), dtype=torch.int32, device=dev)
-    src = [torch.empty((cap,), dtype=torch.int32, device=dev) for _ in range(R)]
+    if want("moe_r8_t4096_h4096_e64_f1408"):
+        w = synth.WORKLOADS["moe_r8_t4096_h4096_e64_f1408"]
+        R, T, H, F, E, topk = w.R, w.T, w.H, w.F, w.E, w.topk
+        X, logits, Wt = synth.moe_inputs(R, T, H, E, F, std_x=w.std_a, std_w=w.std_b, seed=0)
+        Xall = up(np.concatenate(X))           # the sources as one [R*T, H] array
+        dX = [Xall[s * T:(s + 1) * T] for s in range(R)]
+        dL = [torch.from_numpy(l).to(dev) for l in logits]
+        dW = [up(x) for x in Wt]
+        cap = 2 * T * topk
+        recv_y = [torch.empty((cap, F), dtype=torch.bfloat16, device=dev) for _ in range(R)]
+        recv_x = [torch.empty((cap, H), dtype=torch.bfloat16, device=dev) for _ in range(R)]
+        idx = [torch.empty((T, topk), dtype=torch.int32, device=dev) for _ in range(R)]
+        gate = [torch.empty((T, topk), dtype=torch.float32, device=dev) for _ in range(R)]
+        counts = torch.empty((E,), dtype=torch.int32, device=dev)
+        send = torch.empty((R * R,), dtype=torch.int32, device=dev)
+        src = [torch.empty((cap,), dtype=torch.int32, device=dev) for _ in range(R)]
 
-    def moe(rx=None, o=None):
-        fcc.fcc_moe_dispatch_gemm(R, dX, dL, dW, T, H, F, E, topk, rx, recv_y, cap, idx,
-                                  gate, counts, send, src, 0, 0, o, stream)
+        def moe(rx=None, o=None):
+            fcc.fcc_moe_dispatch_gemm(R, dX, dL, dW, T, H, F, E, topk, rx, recv_y, cap, idx,
+                                      gate, counts, send, src, 0, 0, o, stream)
 
-    t = time_calls(moe, 10, 3, stream)
-    og = fcc.make_opts(algo=fcc.FCC_ALGO_FUSED)
-    tg = time_calls(lambda: moe(None, og), 5, 2, stream)
-    tx = time_calls(lambda: moe(recv_x, og), 5, 2, stream)
-    # algorithmic bytes: X once, logits once, W once, Y once (indices negligible)
-    byts = R * T * H * 2 + R * T * E * 4 + E * H * F * 2 + R * T * topk * F * 2
+        t = time_calls(moe, 10, 3, stream)
+        og = fcc.make_opts(algo=fcc.FCC_ALGO_FUSED)
+        tg = time_calls(lambda: moe(None, og), 5, 2, stream)
+        tx = time_calls(lambda: moe(recv_x, og), 5, 2, stream)
+        # algorithmic bytes: X once, logits once, W once, Y once (indices negligible)
+        byts = R * T * H * 2 + R * T * E * 4 + E * H * F * 2 + R * T * topk * F * 2
 
-    def leg(ms, path):
-        return {"ms": ms, "TFLOP/s": w.flops() / (ms * 1e-3) / 1e12, "path": path}
+        def leg(ms, path):
+            return {"ms": ms, "TFLOP/s": w.flops() / (ms * 1e-3) / 1e12, "path": path}
 
-    res = {"fused": leg(t, "route, dispatch copy into workspace, grouped GEMM on the copy"),
-           "gather_in_gemm": leg(tg, "route, grouped GEMM gathering its rows by TMA gather4"),
-           "gather_with_recv_x": leg(tx, "the same, recv_x copied on a side stream beside "
-                                         "the GEMM"),
-           "roofline_frac": (w.flops() / (t * 1e-3) / 1e12) / tc,
-           "algorithmic_bytes": byts}
-    ops[w.name] = res
-    del Xall, dX, dL, dW, recv_y, recv_x
+        res = {"fused": leg(t, "route, dispatch copy into workspace, grouped GEMM on the copy"),
+               "gather_in_gemm": leg(tg, "route, grouped GEMM gathering its rows by TMA gather4"),
+               "gather_with_recv_x": leg(tx, "the same, recv_x copied on a side stream beside "
+                                             "the GEMM"),
+               "roofline_frac": (w.flops() / (t * 1e-3) / 1e12) / tc,
+               "algorithmic_bytes": byts}
+        ops[w.name] = res
+        del Xall, dX, dL, dW, recv_y, recv_x
+
     st = fcc.fcc_stream_status(stream)
     if st != fcc.FCC_OK:
         raise RuntimeError(f"device status after the operator legs: {fcc.fcc_status_string(st)}")
@@ -471,6 +483,19 @@ def run_fcc(args, world, rank, local, pg):
 
     def step():
         fcc.fcc_gemm_rs(R, dA, dB, outs, M, N, K, fcc.FCC_BF16, fcc.FCC_BF16, None, stream)
+
+    if args.op is not None:
+        # One operator leg alone (no headline, no baselines).
+        if args.op == "gemm_rs_r2_256x256x128":
+            res = small_rs_latency(fcc, torch, np, synth, dev, stream)
+        else:
+            res = other_ops(fcc, torch, np, synth, dev, stream, dA, dB, pk, only=args.op)
+            if args.op not in res:
+                raise SystemExit(f"unknown --op {args.op}")
+            res = res[args.op]
+        if rank == 0:
+            print(json.dumps({"op": args.op, "result": res}), flush=True)
+        return
 
     # ---- headline: device-resident inputs
     clocks = ClockSampler(local)

@@ -236,13 +236,27 @@ fcc_status gemm_params(GemmParams& p, DeviceState* d, int mode, int R, const voi
     default:
       return FCC_ERR_INVALID;
   }
+  p.split_first = p.num_tiles;  // no half tiles unless run_gemm makes them
   return FCC_OK;
 }
 
-fcc_status run_gemm(const GemmParams& p, int mode, DeviceState* d, const fcc_opts* o,
+fcc_status run_gemm(const GemmParams& p0, int mode, DeviceState* d, const fcc_opts* o,
                     cudaStream_t st) {
-  if (p.num_tiles <= 0) return FCC_OK;
-  // Grid in CTAs: one CTA (or CTA pair) per SM (pair of SMs), at most one per tile.
+  if (p0.num_tiles <= 0) return FCC_OK;
+  GemmParams p = p0;
+  // Tiles go round-robin over `slots` CTAs (CTA pairs).  When the last round
+  // would hold at most half a round of tiles, each of those tiles runs as two
+  // 128-column halves on two slots, so the round takes half a tile's time.
+  // A half keeps the tile's whole K loop: the results are unchanged.
+  const int slots = std::max(1, grid_for(d, o, INT64_MAX) / p.cg);
+  const int rem = p.num_tiles % slots;
+  p.split_first = p.num_tiles;
+  if ((mode == MODE_RS || mode == MODE_AR || mode == MODE_AG || mode == MODE_PARTIAL) &&
+      rem > 0 && 2 * rem <= slots) {
+    p.split_first = p.num_tiles - rem;
+    p.num_tiles += rem;
+  }
+  // Grid in CTAs: one CTA (or CTA pair) per SM (pair of SMs), at most one per work item.
   int grid = grid_for(d, o, static_cast<int64_t>(p.num_tiles) * p.cg);
   grid = std::max(p.cg, (grid / p.cg) * p.cg);
   cudaError_t e = launch_gemm(p, mode, p.cg, grid, st);
@@ -523,7 +537,7 @@ fcc_status fcc_gemv_ar(int R, const void* const* A, const void* const* B, void* 
   GemvParams p;
   std::memset(&p, 0, sizeof(p));
   for (int r = 0; r < R; ++r) {
-    if ((s = make_map(&p.mapA[r], A[r], M, K, kBM)) != FCC_OK) return s;
+    if ((s = make_map(&p.mapA[r], A[r], M, K, kGemvTok)) != FCC_OK) return s;
     if ((s = make_map(&p.mapB[r], B[r], K, N, kBK)) != FCC_OK) return s;
     p.out[r] = out[r];
   }

@@ -53,7 +53,7 @@ template <int CG>
 struct Cfg {
   static constexpr int kTileM = kBM * CG;                   // rows of one (pair) tile
   static constexpr int kBNcta = kBN / CG;                   // B columns this CTA loads
-  static constexpr int kStages = CG == 2 ? 6 : 4;
+  static constexpr int kStages = CG == 2 ? 7 : 4;
   static constexpr uint32_t kBBytes = kBK * kBNcta * 2;     // 32 or 16 KiB
   static constexpr uint32_t kStageBytes = kABytes + kBBytes;
   static constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(kTileM, kBN, false, true);
@@ -71,6 +71,7 @@ struct Tile {
   int expert;  // GROUPED: expert of the tile
   int row0;    // GROUPED: first receive-buffer row of the tile
   int rows;    // GROUPED: valid rows of the tile
+  int half;    // -1: the whole 256-column tile; 0 / 1: its first / second 128 columns
 };
 
 __device__ __forceinline__ void raster(int t, int tiles_m, int tiles_n, int group, int& mt,
@@ -111,6 +112,16 @@ __device__ __forceinline__ Tile tile_of(const P& p, int t) {
   tl.expert = 0;
   tl.row0 = 0;
   tl.rows = 0;
+  tl.half = -1;
+  if constexpr (MODE == MODE_RS || MODE == MODE_AR || MODE == MODE_AG || MODE == MODE_PARTIAL) {
+    // Work items from split_first on are halves of the last round's tiles
+    // (two per tile), so that round takes half a tile's time.
+    if (t >= p.split_first) {
+      const int h = t - p.split_first;
+      t = p.split_first + (h >> 1);
+      tl.half = h & 1;
+    }
+  }
   if constexpr (MODE == MODE_GROUPED) {
     // Expert of tile t: the last e with tile_start[e] <= t (binary search).
     t += __ldcg(p.tile_start + p.e_lo);
@@ -244,9 +255,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
   }
   const int num_tiles = num_tiles_of<MODE>(p);
   const int k_iters = k_iters_of<MODE>(p);
-  // Narrow tile: the output's last columns fit in the first half of the
-  // 256-wide tile, so the B loads, the MMA width and the epilogue are halved.
-  auto narrow = [&](int nt) { return p.N - nt * kBN <= kBN / 2; };
+  // Narrow tile: a half tile, or one whose output columns end in the first
+  // half of its 256, so the B loads, the MMA width and the epilogue are halved.
+  auto narrow = [&](const Tile& tl) { return tl.half >= 0 || p.N - tl.nt * kBN <= kBN / 2; };
+  auto col_base = [&](const Tile& tl) { return tl.nt * kBN + (tl.half > 0 ? kBN / 2 : 0); };
   if (warp == 1) {
     if constexpr (CG == 2) {
       ptx::tmem_alloc_pair(tmem_slot, kTmemCols);
@@ -280,8 +292,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
       const CUtensorMap* ma = &p.mapA[0];
       for (int t = pair; t < num_tiles && ok; t += npairs) {
         const Tile tl = tile_of<MODE, TM>(p, t);
-        const int bn_cta = narrow(tl.nt) ? C::kBNcta / 2 : C::kBNcta;
-        const int b_col = tl.nt * kBN + static_cast<int>(cta) * bn_cta;
+        const int bn_cta = narrow(tl) ? C::kBNcta / 2 : C::kBNcta;
+        const int b_col = col_base(tl) + static_cast<int>(cta) * bn_cta;
         const uint32_t stage_bytes = kABytes + static_cast<uint32_t>(bn_cta) * kBK * 2;
         // Source rows of this lane's four A rows; padding rows read row 0 (their
         // results are never stored).
@@ -350,8 +362,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
           a_row = tl.mt * TM;
         }
         a_row += static_cast<int>(cta) * kBM;                 // this CTA's half of the rows
-        const int bn_cta = narrow(tl.nt) ? C::kBNcta / 2 : C::kBNcta;  // B columns of this CTA
-        const int b_col = tl.nt * kBN + static_cast<int>(cta) * bn_cta;
+        const int bn_cta = narrow(tl) ? C::kBNcta / 2 : C::kBNcta;  // B columns of this CTA
+        const int b_col = col_base(tl) + static_cast<int>(cta) * bn_cta;
         const uint32_t stage_bytes = kABytes + static_cast<uint32_t>(bn_cta) * kBK * 2;
         int r = (tl.rank >= 0) ? tl.rank : 0;
         int kb = 0;
@@ -406,7 +418,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
       uint32_t acc = 0, acc_phase = 0;
       bool any = false, ok = true;
       for (int t = pair; t < num_tiles && ok; t += npairs) {
-        const uint32_t idesc = narrow(tile_of<MODE, TM>(p, t).nt) ? C::kIdescNarrow : C::kIdesc;
+        const uint32_t idesc = narrow(tile_of<MODE, TM>(p, t)) ? C::kIdescNarrow : C::kIdesc;
         if (!W.wait(&tempty[acc], acc_phase ^ 1u)) break;
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * kBN;
@@ -503,8 +515,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
       }
 
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kBN;
-      const int col0 = tl.nt * kBN;
-      const int cend = narrow(tl.nt) ? kBN / 2 : kBN;  // accumulator columns written
+      const int col0 = col_base(tl);
+      const int cend = narrow(tl) ? kBN / 2 : kBN;  // accumulator columns written
 #pragma unroll 1
       for (int c = 0; c < cend; c += 32) {
         uint32_t v[32];

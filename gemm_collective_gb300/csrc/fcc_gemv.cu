@@ -8,11 +8,14 @@
 // B across all groups at the same time, so B is read in whole rows.
 //
 // Each stage is one 64-row block of 256 columns (32 KiB, four TMA boxes) plus
-// the token rows of that block, loaded as a 128-row TMA box whose rows past M
-// are filled with zeros.  One tcgen05.mma per 16 k (M = 128 token rows, N =
-// 256 columns) accumulates into one of the group's two TMEM accumulators, so
-// the tensor core does little work per byte and keeps up with HBM; TMEM lane t
-// holds token t's row.
+// the 16 token rows of that block (2 KiB, one TMA box; rows past M read as
+// zeros).  One tcgen05.mma per 16 k (M = 128 rows, N = 256 columns)
+// accumulates into one of the group's two TMEM accumulators; TMEM lane t holds
+// token t's row.  The MMA's A operand is 128 rows, of which only the first 16
+// are loaded: rows 16-127 read whatever shared memory follows (later stages),
+// and each output row depends on its own A row only, so those lanes hold
+// values nobody reads.  The stage thus costs 34 KiB instead of 48, and six
+// stages (204 KiB of B in flight) fit where four did.
 //
 // Cross-CTA sum: each CTA writes its f32 partial rows for the group to its
 // own workspace slot and takes the group's ticket; the last to arrive adds the
@@ -34,22 +37,28 @@ namespace {
 
 constexpr int kGroupCols = 512;                 // columns per CTA group (two accumulators)
 constexpr int kStageCols = 256;                 // columns per pipeline stage (UMMA N)
-constexpr int kTok = 16;                        // tokens handled (M <= 16)
-constexpr int kStages = 4;
+constexpr int kTok = kGemvTok;                  // token rows loaded per stage (M <= 16)
+constexpr int kTokStep = 8;                     // tokens per step of the final sum
+constexpr int kStages = 6;
 constexpr uint32_t kBBox = kBK * 64 * 2;        // [64 k][64 n] bf16 = 8 KiB
 constexpr uint32_t kBStage = 4 * kBBox;         // 32 KiB: [64 k][256 n]
-constexpr uint32_t kAStage = kBM * kBK * 2;     // 16 KiB: [128 rows][64 k], rows >= M zero
+constexpr uint32_t kAStage = kTok * kBK * 2;    // 2 KiB: [16 rows][64 k], rows >= M zero
 constexpr uint32_t kStageBytes = kBStage + kAStage;
 constexpr uint32_t kTmemCols = 512;             // 2 accumulators x 256 columns
 constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(kBM, kStageCols, /*a_mn=*/false, /*b_mn=*/true);
 constexpr uint64_t kDrainNs = 50ull * 1000 * 1000;
 constexpr int kSmemBytes = 1024 + kStages * kStageBytes + (2 * kStages + 4) * 8 + 16;
+// The MMA reads 128 A rows (16 KiB) from each A stage: for the last one they
+// run on into the B stages, which must therefore follow within the buffer.
+static_assert((kStages - 1) * kAStage + kBM * kBK * 2 <= kStages * kStageBytes,
+              "A operand read past the stages");
+static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 
 __global__ void __launch_bounds__(kGemmThreads, 1) gemv_ar_kernel(const __grid_constant__ GemvParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  uint8_t* sA = smem;                          // kStages x 16 KiB
+  uint8_t* sA = smem;                          // kStages x 2 KiB (MMA reads 16 KiB from each)
   uint8_t* sB = smem + kStages * kAStage;      // kStages x 32 KiB
   uint64_t* bars = reinterpret_cast<uint64_t*>(sB + kStages * kBStage);
   uint64_t* full = bars;
@@ -146,7 +155,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemv_ar_kernel(const __grid_c
           const uint32_t b_addr = ptx::smem_addr(sB + stage * kBStage);
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk) {
-            // A = the token rows (zero past M): K-major, 32 B per 16 k.
+            // A = the token rows (zero past M, unread lanes past 16): K-major, 32 B per 16 k.
             const uint64_t ad = ptx::smem_desc_sw128(a_addr + kk * 32, 16, 1024);
             // B = 256 columns: MN-major, 16 k-rows per step, 64-column atoms 8 KiB apart.
             const uint64_t bd = ptx::smem_desc_sw128(b_addr + kk * 2048, kBBox, 1024);
@@ -216,27 +225,59 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemv_ar_kernel(const __grid_c
       ptx::named_barrier_sync(1, 128);
       if (*bcast) {
         // Last of the group: sum the splits' partials in split order; each
-        // thread handles 4 consecutive columns (one 16-byte load per partial).
+        // thread handles 4 consecutive columns (one 16-byte load per partial)
+        // of up to 8 tokens at a time, two splits per step, so 16 loads are in
+        // flight instead of one: this sum is the kernel's serial tail.
         __threadfence();
         const int c = ep_tid * 4;
         if (c < ncols) {
           const float* base = p.partials + static_cast<long long>(g) * p.splits * p.M * kGroupCols;
-          for (int t = 0; t < p.M; ++t) {
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int sp = 0; sp < p.splits; ++sp) {
-              const float4 x = __ldcg(reinterpret_cast<const float4*>(
-                  base + (static_cast<long long>(sp) * p.M + t) * kGroupCols + c));
-              acc.x += x.x; acc.y += x.y; acc.z += x.z; acc.w += x.w;
+          auto part = [&](int sp, int t) {
+            return __ldcg(reinterpret_cast<const float4*>(
+                base + (static_cast<long long>(sp) * p.M + t) * kGroupCols + c));
+          };
+          auto add = [](float4& a, const float4& x) {
+            a.x += x.x; a.y += x.y; a.z += x.z; a.w += x.w;
+          };
+          for (int t0 = 0; t0 < p.M; t0 += kTokStep) {
+            const int nt = min(kTokStep, p.M - t0);
+            float4 acc[kTokStep];
+#pragma unroll
+            for (int i = 0; i < kTokStep; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            int sp = 0;
+            for (; sp + 2 <= p.splits; sp += 2) {
+              float4 x0[kTokStep], x1[kTokStep];
+#pragma unroll
+              for (int i = 0; i < kTokStep; ++i)
+                if (i < nt) {
+                  x0[i] = part(sp, t0 + i);
+                  x1[i] = part(sp + 1, t0 + i);
+                }
+#pragma unroll
+              for (int i = 0; i < kTokStep; ++i)
+                if (i < nt) {
+                  add(acc[i], x0[i]);
+                  add(acc[i], x1[i]);
+                }
             }
-            const long long o = static_cast<long long>(t) * p.N + col0 + c;
-            for (int r = 0; r < p.R; ++r) {
-              if (p.out_f32) {
-                *reinterpret_cast<float4*>(static_cast<float*>(p.out[r]) + o) = acc;
-              } else {
-                uint2 w;
-                w.x = ptx::pack_bf16x2(acc.x, acc.y);
-                w.y = ptx::pack_bf16x2(acc.z, acc.w);
-                *reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.out[r]) + o) = w;
+            if (sp < p.splits) {
+#pragma unroll
+              for (int i = 0; i < kTokStep; ++i)
+                if (i < nt) add(acc[i], part(sp, t0 + i));
+            }
+#pragma unroll
+            for (int i = 0; i < kTokStep; ++i) {
+              if (i >= nt) break;
+              const long long o = static_cast<long long>(t0 + i) * p.N + col0 + c;
+              for (int r = 0; r < p.R; ++r) {
+                if (p.out_f32) {
+                  *reinterpret_cast<float4*>(static_cast<float*>(p.out[r]) + o) = acc[i];
+                } else {
+                  uint2 w;
+                  w.x = ptx::pack_bf16x2(acc[i].x, acc[i].y);
+                  w.y = ptx::pack_bf16x2(acc[i].z, acc[i].w);
+                  *reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.out[r]) + o) = w;
+                }
               }
             }
           }
@@ -398,7 +439,7 @@ extern "C" fcc_status fcc_gemv_ar_static(int R, const void* const* A, const void
   GemvParams p;
   std::memset(&p, 0, sizeof(p));
   for (int r = 0; r < R; ++r) {
-    if ((s = light_make_map(&p.mapA[r], A[r], M, K, kBM)) != FCC_OK) return s;
+    if ((s = light_make_map(&p.mapA[r], A[r], M, K, kTok)) != FCC_OK) return s;
     if ((s = light_make_map(&p.mapB[r], B[r], K, N, kBK)) != FCC_OK) return s;
     p.out[r] = out[r];
   }

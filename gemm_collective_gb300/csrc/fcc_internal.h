@@ -14,6 +14,7 @@ namespace fcc {
 constexpr int kBM = 128;       // output tile rows (one TMEM lane per row)
 constexpr int kBK = 64;        // K per pipeline stage (128 bytes of bf16: one swizzle row)
 constexpr int kGemmThreads = 192;  // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
+constexpr int kGemvTok = 16;   // GEMV: token rows per TMA box (M <= 16)
 
 enum GemmMode : int {
   MODE_RS = 0,         // reduce-scatter, ordered tile-owner accumulation over ranks
@@ -34,7 +35,8 @@ struct GemmParams {
   int Ms;               // rows per shard (RS, AG)
   int m_begin, m_end;   // row window (PARTIAL; others 0..M)
   int tiles_m, tiles_n; // tile grid of one rank's output
-  int num_tiles;
+  int num_tiles;        // work items: whole tiles, then the halves from split_first on
+  int split_first;      // RS/AR/AG/PARTIAL: first half-tile item (= num_tiles: none)
   int k_iters;          // pipeline stages per tile
   int kb_per_rank;      // ceil(K / kBK)
   int out_f32;          // output storage: 1 = f32, 0 = bf16
@@ -47,7 +49,7 @@ struct GemmParams {
 };
 
 struct GemvParams {
-  CUtensorMap mapA[FCC_MAX_RANKS];  // [M, K], rows padded to 128 by out-of-bounds fill
+  CUtensorMap mapA[FCC_MAX_RANKS];  // [M, K], box of 16 rows (rows past M read as zeros)
   CUtensorMap mapB[FCC_MAX_RANKS];  // [K, N]
   void* out[FCC_MAX_RANKS];
   int R, M, N, K;

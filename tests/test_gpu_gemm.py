@@ -125,6 +125,25 @@ def test_ar_all_buffers_identical_and_equal_rs(R, M, N, K, pair):
         assert np.array_equal(cat, bits(outs[0])), "RS shards != AR rows (deterministic mode)"
 
 
+@pytest.mark.parametrize("pair", [1, 2])
+@pytest.mark.parametrize("op", ["rs", "ar"])
+def test_last_round_half_tiles_bit_identical(op, pair):
+    """The last round's tiles run as two 128-column halves when they fill at most
+    half the grid.  16 pair tiles (32 single-CTA tiles) on 10 CTAs leave 1 (2) in
+    the last round and are split; on 8 CTAs nothing is left over.  Integer inputs
+    keep every partial sum exact: both equal the oracle bit for bit."""
+    R, M, N, K = 2, 1024, 1024, 128
+    A, B = synth.integer_gemm_inputs(R, M, N, K, -4, 4, seed=11)
+    dA, dB = _upload(A, B)
+    run = _rs if op == "rs" else _ar
+    split = run(R, dA, dB, M, N, K, fcc.FCC_F32, fcc.make_opts(cta_pair=pair, max_ctas=10))
+    whole = run(R, dA, dB, M, N, K, fcc.FCC_F32, fcc.make_opts(cta_pair=pair, max_ctas=8))
+    for j in range(R):
+        assert np.array_equal(bits(split[j]), bits(whole[j])), f"buffer {j}"
+        ref = oracle.gemm_rs(A, B, j) if op == "rs" else oracle.gemm_ar(A, B)
+        assert np.array_equal(to_f64(split[j]), ref), f"buffer {j} vs oracle"
+
+
 def test_rank_permutation_within_tolerance():
     R, M, N, K = 4, 256, 512, 128
     A, B = synth.gemm_inputs(R, M, N, K, 1.0, 1.0, seed=5)
