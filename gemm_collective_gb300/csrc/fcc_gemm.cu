@@ -49,6 +49,11 @@ constexpr uint32_t kBBoxBytes = kBK * 64 * 2;       // 8 KiB: [64 k][64 n]
 constexpr uint32_t kTmemCols = 2 * kBN;             // double-buffered accumulator
 constexpr uint64_t kDrainNs = 50ull * 1000 * 1000;  // unwinding limit after an abort
 
+// Grouped mode: tile_start[0..E], expert_rows[0..E), expert_base[0..E) copied
+// into shared memory once per CTA, so finding a tile's expert (a binary search)
+// costs no global-memory round trips on the producer's or the MMA warp's path.
+constexpr int kTabInts = 3 * FCC_MAX_EXPERTS + 1;
+
 template <int CG>
 struct Cfg {
   static constexpr int kTileM = kBM * CG;                   // rows of one (pair) tile
@@ -59,9 +64,10 @@ struct Cfg {
   static constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(kTileM, kBN, false, true);
   // A tile whose columns end in the first half of its 256 runs 128 wide.
   static constexpr uint32_t kIdescNarrow = ptx::idesc_bf16_f32(kTileM, kBN / 2, false, true);
-  // ... + barriers + flags.
+  // ... + barriers + flags + the grouped mode's expert tables.
   static constexpr int kSmem = 1024 + kStages * static_cast<int>(kStageBytes) +
-                               (2 * kStages + 5) * 8 + 16;
+                               (2 * kStages + 5) * 8 + 16 + kTabInts * 4;
+  static_assert(kSmem <= 232448, "shared memory per CTA");
 };
 
 struct Tile {
@@ -86,10 +92,10 @@ __device__ __forceinline__ void raster(int t, int tiles_m, int tiles_n, int grou
 }
 
 template <int MODE, class P>
-__device__ __forceinline__ int num_tiles_of(const P& p) {
+__device__ __forceinline__ int num_tiles_of(const P& p, const int* tab) {
   if constexpr (MODE == MODE_GROUPED) {
     // Tiles of experts [e_lo, e_hi); the table is written by the dispatch kernels.
-    return __ldcg(p.tile_start + p.e_hi) - __ldcg(p.tile_start + p.e_lo);
+    return tab[p.e_hi] - tab[p.e_lo];
   } else {
     return p.num_tiles;
   }
@@ -105,7 +111,7 @@ __device__ __forceinline__ int k_iters_of(const P& p) {
 }
 
 template <int MODE, int TM, class P>
-__device__ __forceinline__ Tile tile_of(const P& p, int t) {
+__device__ __forceinline__ Tile tile_of(const P& p, int t, const int* tab) {
   Tile tl;
   tl.rank = -1;
   tl.shard = 0;
@@ -124,25 +130,28 @@ __device__ __forceinline__ Tile tile_of(const P& p, int t) {
   }
   if constexpr (MODE == MODE_GROUPED) {
     // Expert of tile t: the last e with tile_start[e] <= t (binary search).
-    t += __ldcg(p.tile_start + p.e_lo);
+    const int* ts = tab;                   // tile_start
+    const int* rows = tab + p.E + 1;       // expert_rows
+    const int* base = tab + 2 * p.E + 1;   // expert_base
+    t += ts[p.e_lo];
     int lo = p.e_lo, hi = p.e_hi - 1;
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
-      if (__ldcg(p.tile_start + mid) <= t)
+      if (ts[mid] <= t)
         lo = mid;
       else
         hi = mid - 1;
     }
     const int e = lo;
-    const int rows_e = __ldcg(p.expert_rows + e);
+    const int rows_e = rows[e];
     const int tm = (rows_e + TM - 1) / TM;
-    const int lt = t - __ldcg(p.tile_start + e);
+    const int lt = t - ts[e];
     // m fastest: CTAs running at the same time share the expert's weight slab.
     tl.mt = lt % tm;
     tl.nt = lt / tm;
     tl.expert = e;
     tl.shard = e / p.Eloc;
-    tl.row0 = __ldcg(p.expert_base + e) + tl.mt * TM;
+    tl.row0 = base[e] + tl.mt * TM;
     tl.rows = min(TM, rows_e - tl.mt * TM);
   } else if constexpr (MODE == MODE_RS || MODE == MODE_AR) {
     raster(t, p.tiles_m, p.tiles_n, p.group_m, tl.mt, tl.nt);
@@ -221,6 +230,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* bcast = reinterpret_cast<volatile int*>(tmem_slot + 2);
+  int* tab = reinterpret_cast<int*>(tmem_slot + 4);  // grouped mode: expert tables
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -253,7 +263,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
       if constexpr (MODE != MODE_GROUPED) ptx::tma_prefetch_desc(&p.mapB[r]);
     }
   }
-  const int num_tiles = num_tiles_of<MODE>(p);
+  if constexpr (MODE == MODE_GROUPED) {
+    // The tables were written by the dispatch kernels before this launch.
+    for (int i = threadIdx.x; i <= p.E; i += blockDim.x) tab[i] = __ldcg(p.tile_start + i);
+    for (int i = threadIdx.x; i < p.E; i += blockDim.x) {
+      tab[p.E + 1 + i] = __ldcg(p.expert_rows + i);
+      tab[2 * p.E + 1 + i] = __ldcg(p.expert_base + i);
+    }
+  }
   const int k_iters = k_iters_of<MODE>(p);
   // Narrow tile: a half tile, or one whose output columns end in the first
   // half of its 256, so the B loads, the MMA width and the epilogue are halved.
@@ -277,6 +294,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const ptx::Waiter W{abort_flag, p.status, p.timeout_ns};
+  const int num_tiles = num_tiles_of<MODE>(p, tab);  // (after the barrier: tables loaded)
 
   if (warp == 0 && gather) {
     // ----------------------------------------------- producer, gather mode
@@ -291,7 +309,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
       bool ok = true;
       const CUtensorMap* ma = &p.mapA[0];
       for (int t = pair; t < num_tiles && ok; t += npairs) {
-        const Tile tl = tile_of<MODE, TM>(p, t);
+        const Tile tl = tile_of<MODE, TM>(p, t, tab);
         const int bn_cta = narrow(tl) ? C::kBNcta / 2 : C::kBNcta;
         const int b_col = col_base(tl) + static_cast<int>(cta) * bn_cta;
         const uint32_t stage_bytes = kABytes + static_cast<uint32_t>(bn_cta) * kBK * 2;
@@ -352,7 +370,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
       uint32_t issued = 0, last_parity = 0;
       bool ok = true;
       for (int t = pair; t < num_tiles && ok; t += npairs) {
-        const Tile tl = tile_of<MODE, TM>(p, t);
+        const Tile tl = tile_of<MODE, TM>(p, t, tab);
         int a_row;
         if constexpr (MODE == MODE_GROUPED) {
           a_row = tl.row0;
@@ -418,7 +436,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
       uint32_t acc = 0, acc_phase = 0;
       bool any = false, ok = true;
       for (int t = pair; t < num_tiles && ok; t += npairs) {
-        const uint32_t idesc = narrow(tile_of<MODE, TM>(p, t)) ? C::kIdescNarrow : C::kIdesc;
+        const uint32_t idesc = narrow(tile_of<MODE, TM>(p, t, tab)) ? C::kIdescNarrow : C::kIdesc;
         if (!W.wait(&tempty[acc], acc_phase ^ 1u)) break;
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * kBN;
@@ -474,7 +492,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
     const uint32_t tempty_leader0 = (CG == 2) ? ptx::mapa(ptx::smem_addr(&tempty[0]), 0) : 0u;
     uint32_t acc = 0, acc_phase = 0;
     for (int t = pair; t < num_tiles; t += npairs) {
-      const Tile tl = tile_of<MODE, TM>(p, t);
+      const Tile tl = tile_of<MODE, TM>(p, t, tab);
       const bool failed = !W.wait(&tfull[acc], acc_phase);
       if constexpr (MODE == MODE_RS_PUSH || MODE == MODE_AR_PUSH) {
         // The four epilogue warps meet at named barriers below: stop together.
