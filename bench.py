@@ -346,6 +346,33 @@ def small_rs_latency(fcc, torch, np, synth, dev, stream):
     return res
 
 
+def gemv_size_scan(fcc, torch, np, synth, dev, stream, pk):
+    """The GEMV + AllReduce (8 ranks, 8 tokens, f32 out) at five sizes, fused and
+    plain, beside a device copy of the same bytes: separates the fixed cost of
+    a call from its streaming rate."""
+    R, M = 8, 8
+    rng = np.random.Generator(np.random.PCG64(7))
+    res = {}
+    for N, K in [(8192, 3584), (8192, 7168), (8192, 14336), (16384, 3584), (4096, 3584)]:
+        dA = [torch.from_numpy(synth.normal_bf16(rng, (M, K), 1.0).view(np.int16)).to(dev)
+              for _ in range(R)]
+        dB = [torch.from_numpy(synth.normal_bf16(rng, (K, N), 0.02).view(np.int16)).to(dev)
+              for _ in range(R)]
+        outs = [torch.empty((M, N), dtype=torch.float32, device=dev) for _ in range(R)]
+        byts = R * (K * N * 2 + M * K * 2 + M * N * 4)
+        row = {"bytes": byts}
+        for name, o in [("fused", None), ("unfused", fcc.make_opts(algo=fcc.FCC_ALGO_UNFUSED))]:
+            t = time_calls(lambda o=o: fcc.fcc_gemv_ar(R, dA, dB, outs, M, N, K, 0, 2, o, stream),
+                           50, 5, stream)
+            row[name + "_us"] = t * 1e3
+        x = torch.empty(byts // 2, dtype=torch.uint8, device=dev)
+        y = torch.empty_like(x)
+        row["copy_us"] = 1e3 * time_calls(lambda: y.copy_(x), 50, 5, stream)
+        res[f"{N}x{K}"] = row
+        del dA, dB, outs, x, y
+    return res
+
+
 def other_ops(fcc, torch, np, synth, dev, stream, dA_rs, dB_rs, pk, only=None):
     """The other fused operators at their workload sizes, each with its baselines
     (only: the one workload name to run)."""
@@ -488,6 +515,8 @@ def run_fcc(args, world, rank, local, pg):
         # One operator leg alone (no headline, no baselines).
         if args.op == "gemm_rs_r2_256x256x128":
             res = small_rs_latency(fcc, torch, np, synth, dev, stream)
+        elif args.op == "gemv_size_scan":
+            res = gemv_size_scan(fcc, torch, np, synth, dev, stream, pk)
         else:
             res = other_ops(fcc, torch, np, synth, dev, stream, dA, dB, pk, only=args.op)
             if args.op not in res:
@@ -540,26 +569,72 @@ def run_fcc(args, world, rank, local, pg):
                 "algorithmic_bytes_per_launch": float(R * (M * K + K * N) * 2 + M * N * 2)}
 
     # ---- e2e: host buffers, copies inside the timed region
+    # Every step uploads its inputs from pinned host memory and downloads its
+    # result.  Two device buffer sets let step i+1's upload (one copy stream)
+    # and step i-1's download (another) run beside step i's kernel, as a
+    # serving loop would; the timed region spans all steps' copies.
     hA = [torch.from_numpy(a.view(np.int16)).pin_memory() for a in A]
     hB = [torch.from_numpy(b.view(np.int16)).pin_memory() for b in B]
-    hO = [torch.empty((M // R, N), dtype=torch.bfloat16).pin_memory() for _ in range(R)]
+    hO = [[torch.empty((M // R, N), dtype=torch.bfloat16).pin_memory() for _ in range(R)]
+          for _ in range(2)]
     h2d = sum(t.numel() * 2 for t in hA + hB)
-    d2h = sum(t.numel() * 2 for t in hO)
+    d2h = sum(t.numel() * 2 for t in hO[0])
 
-    def e2e_step():
-        for d, h in zip(dA + dB, hA + hB):
-            d.copy_(h, non_blocking=True)
-        step()
-        for h, d in zip(hO, outs):
-            h.copy_(d, non_blocking=True)
+    def e2e_run(n):
+        """n pipelined steps; returns ms per step (CUDA events on the compute stream)."""
+        sets = [(dA, dB, outs), (dA2, dB2, outs2)]
+        up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        ev = lambda: torch.cuda.Event()  # noqa: E731
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        t0.record(stream)
+        up.wait_event(t0)
+        done, fetched = [None, None], [None, None]
+        for i in range(n):
+            a, b, o = sets[i % 2]
+            if done[i % 2] is not None:
+                up.wait_event(done[i % 2])          # step i-2 has finished reading the set
+            with torch.cuda.stream(up):
+                for d, h in zip(a + b, hA + hB):
+                    d.copy_(h, non_blocking=True)
+            ready = ev()
+            ready.record(up)
+            stream.wait_event(ready)
+            if fetched[i % 2] is not None:
+                stream.wait_event(fetched[i % 2])   # step i-2's result is on the host
+            fcc.fcc_gemm_rs(R, a, b, o, M, N, K, fcc.FCC_BF16, fcc.FCC_BF16, None, stream)
+            done[i % 2] = ev()
+            done[i % 2].record(stream)
+            down.wait_event(done[i % 2])
+            with torch.cuda.stream(down):
+                for h, d in zip(hO[i % 2], o):
+                    h.copy_(d, non_blocking=True)
+            fetched[i % 2] = ev()
+            fetched[i % 2].record(down)
+        stream.wait_event(fetched[(n - 1) % 2])
+        if n > 1:
+            stream.wait_event(fetched[n % 2])
+        t1.record(stream)
+        torch.cuda.synchronize()
+        return t0.elapsed_time(t1) / n
 
     e2e = None
     if not args.no_e2e:
+        dA2 = [torch.empty_like(x) for x in dA]
+        dB2 = [torch.empty_like(x) for x in dB]
+        outs2 = [torch.empty_like(x) for x in outs]
         e2e_steps = max(3, min(args.steps, 20))
+        e2e_run(3)  # warm-up
         barrier(pg)
-        e2e_ms = max_over_ranks(time_calls(e2e_step, e2e_steps, 3, stream), pg)
+        e2e_ms = max_over_ranks(e2e_run(e2e_steps), pg)
         e2e = {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+               "pipeline": "two buffer sets; upload, kernel and download on three streams"}
+        # the last step's result came back through the host: check it
+        ref = outs[0].cpu() if (e2e_steps - 1) % 2 == 0 else outs2[0].cpu()
+        if not torch.equal(hO[(e2e_steps - 1) % 2][0], ref):
+            raise RuntimeError("e2e: downloaded result differs from the device result")
+        del dA2, dB2, outs2
     del hA, hB, hO
 
     line = {
