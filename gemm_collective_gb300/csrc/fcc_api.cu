@@ -115,10 +115,16 @@ fcc_algo algo_of(const fcc_opts* o) {
 
 bool deterministic_of(const fcc_opts* o) { return o == nullptr || o->deterministic != 0; }
 
-// Tensor-core tile shape: a CTA pair per 256-row tile unless the rows are few
-// (or the caller forces a shape).
+// Tensor-core tile shape (CTAs per cluster): a CTA pair per 256-row tile
+// unless the rows are few (one CTA per 128-row tile), or the caller's shape.
+// Two pairs sharing multicast B tiles (4) only when asked for: on the 8-rank
+// 8192 x 8192 x 3584 reduce-scatter they ran 2.51 ms against 2.10-2.28 ms for
+// single pairs (burst) and 2.41 against 2.37 ms (400 calls), as each stage
+// then waits for both pairs' MMAs.  gemm_params falls back from 4 to 2 where
+// the mode or tile count rules it out.
 int choose_cg(const fcc_opts* o, int64_t rows) {
-  if (o != nullptr && (o->cta_pair == 1 || o->cta_pair == 2)) return o->cta_pair;
+  if (o != nullptr && (o->cta_pair == 1 || o->cta_pair == 2 || o->cta_pair == 4))
+    return o->cta_pair;
   return rows > kBM ? 2 : 1;
 }
 
@@ -204,13 +210,23 @@ fcc_status gemm_params(GemmParams& p, DeviceState* d, int mode, int R, const voi
   const int tn = static_cast<int>(cdiv(N, kGemmBN));
   const int64_t rows = (mode == MODE_AG) ? Ms : (mode == MODE_PARTIAL ? m_end - m_begin : M);
   p.cg = choose_cg(o, rows);
-  const int64_t tm = static_cast<int64_t>(kBM) * p.cg;
+  if (p.cg == 4) {
+    // Two pairs per cluster take the m tiles 2i, 2i+1 of one tile column: the
+    // modes without tickets, with an even number of 256-row tiles.
+    const int64_t tm2 = cdiv(rows, 2 * kBM);
+    const bool even = mode == MODE_AG ? (R * tm2) % 2 == 0 : tm2 % 2 == 0;
+    if (!(mode == MODE_RS || mode == MODE_AR || mode == MODE_AG || mode == MODE_PARTIAL) ||
+        !even)
+      p.cg = 2;
+  }
+  const int64_t tm = static_cast<int64_t>(kBM) * std::min(p.cg, 2);
+  const int sup = p.cg == 4 ? 2 : 1;  // m tiles per work unit
   switch (mode) {
     case MODE_RS:
     case MODE_AR:
       p.tiles_m = static_cast<int>(cdiv(M, tm));
       p.tiles_n = tn;
-      p.num_tiles = p.tiles_m * p.tiles_n;
+      p.num_tiles = p.tiles_m / sup * p.tiles_n;
       p.k_iters = R * p.kb_per_rank;
       break;
     case MODE_RS_PUSH:
@@ -223,13 +239,13 @@ fcc_status gemm_params(GemmParams& p, DeviceState* d, int mode, int R, const voi
     case MODE_PARTIAL:
       p.tiles_m = static_cast<int>(cdiv(m_end - m_begin, tm));
       p.tiles_n = tn;
-      p.num_tiles = R * p.tiles_m * p.tiles_n;
+      p.num_tiles = R * (p.tiles_m / sup) * p.tiles_n;
       p.k_iters = p.kb_per_rank;
       break;
     case MODE_AG:
       p.tiles_m = R * static_cast<int>(cdiv(Ms, tm));
       p.tiles_n = R * tn;
-      p.num_tiles = p.tiles_m * p.tiles_n;
+      p.num_tiles = p.tiles_m / sup * p.tiles_n;
       p.k_iters = p.kb_per_rank;
       p.group_m = 8;
       break;
@@ -248,7 +264,9 @@ fcc_status run_gemm(const GemmParams& p0, int mode, DeviceState* d, const fcc_op
   // would hold at most half a round of tiles, each of those tiles runs as two
   // 128-column halves on two slots, so the round takes half a tile's time.
   // A half keeps the tile's whole K loop: the results are unchanged.
-  const int slots = std::max(1, grid_for(d, o, INT64_MAX) / p.cg);
+  // (clusters of 4 must fit in a GPC: at most the device's co-resident count)
+  const int slots = std::max(1, std::min(grid_for(d, o, INT64_MAX) / p.cg,
+                                         gemm_max_clusters(p.cg)));
   const int rem = p.num_tiles % slots;
   p.split_first = p.num_tiles;
   if ((mode == MODE_RS || mode == MODE_AR || mode == MODE_AG || mode == MODE_PARTIAL) &&
@@ -256,9 +274,8 @@ fcc_status run_gemm(const GemmParams& p0, int mode, DeviceState* d, const fcc_op
     p.split_first = p.num_tiles - rem;
     p.num_tiles += rem;
   }
-  // Grid in CTAs: one CTA (or CTA pair) per SM (pair of SMs), at most one per work item.
-  int grid = grid_for(d, o, static_cast<int64_t>(p.num_tiles) * p.cg);
-  grid = std::max(p.cg, (grid / p.cg) * p.cg);
+  // Grid in CTAs: one cluster per slot, at most one per work item.
+  const int grid = p.cg * static_cast<int>(std::min<int64_t>(slots, p.num_tiles));
   cudaError_t e = launch_gemm(p, mode, p.cg, grid, st);
   if (e != cudaSuccess) return FCC_ERR_CUDA;
   g_launches.fetch_add(1);

@@ -37,6 +37,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
+
 #include "fcc_internal.h"
 #include "fcc_ptx.cuh"
 
@@ -54,11 +56,15 @@ constexpr uint64_t kDrainNs = 50ull * 1000 * 1000;  // unwinding limit after an 
 // costs no global-memory round trips on the producer's or the MMA warp's path.
 constexpr int kTabInts = 3 * FCC_MAX_EXPERTS + 1;
 
+// CG = CTAs per cluster: 1 (one CTA per 128x256 tile), 2 (a CTA pair per
+// 256x256 tile) or 4 (two pairs on the tiles of rows 2m and 2m+1 of one tile
+// column, each B box loaded once and multicast to both pairs).
 template <int CG>
 struct Cfg {
-  static constexpr int kTileM = kBM * CG;                   // rows of one (pair) tile
-  static constexpr int kBNcta = kBN / CG;                   // B columns this CTA loads
-  static constexpr int kStages = CG == 2 ? 7 : 4;
+  static constexpr int kPairCtas = CG >= 2 ? 2 : 1;         // CTAs of one MMA
+  static constexpr int kTileM = kBM * kPairCtas;            // rows of one (pair) tile
+  static constexpr int kBNcta = kBN / kPairCtas;            // B columns this CTA holds
+  static constexpr int kStages = CG >= 2 ? 7 : 4;
   static constexpr uint32_t kBBytes = kBK * kBNcta * 2;     // 32 or 16 KiB
   static constexpr uint32_t kStageBytes = kABytes + kBBytes;
   static constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(kTileM, kBN, false, true);
@@ -110,8 +116,10 @@ __device__ __forceinline__ int k_iters_of(const P& p) {
   }
 }
 
-template <int MODE, int TM, class P>
-__device__ __forceinline__ Tile tile_of(const P& p, int t, const int* tab) {
+// SUP: the index t counts super-tiles of two m tiles (rows 2m, 2m+1), of which
+// pair pj of the cluster takes m tile 2m + pj (tiles_m is then even).
+template <int MODE, int TM, bool SUP = false, class P>
+__device__ __forceinline__ Tile tile_of(const P& p, int t, const int* tab, int pj = 0) {
   Tile tl;
   tl.rank = -1;
   tl.shard = 0;
@@ -154,11 +162,21 @@ __device__ __forceinline__ Tile tile_of(const P& p, int t, const int* tab) {
     tl.row0 = base[e] + tl.mt * TM;
     tl.rows = min(TM, rows_e - tl.mt * TM);
   } else if constexpr (MODE == MODE_RS || MODE == MODE_AR) {
-    raster(t, p.tiles_m, p.tiles_n, p.group_m, tl.mt, tl.nt);
+    if constexpr (SUP) {
+      raster(t, p.tiles_m / 2, p.tiles_n, max(1, p.group_m / 2), tl.mt, tl.nt);
+      tl.mt = 2 * tl.mt + pj;
+    } else {
+      raster(t, p.tiles_m, p.tiles_n, p.group_m, tl.mt, tl.nt);
+    }
   } else if constexpr (MODE == MODE_AG) {
     // tiles_m = R * (tiles per shard), tiles_n = R * (tiles per rank)
     int gm, gn;
-    raster(t, p.tiles_m, p.tiles_n, p.group_m, gm, gn);
+    if constexpr (SUP) {
+      raster(t, p.tiles_m / 2, p.tiles_n, max(1, p.group_m / 2), gm, gn);
+      gm = 2 * gm + pj;
+    } else {
+      raster(t, p.tiles_m, p.tiles_n, p.group_m, gm, gn);
+    }
     const int mt_per_shard = p.tiles_m / p.R;
     const int nt_per_rank = p.tiles_n / p.R;
     tl.shard = gm / mt_per_shard;
@@ -166,9 +184,12 @@ __device__ __forceinline__ Tile tile_of(const P& p, int t, const int* tab) {
     tl.rank = gn / nt_per_rank;
     tl.nt = gn - tl.rank * nt_per_rank;
   } else {
-    const int per_rank = p.tiles_m * p.tiles_n;
+    const int tm = SUP ? p.tiles_m / 2 : p.tiles_m;
+    const int per_rank = tm * p.tiles_n;
     tl.rank = t / per_rank;
-    raster(t - tl.rank * per_rank, p.tiles_m, p.tiles_n, p.group_m, tl.mt, tl.nt);
+    raster(t - tl.rank * per_rank, tm, p.tiles_n, SUP ? max(1, p.group_m / 2) : p.group_m, tl.mt,
+           tl.nt);
+    if constexpr (SUP) tl.mt = 2 * tl.mt + pj;
   }
   return tl;
 }
@@ -234,8 +255,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  // Rank of this CTA in its pair (0 = leader, which issues the MMAs).
-  const uint32_t cta = (CG == 2) ? ptx::cluster_ctarank() : 0u;
+  constexpr bool kPair = CG >= 2;                      // tcgen05 cta_group::2 MMAs
+  constexpr bool SUP = CG == 4;                        // two pairs share the B tiles
+  const uint32_t crank = kPair ? ptx::cluster_ctarank() : 0u;
+  const uint32_t cta = crank & 1u;   // rank of this CTA in its pair (0 = leader, issues the MMAs)
+  const uint32_t lead = crank & ~1u;                   // cluster rank of the pair's leader
+  const int pj = static_cast<int>(crank >> 1);         // pair within the cluster (CG = 4)
+  // Work units (tiles, or super-tiles for CG = 4) go round-robin over clusters.
   const int pair = blockIdx.x / CG;
   const int npairs = gridDim.x / CG;
 
@@ -247,11 +273,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(&full[s], 1);
-      ptx::mbar_init(&empty[s], 1);
+      ptx::mbar_init(&empty[s], SUP ? 2 : 1);  // CG = 4: both pairs' MMAs release a stage
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(&tfull[b], 1);
-      ptx::mbar_init(&tempty[b], 4 * CG);  // every epilogue warp of the pair
+      ptx::mbar_init(&tempty[b], 4 * C::kPairCtas);  // every epilogue warp of the pair
     }
     ptx::mbar_init(mma_done, 1);
     *abort_flag = 0;
@@ -277,7 +303,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
   auto narrow = [&](const Tile& tl) { return tl.half >= 0 || p.N - tl.nt * kBN <= kBN / 2; };
   auto col_base = [&](const Tile& tl) { return tl.nt * kBN + (tl.half > 0 ? kBN / 2 : 0); };
   if (warp == 1) {
-    if constexpr (CG == 2) {
+    if constexpr (kPair) {
       ptx::tmem_alloc_pair(tmem_slot, kTmemCols);
       ptx::tmem_relinquish_pair();
     } else {
@@ -286,7 +312,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
     }
   }
   ptx::tc_fence_before();
-  if constexpr (CG == 2) {
+  if constexpr (kPair) {
     ptx::cluster_sync_all();  // the peer's barriers exist before anyone signals them
   } else {
     __syncthreads();
@@ -309,7 +335,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
       bool ok = true;
       const CUtensorMap* ma = &p.mapA[0];
       for (int t = pair; t < num_tiles && ok; t += npairs) {
-        const Tile tl = tile_of<MODE, TM>(p, t, tab);
+        const Tile tl = tile_of<MODE, TM, SUP>(p, t, tab, pj);
         const int bn_cta = narrow(tl) ? C::kBNcta / 2 : C::kBNcta;
         const int b_col = col_base(tl) + static_cast<int>(cta) * bn_cta;
         const uint32_t stage_bytes = kABytes + static_cast<uint32_t>(bn_cta) * kBK * 2;
@@ -331,8 +357,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
           const CUtensorMap* mb = &p.mapB[tl.expert];
           uint8_t* a_dst = sA + stage * kABytes + lane * (4 * 128);
           uint8_t* b_dst = sB + stage * C::kBBytes;
-          if constexpr (CG == 2) {
-            const uint32_t bar = ptx::mapa(ptx::smem_addr(&full[stage]), 0);
+          if constexpr (kPair) {
+            const uint32_t bar = ptx::mapa(ptx::smem_addr(&full[stage]), lead);
             if (lane == 0) {
               if (cta == 0) ptx::mbar_arrive_expect_tx(&full[stage], 2 * stage_bytes);
               for (int i = 0; i < bn_cta / 64; ++i)
@@ -370,7 +396,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
       uint32_t issued = 0, last_parity = 0;
       bool ok = true;
       for (int t = pair; t < num_tiles && ok; t += npairs) {
-        const Tile tl = tile_of<MODE, TM>(p, t, tab);
+        const Tile tl = tile_of<MODE, TM, SUP>(p, t, tab, pj);
         int a_row;
         if constexpr (MODE == MODE_GROUPED) {
           a_row = tl.row0;
@@ -395,13 +421,23 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
           const CUtensorMap* mb = (MODE == MODE_GROUPED) ? &p.mapB[tl.expert] : &p.mapB[r];
           uint8_t* a_dst = sA + stage * kABytes;
           uint8_t* b_dst = sB + stage * C::kBBytes;
-          if constexpr (CG == 2) {
+          if constexpr (kPair) {
             // Both CTAs' bytes are counted on the leader's full barrier.
-            const uint32_t bar = ptx::mapa(ptx::smem_addr(&full[stage]), 0);
+            const uint32_t bar = ptx::mapa(ptx::smem_addr(&full[stage]), lead);
             if (cta == 0) ptx::mbar_arrive_expect_tx(&full[stage], 2 * stage_bytes);
             ptx::tma_load_2d_pair(a_dst, ma, bar, kb * kBK, a_row);
-            for (int i = 0; i < bn_cta / 64; ++i)
-              ptx::tma_load_2d_pair(b_dst + i * kBBoxBytes, mb, bar, b_col + 64 * i, kb * kBK);
+            for (int i = 0; i < bn_cta / 64; ++i) {
+              if constexpr (SUP) {
+                // Box i is loaded by pair i % 2 for both pairs: it lands in this
+                // rank-in-pair's CTA of each pair, counted on each pair's leader.
+                if ((i & 1) == pj)
+                  ptx::tma_load_2d_pair_mc(b_dst + i * kBBoxBytes, mb, bar, b_col + 64 * i,
+                                           kb * kBK,
+                                           static_cast<uint16_t>((1u << cta) | (4u << cta)));
+              } else {
+                ptx::tma_load_2d_pair(b_dst + i * kBBoxBytes, mb, bar, b_col + 64 * i, kb * kBK);
+              }
+            }
           } else {
             ptx::mbar_arrive_expect_tx(&full[stage], stage_bytes);
             ptx::tma_load_2d(a_dst, ma, &full[stage], kb * kBK, a_row);
@@ -436,7 +472,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
       uint32_t acc = 0, acc_phase = 0;
       bool any = false, ok = true;
       for (int t = pair; t < num_tiles && ok; t += npairs) {
-        const uint32_t idesc = narrow(tile_of<MODE, TM>(p, t, tab)) ? C::kIdescNarrow : C::kIdesc;
+        const uint32_t idesc = narrow(tile_of<MODE, TM, SUP>(p, t, tab, pj)) ? C::kIdescNarrow : C::kIdesc;
         if (!W.wait(&tempty[acc], acc_phase ^ 1u)) break;
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * kBN;
@@ -454,13 +490,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
             const uint64_t ad = ptx::smem_desc_sw128(a_addr + kk * 32, 16, 1024);
             // B: MN-major, advance 16 k-rows (2 KiB); 64-wide n atoms 8 KiB apart.
             const uint64_t bd = ptx::smem_desc_sw128(b_addr + kk * 2048, kBBoxBytes, 1024);
-            if constexpr (CG == 2)
+            if constexpr (kPair)
               ptx::mma_f16_pair(d_tmem, ad, bd, idesc, (it > 0 || kk > 0) ? 1u : 0u);
             else
               ptx::mma_f16(d_tmem, ad, bd, idesc, (it > 0 || kk > 0) ? 1u : 0u);
           }
-          if constexpr (CG == 2)
-            ptx::mma_commit_pair_multicast(&empty[stage], 0x3);  // frees the stage in both CTAs
+          if constexpr (kPair)
+            // Frees the stage in both CTAs of the pair (CG = 4: of both pairs,
+            // whose B boxes share the stage).
+            ptx::mma_commit_pair_multicast(&empty[stage], SUP ? 0xF : 0x3);
           else
             ptx::mma_commit(&empty[stage]);
           any = true;
@@ -470,15 +508,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
           }
         }
         if (!ok) break;
-        if constexpr (CG == 2)
-          ptx::mma_commit_pair_multicast(&tfull[acc], 0x3);
+        if constexpr (kPair)
+          ptx::mma_commit_pair_multicast(&tfull[acc], static_cast<uint16_t>(0x3u << lead));
         else
           ptx::mma_commit(&tfull[acc]);
         acc ^= 1u;
         if (acc == 0) acc_phase ^= 1u;
       }
       if (any) {
-        if constexpr (CG == 2)
+        if constexpr (kPair)
           ptx::mma_commit_pair(mma_done);
         else
           ptx::mma_commit(mma_done);
@@ -489,10 +527,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
     // ------------------------------------------------------------- epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int row_in_tile = static_cast<int>(cta) * kBM + q * 32 + lane;  // row of the pair tile
-    const uint32_t tempty_leader0 = (CG == 2) ? ptx::mapa(ptx::smem_addr(&tempty[0]), 0) : 0u;
+    const uint32_t tempty_leader0 = kPair ? ptx::mapa(ptx::smem_addr(&tempty[0]), lead) : 0u;
     uint32_t acc = 0, acc_phase = 0;
     for (int t = pair; t < num_tiles; t += npairs) {
-      const Tile tl = tile_of<MODE, TM>(p, t, tab);
+      const Tile tl = tile_of<MODE, TM, SUP>(p, t, tab, pj);
       const bool failed = !W.wait(&tfull[acc], acc_phase);
       if constexpr (MODE == MODE_RS_PUSH || MODE == MODE_AR_PUSH) {
         // The four epilogue warps meet at named barriers below: stop together.
@@ -545,7 +583,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
           ptx::tc_fence_before();
           __syncwarp();
           if (lane == 0) {
-            if constexpr (CG == 2)
+            if constexpr (kPair)
               ptx::mbar_arrive_cluster(tempty_leader0 + acc * 8);
             else
               ptx::mbar_arrive(&tempty[acc]);
@@ -623,7 +661,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
 
   __syncwarp();
   ptx::tc_fence_before();
-  if constexpr (CG == 2) {
+  if constexpr (kPair) {
     // The leader's MMAs read the peer's shared memory and write the peer's TMEM:
     // neither CTA frees anything before both are done.
     ptx::cluster_sync_all();
@@ -632,7 +670,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
   }
   if (warp == 1) {
     ptx::tc_fence_after();
-    if constexpr (CG == 2)
+    if constexpr (kPair)
       ptx::tmem_dealloc_pair(tmem_base, kTmemCols);
     else
       ptx::tmem_dealloc(tmem_base, kTmemCols);
@@ -677,9 +715,69 @@ cudaError_t launch_cg(const GemmParams& p, int mode, int grid, cudaStream_t st) 
 
 }  // namespace
 
-int gemm_smem_bytes(int cg) { return cg == 2 ? Cfg<2>::kSmem : Cfg<1>::kSmem; }
+int gemm_smem_bytes(int cg) { return cg >= 2 ? Cfg<2>::kSmem : Cfg<1>::kSmem; }
+
+namespace {
+template <int CG>
+int query_max_clusters() {
+  auto kern = gemm_kernel<MODE_RS, CG, GemmParams>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<CG>::kSmem) !=
+      cudaSuccess)
+    return 0;
+  int sms = 0, dev = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(std::max(CG, (sms / CG) * CG)), 1, 1);
+  cfg.blockDim = dim3(kGemmThreads, 1, 1);
+  cfg.dynamicSmemBytes = Cfg<CG>::kSmem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CG;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
+}  // namespace
+
+int gemm_max_clusters(int cg) {
+  constexpr int kDevs = 16;
+  static int cache[kDevs][5] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kDevs) dev = 0;
+  const int k = cg == 4 ? 4 : (cg == 2 ? 2 : 1);
+  if (cache[dev][k] == 0) {
+    int n = k == 4 ? query_max_clusters<4>() : (k == 2 ? query_max_clusters<2>()
+                                                       : query_max_clusters<1>());
+    // (no answer: one cluster per group of k SMs)
+    if (n <= 0) {
+      int sms = 0;
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+      n = std::max(1, sms / k);
+    }
+    cache[dev][k] = n;
+  }
+  return cache[dev][k];
+}
 
 cudaError_t launch_gemm(const GemmParams& p, int mode, int cg, int grid, cudaStream_t st) {
+  if (cg == 4) {
+    // Two pairs per cluster: the modes without tickets.
+    switch (mode) {
+      case MODE_RS: return launch_mode<MODE_RS, 4, GemmParams>(p, grid, st);
+      case MODE_AR: return launch_mode<MODE_AR, 4, GemmParams>(p, grid, st);
+      case MODE_PARTIAL: return launch_mode<MODE_PARTIAL, 4, GemmParams>(p, grid, st);
+      case MODE_AG: return launch_mode<MODE_AG, 4, GemmParams>(p, grid, st);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   if (cg == 2) return launch_cg<2>(p, mode, grid, st);
   if (cg == 1) return launch_cg<1>(p, mode, grid, st);
   return cudaErrorInvalidValue;

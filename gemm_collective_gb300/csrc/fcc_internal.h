@@ -45,7 +45,7 @@ struct GemmParams {
   unsigned long long timeout_ns;
   float* acc_ws;        // push mode with bf16 output: f32 accumulation rows (M x N)
   int* tickets;         // push mode with bf16 output: per (tile, CTA of the pair) counters
-  int cg;               // host side: tile shape of the launch (1 or 2 CTAs per tile)
+  int cg;               // host side: CTAs per cluster (1, 2 or 4)
 };
 
 struct GemvParams {
@@ -93,10 +93,13 @@ struct GroupedParams {
 };
 
 // cg = 1: one CTA per 128 x 256 tile; cg = 2: a CTA pair (cluster of 2) per
-// 256 x 256 tile.  grid is in CTAs (a multiple of cg).
+// 256 x 256 tile; cg = 4: two pairs (cluster of 4) on the m tiles 2i, 2i+1 of
+// one tile column, sharing its B tiles.  grid is in CTAs (a multiple of cg).
 cudaError_t launch_gemm(const GemmParams& p, int mode, int cg, int grid, cudaStream_t st);
 cudaError_t launch_grouped_gemm(const GroupedParams& p, int cg, int grid, cudaStream_t st);
 int gemm_smem_bytes(int cg);
+// Clusters of cg CTAs of the GEMM kernel that fit on the current device at once.
+int gemm_max_clusters(int cg);
 cudaError_t launch_gemv(const GemvParams& p, int grid, cudaStream_t st);
 int gemv_smem_bytes();
 // GEMV grid shape for N columns and R*K rows over `sms` SMs (max_ctas 0 = no cap).

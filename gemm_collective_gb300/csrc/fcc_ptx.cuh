@@ -325,6 +325,19 @@ __device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* m
       : "memory");
 }
 
+// Same, multicast: the box lands at dst's offset in every CTA of `mask`, and
+// each destination's bytes are counted on the barrier at bar's offset in the
+// leader of that destination's pair.
+__device__ __forceinline__ void tma_load_2d_pair_mc(void* dst, const CUtensorMap* map,
+                                                    uint32_t bar_cluster_addr, int32_t x,
+                                                    int32_t y, uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster_addr), "r"(x), "r"(y), "h"(mask)
+      : "memory");
+}
+
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t* dst, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                    smem_addr(dst)),

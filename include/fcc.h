@@ -85,9 +85,15 @@ typedef struct {
   int64_t timeout_ns;      /* device wait limit; 0 = 1 s */
   void *workspace;         /* device scratch, or NULL for the internal pool */
   size_t workspace_bytes;
-  /* Tensor-core tile shape of the GEMMs: 0 = automatic (a CTA pair per
-   * 256 x 256 tile when the rows exceed 128), 1 = one CTA per 128 x 256 tile,
-   * 2 = a CTA pair (cluster of 2, tcgen05 cta_group::2) per 256 x 256 tile. */
+  /* Tensor-core tile shape of the GEMMs: 0 = automatic (a CTA pair when the
+   * rows exceed 128, else 1), 1 = one CTA per
+   * 128 x 256 tile, 2 = a CTA pair (cluster of 2, tcgen05 cta_group::2) per
+   * 256 x 256 tile, 4 = two CTA pairs (cluster of 4) on vertically adjacent
+   * 256 x 256 tiles, each B tile loaded once by TMA multicast for both.  4
+   * applies to the reduce-scatter, all-reduce and all-gather GEMMs in
+   * deterministic mode with an even number of 256-row tiles, and falls back
+   * to 2 elsewhere (measured slower than 2 on the 8-rank reduce-scatter:
+   * each stage waits for both pairs); the MoE expert GEMM takes 1 or 2. */
   int cta_pair;
 } fcc_opts;
 

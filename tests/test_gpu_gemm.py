@@ -44,7 +44,7 @@ def _ar(R, dA, dB, M, N, K, out_dtype, opts=None):
 
 # ------------------------------------------------------------ exactness first
 
-@pytest.mark.parametrize("pair", [1, 2])
+@pytest.mark.parametrize("pair", [1, 2, 4])
 def test_rs_integer_inputs_bit_exact(pair):
     """Small integers: every f32 partial sum is exact, so GPU == oracle exactly."""
     R, M, N, K = 2, 512, 512, 128
@@ -98,7 +98,7 @@ RAGGED = [
 
 @pytest.mark.parametrize("R,M,N,K", RAGGED)
 @pytest.mark.parametrize("out_dtype", [0, 2])
-@pytest.mark.parametrize("pair", [1, 2])
+@pytest.mark.parametrize("pair", [1, 2, 4])
 def test_rs_ragged(R, M, N, K, out_dtype, pair):
     A, B = synth.gemm_inputs(R, M, N, K, 1.0, 1.0, seed=R * 7 + K)
     dA, dB = _upload(A, B)
@@ -109,7 +109,7 @@ def test_rs_ragged(R, M, N, K, out_dtype, pair):
 
 @pytest.mark.parametrize("R,M,N,K", [(4, 200, 264, 136), (2, 130, 16, 64), (8, 256, 256, 64),
                                      (4, 1032, 264, 128)])
-@pytest.mark.parametrize("pair", [0, 1])
+@pytest.mark.parametrize("pair", [0, 1, 2])
 def test_ar_all_buffers_identical_and_equal_rs(R, M, N, K, pair):
     A, B = synth.gemm_inputs(R, M, N, K, 1.0, 1.0, seed=3)
     dA, dB = _upload(A, B)
@@ -125,23 +125,44 @@ def test_ar_all_buffers_identical_and_equal_rs(R, M, N, K, pair):
         assert np.array_equal(cat, bits(outs[0])), "RS shards != AR rows (deterministic mode)"
 
 
-@pytest.mark.parametrize("pair", [1, 2])
+# (pair, N, max_ctas that leave a short last round, max_ctas that leave none):
+# 32 single-CTA tiles on 10 / 8 CTAs; 16 pair tiles on 5 / 4 pairs; 10 two-pair
+# units (N = 1280) on 4 / 5 clusters of 4.
+HALF_CASES = [(1, 1024, 10, 8), (2, 1024, 10, 8), (4, 1280, 16, 20)]
+
+
+@pytest.mark.parametrize("pair,N,split_ctas,whole_ctas", HALF_CASES)
 @pytest.mark.parametrize("op", ["rs", "ar"])
-def test_last_round_half_tiles_bit_identical(op, pair):
+def test_last_round_half_tiles_bit_identical(op, pair, N, split_ctas, whole_ctas):
     """The last round's tiles run as two 128-column halves when they fill at most
-    half the grid.  16 pair tiles (32 single-CTA tiles) on 10 CTAs leave 1 (2) in
-    the last round and are split; on 8 CTAs nothing is left over.  Integer inputs
-    keep every partial sum exact: both equal the oracle bit for bit."""
-    R, M, N, K = 2, 1024, 1024, 128
+    half the grid.  Integer inputs keep every partial sum exact: the split and
+    the unsplit launch both equal the oracle bit for bit."""
+    R, M, K = 2, 1024, 128
     A, B = synth.integer_gemm_inputs(R, M, N, K, -4, 4, seed=11)
     dA, dB = _upload(A, B)
     run = _rs if op == "rs" else _ar
-    split = run(R, dA, dB, M, N, K, fcc.FCC_F32, fcc.make_opts(cta_pair=pair, max_ctas=10))
-    whole = run(R, dA, dB, M, N, K, fcc.FCC_F32, fcc.make_opts(cta_pair=pair, max_ctas=8))
+    split = run(R, dA, dB, M, N, K, fcc.FCC_F32,
+                fcc.make_opts(cta_pair=pair, max_ctas=split_ctas))
+    whole = run(R, dA, dB, M, N, K, fcc.FCC_F32,
+                fcc.make_opts(cta_pair=pair, max_ctas=whole_ctas))
     for j in range(R):
         assert np.array_equal(bits(split[j]), bits(whole[j])), f"buffer {j}"
         ref = oracle.gemm_rs(A, B, j) if op == "rs" else oracle.gemm_ar(A, B)
         assert np.array_equal(to_f64(split[j]), ref), f"buffer {j} vs oracle"
+
+
+@pytest.mark.parametrize("R,M,N,K", [(2, 1024, 136, 64), (4, 512, 128, 192), (2, 2048, 264, 64)])
+def test_two_pair_clusters_match_pairs_bitwise(R, M, N, K):
+    """Two pairs sharing multicast B tiles (cta_pair = 4) against one pair per
+    tile: the same K order per element, so bit-identical outputs; narrow last
+    column tiles (N % 256 <= 128) included."""
+    A, B = synth.gemm_inputs(R, M, N, K, 1.0, 1.0, seed=R + N)
+    dA, dB = _upload(A, B)
+    four = _rs(R, dA, dB, M, N, K, fcc.FCC_F32, fcc.make_opts(cta_pair=4))
+    two = _rs(R, dA, dB, M, N, K, fcc.FCC_F32, fcc.make_opts(cta_pair=2))
+    for j in range(R):
+        assert np.array_equal(bits(four[j]), bits(two[j])), f"shard {j}"
+        assert_close(to_f64(four[j]), oracle.gemm_rs(A, B, j), f"shard {j}")
 
 
 def test_rank_permutation_within_tolerance():
@@ -211,15 +232,18 @@ def test_caller_workspace_and_too_small():
 
 @pytest.mark.parametrize("R,Ms,N,K", [(4, 136, 200, 96), (2, 128, 512, 64), (8, 64, 264, 136),
                                       (2, 520, 264, 64)])
-@pytest.mark.parametrize("algo", [1, 2, 4])
-def test_ag_gemm(R, Ms, N, K, algo):
+@pytest.mark.parametrize("algo,pair", [(1, 0), (2, 0), (4, 0), (1, 4)])
+def test_ag_gemm(R, Ms, N, K, algo, pair):
+    """pair = 4: two pairs per cluster where the 256-row tile count over all
+    shards is even (R x ceil(Ms / 256)); a unit's two tiles may then lie in
+    two shards (Ms = 136 with 4 ranks, Ms = 520 with 2)."""
     X, B = synth.gemm_inputs(R, Ms, N, K, 1.0, 1.0, seed=17 + R)
     dX, dB = _upload(X, B)
     M = R * Ms
     outs = [empty((M, N), torch.bfloat16, fill=float("nan")) for _ in range(R)]
     gath = [empty((M, K), torch.bfloat16, fill=0.0) for _ in range(R)]
     fcc.fcc_ag_gemm(R, dX, dB, outs, gath, M, N, K, fcc.FCC_BF16, fcc.FCC_BF16,
-                    fcc.make_opts(algo=algo))
+                    fcc.make_opts(algo=algo, cta_pair=pair))
     assert fcc.fcc_stream_status() == fcc.FCC_OK
     full = np.concatenate(X)
     for r in range(R):
