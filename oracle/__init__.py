@@ -56,8 +56,11 @@ def _load():
         lib.orc_moe_route.argtypes = [I64, I, I, P, P, P]
         lib.orc_moe_dispatch.argtypes = [I, I64, I, I, P, I64, P, P, P, P, P, P]
         lib.orc_moe_expert_rows.argtypes = [I, P, P, I64, I64, I64, I, P, P, P, I64, P]
+        lib.orc_moe_combine_rows.argtypes = [I, P, P, I64, I64, I64, I, I, P, P, P, P, I64,
+                                             P]
         for f in (lib.orc_rank_sum_rows, lib.orc_gemm_rs_rows, lib.orc_ag_gemm_rows,
-                  lib.orc_moe_route, lib.orc_moe_dispatch, lib.orc_moe_expert_rows):
+                  lib.orc_moe_route, lib.orc_moe_dispatch, lib.orc_moe_expert_rows,
+                  lib.orc_moe_combine_rows):
             f.restype = I
         _lib = lib
         return lib
@@ -205,6 +208,30 @@ def moe_expert_rows(X, W, src_rank, src_tok, expert) -> np.ndarray:
                                      ex.ctypes.data, sr.size, out.ctypes.data)
     if rc:
         raise ValueError(f"orc_moe_expert_rows: bad argument ({rc})")
+    return out
+
+
+def moe_combine(X, W, src_rank, src_tok, idx, gate) -> np.ndarray:
+    """Per token (src_rank[i], src_tok[i]): sum over its slots j of
+    gate[i, j] * (X_s[t] @ W_{idx[i, j]}) in fp64, slots in order; idx < 0 = a
+    slot whose row was not received (adds nothing).  [n, F]."""
+    R = len(X)
+    T, H = X[0].shape
+    E = len(W)
+    F = W[0].shape[1]
+    sr = np.ascontiguousarray(src_rank, dtype=np.int32)
+    st = np.ascontiguousarray(src_tok, dtype=np.int32)
+    ix = np.ascontiguousarray(idx, dtype=np.int32).reshape(sr.size, -1)
+    g = np.ascontiguousarray(gate, dtype=np.float64).reshape(ix.shape)
+    topk = ix.shape[1]
+    out = np.empty((sr.size, F), dtype=np.float64)
+    kx, px = _ptr_array(X, np.uint16)
+    kw, pw = _ptr_array(W, np.uint16)
+    rc = _load().orc_moe_combine_rows(R, px, pw, T, H, F, E, topk, sr.ctypes.data,
+                                      st.ctypes.data, ix.ctypes.data, g.ctypes.data, sr.size,
+                                      out.ctypes.data)
+    if rc:
+        raise ValueError(f"orc_moe_combine_rows: bad argument ({rc})")
     return out
 
 

@@ -22,6 +22,8 @@
  *   - AllGather + GEMM: the mKernel article, fused kernel list.
  *   - MoE Dispatch + GEMM: the mKernel article, fused kernel list; the SC24
  *     abstract, GEMM + All-to-All for MoE.
+ *   - MoE combine (the return all-to-all and the gate-weighted sum): the SC24
+ *     abstract, GEMM + All-to-All for MoE.
  * Rows are row-major and contiguous: A_r is [M,K], B_r is [K,N]; shard j of an
  * M-row result is the contiguous row block [j*M/R, (j+1)*M/R).
  *
@@ -292,6 +294,52 @@ int orc_moe_expert_rows(int R, const uint16_t *const *X, const uint16_t *const *
             const uint16_t *wr = w + h * F;
             for (int64_t f = 0; f < F; ++f)
                 o[f] += xv * bf16_to_double(wr[f]);
+        }
+    }
+    return 0;
+}
+
+/*
+ * MoE combine: the return all-to-all and the gate-weighted sum of each
+ * token's top-k expert outputs (the step after the expert GEMM in the SC24
+ * paper's GEMM + All-to-All operator for MoE):
+ *   out[i][f] = sum over j < topk with idx[i][j] >= 0 of
+ *               gate[i][j] * sum_h X_{src_rank[i]}[src_tok[i]][h] * W_{idx[i][j]}[h][f]
+ * with the slots added in order j = 0, 1, ...  idx[i][j] < 0 marks a slot whose
+ * row was not received (dropped for capacity): it adds nothing.
+ */
+int orc_moe_combine_rows(int R, const uint16_t *const *X, const uint16_t *const *W,
+                         int64_t T, int64_t H, int64_t F, int E, int topk,
+                         const int32_t *src_rank, const int32_t *src_tok,
+                         const int32_t *idx, const double *gate, int64_t n, double *out)
+{
+    if (R < 1 || E < 1 || topk < 1 || n < 0)
+        return 1;
+    for (int64_t i = 0; i < n; ++i) {
+        if (src_rank[i] < 0 || src_rank[i] >= R || src_tok[i] < 0 || src_tok[i] >= T)
+            return 1;
+        for (int j = 0; j < topk; ++j)
+            if (idx[i * topk + j] >= E)
+                return 1;
+    }
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t i = 0; i < n; ++i) {
+        const uint16_t *x = X[src_rank[i]] + (int64_t)src_tok[i] * H;
+        double *o = out + i * F;
+        for (int64_t f = 0; f < F; ++f)
+            o[f] = 0.0;
+        for (int j = 0; j < topk; ++j) {
+            const int e = idx[i * topk + j];
+            if (e < 0)
+                continue;
+            const uint16_t *w = W[e];
+            const double g = gate[i * topk + j];
+            for (int64_t f = 0; f < F; ++f) {
+                double acc = 0.0;
+                for (int64_t h = 0; h < H; ++h)
+                    acc += bf16_to_double(x[h]) * bf16_to_double(w[h * F + f]);
+                o[f] += g * acc;
+            }
         }
     }
     return 0;

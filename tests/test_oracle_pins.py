@@ -375,5 +375,76 @@ def test_expert_rows_vs_library_matmul():
         assert np.allclose(got[i], ref, rtol=1e-12, atol=1e-12)
 
 
+# ----------------------------------------------------------------- MoE combine
+
+def _combine_case(R=2, T=6, H=16, E=4, F=12, seed=31):
+    X, logits, W = synth.moe_inputs(R=R, T=T, H=H, E=E, F=F, seed=seed)
+    sr = np.repeat(np.arange(R), T)
+    st = np.tile(np.arange(T), R)
+    return X, logits, W, sr, st
+
+
+def test_combine_brute_force_exact():
+    """Exact rational sum of gate * (x . w) per token and slot (Fraction)."""
+    X, logits, W, sr, st = _combine_case(T=3, H=5, F=4)
+    idx = np.array([[2, 0], [1, 3], [3, 2], [0, 1], [2, 1], [3, 0]], dtype=np.int32)
+    gate = np.array([[0.5, 0.25], [0.375, 0.125], [0.75, 0.0625],
+                     [0.1, 0.3], [0.6, 0.2], [0.05, 0.45]])
+    got = oracle.moe_combine(X, W, sr, st, idx, gate)
+    xs = [_f64(x) for x in X]
+    ws = [_f64(w) for w in W]
+    for i in range(len(sr)):
+        for f in range(4):
+            tot = Fraction(0)
+            for j in range(2):
+                dot = sum(Fraction(xs[sr[i]][st[i], h]) * Fraction(ws[idx[i, j]][h, f])
+                          for h in range(5))
+                tot += Fraction(gate[i, j]) * dot
+            assert abs(got[i, f] - float(tot)) <= 1e-15 * max(1.0, abs(float(tot)))
+
+
+def test_combine_top1_is_gate_times_library_matmul():
+    X, logits, W, sr, st = _combine_case()
+    idx, gate = oracle.moe_route(np.stack(logits), 1)
+    got = oracle.moe_combine(X, W, sr, st, idx.reshape(-1, 1), gate.reshape(-1, 1))
+    for i in range(len(sr)):
+        e = idx.reshape(-1)[i]
+        ref = gate.reshape(-1)[i] * (_f64(X[sr[i]])[st[i]] @ _f64(W[e]))
+        assert np.allclose(got[i], ref, rtol=1e-12, atol=1e-14)
+
+
+def test_combine_identical_experts_sum_the_gates():
+    """All W_e equal: y = (sum of the token's gates) * x . W (no slot dropped or doubled)."""
+    X, logits, W, sr, st = _combine_case()
+    W = [W[0]] * len(W)
+    idx, gate = oracle.moe_route(np.stack(logits), 2)
+    got = oracle.moe_combine(X, W, sr, st, idx.reshape(-1, 2), gate.reshape(-1, 2))
+    gsum = gate.reshape(-1, 2).sum(axis=1)
+    for i in range(len(sr)):
+        ref = gsum[i] * (_f64(X[sr[i]])[st[i]] @ _f64(W[0]))
+        assert np.allclose(got[i], ref, rtol=1e-12, atol=1e-14)
+
+
+def test_combine_linear_in_gates_and_slot_order_free():
+    X, logits, W, sr, st = _combine_case()
+    idx, gate = oracle.moe_route(np.stack(logits), 2)
+    idx, gate = idx.reshape(-1, 2), gate.reshape(-1, 2)
+    y1 = oracle.moe_combine(X, W, sr, st, idx, gate)
+    y2 = oracle.moe_combine(X, W, sr, st, idx, 3.0 * gate)
+    assert np.allclose(y2, 3.0 * y1, rtol=1e-13, atol=1e-15)
+    ysw = oracle.moe_combine(X, W, sr, st, idx[:, ::-1], gate[:, ::-1])
+    assert np.allclose(ysw, y1, rtol=1e-13, atol=1e-15)
+
+
+def test_combine_dropped_slot_adds_nothing():
+    X, logits, W, sr, st = _combine_case()
+    idx, gate = oracle.moe_route(np.stack(logits), 2)
+    idx, gate = idx.reshape(-1, 2).copy(), gate.reshape(-1, 2)
+    only0 = oracle.moe_combine(X, W, sr, st, idx[:, :1], gate[:, :1])
+    idx[:, 1] = -1
+    got = oracle.moe_combine(X, W, sr, st, idx, gate)
+    assert np.array_equal(got, only0)
+
+
 def test_oracle_threads_reported():
     assert oracle.num_threads() >= 1
