@@ -86,6 +86,9 @@ _ag_gemm = _sig("fcc_ag_gemm", _I, [_I, _P, _P, _P, _P, _I64, _I64, _I64, _I, _I
 _moe = _sig("fcc_moe_dispatch_gemm", _I,
             [_I, _P, _P, _P, _I64, _I64, _I64, _I, _I, _P, _P, _I64, _P, _P, _P, _P, _P, _I, _I,
              _OPTS, _P])
+_combine = _sig("fcc_moe_combine", _I,
+                [_I, _P, _I64, _I64, _I64, _I, _I, _P, _P, _P, _P, _P, _I, _I, _OPTS, _P])
+_combine_ws = _sig("fcc_moe_combine_workspace_size", ctypes.c_size_t, [_I, _I64, _I])
 _ws = _sig("fcc_workspace_size", ctypes.c_size_t, [_I, _I, _I64, _I64, _I64, _OPTS])
 _moe_ws = _sig("fcc_moe_workspace_size", ctypes.c_size_t,
                [_I, _I64, _I64, _I64, _I, _I, _I64, _OPTS])
@@ -172,6 +175,18 @@ def fcc_moe_dispatch_gemm(R, X, logits, W, T, H, F, E, topk, recv_x, recv_y, cap
                 _ptrs(recv_y), cap, _ptrs(topk_idx), _ptrs(topk_gate), _addr(expert_counts),
                 _addr(send_counts), _ptrs(recv_src), in_dtype, out_dtype, _opts(opts),
                 _stream(stream)), "fcc_moe_dispatch_gemm")
+
+
+def fcc_moe_combine(R, recv_y, cap, T, F, E, topk, topk_idx, topk_gate, recv_src,
+                    expert_counts, y, in_dtype=FCC_BF16, out_dtype=FCC_BF16, opts=None,
+                    stream=None):
+    _check(_combine(R, _ptrs(recv_y), cap, T, F, E, topk, _ptrs(topk_idx), _ptrs(topk_gate),
+                    _ptrs(recv_src), _addr(expert_counts), _ptrs(y), in_dtype, out_dtype,
+                    _opts(opts), _stream(stream)), "fcc_moe_combine")
+
+
+def fcc_moe_combine_workspace_size(R, T, topk) -> int:
+    return int(_combine_ws(R, T, topk))
 
 
 def fcc_workspace_size(op, R, M, N, K, opts=None) -> int:

@@ -212,11 +212,36 @@ fcc_status fcc_moe_dispatch_gemm(int R, const void *const *X, const float *const
                                  fcc_dtype out_dtype, const fcc_opts *opts,
                                  fcc_stream_t stream);
 
+/*
+ * MoE combine: the return all-to-all and the gate-weighted top-k sum (SC24
+ * abstract, GEMM + All-to-All for MoE: the direction back to the token
+ * owners).  For every source rank s and token t:
+ *   y[s][t][f] = sum over slots j < topk of topk_gate[s][t][j] * recv_y[d][i][f]
+ * where row i of receiving rank d is the row that assignment (s, t, j) was
+ * given by the dispatch that produced recv_y (d = topk_idx[s][t][j] / (E/R)),
+ * the slots added in order in f32 (so the result is repeatable).  A slot
+ * whose row was dropped for capacity adds nothing.  The receive rows are
+ * found from recv_src and expert_counts as fcc_moe_dispatch_gemm wrote them:
+ * rank d holds its E/R experts' rows in expert order, min(cap, their total)
+ * rows in all.
+ * recv_y[d]: [cap,F] (in: bf16 or f32); topk_idx[s]: [T,topk] int32;
+ * topk_gate[s]: [T,topk] f32; recv_src[d]: [cap] int32; expert_counts: [E]
+ * int32 (device); y[s]: [T,F] (out_dtype: bf16 or f32).  topk in {1, 2};
+ * R <= E <= 64, E % R == 0; F % 8 == 0.  Uses workspace
+ * (fcc_moe_combine_workspace_size).
+ */
+fcc_status fcc_moe_combine(int R, const void *const *recv_y, int64_t cap, int64_t T, int64_t F,
+                           int E, int topk, const int32_t *const *topk_idx,
+                           const float *const *topk_gate, const int32_t *const *recv_src,
+                           const int32_t *expert_counts, void *const *y, fcc_dtype in,
+                           fcc_dtype out_dtype, const fcc_opts *opts, fcc_stream_t stream);
+
 /* Scratch bytes a call needs (for opts->workspace); 0 if none. */
 size_t fcc_workspace_size(fcc_op op, int R, int64_t M, int64_t N, int64_t K,
                           const fcc_opts *opts);
 size_t fcc_moe_workspace_size(int R, int64_t T, int64_t H, int64_t F, int E, int topk,
                               int64_t cap, const fcc_opts *opts);
+size_t fcc_moe_combine_workspace_size(int R, int64_t T, int topk);
 
 /*
  * Synchronises `stream`, then returns and clears the device status word of

@@ -322,25 +322,38 @@ int orc_moe_combine_rows(int R, const uint16_t *const *X, const uint16_t *const 
             if (idx[i * topk + j] >= E)
                 return 1;
     }
+    int bad = 0;
 #pragma omp parallel for schedule(dynamic, 1)
     for (int64_t i = 0; i < n; ++i) {
         const uint16_t *x = X[src_rank[i]] + (int64_t)src_tok[i] * H;
         double *o = out + i * F;
+        double *row = (double *)malloc((size_t)F * sizeof(double));
+        if (row == NULL) {
+#pragma omp atomic write
+            bad = 1;
+            continue;
+        }
         for (int64_t f = 0; f < F; ++f)
             o[f] = 0.0;
         for (int j = 0; j < topk; ++j) {
             const int e = idx[i * topk + j];
             if (e < 0)
                 continue;
+            /* the slot's expert row x . W_e, each element summed over h in order */
             const uint16_t *w = W[e];
-            const double g = gate[i * topk + j];
-            for (int64_t f = 0; f < F; ++f) {
-                double acc = 0.0;
-                for (int64_t h = 0; h < H; ++h)
-                    acc += bf16_to_double(x[h]) * bf16_to_double(w[h * F + f]);
-                o[f] += g * acc;
+            for (int64_t f = 0; f < F; ++f)
+                row[f] = 0.0;
+            for (int64_t h = 0; h < H; ++h) {
+                const double xv = bf16_to_double(x[h]);
+                const uint16_t *wr = w + h * F;
+                for (int64_t f = 0; f < F; ++f)
+                    row[f] += xv * bf16_to_double(wr[f]);
             }
+            const double g = gate[i * topk + j];
+            for (int64_t f = 0; f < F; ++f)
+                o[f] += g * row[f];
         }
+        free(row);
     }
-    return 0;
+    return bad ? 3 : 0;
 }

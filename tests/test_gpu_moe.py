@@ -186,3 +186,98 @@ def test_moe_full_workload_sampled(path):
     out = _run(X, logits, W, w.R, w.T, w.H, w.F, w.E, w.topk, cap, staged=staged,
                contiguous=contiguous, opts=fcc.make_opts(algo=algo))
     _check(X, logits, W, w.R, w.T, w.H, w.F, w.E, w.topk, cap, out, sample=48)
+
+
+# ------------------------------------------------------------------ MoE combine
+
+def _combine(out, R, T, F, E, topk, cap, in_dtype, out_dtype=fcc.FCC_BF16):
+    tdt = torch.float32 if out_dtype == fcc.FCC_F32 else torch.bfloat16
+    y = [empty((T, F), tdt, fill=float("nan")) for _ in range(R)]
+    fcc.fcc_moe_combine(R, out["recv_y"], cap, T, F, E, topk, out["idx"], out["gate"],
+                        out["src"], out["counts"], y, in_dtype, out_dtype)
+    assert fcc.fcc_stream_status() == fcc.FCC_OK
+    return y
+
+
+def _combine_ref(X, W, logits, R, T, E, topk, cap, tokens=None):
+    """Oracle combine from the oracle's own routing; slots whose row falls past
+    cap in the full dispatch were dropped (they add nothing)."""
+    idx, gate = oracle.moe_route(np.stack(logits), topk)
+    d = oracle.moe_dispatch(idx, R, E, R * T * topk)
+    ix = idx.reshape(R * T, topk).copy()
+    ix[d.recv_row.reshape(R * T, topk) >= cap] = -1
+    g = gate.reshape(R * T, topk)
+    tok = np.arange(R * T) if tokens is None else np.asarray(tokens)
+    return oracle.moe_combine(X, W, tok // T, tok % T, ix[tok], g[tok]), tok
+
+
+@pytest.mark.parametrize("R,T,H,F,E,topk", [
+    (2, 300, 128, 136, 8, 2),
+    (4, 257, 256, 264, 16, 2),
+    (8, 64, 64, 64, 64, 2),
+    (2, 200, 192, 128, 4, 1),
+    (1, 500, 128, 256, 8, 2),
+])
+@pytest.mark.parametrize("dtypes", [(fcc.FCC_BF16, fcc.FCC_BF16), (fcc.FCC_F32, fcc.FCC_F32)])
+def test_moe_combine_small(R, T, H, F, E, topk, dtypes):
+    """The return all-to-all + gate-weighted sum against the oracle's combine."""
+    X, logits, W = synth.moe_inputs(R, T, H, E, F, seed=R * 10 + T)
+    cap = R * T * topk
+    mid, out_dtype = dtypes
+    out = _run(X, logits, W, R, T, H, F, E, topk, cap, mid, staged=False)
+    y = _combine(out, R, T, F, E, topk, cap, mid, out_dtype)
+    ref, _ = _combine_ref(X, W, logits, R, T, E, topk, cap)
+    got = np.concatenate([to_f64(v) for v in y])
+    assert_close(got, ref, "combined rows")
+
+
+def test_moe_combine_capacity_drops_and_repeatable():
+    """Rows dropped for capacity add nothing; two calls agree bit for bit."""
+    R, T, H, F, E, topk = 2, 256, 64, 64, 4, 2
+    X, logits, W = synth.moe_inputs(R, T, H, E, F, seed=7)
+    cap = 100
+    out = _run(X, logits, W, R, T, H, F, E, topk, cap)
+    assert out["status"] == fcc.FCC_ERR_CAPACITY
+    y1 = _combine(out, R, T, F, E, topk, cap, fcc.FCC_BF16, fcc.FCC_F32)
+    y2 = _combine(out, R, T, F, E, topk, cap, fcc.FCC_BF16, fcc.FCC_F32)
+    for a, b in zip(y1, y2):
+        assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+    ref, _ = _combine_ref(X, W, logits, R, T, E, topk, cap)
+    assert_close(np.concatenate([to_f64(v) for v in y1]), ref, "combined rows with drops")
+
+
+def test_moe_combine_invalid_arguments():
+    R, T, F, E, topk, cap = 2, 16, 64, 4, 2, 64
+    dummy = [empty((cap, F), torch.bfloat16) for _ in range(R)]
+    ints = [torch.zeros((T, topk), dtype=torch.int32, device="cuda") for _ in range(R)]
+    flts = [torch.zeros((T, topk), dtype=torch.float32, device="cuda") for _ in range(R)]
+    src = [torch.zeros((cap,), dtype=torch.int32, device="cuda") for _ in range(R)]
+    counts = torch.zeros((E,), dtype=torch.int32, device="cuda")
+    y = [empty((T, F), torch.bfloat16) for _ in range(R)]
+    for bad in [dict(E=3), dict(topk=3), dict(F=60)]:
+        kw = dict(E=E, topk=topk, F=F)
+        kw.update(bad)
+        with pytest.raises(fcc.FccError) as e:
+            fcc.fcc_moe_combine(R, dummy, cap, T, kw["F"], kw["E"], kw["topk"], ints, flts, src,
+                                counts, y)
+        assert e.value.status == fcc.FCC_ERR_INVALID
+    with pytest.raises(fcc.FccError) as e:
+        fcc.fcc_moe_combine(R, dummy, cap, T, F, E, topk, ints, flts, src, counts, y,
+                            fcc.FCC_F16, fcc.FCC_BF16)
+    assert e.value.status == fcc.FCC_ERR_UNSUPPORTED
+
+
+def test_moe_combine_full_workload_sampled():
+    """The benchmark's shapes: dispatch + expert GEMM, then the combine, on 48
+    sampled tokens of the 32768."""
+    w = synth.WORKLOADS["moe_r8_t4096_h4096_e64_f1408"]
+    X, logits, W = synth.moe_inputs(w.R, w.T, w.H, w.E, w.F, std_x=w.std_a, std_w=w.std_b,
+                                    seed=0)
+    cap = 2 * w.T * w.topk
+    out = _run(X, logits, W, w.R, w.T, w.H, w.F, w.E, w.topk, cap, staged=False)
+    y = _combine(out, w.R, w.T, w.F, w.E, w.topk, cap, fcc.FCC_BF16)
+    rng = np.random.Generator(np.random.PCG64(3))
+    tok = np.sort(rng.choice(w.R * w.T, size=48, replace=False))
+    ref, tok = _combine_ref(X, W, logits, w.R, w.T, w.E, w.topk, cap, tok)
+    got = np.stack([to_f64(y[t // w.T][int(t % w.T)]) for t in tok])
+    assert_close(got, ref, "combined rows (sampled)")
