@@ -471,14 +471,30 @@ def other_ops(fcc, torch, np, synth, dev, stream, dA_rs, dB_rs, pk, only=None):
         def leg(ms, path):
             return {"ms": ms, "TFLOP/s": w.flops() / (ms * 1e-3) / 1e12, "path": path}
 
+        # combine: the return all-to-all + gate-weighted top-2 sum of the GEMM's rows
+        y = [torch.empty((T, F), dtype=torch.bfloat16, device=dev) for _ in range(R)]
+
+        def comb():
+            fcc.fcc_moe_combine(R, recv_y, cap, T, F, E, topk, idx, gate, src, counts, y,
+                                0, 0, None, stream)
+
+        moe()
+        tc_ = time_calls(comb, 20, 3, stream)
+        tl = time_calls(lambda: (moe(), comb()), 10, 3, stream)
+        cbytes = R * T * topk * F * 2 + R * T * F * 2  # expert rows read once, y written once
+        combine = {"us": tc_ * 1e3, "GB/s": cbytes / (tc_ * 1e-3) / 1e9,
+                   "roofline_frac": cbytes / (tc_ * 1e-3) / 1e9 / hbm,
+                   "algorithmic_bytes": cbytes}
         res = {"fused": leg(t, "route, dispatch copy into workspace, grouped GEMM on the copy"),
+               "combine": combine,
+               "layer": leg(tl, "dispatch + expert GEMM + combine (two calls)"),
                "gather_in_gemm": leg(tg, "route, grouped GEMM gathering its rows by TMA gather4"),
                "gather_with_recv_x": leg(tx, "the same, recv_x copied on a side stream beside "
                                              "the GEMM"),
                "roofline_frac": (w.flops() / (t * 1e-3) / 1e12) / tc,
                "algorithmic_bytes": byts}
         ops[w.name] = res
-        del Xall, dX, dL, dW, recv_y, recv_x
+        del Xall, dX, dL, dW, recv_y, recv_x, y
 
     st = fcc.fcc_stream_status(stream)
     if st != fcc.FCC_OK:

@@ -9,9 +9,10 @@
 //                     expert from the prefix of d's local expert counts, its
 //                     token from recv_src, its slot from the token's top-k
 //                     list; writes loc[token][slot] = d*cap + i.
-//   2. combine_kernel one warp per token: reads each of its (at most two) rows
-//                     once, 16 bytes per lane, adds gate * row in slot order
-//                     in f32 and stores the token's output row once.
+//   2. combine_kernel one warp per token (a persistent grid): reads each of its
+//                     (at most two) rows once, 16 bytes per lane and four
+//                     steps in flight, adds gate * row in slot order in f32
+//                     and stores the token's output row once.
 // The rows move once each way (HBM bound: recv rows read, outputs written);
 // no atomics, so the result is repeatable.
 #include <cuda_runtime.h>
@@ -68,77 +69,114 @@ __global__ void __launch_bounds__(256) locate_kernel(const CombineArgs a) {
   }
 }
 
-// 8 consecutive values of a row (16 bytes of bf16, 32 of f32) as f32.
-__device__ __forceinline__ void load8(const void* row, int v, int f32, float (&x)[8]) {
-  if (f32) {
-    const float4* p = reinterpret_cast<const float4*>(row) + 2 * v;
-    const float4 a = __ldcs(p), b = __ldcs(p + 1);
-    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
-    x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
-  } else {
-    const uint4 q = __ldcs(reinterpret_cast<const uint4*>(row) + v);
-    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+// One 16-byte vector of a row: 8 bf16 values, or 4 f32 values.  Rows are
+// held raw while in flight (4 registers a vector) and widened at use.
+__device__ __forceinline__ void widen_bf16(const uint4& q, float (&x)[8]) {
+  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-    for (int h = 0; h < 4; ++h) {
-      x[2 * h] = __uint_as_float(w[h] << 16);
-      x[2 * h + 1] = __uint_as_float(w[h] & 0xFFFF0000u);
-    }
+  for (int h = 0; h < 4; ++h) {
+    x[2 * h] = __uint_as_float(w[h] << 16);
+    x[2 * h + 1] = __uint_as_float(w[h] & 0xFFFF0000u);
   }
 }
 
+// Output vector v of the token: 8 values (bf16 rows) or 4 (f32 rows).
+template <bool IN_F32>
+__device__ __forceinline__ void store_vec(char* out, int v, int out_f32, const float* acc) {
+  constexpr int kN = IN_F32 ? 4 : 8;
+  if (out_f32) {
+    float4* p = reinterpret_cast<float4*>(out) + (IN_F32 ? v : 2 * v);
+    __stcs(p, make_float4(acc[0], acc[1], acc[2], acc[3]));
+    if (kN == 8) __stcs(p + 1, make_float4(acc[4], acc[5], acc[6], acc[7]));
+  } else if (kN == 8) {
+    uint4 q;
+    q.x = ptx::pack_bf16x2(acc[0], acc[1]);
+    q.y = ptx::pack_bf16x2(acc[2], acc[3]);
+    q.z = ptx::pack_bf16x2(acc[4], acc[5]);
+    q.w = ptx::pack_bf16x2(acc[6], acc[7]);
+    __stcs(reinterpret_cast<uint4*>(out) + v, q);
+  } else {
+    uint2 q;
+    q.x = ptx::pack_bf16x2(acc[0], acc[1]);
+    q.y = ptx::pack_bf16x2(acc[2], acc[3]);
+    __stcs(reinterpret_cast<uint2*>(out) + v, q);
+  }
+}
+
+template <bool IN_F32>
 __global__ void __launch_bounds__(256) combine_kernel(const CombineArgs a) {
+  constexpr int kN = IN_F32 ? 4 : 8;      // values per 16-byte vector
+  constexpr int kUnroll = 4;              // vectors per lane in flight, per row
   const int lane = threadIdx.x & 31;
   const long long ntok = static_cast<long long>(a.R) * a.T;
   const long long nwarps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
-  const int vecs = a.F / 8;
+  const int vecs = a.F / kN;
+  const long long in_row = static_cast<long long>(a.F) * (IN_F32 ? 4 : 2);
   for (long long tok = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
        tok < ntok; tok += nwarps) {
     const int s = static_cast<int>(tok / a.T);
     const int t = static_cast<int>(tok - static_cast<long long>(s) * a.T);
     // Lane j < topk fetches slot j's receive row and gate; the warp shares them.
-    const void* row = nullptr;
+    const uint4* row = nullptr;
     float g = 0.f;
     if (lane < a.topk) {
       const int l = a.loc[tok * a.topk + lane];
       if (l >= 0) {
         const int d = static_cast<int>(l / a.cap);
         const long long i = l - static_cast<long long>(d) * a.cap;
-        row = static_cast<const char*>(a.recv_y[d]) +
-              i * a.F * static_cast<long long>(a.in_f32 ? 4 : 2);
+        row = reinterpret_cast<const uint4*>(static_cast<const char*>(a.recv_y[d]) + i * in_row);
         g = __ldg(a.gate[s] + static_cast<long long>(t) * a.topk + lane);
       }
     }
-    const void* row0 = reinterpret_cast<const void*>(
+    const uint4* row0 = reinterpret_cast<const uint4*>(
         __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(row), 0));
-    const void* row1 = reinterpret_cast<const void*>(
+    const uint4* row1 = reinterpret_cast<const uint4*>(
         __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(row), 1));
     const float g0 = __shfl_sync(0xffffffffu, g, 0);
     const float g1 = __shfl_sync(0xffffffffu, g, 1);
+    if (a.topk < 2) row1 = nullptr;
     char* out = static_cast<char*>(a.y[s]) + static_cast<long long>(t) * a.F * (a.out_f32 ? 4 : 2);
-    for (int v = lane; v < vecs; v += 32) {
-      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      float x[8];
-      if (row0 != nullptr) {
-        load8(row0, v, a.in_f32, x);
+    // All loads of a step (kUnroll vectors of both rows) are issued before the
+    // first use: 8 x 16 bytes per lane in flight.
+    for (int v0 = lane; v0 < vecs; v0 += 32 * kUnroll) {
+      uint4 q0[kUnroll], q1[kUnroll];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) acc[k] += g0 * x[k];
+      for (int u = 0; u < kUnroll; ++u) {
+        const int v = v0 + 32 * u;
+        q0[u] = make_uint4(0, 0, 0, 0);
+        q1[u] = make_uint4(0, 0, 0, 0);
+        if (v < vecs) {
+          if (row0 != nullptr) q0[u] = __ldcs(row0 + v);
+          if (row1 != nullptr) q1[u] = __ldcs(row1 + v);
+        }
       }
-      if (a.topk > 1 && row1 != nullptr) {
-        load8(row1, v, a.in_f32, x);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) acc[k] += g1 * x[k];
-      }
-      if (a.out_f32) {
-        float4* p = reinterpret_cast<float4*>(out) + 2 * v;
-        __stcs(p, make_float4(acc[0], acc[1], acc[2], acc[3]));
-        __stcs(p + 1, make_float4(acc[4], acc[5], acc[6], acc[7]));
-      } else {
-        uint4 q;
-        q.x = ptx::pack_bf16x2(acc[0], acc[1]);
-        q.y = ptx::pack_bf16x2(acc[2], acc[3]);
-        q.z = ptx::pack_bf16x2(acc[4], acc[5]);
-        q.w = ptx::pack_bf16x2(acc[6], acc[7]);
-        __stcs(reinterpret_cast<uint4*>(out) + v, q);
+      for (int u = 0; u < kUnroll; ++u) {
+        const int v = v0 + 32 * u;
+        if (v >= vecs) break;
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        float x[8];
+        if (row0 != nullptr) {
+          if constexpr (IN_F32) {
+            x[0] = __uint_as_float(q0[u].x); x[1] = __uint_as_float(q0[u].y);
+            x[2] = __uint_as_float(q0[u].z); x[3] = __uint_as_float(q0[u].w);
+          } else {
+            widen_bf16(q0[u], x);
+          }
+#pragma unroll
+          for (int k = 0; k < kN; ++k) acc[k] += g0 * x[k];
+        }
+        if (row1 != nullptr) {
+          if constexpr (IN_F32) {
+            x[0] = __uint_as_float(q1[u].x); x[1] = __uint_as_float(q1[u].y);
+            x[2] = __uint_as_float(q1[u].z); x[3] = __uint_as_float(q1[u].w);
+          } else {
+            widen_bf16(q1[u], x);
+          }
+#pragma unroll
+          for (int k = 0; k < kN; ++k) acc[k] += g1 * x[k];
+        }
+        store_vec<IN_F32>(out, v, a.out_f32, acc);
       }
     }
   }
@@ -224,9 +262,16 @@ fcc_status fcc_moe_combine(int R, const void* const* recv_y, int64_t cap, int64_
   if (cudaMemsetAsync(a.loc, 0xFF, loc_bytes, st) != cudaSuccess) return FCC_ERR_CUDA;  // -1
   const long long rows = static_cast<long long>(R) * cap;
   locate_kernel<<<static_cast<unsigned>((rows + 255) / 256), 256, 0, st>>>(a);
+  // A persistent grid of the blocks that fit at once (warps loop over tokens).
+  auto kern = a.in_f32 ? combine_kernel<true> : combine_kernel<false>;
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 256, 0) != cudaSuccess)
+    per_sm = 4;
+  per_sm = std::max(per_sm, 1);
   const long long ntok = static_cast<long long>(R) * T;
-  const long long blocks = std::min<long long>((ntok + 7) / 8, static_cast<long long>(sms) * 16);
-  combine_kernel<<<static_cast<unsigned>(std::max<long long>(1, blocks)), 256, 0, st>>>(a);
+  const long long blocks =
+      std::min<long long>((ntok + 7) / 8, static_cast<long long>(sms) * per_sm);
+  kern<<<static_cast<unsigned>(std::max<long long>(1, blocks)), 256, 0, st>>>(a);
   if (cudaGetLastError() != cudaSuccess) return FCC_ERR_CUDA;
   bump_launch_count(2);
   return FCC_OK;
