@@ -98,6 +98,7 @@ _chunks = _sig("fcc_interdecom_chunks", _I, [ctypes.c_double, ctypes.c_double,
                                               ctypes.c_double, _I])
 _itime = _sig("fcc_interdecom_time", ctypes.c_double, [ctypes.c_double, ctypes.c_double,
                                                        ctypes.c_double, _I])
+_choose = _sig("fcc_choose_algo", _I, [_I, _I, _I64, _I64, _I64, _I, _I])
 _launches = _sig("fcc_launch_count", ctypes.c_uint64, [])
 _version = _sig("fcc_version", ctypes.c_char_p, [])
 _wait_timeout = _sig("fcc_test_wait_timeout", _I, [_I64, _P])
@@ -187,6 +188,11 @@ def fcc_moe_combine(R, recv_y, cap, T, F, E, topk, topk_idx, topk_gate, recv_src
 
 def fcc_moe_combine_workspace_size(R, T, topk) -> int:
     return int(_combine_ws(R, T, topk))
+
+
+def fcc_choose_algo(op, R, M, N, K, sms=0, max_ctas=0) -> int:
+    """The algorithm FCC_ALGO_AUTO runs for this operator and shape."""
+    return int(_choose(op, R, M, N, K, sms, max_ctas))
 
 
 def fcc_workspace_size(op, R, M, N, K, opts=None) -> int:

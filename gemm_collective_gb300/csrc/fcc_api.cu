@@ -113,6 +113,26 @@ fcc_algo algo_of(const fcc_opts* o) {
   return o->algo;
 }
 
+// The strategy for FCC_ALGO_AUTO, from measurements on GB300 (8 ranks, bf16):
+//  * GEMM + RS / AR and AG + GEMM: the fused kernel beat the plain GEMM +
+//    reduce, the InterDecom pipeline and the copy-engine path at every shape
+//    measured (8192 x 8192 x 3584: 2.10-2.31 ms against 2.47-3.41 ms), and the
+//    2-rank 256 x 256 x 128 call is one launch.
+//  * GEMV + AR: the fused kernel ends with one CTA per column group adding
+//    the group's `splits` partials, a serial tail that grows with the splits:
+//    with 9 splits (N = 8192, K = 3584) fused 81.7 us against 83.0 us for the
+//    plain per-rank GEMM + reduce kernel; with 19 splits (N = 4096) 54.8 us
+//    against 45.5 us.  So the plain form is chosen from 16 splits on.
+fcc_algo choose_algo(fcc_op op, int R, int64_t M, int64_t N, int64_t K, int sms, int max_ctas) {
+  (void)M;
+  if (op == FCC_OP_GEMV_AR) {
+    int groups = 0, splits = 0;
+    gemv_shape(N, R, K, sms, max_ctas, &groups, &splits);
+    return splits >= 16 ? FCC_ALGO_UNFUSED : FCC_ALGO_FUSED;
+  }
+  return FCC_ALGO_FUSED;
+}
+
 bool deterministic_of(const fcc_opts* o) { return o == nullptr || o->deterministic != 0; }
 
 // Tensor-core tile shape (CTAs per cluster): a CTA pair per 256-row tile
@@ -533,21 +553,31 @@ fcc_status fcc_gemv_ar(int R, const void* const* A, const void* const* B, void* 
   if (M > 16) return FCC_ERR_INVALID;
   if ((s = check_out_dtype(out_dtype)) != FCC_OK) return s;
   if (!ptrs_ok(out, R)) return FCC_ERR_INVALID;
-  const fcc_algo algo = algo_of(opts);
+  DeviceState* d = nullptr;
+  if ((s = device_state(&d)) != FCC_OK) return s;
+  // AUTO resolves here; the copy carries the choice to the planning helpers,
+  // which read the algorithm from the options themselves.
+  fcc_opts chosen;
+  if (opts != nullptr) {
+    chosen = *opts;
+  } else {
+    std::memset(&chosen, 0, sizeof(chosen));
+    chosen.deterministic = 1;
+  }
+  if (chosen.algo == FCC_ALGO_AUTO)
+    chosen.algo = choose_algo(FCC_OP_GEMV_AR, R, M, N, K, d->sms, chosen.max_ctas);
+  opts = &chosen;
+  const fcc_algo algo = chosen.algo;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const int out_f32 = out_dtype == FCC_F32 ? 1 : 0;
   if (algo != FCC_ALGO_FUSED) {
     if (algo == FCC_ALGO_INTERDECOM) return FCC_ERR_UNSUPPORTED;  // one 8-row chunk: nothing to split
     if (algo != FCC_ALGO_UNFUSED && algo != FCC_ALGO_CE) return FCC_ERR_INVALID;
-    DeviceState* d = nullptr;
-    if ((s = device_state(&d)) != FCC_OK) return s;
     const RankSumPlan pl = rank_sum_plan(R, M, N, out_f32, opts);
     void* ws = nullptr;
     if ((s = get_workspace(d, opts, pl.total(), &ws)) != FCC_OK) return s;
     return rank_sum_unfused(R, A, B, out, R, false, M, N, K, out_f32, opts, d, ws, pl, st);
   }
-  DeviceState* d = nullptr;
-  if ((s = device_state(&d)) != FCC_OK) return s;
   const GemvPlan g = gemv_plan(R, M, N, K, d->sms, opts);
   void* ws = nullptr;
   if ((s = get_workspace(d, opts, g.total(), &ws)) != FCC_OK) return s;
@@ -664,12 +694,24 @@ size_t fcc_workspace_size(fcc_op op, int R, int64_t M, int64_t N, int64_t K,
       // bf16 vs f32 output only matters for the push mode; report the larger.
       return rank_sum_plan(R, M, N, false, opts).total();
     case FCC_OP_GEMV_AR: {
-      if (algo_of(opts) != FCC_ALGO_FUSED) return rank_sum_plan(R, M, N, false, opts).total();
+      const bool automatic = opts == nullptr || opts->algo == FCC_ALGO_AUTO;
+      fcc_opts plain;
+      if (opts != nullptr) {
+        plain = *opts;
+      } else {
+        std::memset(&plain, 0, sizeof(plain));
+        plain.deterministic = 1;
+      }
+      plain.algo = FCC_ALGO_UNFUSED;
+      const size_t unfused = rank_sum_plan(R, M, N, false, &plain).total();
+      if (!automatic && opts->algo != FCC_ALGO_FUSED) return rank_sum_plan(R, M, N, false, opts).total();
       int sms = 0, dev = 0;
       if (cudaGetDevice(&dev) != cudaSuccess ||
           cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         sms = 256;
-      return gemv_plan(R, M, N, K, sms, opts).total();
+      const size_t fused = gemv_plan(R, M, N, K, sms, opts).total();
+      // AUTO may take either form (per shape): room for both.
+      return automatic ? std::max(fused, unfused) : fused;
     }
     case FCC_OP_AG_GEMM:
       return algo_of(opts) == FCC_ALGO_FUSED ? 0 : static_cast<size_t>(M) * K * 2;
@@ -710,6 +752,20 @@ const char* fcc_status_string(fcc_status s) {
 double fcc_interdecom_time(double G, double X, double alpha, int chunks) {
   if (chunks < 1) chunks = 1;
   return std::max(G, X) + std::min(G, X) / chunks + chunks * alpha;
+}
+
+fcc_algo fcc_choose_algo(fcc_op op, int R, int64_t M, int64_t N, int64_t K, int sms,
+                         int max_ctas) {
+  if (sms <= 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      sms = 152;
+    }
+  }
+  if (R < 1 || R > FCC_MAX_RANKS || N <= 0 || K <= 0) return FCC_ALGO_FUSED;
+  return choose_algo(op, R, M, N, K, sms, max_ctas);
 }
 
 int fcc_interdecom_chunks(double G, double X, double alpha, int max_chunks) {

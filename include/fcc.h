@@ -66,7 +66,7 @@ typedef enum {
 } fcc_status;
 
 typedef enum {
-  FCC_ALGO_AUTO = 0,       /* the fused kernel */
+  FCC_ALGO_AUTO = 0,       /* chosen per operator and shape (fcc_choose_algo) */
   FCC_ALGO_FUSED = 1,      /* fused GEMM + collective in one persistent kernel */
   FCC_ALGO_UNFUSED = 2,    /* per-rank GEMM to f32 partials, then a reduce/copy kernel */
   FCC_ALGO_INTERDECOM = 3, /* row chunks: GEMM of chunk i overlaps the collective of i-1 */
@@ -251,6 +251,21 @@ fcc_status fcc_stream_status(fcc_stream_t stream);
 
 /* Static description of a status code. */
 const char *fcc_status_string(fcc_status s);
+
+/*
+ * The algorithm FCC_ALGO_AUTO runs for a call (the strategy selector, after
+ * Compass's unified framework of operator variants: "Compass: Dissecting
+ * Communication and Computation Operators for Efficient LLM Training",
+ * abstract), from measurements on GB300: FCC_ALGO_FUSED for the GEMM +
+ * ReduceScatter / AllReduce and AllGather + GEMM (fastest at every shape
+ * measured); for the GEMV + AllReduce, FCC_ALGO_UNFUSED when the fused grid
+ * would split the rank-and-K range 16 or more ways (few 512-column groups:
+ * its final serial sum of the splits then costs more than the plain GEMM +
+ * reduce), else FCC_ALGO_FUSED.  sms: SMs to plan for (0 = the current
+ * device's, 152 without one); max_ctas as in fcc_opts.  Host-only.
+ */
+fcc_algo fcc_choose_algo(fcc_op op, int R, int64_t M, int64_t N, int64_t K, int sms,
+                         int max_ctas);
 
 /*
  * InterDecom chunk-count model ("Compass: Dissecting Communication and

@@ -103,3 +103,21 @@ def test_workspace_sizes(fcc):
     o = fcc.make_opts(algo=fcc.FCC_ALGO_CE)
     assert fcc.fcc_workspace_size(fcc.FCC_OP_GEMM_RS, 2, 256, 256, 128, o) >= 2 * 2 * 256 * 256 * 4
     assert fcc.fcc_workspace_size(fcc.FCC_OP_AG_GEMM, 8, 8192, 3584, 8192, None) == 0
+
+
+def test_strategy_selector(fcc):
+    """AUTO's choice per operator and shape (host logic only, no device)."""
+    F, U = fcc.FCC_ALGO_FUSED, fcc.FCC_ALGO_UNFUSED
+    for op in (fcc.FCC_OP_GEMM_RS, fcc.FCC_OP_GEMM_AR, fcc.FCC_OP_AG_GEMM):
+        assert fcc.fcc_choose_algo(op, 8, 8192, 8192, 3584, 152) == F
+        assert fcc.fcc_choose_algo(op, 2, 256, 256, 128, 152) == F
+    gemv = fcc.FCC_OP_GEMV_AR
+    # 16 column groups of 512 -> 9 splits on 152 SMs: fused
+    assert fcc.fcc_choose_algo(gemv, 8, 8, 8192, 3584, 152) == F
+    # 8 groups -> 19 splits: the plain GEMM + reduce
+    assert fcc.fcc_choose_algo(gemv, 8, 8, 4096, 3584, 152) == U
+    # capped grid: 2 groups on 8 CTAs -> 4 splits: fused again
+    assert fcc.fcc_choose_algo(gemv, 8, 8, 1024, 3584, 152, 8) == F
+    assert fcc.fcc_choose_algo(gemv, 8, 8, 1024, 3584, 152, 64) == U
+    # few K blocks bound the splits: 2 ranks x 1 block of 64 -> 2 splits
+    assert fcc.fcc_choose_algo(gemv, 2, 8, 512, 64, 152) == F

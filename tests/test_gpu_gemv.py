@@ -21,6 +21,10 @@ import gemm_collective_gb300 as fcc  # noqa: E402
 
 
 def _run(R, A, B, M, N, K, out_dtype=fcc.FCC_F32, opts=None):
+    """opts None: the fused kernel (asked for explicitly: AUTO may pick the
+    plain form for shapes with few column groups)."""
+    if opts is None:
+        opts = fcc.make_opts(algo=fcc.FCC_ALGO_FUSED)
     dA = [dev_bf16(a) for a in A]
     dB = [dev_bf16(b) for b in B]
     tdt = torch.float32 if out_dtype == fcc.FCC_F32 else torch.bfloat16
@@ -62,7 +66,7 @@ def test_gemv_grid_sizes(ctas):
     """The stream-K split and the last-arriver sum hold for any grid size."""
     R, M, N, K = 4, 8, 1024, 448
     A, B = synth.gemm_inputs(R, M, N, K, 1.0, 0.02, seed=5)
-    outs = _run(R, A, B, M, N, K, opts=fcc.make_opts(max_ctas=ctas))
+    outs = _run(R, A, B, M, N, K, opts=fcc.make_opts(algo=fcc.FCC_ALGO_FUSED, max_ctas=ctas))
     assert_close(to_f64(outs[0]), oracle.gemv_ar(A, B))
 
 
@@ -74,6 +78,19 @@ def test_gemv_unfused_baselines(algo):
     ref = oracle.gemv_ar(A, B)
     for r in range(R):
         assert_close(to_f64(outs[r]), ref)
+
+
+@pytest.mark.parametrize("N,want", [(512, fcc.FCC_ALGO_UNFUSED), (8192, fcc.FCC_ALGO_FUSED)])
+def test_gemv_auto_follows_the_selector(N, want):
+    """AUTO runs what fcc_choose_algo names (the plain form launches two
+    kernels, the fused one), and either is correct."""
+    R, M, K = 8, 8, 512
+    A, B = synth.gemm_inputs(R, M, N, K, 1.0, 0.02, seed=N)
+    assert fcc.fcc_choose_algo(fcc.FCC_OP_GEMV_AR, R, M, N, K) == want
+    l0 = fcc.fcc_launch_count()
+    outs = _run(R, A, B, M, N, K, opts=fcc.make_opts())
+    assert fcc.fcc_launch_count() - l0 == (2 if want == fcc.FCC_ALGO_UNFUSED else 1)
+    assert_close(to_f64(outs[0]), oracle.gemv_ar(A, B))
 
 
 def test_gemv_full_decode_workload():
