@@ -58,9 +58,10 @@ def _load():
         lib.orc_moe_expert_rows.argtypes = [I, P, P, I64, I64, I64, I, P, P, P, I64, P]
         lib.orc_moe_combine_rows.argtypes = [I, P, P, I64, I64, I64, I, I, P, P, P, P, I64,
                                              P]
+        lib.orc_embedding_bags.argtypes = [I, P, I64, I64, P, P, I64, P, P, I64, P]
         for f in (lib.orc_rank_sum_rows, lib.orc_gemm_rs_rows, lib.orc_ag_gemm_rows,
                   lib.orc_moe_route, lib.orc_moe_dispatch, lib.orc_moe_expert_rows,
-                  lib.orc_moe_combine_rows):
+                  lib.orc_moe_combine_rows, lib.orc_embedding_bags):
             f.restype = I
         _lib = lib
         return lib
@@ -233,6 +234,37 @@ def moe_combine(X, W, src_rank, src_tok, idx, gate) -> np.ndarray:
     if rc:
         raise ValueError(f"orc_moe_combine_rows: bad argument ({rc})")
     return out
+
+
+def embedding_bags(tables, offsets, indices, bag_table, bag_sample) -> np.ndarray:
+    """Pooled (summed) rows of the bags (bag_table[i], bag_sample[i]) in fp64, [n, D].
+    tables: list of [V, D] bf16; offsets[tau]: [nsamples + 1]; indices[tau]: [nnz]."""
+    V, D = tables[0].shape
+    nsamples = len(offsets[0]) - 1
+    kt, pt = _ptr_array(tables, np.uint16)
+    ko, po = _ptr_array(offsets, np.int32)
+    ki, pi = _ptr_array(indices, np.int32)
+    bt = np.ascontiguousarray(bag_table, dtype=np.int32)
+    bs = np.ascontiguousarray(bag_sample, dtype=np.int64)
+    out = np.empty((bt.size, D), dtype=np.float64)
+    rc = _load().orc_embedding_bags(len(tables), pt, V, D, po, pi, nsamples, bt.ctypes.data,
+                                    bs.ctypes.data, bt.size, out.ctypes.data)
+    if rc:
+        raise ValueError(f"orc_embedding_bags: bad argument ({rc})")
+    return out
+
+
+def embedding_a2a(tables, offsets, indices, R: int):
+    """The all-to-all result: out[r] is [Bl, ntables, D], row (b, tau) the pooled
+    bag (tau, r*Bl + b), where Bl = nsamples / R samples live on each rank."""
+    ntab = len(tables)
+    nsamples = len(offsets[0]) - 1
+    Bl = nsamples // R
+    g = np.repeat(np.arange(nsamples, dtype=np.int64), ntab)   # sample-major, table-minor
+    tau = np.tile(np.arange(ntab, dtype=np.int32), nsamples)
+    rows = embedding_bags(tables, offsets, indices, tau, g)
+    D = rows.shape[1]
+    return [rows[r * Bl * ntab:(r + 1) * Bl * ntab].reshape(Bl, ntab, D) for r in range(R)]
 
 
 def bf16_to_f64(bits) -> np.ndarray:

@@ -357,3 +357,48 @@ int orc_moe_combine_rows(int R, const uint16_t *const *X, const uint16_t *const 
     }
     return bad ? 3 : 0;
 }
+
+/*
+ * Embedding + All-to-All (SC24 abstract: the embedding + All-to-All operator
+ * for DLRM).  Table tau is a [V, D] matrix; bag (tau, g) of global sample g
+ * is the index list indices_tau[offsets_tau[g] .. offsets_tau[g+1]).  The
+ * pooled vector of a bag is the sum of its rows (an empty bag gives zeros):
+ *   out[i][d] = sum over k in bag (bag_table[i], bag_sample[i]) of
+ *               table_{bag_table[i]}[indices[k]][d]
+ * summed in bag order.  The all-to-all that sends sample g's vectors to its
+ * rank is a placement of these rows, done by the Python wrapper.
+ */
+int orc_embedding_bags(int ntables, const uint16_t *const *tables, int64_t V, int64_t D,
+                       const int32_t *const *offsets, const int32_t *const *indices,
+                       int64_t nsamples, const int32_t *bag_table, const int64_t *bag_sample,
+                       int64_t nbags, double *out)
+{
+    if (ntables < 1 || V < 1 || D < 1 || nbags < 0)
+        return 1;
+    for (int64_t i = 0; i < nbags; ++i) {
+        const int tau = bag_table[i];
+        const int64_t g = bag_sample[i];
+        if (tau < 0 || tau >= ntables || g < 0 || g >= nsamples)
+            return 1;
+        const int32_t k0 = offsets[tau][g], k1 = offsets[tau][g + 1];
+        if (k0 < 0 || k1 < k0)
+            return 1;
+        for (int32_t k = k0; k < k1; ++k)
+            if (indices[tau][k] < 0 || indices[tau][k] >= V)
+                return 1;
+    }
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < nbags; ++i) {
+        const int tau = bag_table[i];
+        const int64_t g = bag_sample[i];
+        double *o = out + i * D;
+        for (int64_t d = 0; d < D; ++d)
+            o[d] = 0.0;
+        for (int32_t k = offsets[tau][g]; k < offsets[tau][g + 1]; ++k) {
+            const uint16_t *row = tables[tau] + (int64_t)indices[tau][k] * D;
+            for (int64_t d = 0; d < D; ++d)
+                o[d] += bf16_to_double(row[d]);
+        }
+    }
+    return 0;
+}

@@ -9,7 +9,8 @@ raw bits; router logits stay float32.
 
 Draw order is fixed per workload so that a seed fully determines every byte:
 GEMM workloads draw A_0..A_{R-1} then B_0..B_{R-1}; the MoE workload draws
-X_0..X_{R-1}, then logits_0..logits_{R-1}, then W_0..W_{E-1}.
+X_0..X_{R-1}, then logits_0..logits_{R-1}, then W_0..W_{E-1}; the embedding
+workload draws the tables 0..n-1, then per table the bag sizes and indices.
 """
 from __future__ import annotations
 
@@ -26,6 +27,7 @@ __all__ = [
     "gemm_inputs",
     "integer_gemm_inputs",
     "moe_inputs",
+    "embedding_inputs",
     "WORKLOADS",
     "Workload",
 ]
@@ -99,11 +101,30 @@ def moe_inputs(R: int, T: int, H: int, E: int, F: int, std_x: float = 1.0,
     return X, logits, W
 
 
+def embedding_inputs(R: int, ntables: int, V: int, D: int, Bl: int, L: int,
+                     min_bag: int = 1, std: float = 1.0, seed: int = 0):
+    """Embedding tables [V, D] bf16 (N(0, std)), and per table the bags of the
+    R * Bl samples of the global batch in CSR form: bag sizes uniform in
+    [min_bag, 2L - min_bag] (mean L), indices uniform in [0, V).
+    Returns (tables, offsets, indices): offsets[t] int32 [R*Bl + 1]."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    tables = [normal_bf16(rng, (V, D), std) for _ in range(ntables)]
+    n = R * Bl
+    offsets, indices = [], []
+    for _ in range(ntables):
+        sizes = rng.integers(min_bag, 2 * L - min_bag + 1, size=n, dtype=np.int64)
+        off = np.zeros(n + 1, dtype=np.int64)
+        np.cumsum(sizes, out=off[1:])
+        offsets.append(off.astype(np.int32))
+        indices.append(rng.integers(0, V, size=int(off[-1]), dtype=np.int32))
+    return tables, offsets, indices
+
+
 @dataclass(frozen=True)
 class Workload:
     """One named workload: shapes, value distributions and output dtype."""
     name: str
-    op: str            # gemm_rs | gemm_ar | gemv_ar | ag_gemm | moe
+    op: str            # gemm_rs | gemm_ar | gemv_ar | ag_gemm | moe | emb_a2a
     R: int
     M: int = 0         # GEMM rows (all ranks for AG: R * rows per rank)
     N: int = 0
@@ -116,6 +137,17 @@ class Workload:
     E: int = 0
     F: int = 0
     topk: int = 0
+    tables: int = 0    # embedding: tables (tables / R owned by each rank)
+    B: int = 0         # embedding: samples per rank
+    V: int = 0         # embedding: rows per table
+    D: int = 0         # embedding: row width
+    L: int = 0         # embedding: mean bag size (pooling factor)
+
+    def emb_bytes(self) -> int:
+        """Embedding: rows read once per lookup plus the pooled outputs written once
+        (bf16), the mean lookup count taken as R * Bl * tables * L."""
+        n = self.R * self.B * self.tables
+        return n * self.L * self.D * 2 + n * self.D * 2
 
     def flops(self) -> float:
         """2 * useful multiply-adds of the workload."""
@@ -150,4 +182,9 @@ WORKLOADS = {
     "moe_r8_t4096_h4096_e64_f1408": Workload("moe_r8_t4096_h4096_e64_f1408", "moe", R=8,
                                              T=4096, H=4096, E=64, F=1408, topk=2,
                                              std_a=1.0, std_b=0.02, out="bf16"),
+    # Embedding + all-to-all (DLRM-style): 8 ranks x 8 tables of 65536 x 128
+    # rows, 2048 samples per rank, bags of 32 rows on average.
+    "emb_a2a_r8_t64_v65536_d128_b2048_l32": Workload(
+        "emb_a2a_r8_t64_v65536_d128_b2048_l32", "emb_a2a", R=8, tables=64, B=2048,
+        V=65536, D=128, L=32, std_a=1.0, out="bf16"),
 }

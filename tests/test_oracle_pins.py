@@ -446,5 +446,62 @@ def test_combine_dropped_slot_adds_nothing():
     assert np.array_equal(got, only0)
 
 
+# ------------------------------------------------------- embedding + all-to-all
+
+def test_embedding_bag_of_one_is_the_row():
+    """Bags of exactly one row: the pooled vector is that table row (numpy indexing)."""
+    R, ntab, V, D, Bl = 2, 4, 50, 8, 6
+    tables, offsets, indices = synth.embedding_inputs(R, ntab, V, D, Bl, L=1, seed=41)
+    out = oracle.embedding_a2a(tables, offsets, indices, R)
+    for r in range(R):
+        for b in range(Bl):
+            for t in range(ntab):
+                g = r * Bl + b
+                row = _f64(tables[t])[indices[t][offsets[t][g]]]
+                assert np.array_equal(out[r][b, t], row)
+
+
+def test_embedding_single_rank_is_reduceat():
+    """R = 1: each table's bags are numpy add.reduceat over the gathered rows."""
+    tables, offsets, indices = synth.embedding_inputs(1, 3, 40, 16, 10, L=4, seed=42)
+    out = oracle.embedding_a2a(tables, offsets, indices, 1)[0]
+    for t in range(3):
+        rows = _f64(tables[t])[indices[t]]
+        ref = np.add.reduceat(rows, offsets[t][:-1], axis=0)
+        assert np.allclose(out[:, t], ref, rtol=1e-14, atol=1e-14)
+
+
+def test_embedding_closed_form_places_bags():
+    """Row v of table t holds t + v + d (exact in bf16): bag (t, g) pools to
+    n*(t + d) + sum of its indices, and lands at rank g // Bl, sample g % Bl."""
+    R, ntab, V, D, Bl = 4, 3, 16, 6, 5
+    _, offsets, indices = synth.embedding_inputs(R, ntab, V, D, Bl, L=3, seed=43)
+    tables = [_bf16([t + v + d for v in range(V) for d in range(D)], (V, D))
+              for t in range(ntab)]
+    out = oracle.embedding_a2a(tables, offsets, indices, R)
+    for g in range(R * Bl):
+        for t in range(ntab):
+            ix = indices[t][offsets[t][g]:offsets[t][g + 1]]
+            want = len(ix) * (t + np.arange(D)) + ix.sum()
+            assert np.array_equal(out[g // Bl][g % Bl, t], want.astype(np.float64))
+
+
+def test_embedding_brute_force_and_empty_bags():
+    R, ntab, V, D, Bl = 2, 2, 9, 4, 4
+    tables, offsets, indices = synth.embedding_inputs(R, ntab, V, D, Bl, L=2, min_bag=0,
+                                                      seed=44)
+    assert any(offsets[t][g] == offsets[t][g + 1] for t in range(ntab) for g in range(R * Bl))
+    out = oracle.embedding_a2a(tables, offsets, indices, R)
+    for r in range(R):
+        for b in range(Bl):
+            for t in range(ntab):
+                g = r * Bl + b
+                acc = [0.0] * D
+                for k in range(offsets[t][g], offsets[t][g + 1]):
+                    for d in range(D):
+                        acc[d] += float(_f64(tables[t])[indices[t][k], d])
+                assert np.allclose(out[r][b, t], acc, rtol=1e-15, atol=0)
+
+
 def test_oracle_threads_reported():
     assert oracle.num_threads() >= 1
