@@ -89,6 +89,10 @@ _moe = _sig("fcc_moe_dispatch_gemm", _I,
 _combine = _sig("fcc_moe_combine", _I,
                 [_I, _P, _I64, _I64, _I64, _I, _I, _P, _P, _P, _P, _P, _I, _I, _OPTS, _P])
 _combine_ws = _sig("fcc_moe_combine_workspace_size", ctypes.c_size_t, [_I, _I64, _I])
+_emb = _sig("fcc_embedding_a2a", _I,
+            [_I, _I, _P, _I64, _I64, _I64, _P, _P, _P, _I, _I, _OPTS, _P])
+_emb_ws = _sig("fcc_embedding_workspace_size", ctypes.c_size_t,
+               [_I, _I, _I64, _I64, _I, _OPTS])
 _ws = _sig("fcc_workspace_size", ctypes.c_size_t, [_I, _I, _I64, _I64, _I64, _OPTS])
 _moe_ws = _sig("fcc_moe_workspace_size", ctypes.c_size_t,
                [_I, _I64, _I64, _I64, _I, _I, _I64, _OPTS])
@@ -188,6 +192,17 @@ def fcc_moe_combine(R, recv_y, cap, T, F, E, topk, topk_idx, topk_gate, recv_src
 
 def fcc_moe_combine_workspace_size(R, T, topk) -> int:
     return int(_combine_ws(R, T, topk))
+
+
+def fcc_embedding_a2a(R, ntables, tables, V, D, Bl, offsets, indices, out,
+                      in_dtype=FCC_BF16, out_dtype=FCC_BF16, opts=None, stream=None):
+    _check(_emb(R, ntables, _ptrs(tables), V, D, Bl, _ptrs(offsets), _ptrs(indices),
+                _ptrs(out), in_dtype, out_dtype, _opts(opts), _stream(stream)),
+           "fcc_embedding_a2a")
+
+
+def fcc_embedding_workspace_size(R, ntables, D, Bl, out_dtype=FCC_BF16, opts=None) -> int:
+    return int(_emb_ws(R, ntables, D, Bl, out_dtype, _opts(opts)))
 
 
 def fcc_choose_algo(op, R, M, N, K, sms=0, max_ctas=0) -> int:

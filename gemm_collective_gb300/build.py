@@ -19,7 +19,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libfcc.so")
-SOURCES = ["fcc_api.cu", "fcc_gemm.cu", "fcc_gemv.cu", "fcc_aux.cu", "fcc_moe.cu", "fcc_combine.cu"]
+SOURCES = ["fcc_api.cu", "fcc_gemm.cu", "fcc_gemv.cu", "fcc_aux.cu", "fcc_moe.cu", "fcc_combine.cu",
+           "fcc_embedding.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

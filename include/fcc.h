@@ -52,6 +52,7 @@ typedef struct CUstream_st *fcc_stream_t;
 
 #define FCC_MAX_RANKS 8
 #define FCC_MAX_EXPERTS 64
+#define FCC_MAX_TABLES 256  /* embedding tables per call */
 
 typedef enum { FCC_BF16 = 0, FCC_F16 = 1, FCC_F32 = 2 } fcc_dtype;
 
@@ -235,6 +236,35 @@ fcc_status fcc_moe_combine(int R, const void *const *recv_y, int64_t cap, int64_
                            const float *const *topk_gate, const int32_t *const *recv_src,
                            const int32_t *expert_counts, void *const *y, fcc_dtype in,
                            fcc_dtype out_dtype, const fcc_opts *opts, fcc_stream_t stream);
+
+/*
+ * Embedding + All-to-All (SC24 abstract: the embedding + All-to-All operator
+ * for DLRM).  ntables embedding tables [V, D] (table t owned by rank
+ * t / (ntables / R)); R ranks with Bl samples each (global sample g lives on
+ * rank g / Bl).  Bag (t, g) is the index list
+ * indices[t][offsets[t][g] .. offsets[t][g + 1]) into table t; its pooled
+ * vector is the sum of those rows (f32, then stored in out_dtype; an empty
+ * bag gives zeros).  The all-to-all delivers it to the sample's rank:
+ *   out[g / Bl][g % Bl][t][:] = pooled vector of bag (t, g)
+ * tables[t]: [V, D] bf16; offsets[t]: [R*Bl + 1] int32, non-decreasing;
+ * indices[t]: [offsets[t][R*Bl]] int32 in [0, V); out[r]: [Bl, ntables, D]
+ * (bf16 or f32).  R <= 8, ntables % R == 0, ntables <= FCC_MAX_TABLES,
+ * D % 8 == 0.  opts->algo: AUTO / FUSED = one kernel pools each bag and
+ * stores it straight into its sample's rank buffer; UNFUSED = each table's
+ * pooled vectors into a [ntables, R*Bl, D] workspace, then a kernel moves
+ * them to the sample ranks; CE = the same workspace moved by copy-engine 2-D
+ * copies (one per table and rank).  A negative offset step or an index
+ * outside [0, V) is not read: the bag skips it and FCC_ERR_INVALID is
+ * recorded in the status word.  Within a call the result is repeatable (a
+ * fixed summation order).  Uses workspace for UNFUSED / CE
+ * (fcc_embedding_workspace_size).
+ */
+fcc_status fcc_embedding_a2a(int R, int ntables, const void *const *tables, int64_t V,
+                             int64_t D, int64_t Bl, const int32_t *const *offsets,
+                             const int32_t *const *indices, void *const *out, fcc_dtype in,
+                             fcc_dtype out_dtype, const fcc_opts *opts, fcc_stream_t stream);
+size_t fcc_embedding_workspace_size(int R, int ntables, int64_t D, int64_t Bl,
+                                    fcc_dtype out_dtype, const fcc_opts *opts);
 
 /* Scratch bytes a call needs (for opts->workspace); 0 if none. */
 size_t fcc_workspace_size(fcc_op op, int R, int64_t M, int64_t N, int64_t K,
