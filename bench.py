@@ -496,6 +496,42 @@ def other_ops(fcc, torch, np, synth, dev, stream, dA_rs, dB_rs, pk, only=None):
         ops[w.name] = res
         del Xall, dX, dL, dW, recv_y, recv_x, y
 
+    # Embedding + all-to-all (DLRM pooled lookups)
+    if want("emb_a2a_r8_t64_v65536_d128_b2048_l32"):
+        w = synth.WORKLOADS["emb_a2a_r8_t64_v65536_d128_b2048_l32"]
+        tables, offsets, indices = synth.embedding_inputs(w.R, w.tables, w.V, w.D, w.B, w.L,
+                                                          std=w.std_a, seed=0)
+        dt = [up(t) for t in tables]
+        do = [torch.from_numpy(o).to(dev) for o in offsets]
+        di = [torch.from_numpy(i).to(dev) for i in indices]
+        out = [torch.empty((w.B, w.tables, w.D), dtype=torch.bfloat16, device=dev)
+               for _ in range(w.R)]
+        lookups = int(sum(int(o[-1]) for o in offsets))
+        # algorithmic bytes: every input read once (tables, indices, offsets) and
+        # every pooled vector written once; the rows gathered (lookups x D x 2)
+        # reach the SMs from L2 and are reported beside it.
+        byts = (w.tables * w.V * w.D * 2 + lookups * 4 + w.tables * (w.R * w.B + 1) * 4
+                + w.R * w.B * w.tables * w.D * 2)
+        gathered = lookups * w.D * 2
+        res = {}
+        for name, a in [("fused", fcc.FCC_ALGO_FUSED), ("unfused", fcc.FCC_ALGO_UNFUSED),
+                        ("copy_engine", fcc.FCC_ALGO_CE)]:
+            o = fcc.make_opts(algo=a)
+            t = time_calls(lambda o=o: fcc.fcc_embedding_a2a(w.R, w.tables, dt, w.V, w.D, w.B,
+                                                             do, di, out, 0, 0, o, stream),
+                           10, 3, stream)
+            res[name] = {"us": t * 1e3, "GB/s": byts / (t * 1e-3) / 1e9,
+                         "gathered_GB/s": gathered / (t * 1e-3) / 1e9}
+        auto = fcc.fcc_choose_algo(fcc.FCC_OP_EMBEDDING_A2A, w.R, 0, 0, 0)
+        res["auto"] = {fcc.FCC_ALGO_FUSED: "fused", fcc.FCC_ALGO_UNFUSED: "unfused",
+                       fcc.FCC_ALGO_CE: "copy_engine"}[auto]
+        res["roofline_frac"] = res[res["auto"]]["GB/s"] / hbm
+        res["algorithmic_bytes"] = byts
+        res["gathered_bytes"] = gathered
+        res["lookups"] = lookups
+        ops[w.name] = res
+        del dt, do, di, out, tables, offsets, indices
+
     st = fcc.fcc_stream_status(stream)
     if st != fcc.FCC_OK:
         raise RuntimeError(f"device status after the operator legs: {fcc.fcc_status_string(st)}")

@@ -33,7 +33,7 @@ FCC_BF16, FCC_F16, FCC_F32 = 0, 1, 2
  FCC_ERR_TIMEOUT, FCC_ERR_WORKSPACE) = range(7)
 (FCC_ALGO_AUTO, FCC_ALGO_FUSED, FCC_ALGO_UNFUSED, FCC_ALGO_INTERDECOM,
  FCC_ALGO_CE) = range(5)
-FCC_OP_GEMM_RS, FCC_OP_GEMM_AR, FCC_OP_GEMV_AR, FCC_OP_AG_GEMM = range(4)
+FCC_OP_GEMM_RS, FCC_OP_GEMM_AR, FCC_OP_GEMV_AR, FCC_OP_AG_GEMM, FCC_OP_EMBEDDING_A2A = range(5)
 FCC_MAX_RANKS = 8
 FCC_MAX_EXPERTS = 64
 

@@ -113,6 +113,8 @@ fcc_algo algo_of(const fcc_opts* o) {
   return o->algo;
 }
 
+}  // namespace
+
 // The strategy for FCC_ALGO_AUTO, from measurements on GB300 (8 ranks, bf16):
 //  * GEMM + RS / AR and AG + GEMM: the fused kernel beat the plain GEMM +
 //    reduce, the InterDecom pipeline and the copy-engine path at every shape
@@ -130,8 +132,16 @@ fcc_algo choose_algo(fcc_op op, int R, int64_t M, int64_t N, int64_t K, int sms,
     gemv_shape(N, R, K, sms, max_ctas, &groups, &splits);
     return splits >= 16 ? FCC_ALGO_UNFUSED : FCC_ALGO_FUSED;
   }
+  //  * Embedding + All-to-All: pooling table by table into a staging buffer,
+  //    then the exchange kernel, took 1.18 ms against 1.30 ms for the fused
+  //    store of each pooled row to its sample's rank (8 ranks x 64 tables of
+  //    65536 x 128, 2048 samples a rank, bags of 32): same SM cycles for the
+  //    gather, slower scattered stores.
+  if (op == FCC_OP_EMBEDDING_A2A) return FCC_ALGO_UNFUSED;
   return FCC_ALGO_FUSED;
 }
+
+namespace {
 
 bool deterministic_of(const fcc_opts* o) { return o == nullptr || o->deterministic != 0; }
 
@@ -764,7 +774,9 @@ fcc_algo fcc_choose_algo(fcc_op op, int R, int64_t M, int64_t N, int64_t K, int 
       sms = 152;
     }
   }
-  if (R < 1 || R > FCC_MAX_RANKS || N <= 0 || K <= 0) return FCC_ALGO_FUSED;
+  // (M, N, K describe the GEMM operators; the embedding's choice needs none)
+  if (op != FCC_OP_EMBEDDING_A2A && (R < 1 || R > FCC_MAX_RANKS || N <= 0 || K <= 0))
+    return FCC_ALGO_FUSED;
   return choose_algo(op, R, M, N, K, sms, max_ctas);
 }
 

@@ -7,8 +7,8 @@
 // result straight into the sample's rank buffer, so the pooled vectors never
 // make a round trip through a staging buffer.
 //
-// The work is a random gather of table rows from HBM (D = 128 bf16: 256-byte
-// rows).  A warp loads its bag's indices 32 at a time (one per lane) and
+// The work is a random gather of table rows (D = 128 bf16: 256-byte rows),
+// done table by table so that a table's rows are served from L2 once read.  A warp loads its bag's indices 32 at a time (one per lane) and
 // passes them round by shuffles; 32 / (D/8) rows are read per step (16 bytes
 // a lane), four steps unrolled, so a warp has up to eight rows in flight.
 // The row groups' f32 partial sums are added by a fixed shuffle tree: the
@@ -127,16 +127,17 @@ __global__ void __launch_bounds__(256) embedding_kernel(const EmbArgs a) {
   const long long esz = a.out_f32 ? 4 : 2;
   for (long long it = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
        it < items; it += nwarps) {
-    long long g;
-    int t;
+    // Table-major order: the warps running at once gather from one table,
+    // which stays in L2 while its bags are pooled (random indices reuse its
+    // rows many times), whichever buffer the vectors go to.  (Interleaving
+    // 4, 8 or 16 tables, so that consecutive bags fill adjacent output rows,
+    // measured slower: the larger live set costs L2 hits.)
+    const int t = static_cast<int>(it / nsamp);
+    const long long g = it - static_cast<long long>(t) * nsamp;
     char* dst;
     if constexpr (STAGED) {
-      t = static_cast<int>(it / nsamp);       // table-major: one owner's bags together
-      g = it - static_cast<long long>(t) * nsamp;
       dst = static_cast<char*>(a.pooled) + (static_cast<long long>(t) * nsamp + g) * a.D * esz;
     } else {
-      g = it / a.ntables;                     // sample-major: output rows in order
-      t = static_cast<int>(it - g * a.ntables);
       const int r = static_cast<int>(g / a.Bl);
       const long long b = g - static_cast<long long>(r) * a.Bl;
       dst = static_cast<char*>(a.out[r]) + (b * a.ntables + t) * a.D * esz;
@@ -182,7 +183,9 @@ size_t emb_ws_bytes(int R, int ntables, int64_t D, int64_t Bl, fcc_dtype out_dty
 }
 
 fcc_algo emb_algo(const fcc_opts* o) {
-  return (o == nullptr || o->algo == FCC_ALGO_AUTO) ? FCC_ALGO_FUSED : o->algo;
+  return (o == nullptr || o->algo == FCC_ALGO_AUTO) ? choose_algo(FCC_OP_EMBEDDING_A2A, 0, 0, 0,
+                                                                  0, 0, 0)
+                                                    : o->algo;
 }
 
 }  // namespace

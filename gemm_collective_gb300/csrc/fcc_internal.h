@@ -149,4 +149,6 @@ fcc_status internal_make_map(CUtensorMap* m, const void* ptr, int64_t rows, int6
                              uint32_t box_rows);
 // A side stream and n <= 8 events of the current device (after internal_prepare).
 fcc_status internal_side_stream(cudaStream_t* side, cudaEvent_t* ev, int n);
+// The algorithm FCC_ALGO_AUTO runs (the strategy selector, fcc_api.cu).
+fcc_algo choose_algo(fcc_op op, int R, int64_t M, int64_t N, int64_t K, int sms, int max_ctas);
 }  // namespace fcc

@@ -118,11 +118,13 @@ def test_embedding_full_workload_sampled():
     w = synth.WORKLOADS["emb_a2a_r8_t64_v65536_d128_b2048_l32"]
     tables, offsets, indices = synth.embedding_inputs(w.R, w.tables, w.V, w.D, w.B, w.L,
                                                       std=w.std_a, seed=0)
-    out, st = _run(w.R, w.tables, w.V, w.D, w.B, *_upload(tables, offsets, indices))
-    assert st == fcc.FCC_OK
+    dev = _upload(tables, offsets, indices)
     rng = np.random.Generator(np.random.PCG64(1))
     g = rng.integers(0, w.R * w.B, size=64)
     t = rng.integers(0, w.tables, size=64)
     ref = oracle.embedding_bags(tables, offsets, indices, t, g)
-    got = np.stack([to_f64(out[gi // w.B][gi % w.B, ti]) for gi, ti in zip(g, t)])
-    assert_close(got, ref, "sampled bags")
+    for algo in (fcc.FCC_ALGO_AUTO, fcc.FCC_ALGO_FUSED):
+        out, st = _run(w.R, w.tables, w.V, w.D, w.B, *dev, algo=algo)
+        assert st == fcc.FCC_OK
+        got = np.stack([to_f64(out[gi // w.B][gi % w.B, ti]) for gi, ti in zip(g, t)])
+        assert_close(got, ref, f"sampled bags (algo {algo})")
