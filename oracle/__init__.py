@@ -59,9 +59,10 @@ def _load():
         lib.orc_moe_combine_rows.argtypes = [I, P, P, I64, I64, I64, I, I, P, P, P, P, I64,
                                              P]
         lib.orc_embedding_bags.argtypes = [I, P, I64, I64, P, P, I64, P, P, I64, P]
+        lib.orc_attention_rows.argtypes = [I, P, P, P, I64, I, I64, I, I64, P, P, P, P]
         for f in (lib.orc_rank_sum_rows, lib.orc_gemm_rs_rows, lib.orc_ag_gemm_rows,
                   lib.orc_moe_route, lib.orc_moe_dispatch, lib.orc_moe_expert_rows,
-                  lib.orc_moe_combine_rows, lib.orc_embedding_bags):
+                  lib.orc_moe_combine_rows, lib.orc_embedding_bags, lib.orc_attention_rows):
             f.restype = I
         _lib = lib
         return lib
@@ -265,6 +266,37 @@ def embedding_a2a(tables, offsets, indices, R: int):
     rows = embedding_bags(tables, offsets, indices, tau, g)
     D = rows.shape[1]
     return [rows[r * Bl * ntab:(r + 1) * Bl * ntab].reshape(Bl, ntab, D) for r in range(R)]
+
+
+def attention_rows(Q, K, V, causal, rank, row, head) -> np.ndarray:
+    """Exact softmax attention (fp64) of the query rows (rank[i], row[i], head[i])
+    over the keys and values of all shards; Q[r], K[r], V[r] are [S, H, d] bf16."""
+    R = len(Q)
+    S, H, d = Q[0].shape
+    kq, pq = _ptr_array([q.reshape(-1) for q in Q], np.uint16)
+    kk, pk = _ptr_array([k.reshape(-1) for k in K], np.uint16)
+    kv, pv = _ptr_array([v.reshape(-1) for v in V], np.uint16)
+    rk = np.ascontiguousarray(rank, dtype=np.int32)
+    rw = np.ascontiguousarray(row, dtype=np.int64)
+    hd = np.ascontiguousarray(head, dtype=np.int32)
+    out = np.empty((rk.size, d), dtype=np.float64)
+    rc = _load().orc_attention_rows(R, pq, pk, pv, S, H, d, 1 if causal else 0, rk.size,
+                                    rk.ctypes.data, rw.ctypes.data, hd.ctypes.data,
+                                    out.ctypes.data)
+    if rc:
+        raise ValueError(f"orc_attention_rows: bad argument ({rc})")
+    return out
+
+
+def ring_attention(Q, K, V, causal=False):
+    """All output rows: a list of [S, H, d] fp64 arrays, one per rank."""
+    R = len(Q)
+    S, H, d = Q[0].shape
+    rank = np.repeat(np.arange(R), S * H)
+    row = np.tile(np.repeat(np.arange(S), H), R)
+    head = np.tile(np.arange(H), R * S)
+    o = attention_rows(Q, K, V, causal, rank, row, head)
+    return [o[r * S * H:(r + 1) * S * H].reshape(S, H, d) for r in range(R)]
 
 
 def bf16_to_f64(bits) -> np.ndarray:

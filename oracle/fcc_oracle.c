@@ -402,3 +402,67 @@ int orc_embedding_bags(int ntables, const uint16_t *const *tables, int64_t V, in
     }
     return 0;
 }
+
+/*
+ * Ring attention (the mKernel article's fused kernel list names Ring
+ * Attention; read as exact softmax attention of each rank's queries over the
+ * keys and values of all R sequence shards, which the ring brings round).
+ * The global sequence is shard-major: rank q's row t is position q*S + t.
+ *   s_j   = (Q_r[i][h] . K_{j/S}[j%S][h]) / sqrt(d)
+ *   O_r[i][h][:] = sum_j exp(s_j - max s) V_{j/S}[j%S][h][:] / sum_j exp(s_j - max s)
+ * over all positions j (causal: only j <= r*S + i).  Q, K, V, O rows are
+ * [S][H][d].  One output row (rank[i], row[i], head[i]) per entry.
+ */
+int orc_attention_rows(int R, const uint16_t *const *Q, const uint16_t *const *K,
+                       const uint16_t *const *V, int64_t S, int H, int64_t d, int causal,
+                       int64_t n, const int32_t *rank, const int64_t *row, const int32_t *head,
+                       double *out)
+{
+    if (R < 1 || S < 1 || H < 1 || d < 1 || n < 0)
+        return 1;
+    for (int64_t i = 0; i < n; ++i)
+        if (rank[i] < 0 || rank[i] >= R || row[i] < 0 || row[i] >= S || head[i] < 0 ||
+            head[i] >= H)
+            return 1;
+    const int64_t L = (int64_t)R * S;
+    const double scale = 1.0 / sqrt((double)d);
+    int bad = 0;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t i = 0; i < n; ++i) {
+        double *s = (double *)malloc((size_t)L * sizeof(double));
+        if (s == NULL) {
+#pragma omp atomic write
+            bad = 1;
+            continue;
+        }
+        const int r = rank[i], h = head[i];
+        const uint16_t *q = Q[r] + (row[i] * H + h) * d;
+        const int64_t pos = (int64_t)r * S + row[i];
+        const int64_t jend = causal ? pos + 1 : L;
+        double m = -INFINITY;
+        for (int64_t j = 0; j < jend; ++j) {
+            const uint16_t *k = K[j / S] + ((j % S) * H + h) * d;
+            double dot = 0.0;
+            for (int64_t c = 0; c < d; ++c)
+                dot += bf16_to_double(q[c]) * bf16_to_double(k[c]);
+            s[j] = dot * scale;
+            if (s[j] > m)
+                m = s[j];
+        }
+        double *o = out + i * d;
+        for (int64_t c = 0; c < d; ++c)
+            o[c] = 0.0;
+        double l = 0.0;
+        for (int64_t j = 0; j < jend; ++j) {
+            const double p = exp(s[j] - m);
+            l += p;
+            const uint16_t *v = V[j / S] + ((j % S) * H + h) * d;
+            for (int64_t c = 0; c < d; ++c)
+                o[c] += p * bf16_to_double(v[c]);
+        }
+        for (int64_t c = 0; c < d; ++c)
+            o[c] /= l;
+        free(s);
+    }
+    return bad ? 3 : 0;
+}

@@ -28,6 +28,7 @@ __all__ = [
     "integer_gemm_inputs",
     "moe_inputs",
     "embedding_inputs",
+    "attention_inputs",
     "WORKLOADS",
     "Workload",
 ]
@@ -118,6 +119,16 @@ def embedding_inputs(R: int, ntables: int, V: int, D: int, Bl: int, L: int,
         offsets.append(off.astype(np.int32))
         indices.append(rng.integers(0, V, size=int(off[-1]), dtype=np.int32))
     return tables, offsets, indices
+
+
+def attention_inputs(R: int, S: int, H: int, d: int, std: float = 1.0, seed: int = 0):
+    """Per rank Q_r, K_r, V_r [S, H, d] bf16, N(0, std), drawn Q_0..Q_{R-1},
+    K_0..K_{R-1}, V_0..V_{R-1}."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    Q = [normal_bf16(rng, (S, H, d), std) for _ in range(R)]
+    K = [normal_bf16(rng, (S, H, d), std) for _ in range(R)]
+    V = [normal_bf16(rng, (S, H, d), std) for _ in range(R)]
+    return Q, K, V
 
 
 @dataclass(frozen=True)

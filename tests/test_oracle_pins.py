@@ -503,5 +503,74 @@ def test_embedding_brute_force_and_empty_bags():
                 assert np.allclose(out[r][b, t], acc, rtol=1e-15, atol=0)
 
 
+# -------------------------------------------------------------- ring attention
+
+def _att(Q):
+    return [_f64(q.reshape(-1)).reshape(q.shape) for q in Q]
+
+
+def test_attention_one_rank_vs_library_softmax():
+    from scipy.special import softmax
+    Q, K, V = synth.attention_inputs(1, 12, 2, 16, seed=51)
+    got = oracle.ring_attention(Q, K, V)[0]
+    q, k, v = _att(Q)[0], _att(K)[0], _att(V)[0]
+    for h in range(2):
+        p = softmax(q[:, h] @ k[:, h].T / np.sqrt(16.0), axis=1)
+        assert np.allclose(got[:, h], p @ v[:, h], rtol=1e-12, atol=1e-13)
+
+
+def test_attention_shard_permutation_invariant():
+    """Non-causal: every query sees all (key, value) pairs; swapping two
+    ranks' K and V shards together changes nothing."""
+    Q, K, V = synth.attention_inputs(3, 7, 2, 8, seed=52)
+    a = oracle.ring_attention(Q, K, V)
+    perm = [2, 0, 1]
+    b = oracle.ring_attention(Q, [K[i] for i in perm], [V[i] for i in perm])
+    for r in range(3):
+        assert np.allclose(a[r], b[r], rtol=1e-12, atol=1e-14)
+
+
+def test_attention_zero_queries_average_the_values():
+    R, S, H, d = 2, 5, 3, 8
+    Q, K, V = synth.attention_inputs(R, S, H, d, seed=53)
+    Q = [np.zeros_like(q) for q in Q]
+    vall = np.concatenate(_att(V))                           # [R*S, H, d]
+    full = oracle.ring_attention(Q, K, V, causal=False)
+    caus = oracle.ring_attention(Q, K, V, causal=True)
+    for r in range(R):
+        assert np.allclose(full[r], vall.mean(axis=0)[None], rtol=1e-13, atol=1e-14)
+        for t in range(S):
+            p = r * S + t
+            assert np.allclose(caus[r][t], vall[:p + 1].mean(axis=0), rtol=1e-13, atol=1e-14)
+
+
+def test_attention_dominant_key_selects_its_value():
+    R, S, H, d = 2, 4, 1, 8
+    Q, K, V = synth.attention_inputs(R, S, H, d, seed=54)
+    q = np.full((S, H, d), 2.0, dtype=np.float32)
+    Q = [synth.f32_to_bf16_bits(q)] * R
+    k = synth.bf16_bits_to_f32(K[1]).copy()
+    k[2, 0, :] = 8.0                                         # score 2*8*8/sqrt(8) = 45 above the rest
+    K = [K[0], synth.f32_to_bf16_bits(k)]
+    got = oracle.ring_attention(Q, K, V)
+    want = _f64(V[1][2, 0])
+    for r in range(R):
+        assert np.allclose(got[r][:, 0], want[None], rtol=0, atol=1e-12)
+
+
+def test_attention_causal_brute_force():
+    import math
+    R, S, H, d = 2, 3, 1, 4
+    Q, K, V = synth.attention_inputs(R, S, H, d, seed=55)
+    q, k, v = (np.concatenate(_att(x)) for x in (Q, K, V))   # global positions
+    got = np.concatenate(oracle.ring_attention(Q, K, V, causal=True))
+    for p in range(R * S):
+        sc = [sum(q[p, 0, c] * k[j, 0, c] for c in range(d)) / math.sqrt(d) for j in range(p + 1)]
+        m = max(sc)
+        w = [math.exp(x - m) for x in sc]
+        o = [sum(w[j] * v[j, 0, c] for j in range(p + 1)) / sum(w) for c in range(d)]
+        assert np.allclose(got[p, 0], o, rtol=1e-13, atol=1e-15)
+
+
 def test_oracle_threads_reported():
     assert oracle.num_threads() >= 1
