@@ -103,6 +103,8 @@ _chunks = _sig("fcc_interdecom_chunks", _I, [ctypes.c_double, ctypes.c_double,
 _itime = _sig("fcc_interdecom_time", ctypes.c_double, [ctypes.c_double, ctypes.c_double,
                                                        ctypes.c_double, _I])
 _choose = _sig("fcc_choose_algo", _I, [_I, _I, _I64, _I64, _I64, _I, _I])
+_attn = _sig("fcc_ring_attention", _I,
+             [_I, _P, _P, _P, _P, _I64, _I, _I64, _I, _I, _I, _OPTS, _P])
 _launches = _sig("fcc_launch_count", ctypes.c_uint64, [])
 _version = _sig("fcc_version", ctypes.c_char_p, [])
 _wait_timeout = _sig("fcc_test_wait_timeout", _I, [_I64, _P])
@@ -203,6 +205,12 @@ def fcc_embedding_a2a(R, ntables, tables, V, D, Bl, offsets, indices, out,
 
 def fcc_embedding_workspace_size(R, ntables, D, Bl, out_dtype=FCC_BF16, opts=None) -> int:
     return int(_emb_ws(R, ntables, D, Bl, out_dtype, _opts(opts)))
+
+
+def fcc_ring_attention(R, Q, K, V, O, S, H, d, causal=False, in_dtype=FCC_BF16,
+                       out_dtype=FCC_BF16, opts=None, stream=None):
+    _check(_attn(R, _ptrs(Q), _ptrs(K), _ptrs(V), _ptrs(O), S, H, d, 1 if causal else 0,
+                 in_dtype, out_dtype, _opts(opts), _stream(stream)), "fcc_ring_attention")
 
 
 def fcc_choose_algo(op, R, M, N, K, sms=0, max_ctas=0) -> int:

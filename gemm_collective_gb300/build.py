@@ -20,7 +20,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libfcc.so")
 SOURCES = ["fcc_api.cu", "fcc_gemm.cu", "fcc_gemv.cu", "fcc_aux.cu", "fcc_moe.cu", "fcc_combine.cu",
-           "fcc_embedding.cu"]
+           "fcc_embedding.cu", "fcc_attention.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -1,0 +1,478 @@
+// fcc_attention.cu -- Ring attention over R sequence shards, tcgen05 (sm_103a).
+//
+// The mKernel article lists Ring Attention among its fused kernels: the
+// sequence is split over R ranks, each rank's queries attend to the keys and
+// values of every shard as the ring brings them round.  Here the R shards are
+// buffers of one GPU and a CTA walks the key/value blocks in ring order
+// (its own shard first, then r+1, r+2, ...), reading each block straight from
+// the shard that holds it: the ring's transfers are the CTA's own loads.
+//
+// One CTA per (rank, head, 128-query tile); d = 128.  Two passes over the
+// key/value blocks of 128 positions:
+//   pass 1  S = Q K^T (tcgen05, M = N = K = 128, f32 in TMEM) -> row maxima m;
+//   pass 2  S again; p = exp(s - m) (f32, <= 1), l += p; P (bf16) into shared
+//           memory as the A operand of O += P V (tcgen05, O in TMEM); at the
+//           end O / l.
+// With the final maxima known before any exponential, no accumulator ever
+// needs rescaling: one exponential per score, at the price of a second Q K^T.
+//
+// Warps: 0 = TMA producer (Q once, then K [and V] blocks into a two-stage
+// ring), 1 = MMA issue, 2-5 = softmax (TMEM lane quarter = 32 query rows each)
+// and the output.  Shared memory (128-byte swizzle throughout):
+//   Q   [128 q][128 d]    K-major, two 64-column atoms of 16 KiB
+//   K_j [128 keys][128 d] K-major (the B operand of Q K^T)
+//   V_j [128 keys][128 d] MN-major B operand of P V: two 64-column atoms
+//   P   [128 q][128 keys] K-major, written by the softmax threads
+// TMEM: S double buffer (2 x 128 columns) and O (128 columns).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+
+#include "fcc.h"
+#include "fcc_internal.h"
+#include "fcc_ptx.cuh"
+
+namespace fcc {
+namespace {
+
+constexpr int kD = 128;                          // head dimension
+constexpr int kBQ = 128;                         // query rows per CTA (MMA M)
+constexpr int kBKV = 128;                        // keys per block
+constexpr int kNS = 2;                           // key/value ring stages
+constexpr uint32_t kAtom = 128 * 128;            // 16 KiB: [128 rows][64 bf16]
+constexpr uint32_t kTile = 2 * kAtom;            // 32 KiB: [128][128] bf16
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS = 0, kColO = 256;       // S buffers at 0 and 128, O at 256
+constexpr uint64_t kDrainNs = 50ull * 1000 * 1000;
+// S = Q K^T: both operands K-major.  O += P V: A K-major, B (V) MN-major.
+constexpr uint32_t kIdescS = ptx::idesc_bf16_f32(kBQ, kBKV, false, false);
+constexpr uint32_t kIdescO = ptx::idesc_bf16_f32(kBQ, kD, false, true);
+// Q, 2 stages of K + V, P, then 12 barriers and 4 words.
+constexpr int kSmem = 1024 + kTile * (1 + 2 * kNS + 1) + 12 * 8 + 16;
+static_assert(kSmem <= 232448, "shared memory per CTA");
+
+struct AttnParams {
+  CUtensorMap mapQ[FCC_MAX_RANKS];   // [S, H*d] bf16, box {64, 128}
+  CUtensorMap mapK[FCC_MAX_RANKS];
+  CUtensorMap mapV[FCC_MAX_RANKS];
+  void* out[FCC_MAX_RANKS];          // [S, H, d]
+  int R, S, H;
+  int qtiles;                        // ceil(S / 128)
+  int kvb;                           // key blocks per shard: ceil(S / 128)
+  int causal;
+  int out_f32;
+  float scale_log2;                  // log2(e) / sqrt(d)
+  int* status;
+  unsigned long long timeout_ns;
+};
+
+// The key blocks a CTA visits, in ring order: block i of the walk is block
+// i % kvb of shard (r + i / kvb) % R.  With the causal mask a block whose
+// first position lies past the tile's last query is skipped (every role
+// applies the same test, so the barrier counts agree).
+struct Walk {
+  int r, kvb, R, S, causal;
+  long long q_last;                  // global position of the tile's last query row
+  __device__ __forceinline__ int total() const { return R * kvb; }
+  __device__ __forceinline__ int shard(int i) const { return (r + i / kvb) % R; }
+  __device__ __forceinline__ int row0(int i) const { return (i % kvb) * kBKV; }
+  __device__ __forceinline__ bool visible(int i) const {
+    if (!causal) return true;
+    return static_cast<long long>(shard(i)) * S + row0(i) <= q_last;
+  }
+};
+
+// K-major SW128 operand of 128 rows x 128 elements (two 64-element atoms):
+// descriptor of the 16-element K step kk.
+__device__ __forceinline__ uint64_t desc_kmajor(uint32_t base, int kk) {
+  return ptx::smem_desc_sw128(base + (kk >> 2) * kAtom + (kk & 3) * 32, 16, 1024);
+}
+// MN-major SW128 operand (V: keys down, d across in two 64-column atoms 16 KiB
+// apart): descriptor of the 16-key K step kk.
+__device__ __forceinline__ uint64_t desc_mnmajor(uint32_t base, int kk) {
+  return ptx::smem_desc_sw128(base + kk * 2048, kAtom, 1024);
+}
+
+
+__global__ void __launch_bounds__(192, 1) ring_attention_kernel(const __grid_constant__ AttnParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* sQ = smem;
+  uint8_t* sK = sQ + kTile;                    // stage s: sK + s * 2 * kTile
+  uint8_t* sP = sQ + kTile * (1 + 2 * kNS);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sP + kTile);
+  uint64_t* q_full = bars;
+  uint64_t* kv_full = bars + 1;                // [kNS]
+  uint64_t* kv_empty = bars + 1 + kNS;         // [kNS]
+  uint64_t* s_full = bars + 1 + 2 * kNS;       // [2]
+  uint64_t* s_empty = s_full + 2;              // [2]
+  uint64_t* p_full = s_empty + 2;
+  uint64_t* p_empty = p_full + 1;
+  uint64_t* o_full = p_empty + 1;
+  uint64_t* mma_done = o_full + 1;             // 1 + 2*kNS + 7 = 12 barriers
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  // CTA -> (rank, head, query tile)
+  const int per_rank = p.H * p.qtiles;
+  const int r = blockIdx.x / per_rank;
+  const int h = (blockIdx.x - r * per_rank) / p.qtiles;
+  const int qt = blockIdx.x - r * per_rank - h * p.qtiles;
+  Walk walk;
+  walk.r = r;
+  walk.kvb = p.kvb;
+  walk.R = p.R;
+  walk.S = p.S;
+  walk.causal = p.causal;
+  walk.q_last = static_cast<long long>(r) * p.S + min(p.S, (qt + 1) * kBQ) - 1;
+  const int nwalk = walk.total();
+
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(q_full, 1);
+    for (int i = 0; i < kNS; ++i) {
+      ptx::mbar_init(&kv_full[i], 1);
+      ptx::mbar_init(&kv_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(&s_full[i], 1);
+      ptx::mbar_init(&s_empty[i], 4);          // the four softmax warps
+    }
+    ptx::mbar_init(p_full, 4);
+    ptx::mbar_init(p_empty, 1);
+    ptx::mbar_init(o_full, 1);
+    ptx::mbar_init(mma_done, 1);
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    ptx::tma_prefetch_desc(&p.mapQ[r]);
+    for (int i = 0; i < p.R; ++i) {
+      ptx::tma_prefetch_desc(&p.mapK[i]);
+      ptx::tma_prefetch_desc(&p.mapV[i]);
+    }
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(tmem_slot, kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const ptx::Waiter W{abort_flag, p.status, p.timeout_ns};
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t issued = 0, last_parity = 0;     // stages with loads in flight (abort drain)
+      bool ok = true;
+      ptx::mbar_arrive_expect_tx(q_full, kTile);
+      for (int b = 0; b < 2; ++b)
+        ptx::tma_load_2d(sQ + b * kAtom, &p.mapQ[r], q_full, h * kD + 64 * b, qt * kBQ);
+      int u = 0;                                // ring uses
+      for (int pass = 0; pass < 2 && ok; ++pass) {
+        const uint32_t bytes = pass == 0 ? kTile : 2 * kTile;
+        for (int i = 0; i < nwalk && ok; ++i) {
+          if (!walk.visible(i)) continue;
+          const int st = u % kNS;
+          const uint32_t ph = (u / kNS) & 1u;
+          if (!W.wait(&kv_empty[st], ph ^ 1u)) {
+            ok = false;
+            break;
+          }
+          const int sh = walk.shard(i);
+          const int y = walk.row0(i);
+          uint8_t* kdst = sK + st * 2 * kTile;
+          ptx::mbar_arrive_expect_tx(&kv_full[st], bytes);
+          for (int b = 0; b < 2; ++b)
+            ptx::tma_load_2d(kdst + b * kAtom, &p.mapK[sh], &kv_full[st], h * kD + 64 * b, y);
+          if (pass == 1)
+            for (int b = 0; b < 2; ++b)
+              ptx::tma_load_2d(kdst + kTile + b * kAtom, &p.mapV[sh], &kv_full[st],
+                               h * kD + 64 * b, y);
+          issued |= 1u << st;
+          last_parity = (last_parity & ~(1u << st)) | (ph << st);
+          ++u;
+        }
+      }
+      if (*abort_flag) {
+        W.drain(q_full, 0, kDrainNs);
+        for (int st = 0; st < kNS; ++st)
+          if (issued & (1u << st)) W.drain(&kv_full[st], (last_parity >> st) & 1u, kDrainNs);
+      }
+    }
+  } else if (warp == 1) {
+    // ----------------------------------------------------------- MMA issue
+    if (lane == 0) {
+      bool ok = W.wait(q_full, 0);
+      const uint32_t qa = ptx::smem_addr(sQ);
+      const uint32_t pa = ptx::smem_addr(sP);
+      int u = 0, n = 0, m = 0;                 // ring uses, S buffers issued, P uses
+      bool any = false;
+      // Issues S_n = Q K^T from ring use u into S buffer n & 1.
+      auto issue_s = [&](int st) -> bool {
+        const int b = n & 1;
+        if (!W.wait(&s_empty[b], ((n >> 1) & 1u) ^ 1u)) return false;
+        ptx::tc_fence_after();
+        const uint32_t ka = ptx::smem_addr(sK + st * 2 * kTile);
+        const uint32_t d_tmem = tmem_base + kColS + b * kBKV;
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk)
+          ptx::mma_f16(d_tmem, desc_kmajor(qa, kk), desc_kmajor(ka, kk), kIdescS,
+                       kk > 0 ? 1u : 0u);
+        ptx::mma_commit(&s_full[b]);
+        ++n;
+        any = true;
+        return true;
+      };
+      // Pass 1: maxima only; the stage is free once its S is computed.
+      for (int i = 0; i < nwalk && ok; ++i) {
+        if (!walk.visible(i)) continue;
+        const int st = u % kNS;
+        if (!(ok = W.wait(&kv_full[st], (u / kNS) & 1u))) break;
+        ptx::tc_fence_after();
+        if (!(ok = issue_s(st))) break;
+        ptx::mma_commit(&kv_empty[st]);
+        ++u;
+      }
+      // Pass 2: S_i, then (once the softmax warps have written P_i) O += P_i V_i.
+      // S_{i+1} is issued before waiting for P_i, so the softmax of one block
+      // overlaps the tensor core's work on the next.
+      int pending_st = -1;                     // stage whose P V is still to issue
+      bool first_pv = true;
+      auto issue_pv = [&](int st) -> bool {
+        if (!W.wait(p_full, m & 1u)) return false;
+        ptx::tc_fence_after();
+        const uint32_t va = ptx::smem_addr(sK + st * 2 * kTile + kTile);
+#pragma unroll
+        for (int kk = 0; kk < kBKV / 16; ++kk)
+          ptx::mma_f16(tmem_base + kColO, desc_kmajor(pa, kk), desc_mnmajor(va, kk), kIdescO,
+                       (!first_pv || kk > 0) ? 1u : 0u);
+        first_pv = false;
+        ptx::mma_commit(p_empty);
+        ptx::mma_commit(&kv_empty[st]);
+        ++m;
+        return true;
+      };
+      for (int i = 0; i < nwalk && ok; ++i) {
+        if (!walk.visible(i)) continue;
+        const int st = u % kNS;
+        if (!(ok = W.wait(&kv_full[st], (u / kNS) & 1u))) break;
+        ptx::tc_fence_after();
+        if (!(ok = issue_s(st))) break;
+        if (pending_st >= 0 && !(ok = issue_pv(pending_st))) break;
+        pending_st = st;
+        ++u;
+      }
+      if (ok && pending_st >= 0) ok = issue_pv(pending_st);
+      if (ok) ptx::mma_commit(o_full);
+      if (any) {
+        ptx::mma_commit(mma_done);
+        W.drain(mma_done, 0, kDrainNs);
+      }
+    }
+  } else {
+    // ------------------------------------------------- softmax and output
+    const int q = warp & 3;                     // TMEM lane quarter of this warp
+    const int row = q * 32 + lane;              // query row of the tile
+    const long long qpos = static_cast<long long>(r) * p.S + qt * kBQ + row;
+    const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+    // Lane 0 waits, the warp follows (the warp stops as one).
+    auto wait_warp = [&](uint64_t* bar, uint32_t parity) -> bool {
+      int good = 1;
+      if (lane == 0) good = W.wait(bar, parity) ? 1 : 0;
+      return __shfl_sync(0xffffffffu, good, 0) != 0;
+    };
+    auto valid = [&](int i, int col) -> bool {
+      const int k = walk.row0(i) + col;
+      if (k >= p.S) return false;
+      return !p.causal || static_cast<long long>(walk.shard(i)) * p.S + k <= qpos;
+    };
+    bool ok = true;
+    int n = 0;                                  // S buffers consumed
+    float mx = -INFINITY;
+    // Pass 1: the row maximum of the raw scores.
+    for (int i = 0; i < nwalk && ok; ++i) {
+      if (!walk.visible(i)) continue;
+      const int b = n & 1;
+      if (!(ok = wait_warp(&s_full[b], (n >> 1) & 1u))) break;
+      ptx::tc_fence_after();
+#pragma unroll 1
+      for (int c = 0; c < kBKV; c += 32) {
+        uint32_t v[32];
+        ptx::tmem_ld_32x32b_x32(lane_addr + kColS + b * kBKV + c, v);
+        ptx::tmem_ld_wait();
+#pragma unroll
+        for (int k = 0; k < 32; ++k)
+          if (valid(i, c + k)) mx = fmaxf(mx, __uint_as_float(v[k]));
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&s_empty[b]);
+      ++n;
+    }
+    // Pass 2: p = exp(s - m) into P (bf16), l = sum of p.
+    const float msc = mx * p.scale_log2;
+    float l = 0.f;
+    int mcount = 0;                             // P buffers written
+    uint8_t* prow = sP + row * 128;
+    for (int i = 0; i < nwalk && ok; ++i) {
+      if (!walk.visible(i)) continue;
+      const int b = n & 1;
+      if (!(ok = wait_warp(&s_full[b], (n >> 1) & 1u))) break;
+      ptx::tc_fence_after();
+      uint32_t pk[kBKV / 2];                    // bf16 pairs of p
+#pragma unroll
+      for (int c = 0; c < kBKV; c += 32) {
+        uint32_t v[32];
+        ptx::tmem_ld_32x32b_x32(lane_addr + kColS + b * kBKV + c, v);
+        ptx::tmem_ld_wait();
+#pragma unroll
+        for (int k = 0; k < 32; k += 2) {
+          const float p0 = valid(i, c + k)
+                               ? exp2f(fmaf(__uint_as_float(v[k]), p.scale_log2, -msc)) : 0.f;
+          const float p1 = valid(i, c + k + 1)
+                               ? exp2f(fmaf(__uint_as_float(v[k + 1]), p.scale_log2, -msc))
+                               : 0.f;
+          l += p0 + p1;
+          pk[(c + k) / 2] = ptx::pack_bf16x2(p0, p1);
+        }
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&s_empty[b]);
+      ++n;
+      // P is free once the tensor core has read the previous block's.
+      if (!(ok = wait_warp(p_empty, (mcount & 1u) ^ 1u))) break;
+#pragma unroll
+      for (int c16 = 0; c16 < kBKV / 8; ++c16) {
+        const int cc = c16 & 7;
+        const uint32_t addr = ptx::smem_addr(prow + (c16 >> 3) * kAtom) + ((cc ^ (row & 7)) << 4);
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr),
+                     "r"(pk[4 * c16]), "r"(pk[4 * c16 + 1]), "r"(pk[4 * c16 + 2]),
+                     "r"(pk[4 * c16 + 3])
+                     : "memory");
+      }
+      ptx::fence_proxy_async_smem();            // the tensor core reads P next
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(p_full);
+      ++mcount;
+    }
+    // Output: O / l for the tile's rows inside the shard.
+    if (ok && wait_warp(o_full, 0)) {
+      ptx::tc_fence_after();
+      const int grow = qt * kBQ + row;
+      const float inv = 1.f / l;
+      char* dst = static_cast<char*>(p.out[r]) +
+                  (static_cast<long long>(grow) * p.H + h) * kD * (p.out_f32 ? 4 : 2);
+#pragma unroll 1
+      for (int c = 0; c < kD; c += 32) {
+        uint32_t v[32];
+        ptx::tmem_ld_32x32b_x32(lane_addr + kColO + c, v);
+        ptx::tmem_ld_wait();
+        if (grow < p.S) {
+          if (p.out_f32) {
+            float4* o = reinterpret_cast<float4*>(dst) + c / 4;
+#pragma unroll
+            for (int k = 0; k < 32; k += 4)
+              o[k / 4] = make_float4(__uint_as_float(v[k]) * inv, __uint_as_float(v[k + 1]) * inv,
+                                     __uint_as_float(v[k + 2]) * inv,
+                                     __uint_as_float(v[k + 3]) * inv);
+          } else {
+            uint4* o = reinterpret_cast<uint4*>(dst) + c / 8;
+#pragma unroll
+            for (int k = 0; k < 32; k += 8) {
+              uint4 w;
+              w.x = ptx::pack_bf16x2(__uint_as_float(v[k]) * inv, __uint_as_float(v[k + 1]) * inv);
+              w.y = ptx::pack_bf16x2(__uint_as_float(v[k + 2]) * inv,
+                                     __uint_as_float(v[k + 3]) * inv);
+              w.z = ptx::pack_bf16x2(__uint_as_float(v[k + 4]) * inv,
+                                     __uint_as_float(v[k + 5]) * inv);
+              w.w = ptx::pack_bf16x2(__uint_as_float(v[k + 6]) * inv,
+                                     __uint_as_float(v[k + 7]) * inv);
+              o[k / 8] = w;
+            }
+          }
+        }
+      }
+    }
+  }
+
+  __syncwarp();
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+}  // namespace
+}  // namespace fcc
+
+using namespace fcc;
+
+extern "C" {
+
+fcc_status fcc_ring_attention(int R, const void* const* Q, const void* const* K,
+                              const void* const* V, void* const* O, int64_t S, int H, int64_t d,
+                              int causal, fcc_dtype in, fcc_dtype out_dtype, const fcc_opts* opts,
+                              fcc_stream_t stream) {
+  if (R < 1 || R > FCC_MAX_RANKS || S < 1 || S > (1ll << 30) || H < 1 || H > 1024 || d < 1)
+    return FCC_ERR_INVALID;
+  if (static_cast<int64_t>(R) * H * ((S + kBQ - 1) / kBQ) > (1ll << 31) - 1)
+    return FCC_ERR_INVALID;
+  if (Q == nullptr || K == nullptr || V == nullptr || O == nullptr) return FCC_ERR_INVALID;
+  for (int r = 0; r < R; ++r)
+    for (const void* ptr : {Q[r], K[r], V[r], static_cast<const void*>(O[r])})
+      if (ptr == nullptr || (reinterpret_cast<uintptr_t>(ptr) & 15u)) return FCC_ERR_INVALID;
+  if ((in != FCC_BF16 && in != FCC_F16 && in != FCC_F32) ||
+      (out_dtype != FCC_BF16 && out_dtype != FCC_F16 && out_dtype != FCC_F32))
+    return FCC_ERR_INVALID;
+  if (in != FCC_BF16 || out_dtype == FCC_F16 || d != kD) return FCC_ERR_UNSUPPORTED;
+  if (opts != nullptr && opts->algo != FCC_ALGO_AUTO && opts->algo != FCC_ALGO_FUSED)
+    return FCC_ERR_UNSUPPORTED;
+
+  void* ws = nullptr;
+  int* status = nullptr;
+  int sms = 0;
+  unsigned long long timeout_ns = 0;
+  fcc_status s = internal_prepare(opts, 0, &ws, &status, &sms, &timeout_ns);
+  if (s != FCC_OK) return s;
+  AttnParams p;
+  std::memset(&p, 0, sizeof(p));
+  for (int r = 0; r < R; ++r) {
+    if ((s = internal_make_map(&p.mapQ[r], Q[r], S, static_cast<int64_t>(H) * kD, kBQ)) != FCC_OK ||
+        (s = internal_make_map(&p.mapK[r], K[r], S, static_cast<int64_t>(H) * kD, kBKV)) != FCC_OK ||
+        (s = internal_make_map(&p.mapV[r], V[r], S, static_cast<int64_t>(H) * kD, kBKV)) != FCC_OK)
+      return s;
+    p.out[r] = O[r];
+  }
+  p.R = R;
+  p.S = static_cast<int>(S);
+  p.H = H;
+  p.qtiles = static_cast<int>((S + kBQ - 1) / kBQ);
+  p.kvb = static_cast<int>((S + kBKV - 1) / kBKV);
+  p.causal = causal ? 1 : 0;
+  p.out_f32 = out_dtype == FCC_F32 ? 1 : 0;
+  p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(kD)));
+  p.status = status;
+  p.timeout_ns = timeout_ns;
+
+  if (cudaFuncSetAttribute(ring_attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kSmem) != cudaSuccess)
+    return FCC_ERR_CUDA;
+  const unsigned grid = static_cast<unsigned>(R * H * p.qtiles);
+  ring_attention_kernel<<<grid, 192, kSmem, reinterpret_cast<cudaStream_t>(stream)>>>(p);
+  if (cudaGetLastError() != cudaSuccess) return FCC_ERR_CUDA;
+  bump_launch_count(1);
+  return FCC_OK;
+}
+
+}  // extern "C"

@@ -267,6 +267,23 @@ fcc_status fcc_embedding_a2a(int R, int ntables, const void *const *tables, int6
 size_t fcc_embedding_workspace_size(int R, int ntables, int64_t D, int64_t Bl,
                                     fcc_dtype out_dtype, const fcc_opts *opts);
 
+/*
+ * Ring attention (the mKernel article's fused kernel list: Ring Attention).
+ * The sequence is split over R ranks, S positions each (rank r's row t is
+ * global position r*S + t); every rank's queries attend to the keys and
+ * values of all shards, which the ring brings round (here: each CTA reads
+ * the blocks of every shard in ring order, its own shard first):
+ *   O_r[t][h] = sum_j softmax_j(Q_r[t][h] . K[j][h] / sqrt(d)) V[j][h]
+ * over all global positions j (causal != 0: only j <= r*S + t).
+ * Q[r], K[r], V[r]: [S, H, d] bf16; O[r]: [S, H, d] (bf16 or f32).  d = 128
+ * (others: FCC_ERR_UNSUPPORTED).  Scores, softmax and sums in f32; the
+ * probabilities enter the P V product as bf16.  No workspace.
+ */
+fcc_status fcc_ring_attention(int R, const void *const *Q, const void *const *K,
+                              const void *const *V, void *const *O, int64_t S, int H, int64_t d,
+                              int causal, fcc_dtype in, fcc_dtype out_dtype,
+                              const fcc_opts *opts, fcc_stream_t stream);
+
 /* Scratch bytes a call needs (for opts->workspace); 0 if none. */
 size_t fcc_workspace_size(fcc_op op, int R, int64_t M, int64_t N, int64_t K,
                           const fcc_opts *opts);

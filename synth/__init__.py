@@ -135,7 +135,7 @@ def attention_inputs(R: int, S: int, H: int, d: int, std: float = 1.0, seed: int
 class Workload:
     """One named workload: shapes, value distributions and output dtype."""
     name: str
-    op: str            # gemm_rs | gemm_ar | gemv_ar | ag_gemm | moe | emb_a2a
+    op: str            # gemm_rs | gemm_ar | gemv_ar | ag_gemm | moe | emb_a2a | attention
     R: int
     M: int = 0         # GEMM rows (all ranks for AG: R * rows per rank)
     N: int = 0
@@ -164,6 +164,9 @@ class Workload:
         """2 * useful multiply-adds of the workload."""
         if self.op == "moe":
             return 2.0 * self.R * self.T * self.topk * self.H * self.F
+        if self.op == "attention":
+            # Q K^T and P V over every (query, key) pair: 4 * S_q * S_k * d per head
+            return 4.0 * (self.R * self.M) * (self.R * self.M) * self.K * self.H
         if self.op == "ag_gemm":
             return 2.0 * self.R * self.M * self.N * self.K
         return 2.0 * self.R * self.M * self.N * self.K
@@ -195,6 +198,10 @@ WORKLOADS = {
                                              std_a=1.0, std_b=0.02, out="bf16"),
     # Embedding + all-to-all (DLRM-style): 8 ranks x 8 tables of 65536 x 128
     # rows, 2048 samples per rank, bags of 32 rows on average.
+    # Ring attention: 8 ranks x 4096 positions (32768 in all), 8 heads, d = 128
+    # (M = positions per rank, K = head dimension).
+    "attn_r8_s4096_h8_d128": Workload("attn_r8_s4096_h8_d128", "attention", R=8, M=4096,
+                                      K=128, H=8, std_a=1.0, out="bf16"),
     "emb_a2a_r8_t64_v65536_d128_b2048_l32": Workload(
         "emb_a2a_r8_t64_v65536_d128_b2048_l32", "emb_a2a", R=8, tables=64, B=2048,
         V=65536, D=128, L=32, std_a=1.0, out="bf16"),
