@@ -496,6 +496,25 @@ def other_ops(fcc, torch, np, synth, dev, stream, dA_rs, dB_rs, pk, only=None):
         ops[w.name] = res
         del Xall, dX, dL, dW, recv_y, recv_x, y
 
+    # Ring attention over 8 sequence shards
+    if want("attn_r8_s4096_h8_d128"):
+        w = synth.WORKLOADS["attn_r8_s4096_h8_d128"]
+        Q, K, V = synth.attention_inputs(w.R, w.M, w.H, w.K, seed=0)
+        dq, dk, dv = ([up(x) for x in X] for X in (Q, K, V))
+        O = [torch.empty((w.M, w.H, w.K), dtype=torch.bfloat16, device=dev) for _ in range(w.R)]
+        res = {}
+        for name, causal in [("full", False), ("causal", True)]:
+            t = time_calls(lambda c=causal: fcc.fcc_ring_attention(w.R, dq, dk, dv, O, w.M, w.H,
+                                                                   w.K, c, 0, 0, None, stream),
+                           5, 2, stream)
+            fl = w.flops() * (0.5 if causal else 1.0)   # causal: the lower triangle
+            res[name] = {"ms": t, "TFLOP/s": fl / (t * 1e-3) / 1e12,
+                         "roofline_frac": fl / (t * 1e-3) / 1e12 / tc}
+        res["note"] = ("useful FLOPs 4 L^2 d H (half with the mask); the kernel computes Q K^T "
+                       "twice (two-pass softmax): 1.5x those on the tensor cores")
+        ops[w.name] = res
+        del dq, dk, dv, O, Q, K, V
+
     # Embedding + all-to-all (DLRM pooled lookups)
     if want("emb_a2a_r8_t64_v65536_d128_b2048_l32"):
         w = synth.WORKLOADS["emb_a2a_r8_t64_v65536_d128_b2048_l32"]

@@ -289,10 +289,16 @@ __global__ void __launch_bounds__(192, 1) ring_attention_kernel(const __grid_con
       if (lane == 0) good = W.wait(bar, parity) ? 1 : 0;
       return __shfl_sync(0xffffffffu, good, 0) != 0;
     };
-    auto valid = [&](int i, int col) -> bool {
-      const int k = walk.row0(i) + col;
-      if (k >= p.S) return false;
-      return !p.causal || static_cast<long long>(walk.shard(i)) * p.S + k <= qpos;
+    // The last valid column of block i for this row: keys past the shard's
+    // end, and (causal) past the row's own position, are masked.
+    auto last_col = [&](int i) -> int {
+      const int r0 = walk.row0(i);
+      int c = min(kBKV, p.S - r0) - 1;
+      if (p.causal) {
+        const long long lim = qpos - (static_cast<long long>(walk.shard(i)) * p.S + r0);
+        c = static_cast<int>(min(static_cast<long long>(c), lim));
+      }
+      return c;                                 // -1: nothing valid
     };
     bool ok = true;
     int n = 0;                                  // S buffers consumed
@@ -303,14 +309,19 @@ __global__ void __launch_bounds__(192, 1) ring_attention_kernel(const __grid_con
       const int b = n & 1;
       if (!(ok = wait_warp(&s_full[b], (n >> 1) & 1u))) break;
       ptx::tc_fence_after();
-#pragma unroll 1
-      for (int c = 0; c < kBKV; c += 32) {
-        uint32_t v[32];
-        ptx::tmem_ld_32x32b_x32(lane_addr + kColS + b * kBKV + c, v);
-        ptx::tmem_ld_wait();
+      const int cmax = last_col(i);
+      uint32_t v[kBKV];
 #pragma unroll
-        for (int k = 0; k < 32; ++k)
-          if (valid(i, c + k)) mx = fmaxf(mx, __uint_as_float(v[k]));
+      for (int c = 0; c < kBKV; c += 32)
+        ptx::tmem_ld_32x32b_x32(lane_addr + kColS + b * kBKV + c, *reinterpret_cast<uint32_t(*)[32]>(v + c));
+      ptx::tmem_ld_wait();
+      if (cmax >= kBKV - 1) {
+#pragma unroll
+        for (int k = 0; k < kBKV; ++k) mx = fmaxf(mx, __uint_as_float(v[k]));
+      } else {
+#pragma unroll
+        for (int k = 0; k < kBKV; ++k)
+          if (k <= cmax) mx = fmaxf(mx, __uint_as_float(v[k]));
       }
       ptx::tc_fence_before();
       __syncwarp();
@@ -327,19 +338,21 @@ __global__ void __launch_bounds__(192, 1) ring_attention_kernel(const __grid_con
       const int b = n & 1;
       if (!(ok = wait_warp(&s_full[b], (n >> 1) & 1u))) break;
       ptx::tc_fence_after();
+      const int cmax = last_col(i);
       uint32_t pk[kBKV / 2];                    // bf16 pairs of p
 #pragma unroll
-      for (int c = 0; c < kBKV; c += 32) {
-        uint32_t v[32];
-        ptx::tmem_ld_32x32b_x32(lane_addr + kColS + b * kBKV + c, v);
+      for (int c = 0; c < kBKV; c += 64) {      // two TMEM loads in flight
+        uint32_t v[64];
+        ptx::tmem_ld_32x32b_x32(lane_addr + kColS + b * kBKV + c, *reinterpret_cast<uint32_t(*)[32]>(v));
+        ptx::tmem_ld_32x32b_x32(lane_addr + kColS + b * kBKV + c + 32,
+                                *reinterpret_cast<uint32_t(*)[32]>(v + 32));
         ptx::tmem_ld_wait();
 #pragma unroll
-        for (int k = 0; k < 32; k += 2) {
-          const float p0 = valid(i, c + k)
-                               ? exp2f(fmaf(__uint_as_float(v[k]), p.scale_log2, -msc)) : 0.f;
-          const float p1 = valid(i, c + k + 1)
-                               ? exp2f(fmaf(__uint_as_float(v[k + 1]), p.scale_log2, -msc))
-                               : 0.f;
+        for (int k = 0; k < 64; k += 2) {
+          float p0 = ptx::ex2_approx(fmaf(__uint_as_float(v[k]), p.scale_log2, -msc));
+          float p1 = ptx::ex2_approx(fmaf(__uint_as_float(v[k + 1]), p.scale_log2, -msc));
+          if (c + k > cmax) p0 = 0.f;
+          if (c + k + 1 > cmax) p1 = 0.f;
           l += p0 + p1;
           pk[(c + k) / 2] = ptx::pack_bf16x2(p0, p1);
         }
