@@ -16,8 +16,8 @@
 // With the final maxima known before any exponential, no accumulator ever
 // needs rescaling: one exponential per score, at the price of a second Q K^T.
 //
-// Warps: 0 = TMA producer (Q once, then K [and V] blocks into a two-stage
-// ring), 1 = MMA issue, 2-5 = softmax (TMEM lane quarter = 32 query rows each)
+// Warps: 0 = TMA producer (Q once, then K blocks into a three-stage ring and,
+// in pass 2, V blocks into a two-stage ring), 1 = MMA issue, 2-5 = softmax (TMEM lane quarter = 32 query rows each)
 // and the output.  Shared memory (128-byte swizzle throughout):
 //   Q   [128 q][128 d]    K-major, two 64-column atoms of 16 KiB
 //   K_j [128 keys][128 d] K-major (the B operand of Q K^T)
@@ -41,7 +41,8 @@ namespace {
 constexpr int kD = 128;                          // head dimension
 constexpr int kBQ = 128;                         // query rows per CTA (MMA M)
 constexpr int kBKV = 128;                        // keys per block
-constexpr int kNS = 2;                           // key/value ring stages
+constexpr int kKS = 3;                           // key ring stages
+constexpr int kVS = 2;                           // value ring stages
 constexpr uint32_t kAtom = 128 * 128;            // 16 KiB: [128 rows][64 bf16]
 constexpr uint32_t kTile = 2 * kAtom;            // 32 KiB: [128][128] bf16
 constexpr uint32_t kTmemCols = 512;
@@ -50,8 +51,9 @@ constexpr uint64_t kDrainNs = 50ull * 1000 * 1000;
 // S = Q K^T: both operands K-major.  O += P V: A K-major, B (V) MN-major.
 constexpr uint32_t kIdescS = ptx::idesc_bf16_f32(kBQ, kBKV, false, false);
 constexpr uint32_t kIdescO = ptx::idesc_bf16_f32(kBQ, kD, false, true);
-// Q, 2 stages of K + V, P, then 12 barriers and 4 words.
-constexpr int kSmem = 1024 + kTile * (1 + 2 * kNS + 1) + 12 * 8 + 16;
+// Q, the key and value rings, P, then the barriers and 4 words.
+constexpr int kBars = 1 + 2 * kKS + 2 * kVS + 2 + 2 + 4;
+constexpr int kSmem = 1024 + kTile * (1 + kKS + kVS + 1) + kBars * 8 + 16;
 static_assert(kSmem <= 232448, "shared memory per CTA");
 
 struct AttnParams {
@@ -102,28 +104,34 @@ __global__ void __launch_bounds__(192, 1) ring_attention_kernel(const __grid_con
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* sQ = smem;
-  uint8_t* sK = sQ + kTile;                    // stage s: sK + s * 2 * kTile
-  uint8_t* sP = sQ + kTile * (1 + 2 * kNS);
+  uint8_t* sK = sQ + kTile;                    // key stage s: sK + s * kTile
+  uint8_t* sV = sK + kKS * kTile;              // value stage s: sV + s * kTile
+  uint8_t* sP = sV + kVS * kTile;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sP + kTile);
   uint64_t* q_full = bars;
-  uint64_t* kv_full = bars + 1;                // [kNS]
-  uint64_t* kv_empty = bars + 1 + kNS;         // [kNS]
-  uint64_t* s_full = bars + 1 + 2 * kNS;       // [2]
+  uint64_t* k_full = bars + 1;                 // [kKS]
+  uint64_t* k_empty = k_full + kKS;            // [kKS]
+  uint64_t* v_full = k_empty + kKS;            // [kVS]
+  uint64_t* v_empty = v_full + kVS;            // [kVS]
+  uint64_t* s_full = v_empty + kVS;            // [2]
   uint64_t* s_empty = s_full + 2;              // [2]
   uint64_t* p_full = s_empty + 2;
   uint64_t* p_empty = p_full + 1;
   uint64_t* o_full = p_empty + 1;
-  uint64_t* mma_done = o_full + 1;             // 1 + 2*kNS + 7 = 12 barriers
+  uint64_t* mma_done = o_full + 1;             // kBars barriers in all
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  // CTA -> (rank, head, query tile)
+  // CTA -> (rank, head, query tile), in reverse: with the causal mask the
+  // last ranks' last tiles see the most keys, and launching them first keeps
+  // them out of the final wave.
+  const int bid = static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x);
   const int per_rank = p.H * p.qtiles;
-  const int r = blockIdx.x / per_rank;
-  const int h = (blockIdx.x - r * per_rank) / p.qtiles;
-  const int qt = blockIdx.x - r * per_rank - h * p.qtiles;
+  const int r = bid / per_rank;
+  const int h = (bid - r * per_rank) / p.qtiles;
+  const int qt = bid - r * per_rank - h * p.qtiles;
   Walk walk;
   walk.r = r;
   walk.kvb = p.kvb;
@@ -135,9 +143,13 @@ __global__ void __launch_bounds__(192, 1) ring_attention_kernel(const __grid_con
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(q_full, 1);
-    for (int i = 0; i < kNS; ++i) {
-      ptx::mbar_init(&kv_full[i], 1);
-      ptx::mbar_init(&kv_empty[i], 1);
+    for (int i = 0; i < kKS; ++i) {
+      ptx::mbar_init(&k_full[i], 1);
+      ptx::mbar_init(&k_empty[i], 1);
+    }
+    for (int i = 0; i < kVS; ++i) {
+      ptx::mbar_init(&v_full[i], 1);
+      ptx::mbar_init(&v_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(&s_full[i], 1);
@@ -170,41 +182,42 @@ __global__ void __launch_bounds__(192, 1) ring_attention_kernel(const __grid_con
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      uint32_t issued = 0, last_parity = 0;     // stages with loads in flight (abort drain)
+      // Loads still in flight at an abort: per ring, the stages issued and the
+      // parity of their last use.
+      uint32_t kiss = 0, kpar = 0, viss = 0, vpar = 0;
       bool ok = true;
       ptx::mbar_arrive_expect_tx(q_full, kTile);
       for (int b = 0; b < 2; ++b)
         ptx::tma_load_2d(sQ + b * kAtom, &p.mapQ[r], q_full, h * kD + 64 * b, qt * kBQ);
-      int u = 0;                                // ring uses
+      int uk = 0, uv = 0;                       // uses of the key and value rings
+      auto load = [&](const CUtensorMap* map, uint8_t* ring, uint64_t* full, uint64_t* empty,
+                      int nst, int& u, uint32_t& iss, uint32_t& par, int y) -> bool {
+        const int st = u % nst;
+        const uint32_t ph = (u / nst) & 1u;
+        if (!W.wait(&empty[st], ph ^ 1u)) return false;
+        ptx::mbar_arrive_expect_tx(&full[st], kTile);
+        for (int b = 0; b < 2; ++b)
+          ptx::tma_load_2d(ring + st * kTile + b * kAtom, map, &full[st], h * kD + 64 * b, y);
+        iss |= 1u << st;
+        par = (par & ~(1u << st)) | (ph << st);
+        ++u;
+        return true;
+      };
       for (int pass = 0; pass < 2 && ok; ++pass) {
-        const uint32_t bytes = pass == 0 ? kTile : 2 * kTile;
         for (int i = 0; i < nwalk && ok; ++i) {
           if (!walk.visible(i)) continue;
-          const int st = u % kNS;
-          const uint32_t ph = (u / kNS) & 1u;
-          if (!W.wait(&kv_empty[st], ph ^ 1u)) {
-            ok = false;
-            break;
-          }
           const int sh = walk.shard(i);
           const int y = walk.row0(i);
-          uint8_t* kdst = sK + st * 2 * kTile;
-          ptx::mbar_arrive_expect_tx(&kv_full[st], bytes);
-          for (int b = 0; b < 2; ++b)
-            ptx::tma_load_2d(kdst + b * kAtom, &p.mapK[sh], &kv_full[st], h * kD + 64 * b, y);
-          if (pass == 1)
-            for (int b = 0; b < 2; ++b)
-              ptx::tma_load_2d(kdst + kTile + b * kAtom, &p.mapV[sh], &kv_full[st],
-                               h * kD + 64 * b, y);
-          issued |= 1u << st;
-          last_parity = (last_parity & ~(1u << st)) | (ph << st);
-          ++u;
+          ok = load(&p.mapK[sh], sK, k_full, k_empty, kKS, uk, kiss, kpar, y);
+          if (ok && pass == 1) ok = load(&p.mapV[sh], sV, v_full, v_empty, kVS, uv, viss, vpar, y);
         }
       }
       if (*abort_flag) {
         W.drain(q_full, 0, kDrainNs);
-        for (int st = 0; st < kNS; ++st)
-          if (issued & (1u << st)) W.drain(&kv_full[st], (last_parity >> st) & 1u, kDrainNs);
+        for (int st = 0; st < kKS; ++st)
+          if (kiss & (1u << st)) W.drain(&k_full[st], (kpar >> st) & 1u, kDrainNs);
+        for (int st = 0; st < kVS; ++st)
+          if (viss & (1u << st)) W.drain(&v_full[st], (vpar >> st) & 1u, kDrainNs);
       }
     }
   } else if (warp == 1) {
@@ -213,64 +226,63 @@ __global__ void __launch_bounds__(192, 1) ring_attention_kernel(const __grid_con
       bool ok = W.wait(q_full, 0);
       const uint32_t qa = ptx::smem_addr(sQ);
       const uint32_t pa = ptx::smem_addr(sP);
-      int u = 0, n = 0, m = 0;                 // ring uses, S buffers issued, P uses
+      int uk = 0, uv = 0, n = 0, m = 0;        // key / value ring uses, S buffers, P uses
       bool any = false;
-      // Issues S_n = Q K^T from ring use u into S buffer n & 1.
-      auto issue_s = [&](int st) -> bool {
+      // Issues S_n = Q K^T from the next key stage into S buffer n & 1 and
+      // frees the key stage once the product is done.
+      auto issue_s = [&]() -> bool {
+        const int st = uk % kKS;
+        if (!W.wait(&k_full[st], (uk / kKS) & 1u)) return false;
         const int b = n & 1;
         if (!W.wait(&s_empty[b], ((n >> 1) & 1u) ^ 1u)) return false;
         ptx::tc_fence_after();
-        const uint32_t ka = ptx::smem_addr(sK + st * 2 * kTile);
+        const uint32_t ka = ptx::smem_addr(sK + st * kTile);
         const uint32_t d_tmem = tmem_base + kColS + b * kBKV;
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk)
           ptx::mma_f16(d_tmem, desc_kmajor(qa, kk), desc_kmajor(ka, kk), kIdescS,
                        kk > 0 ? 1u : 0u);
         ptx::mma_commit(&s_full[b]);
+        ptx::mma_commit(&k_empty[st]);
         ++n;
+        ++uk;
         any = true;
         return true;
       };
-      // Pass 1: maxima only; the stage is free once its S is computed.
+      // Pass 1: maxima only.
       for (int i = 0; i < nwalk && ok; ++i) {
         if (!walk.visible(i)) continue;
-        const int st = u % kNS;
-        if (!(ok = W.wait(&kv_full[st], (u / kNS) & 1u))) break;
-        ptx::tc_fence_after();
-        if (!(ok = issue_s(st))) break;
-        ptx::mma_commit(&kv_empty[st]);
-        ++u;
+        ok = issue_s();
       }
       // Pass 2: S_i, then (once the softmax warps have written P_i) O += P_i V_i.
       // S_{i+1} is issued before waiting for P_i, so the softmax of one block
       // overlaps the tensor core's work on the next.
-      int pending_st = -1;                     // stage whose P V is still to issue
+      bool pending = false;                    // a block whose P V is still to issue
       bool first_pv = true;
-      auto issue_pv = [&](int st) -> bool {
+      auto issue_pv = [&]() -> bool {
+        const int st = uv % kVS;
+        if (!W.wait(&v_full[st], (uv / kVS) & 1u)) return false;
         if (!W.wait(p_full, m & 1u)) return false;
         ptx::tc_fence_after();
-        const uint32_t va = ptx::smem_addr(sK + st * 2 * kTile + kTile);
+        const uint32_t va = ptx::smem_addr(sV + st * kTile);
 #pragma unroll
         for (int kk = 0; kk < kBKV / 16; ++kk)
           ptx::mma_f16(tmem_base + kColO, desc_kmajor(pa, kk), desc_mnmajor(va, kk), kIdescO,
                        (!first_pv || kk > 0) ? 1u : 0u);
         first_pv = false;
         ptx::mma_commit(p_empty);
-        ptx::mma_commit(&kv_empty[st]);
+        ptx::mma_commit(&v_empty[st]);
         ++m;
+        ++uv;
         return true;
       };
       for (int i = 0; i < nwalk && ok; ++i) {
         if (!walk.visible(i)) continue;
-        const int st = u % kNS;
-        if (!(ok = W.wait(&kv_full[st], (u / kNS) & 1u))) break;
-        ptx::tc_fence_after();
-        if (!(ok = issue_s(st))) break;
-        if (pending_st >= 0 && !(ok = issue_pv(pending_st))) break;
-        pending_st = st;
-        ++u;
+        if (!(ok = issue_s())) break;
+        if (pending && !(ok = issue_pv())) break;
+        pending = true;
       }
-      if (ok && pending_st >= 0) ok = issue_pv(pending_st);
+      if (ok && pending) ok = issue_pv();
       if (ok) ptx::mma_commit(o_full);
       if (any) {
         ptx::mma_commit(mma_done);
