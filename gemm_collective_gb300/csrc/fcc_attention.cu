@@ -17,8 +17,9 @@
 // needs rescaling: one exponential per score, at the price of a second Q K^T.
 //
 // Warps: 0 = TMA producer (Q once, then K blocks into a three-stage ring and,
-// in pass 2, V blocks into a two-stage ring), 1 = MMA issue, 2-5 = softmax (TMEM lane quarter = 32 query rows each)
-// and the output.  Shared memory (128-byte swizzle throughout):
+// in pass 2, V blocks into a two-stage ring), 1 = MMA issue, 2-9 = softmax and
+// output (two warps per TMEM lane quarter of 32 query rows, one for each half
+// of the key columns).  Shared memory (128-byte swizzle throughout):
 //   Q   [128 q][128 d]    K-major, two 64-column atoms of 16 KiB
 //   K_j [128 keys][128 d] K-major (the B operand of Q K^T)
 //   V_j [128 keys][128 d] MN-major B operand of P V: two 64-column atoms
@@ -53,7 +54,8 @@ constexpr uint32_t kIdescS = ptx::idesc_bf16_f32(kBQ, kBKV, false, false);
 constexpr uint32_t kIdescO = ptx::idesc_bf16_f32(kBQ, kD, false, true);
 // Q, the key and value rings, P, then the barriers and 4 words.
 constexpr int kBars = 1 + 2 * kKS + 2 * kVS + 2 + 2 + 4;
-constexpr int kSmem = 1024 + kTile * (1 + kKS + kVS + 1) + kBars * 8 + 16;
+constexpr int kThreads = 320;                    // warps 0-1 + eight softmax warps
+constexpr int kSmem = 1024 + kTile * (1 + kKS + kVS + 1) + kBars * 8 + 16 + 2 * kBQ * 4;
 static_assert(kSmem <= 232448, "shared memory per CTA");
 
 struct AttnParams {
@@ -99,7 +101,7 @@ __device__ __forceinline__ uint64_t desc_mnmajor(uint32_t base, int kk) {
 }
 
 
-__global__ void __launch_bounds__(192, 1) ring_attention_kernel(const __grid_constant__ AttnParams p) {
+__global__ void __launch_bounds__(kThreads, 1) ring_attention_kernel(const __grid_constant__ AttnParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -121,6 +123,7 @@ __global__ void __launch_bounds__(192, 1) ring_attention_kernel(const __grid_con
   uint64_t* mma_done = o_full + 1;             // kBars barriers in all
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float* red = reinterpret_cast<float*>(tmem_slot + 4);  // [2][128]: the halves' row values
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -153,9 +156,9 @@ __global__ void __launch_bounds__(192, 1) ring_attention_kernel(const __grid_con
     }
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(&s_full[i], 1);
-      ptx::mbar_init(&s_empty[i], 4);          // the four softmax warps
+      ptx::mbar_init(&s_empty[i], 8);          // the eight softmax warps
     }
-    ptx::mbar_init(p_full, 4);
+    ptx::mbar_init(p_full, 8);
     ptx::mbar_init(p_empty, 1);
     ptx::mbar_init(o_full, 1);
     ptx::mbar_init(mma_done, 1);
@@ -291,7 +294,13 @@ __global__ void __launch_bounds__(192, 1) ring_attention_kernel(const __grid_con
     }
   } else {
     // ------------------------------------------------- softmax and output
+    // Eight warps: warp w reads TMEM lane quarter w % 4 (32 query rows) and
+    // columns [64 c, 64 c + 64) of each block, c = (w - 2) / 4.  The two
+    // halves of a row meet twice through shared memory: for the row maximum
+    // after pass 1 and for the row sum at the end.
     const int q = warp & 3;                     // TMEM lane quarter of this warp
+    const int half = (warp - 2) >> 2;           // column half of the blocks
+    const int c0 = half * (kBKV / 2);
     const int row = q * 32 + lane;              // query row of the tile
     const long long qpos = static_cast<long long>(r) * p.S + qt * kBQ + row;
     const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
@@ -301,8 +310,8 @@ __global__ void __launch_bounds__(192, 1) ring_attention_kernel(const __grid_con
       if (lane == 0) good = W.wait(bar, parity) ? 1 : 0;
       return __shfl_sync(0xffffffffu, good, 0) != 0;
     };
-    // The last valid column of block i for this row: keys past the shard's
-    // end, and (causal) past the row's own position, are masked.
+    // The last valid column of block i for this row (keys past the shard's
+    // end, and with the mask past the row's own position, are out).
     auto last_col = [&](int i) -> int {
       const int r0 = walk.row0(i);
       int c = min(kBKV, p.S - r0) - 1;
@@ -312,27 +321,32 @@ __global__ void __launch_bounds__(192, 1) ring_attention_kernel(const __grid_con
       }
       return c;                                 // -1: nothing valid
     };
+    // This half's 64 columns of S buffer b.
+    auto load_s = [&](int b, uint32_t (&v)[64]) {
+      ptx::tmem_ld_32x32b_x32(lane_addr + kColS + b * kBKV + c0,
+                              *reinterpret_cast<uint32_t(*)[32]>(v));
+      ptx::tmem_ld_32x32b_x32(lane_addr + kColS + b * kBKV + c0 + 32,
+                              *reinterpret_cast<uint32_t(*)[32]>(v + 32));
+      ptx::tmem_ld_wait();
+    };
     bool ok = true;
     int n = 0;                                  // S buffers consumed
     float mx = -INFINITY;
-    // Pass 1: the row maximum of the raw scores.
+    // Pass 1: the row maximum of the raw scores (this half's columns).
     for (int i = 0; i < nwalk && ok; ++i) {
       if (!walk.visible(i)) continue;
       const int b = n & 1;
       if (!(ok = wait_warp(&s_full[b], (n >> 1) & 1u))) break;
       ptx::tc_fence_after();
-      const int cmax = last_col(i);
-      uint32_t v[kBKV];
+      const int cmax = last_col(i) - c0;        // in this half's columns
+      uint32_t v[64];
+      load_s(b, v);
+      if (cmax >= 63) {
 #pragma unroll
-      for (int c = 0; c < kBKV; c += 32)
-        ptx::tmem_ld_32x32b_x32(lane_addr + kColS + b * kBKV + c, *reinterpret_cast<uint32_t(*)[32]>(v + c));
-      ptx::tmem_ld_wait();
-      if (cmax >= kBKV - 1) {
-#pragma unroll
-        for (int k = 0; k < kBKV; ++k) mx = fmaxf(mx, __uint_as_float(v[k]));
+        for (int k = 0; k < 64; ++k) mx = fmaxf(mx, __uint_as_float(v[k]));
       } else {
 #pragma unroll
-        for (int k = 0; k < kBKV; ++k)
+        for (int k = 0; k < 64; ++k)
           if (k <= cmax) mx = fmaxf(mx, __uint_as_float(v[k]));
       }
       ptx::tc_fence_before();
@@ -340,33 +354,42 @@ __global__ void __launch_bounds__(192, 1) ring_attention_kernel(const __grid_con
       if (lane == 0) ptx::mbar_arrive(&s_empty[b]);
       ++n;
     }
-    // Pass 2: p = exp(s - m) into P (bf16), l = sum of p.
+    // The row's maximum over both halves (every softmax warp gets here, also
+    // after a failed wait, so the barrier always completes).
+    red[half * kBQ + row] = mx;
+    if (ptx::named_barrier_or(1, 256, !ok)) ok = false;
+    mx = fmaxf(mx, red[(half ^ 1) * kBQ + row]);
+    // Pass 2: p = exp(s - m) into this half of P (bf16), l = this half's sum.
     const float msc = mx * p.scale_log2;
     float l = 0.f;
     int mcount = 0;                             // P buffers written
-    uint8_t* prow = sP + row * 128;
+    const uint32_t prow = ptx::smem_addr(sP + half * kAtom + row * 128);
     for (int i = 0; i < nwalk && ok; ++i) {
       if (!walk.visible(i)) continue;
       const int b = n & 1;
       if (!(ok = wait_warp(&s_full[b], (n >> 1) & 1u))) break;
       ptx::tc_fence_after();
-      const int cmax = last_col(i);
-      uint32_t pk[kBKV / 2];                    // bf16 pairs of p
+      const int cmax = last_col(i) - c0;
+      uint32_t v[64];
+      load_s(b, v);
+      uint32_t pk[32];                          // bf16 pairs of p
+      if (cmax >= 63) {
 #pragma unroll
-      for (int c = 0; c < kBKV; c += 64) {      // two TMEM loads in flight
-        uint32_t v[64];
-        ptx::tmem_ld_32x32b_x32(lane_addr + kColS + b * kBKV + c, *reinterpret_cast<uint32_t(*)[32]>(v));
-        ptx::tmem_ld_32x32b_x32(lane_addr + kColS + b * kBKV + c + 32,
-                                *reinterpret_cast<uint32_t(*)[32]>(v + 32));
-        ptx::tmem_ld_wait();
+        for (int k = 0; k < 64; k += 2) {
+          const float p0 = ptx::ex2_approx(fmaf(__uint_as_float(v[k]), p.scale_log2, -msc));
+          const float p1 = ptx::ex2_approx(fmaf(__uint_as_float(v[k + 1]), p.scale_log2, -msc));
+          l += p0 + p1;
+          pk[k / 2] = ptx::pack_bf16x2(p0, p1);
+        }
+      } else {
 #pragma unroll
         for (int k = 0; k < 64; k += 2) {
           float p0 = ptx::ex2_approx(fmaf(__uint_as_float(v[k]), p.scale_log2, -msc));
           float p1 = ptx::ex2_approx(fmaf(__uint_as_float(v[k + 1]), p.scale_log2, -msc));
-          if (c + k > cmax) p0 = 0.f;
-          if (c + k + 1 > cmax) p1 = 0.f;
+          if (k > cmax) p0 = 0.f;
+          if (k + 1 > cmax) p1 = 0.f;
           l += p0 + p1;
-          pk[(c + k) / 2] = ptx::pack_bf16x2(p0, p1);
+          pk[k / 2] = ptx::pack_bf16x2(p0, p1);
         }
       }
       ptx::tc_fence_before();
@@ -376,12 +399,11 @@ __global__ void __launch_bounds__(192, 1) ring_attention_kernel(const __grid_con
       // P is free once the tensor core has read the previous block's.
       if (!(ok = wait_warp(p_empty, (mcount & 1u) ^ 1u))) break;
 #pragma unroll
-      for (int c16 = 0; c16 < kBKV / 8; ++c16) {
-        const int cc = c16 & 7;
-        const uint32_t addr = ptx::smem_addr(prow + (c16 >> 3) * kAtom) + ((cc ^ (row & 7)) << 4);
+      for (int cc = 0; cc < 8; ++cc) {
+        const uint32_t addr = prow + ((cc ^ (row & 7)) << 4);
         asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr),
-                     "r"(pk[4 * c16]), "r"(pk[4 * c16 + 1]), "r"(pk[4 * c16 + 2]),
-                     "r"(pk[4 * c16 + 3])
+                     "r"(pk[4 * cc]), "r"(pk[4 * cc + 1]), "r"(pk[4 * cc + 2]),
+                     "r"(pk[4 * cc + 3])
                      : "memory");
       }
       ptx::fence_proxy_async_smem();            // the tensor core reads P next
@@ -389,7 +411,12 @@ __global__ void __launch_bounds__(192, 1) ring_attention_kernel(const __grid_con
       if (lane == 0) ptx::mbar_arrive(p_full);
       ++mcount;
     }
-    // Output: O / l for the tile's rows inside the shard.
+    // The row's sum over both halves.
+    ptx::named_barrier_sync(1, 256);            // both halves have read red
+    red[half * kBQ + row] = l;
+    if (ptx::named_barrier_or(1, 256, !ok)) ok = false;
+    l += red[(half ^ 1) * kBQ + row];
+    // Output: this half's 64 columns of O / l, for rows inside the shard.
     if (ok && wait_warp(o_full, 0)) {
       ptx::tc_fence_after();
       const int grow = qt * kBQ + row;
@@ -397,7 +424,7 @@ __global__ void __launch_bounds__(192, 1) ring_attention_kernel(const __grid_con
       char* dst = static_cast<char*>(p.out[r]) +
                   (static_cast<long long>(grow) * p.H + h) * kD * (p.out_f32 ? 4 : 2);
 #pragma unroll 1
-      for (int c = 0; c < kD; c += 32) {
+      for (int c = c0; c < c0 + kD / 2; c += 32) {
         uint32_t v[32];
         ptx::tmem_ld_32x32b_x32(lane_addr + kColO + c, v);
         ptx::tmem_ld_wait();
@@ -428,7 +455,6 @@ __global__ void __launch_bounds__(192, 1) ring_attention_kernel(const __grid_con
       }
     }
   }
-
   __syncwarp();
   ptx::tc_fence_before();
   __syncthreads();
@@ -494,7 +520,7 @@ fcc_status fcc_ring_attention(int R, const void* const* Q, const void* const* K,
                            kSmem) != cudaSuccess)
     return FCC_ERR_CUDA;
   const unsigned grid = static_cast<unsigned>(R * H * p.qtiles);
-  ring_attention_kernel<<<grid, 192, kSmem, reinterpret_cast<cudaStream_t>(stream)>>>(p);
+  ring_attention_kernel<<<grid, kThreads, kSmem, reinterpret_cast<cudaStream_t>(stream)>>>(p);
   if (cudaGetLastError() != cudaSuccess) return FCC_ERR_CUDA;
   bump_launch_count(1);
   return FCC_OK;
