@@ -16,8 +16,9 @@
 // With the final maxima known before any exponential, no accumulator ever
 // needs rescaling: one exponential per score, at the price of a second Q K^T.
 //
-// Warps: 0 = TMA producer (Q once, then K blocks into a three-stage ring and,
-// in pass 2, V blocks into a two-stage ring), 1 = MMA issue, 2-9 = softmax and
+// Warps: 0 = TMA producer (Q once, then a ring of five 32 KiB slots filled in
+// a fixed order: K_0, K_1, ... in pass 1, K_0, V_0, K_1, V_1, ... in pass 2,
+// so pass 1 has five key blocks in flight), 1 = MMA issue, 2-9 = softmax and
 // output (two warps per TMEM lane quarter of 32 query rows, one for each half
 // of the key columns).  Shared memory (128-byte swizzle throughout):
 //   Q   [128 q][128 d]    K-major, two 64-column atoms of 16 KiB
@@ -42,8 +43,7 @@ namespace {
 constexpr int kD = 128;                          // head dimension
 constexpr int kBQ = 128;                         // query rows per CTA (MMA M)
 constexpr int kBKV = 128;                        // keys per block
-constexpr int kKS = 3;                           // key ring stages
-constexpr int kVS = 2;                           // value ring stages
+constexpr int kSlots = 5;                        // operand ring: 32 KiB slots
 constexpr uint32_t kAtom = 128 * 128;            // 16 KiB: [128 rows][64 bf16]
 constexpr uint32_t kTile = 2 * kAtom;            // 32 KiB: [128][128] bf16
 constexpr uint32_t kTmemCols = 512;
@@ -53,9 +53,9 @@ constexpr uint64_t kDrainNs = 50ull * 1000 * 1000;
 constexpr uint32_t kIdescS = ptx::idesc_bf16_f32(kBQ, kBKV, false, false);
 constexpr uint32_t kIdescO = ptx::idesc_bf16_f32(kBQ, kD, false, true);
 // Q, the key and value rings, P, then the barriers and 4 words.
-constexpr int kBars = 1 + 2 * kKS + 2 * kVS + 2 + 2 + 4;
+constexpr int kBars = 1 + 2 * kSlots + 2 + 2 + 4;
 constexpr int kThreads = 320;                    // warps 0-1 + eight softmax warps
-constexpr int kSmem = 1024 + kTile * (1 + kKS + kVS + 1) + kBars * 8 + 16 + 2 * kBQ * 4;
+constexpr int kSmem = 1024 + kTile * (1 + kSlots + 1) + kBars * 8 + 16 + 2 * kBQ * 4;
 static_assert(kSmem <= 232448, "shared memory per CTA");
 
 struct AttnParams {
@@ -106,16 +106,13 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attention_kernel(const __gri
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* sQ = smem;
-  uint8_t* sK = sQ + kTile;                    // key stage s: sK + s * kTile
-  uint8_t* sV = sK + kKS * kTile;              // value stage s: sV + s * kTile
-  uint8_t* sP = sV + kVS * kTile;
+  uint8_t* sR = sQ + kTile;                    // ring slot s: sR + s * kTile
+  uint8_t* sP = sR + kSlots * kTile;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sP + kTile);
   uint64_t* q_full = bars;
-  uint64_t* k_full = bars + 1;                 // [kKS]
-  uint64_t* k_empty = k_full + kKS;            // [kKS]
-  uint64_t* v_full = k_empty + kKS;            // [kVS]
-  uint64_t* v_empty = v_full + kVS;            // [kVS]
-  uint64_t* s_full = v_empty + kVS;            // [2]
+  uint64_t* r_full = bars + 1;                 // [kSlots]
+  uint64_t* r_empty = r_full + kSlots;         // [kSlots]
+  uint64_t* s_full = r_empty + kSlots;         // [2]
   uint64_t* s_empty = s_full + 2;              // [2]
   uint64_t* p_full = s_empty + 2;
   uint64_t* p_empty = p_full + 1;
@@ -146,13 +143,9 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attention_kernel(const __gri
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(q_full, 1);
-    for (int i = 0; i < kKS; ++i) {
-      ptx::mbar_init(&k_full[i], 1);
-      ptx::mbar_init(&k_empty[i], 1);
-    }
-    for (int i = 0; i < kVS; ++i) {
-      ptx::mbar_init(&v_full[i], 1);
-      ptx::mbar_init(&v_empty[i], 1);
+    for (int i = 0; i < kSlots; ++i) {
+      ptx::mbar_init(&r_full[i], 1);
+      ptx::mbar_init(&r_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(&s_full[i], 1);
@@ -185,22 +178,19 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attention_kernel(const __gri
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      // Loads still in flight at an abort: per ring, the stages issued and the
-      // parity of their last use.
-      uint32_t kiss = 0, kpar = 0, viss = 0, vpar = 0;
+      uint32_t iss = 0, par = 0;                // slots with loads in flight (abort drain)
       bool ok = true;
       ptx::mbar_arrive_expect_tx(q_full, kTile);
       for (int b = 0; b < 2; ++b)
         ptx::tma_load_2d(sQ + b * kAtom, &p.mapQ[r], q_full, h * kD + 64 * b, qt * kBQ);
-      int uk = 0, uv = 0;                       // uses of the key and value rings
-      auto load = [&](const CUtensorMap* map, uint8_t* ring, uint64_t* full, uint64_t* empty,
-                      int nst, int& u, uint32_t& iss, uint32_t& par, int y) -> bool {
-        const int st = u % nst;
-        const uint32_t ph = (u / nst) & 1u;
-        if (!W.wait(&empty[st], ph ^ 1u)) return false;
-        ptx::mbar_arrive_expect_tx(&full[st], kTile);
+      int u = 0;                                // ring position
+      auto load = [&](const CUtensorMap* map, int y) -> bool {
+        const int st = u % kSlots;
+        const uint32_t ph = (u / kSlots) & 1u;
+        if (!W.wait(&r_empty[st], ph ^ 1u)) return false;
+        ptx::mbar_arrive_expect_tx(&r_full[st], kTile);
         for (int b = 0; b < 2; ++b)
-          ptx::tma_load_2d(ring + st * kTile + b * kAtom, map, &full[st], h * kD + 64 * b, y);
+          ptx::tma_load_2d(sR + st * kTile + b * kAtom, map, &r_full[st], h * kD + 64 * b, y);
         iss |= 1u << st;
         par = (par & ~(1u << st)) | (ph << st);
         ++u;
@@ -211,16 +201,14 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attention_kernel(const __gri
           if (!walk.visible(i)) continue;
           const int sh = walk.shard(i);
           const int y = walk.row0(i);
-          ok = load(&p.mapK[sh], sK, k_full, k_empty, kKS, uk, kiss, kpar, y);
-          if (ok && pass == 1) ok = load(&p.mapV[sh], sV, v_full, v_empty, kVS, uv, viss, vpar, y);
+          ok = load(&p.mapK[sh], y);
+          if (ok && pass == 1) ok = load(&p.mapV[sh], y);
         }
       }
       if (*abort_flag) {
         W.drain(q_full, 0, kDrainNs);
-        for (int st = 0; st < kKS; ++st)
-          if (kiss & (1u << st)) W.drain(&k_full[st], (kpar >> st) & 1u, kDrainNs);
-        for (int st = 0; st < kVS; ++st)
-          if (viss & (1u << st)) W.drain(&v_full[st], (vpar >> st) & 1u, kDrainNs);
+        for (int st = 0; st < kSlots; ++st)
+          if (iss & (1u << st)) W.drain(&r_full[st], (par >> st) & 1u, kDrainNs);
       }
     }
   } else if (warp == 1) {
@@ -229,26 +217,30 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attention_kernel(const __gri
       bool ok = W.wait(q_full, 0);
       const uint32_t qa = ptx::smem_addr(sQ);
       const uint32_t pa = ptx::smem_addr(sP);
-      int uk = 0, uv = 0, n = 0, m = 0;        // key / value ring uses, S buffers, P uses
+      // Ring positions: pass 1's key blocks are 0 .. nv-1; pass 2's block j
+      // (j-th visible) has its keys at nv + 2j and its values at nv + 2j + 1.
+      int nv = 0;
+      for (int i = 0; i < nwalk; ++i) nv += walk.visible(i) ? 1 : 0;
+      int kpos = 0, vpos = nv + 1, n = 0, m = 0;  // next key / value positions, S, P uses
       bool any = false;
-      // Issues S_n = Q K^T from the next key stage into S buffer n & 1 and
-      // frees the key stage once the product is done.
+      // Issues S_n = Q K^T from the next key slot into S buffer n & 1 and
+      // frees the slot once the product is done.
       auto issue_s = [&]() -> bool {
-        const int st = uk % kKS;
-        if (!W.wait(&k_full[st], (uk / kKS) & 1u)) return false;
+        const int st = kpos % kSlots;
+        if (!W.wait(&r_full[st], (kpos / kSlots) & 1u)) return false;
         const int b = n & 1;
         if (!W.wait(&s_empty[b], ((n >> 1) & 1u) ^ 1u)) return false;
         ptx::tc_fence_after();
-        const uint32_t ka = ptx::smem_addr(sK + st * kTile);
+        const uint32_t ka = ptx::smem_addr(sR + st * kTile);
         const uint32_t d_tmem = tmem_base + kColS + b * kBKV;
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk)
           ptx::mma_f16(d_tmem, desc_kmajor(qa, kk), desc_kmajor(ka, kk), kIdescS,
                        kk > 0 ? 1u : 0u);
         ptx::mma_commit(&s_full[b]);
-        ptx::mma_commit(&k_empty[st]);
+        ptx::mma_commit(&r_empty[st]);
         ++n;
-        ++uk;
+        kpos += kpos < nv ? 1 : 2;             // pass 2 interleaves keys and values
         any = true;
         return true;
       };
@@ -263,20 +255,20 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attention_kernel(const __gri
       bool pending = false;                    // a block whose P V is still to issue
       bool first_pv = true;
       auto issue_pv = [&]() -> bool {
-        const int st = uv % kVS;
-        if (!W.wait(&v_full[st], (uv / kVS) & 1u)) return false;
+        const int st = vpos % kSlots;
+        if (!W.wait(&r_full[st], (vpos / kSlots) & 1u)) return false;
         if (!W.wait(p_full, m & 1u)) return false;
         ptx::tc_fence_after();
-        const uint32_t va = ptx::smem_addr(sV + st * kTile);
+        const uint32_t va = ptx::smem_addr(sR + st * kTile);
 #pragma unroll
         for (int kk = 0; kk < kBKV / 16; ++kk)
           ptx::mma_f16(tmem_base + kColO, desc_kmajor(pa, kk), desc_mnmajor(va, kk), kIdescO,
                        (!first_pv || kk > 0) ? 1u : 0u);
         first_pv = false;
         ptx::mma_commit(p_empty);
-        ptx::mma_commit(&v_empty[st]);
+        ptx::mma_commit(&r_empty[st]);
         ++m;
-        ++uv;
+        vpos += 2;
         return true;
       };
       for (int i = 0; i < nwalk && ok; ++i) {
