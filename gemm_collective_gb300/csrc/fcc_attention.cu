@@ -16,15 +16,16 @@
 // With the final maxima known before any exponential, no accumulator ever
 // needs rescaling: one exponential per score, at the price of a second Q K^T.
 //
-// Warps: 0 = TMA producer (Q once, then a ring of five 32 KiB slots filled in
-// a fixed order: K_0, K_1, ... in pass 1, K_0, V_0, K_1, V_1, ... in pass 2,
-// so pass 1 has five key blocks in flight), 1 = MMA issue, 2-9 = softmax and
+// Warps: 0 = TMA producer (Q once, then a ring of four 32 KiB slots filled in
+// a fixed order: K_0, K_1, ... in pass 1, K_0, V_0, K_1, V_1, ... in pass 2),
+// 1 = MMA issue, 2-9 = softmax and
 // output (two warps per TMEM lane quarter of 32 query rows, one for each half
 // of the key columns).  Shared memory (128-byte swizzle throughout):
 //   Q   [128 q][128 d]    K-major, two 64-column atoms of 16 KiB
 //   K_j [128 keys][128 d] K-major (the B operand of Q K^T)
 //   V_j [128 keys][128 d] MN-major B operand of P V: two 64-column atoms
-//   P   [128 q][128 keys] K-major, written by the softmax threads
+//   P   [128 q][128 keys] K-major, written by the softmax threads; two
+//       buffers, so the softmax of block i+1 overlaps the P V of block i
 // TMEM: S double buffer (2 x 128 columns) and O (128 columns).
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -43,7 +44,7 @@ namespace {
 constexpr int kD = 128;                          // head dimension
 constexpr int kBQ = 128;                         // query rows per CTA (MMA M)
 constexpr int kBKV = 128;                        // keys per block
-constexpr int kSlots = 5;                        // operand ring: 32 KiB slots
+constexpr int kSlots = 4;                        // operand ring: 32 KiB slots
 constexpr uint32_t kAtom = 128 * 128;            // 16 KiB: [128 rows][64 bf16]
 constexpr uint32_t kTile = 2 * kAtom;            // 32 KiB: [128][128] bf16
 constexpr uint32_t kTmemCols = 512;
@@ -53,9 +54,9 @@ constexpr uint64_t kDrainNs = 50ull * 1000 * 1000;
 constexpr uint32_t kIdescS = ptx::idesc_bf16_f32(kBQ, kBKV, false, false);
 constexpr uint32_t kIdescO = ptx::idesc_bf16_f32(kBQ, kD, false, true);
 // Q, the key and value rings, P, then the barriers and 4 words.
-constexpr int kBars = 1 + 2 * kSlots + 2 + 2 + 4;
+constexpr int kBars = 1 + 2 * kSlots + 2 + 2 + 2 + 2 + 2;
 constexpr int kThreads = 320;                    // warps 0-1 + eight softmax warps
-constexpr int kSmem = 1024 + kTile * (1 + kSlots + 1) + kBars * 8 + 16 + 2 * kBQ * 4;
+constexpr int kSmem = 1024 + kTile * (1 + kSlots + 2) + kBars * 8 + 16 + 2 * kBQ * 4;
 static_assert(kSmem <= 232448, "shared memory per CTA");
 
 struct AttnParams {
@@ -107,16 +108,16 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attention_kernel(const __gri
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* sQ = smem;
   uint8_t* sR = sQ + kTile;                    // ring slot s: sR + s * kTile
-  uint8_t* sP = sR + kSlots * kTile;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sP + kTile);
+  uint8_t* sP = sR + kSlots * kTile;          // P buffer b: sP + b * kTile
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sP + 2 * kTile);
   uint64_t* q_full = bars;
   uint64_t* r_full = bars + 1;                 // [kSlots]
   uint64_t* r_empty = r_full + kSlots;         // [kSlots]
   uint64_t* s_full = r_empty + kSlots;         // [2]
   uint64_t* s_empty = s_full + 2;              // [2]
-  uint64_t* p_full = s_empty + 2;
-  uint64_t* p_empty = p_full + 1;
-  uint64_t* o_full = p_empty + 1;
+  uint64_t* p_full = s_empty + 2;              // [2]
+  uint64_t* p_empty = p_full + 2;              // [2]
+  uint64_t* o_full = p_empty + 2;
   uint64_t* mma_done = o_full + 1;             // kBars barriers in all
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -151,8 +152,10 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attention_kernel(const __gri
       ptx::mbar_init(&s_full[i], 1);
       ptx::mbar_init(&s_empty[i], 8);          // the eight softmax warps
     }
-    ptx::mbar_init(p_full, 8);
-    ptx::mbar_init(p_empty, 1);
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(&p_full[i], 8);
+      ptx::mbar_init(&p_empty[i], 1);
+    }
     ptx::mbar_init(o_full, 1);
     ptx::mbar_init(mma_done, 1);
     *abort_flag = 0;
@@ -216,7 +219,7 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attention_kernel(const __gri
     if (lane == 0) {
       bool ok = W.wait(q_full, 0);
       const uint32_t qa = ptx::smem_addr(sQ);
-      const uint32_t pa = ptx::smem_addr(sP);
+      const uint32_t pa0 = ptx::smem_addr(sP);
       // Ring positions: pass 1's key blocks are 0 .. nv-1; pass 2's block j
       // (j-th visible) has its keys at nv + 2j and its values at nv + 2j + 1.
       int nv = 0;
@@ -257,15 +260,17 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attention_kernel(const __gri
       auto issue_pv = [&]() -> bool {
         const int st = vpos % kSlots;
         if (!W.wait(&r_full[st], (vpos / kSlots) & 1u)) return false;
-        if (!W.wait(p_full, m & 1u)) return false;
+        const int pb = m & 1;
+        if (!W.wait(&p_full[pb], (m >> 1) & 1u)) return false;
         ptx::tc_fence_after();
+        const uint32_t pa = pa0 + pb * kTile;
         const uint32_t va = ptx::smem_addr(sR + st * kTile);
 #pragma unroll
         for (int kk = 0; kk < kBKV / 16; ++kk)
           ptx::mma_f16(tmem_base + kColO, desc_kmajor(pa, kk), desc_mnmajor(va, kk), kIdescO,
                        (!first_pv || kk > 0) ? 1u : 0u);
         first_pv = false;
-        ptx::mma_commit(p_empty);
+        ptx::mma_commit(&p_empty[pb]);
         ptx::mma_commit(&r_empty[st]);
         ++m;
         vpos += 2;
@@ -355,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attention_kernel(const __gri
     const float msc = mx * p.scale_log2;
     float l = 0.f;
     int mcount = 0;                             // P buffers written
-    const uint32_t prow = ptx::smem_addr(sP + half * kAtom + row * 128);
+    const uint32_t prow0 = ptx::smem_addr(sP + half * kAtom + row * 128);
     for (int i = 0; i < nwalk && ok; ++i) {
       if (!walk.visible(i)) continue;
       const int b = n & 1;
@@ -388,8 +393,11 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attention_kernel(const __gri
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&s_empty[b]);
       ++n;
-      // P is free once the tensor core has read the previous block's.
-      if (!(ok = wait_warp(p_empty, (mcount & 1u) ^ 1u))) break;
+      // P buffer mcount & 1 is free once the tensor core has read the block
+      // two before.
+      const int pb = mcount & 1;
+      if (!(ok = wait_warp(&p_empty[pb], ((mcount >> 1) & 1u) ^ 1u))) break;
+      const uint32_t prow = prow0 + pb * kTile;
 #pragma unroll
       for (int cc = 0; cc < 8; ++cc) {
         const uint32_t addr = prow + ((cc ^ (row & 7)) << 4);
@@ -400,7 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attention_kernel(const __gri
       }
       ptx::fence_proxy_async_smem();            // the tensor core reads P next
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(p_full);
+      if (lane == 0) ptx::mbar_arrive(&p_full[pb]);
       ++mcount;
     }
     // The row's sum over both halves.
