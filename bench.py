@@ -510,8 +510,8 @@ def other_ops(fcc, torch, np, synth, dev, stream, dA_rs, dB_rs, pk, only=None):
             fl = w.flops() * (0.5 if causal else 1.0)   # causal: the lower triangle
             res[name] = {"ms": t, "TFLOP/s": fl / (t * 1e-3) / 1e12,
                          "roofline_frac": fl / (t * 1e-3) / 1e12 / tc}
-        res["note"] = ("useful FLOPs 4 L^2 d H (half with the mask); the kernel computes Q K^T "
-                       "twice (two-pass softmax): 1.5x those on the tensor cores")
+        res["note"] = ("useful FLOPs 4 L^2 d H (half with the mask); one pass, softmax with a "
+                       "lazily raised maximum")
         ops[w.name] = res
         del dq, dk, dv, O, Q, K, V
 

@@ -7,25 +7,26 @@
 // (its own shard first, then r+1, r+2, ...), reading each block straight from
 // the shard that holds it: the ring's transfers are the CTA's own loads.
 //
-// One CTA per (rank, head, 128-query tile); d = 128.  Two passes over the
-// key/value blocks of 128 positions:
-//   pass 1  S = Q K^T (tcgen05, M = N = K = 128, f32 in TMEM) -> row maxima m;
-//   pass 2  S again; p = exp(s - m) (f32, <= 1), l += p; P (bf16) into shared
-//           memory as the A operand of O += P V (tcgen05, O in TMEM); at the
-//           end O / l.
-// With the final maxima known before any exponential, no accumulator ever
-// needs rescaling: one exponential per score, at the price of a second Q K^T.
+// One CTA per (rank, head, 128-query tile); d = 128.  One pass over the
+// key/value blocks of 128 positions, softmax with a lazily raised maximum:
+//   S = Q K^T (tcgen05, M = N = K = 128, f32 in TMEM); each row keeps the
+//   maximum m it exponentiates against and raises it only when a block's
+//   maximum exceeds it by more than 8 (log2 units), so p = 2^(s c - m c)
+//   stays <= 2^8; raising it rescales the row's O accumulator (in TMEM) and
+//   its sum l by 2^(m_old c - m_new c) while no P V is in flight;
+//   P (bf16) goes to shared memory as the A operand of O += P V (tcgen05,
+//   O in TMEM); at the end O / l.
 //
-// Warps: 0 = TMA producer (Q once, then a ring of four 32 KiB slots filled in
-// a fixed order: K_0, K_1, ... in pass 1, K_0, V_0, K_1, V_1, ... in pass 2),
-// 1 = MMA issue, 2-9 = softmax and
+// Warps: 0 = TMA producer (Q once, then a ring of five 32 KiB slots filled
+// K_0, V_0, K_1, V_1, ...), 1 = MMA issue (S_{i+1} is issued before P_i is
+// ready, so the tensor core works while the softmax runs), 2-9 = softmax and
 // output (two warps per TMEM lane quarter of 32 query rows, one for each half
-// of the key columns).  Shared memory (128-byte swizzle throughout):
+// of the key and output columns; the halves agree on each block's row maximum
+// through shared memory).  Shared memory (128-byte swizzle throughout):
 //   Q   [128 q][128 d]    K-major, two 64-column atoms of 16 KiB
 //   K_j [128 keys][128 d] K-major (the B operand of Q K^T)
 //   V_j [128 keys][128 d] MN-major B operand of P V: two 64-column atoms
-//   P   [128 q][128 keys] K-major, written by the softmax threads; two
-//       buffers, so the softmax of block i+1 overlaps the P V of block i
+//   P   [128 q][128 keys] K-major, written by the softmax threads
 // TMEM: S double buffer (2 x 128 columns) and O (128 columns).
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -44,19 +45,20 @@ namespace {
 constexpr int kD = 128;                          // head dimension
 constexpr int kBQ = 128;                         // query rows per CTA (MMA M)
 constexpr int kBKV = 128;                        // keys per block
-constexpr int kSlots = 4;                        // operand ring: 32 KiB slots
+constexpr int kSlots = 5;                        // operand ring: 32 KiB slots
 constexpr uint32_t kAtom = 128 * 128;            // 16 KiB: [128 rows][64 bf16]
 constexpr uint32_t kTile = 2 * kAtom;            // 32 KiB: [128][128] bf16
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0, kColO = 256;       // S buffers at 0 and 128, O at 256
+constexpr float kRaise = 8.f;                    // raise the maximum past this (log2 units)
 constexpr uint64_t kDrainNs = 50ull * 1000 * 1000;
 // S = Q K^T: both operands K-major.  O += P V: A K-major, B (V) MN-major.
 constexpr uint32_t kIdescS = ptx::idesc_bf16_f32(kBQ, kBKV, false, false);
 constexpr uint32_t kIdescO = ptx::idesc_bf16_f32(kBQ, kD, false, true);
-// Q, the key and value rings, P, then the barriers and 4 words.
-constexpr int kBars = 1 + 2 * kSlots + 2 + 2 + 2 + 2 + 2;
+// Q, the ring, P, then the barriers, 4 words and the halves' exchange row.
+constexpr int kBars = 1 + 2 * kSlots + 2 + 2 + 1 + 1 + 2;
 constexpr int kThreads = 320;                    // warps 0-1 + eight softmax warps
-constexpr int kSmem = 1024 + kTile * (1 + kSlots + 2) + kBars * 8 + 16 + 2 * kBQ * 4;
+constexpr int kSmem = 1024 + kTile * (1 + kSlots + 1) + kBars * 8 + 16 + 2 * kBQ * 4;
 static_assert(kSmem <= 232448, "shared memory per CTA");
 
 struct AttnParams {
@@ -108,16 +110,16 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attention_kernel(const __gri
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* sQ = smem;
   uint8_t* sR = sQ + kTile;                    // ring slot s: sR + s * kTile
-  uint8_t* sP = sR + kSlots * kTile;          // P buffer b: sP + b * kTile
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sP + 2 * kTile);
+  uint8_t* sP = sR + kSlots * kTile;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sP + kTile);
   uint64_t* q_full = bars;
   uint64_t* r_full = bars + 1;                 // [kSlots]
   uint64_t* r_empty = r_full + kSlots;         // [kSlots]
   uint64_t* s_full = r_empty + kSlots;         // [2]
   uint64_t* s_empty = s_full + 2;              // [2]
-  uint64_t* p_full = s_empty + 2;              // [2]
-  uint64_t* p_empty = p_full + 2;              // [2]
-  uint64_t* o_full = p_empty + 2;
+  uint64_t* p_full = s_empty + 2;
+  uint64_t* p_empty = p_full + 1;
+  uint64_t* o_full = p_empty + 1;
   uint64_t* mma_done = o_full + 1;             // kBars barriers in all
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -152,10 +154,8 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attention_kernel(const __gri
       ptx::mbar_init(&s_full[i], 1);
       ptx::mbar_init(&s_empty[i], 8);          // the eight softmax warps
     }
-    for (int i = 0; i < 2; ++i) {
-      ptx::mbar_init(&p_full[i], 8);
-      ptx::mbar_init(&p_empty[i], 1);
-    }
+    ptx::mbar_init(p_full, 8);
+    ptx::mbar_init(p_empty, 1);
     ptx::mbar_init(o_full, 1);
     ptx::mbar_init(mma_done, 1);
     *abort_flag = 0;
@@ -186,7 +186,7 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attention_kernel(const __gri
       ptx::mbar_arrive_expect_tx(q_full, kTile);
       for (int b = 0; b < 2; ++b)
         ptx::tma_load_2d(sQ + b * kAtom, &p.mapQ[r], q_full, h * kD + 64 * b, qt * kBQ);
-      int u = 0;                                // ring position
+      int u = 0;                                // ring position: K_j at 2j, V_j at 2j + 1
       auto load = [&](const CUtensorMap* map, int y) -> bool {
         const int st = u % kSlots;
         const uint32_t ph = (u / kSlots) & 1u;
@@ -199,14 +199,11 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attention_kernel(const __gri
         ++u;
         return true;
       };
-      for (int pass = 0; pass < 2 && ok; ++pass) {
-        for (int i = 0; i < nwalk && ok; ++i) {
-          if (!walk.visible(i)) continue;
-          const int sh = walk.shard(i);
-          const int y = walk.row0(i);
-          ok = load(&p.mapK[sh], y);
-          if (ok && pass == 1) ok = load(&p.mapV[sh], y);
-        }
+      for (int i = 0; i < nwalk && ok; ++i) {
+        if (!walk.visible(i)) continue;
+        const int sh = walk.shard(i);
+        const int y = walk.row0(i);
+        ok = load(&p.mapK[sh], y) && load(&p.mapV[sh], y);
       }
       if (*abort_flag) {
         W.drain(q_full, 0, kDrainNs);
@@ -219,15 +216,11 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attention_kernel(const __gri
     if (lane == 0) {
       bool ok = W.wait(q_full, 0);
       const uint32_t qa = ptx::smem_addr(sQ);
-      const uint32_t pa0 = ptx::smem_addr(sP);
-      // Ring positions: pass 1's key blocks are 0 .. nv-1; pass 2's block j
-      // (j-th visible) has its keys at nv + 2j and its values at nv + 2j + 1.
-      int nv = 0;
-      for (int i = 0; i < nwalk; ++i) nv += walk.visible(i) ? 1 : 0;
-      int kpos = 0, vpos = nv + 1, n = 0, m = 0;  // next key / value positions, S, P uses
+      const uint32_t pa = ptx::smem_addr(sP);
+      int kpos = 0, vpos = 1, n = 0, m = 0;    // next key / value ring positions, S, P uses
       bool any = false;
-      // Issues S_n = Q K^T from the next key slot into S buffer n & 1 and
-      // frees the slot once the product is done.
+      // S_n = Q K^T from the next key slot into S buffer n & 1; the key slot is
+      // free once the product is done.
       auto issue_s = [&]() -> bool {
         const int st = kpos % kSlots;
         if (!W.wait(&r_full[st], (kpos / kSlots) & 1u)) return false;
@@ -243,39 +236,30 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attention_kernel(const __gri
         ptx::mma_commit(&s_full[b]);
         ptx::mma_commit(&r_empty[st]);
         ++n;
-        kpos += kpos < nv ? 1 : 2;             // pass 2 interleaves keys and values
+        kpos += 2;
         any = true;
         return true;
       };
-      // Pass 1: maxima only.
-      for (int i = 0; i < nwalk && ok; ++i) {
-        if (!walk.visible(i)) continue;
-        ok = issue_s();
-      }
-      // Pass 2: S_i, then (once the softmax warps have written P_i) O += P_i V_i.
-      // S_{i+1} is issued before waiting for P_i, so the softmax of one block
-      // overlaps the tensor core's work on the next.
-      bool pending = false;                    // a block whose P V is still to issue
-      bool first_pv = true;
+      // O += P_m V_m once the softmax warps have written P_m (and, if a row's
+      // maximum was raised, rescaled O).
       auto issue_pv = [&]() -> bool {
         const int st = vpos % kSlots;
         if (!W.wait(&r_full[st], (vpos / kSlots) & 1u)) return false;
-        const int pb = m & 1;
-        if (!W.wait(&p_full[pb], (m >> 1) & 1u)) return false;
+        if (!W.wait(p_full, m & 1u)) return false;
         ptx::tc_fence_after();
-        const uint32_t pa = pa0 + pb * kTile;
         const uint32_t va = ptx::smem_addr(sR + st * kTile);
 #pragma unroll
         for (int kk = 0; kk < kBKV / 16; ++kk)
           ptx::mma_f16(tmem_base + kColO, desc_kmajor(pa, kk), desc_mnmajor(va, kk), kIdescO,
-                       (!first_pv || kk > 0) ? 1u : 0u);
-        first_pv = false;
-        ptx::mma_commit(&p_empty[pb]);
+                       (m > 0 || kk > 0) ? 1u : 0u);
+        ptx::mma_commit(p_empty);
         ptx::mma_commit(&r_empty[st]);
         ++m;
         vpos += 2;
         return true;
       };
+      // S_{i+1} goes in before P_i is awaited.
+      bool pending = false;
       for (int i = 0; i < nwalk && ok; ++i) {
         if (!walk.visible(i)) continue;
         if (!(ok = issue_s())) break;
@@ -292,11 +276,9 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attention_kernel(const __gri
   } else {
     // ------------------------------------------------- softmax and output
     // Eight warps: warp w reads TMEM lane quarter w % 4 (32 query rows) and
-    // columns [64 c, 64 c + 64) of each block, c = (w - 2) / 4.  The two
-    // halves of a row meet twice through shared memory: for the row maximum
-    // after pass 1 and for the row sum at the end.
+    // columns [64 c, 64 c + 64) of each block and of O, c = (w - 2) / 4.
     const int q = warp & 3;                     // TMEM lane quarter of this warp
-    const int half = (warp - 2) >> 2;           // column half of the blocks
+    const int half = (warp - 2) >> 2;           // column half
     const int c0 = half * (kBKV / 2);
     const int row = q * 32 + lane;              // query row of the tile
     const long long qpos = static_cast<long long>(r) * p.S + qt * kBQ + row;
@@ -318,57 +300,55 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attention_kernel(const __gri
       }
       return c;                                 // -1: nothing valid
     };
-    // This half's 64 columns of S buffer b.
-    auto load_s = [&](int b, uint32_t (&v)[64]) {
-      ptx::tmem_ld_32x32b_x32(lane_addr + kColS + b * kBKV + c0,
-                              *reinterpret_cast<uint32_t(*)[32]>(v));
-      ptx::tmem_ld_32x32b_x32(lane_addr + kColS + b * kBKV + c0 + 32,
-                              *reinterpret_cast<uint32_t(*)[32]>(v + 32));
-      ptx::tmem_ld_wait();
+    // The row value v of both halves (every softmax warp calls it the same
+    // number of times, also after a failed wait, so the barriers complete).
+    auto exchange_max = [&](float v, bool& fail) -> float {
+      red[half * kBQ + row] = v;
+      if (ptx::named_barrier_or(1, 256, fail)) fail = true;
+      const float o = red[(half ^ 1) * kBQ + row];
+      ptx::named_barrier_sync(1, 256);          // both read before the next write
+      return fmaxf(v, o);
     };
     bool ok = true;
-    int n = 0;                                  // S buffers consumed
-    float mx = -INFINITY;
-    // Pass 1: the row maximum of the raw scores (this half's columns).
-    for (int i = 0; i < nwalk && ok; ++i) {
+    int n = 0;                                  // S buffers consumed (= P buffers written)
+    float m_used = -INFINITY;                   // the maximum p is taken against
+    float l = 0.f;                              // this half's sum of p
+    const uint32_t prow = ptx::smem_addr(sP + half * kAtom + row * 128);
+    for (int i = 0; i < nwalk; ++i) {
       if (!walk.visible(i)) continue;
       const int b = n & 1;
-      if (!(ok = wait_warp(&s_full[b], (n >> 1) & 1u))) break;
-      ptx::tc_fence_after();
+      bool fail = !ok || !wait_warp(&s_full[b], (n >> 1) & 1u);
+      uint32_t v[64];
       const int cmax = last_col(i) - c0;        // in this half's columns
-      uint32_t v[64];
-      load_s(b, v);
-      if (cmax >= 63) {
+      float bm = -INFINITY;
+      if (!fail) {
+        ptx::tc_fence_after();
+        ptx::tmem_ld_32x32b_x32(lane_addr + kColS + b * kBKV + c0,
+                                *reinterpret_cast<uint32_t(*)[32]>(v));
+        ptx::tmem_ld_32x32b_x32(lane_addr + kColS + b * kBKV + c0 + 32,
+                                *reinterpret_cast<uint32_t(*)[32]>(v + 32));
+        ptx::tmem_ld_wait();
+        if (cmax >= 63) {
 #pragma unroll
-        for (int k = 0; k < 64; ++k) mx = fmaxf(mx, __uint_as_float(v[k]));
-      } else {
+          for (int k = 0; k < 64; ++k) bm = fmaxf(bm, __uint_as_float(v[k]));
+        } else {
 #pragma unroll
-        for (int k = 0; k < 64; ++k)
-          if (k <= cmax) mx = fmaxf(mx, __uint_as_float(v[k]));
+          for (int k = 0; k < 64; ++k)
+            if (k <= cmax) bm = fmaxf(bm, __uint_as_float(v[k]));
+        }
       }
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&s_empty[b]);
-      ++n;
-    }
-    // The row's maximum over both halves (every softmax warp gets here, also
-    // after a failed wait, so the barrier always completes).
-    red[half * kBQ + row] = mx;
-    if (ptx::named_barrier_or(1, 256, !ok)) ok = false;
-    mx = fmaxf(mx, red[(half ^ 1) * kBQ + row]);
-    // Pass 2: p = exp(s - m) into this half of P (bf16), l = this half's sum.
-    const float msc = mx * p.scale_log2;
-    float l = 0.f;
-    int mcount = 0;                             // P buffers written
-    const uint32_t prow0 = ptx::smem_addr(sP + half * kAtom + row * 128);
-    for (int i = 0; i < nwalk && ok; ++i) {
-      if (!walk.visible(i)) continue;
-      const int b = n & 1;
-      if (!(ok = wait_warp(&s_full[b], (n >> 1) & 1u))) break;
-      ptx::tc_fence_after();
-      const int cmax = last_col(i) - c0;
-      uint32_t v[64];
-      load_s(b, v);
+      bm = exchange_max(bm, fail);              // the block's row maximum (both halves)
+      if (fail) {
+        ok = false;
+        break;
+      }
+      // Raise the maximum when this block's exceeds it by more than kRaise.
+      const bool raise = bm * p.scale_log2 > m_used * p.scale_log2 + kRaise;
+      const float m_new = raise ? bm : m_used;
+      const float corr = ptx::ex2_approx((m_used - m_new) * p.scale_log2);  // 0 at the start
+      if (raise) l *= (m_used == -INFINITY) ? 0.f : corr;
+      m_used = m_new;
+      const float msc = m_used * p.scale_log2;
       uint32_t pk[32];                          // bf16 pairs of p
       if (cmax >= 63) {
 #pragma unroll
@@ -392,12 +372,32 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attention_kernel(const __gri
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&s_empty[b]);
-      ++n;
-      // P buffer mcount & 1 is free once the tensor core has read the block
-      // two before.
-      const int pb = mcount & 1;
-      if (!(ok = wait_warp(&p_empty[pb], ((mcount >> 1) & 1u) ^ 1u))) break;
-      const uint32_t prow = prow0 + pb * kTile;
+      // P (and O) are free once the tensor core has finished the previous
+      // block's P V: no P V is in flight from here until P_n is signalled.
+      // (A failed wait is carried to the next exchange, where all eight
+      // warps leave the loop together.)
+      if (!wait_warp(p_empty, (n & 1u) ^ 1u)) {
+        ok = false;
+        ++n;
+        continue;
+      }
+      // Rows whose maximum was raised rescale their half of O (after the
+      // first block, when O holds earlier blocks' sums).
+      if (n > 0 && __any_sync(0xffffffffu, raise)) {
+        ptx::tc_fence_after();
+        const float f = raise ? corr : 1.f;
+#pragma unroll 1
+        for (int c = c0; c < c0 + kD / 2; c += 32) {
+          uint32_t o[32];
+          ptx::tmem_ld_32x32b_x32(lane_addr + kColO + c, o);
+          ptx::tmem_ld_wait();
+#pragma unroll
+          for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * f);
+          ptx::tmem_st_32x32b_x32(lane_addr + kColO + c, o);
+        }
+        ptx::tmem_st_wait();
+        ptx::tc_fence_before();                 // the tensor core accumulates on top next
+      }
 #pragma unroll
       for (int cc = 0; cc < 8; ++cc) {
         const uint32_t addr = prow + ((cc ^ (row & 7)) << 4);
@@ -408,11 +408,10 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attention_kernel(const __gri
       }
       ptx::fence_proxy_async_smem();            // the tensor core reads P next
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&p_full[pb]);
-      ++mcount;
+      if (lane == 0) ptx::mbar_arrive(p_full);
+      ++n;
     }
-    // The row's sum over both halves.
-    ptx::named_barrier_sync(1, 256);            // both halves have read red
+    // The row's sum over both halves (both used the same maxima).
     red[half * kBQ + row] = l;
     if (ptx::named_barrier_or(1, 256, !ok)) ok = false;
     l += red[(half ^ 1) * kBQ + row];
@@ -455,6 +454,7 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attention_kernel(const __gri
       }
     }
   }
+
   __syncwarp();
   ptx::tc_fence_before();
   __syncthreads();

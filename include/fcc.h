@@ -277,7 +277,8 @@ size_t fcc_embedding_workspace_size(int R, int ntables, int64_t D, int64_t Bl,
  * over all global positions j (causal != 0: only j <= r*S + t).
  * Q[r], K[r], V[r]: [S, H, d] bf16; O[r]: [S, H, d] (bf16 or f32).  d = 128
  * (others: FCC_ERR_UNSUPPORTED).  Scores, softmax and sums in f32; the
- * probabilities enter the P V product as bf16.  No workspace.
+ * probabilities (relative to a running row maximum) enter the P V product as
+ * bf16.  Repeatable (a fixed order).  No workspace.
  */
 fcc_status fcc_ring_attention(int R, const void *const *Q, const void *const *K,
                               const void *const *V, void *const *O, int64_t S, int H, int64_t d,
