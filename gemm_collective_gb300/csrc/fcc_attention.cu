@@ -330,7 +330,8 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attention_kernel(const __gri
         ptx::tmem_ld_wait();
         if (cmax >= 63) {
 #pragma unroll
-          for (int k = 0; k < 64; ++k) bm = fmaxf(bm, __uint_as_float(v[k]));
+          for (int k = 0; k < 64; k += 2)
+            bm = ptx::max3(bm, __uint_as_float(v[k]), __uint_as_float(v[k + 1]));
         } else {
 #pragma unroll
           for (int k = 0; k < 64; ++k)

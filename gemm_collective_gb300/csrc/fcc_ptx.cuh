@@ -422,6 +422,13 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return r;
 }
 
+// max(a, b, c) in one instruction (PTX three-input max.f32).
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 // 2^x by the hardware's approximate exponential (PTX ex2.approx.ftz.f32,
 // relative error about 2^-22; subnormal results flush to zero).
 __device__ __forceinline__ float ex2_approx(float x) {
