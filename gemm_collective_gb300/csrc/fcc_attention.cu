@@ -17,7 +17,7 @@
 //   P (bf16) goes to shared memory as the A operand of O += P V (tcgen05,
 //   O in TMEM); at the end O / l.
 //
-// Warps: 0 = TMA producer (Q once, then a ring of five 32 KiB slots filled
+// Warps: 0 = TMA producer (Q once, then a ring of four 32 KiB slots filled
 // K_0, V_0, K_1, V_1, ...), 1 = MMA issue (S_{i+1} is issued before P_i is
 // ready, so the tensor core works while the softmax runs), 2-9 = softmax and
 // output (two warps per TMEM lane quarter of 32 query rows, one for each half
@@ -45,7 +45,7 @@ namespace {
 constexpr int kD = 128;                          // head dimension
 constexpr int kBQ = 128;                         // query rows per CTA (MMA M)
 constexpr int kBKV = 128;                        // keys per block
-constexpr int kSlots = 5;                        // operand ring: 32 KiB slots
+constexpr int kSlots = 4;                        // operand ring: 32 KiB slots (5 measured slower)
 constexpr uint32_t kAtom = 128 * 128;            // 16 KiB: [128 rows][64 bf16]
 constexpr uint32_t kTile = 2 * kAtom;            // 32 KiB: [128][128] bf16
 constexpr uint32_t kTmemCols = 512;
