@@ -14,20 +14,22 @@
 //   maximum exceeds it by more than 8 (log2 units), so p = 2^(s c - m c)
 //   stays <= 2^8; raising it rescales the row's O accumulator (in TMEM) and
 //   its sum l by 2^(m_old c - m_new c) while no P V is in flight;
-//   P (bf16) goes to shared memory as the A operand of O += P V (tcgen05,
-//   O in TMEM); at the end O / l.
+//   P (bf16) goes to shared memory as the A operand of O_c += P_c V_c
+//   (tcgen05, O_c in TMEM, c the key half); at the end, with m = max(m_0, m_1)
+//   and f_c = 2^(m_c c - m c), O = (f_0 O_0 + f_1 O_1) / (f_0 l_0 + f_1 l_1).
 //
 // Warps: 0 = TMA producer (Q once, then a ring of four 32 KiB slots filled
 // K_0, V_0, K_1, V_1, ...), 1 = MMA issue (S_{i+1} is issued before P_i is
 // ready, so the tensor core works while the softmax runs), 2-9 = softmax and
 // output (two warps per TMEM lane quarter of 32 query rows, one for each half
-// of the key and output columns; the halves agree on each block's row maximum
-// through shared memory).  Shared memory (128-byte swizzle throughout):
+// of a block's key columns).  Each half keeps its own row maximum, sum and
+// O accumulator, so the halves never wait on each other inside the walk;
+// they are combined once, at the end.  Shared memory (128-byte swizzle throughout):
 //   Q   [128 q][128 d]    K-major, two 64-column atoms of 16 KiB
 //   K_j [128 keys][128 d] K-major (the B operand of Q K^T)
 //   V_j [128 keys][128 d] MN-major B operand of P V: two 64-column atoms
 //   P   [128 q][128 keys] K-major, written by the softmax threads
-// TMEM: S double buffer (2 x 128 columns) and O (128 columns).
+// TMEM: S double buffer (2 x 128 columns) and O_0, O_1 (128 columns each).
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -49,16 +51,18 @@ constexpr int kSlots = 4;                        // operand ring: 32 KiB slots (
 constexpr uint32_t kAtom = 128 * 128;            // 16 KiB: [128 rows][64 bf16]
 constexpr uint32_t kTile = 2 * kAtom;            // 32 KiB: [128][128] bf16
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0, kColO = 256;       // S buffers at 0 and 128, O at 256
+constexpr uint32_t kColS = 0, kColO = 256;       // S buffers at 0 and 128, O_0 at 256, O_1 at 384
 constexpr float kRaise = 8.f;                    // raise the maximum past this (log2 units)
 constexpr uint64_t kDrainNs = 50ull * 1000 * 1000;
 // S = Q K^T: both operands K-major.  O += P V: A K-major, B (V) MN-major.
 constexpr uint32_t kIdescS = ptx::idesc_bf16_f32(kBQ, kBKV, false, false);
 constexpr uint32_t kIdescO = ptx::idesc_bf16_f32(kBQ, kD, false, true);
-// Q, the ring, P, then the barriers, 4 words and the halves' exchange row.
+// Q, the ring, P, then the barriers, 4 words and the parts' exchange rows.
 constexpr int kBars = 1 + 2 * kSlots + 2 + 2 + 1 + 1 + 2;
-constexpr int kThreads = 320;                    // warps 0-1 + eight softmax warps
-constexpr int kSmem = 1024 + kTile * (1 + kSlots + 1) + kBars * 8 + 16 + 2 * kBQ * 4;
+constexpr int kHalf = kBKV / 2;                  // key columns of a block per softmax warp
+constexpr int kSoftmax = 8;                      // softmax warps: two per TMEM lane quarter
+constexpr int kThreads = 64 + 32 * kSoftmax;     // warps 0-1 + the softmax warps
+constexpr int kSmem = 1024 + kTile * (1 + kSlots + 1) + kBars * 8 + 16 + 4 * kBQ * 4;
 static_assert(kSmem <= 232448, "shared memory per CTA");
 
 struct AttnParams {
@@ -123,7 +127,7 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attention_kernel(const __gri
   uint64_t* mma_done = o_full + 1;             // kBars barriers in all
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  float* red = reinterpret_cast<float*>(tmem_slot + 4);  // [2][128]: the halves' row values
+  float* red = reinterpret_cast<float*>(tmem_slot + 4);  // [2][2][128]: the halves' (m, l)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -152,9 +156,9 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attention_kernel(const __gri
     }
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(&s_full[i], 1);
-      ptx::mbar_init(&s_empty[i], 8);          // the eight softmax warps
+      ptx::mbar_init(&s_empty[i], kSoftmax);   // every softmax warp
     }
-    ptx::mbar_init(p_full, 8);
+    ptx::mbar_init(p_full, kSoftmax);
     ptx::mbar_init(p_empty, 1);
     ptx::mbar_init(o_full, 1);
     ptx::mbar_init(mma_done, 1);
@@ -240,8 +244,8 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attention_kernel(const __gri
         any = true;
         return true;
       };
-      // O += P_m V_m once the softmax warps have written P_m (and, if a row's
-      // maximum was raised, rescaled O).
+      // O_c += P_m V_m over key half c, once the softmax warps have written
+      // P_m (and, where a row's maximum was raised, rescaled O_c).
       auto issue_pv = [&]() -> bool {
         const int st = vpos % kSlots;
         if (!W.wait(&r_full[st], (vpos / kSlots) & 1u)) return false;
@@ -249,9 +253,9 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attention_kernel(const __gri
         ptx::tc_fence_after();
         const uint32_t va = ptx::smem_addr(sR + st * kTile);
 #pragma unroll
-        for (int kk = 0; kk < kBKV / 16; ++kk)
-          ptx::mma_f16(tmem_base + kColO, desc_kmajor(pa, kk), desc_mnmajor(va, kk), kIdescO,
-                       (m > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < kBKV / 16; ++kk)             // keys 16 kk: half kk / 4
+          ptx::mma_f16(tmem_base + kColO + (kk / 4) * kD, desc_kmajor(pa, kk),
+                       desc_mnmajor(va, kk), kIdescO, (m > 0 || kk % 4 > 0) ? 1u : 0u);
         ptx::mma_commit(p_empty);
         ptx::mma_commit(&r_empty[st]);
         ++m;
@@ -275,14 +279,16 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attention_kernel(const __gri
     }
   } else {
     // ------------------------------------------------- softmax and output
-    // Eight warps: warp w reads TMEM lane quarter w % 4 (32 query rows) and
-    // columns [64 c, 64 c + 64) of each block and of O, c = (w - 2) / 4.
+    // Warp w reads TMEM lane quarter w % 4 (32 query rows) and key columns
+    // [64 c, 64 c + 64) of each block, c = (w - 2) / 4; its rows' maximum m_c,
+    // sum l_c and accumulator O_c (TMEM columns kColO + 128 c) cover those keys.
     const int q = warp & 3;                     // TMEM lane quarter of this warp
-    const int half = (warp - 2) >> 2;           // column half
-    const int c0 = half * (kBKV / 2);
+    const int half = (warp - 2) >> 2;           // key column half
+    const int c0 = half * kHalf;
     const int row = q * 32 + lane;              // query row of the tile
     const long long qpos = static_cast<long long>(r) * p.S + qt * kBQ + row;
     const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+    const uint32_t o_own = lane_addr + kColO + half * kD;
     // Lane 0 waits, the warp follows (the warp stops as one).
     auto wait_warp = [&](uint64_t* bar, uint32_t parity) -> bool {
       int good = 1;
@@ -300,48 +306,37 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attention_kernel(const __gri
       }
       return c;                                 // -1: nothing valid
     };
-    // The row value v of both halves (every softmax warp calls it the same
-    // number of times, also after a failed wait, so the barriers complete).
-    auto exchange_max = [&](float v, bool& fail) -> float {
-      red[half * kBQ + row] = v;
-      if (ptx::named_barrier_or(1, 256, fail)) fail = true;
-      const float o = red[(half ^ 1) * kBQ + row];
-      ptx::named_barrier_sync(1, 256);          // both read before the next write
-      return fmaxf(v, o);
-    };
     bool ok = true;
     int n = 0;                                  // S buffers consumed (= P buffers written)
-    float m_used = -INFINITY;                   // the maximum p is taken against
+    float m_used = -INFINITY;                   // the maximum this half's p is taken against
     float l = 0.f;                              // this half's sum of p
     const uint32_t prow = ptx::smem_addr(sP + half * kAtom + row * 128);
     for (int i = 0; i < nwalk; ++i) {
       if (!walk.visible(i)) continue;
       const int b = n & 1;
-      bool fail = !ok || !wait_warp(&s_full[b], (n >> 1) & 1u);
-      uint32_t v[64];
-      const int cmax = last_col(i) - c0;        // in this half's columns
-      float bm = -INFINITY;
-      if (!fail) {
-        ptx::tc_fence_after();
-        ptx::tmem_ld_32x32b_x32(lane_addr + kColS + b * kBKV + c0,
-                                *reinterpret_cast<uint32_t(*)[32]>(v));
-        ptx::tmem_ld_32x32b_x32(lane_addr + kColS + b * kBKV + c0 + 32,
-                                *reinterpret_cast<uint32_t(*)[32]>(v + 32));
-        ptx::tmem_ld_wait();
-        if (cmax >= 63) {
-#pragma unroll
-          for (int k = 0; k < 64; k += 2)
-            bm = ptx::max3(bm, __uint_as_float(v[k]), __uint_as_float(v[k + 1]));
-        } else {
-#pragma unroll
-          for (int k = 0; k < 64; ++k)
-            if (k <= cmax) bm = fmaxf(bm, __uint_as_float(v[k]));
-        }
-      }
-      bm = exchange_max(bm, fail);              // the block's row maximum (both halves)
-      if (fail) {
+      // A failed wait ends this warp's walk; the others' waits then end on
+      // the abort flag or their own limit (no barrier inside the walk).
+      if (!wait_warp(&s_full[b], (n >> 1) & 1u)) {
         ok = false;
         break;
+      }
+      uint32_t v[kHalf];
+      const int cmax = last_col(i) - c0;        // in this half's columns
+      ptx::tc_fence_after();
+      ptx::tmem_ld_32x32b_x32(lane_addr + kColS + b * kBKV + c0,
+                              *reinterpret_cast<uint32_t(*)[32]>(v));
+      ptx::tmem_ld_32x32b_x32(lane_addr + kColS + b * kBKV + c0 + 32,
+                              *reinterpret_cast<uint32_t(*)[32]>(v + 32));
+      ptx::tmem_ld_wait();
+      float bm = -INFINITY;
+      if (cmax >= kHalf - 1) {
+#pragma unroll
+        for (int k = 0; k < kHalf; k += 2)
+          bm = ptx::max3(bm, __uint_as_float(v[k]), __uint_as_float(v[k + 1]));
+      } else {
+#pragma unroll
+        for (int k = 0; k < kHalf; ++k)
+          if (k <= cmax) bm = fmaxf(bm, __uint_as_float(v[k]));
       }
       // Raise the maximum when this block's exceeds it by more than kRaise.
       const bool raise = bm * p.scale_log2 > m_used * p.scale_log2 + kRaise;
@@ -350,10 +345,10 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attention_kernel(const __gri
       if (raise) l *= (m_used == -INFINITY) ? 0.f : corr;
       m_used = m_new;
       const float msc = m_used * p.scale_log2;
-      uint32_t pk[32];                          // bf16 pairs of p
-      if (cmax >= 63) {
+      uint32_t pk[kHalf / 2];                   // bf16 pairs of p
+      if (cmax >= kHalf - 1) {
 #pragma unroll
-        for (int k = 0; k < 64; k += 2) {
+        for (int k = 0; k < kHalf; k += 2) {
           const float p0 = ptx::ex2_approx(fmaf(__uint_as_float(v[k]), p.scale_log2, -msc));
           const float p1 = ptx::ex2_approx(fmaf(__uint_as_float(v[k + 1]), p.scale_log2, -msc));
           l += p0 + p1;
@@ -361,7 +356,7 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attention_kernel(const __gri
         }
       } else {
 #pragma unroll
-        for (int k = 0; k < 64; k += 2) {
+        for (int k = 0; k < kHalf; k += 2) {
           float p0 = ptx::ex2_approx(fmaf(__uint_as_float(v[k]), p.scale_log2, -msc));
           float p1 = ptx::ex2_approx(fmaf(__uint_as_float(v[k + 1]), p.scale_log2, -msc));
           if (k > cmax) p0 = 0.f;
@@ -373,28 +368,25 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attention_kernel(const __gri
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&s_empty[b]);
-      // P (and O) are free once the tensor core has finished the previous
+      // P (and O_c) are free once the tensor core has finished the previous
       // block's P V: no P V is in flight from here until P_n is signalled.
-      // (A failed wait is carried to the next exchange, where all eight
-      // warps leave the loop together.)
       if (!wait_warp(p_empty, (n & 1u) ^ 1u)) {
         ok = false;
-        ++n;
-        continue;
+        break;
       }
-      // Rows whose maximum was raised rescale their half of O (after the
-      // first block, when O holds earlier blocks' sums).
+      // Rows whose maximum was raised rescale their O_c (after the first
+      // block, when it holds earlier blocks' sums).
       if (n > 0 && __any_sync(0xffffffffu, raise)) {
         ptx::tc_fence_after();
         const float f = raise ? corr : 1.f;
 #pragma unroll 1
-        for (int c = c0; c < c0 + kD / 2; c += 32) {
+        for (int c = 0; c < kD; c += 32) {
           uint32_t o[32];
-          ptx::tmem_ld_32x32b_x32(lane_addr + kColO + c, o);
+          ptx::tmem_ld_32x32b_x32(o_own + c, o);
           ptx::tmem_ld_wait();
 #pragma unroll
           for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * f);
-          ptx::tmem_st_32x32b_x32(lane_addr + kColO + c, o);
+          ptx::tmem_st_32x32b_x32(o_own + c, o);
         }
         ptx::tmem_st_wait();
         ptx::tc_fence_before();                 // the tensor core accumulates on top next
@@ -412,42 +404,49 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attention_kernel(const __gri
       if (lane == 0) ptx::mbar_arrive(p_full);
       ++n;
     }
-    // The row's sum over both halves (both used the same maxima).
-    red[half * kBQ + row] = l;
-    if (ptx::named_barrier_or(1, 256, !ok)) ok = false;
-    l += red[(half ^ 1) * kBQ + row];
-    // Output: this half's 64 columns of O / l, for rows inside the shard.
+    // Combine the halves: each publishes its (m_c, l_c); both form the same
+    // factors f_c = 2^(m_c c - m c) and denominator f_0 l_0 + f_1 l_1.
+    red[half * kBQ + row] = m_used;
+    red[(2 + half) * kBQ + row] = l;
+    if (ptx::named_barrier_or(1, 32 * kSoftmax, !ok)) ok = false;
+    const float m0 = red[row], m1 = red[kBQ + row];
+    const float l0 = red[2 * kBQ + row], l1 = red[3 * kBQ + row];
+    const float mm = fmaxf(m0, m1);
+    const float f0 = m0 == -INFINITY ? 0.f : ptx::ex2_approx((m0 - mm) * p.scale_log2);
+    const float f1 = m1 == -INFINITY ? 0.f : ptx::ex2_approx((m1 - mm) * p.scale_log2);
+    // Output: this half's 64 columns of (f_0 O_0 + f_1 O_1) / l, for rows
+    // inside the shard.
     if (ok && wait_warp(o_full, 0)) {
       ptx::tc_fence_after();
       const int grow = qt * kBQ + row;
-      const float inv = 1.f / l;
+      const float inv = 1.f / (l0 * f0 + l1 * f1);
+      const float g0 = f0 * inv, g1 = f1 * inv;
       char* dst = static_cast<char*>(p.out[r]) +
                   (static_cast<long long>(grow) * p.H + h) * kD * (p.out_f32 ? 4 : 2);
 #pragma unroll 1
-      for (int c = c0; c < c0 + kD / 2; c += 32) {
-        uint32_t v[32];
-        ptx::tmem_ld_32x32b_x32(lane_addr + kColO + c, v);
+      for (int c = c0; c < c0 + kHalf; c += 32) {
+        uint32_t a[32], v[32];
+        ptx::tmem_ld_32x32b_x32(lane_addr + kColO + c, a);
+        ptx::tmem_ld_32x32b_x32(lane_addr + kColO + kD + c, v);
         ptx::tmem_ld_wait();
+        float x[32];
+#pragma unroll
+        for (int k = 0; k < 32; ++k)
+          x[k] = fmaf(__uint_as_float(a[k]), g0, __uint_as_float(v[k]) * g1);
         if (grow < p.S) {
           if (p.out_f32) {
             float4* o = reinterpret_cast<float4*>(dst) + c / 4;
 #pragma unroll
-            for (int k = 0; k < 32; k += 4)
-              o[k / 4] = make_float4(__uint_as_float(v[k]) * inv, __uint_as_float(v[k + 1]) * inv,
-                                     __uint_as_float(v[k + 2]) * inv,
-                                     __uint_as_float(v[k + 3]) * inv);
+            for (int k = 0; k < 32; k += 4) o[k / 4] = make_float4(x[k], x[k + 1], x[k + 2], x[k + 3]);
           } else {
             uint4* o = reinterpret_cast<uint4*>(dst) + c / 8;
 #pragma unroll
             for (int k = 0; k < 32; k += 8) {
               uint4 w;
-              w.x = ptx::pack_bf16x2(__uint_as_float(v[k]) * inv, __uint_as_float(v[k + 1]) * inv);
-              w.y = ptx::pack_bf16x2(__uint_as_float(v[k + 2]) * inv,
-                                     __uint_as_float(v[k + 3]) * inv);
-              w.z = ptx::pack_bf16x2(__uint_as_float(v[k + 4]) * inv,
-                                     __uint_as_float(v[k + 5]) * inv);
-              w.w = ptx::pack_bf16x2(__uint_as_float(v[k + 6]) * inv,
-                                     __uint_as_float(v[k + 7]) * inv);
+              w.x = ptx::pack_bf16x2(x[k], x[k + 1]);
+              w.y = ptx::pack_bf16x2(x[k + 2], x[k + 3]);
+              w.z = ptx::pack_bf16x2(x[k + 4], x[k + 5]);
+              w.w = ptx::pack_bf16x2(x[k + 6], x[k + 7]);
               o[k / 8] = w;
             }
           }
