@@ -14,13 +14,16 @@
 //   maximum exceeds it by more than 8 (log2 units), so p = 2^(s c - m c)
 //   stays <= 2^8; raising it rescales the row's O accumulator (in TMEM) and
 //   its sum l by 2^(m_old c - m_new c) while no P V is in flight;
-//   P (bf16) goes to shared memory as the A operand of O_c += P_c V_c
-//   (tcgen05, O_c in TMEM, c the key half); at the end, with m = max(m_0, m_1)
-//   and f_c = 2^(m_c c - m c), O = (f_0 O_0 + f_1 O_1) / (f_0 l_0 + f_1 l_1).
+//   P (bf16) is written into TMEM over the S columns it came from and is the
+//   A operand of O_c += P_c V_c (tcgen05, A from TMEM, O_c in TMEM, c the key
+//   half); at the end, with m = max(m_0, m_1) and f_c = 2^(m_c c - m c),
+//   O = (f_0 O_0 + f_1 O_1) / (f_0 l_0 + f_1 l_1).
 //
 // Warps: 0 = TMA producer (Q once, then a ring of four 32 KiB slots filled
 // K_0, V_0, K_1, V_1, ...), 1 = MMA issue (S_{i+1} is issued before P_i is
-// ready, so the tensor core works while the softmax runs), 2-9 = softmax and
+// ready, so the tensor core works while the softmax runs; S_{i+2} reuses
+// S_i's columns and is issued after P_i V_i, which the tensor core runs
+// first), 2-9 = softmax and
 // output (two warps per TMEM lane quarter of 32 query rows, one for each half
 // of a block's key columns).  Each half keeps its own row maximum, sum and
 // O accumulator, so the halves never wait on each other inside the walk;
@@ -28,8 +31,9 @@
 //   Q   [128 q][128 d]    K-major, two 64-column atoms of 16 KiB
 //   K_j [128 keys][128 d] K-major (the B operand of Q K^T)
 //   V_j [128 keys][128 d] MN-major B operand of P V: two 64-column atoms
-//   P   [128 q][128 keys] K-major, written by the softmax threads
-// TMEM: S double buffer (2 x 128 columns) and O_0, O_1 (128 columns each).
+// TMEM: S double buffer (2 x 128 columns; P_i in bf16 pairs over the first
+// 32 columns of each half of S_i's) and O_0, O_1 (128 columns each).  No P in
+// shared memory: the tensor core's shared-memory reads are Q, K and V only.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -57,12 +61,12 @@ constexpr uint64_t kDrainNs = 50ull * 1000 * 1000;
 // S = Q K^T: both operands K-major.  O += P V: A K-major, B (V) MN-major.
 constexpr uint32_t kIdescS = ptx::idesc_bf16_f32(kBQ, kBKV, false, false);
 constexpr uint32_t kIdescO = ptx::idesc_bf16_f32(kBQ, kD, false, true);
-// Q, the ring, P, then the barriers, 4 words and the parts' exchange rows.
-constexpr int kBars = 1 + 2 * kSlots + 2 + 2 + 1 + 1 + 2;
+// Q, the ring, then the barriers, 4 words and the halves' (m, l) rows.
+constexpr int kBars = 1 + 2 * kSlots + 2 + 1 + 1 + 2;
 constexpr int kHalf = kBKV / 2;                  // key columns of a block per softmax warp
 constexpr int kSoftmax = 8;                      // softmax warps: two per TMEM lane quarter
 constexpr int kThreads = 64 + 32 * kSoftmax;     // warps 0-1 + the softmax warps
-constexpr int kSmem = 1024 + kTile * (1 + kSlots + 1) + kBars * 8 + 16 + 4 * kBQ * 4;
+constexpr int kSmem = 1024 + kTile * (1 + kSlots) + kBars * 8 + 16 + 4 * kBQ * 4;
 static_assert(kSmem <= 232448, "shared memory per CTA");
 
 struct AttnParams {
@@ -114,14 +118,12 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attention_kernel(const __gri
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* sQ = smem;
   uint8_t* sR = sQ + kTile;                    // ring slot s: sR + s * kTile
-  uint8_t* sP = sR + kSlots * kTile;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sP + kTile);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sR + kSlots * kTile);
   uint64_t* q_full = bars;
   uint64_t* r_full = bars + 1;                 // [kSlots]
   uint64_t* r_empty = r_full + kSlots;         // [kSlots]
   uint64_t* s_full = r_empty + kSlots;         // [2]
-  uint64_t* s_empty = s_full + 2;              // [2]
-  uint64_t* p_full = s_empty + 2;
+  uint64_t* p_full = s_full + 2;
   uint64_t* p_empty = p_full + 1;
   uint64_t* o_full = p_empty + 1;
   uint64_t* mma_done = o_full + 1;             // kBars barriers in all
@@ -154,10 +156,7 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attention_kernel(const __gri
       ptx::mbar_init(&r_full[i], 1);
       ptx::mbar_init(&r_empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      ptx::mbar_init(&s_full[i], 1);
-      ptx::mbar_init(&s_empty[i], kSoftmax);   // every softmax warp
-    }
+    for (int i = 0; i < 2; ++i) ptx::mbar_init(&s_full[i], 1);
     ptx::mbar_init(p_full, kSoftmax);
     ptx::mbar_init(p_empty, 1);
     ptx::mbar_init(o_full, 1);
@@ -220,16 +219,16 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attention_kernel(const __gri
     if (lane == 0) {
       bool ok = W.wait(q_full, 0);
       const uint32_t qa = ptx::smem_addr(sQ);
-      const uint32_t pa = ptx::smem_addr(sP);
       int kpos = 0, vpos = 1, n = 0, m = 0;    // next key / value ring positions, S, P uses
       bool any = false;
       // S_n = Q K^T from the next key slot into S buffer n & 1; the key slot is
-      // free once the product is done.
+      // free once the product is done.  The buffer's last reader, P_{n-2} V,
+      // was issued before (it waited for the softmax to finish with S_{n-2}),
+      // and the tensor core runs this thread's MMAs in issue order.
       auto issue_s = [&]() -> bool {
         const int st = kpos % kSlots;
         if (!W.wait(&r_full[st], (kpos / kSlots) & 1u)) return false;
         const int b = n & 1;
-        if (!W.wait(&s_empty[b], ((n >> 1) & 1u) ^ 1u)) return false;
         ptx::tc_fence_after();
         const uint32_t ka = ptx::smem_addr(sR + st * kTile);
         const uint32_t d_tmem = tmem_base + kColS + b * kBKV;
@@ -245,17 +244,20 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attention_kernel(const __gri
         return true;
       };
       // O_c += P_m V_m over key half c, once the softmax warps have written
-      // P_m (and, where a row's maximum was raised, rescaled O_c).
+      // P_m into TMEM (and, where a row's maximum was raised, rescaled O_c).
+      // Keys 16 kk of P_m: S buffer m & 1, half c = kk / 4, 8 columns a step.
       auto issue_pv = [&]() -> bool {
         const int st = vpos % kSlots;
         if (!W.wait(&r_full[st], (vpos / kSlots) & 1u)) return false;
         if (!W.wait(p_full, m & 1u)) return false;
         ptx::tc_fence_after();
         const uint32_t va = ptx::smem_addr(sR + st * kTile);
+        const uint32_t p_tmem = tmem_base + kColS + (m & 1) * kBKV;
 #pragma unroll
-        for (int kk = 0; kk < kBKV / 16; ++kk)             // keys 16 kk: half kk / 4
-          ptx::mma_f16(tmem_base + kColO + (kk / 4) * kD, desc_kmajor(pa, kk),
-                       desc_mnmajor(va, kk), kIdescO, (m > 0 || kk % 4 > 0) ? 1u : 0u);
+        for (int kk = 0; kk < kBKV / 16; ++kk)
+          ptx::mma_f16_tmem_a(tmem_base + kColO + (kk / 4) * kD,
+                              p_tmem + (kk / 4) * kHalf + (kk % 4) * 8, desc_mnmajor(va, kk),
+                              kIdescO, (m > 0 || kk % 4 > 0) ? 1u : 0u);
         ptx::mma_commit(p_empty);
         ptx::mma_commit(&r_empty[st]);
         ++m;
@@ -310,7 +312,6 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attention_kernel(const __gri
     int n = 0;                                  // S buffers consumed (= P buffers written)
     float m_used = -INFINITY;                   // the maximum this half's p is taken against
     float l = 0.f;                              // this half's sum of p
-    const uint32_t prow = ptx::smem_addr(sP + half * kAtom + row * 128);
     for (int i = 0; i < nwalk; ++i) {
       if (!walk.visible(i)) continue;
       const int b = n & 1;
@@ -330,9 +331,12 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attention_kernel(const __gri
       ptx::tmem_ld_wait();
       float bm = -INFINITY;
       if (cmax >= kHalf - 1) {
+        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};  // four short chains
 #pragma unroll
         for (int k = 0; k < kHalf; k += 2)
-          bm = ptx::max3(bm, __uint_as_float(v[k]), __uint_as_float(v[k + 1]));
+          mx[(k / 2) & 3] = ptx::max3(mx[(k / 2) & 3], __uint_as_float(v[k]),
+                                      __uint_as_float(v[k + 1]));
+        bm = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
       } else {
 #pragma unroll
         for (int k = 0; k < kHalf; ++k)
@@ -346,12 +350,13 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attention_kernel(const __gri
       m_used = m_new;
       const float msc = m_used * p.scale_log2;
       uint32_t pk[kHalf / 2];                   // bf16 pairs of p
+      float ls[4] = {0.f, 0.f, 0.f, 0.f};       // four partial sums of this block's p
       if (cmax >= kHalf - 1) {
 #pragma unroll
         for (int k = 0; k < kHalf; k += 2) {
           const float p0 = ptx::ex2_approx(fmaf(__uint_as_float(v[k]), p.scale_log2, -msc));
           const float p1 = ptx::ex2_approx(fmaf(__uint_as_float(v[k + 1]), p.scale_log2, -msc));
-          l += p0 + p1;
+          ls[(k / 2) & 3] += p0 + p1;
           pk[k / 2] = ptx::pack_bf16x2(p0, p1);
         }
       } else {
@@ -361,22 +366,24 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attention_kernel(const __gri
           float p1 = ptx::ex2_approx(fmaf(__uint_as_float(v[k + 1]), p.scale_log2, -msc));
           if (k > cmax) p0 = 0.f;
           if (k + 1 > cmax) p1 = 0.f;
-          l += p0 + p1;
+          ls[(k / 2) & 3] += p0 + p1;
           pk[k / 2] = ptx::pack_bf16x2(p0, p1);
         }
       }
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&s_empty[b]);
-      // P (and O_c) are free once the tensor core has finished the previous
-      // block's P V: no P V is in flight from here until P_n is signalled.
-      if (!wait_warp(p_empty, (n & 1u) ^ 1u)) {
-        ok = false;
-        break;
-      }
+      l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+      // P_n over the first 32 columns of this half of S_n (read above; the
+      // other half's warp reads and writes only its own columns).
+      ptx::tmem_st_32x32b_x32(lane_addr + kColS + b * kBKV + c0, pk);
       // Rows whose maximum was raised rescale their O_c (after the first
-      // block, when it holds earlier blocks' sums).
+      // block, when it holds earlier blocks' sums) once P_{n-1} V, the last
+      // product on O_c, is done.  P_{n-2} V finished before S_n did and P_n V
+      // waits for this warp, so the wait sees phase n - 1 of p_empty or n.
       if (n > 0 && __any_sync(0xffffffffu, raise)) {
+        if (!wait_warp(p_empty, (n & 1u) ^ 1u)) {
+          ptx::tmem_st_wait();
+          ok = false;
+          break;
+        }
         ptx::tc_fence_after();
         const float f = raise ? corr : 1.f;
 #pragma unroll 1
@@ -388,18 +395,9 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attention_kernel(const __gri
           for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * f);
           ptx::tmem_st_32x32b_x32(o_own + c, o);
         }
-        ptx::tmem_st_wait();
-        ptx::tc_fence_before();                 // the tensor core accumulates on top next
       }
-#pragma unroll
-      for (int cc = 0; cc < 8; ++cc) {
-        const uint32_t addr = prow + ((cc ^ (row & 7)) << 4);
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr),
-                     "r"(pk[4 * cc]), "r"(pk[4 * cc + 1]), "r"(pk[4 * cc + 2]),
-                     "r"(pk[4 * cc + 3])
-                     : "memory");
-      }
-      ptx::fence_proxy_async_smem();            // the tensor core reads P next
+      ptx::tmem_st_wait();
+      ptx::tc_fence_before();                   // the tensor core reads P_n, adds to O_c
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(p_full);
       ++n;
