@@ -51,7 +51,7 @@ namespace {
 constexpr int kD = 128;                          // head dimension
 constexpr int kBQ = 128;                         // query rows per CTA (MMA M)
 constexpr int kBKV = 128;                        // keys per block
-constexpr int kSlots = 4;                        // operand ring: 32 KiB slots (5 measured slower)
+constexpr int kSlots = 4;
 constexpr uint32_t kAtom = 128 * 128;            // 16 KiB: [128 rows][64 bf16]
 constexpr uint32_t kTile = 2 * kAtom;            // 32 KiB: [128][128] bf16
 constexpr uint32_t kTmemCols = 512;
@@ -61,12 +61,12 @@ constexpr uint64_t kDrainNs = 50ull * 1000 * 1000;
 // S = Q K^T: both operands K-major.  O += P V: A K-major, B (V) MN-major.
 constexpr uint32_t kIdescS = ptx::idesc_bf16_f32(kBQ, kBKV, false, false);
 constexpr uint32_t kIdescO = ptx::idesc_bf16_f32(kBQ, kD, false, true);
-// Q, the ring, then the barriers, 4 words and the halves' (m, l) rows.
+// Q, the ring, then the barriers and 4 words.
 constexpr int kBars = 1 + 2 * kSlots + 2 + 1 + 1 + 2;
 constexpr int kHalf = kBKV / 2;                  // key columns of a block per softmax warp
 constexpr int kSoftmax = 8;                      // softmax warps: two per TMEM lane quarter
 constexpr int kThreads = 64 + 32 * kSoftmax;     // warps 0-1 + the softmax warps
-constexpr int kSmem = 1024 + kTile * (1 + kSlots) + kBars * 8 + 16 + 4 * kBQ * 4;
+constexpr int kSmem = 1024 + kTile * (1 + kSlots) + kBars * 8 + 16;
 static_assert(kSmem <= 232448, "shared memory per CTA");
 
 struct AttnParams {
@@ -129,7 +129,9 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attention_kernel(const __gri
   uint64_t* mma_done = o_full + 1;             // kBars barriers in all
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  float* red = reinterpret_cast<float*>(tmem_slot + 4);  // [2][2][128]: the halves' (m, l)
+  // The halves' (m, l) rows, [2][2][128], over Q's tile: written only after
+  // a softmax warp's walk, when every S = Q K^T has completed.
+  float* red = reinterpret_cast<float*>(sQ);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -352,12 +354,24 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attention_kernel(const __gri
       uint32_t pk[kHalf / 2];                   // bf16 pairs of p
       float ls[4] = {0.f, 0.f, 0.f, 0.f};       // four partial sums of this block's p
       if (cmax >= kHalf - 1) {
+        const uint64_t c2 = ptx::f32x2_pack(p.scale_log2, p.scale_log2);
+        const uint64_t n2 = ptx::f32x2_pack(-msc, -msc);
+        uint64_t s2[4] = {0, 0, 0, 0};          // four chains of packed partial sums
 #pragma unroll
         for (int k = 0; k < kHalf; k += 2) {
-          const float p0 = ptx::ex2_approx(fmaf(__uint_as_float(v[k]), p.scale_log2, -msc));
-          const float p1 = ptx::ex2_approx(fmaf(__uint_as_float(v[k + 1]), p.scale_log2, -msc));
-          ls[(k / 2) & 3] += p0 + p1;
+          float y0, y1;
+          const uint64_t x2 = ptx::f32x2_pack(__uint_as_float(v[k]), __uint_as_float(v[k + 1]));
+          ptx::f32x2_unpack(ptx::f32x2_fma(x2, c2, n2), y0, y1);   // s c - m c, two at once
+          const float p0 = ptx::ex2_approx(y0);
+          const float p1 = ptx::ex2_approx(y1);
+          s2[(k / 2) & 3] = ptx::f32x2_add(s2[(k / 2) & 3], ptx::f32x2_pack(p0, p1));
           pk[k / 2] = ptx::pack_bf16x2(p0, p1);
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          float a0, a1;
+          ptx::f32x2_unpack(s2[j], a0, a1);
+          ls[j] = a0 + a1;
         }
       } else {
 #pragma unroll
