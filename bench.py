@@ -462,6 +462,9 @@ def other_ops(fcc, torch, np, synth, dev, stream, dA_rs, dB_rs, pk, only=None):
                                       gate, counts, send, src, 0, 0, o, stream)
 
         t = time_calls(moe, 10, 3, stream)
+        ou = fcc.make_opts(algo=fcc.FCC_ALGO_UNFUSED)
+        tu = time_calls(lambda: moe(None, ou), 5, 2, stream)
+        tr = time_calls(lambda: moe(recv_x, None), 5, 2, stream)
         og = fcc.make_opts(algo=fcc.FCC_ALGO_FUSED)
         tg = time_calls(lambda: moe(None, og), 5, 2, stream)
         tx = time_calls(lambda: moe(recv_x, og), 5, 2, stream)
@@ -485,7 +488,12 @@ def other_ops(fcc, torch, np, synth, dev, stream, dA_rs, dB_rs, pk, only=None):
         combine = {"us": tc_ * 1e3, "GB/s": cbytes / (tc_ * 1e-3) / 1e9,
                    "roofline_frac": cbytes / (tc_ * 1e-3) / 1e9 / hbm,
                    "algorithmic_bytes": cbytes}
-        res = {"fused": leg(t, "route, dispatch copy into workspace, grouped GEMM on the copy"),
+        res = {"fused": leg(t, "route, grouped GEMM whose copy warps stage the rows into "
+                               "workspace while its tensor cores consume the units already "
+                               "staged"),
+               "fused_recv_x": leg(tr, "the same, staging into the caller's recv_x"),
+               "unfused": leg(tu, "route, separate dispatch copy kernel into workspace, then "
+                                  "the grouped GEMM"),
                "combine": combine,
                "layer": leg(tl, "dispatch + expert GEMM + combine (two calls)"),
                "gather_in_gemm": leg(tg, "route, grouped GEMM gathering its rows by TMA gather4"),

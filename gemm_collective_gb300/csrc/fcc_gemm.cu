@@ -30,6 +30,11 @@
 //                 (the gather), the B tile and output from the column's rank.
 //   MODE_PARTIAL  plain per-rank GEMM over a row window (unfused baselines).
 //   MODE_GROUPED  MoE expert GEMM over a tile table built on the device.
+//                 With in-kernel staging, eight more warps (6-13) copy each
+//                 expert's rows from the source tokens into the receive
+//                 buffers (the all-to-all) while the tensor cores work on the
+//                 units already copied; the TMA producer waits, per tile, for
+//                 its unit's row count.
 //
 // Shared memory operand layouts (128-byte swizzle, as written by TMA):
 //   A stage  [128 rows][64 k]   K-major: row m at m*128 B, 8-row groups 1 KiB apart
@@ -53,8 +58,15 @@ constexpr uint64_t kDrainNs = 50ull * 1000 * 1000;  // unwinding limit after an 
 
 // Grouped mode: tile_start[0..E], expert_rows[0..E), expert_base[0..E) copied
 // into shared memory once per CTA, so finding a tile's expert (a binary search)
-// costs no global-memory round trips on the producer's or the MMA warp's path.
-constexpr int kTabInts = 3 * FCC_MAX_EXPERTS + 1;
+// costs no global-memory round trips on the producer's or the MMA warp's path;
+// then the copy warps' chunk prefix [0..E].
+constexpr int kTabInts = 4 * FCC_MAX_EXPERTS + 2;
+constexpr int kCopyRows = 4;  // rows per claimed chunk of the in-kernel staging copy
+
+template <int MODE>
+constexpr int threads_of() {
+  return MODE == MODE_GROUPED ? kGemmThreads + 32 * kCopyWarps : kGemmThreads;
+}
 
 // CG = CTAs per cluster: 1 (one CTA per 128x256 tile), 2 (a CTA pair per
 // 256x256 tile) or 4 (two pairs on the tiles of rows 2m and 2m+1 of one tile
@@ -233,7 +245,7 @@ __device__ __forceinline__ void red_row_chunk(float* row_ptr, int col, int N,
 }
 
 template <int MODE, int CG, class P>
-__global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_constant__ P p) {
+__global__ void __launch_bounds__(threads_of<MODE>(), 1) gemm_kernel(const __grid_constant__ P p) {
   using C = Cfg<CG>;
   constexpr int kStages = C::kStages;
   constexpr int TM = C::kTileM;
@@ -409,6 +421,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         const int bn_cta = narrow(tl) ? C::kBNcta / 2 : C::kBNcta;  // B columns of this CTA
         const int b_col = col_base(tl) + static_cast<int>(cta) * bn_cta;
         const uint32_t stage_bytes = kABytes + static_cast<uint32_t>(bn_cta) * kBK * 2;
+        if constexpr (MODE == MODE_GROUPED) {
+          if (p.stage_copy) {
+            // The unit's rows are written by the copy warps (of any CTA):
+            // wait for its count, then order the TMA reads after it.
+            const int u = tab[tl.expert] / p.tiles_n + tl.mt;
+            if (!W.wait_geq(p.ready + u, tl.rows)) {
+              ok = false;
+              break;
+            }
+            ptx::fence_proxy_async_global();
+          }
+        }
         int r = (tl.rank >= 0) ? tl.rank : 0;
         int kb = 0;
         for (int it = 0; it < k_iters; ++it) {
@@ -521,6 +545,76 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_kernel(const __grid_cons
         else
           ptx::mma_commit(mma_done);
         W.drain(mma_done, 0, kDrainNs);
+      }
+    }
+  } else if (warp >= kGemmThreads / 32) {
+    // ------------------------------------------- staging copy (grouped mode)
+    if constexpr (MODE == MODE_GROUPED) {
+      if (p.stage_copy) {
+        const int* rows_t = tab + p.E + 1;
+        const int* base_t = tab + 2 * p.E + 1;
+        int* cstart = tab + 3 * p.E + 1;  // chunks of experts before e, from e_lo
+        const int cw = warp - kGemmThreads / 32;
+        if (cw == 0 && lane == 0) {
+          int acc = 0;
+          for (int e = p.e_lo; e < p.e_hi; ++e) {
+            cstart[e] = acc;
+            acc += (rows_t[e] + kCopyRows - 1) / kCopyRows;
+          }
+          cstart[p.e_hi] = acc;
+        }
+        ptx::named_barrier_sync(2, 32 * kCopyWarps);
+        const int total = cstart[p.e_hi];
+        const int vec = p.K / 8;  // 16-byte vectors per row
+        constexpr int kV = 16;    // vectors in flight per lane
+        while (true) {
+          int c = 0;
+          if (lane == 0) c = atomicAdd(p.copy_cursor, 1);
+          c = __shfl_sync(0xffffffffu, c, 0);
+          if (c >= total) break;
+          // expert of chunk c: the last e with cstart[e] <= c
+          int lo = p.e_lo, hi = p.e_hi - 1;
+          while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (cstart[mid] <= c)
+              lo = mid;
+            else
+              hi = mid - 1;
+          }
+          const int e = lo;
+          const int r0 = (c - cstart[e]) * kCopyRows;  // first row within the expert
+          const int n = min(kCopyRows, rows_t[e] - r0);
+          const int d = e / p.Eloc;
+          for (int i = 0; i < n; ++i) {
+            const int row = base_t[e] + r0 + i;
+            const int src = __ldcg(p.recv_src[d] + row);
+            const int s = src / p.T;
+            const int t = src - s * p.T;
+            const uint4* sp =
+                reinterpret_cast<const uint4*>(p.src_x[s]) + static_cast<long long>(t) * vec;
+            uint4* dp = reinterpret_cast<uint4*>(p.stage_x[d]) + static_cast<long long>(row) * vec;
+            for (int v0 = 0; v0 < vec; v0 += 32 * kV) {
+              uint4 x[kV];
+#pragma unroll
+              for (int j = 0; j < kV; ++j) {
+                const int v = v0 + 32 * j + lane;
+                if (v < vec) x[j] = __ldcs(sp + v);
+              }
+#pragma unroll
+              for (int j = 0; j < kV; ++j) {
+                const int v = v0 + 32 * j + lane;
+                if (v < vec) dp[v] = x[j];
+              }
+            }
+          }
+          // Publish: every lane's stores, then the unit's count (release).
+          ptx::fence_proxy_async_global();
+          __syncwarp();
+          if (lane == 0) {
+            __threadfence();
+            atomicAdd(p.ready + tab[e] / p.tiles_n + r0 / TM, n);
+          }
+        }
       }
     }
   } else {
@@ -685,7 +779,7 @@ cudaError_t launch_mode(const P& p, int grid, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid, 1, 1);
-  cfg.blockDim = dim3(kGemmThreads, 1, 1);
+  cfg.blockDim = dim3(threads_of<MODE>(), 1, 1);
   cfg.dynamicSmemBytes = Cfg<CG>::kSmem;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];

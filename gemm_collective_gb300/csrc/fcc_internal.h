@@ -14,6 +14,7 @@ namespace fcc {
 constexpr int kBM = 128;       // output tile rows (one TMEM lane per row)
 constexpr int kBK = 64;        // K per pipeline stage (128 bytes of bf16: one swizzle row)
 constexpr int kGemmThreads = 192;  // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
+constexpr int kCopyWarps = 8;      // grouped mode: warps 6-13 stage the expert rows
 constexpr int kGemvTok = 16;   // GEMV: token rows per TMA box (M <= 16)
 
 enum GemmMode : int {
@@ -90,6 +91,19 @@ struct GroupedParams {
   // i of rank d's receive order is its row recv_src[d][i] (= s*T + t).
   const int* recv_src[FCC_MAX_RANKS];  // [cap] per receiving rank
   int gather;
+  // In-kernel staging (stage_copy = 1): the kernel's copy warps write row i of
+  // receiving rank d's order, source row recv_src[d][i] of src_x, to row i of
+  // stage_x[d] (the buffer mapA[d] maps), one (expert, m tile) unit after
+  // another in tile order.  ready[u] counts the rows of unit u written so far
+  // (u = tile_start[e] / tiles_n + m); the TMA producer waits for a unit's
+  // count to reach its rows before loading them.  ready[] and copy_cursor are
+  // zero at launch.
+  const void* src_x[FCC_MAX_RANKS];    // [T, H] per source rank
+  void* stage_x[FCC_MAX_RANKS];        // [cap, H] per receiving rank
+  int T;                               // tokens per source rank
+  int* ready;                          // [units]
+  int* copy_cursor;                    // next chunk of rows to claim
+  int stage_copy;
 };
 
 // cg = 1: one CTA per 128 x 256 tile; cg = 2: a CTA pair (cluster of 2) per

@@ -14,10 +14,15 @@
 //   3. rank_kernel    one CTA per chunk: the stable rank of every assignment
 //                     within its expert (warp match + popc, then a prefix over
 //                     the CTA's warps), i.e. its receive row; writes recv_src.
-//   4. copy_kernel    one warp per token: reads the token row once and writes
-//                     it to each of its receive rows (the all-to-all): into
-//                     the caller's recv_x, or into workspace when the GEMM
-//                     cannot gather.
+//   4. the all-to-all row movement, into the caller's recv_x or into
+//                     workspace.  By default the grouped GEMM's own copy warps
+//                     move each (expert, m tile) unit of rows, in tile order,
+//                     while its tensor cores work on the units already moved,
+//                     and its TMA producer waits for a unit's row count before
+//                     loading it.  With FCC_ALGO_UNFUSED (the unfused
+//                     baseline) copy_kernel does it first, one warp per token
+//                     (each token row read once, written to each of its
+//                     receive rows).
 //   5. the persistent tcgen05 GEMM in grouped mode: tiles over
 //                     (expert, m tile, n tile) from the device tile table.
 //                     With FCC_ALGO_FUSED and the sources one [R*T, H]
@@ -64,6 +69,8 @@ struct MoeArgs {
   int32_t* expert_rows;   // [E], clamped to cap
   int32_t* tile_start;    // [E + 1]
   int32_t* row_of;        // [R*T*topk]: receive row of each assignment, -1 if dropped
+  int32_t* ready;         // in-kernel staging: rows copied per (expert, m tile) unit
+  int32_t* copy_cursor;   // in-kernel staging: next chunk to claim
   int* status;
 };
 
@@ -215,6 +222,14 @@ __global__ void __launch_bounds__(64) finalize_kernel(const MoeArgs a) {
       acc += ((rows[f] + a.tile_m - 1) / a.tile_m) * a.tiles_n;
     }
     a.tile_start[a.E] = acc;
+    counts[0] = acc / a.tiles_n;  // (m tile units in all)
+  }
+  // The in-kernel staging counters start at zero for every call.
+  if (a.ready != nullptr) {
+    __syncthreads();
+    const int units = counts[0];
+    for (int u = e; u < units; u += blockDim.x) a.ready[u] = 0;
+    if (e == 0) *a.copy_cursor = 0;
   }
 }
 
@@ -302,7 +317,7 @@ struct MoePlan {
   int nchunks = 0;
   size_t off_stage = 0;  // staged rows when the caller passes no recv_x ([R][cap][H] bf16)
   size_t off_chunk_counts = 0, off_chunk_off = 0, off_base = 0, off_rows = 0, off_tiles = 0,
-         off_row_of = 0, total = 0;
+         off_row_of = 0, off_ready = 0, off_cursor = 0, total = 0;
 };
 
 size_t up256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
@@ -339,6 +354,12 @@ MoePlan moe_plan(int R, int64_t T, int E, int topk, int64_t H = 0, int64_t cap =
   off += up256(static_cast<size_t>(E + 1) * 4);
   p.off_row_of = off;
   off += up256(static_cast<size_t>(R) * T * topk * 4);
+  // (expert, m tile) units: at most one partial tile per expert beyond
+  // assignments / 128 full ones, and the rows are at most the assignments.
+  p.off_ready = off;
+  off += up256((static_cast<size_t>(R) * T * topk / 128 + E + 1) * 4);
+  p.off_cursor = off;
+  off += 256;
   p.off_stage = off;
   if (stage_in_workspace) off += up256(static_cast<size_t>(R) * cap * H * 2);
   p.total = off;
@@ -416,6 +437,10 @@ fcc_status fcc_moe_dispatch_gemm(int R, const void* const* X, const float* const
   const bool gather = moe_gathers(opts, R, X, T, H);
   const bool stage_ws = !gather && recv_x == nullptr;
   const bool copy = !gather || recv_x != nullptr;
+  // Staged rows are moved by the GEMM's own copy warps unless the unfused
+  // baseline (a separate copy kernel first) is asked for.
+  const bool unfused = opts != nullptr && opts->algo == FCC_ALGO_UNFUSED;
+  const bool copy_in_gemm = !gather && !unfused;
   const MoePlan plan = moe_plan(R, T, E, topk, H, cap, stage_ws);
   void* ws = nullptr;
   int* status = nullptr;
@@ -459,6 +484,8 @@ fcc_status fcc_moe_dispatch_gemm(int R, const void* const* X, const float* const
   a.expert_rows = reinterpret_cast<int32_t*>(base + plan.off_rows);
   a.tile_start = reinterpret_cast<int32_t*>(base + plan.off_tiles);
   a.row_of = reinterpret_cast<int32_t*>(base + plan.off_row_of);
+  a.ready = copy_in_gemm ? reinterpret_cast<int32_t*>(base + plan.off_ready) : nullptr;
+  a.copy_cursor = copy_in_gemm ? reinterpret_cast<int32_t*>(base + plan.off_cursor) : nullptr;
   a.status = status;
 
   GroupedParams g;
@@ -491,6 +518,16 @@ fcc_status fcc_moe_dispatch_gemm(int R, const void* const* X, const float* const
   g.status = status;
   g.timeout_ns = timeout_ns;
   g.gather = gather ? 1 : 0;
+  if (copy_in_gemm) {
+    for (int r = 0; r < R; ++r) {
+      g.src_x[r] = X[r];
+      g.stage_x[r] = a.recv_x[r];
+    }
+    g.T = static_cast<int>(T);
+    g.ready = a.ready;
+    g.copy_cursor = a.copy_cursor;
+    g.stage_copy = 1;
+  }
 
   route_kernel<<<plan.nchunks, 1024, 0, st>>>(a);
   scan_kernel<<<E, 256, 0, st>>>(a);
@@ -507,13 +544,14 @@ fcc_status fcc_moe_dispatch_gemm(int R, const void* const* X, const float* const
         cudaStreamWaitEvent(side, ev[0], 0) != cudaSuccess)
       return FCC_ERR_CUDA;
   }
-  if (copy) copy_kernel<<<std::max(1, sms) * 4, 256, 0, side_copy ? side : st>>>(a);
+  if (copy && !copy_in_gemm)
+    copy_kernel<<<std::max(1, sms) * 4, 256, 0, side_copy ? side : st>>>(a);
   if (cudaGetLastError() != cudaSuccess) return FCC_ERR_CUDA;
   if (side_copy && cudaEventRecord(ev[1], side) != cudaSuccess) return FCC_ERR_CUDA;
   const int grid = std::max(cg, (sms / cg) * cg);
   if (launch_grouped_gemm(g, cg, grid, st) != cudaSuccess) return FCC_ERR_CUDA;
   if (side_copy && cudaStreamWaitEvent(st, ev[1], 0) != cudaSuccess) return FCC_ERR_CUDA;
-  bump_launch_count(copy ? 6 : 5);
+  bump_launch_count((copy && !copy_in_gemm) ? 6 : 5);
   return FCC_OK;
 }
 

@@ -38,6 +38,18 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Orders this thread's generic-proxy global accesses with its later (or
+// earlier) async-proxy ones, e.g. rows written by plain stores and read by TMA.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
                "r"(bytes)
@@ -86,6 +98,22 @@ struct Waiter {
           fail();
           return false;
         }
+      }
+    }
+  }
+
+  // Wait until the global counter *ctr (written by other CTAs with release
+  // semantics) reaches `target`; acquire ordering on success.
+  __device__ __forceinline__ bool wait_geq(const int* ctr, int target) const {
+    if (ld_acquire_gpu(ctr) >= target) return true;
+    const uint64_t t0 = globaltimer();
+    while (true) {
+      __nanosleep(64);
+      if (ld_acquire_gpu(ctr) >= target) return true;
+      if (*abort_flag) return false;
+      if (globaltimer() - t0 > timeout_ns) {
+        fail();
+        return false;
       }
     }
   }

@@ -87,16 +87,21 @@ def _check(X, logits, W, R, T, H, F, E, topk, cap, out, sample=None, seed=0):
 
 
 # (recv_x given, sources one array, algo) of each launch path:
-#   staged         copy into recv_x, GEMM on the copy (sources separate)
-#   workspace      copy into library workspace, GEMM on the copy (the default)
-#   gather         GEMM gathers from the sources, no copy
+#   staged         the GEMM's copy warps stage the rows into recv_x, its
+#                  tensor cores consume them unit by unit (sources separate)
+#   workspace      the same into library workspace (the default)
+#   gather         GEMM gathers from the sources with TMA gather4, no copy
 #   gather_recv_x  GEMM gathers; recv_x written beside it on a side stream
 #   fused_separate FCC_ALGO_FUSED with separate sources: staged as by default
+#   unfused        a separate copy kernel into recv_x, then the GEMM
+#   unfused_workspace  the same into library workspace
 PATHS = {"staged": (True, False, fcc.FCC_ALGO_AUTO),
          "workspace": (False, True, fcc.FCC_ALGO_AUTO),
          "gather": (False, True, fcc.FCC_ALGO_FUSED),
          "gather_recv_x": (True, True, fcc.FCC_ALGO_FUSED),
-         "fused_separate": (False, False, fcc.FCC_ALGO_FUSED)}
+         "fused_separate": (False, False, fcc.FCC_ALGO_FUSED),
+         "unfused": (True, False, fcc.FCC_ALGO_UNFUSED),
+         "unfused_workspace": (False, True, fcc.FCC_ALGO_UNFUSED)}
 
 
 @pytest.mark.parametrize("R,T,H,F,E,topk", [
@@ -150,6 +155,30 @@ def test_moe_repeatable():
                                b["recv_y"][d].view(torch.int16))
 
 
+@pytest.mark.parametrize("pair", [1, 2])
+def test_moe_in_kernel_staging_equals_copy_kernel(pair):
+    """The rows the GEMM's copy warps stage, and the products of those rows,
+    are bit for bit those of the separate copy kernel (same rows, same MMAs);
+    a second call, whose unit counters restart from zero, repeats them."""
+    R, T, H, F, E, topk = 4, 700, 320, 264, 8, 2   # 350 rows an expert: a ragged unit
+    X, logits, W = synth.moe_inputs(R, T, H, E, F, seed=9)
+    cap = R * T * topk
+    o_in = fcc.make_opts(cta_pair=pair, algo=fcc.FCC_ALGO_AUTO)
+    o_sep = fcc.make_opts(cta_pair=pair, algo=fcc.FCC_ALGO_UNFUSED)
+    a = _run(X, logits, W, R, T, H, F, E, topk, cap, opts=o_in)
+    b = _run(X, logits, W, R, T, H, F, E, topk, cap, opts=o_sep)
+    c = _run(X, logits, W, R, T, H, F, E, topk, cap, opts=o_in)
+    _check(X, logits, W, R, T, H, F, E, topk, cap, a)
+    for d in range(R):
+        n = int((a["src"][d] >= 0).sum())
+        for other in (b, c):
+            assert torch.equal(a["src"][d], other["src"][d])
+            assert torch.equal(a["recv_x"][d][:n].view(torch.int16),
+                               other["recv_x"][d][:n].view(torch.int16))
+            assert torch.equal(a["recv_y"][d][:n].view(torch.int16),
+                               other["recv_y"][d][:n].view(torch.int16))
+
+
 def test_moe_capacity_overflow_reported():
     R, T, H, F, E, topk = 2, 256, 64, 64, 4, 2
     X, logits, W = synth.moe_inputs(R, T, H, E, F, seed=7)
@@ -174,10 +203,12 @@ def test_moe_invalid_arguments():
     assert e.value.status == fcc.FCC_ERR_INVALID
 
 
-@pytest.mark.parametrize("path", ["workspace", "gather", "gather_recv_x"])
+@pytest.mark.parametrize("path", ["workspace", "staged", "unfused_workspace", "gather",
+                                  "gather_recv_x"])
 def test_moe_full_workload_sampled(path):
-    """The benchmark's launches: rows staged in library workspace, gathered by
-    the GEMM, and gathered with recv_x written beside the GEMM."""
+    """The benchmark's launches: rows staged in library workspace (or recv_x)
+    by the GEMM's copy warps or by a separate copy kernel, gathered by the
+    GEMM, and gathered with recv_x written beside the GEMM."""
     w = synth.WORKLOADS["moe_r8_t4096_h4096_e64_f1408"]
     X, logits, W = synth.moe_inputs(w.R, w.T, w.H, w.E, w.F, std_x=w.std_a, std_w=w.std_b,
                                     seed=0)
