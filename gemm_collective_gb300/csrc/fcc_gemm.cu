@@ -30,7 +30,7 @@
 //                 (the gather), the B tile and output from the column's rank.
 //   MODE_PARTIAL  plain per-rank GEMM over a row window (unfused baselines).
 //   MODE_GROUPED  MoE expert GEMM over a tile table built on the device.
-//                 With in-kernel staging, eight more warps (6-13) copy each
+//                 With in-kernel staging, two more warps (6-7) copy each
 //                 expert's rows from the source tokens into the receive
 //                 buffers (the all-to-all) while the tensor cores work on the
 //                 units already copied; the TMA producer waits, per tile, for

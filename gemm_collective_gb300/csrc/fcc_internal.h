@@ -14,7 +14,7 @@ namespace fcc {
 constexpr int kBM = 128;       // output tile rows (one TMEM lane per row)
 constexpr int kBK = 64;        // K per pipeline stage (128 bytes of bf16: one swizzle row)
 constexpr int kGemmThreads = 192;  // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
-constexpr int kCopyWarps = 8;      // grouped mode: warps 6-13 stage the expert rows
+constexpr int kCopyWarps = 2;      // grouped mode: warps 6-7 stage the expert rows
 constexpr int kGemvTok = 16;   // GEMV: token rows per TMA box (M <= 16)
 
 enum GemmMode : int {
