@@ -189,13 +189,16 @@ fcc_status fcc_ag_gemm(int R, const void *const *X_shard, const void *const *B,
  *   GEMM:     recv_y[d][row] = X[s][t] @ W[e]  ([F] per row, dtype out_dtype).
  * X[s]: [T,H] bf16; logits[s]: [T,E] f32, finite; W[e]: [H,F] bf16 (E
  * pointers); recv_x: NULL, or per rank [cap,H] bf16 to receive the
- * dispatched rows.  By default the rows are first staged (in recv_x, or in
- * workspace when it is NULL) and the expert GEMM reads the staged copy.  With
+ * dispatched rows.  By default (AUTO) the expert GEMM kernel moves the rows
+ * itself, into recv_x or into workspace when it is NULL, one (expert,
+ * m tile) unit after another, and its tensor cores read each unit as soon as
+ * it is moved.  FCC_ALGO_UNFUSED (the unfused baseline) moves all rows with a
+ * separate copy kernel before the GEMM.  With
  * opts->algo == FCC_ALGO_FUSED and the sources one [R*T,H] array (X[s] =
  * X[0] + s*T*H elements), the GEMM instead reads each row straight from its
  * source token (TMA gather) and a non-NULL recv_x is filled beside it (slower
  * on sm_103a: the gather is bound by its TMA request rate); FUSED with other
- * sources stages as the default does.  recv_y[d]: [cap,F];
+ * sources moves the rows as the default does.  recv_y[d]: [cap,F];
  * recv_src[d]: [cap] int32; topk_idx[s]: [T,topk] int32; topk_gate[s]:
  * [T,topk] f32; expert_counts: [E] int32 device; send_counts: [R*R] int32
  * device.  Rows of a receive buffer past the received count are left
