@@ -226,8 +226,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemv_ar_kernel(const __grid_c
       if (*bcast) {
         // Last of the group: sum the splits' partials in split order; each
         // thread handles 4 consecutive columns (one 16-byte load per partial)
-        // of up to 8 tokens at a time, two splits per step, so 16 loads are in
-        // flight instead of one: this sum is the kernel's serial tail.
+        // of up to 8 tokens at a time, three splits per step, so 24 loads are
+        // in flight instead of one: this sum is the kernel's serial tail.
         __threadfence();
         const int c = ep_tid * 4;
         if (c < ncols) {
@@ -245,22 +245,24 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemv_ar_kernel(const __grid_c
 #pragma unroll
             for (int i = 0; i < kTokStep; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
             int sp = 0;
-            for (; sp + 2 <= p.splits; sp += 2) {
-              float4 x0[kTokStep], x1[kTokStep];
+            for (; sp + 3 <= p.splits; sp += 3) {
+              float4 x0[kTokStep], x1[kTokStep], x2[kTokStep];
 #pragma unroll
               for (int i = 0; i < kTokStep; ++i)
                 if (i < nt) {
                   x0[i] = part(sp, t0 + i);
                   x1[i] = part(sp + 1, t0 + i);
+                  x2[i] = part(sp + 2, t0 + i);
                 }
 #pragma unroll
               for (int i = 0; i < kTokStep; ++i)
-                if (i < nt) {
+                if (i < nt) {  // (split order: sp, sp + 1, sp + 2)
                   add(acc[i], x0[i]);
                   add(acc[i], x1[i]);
+                  add(acc[i], x2[i]);
                 }
             }
-            if (sp < p.splits) {
+            for (; sp < p.splits; ++sp) {
 #pragma unroll
               for (int i = 0; i < kTokStep; ++i)
                 if (i < nt) add(acc[i], part(sp, t0 + i));
