@@ -477,17 +477,39 @@ def other_ops(fcc, torch, np, synth, dev, stream, dA_rs, dB_rs, pk, only=None):
         # combine: the return all-to-all + gate-weighted top-2 sum of the GEMM's rows
         y = [torch.empty((T, F), dtype=torch.bfloat16, device=dev) for _ in range(R)]
 
-        def comb():
+        def comb(s=None):
             fcc.fcc_moe_combine(R, recv_y, cap, T, F, E, topk, idx, gate, src, counts, y,
-                                0, 0, None, stream)
+                                0, 0, None, stream if s is None else s)
 
         moe()
         tc_ = time_calls(comb, 20, 3, stream)
+        # The same calls replayed from a CUDA graph: the device time alone (a
+        # call's host side, argument marshalling and launches, outlasts its
+        # GPU work, so back-to-back calls leave the GPU idle between them).
+        graph = {}
+        try:
+            side = torch.cuda.Stream(device=dev)
+            with torch.cuda.stream(side):
+                comb(side)  # outside the capture: any device set-up happens here
+                torch.cuda.synchronize()
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=side):
+                    for _ in range(20):
+                        comb(torch.cuda.current_stream(dev))
+            tg_ = time_calls(g.replay, 5, 2, stream) / 20
+            graph = {"us": tg_ * 1e3}
+            del g
+        except Exception as e:  # capture is optional information
+            graph = {"error": str(e)[:200]}
         tl = time_calls(lambda: (moe(), comb()), 10, 3, stream)
         cbytes = R * T * topk * F * 2 + R * T * F * 2  # expert rows read once, y written once
         combine = {"us": tc_ * 1e3, "GB/s": cbytes / (tc_ * 1e-3) / 1e9,
                    "roofline_frac": cbytes / (tc_ * 1e-3) / 1e9 / hbm,
                    "algorithmic_bytes": cbytes}
+        if "us" in graph:
+            graph["GB/s"] = cbytes / (graph["us"] * 1e-6) / 1e9
+            graph["roofline_frac"] = graph["GB/s"] / hbm
+        combine["graph_replay"] = graph
         res = {"fused": leg(t, "route, grouped GEMM whose copy warps stage the rows into "
                                "workspace while its tensor cores consume the units already "
                                "staged"),
