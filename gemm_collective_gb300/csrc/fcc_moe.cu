@@ -112,27 +112,10 @@ __global__ void __launch_bounds__(1024) route_kernel(const MoeArgs a) {
   if (threadIdx.x < FCC_MAX_EXPERTS) hist[threadIdx.x] = 0;
   __syncthreads();
   const float neg_inf = __int_as_float(0xff800000);
-  // The warp's tokens are t0 + warp + 32 j: all their logits are loaded
-  // first, so the loads are in flight together rather than one per token.
-  constexpr int kTokPerWarp = kChunkTok / 32;
-  float l0v[kTokPerWarp], l1v[kTokPerWarp];
-#pragma unroll
-  for (int j = 0; j < kTokPerWarp; ++j) {
-    const int t = t0 + warp + 32 * j;
-    l0v[j] = neg_inf;
-    l1v[j] = neg_inf;
-    if (t < t1) {
-      const float* lg = a.logits[s] + static_cast<long long>(t) * a.E;
-      if (lane < a.E) l0v[j] = lg[lane];
-      if (lane + 32 < a.E) l1v[j] = lg[lane + 32];
-    }
-  }
-#pragma unroll
-  for (int j = 0; j < kTokPerWarp; ++j) {
-    const int t = t0 + warp + 32 * j;
-    if (t >= t1) break;  // (uniform across the warp)
-    const float l0 = l0v[j];
-    const float l1 = l1v[j];
+  for (int t = t0 + warp; t < t1; t += 32) {
+    const float* lg = a.logits[s] + static_cast<long long>(t) * a.E;
+    const float l0 = lane < a.E ? lg[lane] : neg_inf;
+    const float l1 = lane + 32 < a.E ? lg[lane + 32] : neg_inf;
     // candidates this lane holds; experts past E carry index E (never chosen)
     Cand c0{l0, lane < a.E ? lane : a.E};
     Cand c1{l1, lane + 32 < a.E ? lane + 32 : a.E};
