@@ -103,6 +103,12 @@ def test_workspace_sizes(fcc):
     o = fcc.make_opts(algo=fcc.FCC_ALGO_CE)
     assert fcc.fcc_workspace_size(fcc.FCC_OP_GEMM_RS, 2, 256, 256, 128, o) >= 2 * 2 * 256 * 256 * 4
     assert fcc.fcc_workspace_size(fcc.FCC_OP_AG_GEMM, 8, 8192, 3584, 8192, None) == 0
+    # MoE: room to stage every receive row (recv_x NULL), the receive row of
+    # every assignment, and one row counter per (expert, 128-row tile) unit
+    R, T, H, F, E, topk, cap = 8, 4096, 4096, 1408, 64, 2, 16384
+    need = R * cap * H * 2 + R * T * topk * 4 + (R * T * topk // 128 + E) * 4
+    assert fcc.fcc_moe_workspace_size(R, T, H, F, E, topk, cap) >= need
+    assert fcc.fcc_moe_workspace_size(0, T, H, F, E, topk, cap) == 0
 
 
 def test_strategy_selector(fcc):
