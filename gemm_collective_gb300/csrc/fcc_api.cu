@@ -147,15 +147,14 @@ bool deterministic_of(const fcc_opts* o) { return o == nullptr || o->determinist
 
 // Tensor-core tile shape (CTAs per cluster): a CTA pair per 256-row tile
 // unless the rows are few (one CTA per 128-row tile), or the caller's shape.
-// Two pairs sharing multicast B tiles (4) only when asked for: on the 8-rank
-// 8192 x 8192 x 3584 reduce-scatter they ran 2.51 ms against 2.10-2.28 ms for
-// single pairs (burst) and 2.41 against 2.37 ms (400 calls), as each stage
-// then waits for both pairs' MMAs.  gemm_params falls back from 4 to 2 where
-// the mode or tile count rules it out.
 int choose_cg(const fcc_opts* o, int64_t rows) {
-  if (o != nullptr && (o->cta_pair == 1 || o->cta_pair == 2 || o->cta_pair == 4))
-    return o->cta_pair;
+  if (o != nullptr && (o->cta_pair == 1 || o->cta_pair == 2)) return o->cta_pair;
   return rows > kBM ? 2 : 1;
+}
+
+// opts->cta_pair: 0 (automatic), 1 or 2.
+bool tile_shape_ok(const fcc_opts* o) {
+  return o == nullptr || o->cta_pair == 0 || o->cta_pair == 1 || o->cta_pair == 2;
 }
 
 int grid_for(const DeviceState* d, const fcc_opts* o, int64_t units) {
@@ -240,23 +239,13 @@ fcc_status gemm_params(GemmParams& p, DeviceState* d, int mode, int R, const voi
   const int tn = static_cast<int>(cdiv(N, kGemmBN));
   const int64_t rows = (mode == MODE_AG) ? Ms : (mode == MODE_PARTIAL ? m_end - m_begin : M);
   p.cg = choose_cg(o, rows);
-  if (p.cg == 4) {
-    // Two pairs per cluster take the m tiles 2i, 2i+1 of one tile column: the
-    // modes without tickets, with an even number of 256-row tiles.
-    const int64_t tm2 = cdiv(rows, 2 * kBM);
-    const bool even = mode == MODE_AG ? (R * tm2) % 2 == 0 : tm2 % 2 == 0;
-    if (!(mode == MODE_RS || mode == MODE_AR || mode == MODE_AG || mode == MODE_PARTIAL) ||
-        !even)
-      p.cg = 2;
-  }
-  const int64_t tm = static_cast<int64_t>(kBM) * std::min(p.cg, 2);
-  const int sup = p.cg == 4 ? 2 : 1;  // m tiles per work unit
+  const int64_t tm = static_cast<int64_t>(kBM) * p.cg;
   switch (mode) {
     case MODE_RS:
     case MODE_AR:
       p.tiles_m = static_cast<int>(cdiv(M, tm));
       p.tiles_n = tn;
-      p.num_tiles = p.tiles_m / sup * p.tiles_n;
+      p.num_tiles = p.tiles_m * p.tiles_n;
       p.k_iters = R * p.kb_per_rank;
       break;
     case MODE_RS_PUSH:
@@ -269,13 +258,13 @@ fcc_status gemm_params(GemmParams& p, DeviceState* d, int mode, int R, const voi
     case MODE_PARTIAL:
       p.tiles_m = static_cast<int>(cdiv(m_end - m_begin, tm));
       p.tiles_n = tn;
-      p.num_tiles = R * (p.tiles_m / sup) * p.tiles_n;
+      p.num_tiles = R * p.tiles_m * p.tiles_n;
       p.k_iters = p.kb_per_rank;
       break;
     case MODE_AG:
       p.tiles_m = R * static_cast<int>(cdiv(Ms, tm));
       p.tiles_n = R * tn;
-      p.num_tiles = p.tiles_m / sup * p.tiles_n;
+      p.num_tiles = p.tiles_m * p.tiles_n;
       p.k_iters = p.kb_per_rank;
       p.group_m = 8;
       break;
@@ -294,7 +283,6 @@ fcc_status run_gemm(const GemmParams& p0, int mode, DeviceState* d, const fcc_op
   // would hold at most half a round of tiles, each of those tiles runs as two
   // 128-column halves on two slots, so the round takes half a tile's time.
   // A half keeps the tile's whole K loop: the results are unchanged.
-  // (clusters of 4 must fit in a GPC: at most the device's co-resident count)
   const int slots = std::max(1, std::min(grid_for(d, o, INT64_MAX) / p.cg,
                                          gemm_max_clusters(p.cg)));
   const int rem = p.num_tiles % slots;
@@ -456,6 +444,7 @@ fcc_status rank_sum_call(int R, const void* const* A, const void* const* B, void
   if (algo != FCC_ALGO_FUSED && algo != FCC_ALGO_UNFUSED && algo != FCC_ALGO_INTERDECOM &&
       algo != FCC_ALGO_CE)
     return FCC_ERR_INVALID;
+  if (!tile_shape_ok(o)) return FCC_ERR_INVALID;
   DeviceState* d = nullptr;
   if ((s = device_state(&d)) != FCC_OK) return s;
   const int out_f32 = out_dtype == FCC_F32 ? 1 : 0;
@@ -637,6 +626,7 @@ fcc_status fcc_ag_gemm(int R, const void* const* X_shard, const void* const* B, 
   if (algo == FCC_ALGO_INTERDECOM) return FCC_ERR_UNSUPPORTED;
   if (algo != FCC_ALGO_FUSED && algo != FCC_ALGO_UNFUSED && algo != FCC_ALGO_CE)
     return FCC_ERR_INVALID;
+  if (!tile_shape_ok(opts)) return FCC_ERR_INVALID;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   DeviceState* d = nullptr;
   if ((s = device_state(&d)) != FCC_OK) return s;

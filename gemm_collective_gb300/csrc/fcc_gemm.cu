@@ -12,9 +12,9 @@
 //           4-stage ring of 48 KiB (A 128x64 + B 64x256).
 //   CG = 2  a CTA pair (cluster of 2 on neighbouring SMs) per 256 x 256 tile,
 //           tcgen05.mma.cta_group::2 (M = 256) issued by the pair's leader;
-//           each CTA loads its 128 rows of A and its 128 columns of B (no
-//           multicast), so each SM keeps a 6-stage ring of 32 KiB and reads
-//           half the B bytes per MMA.  Each CTA's TMEM holds its 128 rows.
+//           each CTA loads its 128 rows of A and its 128 columns of B into its
+//           own shared memory, so each SM keeps a 7-stage ring of 32 KiB and
+//           reads half the B bytes per MMA.  Each CTA's TMEM holds its 128 rows.
 //
 // The collective step per mode (the fused operators of the mKernel article's
 // kernel list and of the SC24 paper's abstract, where each workgroup ships
@@ -68,12 +68,12 @@ constexpr int threads_of() {
   return MODE == MODE_GROUPED ? kGemmThreads + 32 * kCopyWarps : kGemmThreads;
 }
 
-// CG = CTAs per cluster: 1 (one CTA per 128x256 tile), 2 (a CTA pair per
-// 256x256 tile) or 4 (two pairs on the tiles of rows 2m and 2m+1 of one tile
-// column, each B box loaded once and multicast to both pairs).
+// CG = CTAs per cluster: 1 (one CTA per 128x256 tile) or 2 (a CTA pair per
+// 256x256 tile).  Every TMA load goes to the issuing CTA's own shared memory.
 template <int CG>
 struct Cfg {
-  static constexpr int kPairCtas = CG >= 2 ? 2 : 1;         // CTAs of one MMA
+  static_assert(CG == 1 || CG == 2, "one CTA or a CTA pair per tile");
+  static constexpr int kPairCtas = CG;                      // CTAs of one MMA
   static constexpr int kTileM = kBM * kPairCtas;            // rows of one (pair) tile
   static constexpr int kBNcta = kBN / kPairCtas;            // B columns this CTA holds
   static constexpr int kStages = CG >= 2 ? 7 : 4;
@@ -128,10 +128,8 @@ __device__ __forceinline__ int k_iters_of(const P& p) {
   }
 }
 
-// SUP: the index t counts super-tiles of two m tiles (rows 2m, 2m+1), of which
-// pair pj of the cluster takes m tile 2m + pj (tiles_m is then even).
-template <int MODE, int TM, bool SUP = false, class P>
-__device__ __forceinline__ Tile tile_of(const P& p, int t, const int* tab, int pj = 0) {
+template <int MODE, int TM, class P>
+__device__ __forceinline__ Tile tile_of(const P& p, int t, const int* tab) {
   Tile tl;
   tl.rank = -1;
   tl.shard = 0;
@@ -174,21 +172,11 @@ __device__ __forceinline__ Tile tile_of(const P& p, int t, const int* tab, int p
     tl.row0 = base[e] + tl.mt * TM;
     tl.rows = min(TM, rows_e - tl.mt * TM);
   } else if constexpr (MODE == MODE_RS || MODE == MODE_AR) {
-    if constexpr (SUP) {
-      raster(t, p.tiles_m / 2, p.tiles_n, max(1, p.group_m / 2), tl.mt, tl.nt);
-      tl.mt = 2 * tl.mt + pj;
-    } else {
-      raster(t, p.tiles_m, p.tiles_n, p.group_m, tl.mt, tl.nt);
-    }
+    raster(t, p.tiles_m, p.tiles_n, p.group_m, tl.mt, tl.nt);
   } else if constexpr (MODE == MODE_AG) {
     // tiles_m = R * (tiles per shard), tiles_n = R * (tiles per rank)
     int gm, gn;
-    if constexpr (SUP) {
-      raster(t, p.tiles_m / 2, p.tiles_n, max(1, p.group_m / 2), gm, gn);
-      gm = 2 * gm + pj;
-    } else {
-      raster(t, p.tiles_m, p.tiles_n, p.group_m, gm, gn);
-    }
+    raster(t, p.tiles_m, p.tiles_n, p.group_m, gm, gn);
     const int mt_per_shard = p.tiles_m / p.R;
     const int nt_per_rank = p.tiles_n / p.R;
     tl.shard = gm / mt_per_shard;
@@ -196,12 +184,9 @@ __device__ __forceinline__ Tile tile_of(const P& p, int t, const int* tab, int p
     tl.rank = gn / nt_per_rank;
     tl.nt = gn - tl.rank * nt_per_rank;
   } else {
-    const int tm = SUP ? p.tiles_m / 2 : p.tiles_m;
-    const int per_rank = tm * p.tiles_n;
+    const int per_rank = p.tiles_m * p.tiles_n;
     tl.rank = t / per_rank;
-    raster(t - tl.rank * per_rank, tm, p.tiles_n, SUP ? max(1, p.group_m / 2) : p.group_m, tl.mt,
-           tl.nt);
-    if constexpr (SUP) tl.mt = 2 * tl.mt + pj;
+    raster(t - tl.rank * per_rank, p.tiles_m, p.tiles_n, p.group_m, tl.mt, tl.nt);
   }
   return tl;
 }
@@ -267,13 +252,10 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) gemm_kernel(const __gri
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  constexpr bool kPair = CG >= 2;                      // tcgen05 cta_group::2 MMAs
-  constexpr bool SUP = CG == 4;                        // two pairs share the B tiles
-  const uint32_t crank = kPair ? ptx::cluster_ctarank() : 0u;
-  const uint32_t cta = crank & 1u;   // rank of this CTA in its pair (0 = leader, issues the MMAs)
-  const uint32_t lead = crank & ~1u;                   // cluster rank of the pair's leader
-  const int pj = static_cast<int>(crank >> 1);         // pair within the cluster (CG = 4)
-  // Work units (tiles, or super-tiles for CG = 4) go round-robin over clusters.
+  constexpr bool kPair = CG == 2;                      // tcgen05 cta_group::2 MMAs
+  const uint32_t cta = kPair ? ptx::cluster_ctarank() : 0u;  // 0 = the pair's leader (issues the MMAs)
+  constexpr uint32_t lead = 0;                          // cluster rank of the pair's leader
+  // Work units (tiles) go round-robin over clusters.
   const int pair = blockIdx.x / CG;
   const int npairs = gridDim.x / CG;
 
@@ -285,7 +267,7 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) gemm_kernel(const __gri
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(&full[s], 1);
-      ptx::mbar_init(&empty[s], SUP ? 2 : 1);  // CG = 4: both pairs' MMAs release a stage
+      ptx::mbar_init(&empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(&tfull[b], 1);
@@ -347,7 +329,7 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) gemm_kernel(const __gri
       bool ok = true;
       const CUtensorMap* ma = &p.mapA[0];
       for (int t = pair; t < num_tiles && ok; t += npairs) {
-        const Tile tl = tile_of<MODE, TM, SUP>(p, t, tab, pj);
+        const Tile tl = tile_of<MODE, TM>(p, t, tab);
         const int bn_cta = narrow(tl) ? C::kBNcta / 2 : C::kBNcta;
         const int b_col = col_base(tl) + static_cast<int>(cta) * bn_cta;
         const uint32_t stage_bytes = kABytes + static_cast<uint32_t>(bn_cta) * kBK * 2;
@@ -408,7 +390,7 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) gemm_kernel(const __gri
       uint32_t issued = 0, last_parity = 0;
       bool ok = true;
       for (int t = pair; t < num_tiles && ok; t += npairs) {
-        const Tile tl = tile_of<MODE, TM, SUP>(p, t, tab, pj);
+        const Tile tl = tile_of<MODE, TM>(p, t, tab);
         int a_row;
         if constexpr (MODE == MODE_GROUPED) {
           a_row = tl.row0;
@@ -450,18 +432,8 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) gemm_kernel(const __gri
             const uint32_t bar = ptx::mapa(ptx::smem_addr(&full[stage]), lead);
             if (cta == 0) ptx::mbar_arrive_expect_tx(&full[stage], 2 * stage_bytes);
             ptx::tma_load_2d_pair(a_dst, ma, bar, kb * kBK, a_row);
-            for (int i = 0; i < bn_cta / 64; ++i) {
-              if constexpr (SUP) {
-                // Box i is loaded by pair i % 2 for both pairs: it lands in this
-                // rank-in-pair's CTA of each pair, counted on each pair's leader.
-                if ((i & 1) == pj)
-                  ptx::tma_load_2d_pair_mc(b_dst + i * kBBoxBytes, mb, bar, b_col + 64 * i,
-                                           kb * kBK,
-                                           static_cast<uint16_t>((1u << cta) | (4u << cta)));
-              } else {
-                ptx::tma_load_2d_pair(b_dst + i * kBBoxBytes, mb, bar, b_col + 64 * i, kb * kBK);
-              }
-            }
+            for (int i = 0; i < bn_cta / 64; ++i)
+              ptx::tma_load_2d_pair(b_dst + i * kBBoxBytes, mb, bar, b_col + 64 * i, kb * kBK);
           } else {
             ptx::mbar_arrive_expect_tx(&full[stage], stage_bytes);
             ptx::tma_load_2d(a_dst, ma, &full[stage], kb * kBK, a_row);
@@ -496,7 +468,7 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) gemm_kernel(const __gri
       uint32_t acc = 0, acc_phase = 0;
       bool any = false, ok = true;
       for (int t = pair; t < num_tiles && ok; t += npairs) {
-        const uint32_t idesc = narrow(tile_of<MODE, TM, SUP>(p, t, tab, pj)) ? C::kIdescNarrow : C::kIdesc;
+        const uint32_t idesc = narrow(tile_of<MODE, TM>(p, t, tab)) ? C::kIdescNarrow : C::kIdesc;
         if (!W.wait(&tempty[acc], acc_phase ^ 1u)) break;
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * kBN;
@@ -520,9 +492,8 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) gemm_kernel(const __gri
               ptx::mma_f16(d_tmem, ad, bd, idesc, (it > 0 || kk > 0) ? 1u : 0u);
           }
           if constexpr (kPair)
-            // Frees the stage in both CTAs of the pair (CG = 4: of both pairs,
-            // whose B boxes share the stage).
-            ptx::mma_commit_pair_multicast(&empty[stage], SUP ? 0xF : 0x3);
+            // Frees the stage in both CTAs of the pair.
+            ptx::mma_commit_pair_arrive_ctas(&empty[stage], 0x3);
           else
             ptx::mma_commit(&empty[stage]);
           any = true;
@@ -533,7 +504,7 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) gemm_kernel(const __gri
         }
         if (!ok) break;
         if constexpr (kPair)
-          ptx::mma_commit_pair_multicast(&tfull[acc], static_cast<uint16_t>(0x3u << lead));
+          ptx::mma_commit_pair_arrive_ctas(&tfull[acc], 0x3);
         else
           ptx::mma_commit(&tfull[acc]);
         acc ^= 1u;
@@ -624,7 +595,7 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) gemm_kernel(const __gri
     const uint32_t tempty_leader0 = kPair ? ptx::mapa(ptx::smem_addr(&tempty[0]), lead) : 0u;
     uint32_t acc = 0, acc_phase = 0;
     for (int t = pair; t < num_tiles; t += npairs) {
-      const Tile tl = tile_of<MODE, TM, SUP>(p, t, tab, pj);
+      const Tile tl = tile_of<MODE, TM>(p, t, tab);
       const bool failed = !W.wait(&tfull[acc], acc_phase);
       if constexpr (MODE == MODE_RS_PUSH || MODE == MODE_AR_PUSH) {
         // The four epilogue warps meet at named barriers below: stop together.
@@ -809,7 +780,7 @@ cudaError_t launch_cg(const GemmParams& p, int mode, int grid, cudaStream_t st) 
 
 }  // namespace
 
-int gemm_smem_bytes(int cg) { return cg >= 2 ? Cfg<2>::kSmem : Cfg<1>::kSmem; }
+int gemm_smem_bytes(int cg) { return cg == 2 ? Cfg<2>::kSmem : Cfg<1>::kSmem; }
 
 namespace {
 template <int CG>
@@ -843,13 +814,12 @@ int query_max_clusters() {
 
 int gemm_max_clusters(int cg) {
   constexpr int kDevs = 16;
-  static int cache[kDevs][5] = {};
+  static int cache[kDevs][3] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kDevs) dev = 0;
-  const int k = cg == 4 ? 4 : (cg == 2 ? 2 : 1);
+  const int k = cg == 2 ? 2 : 1;
   if (cache[dev][k] == 0) {
-    int n = k == 4 ? query_max_clusters<4>() : (k == 2 ? query_max_clusters<2>()
-                                                       : query_max_clusters<1>());
+    int n = k == 2 ? query_max_clusters<2>() : query_max_clusters<1>();
     // (no answer: one cluster per group of k SMs)
     if (n <= 0) {
       int sms = 0;
@@ -862,16 +832,6 @@ int gemm_max_clusters(int cg) {
 }
 
 cudaError_t launch_gemm(const GemmParams& p, int mode, int cg, int grid, cudaStream_t st) {
-  if (cg == 4) {
-    // Two pairs per cluster: the modes without tickets.
-    switch (mode) {
-      case MODE_RS: return launch_mode<MODE_RS, 4, GemmParams>(p, grid, st);
-      case MODE_AR: return launch_mode<MODE_AR, 4, GemmParams>(p, grid, st);
-      case MODE_PARTIAL: return launch_mode<MODE_PARTIAL, 4, GemmParams>(p, grid, st);
-      case MODE_AG: return launch_mode<MODE_AG, 4, GemmParams>(p, grid, st);
-      default: return cudaErrorInvalidValue;
-    }
-  }
   if (cg == 2) return launch_cg<2>(p, mode, grid, st);
   if (cg == 1) return launch_cg<1>(p, mode, grid, st);
   return cudaErrorInvalidValue;

@@ -333,7 +333,7 @@ fcc_status gemv_internal_tickets(int** out) {
   return FCC_OK;
 }
 
-// Grid shape: groups = ceil(N / 1024) column groups, `splits` CTAs per group
+// Grid shape: groups = ceil(N / 512) column groups, `splits` CTAs per group
 // (about one CTA per SM in total, at most one per 64-row block of K').
 void gemv_shape(int64_t N, int R, int64_t K, int sms, int max_ctas, int* groups, int* splits) {
   const int g = static_cast<int>((N + kGroupCols - 1) / kGroupCols);
@@ -418,6 +418,10 @@ extern "C" fcc_status fcc_gemv_ar_static(int R, const void* const* A, const void
   for (int r = 0; r < R; ++r)
     if (out[r] == nullptr || (reinterpret_cast<uintptr_t>(out[r]) & 15u) != 0)
       return FCC_ERR_INVALID;
+  // The same status as fcc_gemv_ar for a value outside the enum; the valid
+  // unfused forms need allocated partials, which this entry point has not.
+  if (opts != nullptr && (opts->algo < FCC_ALGO_AUTO || opts->algo > FCC_ALGO_CE))
+    return FCC_ERR_INVALID;
   if (opts != nullptr && opts->algo != FCC_ALGO_AUTO && opts->algo != FCC_ALGO_FUSED)
     return FCC_ERR_UNSUPPORTED;
 
@@ -429,9 +433,10 @@ extern "C" fcc_status fcc_gemv_ar_static(int R, const void* const* A, const void
 
   int groups = 0, splits = 0;
   gemv_shape(N, R, K, sms, opts != nullptr ? opts->max_ctas : 0, &groups, &splits);
-  // Size limit of the static array: one ticket per column group, and one
-  // partial (M x 512 f32 = M x 2 KiB) per CTA; fewer CTAs per group are used
-  // when the default number does not fit.
+  // Size limit of the static array: one ticket per column group (4 KiB), and
+  // one partial (M x 512 f32 = M x 2 KiB) per CTA and group in the remaining
+  // 4 MiB - 4 KiB = 2046 x 2 KiB, i.e. ceil(N / 512) * M <= 2046; fewer CTAs
+  // per group are used when the default number does not fit.
   const size_t room = kStaticScratchBytes - kStaticTicketBytes;
   const size_t per_split = gemv_partial_bytes(groups, 1, M);
   if (static_cast<size_t>(groups) * 4 > kStaticTicketBytes || per_split > room)

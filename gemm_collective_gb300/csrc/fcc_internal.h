@@ -46,7 +46,7 @@ struct GemmParams {
   unsigned long long timeout_ns;
   float* acc_ws;        // push mode with bf16 output: f32 accumulation rows (M x N)
   int* tickets;         // push mode with bf16 output: per (tile, CTA of the pair) counters
-  int cg;               // host side: CTAs per cluster (1, 2 or 4)
+  int cg;               // host side: CTAs per cluster (1 or 2)
 };
 
 struct GemvParams {
@@ -107,8 +107,7 @@ struct GroupedParams {
 };
 
 // cg = 1: one CTA per 128 x 256 tile; cg = 2: a CTA pair (cluster of 2) per
-// 256 x 256 tile; cg = 4: two pairs (cluster of 4) on the m tiles 2i, 2i+1 of
-// one tile column, sharing its B tiles.  grid is in CTAs (a multiple of cg).
+// 256 x 256 tile.  grid is in CTAs (a multiple of cg).
 cudaError_t launch_gemm(const GemmParams& p, int mode, int cg, int grid, cudaStream_t st);
 cudaError_t launch_grouped_gemm(const GroupedParams& p, int cg, int grid, cudaStream_t st);
 int gemm_smem_bytes(int cg);

@@ -397,6 +397,8 @@ fcc_status check_moe(int R, const void* const* X, const float* const* logits,
   if (in != FCC_BF16) return FCC_ERR_UNSUPPORTED;
   if (out_dtype != FCC_BF16 && out_dtype != FCC_F32)
     return out_dtype == FCC_F16 ? FCC_ERR_UNSUPPORTED : FCC_ERR_INVALID;
+  if (opts != nullptr && opts->cta_pair != 0 && opts->cta_pair != 1 && opts->cta_pair != 2)
+    return FCC_ERR_INVALID;
   if (opts != nullptr && opts->algo != FCC_ALGO_AUTO && opts->algo != FCC_ALGO_FUSED &&
       opts->algo != FCC_ALGO_UNFUSED)
     return FCC_ERR_UNSUPPORTED;

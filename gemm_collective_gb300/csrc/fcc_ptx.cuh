@@ -1,4 +1,5 @@
-// fcc_ptx.cuh -- inline-PTX wrappers for sm_103a: mbarrier, TMA (no multicast),
+// fcc_ptx.cuh -- inline-PTX wrappers for sm_103a: mbarrier, TMA loads (each
+// into the issuing CTA's own shared memory; no multicast load exists here),
 // tcgen05 (TMEM alloc, MMA, commit, load) and bounded waits.
 //
 // Every spin in this library goes through fcc::ptx::Waiter, which gives up
@@ -407,19 +408,6 @@ __device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* m
       : "memory");
 }
 
-// Same, multicast: the box lands at dst's offset in every CTA of `mask`, and
-// each destination's bytes are counted on the barrier at bar's offset in the
-// leader of that destination's pair.
-__device__ __forceinline__ void tma_load_2d_pair_mc(void* dst, const CUtensorMap* map,
-                                                    uint32_t bar_cluster_addr, int32_t x,
-                                                    int32_t y, uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_addr(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster_addr), "r"(x), "r"(y), "h"(mask)
-      : "memory");
-}
-
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t* dst, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                    smem_addr(dst)),
@@ -447,8 +435,9 @@ __device__ __forceinline__ void mma_f16_pair(uint32_t d_tmem, uint64_t a_desc, u
 }
 
 // Arrive on the mbarrier at the same shared-memory offset in every CTA of
-// `cta_mask` once all previously issued tcgen05 ops of this thread finish.
-__device__ __forceinline__ void mma_commit_pair_multicast(uint64_t* bar, uint16_t cta_mask) {
+// `cta_mask` once all previously issued tcgen05 ops of this thread finish
+// (an arrive signal to the pair's barriers; it moves no data).
+__device__ __forceinline__ void mma_commit_pair_arrive_ctas(uint64_t* bar, uint16_t cta_mask) {
   asm volatile(
       "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
       " [%0], %1;" ::"r"(smem_addr(bar)),

@@ -87,14 +87,11 @@ typedef struct {
   void *workspace;         /* device scratch, or NULL for the internal pool */
   size_t workspace_bytes;
   /* Tensor-core tile shape of the GEMMs: 0 = automatic (a CTA pair when the
-   * rows exceed 128, else 1), 1 = one CTA per
-   * 128 x 256 tile, 2 = a CTA pair (cluster of 2, tcgen05 cta_group::2) per
-   * 256 x 256 tile, 4 = two CTA pairs (cluster of 4) on vertically adjacent
-   * 256 x 256 tiles, each B tile loaded once by TMA multicast for both.  4
-   * applies to the reduce-scatter, all-reduce and all-gather GEMMs in
-   * deterministic mode with an even number of 256-row tiles, and falls back
-   * to 2 elsewhere (measured slower than 2 on the 8-rank reduce-scatter:
-   * each stage waits for both pairs); the MoE expert GEMM takes 1 or 2. */
+   * rows exceed 128, else 1), 1 = one CTA per 128 x 256 tile, 2 = a CTA pair
+   * (cluster of 2, tcgen05 cta_group::2) per 256 x 256 tile.  Any other value
+   * is FCC_ERR_INVALID.  Every TMA load lands in the issuing CTA's own shared
+   * memory (no multicast loads), so the library may run in processes that
+   * drive several GPUs. */
   int cta_pair;
 } fcc_opts;
 
@@ -147,12 +144,15 @@ fcc_status fcc_gemv_ar(int R, const void *const *A, const void *const *B, void *
  * and arrival tickets) is a 4 MiB static device array inside the library,
  * held on every GPU that loads the library until the process exits.
  *  - Limit: each CTA keeps an M x 512 f32 partial (M x 2 KiB) per group of
- *    512 columns, so ceil(N/512) * M <= 2047 (N <= 130,560 for 8 tokens,
+ *    512 columns, in the array's 4 MiB less 4 KiB of tickets, so
+ *    ceil(N/512) * M <= 2046 (N <= 130,560 for 8 tokens,
  *    65,024 for 16); within that the call uses as many CTAs per column group
  *    as fit in the array (possibly fewer than fcc_gemv_ar uses, which changes
  *    only the f32 summation order).  Beyond it the call returns
  *    FCC_ERR_WORKSPACE and launches nothing.  opts->workspace is ignored;
- *    algo must be AUTO or FUSED.
+ *    algo must be AUTO or FUSED (UNFUSED, INTERDECOM and CE give
+ *    FCC_ERR_UNSUPPORTED, values outside the enum FCC_ERR_INVALID, as in
+ *    fcc_gemv_ar).
  *  - The first call on a device looks up the array's device address and the
  *    SM count (cudaGetSymbolAddress, cudaDeviceGetAttribute) with that device
  *    current; make that first call before any stream capture.

@@ -76,6 +76,24 @@ def test_invalid_arguments_rejected_without_cuda(fcc):
     # AG: M % R
     assert fcc.raw_status("fcc_ag_gemm", 2, two, two, two, None, 255, 256, 128, 0, 0, None,
                           None) == fcc.FCC_ERR_INVALID
+    # tile shapes other than automatic, one CTA or a CTA pair
+    for pair in (3, 4, -1):
+        o = ctypes.byref(fcc.make_opts(cta_pair=pair))
+        assert fcc.raw_status("fcc_gemm_rs", 2, two, two, two, 256, 256, 128, 0, 0, o,
+                              None) == fcc.FCC_ERR_INVALID, pair
+        assert fcc.raw_status("fcc_gemm_ar", 2, two, two, two, 256, 256, 128, 0, 0, o,
+                              None) == fcc.FCC_ERR_INVALID, pair
+        assert fcc.raw_status("fcc_ag_gemm", 2, two, two, two, None, 256, 256, 128, 0, 0, o,
+                              None) == fcc.FCC_ERR_INVALID, pair
+    # the no-allocation GEMV: an algorithm outside the enum is invalid, the
+    # valid unfused forms are unsupported there
+    for algo, want in [(99, fcc.FCC_ERR_INVALID), (-1, fcc.FCC_ERR_INVALID),
+                       (fcc.FCC_ALGO_UNFUSED, fcc.FCC_ERR_UNSUPPORTED),
+                       (fcc.FCC_ALGO_INTERDECOM, fcc.FCC_ERR_UNSUPPORTED),
+                       (fcc.FCC_ALGO_CE, fcc.FCC_ERR_UNSUPPORTED)]:
+        o = ctypes.byref(fcc.make_opts(algo=algo))
+        assert fcc.raw_status("fcc_gemv_ar_static", 2, two, two, two, 8, 256, 128, 0, 2, o,
+                              None) == want, algo
     assert fcc.fcc_launch_count() == 0
 
 
