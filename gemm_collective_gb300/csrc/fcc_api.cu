@@ -36,6 +36,8 @@ struct DeviceState {
   int* status = nullptr;
   void* pool = nullptr;
   size_t pool_bytes = 0;
+  void* host = nullptr;  // pinned host memory for values a call reads back
+  size_t host_bytes = 0;
   cudaStream_t side[kSideStreams] = {};
   cudaEvent_t ev[kMaxChunks + kSideStreams + 2] = {};
 };
@@ -329,10 +331,10 @@ RankSumPlan rank_sum_plan(int R, int64_t M, int64_t N, bool out_f32, const fcc_o
   return pl;
 }
 
-// Rows per InterDecom chunk, a multiple of the tile height.
-int64_t chunk_rows(int64_t M, int chunks) {
+// Rows per InterDecom chunk, a multiple of `align` (a tile height).
+int64_t chunk_rows(int64_t M, int chunks, int64_t align = kBM) {
   int64_t rows = cdiv(M, chunks);
-  return cdiv(rows, kBM) * kBM;
+  return cdiv(rows, align) * align;
 }
 
 // Default model constants for the chunk count when the caller gives none:
@@ -346,6 +348,15 @@ int model_chunks(int R, int64_t M, int64_t N, int64_t K, int out_bytes) {
   const double X = (static_cast<double>(R) * M * N * 4 + static_cast<double>(M) * N * out_bytes) /
                    kModelBytesPerS;
   const int maxc = static_cast<int>(std::min<int64_t>(kMaxChunks, cdiv(M, kBM)));
+  return fcc_interdecom_chunks(G, X, kModelAlphaS, maxc);
+}
+
+// AllGather + GEMM: G = the R per-rank GEMMs over all M gathered rows, X = the
+// gather (M x K bf16 read once and written once); chunks of 256-row tiles.
+int ag_model_chunks(int R, int64_t M, int64_t N, int64_t K) {
+  const double G = 2.0 * R * static_cast<double>(M) * N * K / kModelTcFlops;
+  const double X = 2.0 * static_cast<double>(M) * K * 2 / kModelBytesPerS;
+  const int maxc = static_cast<int>(std::min<int64_t>(kMaxChunks, cdiv(M, 2 * kBM)));
   return fcc_interdecom_chunks(G, X, kModelAlphaS, maxc);
 }
 
@@ -623,8 +634,8 @@ fcc_status fcc_ag_gemm(int R, const void* const* X_shard, const void* const* B, 
     for (int r = 0; r < R; ++r)
       if (gathered[r] != nullptr && !aligned16(gathered[r])) return FCC_ERR_INVALID;
   const fcc_algo algo = algo_of(opts);
-  if (algo == FCC_ALGO_INTERDECOM) return FCC_ERR_UNSUPPORTED;
-  if (algo != FCC_ALGO_FUSED && algo != FCC_ALGO_UNFUSED && algo != FCC_ALGO_CE)
+  if (algo != FCC_ALGO_FUSED && algo != FCC_ALGO_UNFUSED && algo != FCC_ALGO_INTERDECOM &&
+      algo != FCC_ALGO_CE)
     return FCC_ERR_INVALID;
   if (!tile_shape_ok(opts)) return FCC_ERR_INVALID;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
@@ -650,8 +661,8 @@ fcc_status fcc_ag_gemm(int R, const void* const* X_shard, const void* const* B, 
     return FCC_OK;
   }
 
-  // Unfused: gather X (SM copy kernel or copy engines), then one GEMM per rank.
-  const void* src = nullptr;
+  // Unfused: gather X (SM copy kernel or copy engines), then one GEMM per rank;
+  // InterDecom: the same in row chunks, gather and GEMM pipelined.
   void* ws = nullptr;
   const bool have_g = gathered != nullptr && gathered[0] != nullptr;
   const size_t xbytes = static_cast<size_t>(M) * K * 2;
@@ -659,22 +670,51 @@ fcc_status fcc_ag_gemm(int R, const void* const* X_shard, const void* const* B, 
     if ((s = get_workspace(d, opts, xbytes, &ws)) != FCC_OK) return s;
   }
   void* g0 = have_g ? gathered[0] : ws;
-  if (algo == FCC_ALGO_CE) {
-    for (int sh = 0; sh < R; ++sh)
-      if (cudaMemcpyAsync(static_cast<char*>(g0) + static_cast<size_t>(sh) * Ms * K * 2, X_shard[sh],
-                          static_cast<size_t>(Ms) * K * 2, cudaMemcpyDeviceToDevice, st) != cudaSuccess)
-        return FCC_ERR_CUDA;
-  } else if (cuda_fail(launch_gather_rows(X_shard, R, Ms, K, g0, st)) != FCC_OK) {
-    return FCC_ERR_CUDA;
-  }
-  src = g0;
   const void* Ag[FCC_MAX_RANKS];
-  for (int r = 0; r < R; ++r) Ag[r] = src;
-  GemmParams p;
-  if ((s = gemm_params(p, d, MODE_PARTIAL, R, Ag, B, out, R, M, N, K, M, 0, M, out_f32, opts)) !=
-      FCC_OK)
-    return s;
-  if ((s = run_gemm(p, MODE_PARTIAL, d, opts, st)) != FCC_OK) return s;
+  for (int r = 0; r < R; ++r) Ag[r] = g0;
+  if (algo == FCC_ALGO_INTERDECOM) {
+    // Row chunks of the gathered X: every chunk's gather is queued on a side
+    // stream at once, and the GEMM of chunk i (rows [m0, m1) of every rank's
+    // output) runs on the caller's stream after chunk i's gather, so chunk
+    // i+1's gather overlaps chunk i's GEMM.  Chunks are whole 256-row tiles.
+    int chunks = (opts != nullptr && opts->chunks > 0) ? opts->chunks
+                                                       : ag_model_chunks(R, M, N, K);
+    chunks = std::max(1, std::min(chunks, kMaxChunks));
+    const int64_t rows = chunk_rows(M, chunks, 2 * kBM);
+    cudaStream_t side = d->side[0];
+    cudaEvent_t fork = d->ev[kMaxChunks];
+    if (cudaEventRecord(fork, st) != cudaSuccess || cudaStreamWaitEvent(side, fork, 0) != cudaSuccess)
+      return FCC_ERR_CUDA;
+    int i = 0;
+    for (int64_t m0 = 0; m0 < M; m0 += rows, ++i) {
+      const int64_t m1 = std::min(M, m0 + rows);
+      if (cuda_fail(launch_gather_rows_range(X_shard, R, Ms, K, g0, m0, m1, side)) != FCC_OK)
+        return FCC_ERR_CUDA;
+      if (cudaEventRecord(d->ev[i], side) != cudaSuccess ||
+          cudaStreamWaitEvent(st, d->ev[i], 0) != cudaSuccess)
+        return FCC_ERR_CUDA;
+      GemmParams p;
+      if ((s = gemm_params(p, d, MODE_PARTIAL, R, Ag, B, out, R, M, N, K, M, m0, m1, out_f32,
+                           opts)) != FCC_OK)
+        return s;
+      if ((s = run_gemm(p, MODE_PARTIAL, d, opts, st)) != FCC_OK) return s;
+    }
+  } else {
+    if (algo == FCC_ALGO_CE) {
+      for (int sh = 0; sh < R; ++sh)
+        if (cudaMemcpyAsync(static_cast<char*>(g0) + static_cast<size_t>(sh) * Ms * K * 2,
+                            X_shard[sh], static_cast<size_t>(Ms) * K * 2,
+                            cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+          return FCC_ERR_CUDA;
+    } else if (cuda_fail(launch_gather_rows(X_shard, R, Ms, K, g0, st)) != FCC_OK) {
+      return FCC_ERR_CUDA;
+    }
+    GemmParams p;
+    if ((s = gemm_params(p, d, MODE_PARTIAL, R, Ag, B, out, R, M, N, K, M, 0, M, out_f32,
+                         opts)) != FCC_OK)
+      return s;
+    if ((s = run_gemm(p, MODE_PARTIAL, d, opts, st)) != FCC_OK) return s;
+  }
   if (have_g) {
     for (int r = 1; r < R; ++r)
       if (gathered[r] != nullptr &&
@@ -863,6 +903,32 @@ fcc_status internal_prepare(const fcc_opts* o, size_t ws_bytes, void** ws, int**
 fcc_status internal_make_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols,
                              uint32_t box_rows) {
   return make_map(m, ptr, rows, cols, box_rows);
+}
+
+fcc_status internal_streams_events(cudaStream_t* side, int nside, cudaEvent_t* ev, int nev) {
+  DeviceState* d = nullptr;
+  fcc_status s = device_state(&d);
+  if (s != FCC_OK) return s;
+  if (nside > kSideStreams || nev > kMaxChunks + kSideStreams + 2) return FCC_ERR_INVALID;
+  for (int i = 0; i < nside; ++i) side[i] = d->side[i];
+  for (int i = 0; i < nev; ++i) ev[i] = d->ev[i];
+  return FCC_OK;
+}
+
+fcc_status internal_host_buffer(size_t bytes, void** out) {
+  DeviceState* d = nullptr;
+  fcc_status s = device_state(&d);
+  if (s != FCC_OK) return s;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (d->host_bytes < bytes) {
+    if (d->host != nullptr && cudaFreeHost(d->host) != cudaSuccess) return FCC_ERR_CUDA;
+    d->host = nullptr;
+    d->host_bytes = 0;
+    if (cudaHostAlloc(&d->host, bytes, cudaHostAllocDefault) != cudaSuccess) return FCC_ERR_CUDA;
+    d->host_bytes = bytes;
+  }
+  *out = d->host;
+  return FCC_OK;
 }
 
 fcc_status internal_side_stream(cudaStream_t* side, cudaEvent_t* ev, int n) {

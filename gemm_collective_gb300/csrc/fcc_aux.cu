@@ -62,15 +62,18 @@ struct GatherArgs {
   void* dst;
   int R;
   long long Ms, K;
+  long long row_begin, row_end;  // rows of the gathered matrix to write
 };
 
-// dst = [X_0; X_1; ...] with 16-byte copies (K % 8 == 0).
+// dst rows [row_begin, row_end) of [X_0; X_1; ...] with 16-byte copies (K % 8 == 0).
 __global__ void __launch_bounds__(256) gather_rows_kernel(const GatherArgs a) {
   const long long vec_per_row = a.K / 8;
   const long long per_shard = a.Ms * vec_per_row;
-  const long long total = per_shard * a.R;
-  for (long long g = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; g < total;
-       g += static_cast<long long>(gridDim.x) * blockDim.x) {
+  const long long first = a.row_begin * vec_per_row;
+  const long long total = (a.row_end - a.row_begin) * vec_per_row;
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long g = first + i;
     const int s = static_cast<int>(g / per_shard);
     const long long off = g - s * per_shard;
     const uint4 v = __ldcs(reinterpret_cast<const uint4*>(a.X[s]) + off);
@@ -128,13 +131,21 @@ cudaError_t launch_reduce_shards(const float* const* P, int R, void* const* out,
 
 cudaError_t launch_gather_rows(const void* const* X, int R, int64_t Ms, int64_t K, void* dst,
                                cudaStream_t st) {
+  return launch_gather_rows_range(X, R, Ms, K, dst, 0, static_cast<int64_t>(R) * Ms, st);
+}
+
+cudaError_t launch_gather_rows_range(const void* const* X, int R, int64_t Ms, int64_t K,
+                                     void* dst, int64_t row_begin, int64_t row_end,
+                                     cudaStream_t st) {
   GatherArgs a{};
   for (int r = 0; r < R; ++r) a.X[r] = X[r];
   a.dst = dst;
   a.R = R;
   a.Ms = Ms;
   a.K = K;
-  const long long work = static_cast<long long>(R) * Ms * (K / 8);
+  a.row_begin = row_begin;
+  a.row_end = row_end;
+  const long long work = (row_end - row_begin) * (K / 8);
   if (work <= 0) return cudaSuccess;
   const int sms = device_sm_count();
   long long blocks = (work + 255) / 256;

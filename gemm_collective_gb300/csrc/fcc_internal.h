@@ -129,9 +129,13 @@ cudaError_t launch_reduce_shards(const float* const* P, int R, void* const* out,
                                  int per_shard, int64_t M, int64_t N, int64_t Ms,
                                  int64_t row_begin, int64_t row_end, int out_f32,
                                  cudaStream_t st);
-// out bf16 = convert(acc f32), rows [row_begin, row_end) of an [M,N] matrix into shards.
+// dst = [X_0; ...; X_{R-1}] (each X_s is [Ms, K] bf16), all rows or rows
+// [row_begin, row_end) of the gathered [R*Ms, K] matrix.
 cudaError_t launch_gather_rows(const void* const* X, int R, int64_t Ms, int64_t K, void* dst,
                                cudaStream_t st);
+cudaError_t launch_gather_rows_range(const void* const* X, int R, int64_t Ms, int64_t K,
+                                     void* dst, int64_t row_begin, int64_t row_end,
+                                     cudaStream_t st);
 cudaError_t launch_wait_probe(int* status, unsigned long long timeout_ns, cudaStream_t st);
 
 // Shared host helpers (fcc_api.cu).
@@ -162,6 +166,12 @@ fcc_status internal_make_map(CUtensorMap* m, const void* ptr, int64_t rows, int6
                              uint32_t box_rows);
 // A side stream and n <= 8 events of the current device (after internal_prepare).
 fcc_status internal_side_stream(cudaStream_t* side, cudaEvent_t* ev, int n);
+// The device's side streams 0..nside-1 (nside <= 4) and events 0..nev-1
+// (nev <= 70), shared with the InterDecom paths of the other operators.
+fcc_status internal_streams_events(cudaStream_t* side, int nside, cudaEvent_t* ev, int nev);
+// A pinned host buffer of at least `bytes` for the current device (grown with
+// cudaHostAlloc; valid until the next call that asks for more).
+fcc_status internal_host_buffer(size_t bytes, void** out);
 // The algorithm FCC_ALGO_AUTO runs (the strategy selector, fcc_api.cu).
 fcc_algo choose_algo(fcc_op op, int R, int64_t M, int64_t N, int64_t K, int sms, int max_ctas);
 }  // namespace fcc

@@ -71,6 +71,15 @@ struct MoeArgs {
   int32_t* row_of;        // [R*T*topk]: receive row of each assignment, -1 if dropped
   int32_t* ready;         // in-kernel staging: rows copied per (expert, m tile) unit
   int32_t* copy_cursor;   // in-kernel staging: next chunk to claim
+  // Copy-engine dispatch: per source rank s a send buffer of its kept rows in
+  // (expert, token, slot) order; srcoff[s][e] = assignments to e from the
+  // sources before s (srcoff[R][e] = all of e's); send_base[s][e] = the first
+  // send row of (s, e); plan[s][e] = {send row, receive row, rows} of the
+  // (s, e) run, which is contiguous on both sides.
+  void* send[FCC_MAX_RANKS];
+  int32_t* ce_srcoff;     // [R + 1][E]
+  int32_t* ce_send_base;  // [R][E]
+  int32_t* ce_plan;       // [R][E][3]
   int* status;
 };
 
@@ -312,12 +321,140 @@ __global__ void __launch_bounds__(256) copy_kernel(const MoeArgs a) {
   }
 }
 
+// Rows of experts [e_lo, e_hi) of their receiving ranks' orders, one warp per
+// receive row: row i of expert e on rank d = e / Eloc is source row
+// recv_src[d][i] (= s*T + t).  The InterDecom baseline moves one expert range
+// per chunk with it, on a side stream ahead of that range's GEMM.
+__global__ void __launch_bounds__(256) copy_expert_rows_kernel(const MoeArgs a, int e_lo,
+                                                               int e_hi) {
+  __shared__ int pre[FCC_MAX_EXPERTS + 1];  // rows of the range's experts before e
+  if (threadIdx.x == 0) {
+    int acc = 0;
+    for (int e = e_lo; e < e_hi; ++e) {
+      pre[e - e_lo] = acc;
+      acc += a.expert_rows[e];
+    }
+    pre[e_hi - e_lo] = acc;
+  }
+  __syncthreads();
+  const int total = pre[e_hi - e_lo];
+  const int lane = threadIdx.x & 31;
+  const int vec = a.H / 8;  // uint4 per row
+  constexpr int kV = 8;     // vectors in flight per lane
+  const int warps = gridDim.x * (blockDim.x >> 5);
+  for (int g = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); g < total; g += warps) {
+    int lo = 0, hi = e_hi - e_lo - 1;  // the last expert whose first row is <= g
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (pre[mid] <= g)
+        lo = mid;
+      else
+        hi = mid - 1;
+    }
+    const int e = e_lo + lo;
+    const int d = e / a.Eloc;
+    const int row = a.expert_base[e] + (g - pre[lo]);
+    const int src = a.recv_src[d][row];
+    const int s = src / a.T;
+    const int t = src - s * a.T;
+    const uint4* sp = reinterpret_cast<const uint4*>(a.X[s]) + static_cast<long long>(t) * vec;
+    uint4* dp = reinterpret_cast<uint4*>(a.recv_x[d]) + static_cast<long long>(row) * vec;
+    for (int v0 = 0; v0 < vec; v0 += 32 * kV) {
+      uint4 x[kV];
+#pragma unroll
+      for (int j = 0; j < kV; ++j) {
+        const int v = v0 + 32 * j + lane;
+        if (v < vec) x[j] = __ldcg(sp + v);
+      }
+#pragma unroll
+      for (int j = 0; j < kV; ++j) {
+        const int v = v0 + 32 * j + lane;
+        if (v < vec) dp[v] = x[j];
+      }
+    }
+  }
+}
+
+// Copy-engine dispatch, step 1 (one CTA of 64 threads, after finalize_kernel):
+// the (source rank, expert) runs.  Source s's assignments to expert e are, in
+// both orders, one contiguous run: rows srcoff[s][e] .. srcoff[s + 1][e] of
+// e's receive rows (receive order is (expert, s, t, slot)), and, packed on
+// the sending side in (expert, t, slot) order, rows send_base[s][e] on of
+// s's send buffer.  Only the kept rows (within the receive capacity) are
+// packed and moved; they are a prefix of each run.
+__global__ void __launch_bounds__(64) ce_plan_kernel(const MoeArgs a) {
+  __shared__ int off[FCC_MAX_RANKS + 1][FCC_MAX_EXPERTS];
+  __shared__ int kept[FCC_MAX_RANKS][FCC_MAX_EXPERTS];
+  const int e = threadIdx.x;
+  if (e < a.E) {
+    for (int s = 0; s <= a.R; ++s) {
+      off[s][e] = s < a.R ? a.chunk_off[static_cast<long long>(s) * a.chunks_per_rank * a.E + e]
+                          : a.expert_counts[e];
+      a.ce_srcoff[s * a.E + e] = off[s][e];
+    }
+    for (int s = 0; s < a.R; ++s)
+      kept[s][e] = max(0, min(off[s + 1][e] - off[s][e], a.expert_rows[e] - off[s][e]));
+  }
+  __syncthreads();
+  if (e < a.R) {
+    int acc = 0;
+    for (int f = 0; f < a.E; ++f) {
+      a.ce_send_base[e * a.E + f] = acc;
+      int32_t* pl = a.ce_plan + 3 * (e * a.E + f);
+      pl[0] = acc;                            // first send row
+      pl[1] = a.expert_base[f] + off[e][f];   // first receive row on rank f / Eloc
+      pl[2] = kept[e][f];                     // rows
+      acc += kept[e][f];
+    }
+  }
+}
+
+// Copy-engine dispatch, step 2 (after rank_kernel): each source rank packs its
+// kept rows into its own send buffer (a copy inside the rank; nothing crosses
+// ranks here), one warp per token, the token's row read once.
+__global__ void __launch_bounds__(256) ce_pack_kernel(const MoeArgs a) {
+  const int lane = threadIdx.x & 31;
+  const long long warps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
+  const long long ntok = static_cast<long long>(a.R) * a.T;
+  const int vec = a.H / 8;
+  for (long long g = blockIdx.x * static_cast<long long>(blockDim.x >> 5) + (threadIdx.x >> 5);
+       g < ntok; g += warps) {
+    const int s = static_cast<int>(g / a.T);
+    const int t = static_cast<int>(g - static_cast<long long>(s) * a.T);
+    int srow = -1;
+    if (lane < a.topk) {
+      const int row = a.row_of[g * a.topk + lane];
+      if (row >= 0) {
+        const int e = a.idx[s][static_cast<long long>(t) * a.topk + lane];
+        // rank of the assignment within its (s, e) run
+        const int k = row - a.expert_base[e] - a.ce_srcoff[s * a.E + e];
+        srow = a.ce_send_base[s * a.E + e] + k;
+      }
+    }
+    const int r0 = __shfl_sync(0xffffffffu, srow, 0);
+    const int r1 = __shfl_sync(0xffffffffu, srow, 1);
+    const uint4* src = reinterpret_cast<const uint4*>(a.X[s]) + static_cast<long long>(t) * vec;
+    uint4* dst0 = r0 >= 0 ? reinterpret_cast<uint4*>(a.send[s]) + static_cast<long long>(r0) * vec
+                          : nullptr;
+    uint4* dst1 = (a.topk > 1 && r1 >= 0)
+                      ? reinterpret_cast<uint4*>(a.send[s]) + static_cast<long long>(r1) * vec
+                      : nullptr;
+    for (int v = lane; v < vec; v += 32) {
+      const uint4 x = __ldcs(src + v);
+      if (dst0 != nullptr) dst0[v] = x;
+      if (dst1 != nullptr) dst1[v] = x;
+    }
+  }
+}
+
 struct MoePlan {
   int chunks_per_rank = 0;
   int nchunks = 0;
   size_t off_stage = 0;  // staged rows when the caller passes no recv_x ([R][cap][H] bf16)
   size_t off_chunk_counts = 0, off_chunk_off = 0, off_base = 0, off_rows = 0, off_tiles = 0,
          off_row_of = 0, off_ready = 0, off_cursor = 0, total = 0;
+  // copy-engine dispatch: tables and the send buffers ([R][T*topk][H] bf16)
+  size_t off_ce_srcoff = 0, off_ce_send_base = 0, off_ce_plan = 0, off_send = 0;
 };
 
 size_t up256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
@@ -337,7 +474,7 @@ bool moe_gathers(const fcc_opts* o, int R, const void* const* X, int64_t T, int6
 }
 
 MoePlan moe_plan(int R, int64_t T, int E, int topk, int64_t H = 0, int64_t cap = 0,
-                 bool stage_in_workspace = false) {
+                 bool stage_in_workspace = false, bool ce = false) {
   MoePlan p;
   p.chunks_per_rank = static_cast<int>((T + kChunkTok - 1) / kChunkTok);
   p.nchunks = R * p.chunks_per_rank;
@@ -360,10 +497,29 @@ MoePlan moe_plan(int R, int64_t T, int E, int topk, int64_t H = 0, int64_t cap =
   off += up256((static_cast<size_t>(R) * T * topk / 128 + E + 1) * 4);
   p.off_cursor = off;
   off += 256;
+  p.off_ce_srcoff = off;
+  off += up256(static_cast<size_t>(R + 1) * E * 4);
+  p.off_ce_send_base = off;
+  off += up256(static_cast<size_t>(R) * E * 4);
+  p.off_ce_plan = off;
+  off += up256(static_cast<size_t>(R) * E * 3 * 4);
   p.off_stage = off;
   if (stage_in_workspace) off += up256(static_cast<size_t>(R) * cap * H * 2);
+  p.off_send = off;
+  if (ce) off += up256(static_cast<size_t>(R) * T * topk * H * 2);
   p.total = off;
   return p;
+}
+
+// Default model constants for the InterDecom chunk count (as for the GEMMs):
+// sustained tensor rate, copy bandwidth and per-chunk overhead on a GB300.
+// G = the expert GEMMs, X = the row copy (each receive row read and written);
+// chunks are expert ranges, at most E.
+int moe_model_chunks(int R, int64_t T, int64_t H, int64_t F, int E, int topk) {
+  const double rows = static_cast<double>(R) * T * topk;
+  const double G = 2.0 * rows * H * F / 1.6e15;
+  const double X = 2.0 * rows * H * 2 / 6.0e12;
+  return fcc_interdecom_chunks(G, X, 6.0e-6, E);
 }
 
 bool al(const void* p, uintptr_t a) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -399,9 +555,8 @@ fcc_status check_moe(int R, const void* const* X, const float* const* logits,
     return out_dtype == FCC_F16 ? FCC_ERR_UNSUPPORTED : FCC_ERR_INVALID;
   if (opts != nullptr && opts->cta_pair != 0 && opts->cta_pair != 1 && opts->cta_pair != 2)
     return FCC_ERR_INVALID;
-  if (opts != nullptr && opts->algo != FCC_ALGO_AUTO && opts->algo != FCC_ALGO_FUSED &&
-      opts->algo != FCC_ALGO_UNFUSED)
-    return FCC_ERR_UNSUPPORTED;
+  if (opts != nullptr && (opts->algo < FCC_ALGO_AUTO || opts->algo > FCC_ALGO_CE))
+    return FCC_ERR_INVALID;
   return FCC_OK;
 }
 
@@ -414,15 +569,14 @@ extern "C" {
 
 size_t fcc_moe_workspace_size(int R, int64_t T, int64_t H, int64_t F, int E, int topk,
                               int64_t cap, const fcc_opts* opts) {
-  (void)H;
   (void)F;
-  (void)cap;
-  (void)opts;
   if (R < 1 || R > FCC_MAX_RANKS || T < 1 || E < 1 || E > FCC_MAX_EXPERTS || topk < 1)
     return 0;
   // Upper bound: includes room to stage the rows (recv_x NULL, and the
-  // sources not one array or FCC_ALGO_UNFUSED asked for).
-  return moe_plan(R, T, E, topk, H, cap, true).total;
+  // sources not one array or another algorithm than the gather asked for),
+  // and with FCC_ALGO_CE the send buffers.
+  const bool ce = opts != nullptr && opts->algo == FCC_ALGO_CE;
+  return moe_plan(R, T, E, topk, H, cap, true, ce).total;
 }
 
 fcc_status fcc_moe_dispatch_gemm(int R, const void* const* X, const float* const* logits,
@@ -436,14 +590,19 @@ fcc_status fcc_moe_dispatch_gemm(int R, const void* const* X, const float* const
   fcc_status s = check_moe(R, X, logits, W, T, H, F, E, topk, recv_x, recv_y, cap, topk_idx,
                            topk_gate, expert_counts, send_counts, recv_src, in, out_dtype, opts);
   if (s != FCC_OK) return s;
+  const fcc_algo algo = opts != nullptr ? opts->algo : FCC_ALGO_AUTO;
   const bool gather = moe_gathers(opts, R, X, T, H);
+  const bool interdecom = algo == FCC_ALGO_INTERDECOM;
+  const bool ce = algo == FCC_ALGO_CE;
+  const bool unfused = algo == FCC_ALGO_UNFUSED;
   const bool stage_ws = !gather && recv_x == nullptr;
-  const bool copy = !gather || recv_x != nullptr;
-  // Staged rows are moved by the GEMM's own copy warps unless the unfused
-  // baseline (a separate copy kernel first) is asked for.
-  const bool unfused = opts != nullptr && opts->algo == FCC_ALGO_UNFUSED;
-  const bool copy_in_gemm = !gather && !unfused;
-  const MoePlan plan = moe_plan(R, T, E, topk, H, cap, stage_ws);
+  // AUTO / FUSED: the rows are moved by the GEMM's own copy warps (or, for
+  // FUSED with one source array, gathered by its TMA).  The baselines move
+  // them first: UNFUSED with one copy kernel, INTERDECOM with one copy kernel
+  // per expert range on a side stream ahead of that range's GEMM, CE with the
+  // copy engines.
+  const bool copy_in_gemm = !gather && !unfused && !interdecom && !ce;
+  const MoePlan plan = moe_plan(R, T, E, topk, H, cap, stage_ws, ce);
   void* ws = nullptr;
   int* status = nullptr;
   int sms = 0;
@@ -466,6 +625,7 @@ fcc_status fcc_moe_dispatch_gemm(int R, const void* const* X, const float* const
                                         static_cast<size_t>(r) * cap * H * 2
                                   : nullptr);
     a.recv_src[r] = recv_src[r];
+    if (ce) a.send[r] = base + plan.off_send + static_cast<size_t>(r) * T * topk * H * 2;
   }
   a.R = R;
   a.E = E;
@@ -488,6 +648,9 @@ fcc_status fcc_moe_dispatch_gemm(int R, const void* const* X, const float* const
   a.row_of = reinterpret_cast<int32_t*>(base + plan.off_row_of);
   a.ready = copy_in_gemm ? reinterpret_cast<int32_t*>(base + plan.off_ready) : nullptr;
   a.copy_cursor = copy_in_gemm ? reinterpret_cast<int32_t*>(base + plan.off_cursor) : nullptr;
+  a.ce_srcoff = reinterpret_cast<int32_t*>(base + plan.off_ce_srcoff);
+  a.ce_send_base = reinterpret_cast<int32_t*>(base + plan.off_ce_send_base);
+  a.ce_plan = reinterpret_cast<int32_t*>(base + plan.off_ce_plan);
   a.status = status;
 
   GroupedParams g;
@@ -535,25 +698,172 @@ fcc_status fcc_moe_dispatch_gemm(int R, const void* const* X, const float* const
   scan_kernel<<<E, 256, 0, st>>>(a);
   finalize_kernel<<<1, 64, 0, st>>>(a);
   rank_kernel<<<plan.nchunks, 256, 0, st>>>(a);
-  // With the gather the copy (only for a requested recv_x) runs beside the
-  // GEMM on a side stream: both only read what the dispatch kernels wrote.
-  const bool side_copy = copy && gather;
-  cudaStream_t side = nullptr;
-  cudaEvent_t ev[2] = {};
-  if (side_copy) {
-    if ((s = internal_side_stream(&side, ev, 2)) != FCC_OK) return s;
-    if (cudaEventRecord(ev[0], st) != cudaSuccess ||
-        cudaStreamWaitEvent(side, ev[0], 0) != cudaSuccess)
-      return FCC_ERR_CUDA;
-  }
-  if (copy && !copy_in_gemm)
-    copy_kernel<<<std::max(1, sms) * 4, 256, 0, side_copy ? side : st>>>(a);
   if (cudaGetLastError() != cudaSuccess) return FCC_ERR_CUDA;
-  if (side_copy && cudaEventRecord(ev[1], side) != cudaSuccess) return FCC_ERR_CUDA;
+  uint64_t launches = 4;
   const int grid = std::max(cg, (sms / cg) * cg);
-  if (launch_grouped_gemm(g, cg, grid, st) != cudaSuccess) return FCC_ERR_CUDA;
-  if (side_copy && cudaStreamWaitEvent(st, ev[1], 0) != cudaSuccess) return FCC_ERR_CUDA;
-  bump_launch_count((copy && !copy_in_gemm) ? 6 : 5);
+
+  if (interdecom) {
+    // Chunks are expert ranges [i*E/c, (i+1)*E/c): every range's row copy is
+    // queued on a side stream at once, and range i's grouped GEMM runs on the
+    // caller's stream after range i's copy, so range i+1's copy overlaps
+    // range i's GEMM.  c from opts->chunks or the chunk model.
+    int chunks = (opts != nullptr && opts->chunks > 0) ? opts->chunks
+                                                       : moe_model_chunks(R, T, H, F, E, topk);
+    chunks = std::max(1, std::min(chunks, E));
+    cudaStream_t side = nullptr;
+    cudaEvent_t ev[FCC_MAX_EXPERTS + 1];
+    if ((s = internal_streams_events(&side, 1, ev, chunks + 1)) != FCC_OK) return s;
+    if (cudaEventRecord(ev[chunks], st) != cudaSuccess ||
+        cudaStreamWaitEvent(side, ev[chunks], 0) != cudaSuccess)
+      return FCC_ERR_CUDA;
+    for (int i = 0; i < chunks; ++i) {
+      const int e_lo = i * E / chunks, e_hi = (i + 1) * E / chunks;
+      if (e_lo == e_hi) continue;
+      copy_expert_rows_kernel<<<std::max(1, sms) * 4, 256, 0, side>>>(a, e_lo, e_hi);
+      if (cudaGetLastError() != cudaSuccess) return FCC_ERR_CUDA;
+      if (cudaEventRecord(ev[i], side) != cudaSuccess ||
+          cudaStreamWaitEvent(st, ev[i], 0) != cudaSuccess)
+        return FCC_ERR_CUDA;
+      g.e_lo = e_lo;
+      g.e_hi = e_hi;
+      if (launch_grouped_gemm(g, cg, grid, st) != cudaSuccess) return FCC_ERR_CUDA;
+      launches += 2;
+    }
+  } else if (ce) {
+    // The (source rank, expert) runs are contiguous on both sides once each
+    // source packs its rows (an SM copy within the rank); the exchange itself
+    // is one cudaMemcpyAsync per run on the copy engines.  The run sizes are
+    // data-dependent, so the host reads them back first: this form
+    // synchronises the stream (as a copy-engine all-to-all with variable
+    // splits needs the split sizes on the host).
+    ce_plan_kernel<<<1, 64, 0, st>>>(a);
+    ce_pack_kernel<<<std::max(1, sms) * 4, 256, 0, st>>>(a);
+    if (cudaGetLastError() != cudaSuccess) return FCC_ERR_CUDA;
+    launches += 2;
+    const size_t plan_bytes = static_cast<size_t>(R) * E * 3 * 4;
+    int32_t* hp = nullptr;
+    if ((s = internal_host_buffer(plan_bytes, reinterpret_cast<void**>(&hp))) != FCC_OK) return s;
+    if (cudaMemcpyAsync(hp, a.ce_plan, plan_bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess)
+      return FCC_ERR_CUDA;
+    constexpr int kCeStreams = 4;
+    cudaStream_t side[kCeStreams];
+    cudaEvent_t ev[kCeStreams + 1];
+    if ((s = internal_streams_events(side, kCeStreams, ev, kCeStreams + 1)) != FCC_OK) return s;
+    if (cudaEventRecord(ev[kCeStreams], st) != cudaSuccess) return FCC_ERR_CUDA;
+    for (int i = 0; i < kCeStreams; ++i)
+      if (cudaStreamWaitEvent(side[i], ev[kCeStreams], 0) != cudaSuccess) return FCC_ERR_CUDA;
+    const size_t row_bytes = static_cast<size_t>(H) * 2;
+    int q = 0;
+    for (int src = 0; src < R; ++src) {
+      for (int e = 0; e < E; ++e) {
+        const int32_t* pl = hp + 3 * (src * E + e);
+        const int64_t send_row = pl[0], recv_row = pl[1], rows = pl[2];
+        if (rows == 0) continue;
+        // The runs come from this call's own kernels; a run outside its
+        // buffers would be a library fault: refuse it rather than copy.
+        if (rows < 0 || send_row < 0 || recv_row < 0 || send_row + rows > T * topk ||
+            recv_row + rows > cap)
+          return FCC_ERR_CUDA;
+        if (cudaMemcpyAsync(static_cast<char*>(a.recv_x[e / a.Eloc]) + recv_row * row_bytes,
+                            static_cast<const char*>(a.send[src]) + send_row * row_bytes,
+                            rows * row_bytes, cudaMemcpyDeviceToDevice,
+                            side[q++ % kCeStreams]) != cudaSuccess)
+          return FCC_ERR_CUDA;
+      }
+    }
+    for (int i = 0; i < kCeStreams; ++i)
+      if (cudaEventRecord(ev[i], side[i]) != cudaSuccess ||
+          cudaStreamWaitEvent(st, ev[i], 0) != cudaSuccess)
+        return FCC_ERR_CUDA;
+    if (launch_grouped_gemm(g, cg, grid, st) != cudaSuccess) return FCC_ERR_CUDA;
+    launches += 1;
+  } else {
+    // With the gather the copy (only for a requested recv_x) runs beside the
+    // GEMM on a side stream: both only read what the dispatch kernels wrote.
+    const bool copy = !gather || recv_x != nullptr;
+    const bool side_copy = copy && gather;
+    cudaStream_t side = nullptr;
+    cudaEvent_t ev[2] = {};
+    if (side_copy) {
+      if ((s = internal_side_stream(&side, ev, 2)) != FCC_OK) return s;
+      if (cudaEventRecord(ev[0], st) != cudaSuccess ||
+          cudaStreamWaitEvent(side, ev[0], 0) != cudaSuccess)
+        return FCC_ERR_CUDA;
+    }
+    if (copy && !copy_in_gemm) {
+      copy_kernel<<<std::max(1, sms) * 4, 256, 0, side_copy ? side : st>>>(a);
+      launches += 1;
+    }
+    if (cudaGetLastError() != cudaSuccess) return FCC_ERR_CUDA;
+    if (side_copy && cudaEventRecord(ev[1], side) != cudaSuccess) return FCC_ERR_CUDA;
+    if (launch_grouped_gemm(g, cg, grid, st) != cudaSuccess) return FCC_ERR_CUDA;
+    if (side_copy && cudaStreamWaitEvent(st, ev[1], 0) != cudaSuccess) return FCC_ERR_CUDA;
+    launches += 1;
+  }
+  bump_launch_count(launches);
+  return FCC_OK;
+}
+
+// Test support: the grouped expert GEMM (with in-kernel staging) on a table
+// of one expert, one 256-row unit holding one row, and one 256-column tile,
+// whose copy cursor starts past the last chunk: the copy warps claim nothing,
+// so the unit's row counter stays at zero and the TMA producers' bounded wait
+// for it runs out after timeout_ns.  The kernel then records FCC_ERR_TIMEOUT,
+// unwinds (no loads or MMAs were issued), frees its tensor memory and exits.
+fcc_status fcc_test_grouped_wait_timeout(int64_t timeout_ns, fcc_stream_t stream) {
+  if (timeout_ns <= 0) return FCC_ERR_INVALID;
+  constexpr int kRows = 256, kH = 64, kF = 256;
+  // ints: tile_start[2], expert_rows[1], expert_base[1], ready[1], cursor, recv_src[1]
+  constexpr size_t kInts = 256;
+  constexpr size_t kA = static_cast<size_t>(kRows) * kH * 2, kB = static_cast<size_t>(kH) * kF * 2,
+                   kOut = static_cast<size_t>(kRows) * kF * 2;
+  void* ws = nullptr;
+  int* status = nullptr;
+  int sms = 0;
+  unsigned long long tmo = 0;
+  fcc_status s = internal_prepare(nullptr, kInts + kA + kB + kOut, &ws, &status, &sms, &tmo);
+  if (s != FCC_OK) return s;
+  char* base = static_cast<char*>(ws);
+  int32_t* ints = reinterpret_cast<int32_t*>(base);
+  void* A = base + kInts;
+  void* Bw = base + kInts + kA;
+  void* out = base + kInts + kA + kB;
+  static const int32_t host_ints[8] = {0, 1, /*rows*/ 1, /*base*/ 0, /*ready*/ 0,
+                                       /*cursor*/ 1 << 30, /*recv_src*/ 0, 0};
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(ws, 0, kInts + kA + kB + kOut, st) != cudaSuccess ||
+      cudaMemcpyAsync(ints, host_ints, sizeof(host_ints), cudaMemcpyHostToDevice, st) !=
+          cudaSuccess)
+    return FCC_ERR_CUDA;
+  GroupedParams g;
+  std::memset(&g, 0, sizeof(g));
+  if ((s = internal_make_map(&g.mapA[0], A, kRows, kH, kBM)) != FCC_OK) return s;
+  if ((s = internal_make_map(&g.mapB[0], Bw, kH, kF, kBK)) != FCC_OK) return s;
+  g.out[0] = out;
+  g.R = 1;
+  g.E = 1;
+  g.Eloc = 1;
+  g.N = kF;
+  g.K = kH;
+  g.tiles_n = 1;
+  g.kb_per_rank = 1;
+  g.tile_start = ints;
+  g.expert_rows = ints + 2;
+  g.expert_base = ints + 3;
+  g.e_lo = 0;
+  g.e_hi = 1;
+  g.status = status;
+  g.timeout_ns = static_cast<unsigned long long>(timeout_ns);
+  g.recv_src[0] = ints + 6;
+  g.src_x[0] = A;
+  g.stage_x[0] = A;
+  g.T = 1;
+  g.ready = ints + 4;
+  g.copy_cursor = ints + 5;
+  g.stage_copy = 1;
+  if (launch_grouped_gemm(g, 2, 2, st) != cudaSuccess) return FCC_ERR_CUDA;
+  bump_launch_count(1);
   return FCC_OK;
 }
 

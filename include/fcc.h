@@ -70,8 +70,10 @@ typedef enum {
   FCC_ALGO_AUTO = 0,       /* chosen per operator and shape (fcc_choose_algo) */
   FCC_ALGO_FUSED = 1,      /* fused GEMM + collective in one persistent kernel */
   FCC_ALGO_UNFUSED = 2,    /* per-rank GEMM to f32 partials, then a reduce/copy kernel */
-  FCC_ALGO_INTERDECOM = 3, /* row chunks: GEMM of chunk i overlaps the collective of i-1 */
-  FCC_ALGO_CE = 4          /* partials moved by copy engines (cudaMemcpyAsync), no SMs */
+  FCC_ALGO_INTERDECOM = 3, /* chunks: the GEMM of one chunk overlaps the data movement of
+                              another (row chunks; MoE: expert ranges) */
+  FCC_ALGO_CE = 4          /* the data between ranks moved by the copy engines
+                              (cudaMemcpyAsync), no SMs */
 } fcc_algo;
 
 typedef struct {
@@ -169,6 +171,14 @@ fcc_status fcc_gemv_ar_static(int R, const void *const *A, const void *const *B,
  *   X = [X_shard[0]; ...; X_shard[R-1]]   (each [M/R, K], X is [M, K])
  *   out[r] = X @ B[r]                      ([M, N] per rank, dtype `out_dtype`)
  *   gathered[r] (nullable array, or NULL entries): receives X ([M, K] bf16).
+ * opts->algo: FUSED (AUTO) = one kernel whose tiles read their A rows from
+ * the owning shard; UNFUSED = a gather kernel into gathered[0] (or
+ * workspace), then the per-rank GEMMs; INTERDECOM = the same in row chunks
+ * of 256-row tiles, each chunk's gather on a side stream ahead of that
+ * chunk's GEMMs (chunk count opts->chunks, else the fcc_interdecom_chunks
+ * model with G = the GEMMs, X = the gather); CE = the gather by one
+ * cudaMemcpyAsync per shard.  The non-fused forms use workspace of M*K*2
+ * bytes when gathered[0] is NULL (fcc_workspace_size).
  */
 fcc_status fcc_ag_gemm(int R, const void *const *X_shard, const void *const *B,
                        void *const *out, void *const *gathered, int64_t M, int64_t N,
@@ -193,7 +203,16 @@ fcc_status fcc_ag_gemm(int R, const void *const *X_shard, const void *const *B,
  * itself, into recv_x or into workspace when it is NULL, one (expert,
  * m tile) unit after another, and its tensor cores read each unit as soon as
  * it is moved.  FCC_ALGO_UNFUSED (the unfused baseline) moves all rows with a
- * separate copy kernel before the GEMM.  With
+ * separate copy kernel before the GEMM.  FCC_ALGO_INTERDECOM (the chunked
+ * baseline) splits the experts into c contiguous ranges (c = opts->chunks,
+ * else the fcc_interdecom_chunks model with G = the expert GEMMs, X = the
+ * row copy; at most E); each range's rows are copied on a side stream ahead
+ * of that range's grouped GEMM, so copy i+1 overlaps GEMM i.  FCC_ALGO_CE
+ * (the copy-engine baseline) packs each source rank's kept rows into a send
+ * buffer in (expert, token, slot) order (a copy within the rank), reads the
+ * (source, expert) run table back to the host (so this form synchronises
+ * `stream` before it returns), and moves each run, contiguous on both sides,
+ * with one cudaMemcpyAsync on the copy engines, then runs the GEMM.  With
  * opts->algo == FCC_ALGO_FUSED and the sources one [R*T,H] array (X[s] =
  * X[0] + s*T*H elements), the GEMM instead reads each row straight from its
  * source token (TMA gather) and a non-NULL recv_x is filled beside it (slower
@@ -206,7 +225,8 @@ fcc_status fcc_ag_gemm(int R, const void *const *X_shard, const void *const *B,
  * F % 8 == 0.  A rank receiving more than cap rows sets FCC_ERR_CAPACITY in
  * the status word; its rows past cap are dropped (not copied, not multiplied).
  * Index outputs are bit-exact and repeatable (no atomics decide a position).
- * Uses workspace (fcc_moe_workspace_size).
+ * Uses workspace (fcc_moe_workspace_size; with FCC_ALGO_CE in opts it
+ * includes the R*T*topk*H*2 bytes of send buffers).
  */
 fcc_status fcc_moe_dispatch_gemm(int R, const void *const *X, const float *const *logits,
                                  const void *const *W, int64_t T, int64_t H, int64_t F, int E,
@@ -343,6 +363,15 @@ double fcc_interdecom_time(double G, double X, double alpha, int chunks);
  * fcc_stream_status() afterwards returns FCC_ERR_TIMEOUT.
  */
 fcc_status fcc_test_wait_timeout(int64_t timeout_ns, fcc_stream_t stream);
+
+/*
+ * Test support: launches the MoE grouped expert GEMM kernel (the in-kernel
+ * staging form of fcc_moe_dispatch_gemm) on a one-tile table whose unit row
+ * counter nothing raises, so its TMA producers' bounded wait for the unit's
+ * rows runs out after timeout_ns; the kernel records FCC_ERR_TIMEOUT and
+ * returns, leaving the context usable.  Uses the internal workspace pool.
+ */
+fcc_status fcc_test_grouped_wait_timeout(int64_t timeout_ns, fcc_stream_t stream);
 
 /* Number of kernels this library has launched in this process (all devices). */
 uint64_t fcc_launch_count(void);

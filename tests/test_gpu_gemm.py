@@ -231,7 +231,7 @@ def test_caller_workspace_and_too_small():
 
 @pytest.mark.parametrize("R,Ms,N,K", [(4, 136, 200, 96), (2, 128, 512, 64), (8, 64, 264, 136),
                                       (2, 520, 264, 64)])
-@pytest.mark.parametrize("algo,pair", [(1, 0), (1, 1), (2, 0), (4, 0)])
+@pytest.mark.parametrize("algo,pair", [(1, 0), (1, 1), (2, 0), (3, 0), (4, 0)])
 def test_ag_gemm(R, Ms, N, K, algo, pair):
     """A 256-row pair tile may span two shards (Ms = 136 with 4 ranks, Ms = 520
     with 2); pair = 1 runs one CTA per 128-row tile."""
@@ -247,6 +247,29 @@ def test_ag_gemm(R, Ms, N, K, algo, pair):
     for r in range(R):
         assert_close(to_f64(outs[r]), oracle.ag_gemm(X, B, r), f"rank {r}")
         assert np.array_equal(bits(gath[r]).view(np.uint16), full), f"gathered copy {r}"
+
+
+@pytest.mark.parametrize("chunks", [1, 2, 3, 64])
+@pytest.mark.parametrize("gathered", [False, True])
+def test_ag_gemm_interdecom_chunks(chunks, gathered):
+    """InterDecom: the gather of each 256-row chunk runs on a side stream ahead
+    of that chunk's GEMM; any chunk count (ragged last chunk, more chunks than
+    tiles) gives the oracle's result, with or without the gathered copies."""
+    R, Ms, N, K = 4, 200, 264, 136
+    X, B = synth.gemm_inputs(R, Ms, N, K, 1.0, 1.0, seed=29)
+    dX, dB = _upload(X, B)
+    M = R * Ms
+    outs = [empty((M, N), torch.float32, fill=float("nan")) for _ in range(R)]
+    gath = [empty((M, K), torch.bfloat16, fill=0.0) for _ in range(R)] if gathered else None
+    fcc.fcc_ag_gemm(R, dX, dB, outs, gath, M, N, K, fcc.FCC_BF16, fcc.FCC_F32,
+                    fcc.make_opts(algo=fcc.FCC_ALGO_INTERDECOM, chunks=chunks))
+    assert fcc.fcc_stream_status() == fcc.FCC_OK
+    full = np.concatenate(X)
+    for r in range(R):
+        fro, _ = assert_close(to_f64(outs[r]), oracle.ag_gemm(X, B, r), f"rank {r}")
+        assert fro < 1e-5  # f32 output
+        if gathered:
+            assert np.array_equal(bits(gath[r]).view(np.uint16), full), f"gathered copy {r}"
 
 
 def test_ag_gemm_without_gathered_output():
@@ -288,13 +311,17 @@ def test_rs_full_size_sampled_rows():
         assert torch.equal(outs[j].view(torch.int16), again[j].view(torch.int16))
 
 
-def test_ag_full_size_sampled_rows():
+@pytest.mark.parametrize("algo", [fcc.FCC_ALGO_AUTO, fcc.FCC_ALGO_INTERDECOM])
+def test_ag_full_size_sampled_rows(algo):
+    """The 8-rank 8192x3584x8192 workload in the benchmark's launch shapes: the
+    fused kernel and the InterDecom baseline (chunk count from the model)."""
     w = synth.WORKLOADS["ag_gemm_r8_8192x3584x8192"]
     Ms = w.M // w.R
     X, B = synth.gemm_inputs(w.R, Ms, w.N, w.K, w.std_a, w.std_b, seed=0)
     dX, dB = _upload(X, B)
     outs = [empty((w.M, w.N), torch.bfloat16, fill=float("nan")) for _ in range(w.R)]
-    fcc.fcc_ag_gemm(w.R, dX, dB, outs, None, w.M, w.N, w.K, fcc.FCC_BF16, fcc.FCC_BF16)
+    fcc.fcc_ag_gemm(w.R, dX, dB, outs, None, w.M, w.N, w.K, fcc.FCC_BF16, fcc.FCC_BF16,
+                    fcc.make_opts(algo=algo))
     assert fcc.fcc_stream_status() == fcc.FCC_OK
     for r in range(w.R):
         rows = _sample_rows(w.M, 12, seed=100 + r)

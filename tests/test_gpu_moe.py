@@ -95,13 +95,23 @@ def _check(X, logits, W, R, T, H, F, E, topk, cap, out, sample=None, seed=0):
 #   fused_separate FCC_ALGO_FUSED with separate sources: staged as by default
 #   unfused        a separate copy kernel into recv_x, then the GEMM
 #   unfused_workspace  the same into library workspace
+#   interdecom     expert-range chunks: each range's rows copied on a side
+#                  stream ahead of that range's GEMM (chunk model), into recv_x
+#   interdecom_workspace  the same into library workspace
+#   ce             each source packs its rows, the copy engines move the
+#                  (source, expert) runs into recv_x, then the GEMM
+#   ce_workspace   the same into library workspace
 PATHS = {"staged": (True, False, fcc.FCC_ALGO_AUTO),
          "workspace": (False, True, fcc.FCC_ALGO_AUTO),
          "gather": (False, True, fcc.FCC_ALGO_FUSED),
          "gather_recv_x": (True, True, fcc.FCC_ALGO_FUSED),
          "fused_separate": (False, False, fcc.FCC_ALGO_FUSED),
          "unfused": (True, False, fcc.FCC_ALGO_UNFUSED),
-         "unfused_workspace": (False, True, fcc.FCC_ALGO_UNFUSED)}
+         "unfused_workspace": (False, True, fcc.FCC_ALGO_UNFUSED),
+         "interdecom": (True, False, fcc.FCC_ALGO_INTERDECOM),
+         "interdecom_workspace": (False, True, fcc.FCC_ALGO_INTERDECOM),
+         "ce": (True, False, fcc.FCC_ALGO_CE),
+         "ce_workspace": (False, True, fcc.FCC_ALGO_CE)}
 
 
 @pytest.mark.parametrize("R,T,H,F,E,topk", [
@@ -179,17 +189,48 @@ def test_moe_in_kernel_staging_equals_copy_kernel(pair):
                                other["recv_y"][d][:n].view(torch.int16))
 
 
-def test_moe_capacity_overflow_reported():
+@pytest.mark.parametrize("algo", [fcc.FCC_ALGO_AUTO, fcc.FCC_ALGO_UNFUSED,
+                                  fcc.FCC_ALGO_INTERDECOM, fcc.FCC_ALGO_CE])
+def test_moe_capacity_overflow_reported(algo):
     R, T, H, F, E, topk = 2, 256, 64, 64, 4, 2
     X, logits, W = synth.moe_inputs(R, T, H, E, F, seed=7)
-    out = _run(X, logits, W, R, T, H, F, E, topk, cap=100)
+    cap = 100
+    out = _run(X, logits, W, R, T, H, F, E, topk, cap, opts=fcc.make_opts(algo=algo))
     assert out["status"] == fcc.FCC_ERR_CAPACITY
     assert fcc.fcc_stream_status() == fcc.FCC_OK
-    # the kept rows are the first cap rows of the full dispatch
+    # the kept rows are the first cap rows of the full dispatch: their sources,
+    # their staged copies and their products
     d = oracle.moe_dispatch(oracle.moe_route(np.stack(logits), topk)[0], R, E, R * T * topk)
     for dst in range(R):
-        n = min(100, int(d.recv_counts[dst]))
+        n = min(cap, int(d.recv_counts[dst]))
         assert np.array_equal(out["src"][dst].cpu().numpy()[:n], d.recv_src[dst, :n])
+        s_rank, s_tok = d.recv_src[dst, :n] // T, d.recv_src[dst, :n] % T
+        rx = out["recv_x"][dst][:n].view(torch.int16).cpu().numpy()
+        want = np.stack([X[s][t] for s, t in zip(s_rank, s_tok)]).view(np.int16)
+        assert np.array_equal(rx, want), f"recv_x of rank {dst}"
+        ref = oracle.moe_expert_rows(X, W, s_rank, s_tok, d.recv_expert[dst, :n])
+        assert_close(to_f64(out["recv_y"][dst][:n]), ref, f"recv_y of rank {dst}")
+
+
+@pytest.mark.parametrize("chunks", [1, 3, 5, 64])
+def test_moe_interdecom_chunk_counts(chunks):
+    """Expert ranges of any size (E = 16 over 1, 3, 5 or, clamped, 16 chunks,
+    uneven ranges included) give the same rows and products, bit for bit, as
+    the separate copy kernel: the same rows and the same MMAs per tile."""
+    R, T, H, F, E, topk = 4, 257, 192, 264, 16, 2
+    X, logits, W = synth.moe_inputs(R, T, H, E, F, seed=19)
+    cap = R * T * topk
+    a = _run(X, logits, W, R, T, H, F, E, topk, cap,
+             opts=fcc.make_opts(algo=fcc.FCC_ALGO_INTERDECOM, chunks=chunks))
+    _check(X, logits, W, R, T, H, F, E, topk, cap, a)
+    b = _run(X, logits, W, R, T, H, F, E, topk, cap,
+             opts=fcc.make_opts(algo=fcc.FCC_ALGO_UNFUSED))
+    for d in range(R):
+        n = int((a["src"][d] >= 0).sum())
+        assert torch.equal(a["recv_x"][d][:n].view(torch.int16),
+                           b["recv_x"][d][:n].view(torch.int16))
+        assert torch.equal(a["recv_y"][d][:n].view(torch.int16),
+                           b["recv_y"][d][:n].view(torch.int16))
 
 
 def test_moe_invalid_arguments():
@@ -204,11 +245,12 @@ def test_moe_invalid_arguments():
 
 
 @pytest.mark.parametrize("path", ["workspace", "staged", "unfused_workspace", "gather",
-                                  "gather_recv_x"])
+                                  "gather_recv_x", "interdecom_workspace", "ce_workspace"])
 def test_moe_full_workload_sampled(path):
     """The benchmark's launches: rows staged in library workspace (or recv_x)
     by the GEMM's copy warps or by a separate copy kernel, gathered by the
-    GEMM, and gathered with recv_x written beside the GEMM."""
+    GEMM, gathered with recv_x written beside the GEMM, moved range by range
+    ahead of each range's GEMM (InterDecom), or by the copy engines."""
     w = synth.WORKLOADS["moe_r8_t4096_h4096_e64_f1408"]
     X, logits, W = synth.moe_inputs(w.R, w.T, w.H, w.E, w.F, std_x=w.std_a, std_w=w.std_b,
                                     seed=0)
@@ -312,3 +354,18 @@ def test_moe_combine_full_workload_sampled():
     ref, tok = _combine_ref(X, W, logits, w.R, w.T, w.E, w.topk, cap, tok)
     got = np.stack([to_f64(y[t // w.T][int(t % w.T)]) for t in tok])
     assert_close(got, ref, "combined rows (sampled)")
+
+
+def test_grouped_gemm_unit_wait_reports_timeout_and_context_survives():
+    """The expert GEMM's TMA producer waits (bounded) for the copy warps to
+    publish a unit's rows.  With a unit whose counter nothing raises, the wait
+    runs out: the status word reports FCC_ERR_TIMEOUT, reading it clears it,
+    and the next dispatch + GEMM on the same context is still correct."""
+    fcc.fcc_test_grouped_wait_timeout(2_000_000)  # 2 ms
+    assert fcc.fcc_stream_status() == fcc.FCC_ERR_TIMEOUT
+    assert fcc.fcc_stream_status() == fcc.FCC_OK
+    R, T, H, F, E, topk = 2, 300, 128, 136, 8, 2
+    X, logits, W = synth.moe_inputs(R, T, H, E, F, seed=21)
+    cap = R * T * topk
+    out = _run(X, logits, W, R, T, H, F, E, topk, cap)
+    _check(X, logits, W, R, T, H, F, E, topk, cap, out)
