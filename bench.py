@@ -20,6 +20,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -49,6 +50,8 @@ def parse():
     ap.add_argument("--ref-seconds", type=float, default=90.0,
                     help="target CPU time of the whole --impl reference run")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg")
+    ap.add_argument("--details", default=None,
+                    help="also write every leg's full results (paths, sweeps) to this file")
     ap.add_argument("--op", default=None,
                     help="run only this operator leg (a workload name of the ops table) "
                          "and print its result; for profiling one kernel")
@@ -67,19 +70,66 @@ def peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 100 ms."""
+    """SM clock and throttle reasons during the timed region.
+
+    Polled through NVML (libnvidia-ml, by ctypes) every 2 ms on a thread, so a
+    timed region of a few tens of milliseconds still holds tens of samples;
+    where NVML cannot be loaded, nvidia-smi at its 100 ms period instead.
+    Reading clocks changes no setting of the GPU."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    # NVML clock-event reason bits
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+    PERIOD_S = 0.002
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
-        self.lines = []
+        self.samples = []        # (time, sm_mhz, sm_max_mhz, reason names)
+        self.source = None
         self.t_start = self.t_stop = None
+        self._stop = threading.Event()
+
+    def _nvml(self):
+        import ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+        h = ctypes.c_void_p()
+        if lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(self.gpu), ctypes.byref(h)) != 0:
+            raise RuntimeError("no NVML handle")
+        reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        return lib, h, reasons
 
     def start(self):
+        try:
+            lib, h, reasons = self._nvml()
+        except Exception:
+            lib = None
+        if lib is not None:
+            import ctypes
+            self.source = f"nvml every {self.PERIOD_S * 1e3:.0f} ms"
+
+            def poll():
+                clk, mx, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+                while not self._stop.is_set():
+                    t = time.time()
+                    ok = (lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0 and
+                          lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0 and
+                          reasons(h, ctypes.byref(rs)) == 0)
+                    if ok:
+                        names = [n for b, n in self.REASONS.items() if rs.value & b]
+                        self.samples.append((t, float(clk.value), float(mx.value), names))
+                    time.sleep(self.PERIOD_S)
+                lib.nvmlShutdown()
+
+            self._t = threading.Thread(target=poll, daemon=True)
+            self._t.start()
+            return
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
@@ -88,12 +138,22 @@ class ClockSampler:
         except Exception:
             self.proc = None
             return
-        self._t = threading.Thread(target=self._read, daemon=True)
+        self.source = "nvidia-smi every 100 ms"
+        self._t = threading.Thread(target=self._read_smi, daemon=True)
         self._t.start()
 
-    def _read(self):
+    def _read_smi(self):
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in self.proc.stdout:
-            self.lines.append((time.time(), line.strip()))
+            parts = [p.strip() for p in line.strip().split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm, smax = float(parts[1]), float(parts[2])
+            except ValueError:
+                continue
+            rs = [n for n, v in zip(names, parts[5:9]) if v.lower() == "active"]
+            self.samples.append((time.time(), sm, smax, rs))
 
     def mark_start(self):
         self.t_start = time.time()
@@ -102,37 +162,31 @@ class ClockSampler:
         self.t_stop = time.time()
 
     def stop(self):
+        self._stop.set()
         if self.proc is not None:
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
             except Exception:
                 self.proc.kill()
+        t = getattr(self, "_t", None)
+        if t is not None:
+            t.join(timeout=5)
 
     def summary(self):
-        rows = [l for (t, l) in self.lines
-                if self.t_start is not None and self.t_start <= t <= (self.t_stop or t)]
+        rows = [x for x in self.samples
+                if self.t_start is not None and self.t_start <= x[0] <= (self.t_stop or x[0])]
+        window = "timed region"
         if not rows:
-            rows = [l for (_, l) in self.lines]
-        sm, smax, reasons = [], [], set()
-        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
-                 "sw_power_cap"]
-        for r in rows:
-            parts = [p.strip() for p in r.split(",")]
-            if len(parts) < 9:
-                continue
-            try:
-                sm.append(float(parts[1]))
-                smax.append(float(parts[2]))
-            except ValueError:
-                continue
-            for name, val in zip(names[1:], parts[5:9]):
-                if val.lower() == "active":
-                    reasons.add(name)
-        if not sm:
+            rows, window = list(self.samples), "whole run (none inside the timed region)"
+        if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
-                "reasons": sorted(reasons), "samples": len(sm)}
+        reasons = sorted({n for x in rows for n in x[3]})
+        out = {"sm_mhz": statistics.median(x[1] for x in rows),
+               "sm_max_mhz": max(x[2] for x in rows), "reasons": reasons, "samples": len(rows)}
+        if window != "timed region":
+            out["window"] = window
+        return out
 
 
 def kernel_traffic(kernel: str, src_files):
@@ -290,30 +344,45 @@ def time_calls(fn, steps, warmup, stream):
     return s.elapsed_time(e) / steps  # ms
 
 
-def interdecom_check(fcc, R, M, N, K, dA, dB, outs, stream, unfused_ms, pk):
+def interdecom_check(run, chunk_counts, X_ms, unfused_ms, maxc, fcc, stream, steps=10):
     """The InterDecom chunk-count model against a sweep of chunk counts.
 
-    Model inputs from measurements of this run: X = the reduce of the R f32
-    partials into the shards at the measured copy bandwidth, G = the unfused
-    time minus X, alpha = what one chunk adds beyond G + X (T(1) - G - X)."""
-    sweep = {}
-    for c in (1, 2, 4, 8, 16, 32, 64):
-        o = fcc.make_opts(algo=fcc.FCC_ALGO_INTERDECOM, chunks=c)
-        sweep[c] = time_calls(lambda o=o: fcc.fcc_gemm_rs(R, dA, dB, outs, M, N, K, 0, 0, o,
-                                                          stream), 10, 2, stream)
-    X = (R * M * N * 4 + M * N * 2) / (pk["hbm_gbs"] * 1e9) * 1e3  # ms
-    G = max(unfused_ms - X, 1e-3)
-    alpha = max(sweep[1] - G - X, 1e-4)
-    c_star = fcc.fcc_interdecom_chunks(G, X, alpha, 64)
-    o = fcc.make_opts(algo=fcc.FCC_ALGO_INTERDECOM, chunks=c_star)
-    t_star = time_calls(lambda: fcc.fcc_gemm_rs(R, dA, dB, outs, M, N, K, 0, 0, o, stream),
-                        10, 2, stream)
+    run(c) makes one call with c chunks.  Model inputs from this run's
+    measurements: X = the movement's bytes at the measured copy bandwidth, G =
+    the unfused time minus X, alpha = what one chunk adds beyond G + X
+    (T(1) - G - X).  Reports whether the model's c* lands within 10 % of the
+    sweep's best time."""
+    sweep = {c: time_calls(lambda c=c: run(c), steps, 2, stream) for c in chunk_counts}
+    G = max(unfused_ms - X_ms, 1e-3)
+    alpha = max(sweep[chunk_counts[0]] - G - X_ms, 1e-4)
+    c_star = fcc.fcc_interdecom_chunks(G, X_ms, alpha, maxc)
+    t_star = sweep[c_star] if c_star in sweep else time_calls(lambda: run(c_star), steps, 2,
+                                                              stream)
     best_c = min(sweep, key=sweep.get)
     return {"sweep_ms": {str(c): t for c, t in sweep.items()}, "best_c": best_c,
-            "model": {"G_ms": G, "X_ms": X, "alpha_ms": alpha, "c_star": c_star,
+            "model": {"G_ms": G, "X_ms": X_ms, "alpha_ms": alpha, "c_star": c_star,
                       "T_cstar_ms": t_star,
-                      "T_model_ms": fcc.fcc_interdecom_time(G, X, alpha, c_star)},
+                      "T_model_ms": fcc.fcc_interdecom_time(G, X_ms, alpha, c_star)},
             "c_star_within_10pct_of_best": t_star <= 1.10 * sweep[best_c]}
+
+
+def phase_fractions(torch, dev, call):
+    """One call with per-CTA phase timing (%globaltimer stamps in the GEMM
+    kernel): the fraction of the CTAs' time their epilogue warps spent on
+    tiles, and the fraction their MMA warps spent waiting for an accumulator
+    the epilogue still held (the part of the epilogue not hidden behind the
+    next tile's MMAs).  call(opts) runs the operator once."""
+    buf = torch.zeros(4 * 1024, dtype=torch.int64, device=dev)
+    call(buf)
+    torch.cuda.synchronize()
+    t = buf.view(-1, 4).cpu().numpy().astype(float)
+    t = t[t[:, 0] > 0]
+    span = t[:, 0].sum()
+    leaders = t[t[:, 2] > 0] if (t[:, 2] > 0).any() else t
+    return {"ctas": int(len(t)), "tiles": int(t[:, 3].sum()),
+            "epilogue_busy_frac": float(t[:, 1].sum() / span),
+            "mma_wait_on_epilogue_frac": float(t[:, 2].sum() / max(leaders[:, 0].sum(), 1.0)),
+            "kernel_us_max_cta": float(t[:, 0].max() / 1e3)}
 
 
 def small_rs_latency(fcc, torch, np, synth, dev, stream):
@@ -326,10 +395,17 @@ def small_rs_latency(fcc, torch, np, synth, dev, stream):
     dB = [torch.from_numpy(b.view(np.int16)).to(dev) for b in B]
     outs = [torch.empty((w.M // w.R, w.N), dtype=torch.float32, device=dev) for _ in range(w.R)]
 
-    def call(s):
-        fcc.fcc_gemm_rs(w.R, dA, dB, outs, w.M, w.N, w.K, 0, 2, None, s)
+    pA, pB, pO = fcc.ptr_array(dA), fcc.ptr_array(dB), fcc.ptr_array(outs)
 
-    res = {"plain_us": 1e3 * time_calls(lambda: call(stream), 200, 10, stream)}
+    def call(s):
+        fcc.fcc_gemm_rs(w.R, pA, pB, pO, w.M, w.N, w.K, 0, 2, None, s)
+
+    # back-to-back calls with the pointer arrays built once, and with the
+    # tensors marshalled on every call
+    res = {"plain_us": 1e3 * time_calls(lambda: call(stream), 200, 10, stream),
+           "marshalled_us": 1e3 * time_calls(
+               lambda: fcc.fcc_gemm_rs(w.R, dA, dB, outs, w.M, w.N, w.K, 0, 2, None, stream),
+               200, 10, stream)}
     try:
         side = torch.cuda.Stream(device=dev)
         with torch.cuda.stream(side):
@@ -394,11 +470,14 @@ def other_ops(fcc, torch, np, synth, dev, stream, dA_rs, dB_rs, pk, only=None):
         outs = [torch.empty((M, N), dtype=torch.bfloat16, device=dev) for _ in range(R)]
         res = {}
         for name, o in [("fused", None), ("unfused", fcc.make_opts(algo=fcc.FCC_ALGO_UNFUSED)),
+                        ("interdecom", fcc.make_opts(algo=fcc.FCC_ALGO_INTERDECOM)),
                         ("copy_engine", fcc.make_opts(algo=fcc.FCC_ALGO_CE))]:
             t = time_calls(lambda o=o: fcc.fcc_gemm_ar(R, dA, dB_rs, outs, M, N, K, 0, 0, o, stream),
                            10, 3, stream)
             res[name] = {"ms": t, "TFLOP/s": w.flops() / (t * 1e-3) / 1e12}
         res["roofline_frac"] = res["fused"]["TFLOP/s"] / tc
+        res["phases"] = phase_fractions(torch, dev, lambda buf: fcc.fcc_gemm_ar(
+            R, dA, dB_rs, outs, M, N, K, 0, 0, fcc.make_opts(phase_ns=buf), stream))
         ops[w.name] = res
         del outs, dA
 
@@ -430,12 +509,20 @@ def other_ops(fcc, torch, np, synth, dev, stream, dA_rs, dB_rs, pk, only=None):
         dBx = [up(b) for b in Bx]
         outs = [torch.empty((M, N), dtype=torch.bfloat16, device=dev) for _ in range(R)]
         res = {}
+        def ag(o):
+            fcc.fcc_ag_gemm(R, dX, dBx, outs, None, M, N, K, 0, 0, o, stream)
+
         for name, o in [("fused", None), ("unfused", fcc.make_opts(algo=fcc.FCC_ALGO_UNFUSED)),
+                        ("interdecom", fcc.make_opts(algo=fcc.FCC_ALGO_INTERDECOM)),
                         ("copy_engine", fcc.make_opts(algo=fcc.FCC_ALGO_CE))]:
-            t = time_calls(lambda o=o: fcc.fcc_ag_gemm(R, dX, dBx, outs, None, M, N, K, 0, 0, o,
-                                                       stream), 10, 3, stream)
+            t = time_calls(lambda o=o: ag(o), 10, 3, stream)
             res[name] = {"ms": t, "TFLOP/s": w.flops() / (t * 1e-3) / 1e12}
         res["roofline_frac"] = res["fused"]["TFLOP/s"] / tc
+        res["phases"] = phase_fractions(torch, dev, lambda buf: ag(fcc.make_opts(phase_ns=buf)))
+        X_ms = 2 * M * K * 2 / (hbm * 1e9) * 1e3  # the gather: X read and written once
+        res["interdecom_check"] = interdecom_check(
+            lambda c: ag(fcc.make_opts(algo=fcc.FCC_ALGO_INTERDECOM, chunks=c)),
+            (1, 2, 4, 8, 16, 32), X_ms, res["unfused"]["ms"], M // 256, fcc, stream)
         ops[w.name] = res
         del outs, dX, dBx
 
@@ -464,6 +551,15 @@ def other_ops(fcc, torch, np, synth, dev, stream, dA_rs, dB_rs, pk, only=None):
         t = time_calls(moe, 10, 3, stream)
         ou = fcc.make_opts(algo=fcc.FCC_ALGO_UNFUSED)
         tu = time_calls(lambda: moe(None, ou), 5, 2, stream)
+        oi = fcc.make_opts(algo=fcc.FCC_ALGO_INTERDECOM)
+        ti = time_calls(lambda: moe(None, oi), 5, 2, stream)
+        oc = fcc.make_opts(algo=fcc.FCC_ALGO_CE)
+        tce = time_calls(lambda: moe(None, oc), 5, 2, stream)
+        phases = phase_fractions(torch, dev, lambda buf: moe(None, fcc.make_opts(phase_ns=buf)))
+        X_ms = 2 * R * T * topk * H * 2 / (hbm * 1e9) * 1e3  # each receive row read and written
+        idc = interdecom_check(
+            lambda c: moe(None, fcc.make_opts(algo=fcc.FCC_ALGO_INTERDECOM, chunks=c)),
+            (1, 2, 4, 8, 16, 32, 64), X_ms, tu, E, fcc, stream, steps=5)
         tr = time_calls(lambda: moe(recv_x, None), 5, 2, stream)
         og = fcc.make_opts(algo=fcc.FCC_ALGO_FUSED)
         tg = time_calls(lambda: moe(None, og), 5, 2, stream)
@@ -477,12 +573,18 @@ def other_ops(fcc, torch, np, synth, dev, stream, dA_rs, dB_rs, pk, only=None):
         # combine: the return all-to-all + gate-weighted top-2 sum of the GEMM's rows
         y = [torch.empty((T, F), dtype=torch.bfloat16, device=dev) for _ in range(R)]
 
+        arrs = [fcc.ptr_array(v) for v in (recv_y, idx, gate, src, y)]
+
         def comb(s=None):
-            fcc.fcc_moe_combine(R, recv_y, cap, T, F, E, topk, idx, gate, src, counts, y,
+            py, pi, pg, ps, pyo = arrs
+            fcc.fcc_moe_combine(R, py, cap, T, F, E, topk, pi, pg, ps, counts, pyo,
                                 0, 0, None, stream if s is None else s)
 
         moe()
         tc_ = time_calls(comb, 20, 3, stream)
+        tcm = time_calls(lambda: fcc.fcc_moe_combine(R, recv_y, cap, T, F, E, topk, idx, gate,
+                                                     src, counts, y, 0, 0, None, stream),
+                         20, 3, stream)
         # The same calls replayed from a CUDA graph: the device time alone (a
         # call's host side, argument marshalling and launches, outlasts its
         # GPU work, so back-to-back calls leave the GPU idle between them).
@@ -505,7 +607,9 @@ def other_ops(fcc, torch, np, synth, dev, stream, dA_rs, dB_rs, pk, only=None):
         cbytes = R * T * topk * F * 2 + R * T * F * 2  # expert rows read once, y written once
         combine = {"us": tc_ * 1e3, "GB/s": cbytes / (tc_ * 1e-3) / 1e9,
                    "roofline_frac": cbytes / (tc_ * 1e-3) / 1e9 / hbm,
-                   "algorithmic_bytes": cbytes}
+                   "algorithmic_bytes": cbytes, "marshalled_us": tcm * 1e3,
+                   "path": "pointer arrays built once (ptr_array); marshalled_us: tensors "
+                           "marshalled on every call"}
         if "us" in graph:
             graph["GB/s"] = cbytes / (graph["us"] * 1e-6) / 1e9
             graph["roofline_frac"] = graph["GB/s"] / hbm
@@ -516,6 +620,13 @@ def other_ops(fcc, torch, np, synth, dev, stream, dA_rs, dB_rs, pk, only=None):
                "fused_recv_x": leg(tr, "the same, staging into the caller's recv_x"),
                "unfused": leg(tu, "route, separate dispatch copy kernel into workspace, then "
                                   "the grouped GEMM"),
+               "interdecom": leg(ti, "route, expert ranges: each range's rows copied on a side "
+                                     "stream ahead of that range's grouped GEMM (chunk model)"),
+               "copy_engine": leg(tce, "route, each source packs its rows, one cudaMemcpyAsync "
+                                       "per (source, expert) run, then the grouped GEMM; the run "
+                                       "table is read back to the host first"),
+               "interdecom_check": idc,
+               "phases": phases,
                "combine": combine,
                "layer": leg(tl, "dispatch + expert GEMM + combine (two calls)"),
                "gather_in_gemm": leg(tg, "route, grouped GEMM gathering its rows by TMA gather4"),
@@ -585,6 +696,89 @@ def other_ops(fcc, torch, np, synth, dev, stream, dA_rs, dB_rs, pk, only=None):
     if st != fcc.FCC_OK:
         raise RuntimeError(f"device status after the operator legs: {fcc.fcc_status_string(st)}")
     return ops
+
+
+def sig(x, n=4):
+    """x rounded to n significant digits (None stays None)."""
+    if x is None:
+        return None
+    if x == 0 or not math.isfinite(x):
+        return x
+    d = n - 1 - int(math.floor(math.log10(abs(x))))
+    v = round(x, d)
+    return int(v) if d <= 0 else v
+
+
+# Columns of the compact per-operator rows on the printed line: the forms'
+# times in microseconds, then the fused form's roofline fraction.
+OP_COLS = ("fused", "unfused", "interdecom", "copy_engine")
+
+
+def compact_ops(base, ops, rs_ms=None):
+    """Per operator a row [fused, unfused, interdecom, ce] in microseconds (null
+    where the form does not exist) and the roofline fraction of the fused form
+    (of the form AUTO runs, for the embedding); combine, attention and the
+    2-rank latency case as short rows of their own.  Per InterDecom check:
+    [model c*, best swept c, c* within 10 % of the best].  Short enough for the
+    whole line to stay under 1500 characters."""
+    out, idc = {"cols": "fused,unfused,interdecom,ce,frac"}, {}
+
+    def us(d, key):
+        v = d.get(key)
+        if isinstance(v, dict):
+            v = v["ms"] if "ms" in v else v["us"] / 1e3
+        return None if v is None else sig(v * 1e3)
+
+    def row(d, fused_us=None):
+        r = [us(d, k) for k in OP_COLS]
+        if fused_us is not None:
+            r[0] = fused_us
+        return r + [sig(d.get("roofline_frac"), 3)]
+
+    if base:
+        r = row(base, None if rs_ms is None else sig(rs_ms * 1e3))
+        r[-1] = sig(base.get("roofline_frac"), 3)
+        out["rs"] = r
+        out["rs_push"] = us(base, "fused_push")
+        out["rs_cublas"] = us(base, "cublas_stacked_gemm")
+        if "interdecom_check" in base:
+            idc["rs"] = base["interdecom_check"]
+    for key, name in [("ar", "gemm_ar_r8_8192x8192x3584"), ("ag", "ag_gemm_r8_8192x3584x8192"),
+                      ("moe", "moe_r8_t4096_h4096_e64_f1408"), ("gemv", "gemv_ar_r8_8x8192x3584"),
+                      ("emb", "emb_a2a_r8_t64_v65536_d128_b2048_l32")]:
+        d = ops.get(name)
+        if not d:
+            continue
+        out[key] = row(d)
+        if "interdecom_check" in d:
+            idc[key] = d["interdecom_check"]
+    d = ops.get("moe_r8_t4096_h4096_e64_f1408", {}).get("combine")
+    if d:  # [back to back, replayed from a CUDA graph, fraction]
+        out["combine"] = [sig(d["us"]), sig(d["graph_replay"].get("us")),
+                          sig(d["roofline_frac"], 3)]
+    d = ops.get("attn_r8_s4096_h8_d128")
+    if d:  # [full, causal, fraction of full]
+        out["attn"] = [sig(d["full"]["ms"] * 1e3), sig(d["causal"]["ms"] * 1e3),
+                       sig(d["full"]["roofline_frac"], 3)]
+    d = ops.get("gemm_rs_r2_256x256x128")
+    if d:  # [back to back, replayed from a CUDA graph]
+        out["rs_r2"] = [sig(d["plain_us"], 3), sig(d.get("graph_us"), 3)]
+    checks = {k: [v["model"]["c_star"], v["best_c"], int(v["c_star_within_10pct_of_best"])]
+              for k, v in idc.items()}
+    return out, checks
+
+
+def compact_phases(base, ops):
+    """Per fused GEMM: [epilogue busy fraction, MMA wait-on-epilogue fraction]."""
+    out = {}
+    src = [("rs", base or {}), ("ar", ops.get("gemm_ar_r8_8192x8192x3584", {})),
+           ("ag", ops.get("ag_gemm_r8_8192x3584x8192", {})),
+           ("moe", ops.get("moe_r8_t4096_h4096_e64_f1408", {}))]
+    for k, d in src:
+        ph = d.get("phases")
+        if ph:
+            out[k] = [sig(ph["epilogue_busy_frac"], 2), sig(ph["mma_wait_on_epilogue_frac"], 2)]
+    return out
 
 
 def run_fcc(args, world, rank, local, pg):
@@ -738,18 +932,27 @@ def run_fcc(args, world, rank, local, pg):
         del dA2, dB2, outs2
     del hA, hB, hO
 
+    clk = clocks.summary()
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic (seeded PCG64 normals rounded to bf16)",
-        "config": {"workload": WORKLOAD, "R": R, "M": M, "N": N, "K": K, "out": "bf16",
-                   "algo": "fused, ordered tile-owner accumulation",
-                   "l2": "inputs (940 MB) larger than L2; no flush",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "l2": "inputs>L2, no flush",
                    "parallelism": f"replicas{world}"},
-        "roofline": roofline, "e2e": e2e, "gpu_launches": launches,
-        "clocks": clocks.summary(),
+        "roofline": {k: roofline[k] for k in ("bound", "achieved", "peak", "unit", "frac",
+                                              "traffic")},
+        "e2e": None if e2e is None else {k: e2e[k] for k in (
+            "value", "unit", "h2d_bytes_per_step", "d2h_bytes_per_step")},
+        "gpu_launches": launches,
+        "clocks": {k: clk[k] for k in ("sm_mhz", "sm_max_mhz", "reasons", "samples")},
     }
+    # Everything, with the legs' paths and the full sweeps, for --details.
+    details = {"config": {"workload": WORKLOAD, "R": R, "M": M, "N": N, "K": K, "out": "bf16",
+                          "algo": "fused, ordered tile-owner accumulation",
+                          "l2": "inputs (940 MB) larger than L2; no flush",
+                          "data": "seeded PCG64 normals rounded to bf16"},
+               "roofline": roofline, "e2e": e2e, "clocks": dict(clk, source=clocks.source)}
 
     # ---- unfused baselines and cuBLAS on the same workload
     if not args.headline_only:
@@ -767,27 +970,62 @@ def run_fcc(args, world, rank, local, pg):
         base["cublas_stacked_gemm"] = {"ms": t, "TFLOP/s": flops / (t * 1e-3) / 1e12,
                                        "note": "one library GEMM of the same FLOPs, no collective"}
         del Acat, Bcat
-        base["interdecom_check"] = interdecom_check(fcc, R, M, N, K, dA, dB, outs, stream,
-                                                    base["unfused"]["ms"], pk)
-        line["baselines"] = base
-        line["ops"] = other_ops(fcc, torch, np, synth, dev, stream, dA, dB, pk)
-        line["ops"]["gemm_rs_r2_256x256x128"] = small_rs_latency(fcc, torch, np, synth, dev,
-                                                                 stream)
+        X_ms = (R * M * N * 4 + M * N * 2) / (pk["hbm_gbs"] * 1e9) * 1e3  # the reduce
+        base["phases"] = phase_fractions(torch, dev, lambda buf: fcc.fcc_gemm_rs(
+            R, dA, dB, outs, M, N, K, 0, 0, fcc.make_opts(phase_ns=buf), stream))
+        base["interdecom_check"] = interdecom_check(
+            lambda c: fcc.fcc_gemm_rs(R, dA, dB, outs, M, N, K, 0, 0,
+                                      fcc.make_opts(algo=fcc.FCC_ALGO_INTERDECOM, chunks=c),
+                                      stream),
+            (1, 2, 4, 8, 16, 32, 64), X_ms, base["unfused"]["ms"], 64, fcc, stream)
+        ops = other_ops(fcc, torch, np, synth, dev, stream, dA, dB, pk)
+        ops["gemm_rs_r2_256x256x128"] = small_rs_latency(fcc, torch, np, synth, dev, stream)
+        details["baselines"] = base
+        details["ops"] = ops
+        base["roofline_frac"] = roofline["frac"]
+        line["ops_us"], line["interdecom"] = compact_ops(base, ops, ms)
+        line["epilogue"] = compact_phases(base, ops)
 
     # ---- CPU oracle on a bounded sample (rank 0 only)
-    if rank == 0 and args.cpu_seconds <= 0:
-        print(json.dumps(line), flush=True)
-    elif rank == 0:
+    if rank == 0 and args.cpu_seconds > 0:
         got = [o.float().cpu().numpy().astype(np.float64) for o in outs]
         per_row, threads = oracle_seconds_per_row(A, B)
         rps = int(max(1, min(M // R, args.cpu_seconds / max(per_row * R, 1e-9))))
         v, secs, rows, chk = oracle_sample(A, B, R, M, rps, gpu_shards=got)
-        line["cpu_baseline"] = {
+        line["cpu_baseline"] = {"value": sig(v), "unit": "TFLOP/s", "cores": threads,
+                                "kind": "oracle", "sample": f"{rows} rows, {secs:.1f} s"}
+        details["cpu_baseline"] = {
             "value": v, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
             "sample": f"{rows} output rows ({rows // R} per shard, seeded choice), "
                       f"{secs:.1f} s of fp64 CPU work",
             "gpu_rows_rel_fro_err": chk}
-        print(json.dumps(line), flush=True)
+    if rank == 0:
+        emit(line, details, args.details)
+
+
+def emit(line, details, path):
+    """Print the one JSON line (the driver keeps the last 1500 characters of
+    the output, so optional keys give way first if it grows past 1490) and
+    write the full results to `path` if one is given."""
+    for k in ("value", "ms_per_step"):
+        line[k] = sig(line[k], 6)
+    for k in ("achieved", "frac"):
+        line["roofline"][k] = sig(line["roofline"][k], 5)
+    if line.get("e2e"):
+        line["e2e"]["value"] = sig(line["e2e"]["value"], 5)
+    text = json.dumps(line, separators=(",", ":"))
+    for drop in ("epilogue", "rs_r2", "combine", "attn", "emb"):
+        if len(text) <= 1490:
+            break
+        if drop in line:
+            line.pop(drop)
+        else:
+            line.get("ops_us", {}).pop(drop, None)
+        text = json.dumps(line, separators=(",", ":"))
+    if path:
+        with open(path, "w") as f:
+            json.dump(dict(details, line=line), f, indent=1)
+    print(text, flush=True)
 
 
 def main():

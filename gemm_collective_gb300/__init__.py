@@ -8,7 +8,8 @@ loads ``libfcc.so``; if the library has not been built the import fails
 loudly -- there is no fallback path.
 
 Pointer-array arguments accept a sequence of ``int`` device addresses or of
-objects with ``data_ptr()`` (torch tensors).  ``stream`` accepts ``None``
+objects with ``data_ptr()`` (torch tensors), or an array made once by
+``ptr_array()``.  ``stream`` accepts ``None``
 (the legacy default stream), an ``int`` handle or an object with a
 ``cuda_stream`` attribute (``torch.cuda.Stream``).
 """
@@ -48,14 +49,16 @@ class fcc_opts(ctypes.Structure):
         ("workspace", ctypes.c_void_p),
         ("workspace_bytes", ctypes.c_size_t),
         ("cta_pair", ctypes.c_int),
+        ("phase_ns", ctypes.c_void_p),
     ]
 
 
 def make_opts(algo=FCC_ALGO_AUTO, deterministic=1, chunks=0, max_ctas=0, timeout_ns=0,
-              workspace=None, workspace_bytes=0, cta_pair=0) -> fcc_opts:
+              workspace=None, workspace_bytes=0, cta_pair=0, phase_ns=None) -> fcc_opts:
     ws = workspace.data_ptr() if hasattr(workspace, "data_ptr") else workspace
+    ph = phase_ns.data_ptr() if hasattr(phase_ns, "data_ptr") else phase_ns
     return fcc_opts(algo, deterministic, chunks, max_ctas, timeout_ns, ws, workspace_bytes,
-                    cta_pair)
+                    cta_pair, ph)
 
 
 class FccError(RuntimeError):
@@ -123,8 +126,20 @@ def _addr(x) -> int:
 def _ptrs(seq):
     if seq is None:
         return None
+    if isinstance(seq, ctypes.Array):  # built once by ptr_array()
+        return seq
     vals = [_addr(x) for x in seq]
     return (ctypes.c_void_p * len(vals))(*vals)
+
+
+def ptr_array(seq):
+    """The C array of device pointers for a sequence of tensors (or addresses).
+
+    Every call accepts it wherever it takes a pointer array; a loop that calls
+    an operator on the same buffers again and again can build its arrays once
+    instead of marshalling the tensors on every call.  It holds addresses
+    only: the tensors must stay alive (and in place) while it is in use."""
+    return _ptrs(list(seq))
 
 
 def _stream(s) -> int:

@@ -529,9 +529,8 @@ fcc_status fcc_ring_attention(int R, const void* const* Q, const void* const* K,
   p.status = status;
   p.timeout_ns = timeout_ns;
 
-  if (cudaFuncSetAttribute(ring_attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           kSmem) != cudaSuccess)
-    return FCC_ERR_CUDA;
+  static bool attr_set[64] = {};
+  if (smem_attr_once(attr_set, ring_attention_kernel, kSmem) != cudaSuccess) return FCC_ERR_CUDA;
   const unsigned grid = static_cast<unsigned>(R * H * p.qpairs);
   ring_attention_kernel<<<grid, kThreads, kSmem, reinterpret_cast<cudaStream_t>(stream)>>>(p);
   if (cudaGetLastError() != cudaSuccess) return FCC_ERR_CUDA;

@@ -264,10 +264,8 @@ fcc_status fcc_moe_combine(int R, const void* const* recv_y, int64_t cap, int64_
   locate_kernel<<<static_cast<unsigned>((rows + 255) / 256), 256, 0, st>>>(a);
   // A persistent grid of the blocks that fit at once (warps loop over tokens).
   auto kern = a.in_f32 ? combine_kernel<true> : combine_kernel<false>;
-  int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 256, 0) != cudaSuccess)
-    per_sm = 4;
-  per_sm = std::max(per_sm, 1);
+  static int occ[2][64] = {};
+  const int per_sm = blocks_per_sm_once(occ[a.in_f32], kern, 256);
   const long long ntok = static_cast<long long>(R) * T;
   const long long blocks =
       std::min<long long>((ntok + 7) / 8, static_cast<long long>(sms) * per_sm);

@@ -254,10 +254,8 @@ fcc_status fcc_embedding_a2a(int R, int ntables, const void* const* tables, int6
 
   // A persistent grid of the warps that fit at once (each loops over bags).
   auto kern = algo == FCC_ALGO_FUSED ? embedding_kernel<false> : embedding_kernel<true>;
-  int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 256, 0) != cudaSuccess)
-    per_sm = 4;
-  per_sm = std::max(per_sm, 1);
+  static int occ[2][64] = {};
+  const int per_sm = blocks_per_sm_once(occ[algo == FCC_ALGO_FUSED ? 0 : 1], kern, 256);
   const long long bags = static_cast<long long>(R) * Bl * ntables;
   const long long blocks = std::min<long long>((bags + 7) / 8, static_cast<long long>(sms) * per_sm);
   kern<<<static_cast<unsigned>(std::max<long long>(1, blocks)), 256, 0, st>>>(a);

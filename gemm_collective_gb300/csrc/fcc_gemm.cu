@@ -315,6 +315,11 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) gemm_kernel(const __gri
   const uint32_t tmem_base = *tmem_slot;
   const ptx::Waiter W{abort_flag, p.status, p.timeout_ns};
   const int num_tiles = num_tiles_of<MODE>(p, tab);  // (after the barrier: tables loaded)
+  // Phase timing (optional): this CTA's span, its epilogue's busy time and
+  // its MMA warp's wait for an accumulator the epilogue still holds.
+  unsigned long long* const times = p.phase_ns != nullptr ? p.phase_ns + 4ull * blockIdx.x
+                                                          : nullptr;
+  const uint64_t t_begin = times != nullptr ? ptx::globaltimer() : 0;
 
   if (warp == 0 && gather) {
     // ----------------------------------------------- producer, gather mode
@@ -467,9 +472,12 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) gemm_kernel(const __gri
       uint32_t stage = 0, phase = 0;
       uint32_t acc = 0, acc_phase = 0;
       bool any = false, ok = true;
+      uint64_t waited = 0;
       for (int t = pair; t < num_tiles && ok; t += npairs) {
         const uint32_t idesc = narrow(tile_of<MODE, TM>(p, t, tab)) ? C::kIdescNarrow : C::kIdesc;
+        const uint64_t w0 = times != nullptr ? ptx::globaltimer() : 0;
         if (!W.wait(&tempty[acc], acc_phase ^ 1u)) break;
+        if (times != nullptr) waited += ptx::globaltimer() - w0;
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * kBN;
         for (int it = 0; it < k_iters; ++it) {
@@ -517,6 +525,7 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) gemm_kernel(const __gri
           ptx::mma_commit(mma_done);
         W.drain(mma_done, 0, kDrainNs);
       }
+      if (times != nullptr) times[2] = waited;
     }
   } else if (warp >= kGemmThreads / 32) {
     // ------------------------------------------- staging copy (grouped mode)
@@ -594,9 +603,12 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) gemm_kernel(const __gri
     const int row_in_tile = static_cast<int>(cta) * kBM + q * 32 + lane;  // row of the pair tile
     const uint32_t tempty_leader0 = kPair ? ptx::mapa(ptx::smem_addr(&tempty[0]), lead) : 0u;
     uint32_t acc = 0, acc_phase = 0;
+    uint64_t busy = 0;
+    int tiles_done = 0;
     for (int t = pair; t < num_tiles; t += npairs) {
       const Tile tl = tile_of<MODE, TM>(p, t, tab);
       const bool failed = !W.wait(&tfull[acc], acc_phase);
+      const uint64_t e0 = times != nullptr ? ptx::globaltimer() : 0;
       if constexpr (MODE == MODE_RS_PUSH || MODE == MODE_AR_PUSH) {
         // The four epilogue warps meet at named barriers below: stop together.
         if (ptx::named_barrier_or(1, 128, failed)) break;
@@ -719,8 +731,16 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) gemm_kernel(const __gri
           ptx::named_barrier_sync(1, 128);
         }
       }
+      if (times != nullptr) {
+        busy += ptx::globaltimer() - e0;
+        ++tiles_done;
+      }
       acc ^= 1u;
       if (acc == 0) acc_phase ^= 1u;
+    }
+    if (times != nullptr && warp == 2 && lane == 0) {
+      times[1] = busy;
+      times[3] = static_cast<unsigned long long>(tiles_done);
     }
   }
 
@@ -740,13 +760,17 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) gemm_kernel(const __gri
     else
       ptx::tmem_dealloc(tmem_base, kTmemCols);
   }
+  if (times != nullptr && threadIdx.x == 0) {
+    times[0] = ptx::globaltimer() - t_begin;
+    if (kPair && cta != 0) times[2] = 0;  // the peer issues no MMAs
+  }
 }
 
 template <int MODE, int CG, class P>
 cudaError_t launch_mode(const P& p, int grid, cudaStream_t st) {
   auto kern = gemm_kernel<MODE, CG, P>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       Cfg<CG>::kSmem);
+  static bool attr_set[64] = {};
+  cudaError_t e = smem_attr_once(attr_set, kern, Cfg<CG>::kSmem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid, 1, 1);

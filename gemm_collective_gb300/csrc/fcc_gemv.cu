@@ -302,8 +302,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemv_ar_kernel(const __grid_c
 int gemv_smem_bytes() { return kSmemBytes; }
 
 cudaError_t launch_gemv(const GemvParams& p, int grid, cudaStream_t st) {
-  cudaError_t e = cudaFuncSetAttribute(gemv_ar_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       kSmemBytes);
+  static bool attr_set[64] = {};
+  const cudaError_t e = smem_attr_once(attr_set, gemv_ar_kernel, kSmemBytes);
   if (e != cudaSuccess) return e;
   gemv_ar_kernel<<<grid, kGemmThreads, kSmemBytes, st>>>(p);
   return cudaGetLastError();

@@ -11,6 +11,34 @@
 
 namespace fcc {
 
+// Sets a kernel's dynamic shared-memory limit once per device (the attribute
+// belongs to the device's context) instead of on every launch; `done` is the
+// kernel's own flag array.  A failed attempt is retried on the next launch.
+template <class Kernel>
+cudaError_t smem_attr_once(bool (&done)[64], Kernel kern, int bytes) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = -1;
+  if (dev >= 0 && done[dev]) return cudaSuccess;
+  const cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && dev >= 0) done[dev] = true;
+  return e;
+}
+
+// Resident blocks per SM of `kern` with `threads` threads and no dynamic
+// shared memory, looked up once per device (`cache` is the kernel's own).
+template <class Kernel>
+int blocks_per_sm_once(int (&cache)[64], Kernel kern, int threads) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = -1;
+  if (dev >= 0 && cache[dev] > 0) return cache[dev];
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, threads, 0) != cudaSuccess || n < 1)
+    return 1;
+  if (dev >= 0) cache[dev] = n;
+  return n;
+}
+
 constexpr int kBM = 128;       // output tile rows (one TMEM lane per row)
 constexpr int kBK = 64;        // K per pipeline stage (128 bytes of bf16: one swizzle row)
 constexpr int kGemmThreads = 192;  // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
@@ -47,6 +75,7 @@ struct GemmParams {
   float* acc_ws;        // push mode with bf16 output: f32 accumulation rows (M x N)
   int* tickets;         // push mode with bf16 output: per (tile, CTA of the pair) counters
   int cg;               // host side: CTAs per cluster (1 or 2)
+  unsigned long long* phase_ns;  // NULL, or 4 per CTA: span, epilogue busy, MMA wait, tiles
 };
 
 struct GemvParams {
@@ -104,6 +133,7 @@ struct GroupedParams {
   int* ready;                          // [units]
   int* copy_cursor;                    // next chunk of rows to claim
   int stage_copy;
+  unsigned long long* phase_ns;        // NULL, or 4 per CTA (as GemmParams)
 };
 
 // cg = 1: one CTA per 128 x 256 tile; cg = 2: a CTA pair (cluster of 2) per

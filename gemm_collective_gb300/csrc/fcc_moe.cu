@@ -682,6 +682,7 @@ fcc_status fcc_moe_dispatch_gemm(int R, const void* const* X, const float* const
   g.e_hi = E;
   g.status = status;
   g.timeout_ns = timeout_ns;
+  g.phase_ns = opts != nullptr ? reinterpret_cast<unsigned long long*>(opts->phase_ns) : nullptr;
   g.gather = gather ? 1 : 0;
   if (copy_in_gemm) {
     for (int r = 0; r < R; ++r) {

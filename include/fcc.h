@@ -95,6 +95,16 @@ typedef struct {
    * memory (no multicast loads), so the library may run in processes that
    * drive several GPUs. */
   int cta_pair;
+  /* Phase timing, for profiling: NULL (the default), or a device array of
+   * 4 uint64 per CTA of the grid (at most the SM count) that the tensor-core
+   * GEMM kernels (RS, AR, AG, their unfused GEMMs and the MoE expert GEMM)
+   * fill from %globaltimer, for the call's last GEMM launch: [0] ns from the
+   * CTA's start to its end, [1] ns its epilogue warps spent on tiles (from an
+   * accumulator becoming ready to its last store issued), [2] ns its MMA
+   * warp waited for an accumulator the epilogue had not yet handed back (the
+   * part of the epilogue not hidden behind the next tile's MMAs; 0 on the
+   * second CTA of a pair, which issues no MMAs), [3] tiles it stored. */
+  uint64_t *phase_ns;
 } fcc_opts;
 
 /* Operator identifiers for fcc_workspace_size. */

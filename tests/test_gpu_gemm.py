@@ -164,6 +164,29 @@ def test_single_ctas_match_pairs_bitwise(R, M, N, K):
         assert_close(to_f64(two[j]), oracle.gemm_rs(A, B, j), f"shard {j}")
 
 
+@pytest.mark.parametrize("pair,ctas", [(1, 8), (2, 8)])
+def test_phase_timing_stamps(pair, ctas):
+    """opts.phase_ns: every CTA records its span, its epilogue's busy time (at
+    most the span), its MMA warp's wait for the epilogue and its tiles; the
+    tiles add up to the launch's work items (a pair's two CTAs each store half
+    of every tile), and the results are unchanged."""
+    R, M, N, K = 2, 1024, 1024, 128
+    A, B = synth.integer_gemm_inputs(R, M, N, K, -4, 4, seed=41)
+    dA, dB = _upload(A, B)
+    buf = torch.zeros(4 * 64, dtype=torch.int64, device="cuda")
+    outs = _rs(R, dA, dB, M, N, K, fcc.FCC_F32,
+               fcc.make_opts(cta_pair=pair, max_ctas=ctas, phase_ns=buf))
+    for j in range(R):
+        assert np.array_equal(to_f64(outs[j]), oracle.gemm_rs(A, B, j))
+    t = buf.view(-1, 4).cpu().numpy()
+    used = t[:ctas]
+    assert np.all(t[ctas:] == 0), "stamps beyond the grid"
+    assert np.all(used[:, 0] > 0)
+    assert np.all(used[:, 1] <= used[:, 0]) and np.all(used[:, 2] <= used[:, 0])
+    tiles = (M // (128 * pair)) * (N // 256)
+    assert used[:, 3].sum() == tiles * pair
+
+
 def test_rank_permutation_within_tolerance():
     R, M, N, K = 4, 256, 512, 128
     A, B = synth.gemm_inputs(R, M, N, K, 1.0, 1.0, seed=5)
