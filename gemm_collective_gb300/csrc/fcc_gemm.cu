@@ -63,9 +63,13 @@ constexpr uint64_t kDrainNs = 50ull * 1000 * 1000;  // unwinding limit after an 
 constexpr int kTabInts = 4 * FCC_MAX_EXPERTS + 2;
 constexpr int kCopyRows = 4;  // rows per claimed chunk of the in-kernel staging copy
 
+constexpr int kLoadLag = 3;   // cp.async groups a loader lane keeps in flight before signalling
+
 template <int MODE>
 constexpr int threads_of() {
-  return MODE == MODE_GROUPED ? kGemmThreads + 32 * kCopyWarps : kGemmThreads;
+  return MODE == MODE_GROUPED
+             ? kGemmThreads + 32 * (kCopyWarps > kLoadWarps ? kCopyWarps : kLoadWarps)
+             : kGemmThreads;
 }
 
 // CG = CTAs per cluster: 1 (one CTA per 128x256 tile) or 2 (a CTA pair per
@@ -259,14 +263,19 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) gemm_kernel(const __gri
   const int pair = blockIdx.x / CG;
   const int npairs = gridDim.x / CG;
 
-  // Gather mode (MoE without a staged copy): the producer warp fetches the A
-  // rows from the source tokens with TMA gather4.
-  bool gather = false;
-  if constexpr (MODE == MODE_GROUPED) gather = p.gather != 0;
+  // Gather modes (MoE without a staged copy): the producer warp fetches the A
+  // rows from the source tokens with TMA gather4 (gather), or the loader
+  // warps do with cp.async while the producer loads only B (lsu).
+  bool gather = false, lsu = false;
+  if constexpr (MODE == MODE_GROUPED) {
+    gather = p.gather == 1;
+    lsu = p.gather == 2;
+  }
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      ptx::mbar_init(&full[s], 1);
+      // lsu: the producer's arrive plus one per loader lane of the pair's CTAs
+      ptx::mbar_init(&full[s], lsu ? 1 + 32 * kLoadWarps * C::kPairCtas : 1);
       ptx::mbar_init(&empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -407,7 +416,8 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) gemm_kernel(const __gri
         a_row += static_cast<int>(cta) * kBM;                 // this CTA's half of the rows
         const int bn_cta = narrow(tl) ? C::kBNcta / 2 : C::kBNcta;  // B columns of this CTA
         const int b_col = col_base(tl) + static_cast<int>(cta) * bn_cta;
-        const uint32_t stage_bytes = kABytes + static_cast<uint32_t>(bn_cta) * kBK * 2;
+        // (lsu: the A rows arrive by the loader warps' cp.async, not counted in bytes)
+        const uint32_t stage_bytes = (lsu ? 0u : kABytes) + static_cast<uint32_t>(bn_cta) * kBK * 2;
         if constexpr (MODE == MODE_GROUPED) {
           if (p.stage_copy) {
             // The unit's rows are written by the copy warps (of any CTA):
@@ -436,12 +446,12 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) gemm_kernel(const __gri
             // Both CTAs' bytes are counted on the leader's full barrier.
             const uint32_t bar = ptx::mapa(ptx::smem_addr(&full[stage]), lead);
             if (cta == 0) ptx::mbar_arrive_expect_tx(&full[stage], 2 * stage_bytes);
-            ptx::tma_load_2d_pair(a_dst, ma, bar, kb * kBK, a_row);
+            if (!lsu) ptx::tma_load_2d_pair(a_dst, ma, bar, kb * kBK, a_row);
             for (int i = 0; i < bn_cta / 64; ++i)
               ptx::tma_load_2d_pair(b_dst + i * kBBoxBytes, mb, bar, b_col + 64 * i, kb * kBK);
           } else {
             ptx::mbar_arrive_expect_tx(&full[stage], stage_bytes);
-            ptx::tma_load_2d(a_dst, ma, &full[stage], kb * kBK, a_row);
+            if (!lsu) ptx::tma_load_2d(a_dst, ma, &full[stage], kb * kBK, a_row);
             for (int i = 0; i < bn_cta / 64; ++i)
               ptx::tma_load_2d(b_dst + i * kBBoxBytes, mb, &full[stage], b_col + 64 * i,
                                kb * kBK);
@@ -527,10 +537,81 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) gemm_kernel(const __gri
       }
       if (times != nullptr) times[2] = waited;
     }
+  } else if (warp >= kGemmThreads / 32 && lsu) {
+    // ------------------------------------------ A-row loaders (grouped, lsu)
+    // Lane l of loader warp w owns row 32w + l of this CTA's 128 A rows: per
+    // stage it copies that row's 64 k (128 bytes, eight 16-byte requests) from
+    // its source token into the stage, at the chunk positions a 128-byte
+    // swizzled TMA box would use (chunk c of row r at c ^ (r mod 8)); rows
+    // past the tile's count and k past H are zero-filled.  A lane signals a
+    // stage kLoadLag stages later: it waits for that stage's copies, makes
+    // them visible to the tensor core's async proxy, and arrives on the pair
+    // leader's full barrier (which also counts the producer's B bytes).
+    if constexpr (MODE == MODE_GROUPED) {
+      const int r_local = (warp - kGemmThreads / 32) * 32 + lane;
+      const uint32_t sw = static_cast<uint32_t>(r_local & 7);
+      const uint32_t full0 =
+          kPair ? ptx::mapa(ptx::smem_addr(&full[0]), lead) : ptx::smem_addr(&full[0]);
+      uint32_t stage = 0, phase = 0;
+      // Stages committed but not yet signalled: the npend stages before `stage`.
+      int npend = 0;
+      auto signal_oldest = [&]() {
+        const uint32_t old = (stage + kStages - static_cast<uint32_t>(npend)) % kStages;
+        ptx::fence_proxy_async_smem();
+        if constexpr (kPair)
+          ptx::mbar_arrive_cluster(full0 + old * 8);
+        else
+          ptx::mbar_arrive(&full[old]);
+        --npend;
+      };
+      bool ok = true;
+      for (int t = pair; t < num_tiles && ok; t += npairs) {
+        const Tile tl = tile_of<MODE, TM>(p, t, tab);
+        const int local = static_cast<int>(cta) * kBM + r_local;
+        const char* src = nullptr;
+        if (local < tl.rows) {
+          const int sidx = __ldcg(p.recv_src[tl.shard] + tl.row0 + local);
+          const int s = sidx / p.T;
+          src = static_cast<const char*>(p.src_x[s]) +
+                static_cast<long long>(sidx - s * p.T) * p.K * 2;
+        }
+        for (int it = 0; it < k_iters; ++it) {
+          int good = 1;
+          if (lane == 0) good = W.wait(&empty[stage], phase ^ 1u) ? 1 : 0;
+          if (!__shfl_sync(0xffffffffu, good, 0)) {
+            ok = false;
+            break;
+          }
+          const uint32_t row_dst = ptx::smem_addr(sA + stage * kABytes) + r_local * 128;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const int k = it * kBK + c * 8;
+            const bool in = src != nullptr && k < p.K;  // (K % 8 == 0: whole chunks)
+            ptx::cp_async_16(row_dst + ((static_cast<uint32_t>(c) ^ sw) << 4),
+                             in ? static_cast<const void*>(src + k * 2) : p.src_x[0],
+                             in ? 16u : 0u);
+          }
+          ptx::cp_async_commit();
+          ++npend;
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+          if (npend > kLoadLag) {
+            ptx::cp_async_wait<kLoadLag>();
+            signal_oldest();
+          }
+        }
+      }
+      // Every copy lands before this CTA can exit (its shared memory is freed
+      // then); the stages still owed a signal get it.
+      ptx::cp_async_wait<0>();
+      while (npend > 0) signal_oldest();
+    }
   } else if (warp >= kGemmThreads / 32) {
     // ------------------------------------------- staging copy (grouped mode)
     if constexpr (MODE == MODE_GROUPED) {
-      if (p.stage_copy) {
+      if (p.stage_copy && warp < kGemmThreads / 32 + kCopyWarps) {
         const int* rows_t = tab + p.E + 1;
         const int* base_t = tab + 2 * p.E + 1;
         int* cstart = tab + 3 * p.E + 1;  // chunks of experts before e, from e_lo

@@ -3,13 +3,12 @@
 // The MoE Dispatch + GEMM kernel of the mKernel article's fused-kernel list
 // (and the GEMM + All-to-All operator for MoE in the SC24 paper's abstract),
 // over R virtual ranks in one GPU:
-//   1. route_kernel   one warp per token: top-k experts by logit (ties to the
-//                     lower index, found with warp shuffles), softmax gates,
-//                     and a per-chunk expert histogram (chunk = 128 tokens of
-//                     one source rank).
-//   2. scan_kernel    one CTA per expert: exclusive prefix of its histogram
-//                     over the chunks (a fixed order) and its count;
-//      finalize_kernel  send counts, each expert's first row in its receiving
+//   1. route_kernel   one thread per token: top-k experts by logit (ties to
+//                     the lower index), softmax gates, and a per-chunk expert
+//                     histogram (chunk = 128 tokens of one source rank).
+//   2. offsets_kernel one CTA: for every expert the exclusive prefix of its
+//                     histogram over the chunks (a fixed order) and its count;
+//                     send counts, each expert's first row in its receiving
 //                     rank's buffer, and the grouped GEMM's tile table.
 //   3. rank_kernel    one CTA per chunk: the stable rank of every assignment
 //                     within its expert (warp match + popc, then a prefix over
@@ -83,121 +82,102 @@ struct MoeArgs {
   int* status;
 };
 
-struct Cand {
-  float v;
-  int i;
-};
+// Grid: one CTA per chunk of 128 tokens (of one source rank), one token per
+// thread.  The chunk's logits are first staged in shared memory with
+// coalesced loads (rows padded to 65 words, so the threads reading their own
+// rows hit 32 different banks); each thread then scans its token's E logits
+// once for the top-k (a strictly larger logit replaces, so an equal logit
+// keeps the lower expert index), and once more for the softmax denominator
+// relative to the largest logit (four partial sums in a fixed order).  The
+// per-chunk expert histogram is counted in shared memory.
+constexpr int kRoutePad = FCC_MAX_EXPERTS + 1;
 
-// a ranks before b: larger logit, or equal logit and lower expert index.
-__device__ __forceinline__ bool better(const Cand& a, const Cand& b) {
-  return a.v > b.v || (a.v == b.v && a.i < b.i);
-}
-
-__device__ __forceinline__ Cand warp_best(Cand c) {
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
-    Cand o;
-    o.v = __shfl_xor_sync(0xffffffffu, c.v, off);
-    o.i = __shfl_xor_sync(0xffffffffu, c.i, off);
-    if (better(o, c)) c = o;
-  }
-  return c;
-}
-
-__device__ __forceinline__ float warp_sum(float x) {
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
-  return x;
-}
-
-// Grid: one CTA per chunk, 1024 threads (32 warps, one token at a time each).
-__global__ void __launch_bounds__(1024) route_kernel(const MoeArgs a) {
+__global__ void __launch_bounds__(kChunkTok) route_kernel(const MoeArgs a) {
+  __shared__ float lg[kChunkTok * kRoutePad];
   __shared__ int hist[FCC_MAX_EXPERTS];
   const int chunk = blockIdx.x;
   const int s = chunk / a.chunks_per_rank;
   const int t0 = (chunk - s * a.chunks_per_rank) * kChunkTok;
-  const int t1 = min(a.T, t0 + kChunkTok);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n = min(a.T - t0, kChunkTok);
+  const int E = a.E;
   if (threadIdx.x < FCC_MAX_EXPERTS) hist[threadIdx.x] = 0;
+  const float* src = a.logits[s] + static_cast<long long>(t0) * E;
+  for (int i = threadIdx.x; i < n * E; i += blockDim.x) {
+    const int t = i / E;
+    lg[t * kRoutePad + (i - t * E)] = __ldcs(src + i);
+  }
   __syncthreads();
-  const float neg_inf = __int_as_float(0xff800000);
-  for (int t = t0 + warp; t < t1; t += 32) {
-    const float* lg = a.logits[s] + static_cast<long long>(t) * a.E;
-    const float l0 = lane < a.E ? lg[lane] : neg_inf;
-    const float l1 = lane + 32 < a.E ? lg[lane + 32] : neg_inf;
-    // candidates this lane holds; experts past E carry index E (never chosen)
-    Cand c0{l0, lane < a.E ? lane : a.E};
-    Cand c1{l1, lane + 32 < a.E ? lane + 32 : a.E};
-    Cand best = better(c1, c0) ? c1 : c0;
-    const Cand first = warp_best(best);
-    // softmax denominator over all E experts, relative to the largest logit
-    float ex = 0.f;
-    if (lane < a.E) ex += expf(l0 - first.v);
-    if (lane + 32 < a.E) ex += expf(l1 - first.v);
-    const float den = warp_sum(ex);
-    Cand picked[2] = {first, first};
+  const int i = threadIdx.x;
+  if (i < n) {
+    const float* row = lg + i * kRoutePad;
+    // top-2 by value, equal values to the lower index (slot 1 unused if topk = 1)
+    float v0 = row[0], v1 = __int_as_float(0xff800000);
+    int i0 = 0, i1 = E;
+    for (int e = 1; e < E; ++e) {
+      const float x = row[e];
+      if (x > v0) {
+        v1 = v0;
+        i1 = i0;
+        v0 = x;
+        i0 = e;
+      } else if (x > v1 || i1 == E) {
+        v1 = x;
+        i1 = e;
+      }
+    }
+    float sum[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int e = 0; e < E; ++e) sum[e & 3] += expf(row[e] - v0);
+    const float den = (sum[0] + sum[1]) + (sum[2] + sum[3]);
+    const int t = t0 + i;
+    const long long o = static_cast<long long>(t) * a.topk;
+    a.idx[s][o] = i0;
+    a.gate[s][o] = 1.0f / den;  // exp(v0 - v0) = 1
+    atomicAdd(&hist[i0], 1);    // a count: order does not matter
     if (a.topk > 1) {
-      if (c0.i == first.i) c0.v = neg_inf, c0.i = a.E;
-      if (c1.i == first.i) c1.v = neg_inf, c1.i = a.E;
-      best = better(c1, c0) ? c1 : c0;
-      picked[1] = warp_best(best);
-    }
-    if (lane < a.topk) {
-      const Cand c = picked[lane];
-      a.idx[s][static_cast<long long>(t) * a.topk + lane] = c.i;
-      a.gate[s][static_cast<long long>(t) * a.topk + lane] = expf(c.v - first.v) / den;
-      atomicAdd(&hist[c.i], 1);  // a count: order does not matter
+      a.idx[s][o + 1] = i1;
+      a.gate[s][o + 1] = expf(v1 - v0) / den;
+      atomicAdd(&hist[i1], 1);
     }
   }
   __syncthreads();
-  if (threadIdx.x < a.E)
-    a.chunk_counts[static_cast<long long>(chunk) * a.E + threadIdx.x] = hist[threadIdx.x];
+  if (threadIdx.x < E)
+    a.chunk_counts[static_cast<long long>(chunk) * E + threadIdx.x] = hist[threadIdx.x];
 }
 
-// One CTA per expert e (256 threads): exclusive prefix of expert e's histogram
-// over the chunks, in chunk order (source rank, then token), so chunk_off[c][e]
-// is the number of assignments to e that precede chunk c in (s, t, slot)
-// order.  Integer sums in a fixed tree of warp shuffles: the result does not
-// depend on any scheduling.
-__global__ void __launch_bounds__(256) scan_kernel(const MoeArgs a) {
-  __shared__ int warp_tot[8];
-  __shared__ int carry_s;
-  const int e = blockIdx.x;
-  const int nchunks = a.R * a.chunks_per_rank;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (threadIdx.x == 0) carry_s = 0;
-  __syncthreads();
-  for (int c0 = 0; c0 < nchunks; c0 += 256) {
-    const int c = c0 + threadIdx.x;
-    const int v = c < nchunks ? a.chunk_counts[static_cast<long long>(c) * a.E + e] : 0;
-    int incl = v;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, incl, off);
-      if (lane >= off) incl += y;
-    }
-    if (lane == 31) warp_tot[warp] = incl;
-    __syncthreads();
-    int before = carry_s;
-    for (int w = 0; w < warp; ++w) before += warp_tot[w];
-    if (c < nchunks) a.chunk_off[static_cast<long long>(c) * a.E + e] = before + incl - v;
-    __syncthreads();
-    if (threadIdx.x == 255) carry_s = before + incl;
-    __syncthreads();
-  }
-  if (threadIdx.x == 0) a.expert_counts[e] = carry_s;
-}
-
-// One CTA of 64 threads after the scan: each expert's first row in its
-// receiving rank's buffer and its kept rows (capacity), the send counts and the
-// grouped GEMM's tile table.
-__global__ void __launch_bounds__(64) finalize_kernel(const MoeArgs a) {
+// One CTA of 1024 threads after the router: for every expert the exclusive
+// prefix of its histogram over the chunks, in chunk order (source rank, then
+// token), so chunk_off[c][e] is the number of assignments to e that precede
+// chunk c in (s, t, slot) order (warp w scans experts w and w + 32, 32 chunks
+// per step, integer sums in a fixed shuffle order); then each expert's first
+// row in its receiving rank's buffer and its kept rows (capacity), the send
+// counts and the grouped GEMM's tile table.
+__global__ void __launch_bounds__(1024) offsets_kernel(const MoeArgs a) {
   __shared__ int counts[FCC_MAX_EXPERTS];
   __shared__ int rows[FCC_MAX_EXPERTS];
-  const int e = threadIdx.x;
+  __shared__ int units_s;
   const int nchunks = a.R * a.chunks_per_rank;
-  if (e < a.E) counts[e] = a.expert_counts[e];
-  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int e = warp; e < a.E; e += 32) {
+    int carry = 0;
+    for (int c0 = 0; c0 < nchunks; c0 += 32) {
+      const int c = c0 + lane;
+      const int v = c < nchunks ? a.chunk_counts[static_cast<long long>(c) * a.E + e] : 0;
+      int incl = v;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += y;
+      }
+      if (c < nchunks) a.chunk_off[static_cast<long long>(c) * a.E + e] = carry + incl - v;
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) {
+      counts[e] = carry;
+      a.expert_counts[e] = carry;
+    }
+  }
+  __syncthreads();  // (also orders this CTA's chunk_off writes before the reads below)
+  const int e = threadIdx.x;
   if (e < a.E) {
     const int d = e / a.Eloc;
     long long base = 0;
@@ -224,21 +204,32 @@ __global__ void __launch_bounds__(64) finalize_kernel(const MoeArgs a) {
     a.send_counts[e] = sum;
   }
   __syncthreads();
-  if (e == 0) {
-    int acc = 0;
-    for (int f = 0; f < a.E; ++f) {
-      a.tile_start[f] = acc;
-      acc += ((rows[f] + a.tile_m - 1) / a.tile_m) * a.tiles_n;
+  if (warp == 0) {
+    // tile_start: exclusive prefix of the experts' tiles, two experts a lane
+    const int ea = 2 * lane, eb = 2 * lane + 1;
+    const int ta = ea < a.E ? ((rows[ea] + a.tile_m - 1) / a.tile_m) * a.tiles_n : 0;
+    const int tb = eb < a.E ? ((rows[eb] + a.tile_m - 1) / a.tile_m) * a.tiles_n : 0;
+    int incl = ta + tb;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += y;
     }
-    a.tile_start[a.E] = acc;
-    counts[0] = acc / a.tiles_n;  // (m tile units in all)
+    const int excl = incl - ta - tb;
+    if (ea < a.E) a.tile_start[ea] = excl;
+    if (eb < a.E) a.tile_start[eb] = excl + ta;
+    const int total = __shfl_sync(0xffffffffu, incl, 31);
+    if (lane == 0) {
+      a.tile_start[a.E] = total;
+      units_s = total / a.tiles_n;  // (m tile units in all)
+    }
   }
   // The in-kernel staging counters start at zero for every call.
   if (a.ready != nullptr) {
     __syncthreads();
-    const int units = counts[0];
-    for (int u = e; u < units; u += blockDim.x) a.ready[u] = 0;
-    if (e == 0) *a.copy_cursor = 0;
+    const int units = units_s;
+    for (int u = threadIdx.x; u < units; u += blockDim.x) a.ready[u] = 0;
+    if (threadIdx.x == 0) *a.copy_cursor = 0;
   }
 }
 
@@ -375,7 +366,7 @@ __global__ void __launch_bounds__(256) copy_expert_rows_kernel(const MoeArgs a, 
   }
 }
 
-// Copy-engine dispatch, step 1 (one CTA of 64 threads, after finalize_kernel):
+// Copy-engine dispatch, step 1 (one CTA of 64 threads, after offsets_kernel):
 // the (source rank, expert) runs.  Source s's assignments to expert e are, in
 // both orders, one contiguous run: rows srcoff[s][e] .. srcoff[s + 1][e] of
 // e's receive rows (receive order is (expert, s, t, slot)), and, packed on
@@ -595,13 +586,17 @@ fcc_status fcc_moe_dispatch_gemm(int R, const void* const* X, const float* const
   const bool interdecom = algo == FCC_ALGO_INTERDECOM;
   const bool ce = algo == FCC_ALGO_CE;
   const bool unfused = algo == FCC_ALGO_UNFUSED;
-  const bool stage_ws = !gather && recv_x == nullptr;
-  // AUTO / FUSED: the rows are moved by the GEMM's own copy warps (or, for
-  // FUSED with one source array, gathered by its TMA).  The baselines move
-  // them first: UNFUSED with one copy kernel, INTERDECOM with one copy kernel
-  // per expert range on a side stream ahead of that range's GEMM, CE with the
-  // copy engines.
-  const bool copy_in_gemm = !gather && !unfused && !interdecom && !ce;
+  // AUTO / FUSED: with no recv_x asked for, the GEMM's loader warps gather
+  // each tile's rows from the source tokens into shared memory (lsu); with a
+  // recv_x, its copy warps write the rows there and the tensor cores read
+  // them back by TMA; FUSED with one source array gathers by TMA gather4.
+  // The baselines move the rows first: UNFUSED with one copy kernel,
+  // INTERDECOM with one copy kernel per expert range on a side stream ahead
+  // of that range's GEMM, CE with the copy engines.
+  const bool baseline = unfused || interdecom || ce;
+  const bool lsu = !gather && !baseline && recv_x == nullptr;
+  const bool stage_ws = !gather && !lsu && recv_x == nullptr;
+  const bool copy_in_gemm = !gather && !lsu && !baseline;
   const MoePlan plan = moe_plan(R, T, E, topk, H, cap, stage_ws, ce);
   void* ws = nullptr;
   int* status = nullptr;
@@ -658,6 +653,8 @@ fcc_status fcc_moe_dispatch_gemm(int R, const void* const* X, const float* const
   for (int d = 0; d < R; ++d) {
     if (gather)
       s = d == 0 ? internal_make_map(&g.mapA[0], X[0], R * T, H, 1) : FCC_OK;
+    else if (lsu)  // (unused by the kernel; a valid map all the same)
+      s = internal_make_map(&g.mapA[d], X[d], T, H, kBM);
     else
       s = internal_make_map(&g.mapA[d], a.recv_x[d], cap, H, kBM);
     if (s != FCC_OK) return s;
@@ -683,7 +680,11 @@ fcc_status fcc_moe_dispatch_gemm(int R, const void* const* X, const float* const
   g.status = status;
   g.timeout_ns = timeout_ns;
   g.phase_ns = opts != nullptr ? reinterpret_cast<unsigned long long*>(opts->phase_ns) : nullptr;
-  g.gather = gather ? 1 : 0;
+  g.gather = gather ? 1 : (lsu ? 2 : 0);
+  if (lsu) {
+    for (int r = 0; r < R; ++r) g.src_x[r] = X[r];
+    g.T = static_cast<int>(T);
+  }
   if (copy_in_gemm) {
     for (int r = 0; r < R; ++r) {
       g.src_x[r] = X[r];
@@ -695,12 +696,11 @@ fcc_status fcc_moe_dispatch_gemm(int R, const void* const* X, const float* const
     g.stage_copy = 1;
   }
 
-  route_kernel<<<plan.nchunks, 1024, 0, st>>>(a);
-  scan_kernel<<<E, 256, 0, st>>>(a);
-  finalize_kernel<<<1, 64, 0, st>>>(a);
+  route_kernel<<<plan.nchunks, kChunkTok, 0, st>>>(a);
+  offsets_kernel<<<1, 1024, 0, st>>>(a);
   rank_kernel<<<plan.nchunks, 256, 0, st>>>(a);
   if (cudaGetLastError() != cudaSuccess) return FCC_ERR_CUDA;
-  uint64_t launches = 4;
+  uint64_t launches = 3;
   const int grid = std::max(cg, (sms / cg) * cg);
 
   if (interdecom) {
@@ -782,7 +782,8 @@ fcc_status fcc_moe_dispatch_gemm(int R, const void* const* X, const float* const
   } else {
     // With the gather the copy (only for a requested recv_x) runs beside the
     // GEMM on a side stream: both only read what the dispatch kernels wrote.
-    const bool copy = !gather || recv_x != nullptr;
+    // The loader warps' gather (lsu) needs no copy at all.
+    const bool copy = (!gather && !lsu) || recv_x != nullptr;
     const bool side_copy = copy && gather;
     cudaStream_t side = nullptr;
     cudaEvent_t ev[2] = {};
