@@ -349,12 +349,14 @@ def interdecom_check(run, chunk_counts, X_ms, unfused_ms, maxc, fcc, stream, ste
 
     run(c) makes one call with c chunks.  Model inputs from this run's
     measurements: X = the movement's bytes at the measured copy bandwidth, G =
-    the unfused time minus X, alpha = what one chunk adds beyond G + X
-    (T(1) - G - X).  Reports whether the model's c* lands within 10 % of the
-    sweep's best time."""
+    the unfused time minus X, alpha = the marginal cost of one more chunk,
+    read off the two largest chunk counts swept, where the chunks' overhead
+    dominates (T(c_max) - T(c_prev)) / (c_max - c_prev).  Reports whether the
+    model's c* lands within 10 % of the sweep's best time."""
     sweep = {c: time_calls(lambda c=c: run(c), steps, 2, stream) for c in chunk_counts}
     G = max(unfused_ms - X_ms, 1e-3)
-    alpha = max(sweep[chunk_counts[0]] - G - X_ms, 1e-4)
+    c_hi, c_lo = chunk_counts[-1], chunk_counts[-2]
+    alpha = max((sweep[c_hi] - sweep[c_lo]) / (c_hi - c_lo), 1e-4)
     c_star = fcc.fcc_interdecom_chunks(G, X_ms, alpha, maxc)
     t_star = sweep[c_star] if c_star in sweep else time_calls(lambda: run(c_star), steps, 2,
                                                               stream)
@@ -808,7 +810,14 @@ def run_fcc(args, world, rank, local, pg):
 
     if args.op is not None:
         # One operator leg alone (no headline, no baselines).
-        if args.op == "gemm_rs_r2_256x256x128":
+        if args.op == WORKLOAD:
+            t = time_calls(step, 20, 5, stream)
+            Acat = torch.cat([a.view(torch.bfloat16) for a in dA], dim=1)
+            Bcat = torch.cat([b.view(torch.bfloat16) for b in dB], dim=0)
+            tb = time_calls(lambda: torch.matmul(Acat, Bcat), 20, 5, stream)
+            res = {"fused": {"ms": t, "TFLOP/s": flops / (t * 1e-3) / 1e12},
+                   "cublas_stacked_gemm": {"ms": tb, "TFLOP/s": flops / (tb * 1e-3) / 1e12}}
+        elif args.op == "gemm_rs_r2_256x256x128":
             res = small_rs_latency(fcc, torch, np, synth, dev, stream)
         elif args.op == "gemv_size_scan":
             res = gemv_size_scan(fcc, torch, np, synth, dev, stream, pk)

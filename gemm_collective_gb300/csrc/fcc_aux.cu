@@ -21,6 +21,8 @@ struct ReduceArgs {
 // Each thread sums 8 consecutive columns of one row over the R partials,
 // in rank order 0..R-1, and stores them (f32 or bf16).
 __global__ void __launch_bounds__(256) reduce_shards_kernel(const ReduceArgs a) {
+  ptx::griddep_wait();  // launched with programmatic stream serialization
+  ptx::griddep_launch_dependents();
   const long long groups_per_row = a.N / 8;
   const long long total = (a.row_end - a.row_begin) * groups_per_row;
   for (long long g = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; g < total;
@@ -67,6 +69,8 @@ struct GatherArgs {
 
 // dst rows [row_begin, row_end) of [X_0; X_1; ...] with 16-byte copies (K % 8 == 0).
 __global__ void __launch_bounds__(256) gather_rows_kernel(const GatherArgs a) {
+  ptx::griddep_wait();  // launched with programmatic stream serialization
+  ptx::griddep_launch_dependents();
   const long long vec_per_row = a.K / 8;
   const long long per_shard = a.Ms * vec_per_row;
   const long long first = a.row_begin * vec_per_row;
@@ -124,9 +128,9 @@ cudaError_t launch_reduce_shards(const float* const* P, int R, void* const* out,
   long long blocks = (work + 255) / 256;
   const long long cap = static_cast<long long>(sms) * 8;
   if (blocks > cap) blocks = cap;
-  reduce_shards_kernel<<<static_cast<int>(blocks), 256, 0, st>>>(a);
   bump_launch_count(1);
-  return cudaGetLastError();
+  return launch_pdl(reduce_shards_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st, 1u,
+                    a);
 }
 
 cudaError_t launch_gather_rows(const void* const* X, int R, int64_t Ms, int64_t K, void* dst,
@@ -151,9 +155,9 @@ cudaError_t launch_gather_rows_range(const void* const* X, int R, int64_t Ms, in
   long long blocks = (work + 255) / 256;
   const long long cap = static_cast<long long>(sms) * 8;
   if (blocks > cap) blocks = cap;
-  gather_rows_kernel<<<static_cast<int>(blocks), 256, 0, st>>>(a);
   bump_launch_count(1);
-  return cudaGetLastError();
+  return launch_pdl(gather_rows_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st, 1u,
+                    a);
 }
 
 cudaError_t launch_wait_probe(int* status, unsigned long long timeout_ns, cudaStream_t st) {

@@ -4,7 +4,8 @@
 // The direction back to the token owners of the SC24 paper's GEMM + All-to-All
 // operator for MoE: token t of source rank s collects the expert outputs of
 // its top-k assignments from the receiving ranks and adds them, each scaled by
-// its gate.  Two kernels:
+// its gate.  Three kernels:
+//   0. clear_loc_kernel  loc[*] = -1.
 //   1. locate_kernel  one thread per receive row (rank d, row i): the row's
 //                     expert from the prefix of d's local expert counts, its
 //                     token from recv_src, its slot from the token's top-k
@@ -40,7 +41,19 @@ struct CombineArgs {
   int in_f32, out_f32;
 };
 
+// loc[*] = -1 (a slot stays -1 unless locate_kernel finds its row).
+__global__ void __launch_bounds__(256) clear_loc_kernel(const CombineArgs a) {
+  ptx::griddep_wait();  // launched with programmatic stream serialization
+  ptx::griddep_launch_dependents();
+  const long long n = static_cast<long long>(a.R) * a.T * a.topk;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += static_cast<long long>(gridDim.x) * blockDim.x)
+    a.loc[i] = -1;
+}
+
 __global__ void __launch_bounds__(256) locate_kernel(const CombineArgs a) {
+  ptx::griddep_wait();  // launched with programmatic stream serialization
+  ptx::griddep_launch_dependents();
   const long long g = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (g >= static_cast<long long>(a.R) * a.cap) return;
   const int d = static_cast<int>(g / a.cap);
@@ -105,6 +118,8 @@ __device__ __forceinline__ void store_vec(char* out, int v, int out_f32, const f
 
 template <bool IN_F32>
 __global__ void __launch_bounds__(256) combine_kernel(const CombineArgs a) {
+  ptx::griddep_wait();  // launched with programmatic stream serialization
+  ptx::griddep_launch_dependents();
   constexpr int kN = IN_F32 ? 4 : 8;      // values per 16-byte vector
   constexpr int kUnroll = 4;              // vectors per lane in flight, per row
   const int lane = threadIdx.x & 31;
@@ -258,10 +273,17 @@ fcc_status fcc_moe_combine(int R, const void* const* recv_y, int64_t cap, int64_
   a.in_f32 = in == FCC_F32 ? 1 : 0;
   a.out_f32 = out_dtype == FCC_F32 ? 1 : 0;
 
-  const size_t loc_bytes = static_cast<size_t>(R) * T * topk * 4;
-  if (cudaMemsetAsync(a.loc, 0xFF, loc_bytes, st) != cudaSuccess) return FCC_ERR_CUDA;  // -1
+  // Three kernels chained with programmatic stream serialization (each one's
+  // launch overlaps the one before it; each waits for it in-kernel).
+  const long long slots = static_cast<long long>(R) * T * topk;
+  const unsigned clear_blocks =
+      static_cast<unsigned>(std::min<long long>((slots + 255) / 256, 4ll * std::max(1, sms)));
+  if (launch_pdl(clear_loc_kernel, dim3(clear_blocks), dim3(256), 0, st, 1u, a) != cudaSuccess)
+    return FCC_ERR_CUDA;
   const long long rows = static_cast<long long>(R) * cap;
-  locate_kernel<<<static_cast<unsigned>((rows + 255) / 256), 256, 0, st>>>(a);
+  if (launch_pdl(locate_kernel, dim3(static_cast<unsigned>((rows + 255) / 256)), dim3(256), 0, st,
+                 1u, a) != cudaSuccess)
+    return FCC_ERR_CUDA;
   // A persistent grid of the blocks that fit at once (warps loop over tokens).
   auto kern = a.in_f32 ? combine_kernel<true> : combine_kernel<false>;
   static int occ[2][64] = {};
@@ -269,9 +291,10 @@ fcc_status fcc_moe_combine(int R, const void* const* recv_y, int64_t cap, int64_
   const long long ntok = static_cast<long long>(R) * T;
   const long long blocks =
       std::min<long long>((ntok + 7) / 8, static_cast<long long>(sms) * per_sm);
-  kern<<<static_cast<unsigned>(std::max<long long>(1, blocks)), 256, 0, st>>>(a);
-  if (cudaGetLastError() != cudaSuccess) return FCC_ERR_CUDA;
-  bump_launch_count(2);
+  if (launch_pdl(kern, dim3(static_cast<unsigned>(std::max<long long>(1, blocks))), dim3(256), 0,
+                 st, 1u, a) != cudaSuccess)
+    return FCC_ERR_CUDA;
+  bump_launch_count(3);
   return FCC_OK;
 }
 

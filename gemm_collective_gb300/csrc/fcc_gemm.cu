@@ -254,6 +254,10 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) gemm_kernel(const __gri
   volatile int* bcast = reinterpret_cast<volatile int*>(tmem_slot + 2);
   int* tab = reinterpret_cast<int*>(tmem_slot + 4);  // grouped mode: expert tables
 
+  // Launched with programmatic stream serialization: no global memory is
+  // touched before the previous kernel on the stream has completed.
+  ptx::griddep_wait();
+  ptx::griddep_launch_dependents();
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   constexpr bool kPair = CG == 2;                      // tcgen05 cta_group::2 MMAs
@@ -539,17 +543,19 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) gemm_kernel(const __gri
     }
   } else if (warp >= kGemmThreads / 32 && lsu) {
     // ------------------------------------------ A-row loaders (grouped, lsu)
-    // Lane l of loader warp w owns row 32w + l of this CTA's 128 A rows: per
-    // stage it copies that row's 64 k (128 bytes, eight 16-byte requests) from
-    // its source token into the stage, at the chunk positions a 128-byte
-    // swizzled TMA box would use (chunk c of row r at c ^ (r mod 8)); rows
-    // past the tile's count and k past H are zero-filled.  A lane signals a
-    // stage kLoadLag stages later: it waits for that stage's copies, makes
-    // them visible to the tensor core's async proxy, and arrives on the pair
-    // leader's full barrier (which also counts the producer's B bytes).
+    // Loader warp w covers rows 32w .. 32w + 31 of this CTA's 128 A rows.  Per
+    // stage each row's 64 k are 128 bytes = eight 16-byte chunks; lane l moves
+    // chunk c = l mod 8 of rows 32w + l/8 + 4j (j < 8), so each of a lane's
+    // eight requests covers, across the warp, four whole rows (four cache
+    // lines).  A chunk lands where a 128-byte swizzled TMA box puts it (chunk
+    // c of row r at c ^ (r mod 8)); rows past the tile's count and k past H
+    // are zero-filled.  A lane signals a stage kLoadLag stages later: it
+    // waits for that stage's copies, makes them visible to the tensor core's
+    // async proxy, and arrives on the pair leader's full barrier (which also
+    // counts the producer's B bytes).
     if constexpr (MODE == MODE_GROUPED) {
-      const int r_local = (warp - kGemmThreads / 32) * 32 + lane;
-      const uint32_t sw = static_cast<uint32_t>(r_local & 7);
+      const int w_row0 = (warp - kGemmThreads / 32) * 32 + (lane >> 3);  // row of j = 0
+      const uint32_t c = static_cast<uint32_t>(lane & 7);
       const uint32_t full0 =
           kPair ? ptx::mapa(ptx::smem_addr(&full[0]), lead) : ptx::smem_addr(&full[0]);
       uint32_t stage = 0, phase = 0;
@@ -567,13 +573,18 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) gemm_kernel(const __gri
       bool ok = true;
       for (int t = pair; t < num_tiles && ok; t += npairs) {
         const Tile tl = tile_of<MODE, TM>(p, t, tab);
-        const int local = static_cast<int>(cta) * kBM + r_local;
-        const char* src = nullptr;
-        if (local < tl.rows) {
-          const int sidx = __ldcg(p.recv_src[tl.shard] + tl.row0 + local);
-          const int s = sidx / p.T;
-          src = static_cast<const char*>(p.src_x[s]) +
-                static_cast<long long>(sidx - s * p.T) * p.K * 2;
+        // This lane's eight source rows (nullptr: past the tile's rows)
+        const char* src[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int local = static_cast<int>(cta) * kBM + w_row0 + 4 * j;
+          src[j] = nullptr;
+          if (local < tl.rows) {
+            const int sidx = __ldcg(p.recv_src[tl.shard] + tl.row0 + local);
+            const int s = sidx / p.T;
+            src[j] = static_cast<const char*>(p.src_x[s]) +
+                     static_cast<long long>(sidx - s * p.T) * p.K * 2;
+          }
         }
         for (int it = 0; it < k_iters; ++it) {
           int good = 1;
@@ -582,13 +593,15 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) gemm_kernel(const __gri
             ok = false;
             break;
           }
-          const uint32_t row_dst = ptx::smem_addr(sA + stage * kABytes) + r_local * 128;
+          const uint32_t a_dst = ptx::smem_addr(sA + stage * kABytes);
+          const int k = it * kBK + static_cast<int>(c) * 8;
+          const bool k_in = k < p.K;  // (K % 8 == 0: whole chunks)
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            const int k = it * kBK + c * 8;
-            const bool in = src != nullptr && k < p.K;  // (K % 8 == 0: whole chunks)
-            ptx::cp_async_16(row_dst + ((static_cast<uint32_t>(c) ^ sw) << 4),
-                             in ? static_cast<const void*>(src + k * 2) : p.src_x[0],
+          for (int j = 0; j < 8; ++j) {
+            const uint32_t r = static_cast<uint32_t>(w_row0 + 4 * j);
+            const bool in = k_in && src[j] != nullptr;
+            ptx::cp_async_16(a_dst + r * 128 + ((c ^ (r & 7u)) << 4),
+                             in ? static_cast<const void*>(src[j] + k * 2) : p.src_x[0],
                              in ? 16u : 0u);
           }
           ptx::cp_async_commit();
@@ -851,23 +864,11 @@ template <int MODE, int CG, class P>
 cudaError_t launch_mode(const P& p, int grid, cudaStream_t st) {
   auto kern = gemm_kernel<MODE, CG, P>;
   static bool attr_set[64] = {};
-  cudaError_t e = smem_attr_once(attr_set, kern, Cfg<CG>::kSmem);
+  const cudaError_t e = smem_attr_once(attr_set, kern, Cfg<CG>::kSmem);
   if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid, 1, 1);
-  cfg.blockDim = dim3(threads_of<MODE>(), 1, 1);
-  cfg.dynamicSmemBytes = Cfg<CG>::kSmem;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = CG;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, kern, p);
-  if (e != cudaSuccess) return e;
-  return cudaGetLastError();
+  // CTA pairs launch as clusters of two; a single CTA is its own cluster.
+  return launch_pdl(kern, dim3(grid, 1, 1), dim3(threads_of<MODE>(), 1, 1), Cfg<CG>::kSmem, st,
+                    CG == 2 ? 2u : 1u, p);
 }
 
 template <int CG>

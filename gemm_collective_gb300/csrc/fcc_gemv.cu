@@ -69,6 +69,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemv_ar_kernel(const __grid_c
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* bcast = reinterpret_cast<volatile int*>(tmem_slot + 2);
 
+  ptx::griddep_wait();  // launched with programmatic stream serialization
+  ptx::griddep_launch_dependents();
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int g = blockIdx.x / p.splits;              // column group
@@ -305,8 +307,8 @@ cudaError_t launch_gemv(const GemvParams& p, int grid, cudaStream_t st) {
   static bool attr_set[64] = {};
   const cudaError_t e = smem_attr_once(attr_set, gemv_ar_kernel, kSmemBytes);
   if (e != cudaSuccess) return e;
-  gemv_ar_kernel<<<grid, kGemmThreads, kSmemBytes, st>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(gemv_ar_kernel, dim3(grid, 1, 1), dim3(kGemmThreads, 1, 1), kSmemBytes, st,
+                    1u, p);
 }
 
 // Arrival tickets of the default path (no caller workspace): a library array,

@@ -39,6 +39,36 @@ int blocks_per_sm_once(int (&cache)[64], Kernel kern, int threads) {
   return n;
 }
 
+// Launches kern<<<grid, block, smem, st>>>(args...) with programmatic stream
+// serialization (and a cluster of `cluster` CTAs when > 1): the launch may
+// overlap the previous kernel on `st`, so every thread of `kern` must call
+// ptx::griddep_wait() before it touches global memory.
+template <class... KArgs, class... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t st, unsigned cluster, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  unsigned n = 0;
+  attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[n].val.programmaticStreamSerializationAllowed = 1;
+  ++n;
+  if (cluster > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = cluster;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
 constexpr int kBM = 128;       // output tile rows (one TMEM lane per row)
 constexpr int kBK = 64;        // K per pipeline stage (128 bytes of bf16: one swizzle row)
 constexpr int kGemmThreads = 192;  // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue

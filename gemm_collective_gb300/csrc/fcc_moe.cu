@@ -3,9 +3,9 @@
 // The MoE Dispatch + GEMM kernel of the mKernel article's fused-kernel list
 // (and the GEMM + All-to-All operator for MoE in the SC24 paper's abstract),
 // over R virtual ranks in one GPU:
-//   1. route_kernel   one thread per token: top-k experts by logit (ties to
-//                     the lower index), softmax gates, and a per-chunk expert
-//                     histogram (chunk = 128 tokens of one source rank).
+//   1. route_kernel   eight threads per token: top-k experts by logit (ties
+//                     to the lower index), softmax gates, and a per-chunk
+//                     expert histogram (chunk = 128 tokens of one source rank).
 //   2. offsets_kernel one CTA: for every expert the exclusive prefix of its
 //                     histogram over the chunks (a fixed order) and its count;
 //                     send counts, each expert's first row in its receiving
@@ -60,7 +60,7 @@ struct MoeArgs {
   int chunks_per_rank;
   int tiles_n;
   int tile_m;             // rows per grouped-GEMM tile
-  int32_t* chunk_counts;  // [nchunks][E]
+  int32_t* chunk_counts;  // [E][nchunks]
   int32_t* chunk_off;     // [nchunks][E]
   int32_t* expert_counts; // [E] (caller's output)
   int32_t* send_counts;   // [R][R] (caller's output)
@@ -82,66 +82,97 @@ struct MoeArgs {
   int* status;
 };
 
-// Grid: one CTA per chunk of 128 tokens (of one source rank), one token per
-// thread.  The chunk's logits are first staged in shared memory with
-// coalesced loads (rows padded to 65 words, so the threads reading their own
-// rows hit 32 different banks); each thread then scans its token's E logits
-// once for the top-k (a strictly larger logit replaces, so an equal logit
-// keeps the lower expert index), and once more for the softmax denominator
-// relative to the largest logit (four partial sums in a fixed order).  The
-// per-chunk expert histogram is counted in shared memory.
-constexpr int kRoutePad = FCC_MAX_EXPERTS + 1;
+// Grid: one CTA per chunk of 128 tokens (of one source rank), eight threads
+// per token (1024 threads).  Thread q of a token scans its slice of the E
+// logits for its own top two (a strictly larger logit replaces, so an equal
+// logit keeps the lower expert index); the eight partial lists are merged by
+// xor shuffles (the same total order: larger logit, then lower index), so
+// all eight hold the token's top two and its largest logit m.  The softmax
+// denominator sum_e exp(l_e - m) is summed per thread in expert order, then
+// over the eight threads in a fixed shuffle tree.  The per-chunk expert
+// histogram is counted in shared memory and stored expert-major
+// (chunk_counts[e][chunk]) for the scan.
+constexpr int kRouteSub = 8;  // threads per token
 
-__global__ void __launch_bounds__(kChunkTok) route_kernel(const MoeArgs a) {
-  __shared__ float lg[kChunkTok * kRoutePad];
+struct Cand {
+  float v;
+  int i;
+};
+
+// a ranks before b: larger logit, or equal logit and lower expert index.
+__device__ __forceinline__ bool better(const Cand& a, const Cand& b) {
+  return a.v > b.v || (a.v == b.v && a.i < b.i);
+}
+
+__global__ void __launch_bounds__(kChunkTok * kRouteSub) route_kernel(const MoeArgs a) {
+  ptx::griddep_wait();  // launched with programmatic stream serialization
+  ptx::griddep_launch_dependents();
   __shared__ int hist[FCC_MAX_EXPERTS];
   const int chunk = blockIdx.x;
   const int s = chunk / a.chunks_per_rank;
   const int t0 = (chunk - s * a.chunks_per_rank) * kChunkTok;
-  const int n = min(a.T - t0, kChunkTok);
   const int E = a.E;
   if (threadIdx.x < FCC_MAX_EXPERTS) hist[threadIdx.x] = 0;
-  const float* src = a.logits[s] + static_cast<long long>(t0) * E;
-  for (int i = threadIdx.x; i < n * E; i += blockDim.x) {
-    const int t = i / E;
-    lg[t * kRoutePad + (i - t * E)] = __ldcs(src + i);
-  }
   __syncthreads();
-  const int i = threadIdx.x;
-  if (i < n) {
-    const float* row = lg + i * kRoutePad;
-    // top-2 by value, equal values to the lower index (slot 1 unused if topk = 1)
-    float v0 = row[0], v1 = __int_as_float(0xff800000);
-    int i0 = 0, i1 = E;
-    for (int e = 1; e < E; ++e) {
-      const float x = row[e];
-      if (x > v0) {
-        v1 = v0;
-        i1 = i0;
-        v0 = x;
-        i0 = e;
-      } else if (x > v1 || i1 == E) {
-        v1 = x;
-        i1 = e;
-      }
+  const int t = t0 + static_cast<int>(threadIdx.x) / kRouteSub;
+  const int q = threadIdx.x % kRouteSub;
+  const bool live = t < a.T;  // (whole 8-thread groups: the shuffles stay uniform)
+  const int per = (E + kRouteSub - 1) / kRouteSub;
+  const int e_lo = min(E, q * per), e_hi = min(E, e_lo + per);
+  const float* row = a.logits[s] + static_cast<long long>(live ? t : t0) * E;
+  const float neg_inf = __int_as_float(0xff800000);
+  Cand c0{neg_inf, E}, c1{neg_inf, E};  // (index E: no expert; loses every comparison)
+  float x[FCC_MAX_EXPERTS / kRouteSub];
+#pragma unroll
+  for (int k = 0; k < FCC_MAX_EXPERTS / kRouteSub; ++k)
+    x[k] = (live && e_lo + k < e_hi) ? __ldcs(row + e_lo + k) : neg_inf;
+#pragma unroll
+  for (int k = 0; k < FCC_MAX_EXPERTS / kRouteSub; ++k) {
+    if (e_lo + k >= e_hi) break;
+    const Cand c{x[k], e_lo + k};
+    if (better(c, c0)) {
+      c1 = c0;
+      c0 = c;
+    } else if (better(c, c1)) {
+      c1 = c;
     }
-    float sum[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int e = 0; e < E; ++e) sum[e & 3] += expf(row[e] - v0);
-    const float den = (sum[0] + sum[1]) + (sum[2] + sum[3]);
-    const int t = t0 + i;
+  }
+#pragma unroll
+  for (int off = kRouteSub / 2; off > 0; off >>= 1) {
+    Cand b0, b1;
+    b0.v = __shfl_xor_sync(0xffffffffu, c0.v, off);
+    b0.i = __shfl_xor_sync(0xffffffffu, c0.i, off);
+    b1.v = __shfl_xor_sync(0xffffffffu, c1.v, off);
+    b1.i = __shfl_xor_sync(0xffffffffu, c1.i, off);
+    if (better(b0, c0)) {
+      c1 = better(b1, c0) ? b1 : c0;
+      c0 = b0;
+    } else if (better(b0, c1)) {
+      c1 = b0;
+    }
+  }
+  const float m = c0.v;
+  float sum = 0.f;
+#pragma unroll
+  for (int k = 0; k < FCC_MAX_EXPERTS / kRouteSub; ++k)
+    if (e_lo + k < e_hi) sum += expf(x[k] - m);
+#pragma unroll
+  for (int off = kRouteSub / 2; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+  if (live && q == 0) {
     const long long o = static_cast<long long>(t) * a.topk;
-    a.idx[s][o] = i0;
-    a.gate[s][o] = 1.0f / den;  // exp(v0 - v0) = 1
-    atomicAdd(&hist[i0], 1);    // a count: order does not matter
+    a.idx[s][o] = c0.i;
+    a.gate[s][o] = 1.0f / sum;  // exp(m - m) = 1
+    atomicAdd(&hist[c0.i], 1);  // a count: order does not matter
     if (a.topk > 1) {
-      a.idx[s][o + 1] = i1;
-      a.gate[s][o + 1] = expf(v1 - v0) / den;
-      atomicAdd(&hist[i1], 1);
+      a.idx[s][o + 1] = c1.i;
+      a.gate[s][o + 1] = expf(c1.v - m) / sum;
+      atomicAdd(&hist[c1.i], 1);
     }
   }
   __syncthreads();
   if (threadIdx.x < E)
-    a.chunk_counts[static_cast<long long>(chunk) * E + threadIdx.x] = hist[threadIdx.x];
+    a.chunk_counts[static_cast<long long>(threadIdx.x) * a.R * a.chunks_per_rank + chunk] =
+        hist[threadIdx.x];
 }
 
 // One CTA of 1024 threads after the router: for every expert the exclusive
@@ -152,27 +183,47 @@ __global__ void __launch_bounds__(kChunkTok) route_kernel(const MoeArgs a) {
 // row in its receiving rank's buffer and its kept rows (capacity), the send
 // counts and the grouped GEMM's tile table.
 __global__ void __launch_bounds__(1024) offsets_kernel(const MoeArgs a) {
+  ptx::griddep_wait();  // launched with programmatic stream serialization
+  ptx::griddep_launch_dependents();
   __shared__ int counts[FCC_MAX_EXPERTS];
   __shared__ int rows[FCC_MAX_EXPERTS];
+  __shared__ int srcoff[FCC_MAX_RANKS + 1][FCC_MAX_EXPERTS];  // prefix at each source's first chunk
   __shared__ int units_s;
   const int nchunks = a.R * a.chunks_per_rank;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int kPer = 8;  // consecutive chunks per lane (one 32-byte run of counts)
   for (int e = warp; e < a.E; e += 32) {
+    const int32_t* cc = a.chunk_counts + static_cast<long long>(e) * nchunks;  // expert-major
     int carry = 0;
-    for (int c0 = 0; c0 < nchunks; c0 += 32) {
-      const int c = c0 + lane;
-      const int v = c < nchunks ? a.chunk_counts[static_cast<long long>(c) * a.E + e] : 0;
-      int incl = v;
+    for (int c0 = 0; c0 < nchunks; c0 += 32 * kPer) {
+      const int cb = c0 + lane * kPer;
+      int v[kPer];
+#pragma unroll
+      for (int j = 0; j < kPer; ++j) v[j] = cb + j < nchunks ? __ldcg(cc + cb + j) : 0;
+      int run = 0;
+#pragma unroll
+      for (int j = 0; j < kPer; ++j) run += v[j];
+      int incl = run;
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {
         const int y = __shfl_up_sync(0xffffffffu, incl, off);
         if (lane >= off) incl += y;
       }
-      if (c < nchunks) a.chunk_off[static_cast<long long>(c) * a.E + e] = carry + incl - v;
+      int before = carry + incl - run;
+#pragma unroll
+      for (int j = 0; j < kPer; ++j) {
+        const int c = cb + j;
+        if (c < nchunks) {
+          a.chunk_off[static_cast<long long>(c) * a.E + e] = before;
+          if (c % a.chunks_per_rank == 0) srcoff[c / a.chunks_per_rank][e] = before;
+        }
+        before += v[j];
+      }
       carry += __shfl_sync(0xffffffffu, incl, 31);
     }
     if (lane == 0) {
       counts[e] = carry;
+      srcoff[a.R][e] = carry;
       a.expert_counts[e] = carry;
     }
   }
@@ -194,13 +245,8 @@ __global__ void __launch_bounds__(1024) offsets_kernel(const MoeArgs a) {
   // read off the prefix at the boundaries of s's chunks.
   if (e < a.R * a.R) {
     const int s = e / a.R, d = e - (e / a.R) * a.R;
-    const int c_lo = s * a.chunks_per_rank, c_hi = (s + 1) * a.chunks_per_rank;
     int sum = 0;
-    for (int f = d * a.Eloc; f < (d + 1) * a.Eloc; ++f) {
-      const int hi = c_hi < nchunks ? a.chunk_off[static_cast<long long>(c_hi) * a.E + f]
-                                    : counts[f];
-      sum += hi - a.chunk_off[static_cast<long long>(c_lo) * a.E + f];
-    }
+    for (int f = d * a.Eloc; f < (d + 1) * a.Eloc; ++f) sum += srcoff[s + 1][f] - srcoff[s][f];
     a.send_counts[e] = sum;
   }
   __syncthreads();
@@ -237,6 +283,8 @@ __global__ void __launch_bounds__(1024) offsets_kernel(const MoeArgs a) {
 // (token t0 + i/topk, slot i%topk), so the 8 warps hold consecutive runs of
 // assignments in (t, slot) order.
 __global__ void __launch_bounds__(256) rank_kernel(const MoeArgs a) {
+  ptx::griddep_wait();  // launched with programmatic stream serialization
+  ptx::griddep_launch_dependents();
   __shared__ int cnt[8][FCC_MAX_EXPERTS];
   const int chunk = blockIdx.x;
   const int s = chunk / a.chunks_per_rank;
@@ -280,6 +328,8 @@ __global__ void __launch_bounds__(256) rank_kernel(const MoeArgs a) {
 // One warp per token: read the token's row once (16-byte loads) and write it to
 // each of its receive rows.
 __global__ void __launch_bounds__(256) copy_kernel(const MoeArgs a) {
+  ptx::griddep_wait();  // launched with programmatic stream serialization
+  ptx::griddep_launch_dependents();
   const int lane = threadIdx.x & 31;
   const long long warps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
   const long long ntok = static_cast<long long>(a.R) * a.T;
@@ -374,6 +424,8 @@ __global__ void __launch_bounds__(256) copy_expert_rows_kernel(const MoeArgs a, 
 // s's send buffer.  Only the kept rows (within the receive capacity) are
 // packed and moved; they are a prefix of each run.
 __global__ void __launch_bounds__(64) ce_plan_kernel(const MoeArgs a) {
+  ptx::griddep_wait();  // launched with programmatic stream serialization
+  ptx::griddep_launch_dependents();
   __shared__ int off[FCC_MAX_RANKS + 1][FCC_MAX_EXPERTS];
   __shared__ int kept[FCC_MAX_RANKS][FCC_MAX_EXPERTS];
   const int e = threadIdx.x;
@@ -404,6 +456,8 @@ __global__ void __launch_bounds__(64) ce_plan_kernel(const MoeArgs a) {
 // kept rows into its own send buffer (a copy inside the rank; nothing crosses
 // ranks here), one warp per token, the token's row read once.
 __global__ void __launch_bounds__(256) ce_pack_kernel(const MoeArgs a) {
+  ptx::griddep_wait();  // launched with programmatic stream serialization
+  ptx::griddep_launch_dependents();
   const int lane = threadIdx.x & 31;
   const long long warps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
   const long long ntok = static_cast<long long>(a.R) * a.T;
@@ -696,10 +750,13 @@ fcc_status fcc_moe_dispatch_gemm(int R, const void* const* X, const float* const
     g.stage_copy = 1;
   }
 
-  route_kernel<<<plan.nchunks, kChunkTok, 0, st>>>(a);
-  offsets_kernel<<<1, 1024, 0, st>>>(a);
-  rank_kernel<<<plan.nchunks, 256, 0, st>>>(a);
-  if (cudaGetLastError() != cudaSuccess) return FCC_ERR_CUDA;
+  // The chain on `st` launches with programmatic stream serialization: each
+  // kernel's launch overlaps the one before it, and waits for it in-kernel.
+  if (launch_pdl(route_kernel, dim3(plan.nchunks), dim3(kChunkTok * kRouteSub), 0, st, 1u, a) !=
+          cudaSuccess ||
+      launch_pdl(offsets_kernel, dim3(1), dim3(1024), 0, st, 1u, a) != cudaSuccess ||
+      launch_pdl(rank_kernel, dim3(plan.nchunks), dim3(256), 0, st, 1u, a) != cudaSuccess)
+    return FCC_ERR_CUDA;
   uint64_t launches = 3;
   const int grid = std::max(cg, (sms / cg) * cg);
 
@@ -737,9 +794,10 @@ fcc_status fcc_moe_dispatch_gemm(int R, const void* const* X, const float* const
     // data-dependent, so the host reads them back first: this form
     // synchronises the stream (as a copy-engine all-to-all with variable
     // splits needs the split sizes on the host).
-    ce_plan_kernel<<<1, 64, 0, st>>>(a);
-    ce_pack_kernel<<<std::max(1, sms) * 4, 256, 0, st>>>(a);
-    if (cudaGetLastError() != cudaSuccess) return FCC_ERR_CUDA;
+    if (launch_pdl(ce_plan_kernel, dim3(1), dim3(64), 0, st, 1u, a) != cudaSuccess ||
+        launch_pdl(ce_pack_kernel, dim3(std::max(1, sms) * 4), dim3(256), 0, st, 1u, a) !=
+            cudaSuccess)
+      return FCC_ERR_CUDA;
     launches += 2;
     const size_t plan_bytes = static_cast<size_t>(R) * E * 3 * 4;
     int32_t* hp = nullptr;
@@ -794,10 +852,11 @@ fcc_status fcc_moe_dispatch_gemm(int R, const void* const* X, const float* const
         return FCC_ERR_CUDA;
     }
     if (copy && !copy_in_gemm) {
-      copy_kernel<<<std::max(1, sms) * 4, 256, 0, side_copy ? side : st>>>(a);
+      if (launch_pdl(copy_kernel, dim3(std::max(1, sms) * 4), dim3(256), 0,
+                     side_copy ? side : st, 1u, a) != cudaSuccess)
+        return FCC_ERR_CUDA;
       launches += 1;
     }
-    if (cudaGetLastError() != cudaSuccess) return FCC_ERR_CUDA;
     if (side_copy && cudaEventRecord(ev[1], side) != cudaSuccess) return FCC_ERR_CUDA;
     if (launch_grouped_gemm(g, cg, grid, st) != cudaSuccess) return FCC_ERR_CUDA;
     if (side_copy && cudaStreamWaitEvent(st, ev[1], 0) != cudaSuccess) return FCC_ERR_CUDA;

@@ -334,6 +334,22 @@ def test_rs_full_size_sampled_rows():
         assert torch.equal(outs[j].view(torch.int16), again[j].view(torch.int16))
 
 
+def test_ar_full_size_sampled_rows_all_buffers():
+    """The all-reduce on the 8-rank 8192x8192x3584 inputs, bf16 outputs, in the
+    benchmark's launch shape: sampled rows of every rank's buffer against the
+    oracle, every buffer bitwise equal to rank 0's, all of them finite."""
+    w = synth.WORKLOADS["gemm_ar_r8_8192x8192x3584"]
+    A, B = synth.gemm_inputs(w.R, w.M, w.N, w.K, w.std_a, w.std_b, seed=0)
+    dA, dB = _upload(A, B)
+    outs = _ar(w.R, dA, dB, w.M, w.N, w.K, fcc.FCC_BF16)
+    for r in range(w.R):
+        rows = _sample_rows(w.M, 8, seed=200 + r)
+        got = to_f64(outs[r][torch.from_numpy(rows).cuda()])
+        assert_close(got, oracle.gemm_ar(A, B, rows), f"rank {r}")
+        assert torch.isfinite(outs[r].float()).all()
+        assert torch.equal(outs[r].view(torch.int16), outs[0].view(torch.int16)), f"rank {r}"
+
+
 @pytest.mark.parametrize("algo", [fcc.FCC_ALGO_AUTO, fcc.FCC_ALGO_INTERDECOM])
 def test_ag_full_size_sampled_rows(algo):
     """The 8-rank 8192x3584x8192 workload in the benchmark's launch shapes: the
