@@ -384,7 +384,9 @@ def phase_fractions(torch, dev, call):
     return {"ctas": int(len(t)), "tiles": int(t[:, 3].sum()),
             "epilogue_busy_frac": float(t[:, 1].sum() / span),
             "mma_wait_on_epilogue_frac": float(t[:, 2].sum() / max(leaders[:, 0].sum(), 1.0)),
-            "kernel_us_max_cta": float(t[:, 0].max() / 1e3)}
+            "kernel_us_max_cta": float(t[:, 0].max() / 1e3),
+            "kernel_us_mean_cta": float(t[:, 0].mean() / 1e3),
+            "kernel_us_min_cta": float(t[:, 0].min() / 1e3)}
 
 
 def small_rs_latency(fcc, torch, np, synth, dev, stream):
@@ -408,6 +410,13 @@ def small_rs_latency(fcc, torch, np, synth, dev, stream):
            "marshalled_us": 1e3 * time_calls(
                lambda: fcc.fcc_gemm_rs(w.R, dA, dB, outs, w.M, w.N, w.K, 0, 2, None, stream),
                200, 10, stream)}
+    # the host's own time per call (enqueueing only; the GPU runs behind)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(200):
+        call(stream)
+    res["host_enqueue_us"] = (time.perf_counter() - t0) / 200 * 1e6
+    torch.cuda.synchronize()
     try:
         side = torch.cuda.Stream(device=dev)
         with torch.cuda.stream(side):

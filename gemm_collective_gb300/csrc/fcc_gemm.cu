@@ -63,13 +63,9 @@ constexpr uint64_t kDrainNs = 50ull * 1000 * 1000;  // unwinding limit after an 
 constexpr int kTabInts = 4 * FCC_MAX_EXPERTS + 2;
 constexpr int kCopyRows = 4;  // rows per claimed chunk of the in-kernel staging copy
 
-constexpr int kLoadLag = 3;   // cp.async groups a loader lane keeps in flight before signalling
-
 template <int MODE>
 constexpr int threads_of() {
-  return MODE == MODE_GROUPED
-             ? kGemmThreads + 32 * (kCopyWarps > kLoadWarps ? kCopyWarps : kLoadWarps)
-             : kGemmThreads;
+  return MODE == MODE_GROUPED ? kGemmThreads + 32 * kCopyWarps : kGemmThreads;
 }
 
 // CG = CTAs per cluster: 1 (one CTA per 128x256 tile) or 2 (a CTA pair per
@@ -86,6 +82,10 @@ struct Cfg {
   static constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(kTileM, kBN, false, true);
   // A tile whose columns end in the first half of its 256 runs 128 wide.
   static constexpr uint32_t kIdescNarrow = ptx::idesc_bf16_f32(kTileM, kBN / 2, false, true);
+  // Grouped mode, CTA pair: an expert's last unit of at most 128 rows runs
+  // as an M = 128 pair MMA (64 rows from each CTA), at half the MMA work.
+  static constexpr uint32_t kIdescShort = ptx::idesc_bf16_f32(128, kBN, false, true);
+  static constexpr uint32_t kIdescShortNarrow = ptx::idesc_bf16_f32(128, kBN / 2, false, true);
   // ... + barriers + flags + the grouped mode's expert tables.
   static constexpr int kSmem = 1024 + kStages * static_cast<int>(kStageBytes) +
                                (2 * kStages + 5) * 8 + 16 + kTabInts * 4;
@@ -100,6 +100,7 @@ struct Tile {
   int row0;    // GROUPED: first receive-buffer row of the tile
   int rows;    // GROUPED: valid rows of the tile
   int half;    // -1: the whole 256-column tile; 0 / 1: its first / second 128 columns
+  int m128;    // GROUPED on CTA pairs: 1 = at most 128 rows, run as an M = 128 pair MMA
 };
 
 __device__ __forceinline__ void raster(int t, int tiles_m, int tiles_n, int group, int& mt,
@@ -141,6 +142,7 @@ __device__ __forceinline__ Tile tile_of(const P& p, int t, const int* tab) {
   tl.row0 = 0;
   tl.rows = 0;
   tl.half = -1;
+  tl.m128 = 0;
   if constexpr (MODE == MODE_RS || MODE == MODE_AR || MODE == MODE_AG || MODE == MODE_PARTIAL) {
     // Work items from split_first on are halves of the last round's tiles
     // (two per tile), so that round takes half a tile's time.
@@ -175,6 +177,7 @@ __device__ __forceinline__ Tile tile_of(const P& p, int t, const int* tab) {
     tl.shard = e / p.Eloc;
     tl.row0 = base[e] + tl.mt * TM;
     tl.rows = min(TM, rows_e - tl.mt * TM);
+    tl.m128 = (TM == 2 * kBM && tl.rows <= kBM) ? 1 : 0;
   } else if constexpr (MODE == MODE_RS || MODE == MODE_AR) {
     raster(t, p.tiles_m, p.tiles_n, p.group_m, tl.mt, tl.nt);
   } else if constexpr (MODE == MODE_AG) {
@@ -267,19 +270,14 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) gemm_kernel(const __gri
   const int pair = blockIdx.x / CG;
   const int npairs = gridDim.x / CG;
 
-  // Gather modes (MoE without a staged copy): the producer warp fetches the A
-  // rows from the source tokens with TMA gather4 (gather), or the loader
-  // warps do with cp.async while the producer loads only B (lsu).
-  bool gather = false, lsu = false;
-  if constexpr (MODE == MODE_GROUPED) {
-    gather = p.gather == 1;
-    lsu = p.gather == 2;
-  }
+  // Gather mode (MoE without a staged copy): the producer warp fetches the A
+  // rows from the source tokens with TMA gather4.
+  bool gather = false;
+  if constexpr (MODE == MODE_GROUPED) gather = p.gather != 0;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      // lsu: the producer's arrive plus one per loader lane of the pair's CTAs
-      ptx::mbar_init(&full[s], lsu ? 1 + 32 * kLoadWarps * C::kPairCtas : 1);
+      ptx::mbar_init(&full[s], 1);
       ptx::mbar_init(&empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -356,7 +354,7 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) gemm_kernel(const __gri
         int y[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const int local = static_cast<int>(cta) * kBM + 4 * lane + i;
+          const int local = static_cast<int>(cta) * (tl.m128 ? kBM / 2 : kBM) + 4 * lane + i;
           y[i] = local < tl.rows ? __ldcg(p.recv_src[tl.shard] + tl.row0 + local) : 0;
         }
         for (int it = 0; it < k_iters; ++it) {
@@ -417,11 +415,12 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) gemm_kernel(const __gri
         } else {
           a_row = tl.mt * TM;
         }
-        a_row += static_cast<int>(cta) * kBM;                 // this CTA's half of the rows
+        // this CTA's half of the rows (an M = 128 pair tile: 64 rows each; the
+        // 128-row box then also loads 64 rows the MMA does not read)
+        a_row += static_cast<int>(cta) * (tl.m128 ? kBM / 2 : kBM);
         const int bn_cta = narrow(tl) ? C::kBNcta / 2 : C::kBNcta;  // B columns of this CTA
         const int b_col = col_base(tl) + static_cast<int>(cta) * bn_cta;
-        // (lsu: the A rows arrive by the loader warps' cp.async, not counted in bytes)
-        const uint32_t stage_bytes = (lsu ? 0u : kABytes) + static_cast<uint32_t>(bn_cta) * kBK * 2;
+        const uint32_t stage_bytes = kABytes + static_cast<uint32_t>(bn_cta) * kBK * 2;
         if constexpr (MODE == MODE_GROUPED) {
           if (p.stage_copy) {
             // The unit's rows are written by the copy warps (of any CTA):
@@ -450,12 +449,12 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) gemm_kernel(const __gri
             // Both CTAs' bytes are counted on the leader's full barrier.
             const uint32_t bar = ptx::mapa(ptx::smem_addr(&full[stage]), lead);
             if (cta == 0) ptx::mbar_arrive_expect_tx(&full[stage], 2 * stage_bytes);
-            if (!lsu) ptx::tma_load_2d_pair(a_dst, ma, bar, kb * kBK, a_row);
+            ptx::tma_load_2d_pair(a_dst, ma, bar, kb * kBK, a_row);
             for (int i = 0; i < bn_cta / 64; ++i)
               ptx::tma_load_2d_pair(b_dst + i * kBBoxBytes, mb, bar, b_col + 64 * i, kb * kBK);
           } else {
             ptx::mbar_arrive_expect_tx(&full[stage], stage_bytes);
-            if (!lsu) ptx::tma_load_2d(a_dst, ma, &full[stage], kb * kBK, a_row);
+            ptx::tma_load_2d(a_dst, ma, &full[stage], kb * kBK, a_row);
             for (int i = 0; i < bn_cta / 64; ++i)
               ptx::tma_load_2d(b_dst + i * kBBoxBytes, mb, &full[stage], b_col + 64 * i,
                                kb * kBK);
@@ -488,7 +487,9 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) gemm_kernel(const __gri
       bool any = false, ok = true;
       uint64_t waited = 0;
       for (int t = pair; t < num_tiles && ok; t += npairs) {
-        const uint32_t idesc = narrow(tile_of<MODE, TM>(p, t, tab)) ? C::kIdescNarrow : C::kIdesc;
+        const Tile tm_ = tile_of<MODE, TM>(p, t, tab);
+        const uint32_t idesc = tm_.m128 ? (narrow(tm_) ? C::kIdescShortNarrow : C::kIdescShort)
+                                        : (narrow(tm_) ? C::kIdescNarrow : C::kIdesc);
         const uint64_t w0 = times != nullptr ? ptx::globaltimer() : 0;
         if (!W.wait(&tempty[acc], acc_phase ^ 1u)) break;
         if (times != nullptr) waited += ptx::globaltimer() - w0;
@@ -541,90 +542,10 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) gemm_kernel(const __gri
       }
       if (times != nullptr) times[2] = waited;
     }
-  } else if (warp >= kGemmThreads / 32 && lsu) {
-    // ------------------------------------------ A-row loaders (grouped, lsu)
-    // Loader warp w covers rows 32w .. 32w + 31 of this CTA's 128 A rows.  Per
-    // stage each row's 64 k are 128 bytes = eight 16-byte chunks; lane l moves
-    // chunk c = l mod 8 of rows 32w + l/8 + 4j (j < 8), so each of a lane's
-    // eight requests covers, across the warp, four whole rows (four cache
-    // lines).  A chunk lands where a 128-byte swizzled TMA box puts it (chunk
-    // c of row r at c ^ (r mod 8)); rows past the tile's count and k past H
-    // are zero-filled.  A lane signals a stage kLoadLag stages later: it
-    // waits for that stage's copies, makes them visible to the tensor core's
-    // async proxy, and arrives on the pair leader's full barrier (which also
-    // counts the producer's B bytes).
-    if constexpr (MODE == MODE_GROUPED) {
-      const int w_row0 = (warp - kGemmThreads / 32) * 32 + (lane >> 3);  // row of j = 0
-      const uint32_t c = static_cast<uint32_t>(lane & 7);
-      const uint32_t full0 =
-          kPair ? ptx::mapa(ptx::smem_addr(&full[0]), lead) : ptx::smem_addr(&full[0]);
-      uint32_t stage = 0, phase = 0;
-      // Stages committed but not yet signalled: the npend stages before `stage`.
-      int npend = 0;
-      auto signal_oldest = [&]() {
-        const uint32_t old = (stage + kStages - static_cast<uint32_t>(npend)) % kStages;
-        ptx::fence_proxy_async_smem();
-        if constexpr (kPair)
-          ptx::mbar_arrive_cluster(full0 + old * 8);
-        else
-          ptx::mbar_arrive(&full[old]);
-        --npend;
-      };
-      bool ok = true;
-      for (int t = pair; t < num_tiles && ok; t += npairs) {
-        const Tile tl = tile_of<MODE, TM>(p, t, tab);
-        // This lane's eight source rows (nullptr: past the tile's rows)
-        const char* src[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int local = static_cast<int>(cta) * kBM + w_row0 + 4 * j;
-          src[j] = nullptr;
-          if (local < tl.rows) {
-            const int sidx = __ldcg(p.recv_src[tl.shard] + tl.row0 + local);
-            const int s = sidx / p.T;
-            src[j] = static_cast<const char*>(p.src_x[s]) +
-                     static_cast<long long>(sidx - s * p.T) * p.K * 2;
-          }
-        }
-        for (int it = 0; it < k_iters; ++it) {
-          int good = 1;
-          if (lane == 0) good = W.wait(&empty[stage], phase ^ 1u) ? 1 : 0;
-          if (!__shfl_sync(0xffffffffu, good, 0)) {
-            ok = false;
-            break;
-          }
-          const uint32_t a_dst = ptx::smem_addr(sA + stage * kABytes);
-          const int k = it * kBK + static_cast<int>(c) * 8;
-          const bool k_in = k < p.K;  // (K % 8 == 0: whole chunks)
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const uint32_t r = static_cast<uint32_t>(w_row0 + 4 * j);
-            const bool in = k_in && src[j] != nullptr;
-            ptx::cp_async_16(a_dst + r * 128 + ((c ^ (r & 7u)) << 4),
-                             in ? static_cast<const void*>(src[j] + k * 2) : p.src_x[0],
-                             in ? 16u : 0u);
-          }
-          ptx::cp_async_commit();
-          ++npend;
-          if (++stage == kStages) {
-            stage = 0;
-            phase ^= 1u;
-          }
-          if (npend > kLoadLag) {
-            ptx::cp_async_wait<kLoadLag>();
-            signal_oldest();
-          }
-        }
-      }
-      // Every copy lands before this CTA can exit (its shared memory is freed
-      // then); the stages still owed a signal get it.
-      ptx::cp_async_wait<0>();
-      while (npend > 0) signal_oldest();
-    }
   } else if (warp >= kGemmThreads / 32) {
     // ------------------------------------------- staging copy (grouped mode)
     if constexpr (MODE == MODE_GROUPED) {
-      if (p.stage_copy && warp < kGemmThreads / 32 + kCopyWarps) {
+      if (p.stage_copy) {
         const int* rows_t = tab + p.E + 1;
         const int* base_t = tab + 2 * p.E + 1;
         int* cstart = tab + 3 * p.E + 1;  // chunks of experts before e, from e_lo
@@ -732,8 +653,13 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) gemm_kernel(const __gri
         grow = static_cast<int64_t>(tl.shard) * p.Ms + local;
         if (row_ok) rowp = static_cast<char*>(p.out[tl.rank]) + grow * p.N * esz;
       } else if constexpr (MODE == MODE_GROUPED) {
-        row_ok = row_in_tile < tl.rows;
-        grow = static_cast<int64_t>(tl.row0) + row_in_tile;
+        // An M = 128 pair tile: this CTA's 64 rows are in TMEM lanes 0-63 for
+        // the first half of the tile's columns and again in lanes 64-127 for
+        // the second half.
+        const int rit = tl.m128 ? static_cast<int>(cta) * (kBM / 2) + ((q * 32 + lane) & 63)
+                                : row_in_tile;
+        row_ok = rit < tl.rows;
+        grow = static_cast<int64_t>(tl.row0) + rit;
         if (row_ok) rowp = static_cast<char*>(p.out[tl.shard]) + grow * p.N * esz;
       } else {  // MODE_PARTIAL
         grow = static_cast<int64_t>(p.m_begin) + static_cast<int64_t>(tl.mt) * TM + row_in_tile;
@@ -742,8 +668,11 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) gemm_kernel(const __gri
       }
 
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kBN;
-      const int col0 = col_base(tl);
-      const int cend = narrow(tl) ? kBN / 2 : kBN;  // accumulator columns written
+      const int ncols = narrow(tl) ? kBN / 2 : kBN;  // the tile's columns
+      // accumulator columns written: an M = 128 pair tile holds half of them
+      // per lane, lanes 64-127 the second half
+      const int cend = tl.m128 ? ncols / 2 : ncols;
+      const int col0 = col_base(tl) + ((tl.m128 && q >= 2) ? ncols / 2 : 0);
 #pragma unroll 1
       for (int c = 0; c < cend; c += 32) {
         uint32_t v[32];

@@ -73,7 +73,6 @@ constexpr int kBM = 128;       // output tile rows (one TMEM lane per row)
 constexpr int kBK = 64;        // K per pipeline stage (128 bytes of bf16: one swizzle row)
 constexpr int kGemmThreads = 192;  // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
 constexpr int kCopyWarps = 2;      // grouped mode: warps 6-7 stage the expert rows
-constexpr int kLoadWarps = 4;      // grouped mode, gather = 2: warps 6-9 load the A rows
 constexpr int kGemvTok = 16;   // GEMV: token rows per TMA box (M <= 16)
 
 enum GemmMode : int {
@@ -145,13 +144,10 @@ struct GroupedParams {
   int e_lo, e_hi;                      // this launch covers the tiles of experts [e_lo, e_hi)
   int* status;
   unsigned long long timeout_ns;
-  // Gather modes: the A rows are read straight from the source tokens
-  // instead of from a staged copy; row i of rank d's receive order is source
-  // row recv_src[d][i] (= s*T + t).  gather = 1: by TMA gather4, every mapA[d]
-  // the map of the sources' concatenated [R*T, H] matrix with a box one row
-  // high.  gather = 2: by the kernel's loader warps (cp.async, 16 bytes a
-  // request) from src_x[s], written into the swizzled shared-memory stage as
-  // a tiled TMA load would; mapA is unused.
+  // Gather mode (gather = 1): the A rows are read straight from the source
+  // tokens instead of from a staged copy.  Every mapA[d] is then the map of
+  // the sources' concatenated [R*T, H] matrix with a box one row high, and row
+  // i of rank d's receive order is its row recv_src[d][i] (= s*T + t).
   const int* recv_src[FCC_MAX_RANKS];  // [cap] per receiving rank
   int gather;
   // In-kernel staging (stage_copy = 1): the kernel's copy warps write row i of

@@ -61,7 +61,7 @@ struct MoeArgs {
   int tiles_n;
   int tile_m;             // rows per grouped-GEMM tile
   int32_t* chunk_counts;  // [E][nchunks]
-  int32_t* chunk_off;     // [nchunks][E]
+  int32_t* chunk_off;     // [E][nchunks]
   int32_t* expert_counts; // [E] (caller's output)
   int32_t* send_counts;   // [R][R] (caller's output)
   int32_t* expert_base;   // [E]
@@ -177,7 +177,7 @@ __global__ void __launch_bounds__(kChunkTok * kRouteSub) route_kernel(const MoeA
 
 // One CTA of 1024 threads after the router: for every expert the exclusive
 // prefix of its histogram over the chunks, in chunk order (source rank, then
-// token), so chunk_off[c][e] is the number of assignments to e that precede
+// token), so chunk_off[e][c] is the number of assignments to e that precede
 // chunk c in (s, t, slot) order (warp w scans experts w and w + 32, 32 chunks
 // per step, integer sums in a fixed shuffle order); then each expert's first
 // row in its receiving rank's buffer and its kept rows (capacity), the send
@@ -214,7 +214,7 @@ __global__ void __launch_bounds__(1024) offsets_kernel(const MoeArgs a) {
       for (int j = 0; j < kPer; ++j) {
         const int c = cb + j;
         if (c < nchunks) {
-          a.chunk_off[static_cast<long long>(c) * a.E + e] = before;
+          a.chunk_off[static_cast<long long>(e) * nchunks + c] = before;  // (coalesced)
           if (c % a.chunks_per_rank == 0) srcoff[c / a.chunks_per_rank][e] = before;
         }
         before += v[j];
@@ -314,7 +314,8 @@ __global__ void __launch_bounds__(256) rank_kernel(const MoeArgs a) {
   }
   __syncthreads();
   if (valid) {
-    const int pos = a.chunk_off[static_cast<long long>(chunk) * a.E + e] + cnt[warp][e] +
+    const int pos = a.chunk_off[static_cast<long long>(e) * a.R * a.chunks_per_rank + chunk] +
+                    cnt[warp][e] +
                     rank_in_warp;
     const int d = e / a.Eloc;
     const int row = a.expert_base[e] + pos;
@@ -431,7 +432,8 @@ __global__ void __launch_bounds__(64) ce_plan_kernel(const MoeArgs a) {
   const int e = threadIdx.x;
   if (e < a.E) {
     for (int s = 0; s <= a.R; ++s) {
-      off[s][e] = s < a.R ? a.chunk_off[static_cast<long long>(s) * a.chunks_per_rank * a.E + e]
+      off[s][e] = s < a.R ? a.chunk_off[static_cast<long long>(e) * a.R * a.chunks_per_rank +
+                                        s * a.chunks_per_rank]
                           : a.expert_counts[e];
       a.ce_srcoff[s * a.E + e] = off[s][e];
     }
@@ -640,17 +642,14 @@ fcc_status fcc_moe_dispatch_gemm(int R, const void* const* X, const float* const
   const bool interdecom = algo == FCC_ALGO_INTERDECOM;
   const bool ce = algo == FCC_ALGO_CE;
   const bool unfused = algo == FCC_ALGO_UNFUSED;
-  // AUTO / FUSED: with no recv_x asked for, the GEMM's loader warps gather
-  // each tile's rows from the source tokens into shared memory (lsu); with a
-  // recv_x, its copy warps write the rows there and the tensor cores read
-  // them back by TMA; FUSED with one source array gathers by TMA gather4.
-  // The baselines move the rows first: UNFUSED with one copy kernel,
-  // INTERDECOM with one copy kernel per expert range on a side stream ahead
-  // of that range's GEMM, CE with the copy engines.
+  // AUTO / FUSED: the rows are moved by the GEMM's own copy warps (or, for
+  // FUSED with one source array, gathered by its TMA).  The baselines move
+  // them first: UNFUSED with one copy kernel, INTERDECOM with one copy kernel
+  // per expert range on a side stream ahead of that range's GEMM, CE with the
+  // copy engines.
   const bool baseline = unfused || interdecom || ce;
-  const bool lsu = !gather && !baseline && recv_x == nullptr;
-  const bool stage_ws = !gather && !lsu && recv_x == nullptr;
-  const bool copy_in_gemm = !gather && !lsu && !baseline;
+  const bool stage_ws = !gather && recv_x == nullptr;
+  const bool copy_in_gemm = !gather && !baseline;
   const MoePlan plan = moe_plan(R, T, E, topk, H, cap, stage_ws, ce);
   void* ws = nullptr;
   int* status = nullptr;
@@ -707,8 +706,6 @@ fcc_status fcc_moe_dispatch_gemm(int R, const void* const* X, const float* const
   for (int d = 0; d < R; ++d) {
     if (gather)
       s = d == 0 ? internal_make_map(&g.mapA[0], X[0], R * T, H, 1) : FCC_OK;
-    else if (lsu)  // (unused by the kernel; a valid map all the same)
-      s = internal_make_map(&g.mapA[d], X[d], T, H, kBM);
     else
       s = internal_make_map(&g.mapA[d], a.recv_x[d], cap, H, kBM);
     if (s != FCC_OK) return s;
@@ -734,11 +731,7 @@ fcc_status fcc_moe_dispatch_gemm(int R, const void* const* X, const float* const
   g.status = status;
   g.timeout_ns = timeout_ns;
   g.phase_ns = opts != nullptr ? reinterpret_cast<unsigned long long*>(opts->phase_ns) : nullptr;
-  g.gather = gather ? 1 : (lsu ? 2 : 0);
-  if (lsu) {
-    for (int r = 0; r < R; ++r) g.src_x[r] = X[r];
-    g.T = static_cast<int>(T);
-  }
+  g.gather = gather ? 1 : 0;
   if (copy_in_gemm) {
     for (int r = 0; r < R; ++r) {
       g.src_x[r] = X[r];
@@ -840,8 +833,7 @@ fcc_status fcc_moe_dispatch_gemm(int R, const void* const* X, const float* const
   } else {
     // With the gather the copy (only for a requested recv_x) runs beside the
     // GEMM on a side stream: both only read what the dispatch kernels wrote.
-    // The loader warps' gather (lsu) needs no copy at all.
-    const bool copy = (!gather && !lsu) || recv_x != nullptr;
+    const bool copy = !gather || recv_x != nullptr;
     const bool side_copy = copy && gather;
     cudaStream_t side = nullptr;
     cudaEvent_t ev[2] = {};

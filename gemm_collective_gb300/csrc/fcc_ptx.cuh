@@ -383,25 +383,6 @@ __device__ __forceinline__ void tma_gather4_pair(void* dst, const CUtensorMap* m
       : "memory");
 }
 
-// ------------------------------------------------------------- cp.async
-// 16 bytes global -> shared (L2 only), the last 16 - src_bytes of them
-// zero-filled (src_bytes 0: all zeros; src must still be a valid address).
-__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint32_t src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
-               "r"(src_bytes)
-               : "memory");
-}
-
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;" ::: "memory");
-}
-
-// Wait until at most N of this thread's committed cp.async groups are pending.
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
 // ------------------------------------------------------- CTA pairs (clusters)
 // A pair of CTAs (cluster of 2) shares one tcgen05.mma.cta_group::2: the
 // leader (rank 0) issues it, each CTA holds half of A and half of B in its own

@@ -210,12 +210,10 @@ fcc_status fcc_ag_gemm(int R, const void *const *X_shard, const void *const *B,
  * X[s]: [T,H] bf16; logits[s]: [T,E] f32, finite; W[e]: [H,F] bf16 (E
  * pointers); recv_x: NULL, or per rank [cap,H] bf16 to receive the
  * dispatched rows.  By default (AUTO) the expert GEMM kernel moves the rows
- * itself: with recv_x NULL, its loader warps gather each tile's rows from the
- * source tokens straight into shared memory (cp.async), so the rows are never
- * staged in device memory; with a recv_x, its copy warps write the rows there
- * one (expert, m tile) unit after another and its tensor cores read each
- * unit back as soon as it is moved.  FCC_ALGO_UNFUSED (the unfused baseline)
- * moves all rows with a separate copy kernel before the GEMM.  FCC_ALGO_INTERDECOM (the chunked
+ * itself, into recv_x or into workspace when it is NULL, one (expert,
+ * m tile) unit after another, and its tensor cores read each unit as soon as
+ * it is moved.  FCC_ALGO_UNFUSED (the unfused baseline) moves all rows with a
+ * separate copy kernel before the GEMM.  FCC_ALGO_INTERDECOM (the chunked
  * baseline) splits the experts into c contiguous ranges (c = opts->chunks,
  * else the fcc_interdecom_chunks model with G = the expert GEMMs, X = the
  * row copy; at most E); each range's rows are copied on a side stream ahead

@@ -89,11 +89,10 @@ def _check(X, logits, W, R, T, H, F, E, topk, cap, out, sample=None, seed=0):
 # (recv_x given, sources one array, algo) of each launch path:
 #   staged         the GEMM's copy warps stage the rows into recv_x, its
 #                  tensor cores consume them unit by unit (sources separate)
-#   workspace      no recv_x: the GEMM's loader warps gather each tile's rows
-#                  from the sources into shared memory (the default)
+#   workspace      the same into library workspace (the default)
 #   gather         GEMM gathers from the sources with TMA gather4, no copy
 #   gather_recv_x  GEMM gathers; recv_x written beside it on a side stream
-#   fused_separate FCC_ALGO_FUSED with separate sources: as the default
+#   fused_separate FCC_ALGO_FUSED with separate sources: staged as by default
 #   unfused        a separate copy kernel into recv_x, then the GEMM
 #   unfused_workspace  the same into library workspace
 #   interdecom     expert-range chunks: each range's rows copied on a side
@@ -374,12 +373,11 @@ def test_grouped_gemm_unit_wait_reports_timeout_and_context_survives():
 
 @pytest.mark.parametrize("pair", [1, 2])
 @pytest.mark.parametrize("H", [320, 200])
-def test_moe_loader_gather_equals_copy_kernel(pair, H):
-    """The default with no recv_x: the GEMM's loader warps write each tile's
-    rows into shared memory with the layout a tiled TMA load gives, so the
-    products are bit for bit those of the rows staged by the copy kernel (the
-    same MMAs); H = 200 ends in a partial 64-wide k block (zero-filled).  A
-    second call repeats them."""
+def test_moe_workspace_staging_equals_copy_kernel(pair, H):
+    """The default with no recv_x: the GEMM's copy warps stage the rows in
+    library workspace, so the products are bit for bit those of the rows
+    staged by the copy kernel (the same MMAs); H = 200 ends in a partial
+    64-wide k block.  A second call repeats them."""
     R, T, F, E, topk = 4, 700, 264, 8, 2   # 350 rows an expert: a ragged unit
     X, logits, W = synth.moe_inputs(R, T, H, E, F, seed=13 + H)
     cap = R * T * topk
