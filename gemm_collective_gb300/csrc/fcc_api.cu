@@ -634,8 +634,12 @@ fcc_status fcc_gemv_ar(int R, const void* const* A, const void* const* B, void* 
     return rank_sum_unfused(R, A, B, out, R, false, M, N, K, out_f32, opts, d, ws, pl, st);
   }
   const GemvPlan g = gemv_plan(R, M, N, K, d->sms, opts);
+  // The splits of a column group sum through distributed shared memory when
+  // they fit on the device as clusters (no partials or tickets in memory);
+  // otherwise the last arriving CTA of a group sums the partials.
+  const bool cluster = gemv_cluster_fits(g.groups, g.splits);
   void* ws = nullptr;
-  if ((s = get_workspace(d, opts, g.total(), &ws)) != FCC_OK) return s;
+  if (!cluster && (s = get_workspace(d, opts, g.total(), &ws)) != FCC_OK) return s;
   GemvParams p;
   std::memset(&p, 0, sizeof(p));
   for (int r = 0; r < R; ++r) {
@@ -656,7 +660,11 @@ fcc_status fcc_gemv_ar(int R, const void* const* A, const void* const* B, void* 
   p.tickets = reinterpret_cast<int*>(static_cast<char*>(ws) + align_up(g.partial_bytes));
   p.status = d->status;
   p.timeout_ns = timeout_of(opts);
-  if ((opts == nullptr || opts->workspace == nullptr) && g.groups <= kMaxGemvGroups) {
+  p.cluster = cluster ? 1 : 0;
+  if (cluster) {
+    p.partials = nullptr;
+    p.tickets = nullptr;
+  } else if ((opts == nullptr || opts->workspace == nullptr) && g.groups <= kMaxGemvGroups) {
     // Library-held tickets: consistent across calls without clearing.
     if ((s = gemv_internal_tickets(&p.tickets)) != FCC_OK) return s;
   } else if (cudaMemsetAsync(p.tickets, 0, g.ticket_bytes, st) != cudaSuccess) {

@@ -257,10 +257,6 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) gemm_kernel(const __gri
   volatile int* bcast = reinterpret_cast<volatile int*>(tmem_slot + 2);
   int* tab = reinterpret_cast<int*>(tmem_slot + 4);  // grouped mode: expert tables
 
-  // Launched with programmatic stream serialization: no global memory is
-  // touched before the previous kernel on the stream has completed.
-  ptx::griddep_wait();
-  ptx::griddep_launch_dependents();
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   constexpr bool kPair = CG == 2;                      // tcgen05 cta_group::2 MMAs
@@ -294,14 +290,6 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) gemm_kernel(const __gri
       if constexpr (MODE != MODE_GROUPED) ptx::tma_prefetch_desc(&p.mapB[r]);
     }
   }
-  if constexpr (MODE == MODE_GROUPED) {
-    // The tables were written by the dispatch kernels before this launch.
-    for (int i = threadIdx.x; i <= p.E; i += blockDim.x) tab[i] = __ldcg(p.tile_start + i);
-    for (int i = threadIdx.x; i < p.E; i += blockDim.x) {
-      tab[p.E + 1 + i] = __ldcg(p.expert_rows + i);
-      tab[2 * p.E + 1 + i] = __ldcg(p.expert_base + i);
-    }
-  }
   const int k_iters = k_iters_of<MODE>(p);
   // Narrow tile: a half tile, or one whose output columns end in the first
   // half of its 256, so the B loads, the MMA width and the epilogue are halved.
@@ -323,9 +311,23 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) gemm_kernel(const __gri
     __syncthreads();
   }
   ptx::tc_fence_after();
+  // Launched with programmatic stream serialization: the set-up above touches
+  // no global memory (the tensor maps are kernel parameters), so it may
+  // overlap the previous kernel on the stream; everything below waits for it.
+  ptx::griddep_wait();
+  ptx::griddep_launch_dependents();
+  if constexpr (MODE == MODE_GROUPED) {
+    // The tables were written by the dispatch kernels before this launch.
+    for (int i = threadIdx.x; i <= p.E; i += blockDim.x) tab[i] = __ldcg(p.tile_start + i);
+    for (int i = threadIdx.x; i < p.E; i += blockDim.x) {
+      tab[p.E + 1 + i] = __ldcg(p.expert_rows + i);
+      tab[2 * p.E + 1 + i] = __ldcg(p.expert_base + i);
+    }
+    __syncthreads();
+  }
   const uint32_t tmem_base = *tmem_slot;
   const ptx::Waiter W{abort_flag, p.status, p.timeout_ns};
-  const int num_tiles = num_tiles_of<MODE>(p, tab);  // (after the barrier: tables loaded)
+  const int num_tiles = num_tiles_of<MODE>(p, tab);  // (tables loaded)
   // Phase timing (optional): this CTA's span, its epilogue's busy time and
   // its MMA warp's wait for an accumulator the epilogue still holds.
   unsigned long long* const times = p.phase_ns != nullptr ? p.phase_ns + 4ull * blockIdx.x

@@ -39,6 +39,7 @@ constexpr int kGroupCols = 512;                 // columns per CTA group (two ac
 constexpr int kStageCols = 256;                 // columns per pipeline stage (UMMA N)
 constexpr int kTok = kGemvTok;                  // token rows loaded per stage (M <= 16)
 constexpr int kTokStep = 8;                     // tokens per step of the final sum
+constexpr int kMaxClusterSplits = 16;           // splits a column group's cluster may hold
 constexpr int kStages = 6;
 constexpr uint32_t kBBox = kBK * 64 * 2;        // [64 k][64 n] bf16 = 8 KiB
 constexpr uint32_t kBStage = 4 * kBBox;         // 32 KiB: [64 k][256 n]
@@ -69,8 +70,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemv_ar_kernel(const __grid_c
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* bcast = reinterpret_cast<volatile int*>(tmem_slot + 2);
 
-  ptx::griddep_wait();  // launched with programmatic stream serialization
-  ptx::griddep_launch_dependents();
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int g = blockIdx.x / p.splits;              // column group
@@ -105,6 +104,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemv_ar_kernel(const __grid_c
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
+  // Launched with programmatic stream serialization: the set-up above touches
+  // no global memory (the tensor maps are kernel parameters), so it may
+  // overlap the previous kernel on the stream; everything below waits for it.
+  ptx::griddep_wait();
+  ptx::griddep_launch_dependents();
   const uint32_t tmem_base = *tmem_slot;
   const ptx::Waiter W{abort_flag, p.status, p.timeout_ns};
 
@@ -185,7 +189,31 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemv_ar_kernel(const __grid_c
     const int q = warp & 3;
     const int ep_tid = threadIdx.x - 64;
     const bool failed = (kb1 <= kb0) || !W.wait(tfull, 0);
-    if (!ptx::named_barrier_or(1, 128, failed)) {  // the epilogue warps stop together
+    if (p.cluster) {
+      // Cluster form: the partial rows stay in this CTA's shared memory (the
+      // stages are free once the accumulators are complete); the cluster
+      // sums them below.  A CTA that failed leaves its rows unwritten (the
+      // status word holds the error).
+      if (!failed && q == 0) {
+        ptx::tc_fence_after();
+        float* part = reinterpret_cast<float*>(sB) + lane * kGroupCols;
+        for (int sc = 0; sc < nstage_cols; ++sc) {
+#pragma unroll 1
+          for (int c = 0; c < kStageCols; c += 32) {
+            uint32_t v[32];
+            ptx::tmem_ld_32x32b_x32(tmem_base + sc * kStageCols + c, v);
+            ptx::tmem_ld_wait();
+            if (lane < p.M) {
+              float4* d = reinterpret_cast<float4*>(part + sc * kStageCols + c);
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                d[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                   __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
+            }
+          }
+        }
+      }
+    } else if (!ptx::named_barrier_or(1, 128, failed)) {  // the epilogue warps stop together
       ptx::tc_fence_after();
       if (q == 0) {
         float* part = p.partials + (static_cast<long long>(blockIdx.x) * p.M + lane) * kGroupCols;
@@ -292,7 +320,54 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemv_ar_kernel(const __grid_c
 
   __syncwarp();
   ptx::tc_fence_before();
-  __syncthreads();
+  if (p.cluster) {
+    // Every CTA of the column group's cluster holds its partial rows; CTA i
+    // (cluster rank i = split i) adds the splits' values of its slice of the
+    // group's columns in split order (the same additions, in the same order,
+    // as the ticket form's last arriver) and stores the sums to all R
+    // outputs.  The second cluster barrier keeps each CTA's shared memory
+    // alive until its peers have read it.
+    ptx::cluster_sync_all();
+    const int nsp = p.splits;
+    const int rank = static_cast<int>(ptx::cluster_ctarank());
+    const int cw = ((kGroupCols + nsp - 1) / nsp + 3) & ~3;  // a slice: whole float4s
+    const int c_lo = min(ncols, rank * cw), c_hi = min(ncols, c_lo + cw);
+    const int nvec = (c_hi - c_lo) / 4;
+    const uint32_t part0 = ptx::smem_addr(sB);
+    for (int item = threadIdx.x; item < p.M * nvec; item += blockDim.x) {
+      const int t = item / nvec;
+      const int c = c_lo + (item - t * nvec) * 4;
+      const uint32_t off = part0 + static_cast<uint32_t>((t * kGroupCols + c) * 4);
+      float4 x[kMaxClusterSplits];  // every split's value in flight, then added in order
+#pragma unroll
+      for (int sp = 0; sp < kMaxClusterSplits; ++sp)
+        if (sp < nsp) x[sp] = ptx::ld_shared_cluster_f4(ptx::mapa(off, static_cast<uint32_t>(sp)));
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int sp = 0; sp < kMaxClusterSplits; ++sp) {
+        if (sp < nsp) {
+          acc.x += x[sp].x;
+          acc.y += x[sp].y;
+          acc.z += x[sp].z;
+          acc.w += x[sp].w;
+        }
+      }
+      const long long o = static_cast<long long>(t) * p.N + col0 + c;
+      for (int r = 0; r < p.R; ++r) {
+        if (p.out_f32) {
+          *reinterpret_cast<float4*>(static_cast<float*>(p.out[r]) + o) = acc;
+        } else {
+          uint2 w;
+          w.x = ptx::pack_bf16x2(acc.x, acc.y);
+          w.y = ptx::pack_bf16x2(acc.z, acc.w);
+          *reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.out[r]) + o) = w;
+        }
+      }
+    }
+    ptx::cluster_sync_all();
+  } else {
+    __syncthreads();
+  }
   if (warp == 1) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem_base, kTmemCols);
@@ -308,7 +383,43 @@ cudaError_t launch_gemv(const GemvParams& p, int grid, cudaStream_t st) {
   const cudaError_t e = smem_attr_once(attr_set, gemv_ar_kernel, kSmemBytes);
   if (e != cudaSuccess) return e;
   return launch_pdl(gemv_ar_kernel, dim3(grid, 1, 1), dim3(kGemmThreads, 1, 1), kSmemBytes, st,
-                    1u, p);
+                    p.cluster ? static_cast<unsigned>(p.splits) : 1u, p);
+}
+
+// Whether `groups` clusters of `splits` GEMV CTAs (one per SM) fit on the
+// current device at once, so the cluster form of the final sum runs in one
+// wave; looked up once per device and split count.
+bool gemv_cluster_fits(int groups, int splits) {
+  if (splits < 2 || splits > kMaxClusterSplits) return false;
+  static int cache[64][kMaxClusterSplits + 1] = {};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+  std::lock_guard<std::mutex> lk(mu);
+  int& n = cache[dev][splits];
+  if (n == 0) {
+    n = -1;
+    if (cudaFuncSetAttribute(gemv_ar_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmemBytes) == cudaSuccess &&
+        cudaFuncSetAttribute(gemv_ar_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+            cudaSuccess) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(static_cast<unsigned>(splits * groups), 1, 1);
+      cfg.blockDim = dim3(kGemmThreads, 1, 1);
+      cfg.dynamicSmemBytes = kSmemBytes;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = static_cast<unsigned>(splits);
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      int c = 0;
+      if (cudaOccupancyMaxActiveClusters(&c, gemv_ar_kernel, &cfg) == cudaSuccess) n = c;
+    }
+    cudaGetLastError();  // (a refused query leaves no sticky error)
+  }
+  return n >= groups;
 }
 
 // Arrival tickets of the default path (no caller workspace): a library array,

@@ -122,6 +122,8 @@ struct GemvParams {
   unsigned gen;         // call generation, 1..2^24-1 (never 0: zeroed tickets are "old")
   int* status;
   unsigned long long timeout_ns;
+  int cluster;          // 1: a column group's splits are one cluster and sum through
+                        // distributed shared memory (no partials, no tickets)
 };
 
 // Launchers (return cudaSuccess or the launch error).
@@ -174,6 +176,8 @@ int gemm_smem_bytes(int cg);
 // Clusters of cg CTAs of the GEMM kernel that fit on the current device at once.
 int gemm_max_clusters(int cg);
 cudaError_t launch_gemv(const GemvParams& p, int grid, cudaStream_t st);
+// Whether the cluster form of the GEMV's final sum fits the current device.
+bool gemv_cluster_fits(int groups, int splits);
 int gemv_smem_bytes();
 // GEMV grid shape for N columns and R*K rows over `sms` SMs (max_ctas 0 = no cap).
 void gemv_shape(int64_t N, int R, int64_t K, int sms, int max_ctas, int* groups, int* splits);

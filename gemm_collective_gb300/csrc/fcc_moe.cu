@@ -6,10 +6,11 @@
 //   1. route_kernel   eight threads per token: top-k experts by logit (ties
 //                     to the lower index), softmax gates, and a per-chunk
 //                     expert histogram (chunk = 128 tokens of one source rank).
-//   2. offsets_kernel one CTA: for every expert the exclusive prefix of its
+//   2. offsets_kernel one CTA per expert: the exclusive prefix of its
 //                     histogram over the chunks (a fixed order) and its count;
-//                     send counts, each expert's first row in its receiving
-//                     rank's buffer, and the grouped GEMM's tile table.
+//                     the last CTA to finish: send counts, each expert's first
+//                     row in its receiving rank's buffer, and the grouped
+//                     GEMM's tile table.
 //   3. rank_kernel    one CTA per chunk: the stable rank of every assignment
 //                     within its expert (warp match + popc, then a prefix over
 //                     the CTA's warps), i.e. its receive row; writes recv_src.
@@ -70,6 +71,7 @@ struct MoeArgs {
   int32_t* row_of;        // [R*T*topk]: receive row of each assignment, -1 if dropped
   int32_t* ready;         // in-kernel staging: rows copied per (expert, m tile) unit
   int32_t* copy_cursor;   // in-kernel staging: next chunk to claim
+  int32_t* offsets_ticket;  // CTAs of offsets_kernel done (the router zeroes it)
   // Copy-engine dispatch: per source rank s a send buffer of its kept rows in
   // (expert, token, slot) order; srcoff[s][e] = assignments to e from the
   // sources before s (srcoff[R][e] = all of e's); send_base[s][e] = the first
@@ -112,6 +114,7 @@ __global__ void __launch_bounds__(kChunkTok * kRouteSub) route_kernel(const MoeA
   const int s = chunk / a.chunks_per_rank;
   const int t0 = (chunk - s * a.chunks_per_rank) * kChunkTok;
   const int E = a.E;
+  if (chunk == 0 && threadIdx.x == 0) *a.offsets_ticket = 0;  // (read after this grid ends)
   if (threadIdx.x < FCC_MAX_EXPERTS) hist[threadIdx.x] = 0;
   __syncthreads();
   const int t = t0 + static_cast<int>(threadIdx.x) / kRouteSub;
@@ -175,59 +178,67 @@ __global__ void __launch_bounds__(kChunkTok * kRouteSub) route_kernel(const MoeA
         hist[threadIdx.x];
 }
 
-// One CTA of 1024 threads after the router: for every expert the exclusive
-// prefix of its histogram over the chunks, in chunk order (source rank, then
-// token), so chunk_off[e][c] is the number of assignments to e that precede
-// chunk c in (s, t, slot) order (warp w scans experts w and w + 32, 32 chunks
-// per step, integer sums in a fixed shuffle order); then each expert's first
-// row in its receiving rank's buffer and its kept rows (capacity), the send
-// counts and the grouped GEMM's tile table.
-__global__ void __launch_bounds__(1024) offsets_kernel(const MoeArgs a) {
+// One CTA of 256 threads per expert e after the router: the exclusive prefix
+// of e's histogram over the chunks, in chunk order (source rank, then token),
+// so chunk_off[e][c] is the number of assignments to e that precede chunk c
+// in (s, t, slot) order (integer sums in a fixed order of warp shuffles);
+// and e's count.  The last CTA to finish (a ticket the router zeroed) then
+// computes each expert's first row in its receiving rank's buffer and its
+// kept rows (capacity), the send counts and the grouped GEMM's tile table.
+__global__ void __launch_bounds__(256) offsets_kernel(const MoeArgs a) {
   ptx::griddep_wait();  // launched with programmatic stream serialization
   ptx::griddep_launch_dependents();
+  __shared__ int wsum[8];
+  __shared__ int last_s;
   __shared__ int counts[FCC_MAX_EXPERTS];
   __shared__ int rows[FCC_MAX_EXPERTS];
   __shared__ int srcoff[FCC_MAX_RANKS + 1][FCC_MAX_EXPERTS];  // prefix at each source's first chunk
   __shared__ int units_s;
   const int nchunks = a.R * a.chunks_per_rank;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  constexpr int kPer = 8;  // consecutive chunks per lane (one 32-byte run of counts)
-  for (int e = warp; e < a.E; e += 32) {
+  {
+    const int e = blockIdx.x;
     const int32_t* cc = a.chunk_counts + static_cast<long long>(e) * nchunks;  // expert-major
     int carry = 0;
-    for (int c0 = 0; c0 < nchunks; c0 += 32 * kPer) {
-      const int cb = c0 + lane * kPer;
-      int v[kPer];
-#pragma unroll
-      for (int j = 0; j < kPer; ++j) v[j] = cb + j < nchunks ? __ldcg(cc + cb + j) : 0;
-      int run = 0;
-#pragma unroll
-      for (int j = 0; j < kPer; ++j) run += v[j];
-      int incl = run;
+    for (int c0 = 0; c0 < nchunks; c0 += 256) {
+      const int c = c0 + static_cast<int>(threadIdx.x);
+      const int v = c < nchunks ? __ldcg(cc + c) : 0;
+      int incl = v;
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {
         const int y = __shfl_up_sync(0xffffffffu, incl, off);
         if (lane >= off) incl += y;
       }
-      int before = carry + incl - run;
+      if (lane == 31) wsum[warp] = incl;
+      __syncthreads();
+      int before = carry + incl - v, total = 0;
 #pragma unroll
-      for (int j = 0; j < kPer; ++j) {
-        const int c = cb + j;
-        if (c < nchunks) {
-          a.chunk_off[static_cast<long long>(e) * nchunks + c] = before;  // (coalesced)
-          if (c % a.chunks_per_rank == 0) srcoff[c / a.chunks_per_rank][e] = before;
-        }
-        before += v[j];
+      for (int w = 0; w < 8; ++w) {
+        if (w < warp) before += wsum[w];
+        total += wsum[w];
       }
-      carry += __shfl_sync(0xffffffffu, incl, 31);
+      if (c < nchunks) a.chunk_off[static_cast<long long>(e) * nchunks + c] = before;
+      carry += total;
+      __syncthreads();
     }
-    if (lane == 0) {
-      counts[e] = carry;
-      srcoff[a.R][e] = carry;
-      a.expert_counts[e] = carry;
-    }
+    if (threadIdx.x == 0) a.expert_counts[e] = carry;
   }
-  __syncthreads();  // (also orders this CTA's chunk_off writes before the reads below)
+  // The last CTA to arrive sees every expert's prefix and count.
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) last_s = atomicAdd(a.offsets_ticket, 1) == a.E - 1 ? 1 : 0;
+  __syncthreads();
+  if (!last_s) return;
+  __threadfence();
+  for (int i = threadIdx.x; i < a.E; i += blockDim.x) {
+    counts[i] = __ldcg(a.expert_counts + i);
+    srcoff[a.R][i] = counts[i];
+  }
+  for (int i = threadIdx.x; i < a.R * a.E; i += blockDim.x) {
+    const int s = i / a.E, f = i - (i / a.E) * a.E;
+    srcoff[s][f] = __ldcg(a.chunk_off + static_cast<long long>(f) * nchunks + s * a.chunks_per_rank);
+  }
+  __syncthreads();
   const int e = threadIdx.x;
   if (e < a.E) {
     const int d = e / a.Eloc;
@@ -499,7 +510,7 @@ struct MoePlan {
   int nchunks = 0;
   size_t off_stage = 0;  // staged rows when the caller passes no recv_x ([R][cap][H] bf16)
   size_t off_chunk_counts = 0, off_chunk_off = 0, off_base = 0, off_rows = 0, off_tiles = 0,
-         off_row_of = 0, off_ready = 0, off_cursor = 0, total = 0;
+         off_row_of = 0, off_ready = 0, off_cursor = 0, off_ticket = 0, total = 0;
   // copy-engine dispatch: tables and the send buffers ([R][T*topk][H] bf16)
   size_t off_ce_srcoff = 0, off_ce_send_base = 0, off_ce_plan = 0, off_send = 0;
 };
@@ -543,6 +554,8 @@ MoePlan moe_plan(int R, int64_t T, int E, int topk, int64_t H = 0, int64_t cap =
   p.off_ready = off;
   off += up256((static_cast<size_t>(R) * T * topk / 128 + E + 1) * 4);
   p.off_cursor = off;
+  off += 256;
+  p.off_ticket = off;
   off += 256;
   p.off_ce_srcoff = off;
   off += up256(static_cast<size_t>(R + 1) * E * 4);
@@ -696,6 +709,7 @@ fcc_status fcc_moe_dispatch_gemm(int R, const void* const* X, const float* const
   a.row_of = reinterpret_cast<int32_t*>(base + plan.off_row_of);
   a.ready = copy_in_gemm ? reinterpret_cast<int32_t*>(base + plan.off_ready) : nullptr;
   a.copy_cursor = copy_in_gemm ? reinterpret_cast<int32_t*>(base + plan.off_cursor) : nullptr;
+  a.offsets_ticket = reinterpret_cast<int32_t*>(base + plan.off_ticket);
   a.ce_srcoff = reinterpret_cast<int32_t*>(base + plan.off_ce_srcoff);
   a.ce_send_base = reinterpret_cast<int32_t*>(base + plan.off_ce_send_base);
   a.ce_plan = reinterpret_cast<int32_t*>(base + plan.off_ce_plan);
@@ -747,7 +761,7 @@ fcc_status fcc_moe_dispatch_gemm(int R, const void* const* X, const float* const
   // kernel's launch overlaps the one before it, and waits for it in-kernel.
   if (launch_pdl(route_kernel, dim3(plan.nchunks), dim3(kChunkTok * kRouteSub), 0, st, 1u, a) !=
           cudaSuccess ||
-      launch_pdl(offsets_kernel, dim3(1), dim3(1024), 0, st, 1u, a) != cudaSuccess ||
+      launch_pdl(offsets_kernel, dim3(E), dim3(256), 0, st, 1u, a) != cudaSuccess ||
       launch_pdl(rank_kernel, dim3(plan.nchunks), dim3(256), 0, st, 1u, a) != cudaSuccess)
     return FCC_ERR_CUDA;
   uint64_t launches = 3;
