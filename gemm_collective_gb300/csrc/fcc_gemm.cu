@@ -564,11 +564,13 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) gemm_kernel(const __gri
         const int total = cstart[p.e_hi];
         const int vec = p.K / 8;  // 16-byte vectors per row
         constexpr int kV = 16;    // vectors in flight per lane
-        while (true) {
-          int c = 0;
-          if (lane == 0) c = atomicAdd(p.copy_cursor, 1);
-          c = __shfl_sync(0xffffffffu, c, 0);
-          if (c >= total) break;
+        int c = 0;
+        if (lane == 0) c = atomicAdd(p.copy_cursor, 1);
+        c = __shfl_sync(0xffffffffu, c, 0);
+        while (c < total) {
+          // The next chunk's claim is in flight while this one is copied.
+          int c_next = 0;
+          if (lane == 0) c_next = atomicAdd(p.copy_cursor, 1);
           // expert of chunk c: the last e with cstart[e] <= c
           int lo = p.e_lo, hi = p.e_hi - 1;
           while (lo < hi) {
@@ -582,13 +584,25 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) gemm_kernel(const __gri
           const int r0 = (c - cstart[e]) * kCopyRows;  // first row within the expert
           const int n = min(kCopyRows, rows_t[e] - r0);
           const int d = e / p.Eloc;
+          // Lane i < n finds row i's source; every lane then prefetches its share
+          // of the chunk's source rows into L2 (128-byte lines, the load path's
+          // own prefetch), so only the chunk's first row waits for DRAM.
+          const uint4* my_src = nullptr;
+          if (lane < n) {
+            const int src = __ldcg(p.recv_src[d] + base_t[e] + r0 + lane);
+            const int s = src / p.T;
+            my_src = reinterpret_cast<const uint4*>(p.src_x[s]) +
+                     static_cast<long long>(src - s * p.T) * vec;
+          }
+          for (int i = 1; i < n; ++i) {
+            const char* rp = reinterpret_cast<const char*>(
+                __shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(my_src), i));
+            for (int off = lane * 128; off < vec * 16; off += 32 * 128) ptx::prefetch_l2(rp + off);
+          }
           for (int i = 0; i < n; ++i) {
             const int row = base_t[e] + r0 + i;
-            const int src = __ldcg(p.recv_src[d] + row);
-            const int s = src / p.T;
-            const int t = src - s * p.T;
-            const uint4* sp =
-                reinterpret_cast<const uint4*>(p.src_x[s]) + static_cast<long long>(t) * vec;
+            const uint4* sp = reinterpret_cast<const uint4*>(
+                __shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(my_src), i));
             uint4* dp = reinterpret_cast<uint4*>(p.stage_x[d]) + static_cast<long long>(row) * vec;
             for (int v0 = 0; v0 < vec; v0 += 32 * kV) {
               uint4 x[kV];
@@ -611,6 +625,7 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) gemm_kernel(const __gri
             __threadfence();
             atomicAdd(p.ready + tab[e] / p.tiles_n + r0 / TM, n);
           }
+          c = __shfl_sync(0xffffffffu, c_next, 0);
         }
       }
     }
