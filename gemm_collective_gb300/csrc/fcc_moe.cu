@@ -6,14 +6,18 @@
 //   1. route_kernel   eight threads per token: top-k experts by logit (ties
 //                     to the lower index), softmax gates, and a per-chunk
 //                     expert histogram (chunk = 128 tokens of one source rank).
-//   2. offsets_kernel one CTA per expert: the exclusive prefix of its
-//                     histogram over the chunks (a fixed order) and its count;
-//                     the last CTA to finish: send counts, each expert's first
-//                     row in its receiving rank's buffer, and the grouped
-//                     GEMM's tile table.
-//   3. rank_kernel    one CTA per chunk: the stable rank of every assignment
-//                     within its expert (warp match + popc, then a prefix over
-//                     the CTA's warps), i.e. its receive row; writes recv_src.
+//   2. place_kernel   one CTA per chunk: its per-expert prefix over the
+//                     chunks before it (a fixed order) and every expert's
+//                     count, each CTA summing the whole histogram itself; then
+//                     the stable rank of each of its assignments within its
+//                     expert (warp match + popc, then a prefix over the CTA's
+//                     warps), i.e. its receive row; writes recv_src.  CTA 0
+//                     also writes each expert's first row in its receiving
+//                     rank's buffer and the grouped GEMM's tile table, and the
+//                     first CTA of each source rank its send counts.  Past 512
+//                     chunks the same integers come from two kernels:
+//                     offsets_kernel (one CTA per expert scans its histogram;
+//                     the last to finish derives the tables) and rank_kernel.
 //   4. the all-to-all row movement, into the caller's recv_x or into
 //                     workspace.  By default the grouped GEMM's own copy warps
 //                     move each (expert, m tile) unit of rows, in tile order,
@@ -85,7 +89,8 @@ struct MoeArgs {
 };
 
 // Grid: one CTA per chunk of 128 tokens (of one source rank), eight threads
-// per token (1024 threads).  Thread q of a token scans its slice of the E
+// per token (1024 threads; at most 32 registers, so two CTAs fit an SM and
+// the 256 chunks of 8 x 4096 tokens run in one wave).  Thread q of a token scans its slice of the E
 // logits for its own top two (a strictly larger logit replaces, so an equal
 // logit keeps the lower expert index); the eight partial lists are merged by
 // xor shuffles (the same total order: larger logit, then lower index), so
@@ -106,7 +111,7 @@ __device__ __forceinline__ bool better(const Cand& a, const Cand& b) {
   return a.v > b.v || (a.v == b.v && a.i < b.i);
 }
 
-__global__ void __launch_bounds__(kChunkTok * kRouteSub) route_kernel(const MoeArgs a) {
+__global__ void __launch_bounds__(kChunkTok * kRouteSub, 2) route_kernel(const MoeArgs a) {
   ptx::griddep_wait();  // launched with programmatic stream serialization
   ptx::griddep_launch_dependents();
   __shared__ int hist[FCC_MAX_EXPERTS];
@@ -176,6 +181,39 @@ __global__ void __launch_bounds__(kChunkTok * kRouteSub) route_kernel(const MoeA
   if (threadIdx.x < E)
     a.chunk_counts[static_cast<long long>(threadIdx.x) * a.R * a.chunks_per_rank + chunk] =
         hist[threadIdx.x];
+}
+
+// The grouped GEMM's tile table from the experts' kept rows (warp 0: the
+// exclusive prefix of the experts' tiles, two experts a lane), then the
+// in-kernel staging counters' reset (the whole CTA), which start at zero for
+// every call.  rows[] is in shared memory, written before a barrier.
+__device__ __forceinline__ void write_tiles(const MoeArgs& a, const int* rows, int* units_s) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (warp == 0) {
+    const int ea = 2 * lane, eb = 2 * lane + 1;
+    const int ta = ea < a.E ? ((rows[ea] + a.tile_m - 1) / a.tile_m) * a.tiles_n : 0;
+    const int tb = eb < a.E ? ((rows[eb] + a.tile_m - 1) / a.tile_m) * a.tiles_n : 0;
+    int incl = ta + tb;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += y;
+    }
+    const int excl = incl - ta - tb;
+    if (ea < a.E) a.tile_start[ea] = excl;
+    if (eb < a.E) a.tile_start[eb] = excl + ta;
+    const int total = __shfl_sync(0xffffffffu, incl, 31);
+    if (lane == 0) {
+      a.tile_start[a.E] = total;
+      *units_s = total / a.tiles_n;  // (m tile units in all)
+    }
+  }
+  if (a.ready != nullptr) {
+    __syncthreads();
+    const int units = *units_s;
+    for (int u = threadIdx.x; u < units; u += blockDim.x) a.ready[u] = 0;
+    if (threadIdx.x == 0) *a.copy_cursor = 0;
+  }
 }
 
 // One CTA of 256 threads per expert e after the router: the exclusive prefix
@@ -261,58 +299,35 @@ __global__ void __launch_bounds__(256) offsets_kernel(const MoeArgs a) {
     a.send_counts[e] = sum;
   }
   __syncthreads();
-  if (warp == 0) {
-    // tile_start: exclusive prefix of the experts' tiles, two experts a lane
-    const int ea = 2 * lane, eb = 2 * lane + 1;
-    const int ta = ea < a.E ? ((rows[ea] + a.tile_m - 1) / a.tile_m) * a.tiles_n : 0;
-    const int tb = eb < a.E ? ((rows[eb] + a.tile_m - 1) / a.tile_m) * a.tiles_n : 0;
-    int incl = ta + tb;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, incl, off);
-      if (lane >= off) incl += y;
-    }
-    const int excl = incl - ta - tb;
-    if (ea < a.E) a.tile_start[ea] = excl;
-    if (eb < a.E) a.tile_start[eb] = excl + ta;
-    const int total = __shfl_sync(0xffffffffu, incl, 31);
-    if (lane == 0) {
-      a.tile_start[a.E] = total;
-      units_s = total / a.tiles_n;  // (m tile units in all)
-    }
-  }
-  // The in-kernel staging counters start at zero for every call.
-  if (a.ready != nullptr) {
-    __syncthreads();
-    const int units = units_s;
-    for (int u = threadIdx.x; u < units; u += blockDim.x) a.ready[u] = 0;
-    if (threadIdx.x == 0) *a.copy_cursor = 0;
-  }
+  write_tiles(a, rows, &units_s);
 }
 
-// One CTA of 256 threads per chunk; thread i holds assignment i of the chunk
-// (token t0 + i/topk, slot i%topk), so the 8 warps hold consecutive runs of
-// assignments in (t, slot) order.
-__global__ void __launch_bounds__(256) rank_kernel(const MoeArgs a) {
-  ptx::griddep_wait();  // launched with programmatic stream serialization
-  ptx::griddep_launch_dependents();
-  __shared__ int cnt[8][FCC_MAX_EXPERTS];
-  const int chunk = blockIdx.x;
+// Receive rows of one chunk's assignments.  Thread i < 256 of the CTA holds
+// assignment i of the chunk (token t0 + i/topk, slot i%topk), so warps 0-7
+// hold consecutive runs in (t, slot) order.  pre[e] = assignments to e in
+// earlier chunks, base[e] = e's first row in its receiving rank's buffer,
+// rows[e] = e's kept rows; all three in shared memory, written before the
+// call (its first barrier orders them).  The rank within the chunk is the
+// warp-match rank plus a prefix over the lower warps, so each expert's rows
+// follow (s, t, slot) order.
+__device__ __forceinline__ void rank_chunk(const MoeArgs& a, int chunk, const int* pre,
+                                           const int* base, const int* rows,
+                                           int (*cnt)[FCC_MAX_EXPERTS]) {
   const int s = chunk / a.chunks_per_rank;
   const int t0 = (chunk - s * a.chunks_per_rank) * kChunkTok;
-  const int t1 = min(a.T, t0 + kChunkTok);
-  const int n_assign = (t1 - t0) * a.topk;
+  const int n_assign = (min(a.T, t0 + kChunkTok) - t0) * a.topk;  // <= 256 (topk <= 2)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int i = threadIdx.x; i < 8 * FCC_MAX_EXPERTS; i += blockDim.x) (&cnt[0][0])[i] = 0;
   __syncthreads();
   const int i = threadIdx.x;
   const bool valid = i < n_assign;
-  const int t = t0 + i / a.topk;
-  const int e = valid ? a.idx[s][static_cast<long long>(t0) * a.topk + i] : -1;
-  const unsigned peers = __match_any_sync(0xffffffffu, e);
-  const unsigned lower = (1u << lane) - 1u;
-  const int rank_in_warp = __popc(peers & lower);
-  if (valid && rank_in_warp == 0) cnt[warp][e] = __popc(peers);
+  int e = -1, rank_in_warp = 0;
+  if (warp < 8) {
+    e = valid ? a.idx[s][static_cast<long long>(t0) * a.topk + i] : -1;
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    rank_in_warp = __popc(peers & ((1u << lane) - 1u));
+    if (valid && rank_in_warp == 0) cnt[warp][e] = __popc(peers);
+  }
   __syncthreads();
   // exclusive prefix over the warps, per expert
   if (threadIdx.x < a.E) {
@@ -325,16 +340,106 @@ __global__ void __launch_bounds__(256) rank_kernel(const MoeArgs a) {
   }
   __syncthreads();
   if (valid) {
-    const int pos = a.chunk_off[static_cast<long long>(e) * a.R * a.chunks_per_rank + chunk] +
-                    cnt[warp][e] +
-                    rank_in_warp;
+    const int pos = pre[e] + cnt[warp][e] + rank_in_warp;
     const int d = e / a.Eloc;
-    const int row = a.expert_base[e] + pos;
-    const bool kept = pos < a.expert_rows[e];
+    const int row = base[e] + pos;
+    const bool kept = pos < rows[e];
     const long long gidx = (static_cast<long long>(s) * a.T + t0) * a.topk + i;
     a.row_of[gidx] = kept ? row : -1;
-    if (kept) a.recv_src[d][row] = s * a.T + t;
+    if (kept) a.recv_src[d][row] = s * a.T + t0 + i / a.topk;
   }
+}
+
+// One CTA of 256 threads per chunk, after offsets_kernel.
+__global__ void __launch_bounds__(256) rank_kernel(const MoeArgs a) {
+  ptx::griddep_wait();  // launched with programmatic stream serialization
+  ptx::griddep_launch_dependents();
+  __shared__ int cnt[8][FCC_MAX_EXPERTS];
+  __shared__ int pre[FCC_MAX_EXPERTS], base[FCC_MAX_EXPERTS], rows[FCC_MAX_EXPERTS];
+  const int chunk = blockIdx.x;
+  const long long nchunks = static_cast<long long>(a.R) * a.chunks_per_rank;
+  for (int e = threadIdx.x; e < a.E; e += blockDim.x) {
+    pre[e] = a.chunk_off[e * nchunks + chunk];
+    base[e] = a.expert_base[e];
+    rows[e] = a.expert_rows[e];
+  }
+  rank_chunk(a, chunk, pre, base, rows, cnt);
+}
+
+// Offsets and ranks in one kernel after the router, for up to
+// kPlaceMaxChunks chunks: one CTA of 1024 threads per chunk.  Every CTA sums
+// the whole chunk histogram itself (16 threads an expert, then a fixed xor
+// tree), which gives its chunk's per-expert prefix and every expert's total,
+// so no CTA waits for another; the chunk's ranks follow as in rank_kernel.
+// CTA 0 also writes the experts' counts, first rows and kept rows, the tile
+// table and the staging counters' reset, and the first CTA of each source
+// rank s writes row s of send_counts.  The same integers as offsets_kernel +
+// rank_kernel, in fewer launches; the histogram is read once per chunk, so
+// past the limit the two-kernel form is used.
+constexpr int kPlaceMaxChunks = 512;
+constexpr int kPlaceSub = 16;  // threads per expert
+
+__global__ void __launch_bounds__(FCC_MAX_EXPERTS * kPlaceSub) place_kernel(const MoeArgs a) {
+  ptx::griddep_wait();  // launched with programmatic stream serialization
+  ptx::griddep_launch_dependents();
+  __shared__ int cnt[8][FCC_MAX_EXPERTS];
+  __shared__ int pre[FCC_MAX_EXPERTS], tot[FCC_MAX_EXPERTS], src_sum[FCC_MAX_EXPERTS];
+  __shared__ int base[FCC_MAX_EXPERTS], rows[FCC_MAX_EXPERTS];
+  __shared__ int units_s;
+  const int nchunks = a.R * a.chunks_per_rank;
+  const int chunk = blockIdx.x;
+  const int s = chunk / a.chunks_per_rank;
+  const int s_lo = s * a.chunks_per_rank, s_hi = s_lo + a.chunks_per_rank;
+  const int e = threadIdx.x / kPlaceSub, j = threadIdx.x % kPlaceSub;
+  int p = 0, n = 0, ns = 0;  // before this chunk, all chunks, chunks of source s
+  if (e < a.E) {
+    const int32_t* cc = a.chunk_counts + static_cast<long long>(e) * nchunks;  // expert-major
+    for (int c = j; c < nchunks; c += kPlaceSub) {
+      const int v = __ldcg(cc + c);
+      n += v;
+      if (c < chunk) p += v;
+      if (c >= s_lo && c < s_hi) ns += v;
+    }
+  }
+#pragma unroll
+  for (int off = kPlaceSub / 2; off > 0; off >>= 1) {
+    p += __shfl_xor_sync(0xffffffffu, p, off);
+    n += __shfl_xor_sync(0xffffffffu, n, off);
+    ns += __shfl_xor_sync(0xffffffffu, ns, off);
+  }
+  if (j == 0 && e < a.E) {
+    pre[e] = p;
+    tot[e] = n;
+    src_sum[e] = ns;
+  }
+  __syncthreads();
+  if (threadIdx.x < a.E) {
+    const int f = threadIdx.x, d = f / a.Eloc;
+    long long b = 0;
+    for (int g = d * a.Eloc; g < f; ++g) b += tot[g];
+    const long long room = static_cast<long long>(a.cap) - b;
+    const int kept = static_cast<int>(max(0ll, min(static_cast<long long>(tot[f]), room)));
+    base[f] = static_cast<int>(min(b, static_cast<long long>(a.cap)));
+    rows[f] = kept;
+    a.chunk_off[static_cast<long long>(f) * nchunks + chunk] = pre[f];
+    if (chunk == 0) {
+      a.expert_counts[f] = tot[f];
+      a.expert_base[f] = base[f];
+      a.expert_rows[f] = kept;
+      if (f == (d + 1) * a.Eloc - 1 && b + tot[f] > a.cap && a.status != nullptr)
+        atomicCAS(a.status, 0, FCC_ERR_CAPACITY);
+    }
+  }
+  if (chunk == s_lo && threadIdx.x < a.R) {
+    // send_counts[s][d]: assignments from source rank s to the experts of rank d
+    const int d = threadIdx.x;
+    int sum = 0;
+    for (int f = d * a.Eloc; f < (d + 1) * a.Eloc; ++f) sum += src_sum[f];
+    a.send_counts[s * a.R + d] = sum;
+  }
+  __syncthreads();
+  if (chunk == 0) write_tiles(a, rows, &units_s);
+  rank_chunk(a, chunk, pre, base, rows, cnt);
 }
 
 // One warp per token: read the token's row once (16-byte loads) and write it to
@@ -759,12 +864,21 @@ fcc_status fcc_moe_dispatch_gemm(int R, const void* const* X, const float* const
 
   // The chain on `st` launches with programmatic stream serialization: each
   // kernel's launch overlaps the one before it, and waits for it in-kernel.
+  // Up to kPlaceMaxChunks chunks, the offsets and ranks are one kernel.
+  const bool place = plan.nchunks <= kPlaceMaxChunks;
   if (launch_pdl(route_kernel, dim3(plan.nchunks), dim3(kChunkTok * kRouteSub), 0, st, 1u, a) !=
-          cudaSuccess ||
-      launch_pdl(offsets_kernel, dim3(E), dim3(256), 0, st, 1u, a) != cudaSuccess ||
-      launch_pdl(rank_kernel, dim3(plan.nchunks), dim3(256), 0, st, 1u, a) != cudaSuccess)
+      cudaSuccess)
     return FCC_ERR_CUDA;
-  uint64_t launches = 3;
+  if (place) {
+    if (launch_pdl(place_kernel, dim3(plan.nchunks), dim3(FCC_MAX_EXPERTS * kPlaceSub), 0, st,
+                   1u, a) != cudaSuccess)
+      return FCC_ERR_CUDA;
+  } else if (launch_pdl(offsets_kernel, dim3(E), dim3(256), 0, st, 1u, a) != cudaSuccess ||
+             launch_pdl(rank_kernel, dim3(plan.nchunks), dim3(256), 0, st, 1u, a) !=
+                 cudaSuccess) {
+    return FCC_ERR_CUDA;
+  }
+  uint64_t launches = place ? 2 : 3;
   const int grid = std::max(cg, (sms / cg) * cg);
 
   if (interdecom) {

@@ -134,6 +134,20 @@ def test_moe_small(R, T, H, F, E, topk, pair, path):
     _check(X, logits, W, R, T, H, F, E, topk, cap, out)
 
 
+@pytest.mark.parametrize("T", [8192, 8193])
+def test_moe_placement_either_side_of_the_one_kernel_limit(T):
+    """Up to 512 chunks of 128 tokens the offsets and the ranks are one kernel
+    (every CTA sums the whole chunk histogram itself); past that, a scan
+    kernel and a rank kernel.  8 x 8192 tokens are 512 chunks, 8 x 8193 are
+    520: both give the oracle's integers and rows."""
+    R, H, F, E, topk = 8, 64, 64, 64, 2
+    X, logits, W = synth.moe_inputs(R, T, H, E, F, seed=23)
+    cap = 2 * T * topk
+    for algo in (fcc.FCC_ALGO_AUTO, fcc.FCC_ALGO_CE):
+        out = _run(X, logits, W, R, T, H, F, E, topk, cap, opts=fcc.make_opts(algo=algo))
+        _check(X, logits, W, R, T, H, F, E, topk, cap, out, sample=384)
+
+
 def test_moe_ties_and_f32_output():
     R, T, H, F, E, topk = 2, 128, 64, 64, 8, 2
     X, logits, W = synth.moe_inputs(R, T, H, E, F, seed=5)
