@@ -89,7 +89,8 @@ typedef struct {
   void *workspace;         /* device scratch, or NULL for the internal pool */
   size_t workspace_bytes;
   /* Tensor-core tile shape of the GEMMs: 0 = automatic (a CTA pair when the
-   * rows exceed 128, else 1), 1 = one CTA per 128 x 256 tile, 2 = a CTA pair
+   * rows exceed 128 and the 128 x 256 tiles outnumber the CTAs, else 1; the
+   * MoE expert GEMM: a CTA pair), 1 = one CTA per 128 x 256 tile, 2 = a CTA pair
    * (cluster of 2, tcgen05 cta_group::2) per 256 x 256 tile.  Any other value
    * is FCC_ERR_INVALID.  Every TMA load lands in the issuing CTA's own shared
    * memory (no multicast loads), so the library may run in processes that
