@@ -429,6 +429,11 @@ def small_rs_latency(fcc, torch, np, synth, dev, stream):
         res["graph_us"] = 1e3 * time_calls(g.replay, 10, 2, stream) / 100
     except Exception as e:  # capture is optional information
         res["graph_error"] = str(e)[:200]
+    # the same call forced onto CTA pairs (the automatic shape runs single
+    # CTAs here: one round of tiles), back to back
+    o2 = fcc.make_opts(cta_pair=2)
+    res["pairs_plain_us"] = 1e3 * time_calls(
+        lambda: fcc.fcc_gemm_rs(w.R, pA, pB, pO, w.M, w.N, w.K, 0, 2, o2, stream), 200, 10, stream)
     res["TFLOP/s_plain"] = w.flops() / (res["plain_us"] * 1e-6) / 1e12
     return res
 
