@@ -123,7 +123,7 @@ def test_embedding_full_workload_sampled():
     g = rng.integers(0, w.R * w.B, size=64)
     t = rng.integers(0, w.tables, size=64)
     ref = oracle.embedding_bags(tables, offsets, indices, t, g)
-    for algo in (fcc.FCC_ALGO_AUTO, fcc.FCC_ALGO_UNFUSED):  # (AUTO is the fused form)
+    for algo in (fcc.FCC_ALGO_AUTO, fcc.FCC_ALGO_FUSED):  # (AUTO is the staged form)
         out, st = _run(w.R, w.tables, w.V, w.D, w.B, *dev, algo=algo)
         assert st == fcc.FCC_OK
         got = np.stack([to_f64(out[gi // w.B][gi % w.B, ti]) for gi, ti in zip(g, t)])
