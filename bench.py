@@ -53,7 +53,8 @@ def parse():
     ap.add_argument("--details", default=None,
                     help="also write every leg's full results (paths, sweeps) to this file")
     ap.add_argument("--op", default=None,
-                    help="run only this operator leg (a workload name of the ops table) "
+                    help="run only this operator leg (a workload name of the ops table, or "
+                         "one of the scans gemv_size_scan, tile_width_scan, moe_f_scan) "
                          "and print its result; for profiling one kernel")
     return ap.parse_args()
 
@@ -435,6 +436,55 @@ def small_rs_latency(fcc, torch, np, synth, dev, stream):
     res["pairs_plain_us"] = 1e3 * time_calls(
         lambda: fcc.fcc_gemm_rs(w.R, pA, pB, pO, w.M, w.N, w.K, 0, 2, o2, stream), 200, 10, stream)
     res["TFLOP/s_plain"] = w.flops() / (res["plain_us"] * 1e-6) / 1e12
+    return res
+
+
+def tile_width_scan(fcc, torch, np, synth, dev, stream):
+    """One-rank GEMMs (fcc_gemm_rs with R = 1) of one round of 256-row tiles
+    (half the SM count of them), K = 4096, whose rows hold 4 full 256-column
+    tiles (N = 1024), 4 full and a 64- or 128-column last tile (N = 1088,
+    1152) or 5 full tiles (N = 1280): what a narrow last tile costs."""
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    K, M = 4096, (sms // 2) * 256
+    rng = np.random.Generator(np.random.PCG64(11))
+    A = torch.from_numpy(synth.normal_bf16(rng, (M, K), 1.0).view(np.int16)).to(dev)
+    res = {"M": M, "K": K}
+    for N in (1024, 1088, 1152, 1280):
+        B = torch.from_numpy(synth.normal_bf16(rng, (K, N), 0.02).view(np.int16)).to(dev)
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        pA, pB, pO = fcc.ptr_array([A]), fcc.ptr_array([B]), fcc.ptr_array([out])
+        t = time_calls(lambda: fcc.fcc_gemm_rs(1, pA, pB, pO, M, N, K, 0, 0, None, stream),
+                       20, 3, stream)
+        res[str(N)] = {"us": t * 1e3, "TFLOP/s": 2.0 * M * N * K / (t * 1e-3) / 1e12}
+    return res
+
+
+def moe_f_scan(fcc, torch, np, synth, dev, stream):
+    """The MoE dispatch + expert GEMM of the benchmark (8 x 4096 tokens, hidden
+    4096, 64 experts, top-2) with expert widths F = 1280, 1408 and 1536 on the
+    same routing: F = 1408 ends each row of tiles with a 128-column tile."""
+    w = synth.WORKLOADS["moe_r8_t4096_h4096_e64_f1408"]
+    R, T, H, E, topk = w.R, w.T, w.H, w.E, w.topk
+    X, logits, W = synth.moe_inputs(R, T, H, E, 1536, std_x=w.std_a, std_w=w.std_b, seed=0)
+    up = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev)  # noqa: E731
+    dX = [up(x) for x in X]
+    dL = [torch.from_numpy(l).to(dev) for l in logits]
+    cap = 2 * T * topk
+    idx = [torch.empty((T, topk), dtype=torch.int32, device=dev) for _ in range(R)]
+    gate = [torch.empty((T, topk), dtype=torch.float32, device=dev) for _ in range(R)]
+    counts = torch.empty((E,), dtype=torch.int32, device=dev)
+    send = torch.empty((R * R,), dtype=torch.int32, device=dev)
+    src = [torch.empty((cap,), dtype=torch.int32, device=dev) for _ in range(R)]
+    ry = [torch.empty((cap * 1536,), dtype=torch.int16, device=dev) for _ in range(R)]
+    res = {}
+    for F in (1280, 1408, 1536):
+        dW = [up(x[:, :F]) for x in W]
+        ys = [y[:cap * F].view(cap, F) for y in ry]
+        t = time_calls(lambda: fcc.fcc_moe_dispatch_gemm(R, dX, dL, dW, T, H, F, E, topk, None, ys,
+                                                         cap, idx, gate, counts, send, src, 0, 0,
+                                                         None, stream), 10, 3, stream)
+        res[str(F)] = {"us": t * 1e3, "TFLOP/s": 2.0 * R * T * topk * H * F / (t * 1e-3) / 1e12}
+        del dW
     return res
 
 
@@ -835,6 +885,10 @@ def run_fcc(args, world, rank, local, pg):
             res = small_rs_latency(fcc, torch, np, synth, dev, stream)
         elif args.op == "gemv_size_scan":
             res = gemv_size_scan(fcc, torch, np, synth, dev, stream, pk)
+        elif args.op == "tile_width_scan":
+            res = tile_width_scan(fcc, torch, np, synth, dev, stream)
+        elif args.op == "moe_f_scan":
+            res = moe_f_scan(fcc, torch, np, synth, dev, stream)
         else:
             res = other_ops(fcc, torch, np, synth, dev, stream, dA, dB, pk, only=args.op)
             if args.op not in res:
