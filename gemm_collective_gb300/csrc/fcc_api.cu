@@ -351,6 +351,14 @@ fcc_status run_gemm(const GemmParams& p0, int mode, DeviceState* d, const fcc_op
   }
   // Grid in CTAs: one cluster per slot, at most one per work item.
   const int grid = p.cg * static_cast<int>(std::min<int64_t>(slots, p.num_tiles));
+  // Release the next launch at the start for the fused GEMMs of several
+  // rounds (the 8-rank AllGather + GEMM: 2.03-2.08 ms that way against
+  // 2.09-2.18 ms released late), late for the per-rank GEMMs of the baselines
+  // (a reduce or gather kernel follows: the 8-rank GEMV + AllReduce baseline
+  // took 91 us with the reduce resident beside its GEMM, 83 us without) and
+  // for launches of one round or less (2-rank 256x256x128 RS: 5.5 against
+  // 5.7 us).
+  p.trigger_late = (mode == MODE_PARTIAL || p.num_tiles <= slots) ? 1 : 0;
   cudaError_t e = launch_gemm(p, mode, p.cg, grid, st);
   if (e != cudaSuccess) return FCC_ERR_CUDA;
   g_launches.fetch_add(1);

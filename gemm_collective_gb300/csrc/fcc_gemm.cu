@@ -314,8 +314,10 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) gemm_kernel(const __gri
   // Launched with programmatic stream serialization: the set-up above touches
   // no global memory (the tensor maps are kernel parameters), so it may
   // overlap the previous kernel on the stream; everything below waits for it.
+  // The next kernel's launch is released here, or (trigger_late) once this
+  // CTA's last accumulator is complete, in the epilogue below.
   ptx::griddep_wait();
-  ptx::griddep_launch_dependents();
+  if (!p.trigger_late) ptx::griddep_launch_dependents();
   if constexpr (MODE == MODE_GROUPED) {
     // The tables were written by the dispatch kernels before this launch.
     for (int i = threadIdx.x; i <= p.E; i += blockDim.x) tab[i] = __ldcg(p.tile_start + i);
@@ -640,6 +642,8 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) gemm_kernel(const __gri
     for (int t = pair; t < num_tiles; t += npairs) {
       const Tile tl = tile_of<MODE, TM>(p, t, tab);
       const bool failed = !W.wait(&tfull[acc], acc_phase);
+      if (p.trigger_late && t + npairs >= num_tiles && warp == 2 && lane == 0)
+        ptx::griddep_launch_dependents();
       const uint64_t e0 = times != nullptr ? ptx::globaltimer() : 0;
       if constexpr (MODE == MODE_RS_PUSH || MODE == MODE_AR_PUSH) {
         // The four epilogue warps meet at named barriers below: stop together.

@@ -107,8 +107,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemv_ar_kernel(const __grid_c
   // Launched with programmatic stream serialization: the set-up above touches
   // no global memory (the tensor maps are kernel parameters), so it may
   // overlap the previous kernel on the stream; everything below waits for it.
+  // The next kernel's launch is released once the accumulators are complete
+  // (epilogue below), so a small next kernel does not sit beside this one.
   ptx::griddep_wait();
-  ptx::griddep_launch_dependents();
   const uint32_t tmem_base = *tmem_slot;
   const ptx::Waiter W{abort_flag, p.status, p.timeout_ns};
 
@@ -189,6 +190,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemv_ar_kernel(const __grid_c
     const int q = warp & 3;
     const int ep_tid = threadIdx.x - 64;
     const bool failed = (kb1 <= kb0) || !W.wait(tfull, 0);
+    if (ep_tid == 0) ptx::griddep_launch_dependents();
     if (p.cluster) {
       // Cluster form: the partial rows stay in this CTA's shared memory (the
       // stages are free once the accumulators are complete); the cluster

@@ -106,6 +106,11 @@ struct GemmParams {
   int* tickets;         // push mode with bf16 output: per (tile, CTA of the pair) counters
   int cg;               // host side: CTAs per cluster (1 or 2)
   unsigned long long* phase_ns;  // NULL, or 4 per CTA: span, epilogue busy, MMA wait, tiles
+  // When the next kernel on the stream may launch (programmatic launch):
+  // 0 = once this kernel has started (its set-up then overlaps our run),
+  // 1 = once each CTA's last accumulator is complete (a small next kernel then
+  // does not sit resident beside this one for its whole run).
+  int trigger_late;
 };
 
 struct GemvParams {
@@ -166,6 +171,7 @@ struct GroupedParams {
   int* copy_cursor;                    // next chunk of rows to claim
   int stage_copy;
   unsigned long long* phase_ns;        // NULL, or 4 per CTA (as GemmParams)
+  int trigger_late;                    // as GemmParams
 };
 
 // cg = 1: one CTA per 128 x 256 tile; cg = 2: a CTA pair (cluster of 2) per

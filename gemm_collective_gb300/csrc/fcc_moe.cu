@@ -850,6 +850,10 @@ fcc_status fcc_moe_dispatch_gemm(int R, const void* const* X, const float* const
   g.status = status;
   g.timeout_ns = timeout_ns;
   g.phase_ns = opts != nullptr ? reinterpret_cast<unsigned long long*>(opts->phase_ns) : nullptr;
+  // Release the next launch (a combine, or the next call's router) when the
+  // expert GEMM's last accumulators are complete: 581-588 against 590-591 us
+  // released at the start.
+  g.trigger_late = 1;
   g.gather = gather ? 1 : 0;
   if (copy_in_gemm) {
     for (int r = 0; r < R; ++r) {
