@@ -96,6 +96,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemv_ar_kernel(const __grid_c
       ptx::tma_prefetch_desc(&p.mapA[r]);
       ptx::tma_prefetch_desc(&p.mapB[r]);
     }
+    // The first stages' weights into L2 while the previous kernel may still
+    // run: an L2 prefetch returns nothing to this CTA, so it cannot see data
+    // older than the loads after the wait below, which read through L2.
+    int kbi = kb0, sc = 0;
+    for (int i = 0; i < kStages && kbi < kb1; ++i) {
+      const int r = kbi / p.kb_per_rank;
+      const int kb = kbi - r * p.kb_per_rank;
+#pragma unroll
+      for (int b = 0; b < kStageCols / 64; ++b)
+        ptx::tma_prefetch_2d(&p.mapB[r], col0 + sc * kStageCols + 64 * b, kb * kBK);
+      if (++sc == nstage_cols) {
+        sc = 0;
+        ++kbi;
+      }
+    }
   }
   if (warp == 1) {
     ptx::tmem_alloc(tmem_slot, kTmemCols);
