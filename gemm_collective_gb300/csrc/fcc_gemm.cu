@@ -225,6 +225,41 @@ __device__ __forceinline__ void store_row_chunk(void* row_ptr, int col, int N, i
   }
 }
 
+// Stores a warp's 32 x 32 block of results as bf16; lane i holds the 32
+// accumulator columns of its row i.  Four shuffle rounds per eight rows hand
+// each lane one 16-byte piece of another lane's row, so that every store
+// instruction writes eight whole 64-byte row pieces (four lanes a row), not
+// a 16-byte piece of each of 32 rows.  emit(src, k, piece) stores piece k
+// (columns 8k .. 8k+7 of the block) of lane src's row; every lane calls it
+// (it may shuffle).
+template <class Emit>
+__device__ __forceinline__ void store_block_bf16(const uint32_t (&v)[32], int lane, Emit&& emit) {
+  uint4 w[4];
+#pragma unroll
+  for (int g = 0; g < 4; ++g) {
+    w[g].x = ptx::pack_bf16x2(__uint_as_float(v[8 * g]), __uint_as_float(v[8 * g + 1]));
+    w[g].y = ptx::pack_bf16x2(__uint_as_float(v[8 * g + 2]), __uint_as_float(v[8 * g + 3]));
+    w[g].z = ptx::pack_bf16x2(__uint_as_float(v[8 * g + 4]), __uint_as_float(v[8 * g + 5]));
+    w[g].w = ptx::pack_bf16x2(__uint_as_float(v[8 * g + 6]), __uint_as_float(v[8 * g + 7]));
+  }
+  const int k = lane & 3;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int src = 8 * j + (lane >> 2);
+    uint4 piece = w[0];
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      uint4 x;
+      x.x = __shfl_sync(0xffffffffu, w[kk].x, src);
+      x.y = __shfl_sync(0xffffffffu, w[kk].y, src);
+      x.z = __shfl_sync(0xffffffffu, w[kk].z, src);
+      x.w = __shfl_sync(0xffffffffu, w[kk].w, src);
+      if (kk == k) piece = x;
+    }
+    emit(src, k, piece);
+  }
+}
+
 __device__ __forceinline__ void red_row_chunk(float* row_ptr, int col, int N,
                                               const uint32_t (&v)[32]) {
   float* dst = row_ptr + col;
@@ -711,7 +746,36 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) gemm_kernel(const __gri
           }
         }
         const int col = col0 + c;
-        if (!row_ok || col >= p.N) continue;
+        if (col >= p.N) continue;
+        // bf16 results as whole 64-byte row pieces per store: the 8-rank
+        // GEMM + AllReduce (eight copies of every tile) went from 2.33 to
+        // 2.16 ms, the MoE expert GEMM from 579-584 to 574 us; the RS did
+        // not move and the AllGather + GEMM lost 15 us, so it keeps the
+        // per-row stores.
+        if constexpr (MODE == MODE_AR || MODE == MODE_RS || MODE == MODE_GROUPED) {
+          if (!p.out_f32) {
+            const int ok = row_ok ? 1 : 0;
+            if constexpr (MODE == MODE_AR) {
+              store_block_bf16(v, lane, [&](int src, int k, const uint4& x) {
+                const long long srow = __shfl_sync(0xffffffffu, static_cast<long long>(grow), src);
+                if (__shfl_sync(0xffffffffu, ok, src) && col + 8 * k + 8 <= p.N)
+                  for (int r = 0; r < p.R; ++r)
+                    ptx::st_global_v4(static_cast<uint16_t*>(p.out[r]) + srow * p.N + col + 8 * k,
+                                      x.x, x.y, x.z, x.w);
+              });
+            } else {
+              store_block_bf16(v, lane, [&](int src, int k, const uint4& x) {
+                const unsigned long long sp =
+                    __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(rowp), src);
+                if (__shfl_sync(0xffffffffu, ok, src) && col + 8 * k + 8 <= p.N)
+                  ptx::st_global_v4(reinterpret_cast<uint16_t*>(sp) + col + 8 * k, x.x, x.y, x.z,
+                                    x.w);
+              });
+            }
+            continue;
+          }
+        }
+        if (!row_ok) continue;
         if constexpr (MODE == MODE_AR) {
           for (int r = 0; r < p.R; ++r)
             store_row_chunk(static_cast<char*>(p.out[r]) + grow * p.N * esz, col, p.N, p.out_f32, v);
