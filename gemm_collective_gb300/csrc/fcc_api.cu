@@ -179,11 +179,11 @@ fcc_algo choose_algo(fcc_op op, int R, int64_t M, int64_t N, int64_t K, int sms,
     return splits >= 16 ? FCC_ALGO_UNFUSED : FCC_ALGO_FUSED;
   }
   //  * Embedding + All-to-All: pooling table by table into a staging buffer,
-  //    then the exchange kernel.  Over the eight recorded runs on GB300s (8
+  //    then the exchange kernel.  Over the nine recorded runs on GB300s (8
   //    ranks x 64 tables of 65536 x 128, 2048 samples a rank, bags of 32) it
-  //    took 1154-1418 us, median 1236, and the fused store of each pooled
-  //    row to its sample's rank 1184-1329 us, median 1317; the staged form
-  //    was the faster in five of the eight.
+  //    took 1154-1418 us, median 1261, and the fused store of each pooled
+  //    row to its sample's rank 1184-1339 us, median 1317; the staged form
+  //    was the faster in five of the nine.
   if (op == FCC_OP_EMBEDDING_A2A) return FCC_ALGO_UNFUSED;
   return FCC_ALGO_FUSED;
 }

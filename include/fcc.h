@@ -346,10 +346,10 @@ const char *fcc_status_string(fcc_status s);
  * its final serial sum of the splits then costs more than the plain GEMM +
  * reduce), else FCC_ALGO_FUSED; for the embedding + All-to-All,
  * FCC_ALGO_UNFUSED (pooling table by table into a staging buffer, then the
- * exchange: median 1236 us over eight runs on 8 ranks x 64 tables of 65536 x
+ * exchange: median 1261 us over nine runs on 8 ranks x 64 tables of 65536 x
  * 128, 2048 samples a rank, bags of 32, against 1317 us for storing each
  * pooled row straight to its sample's rank; the staged form was the faster
- * in five of the eight).  sms: SMs to plan for (0 = the current
+ * in five of the nine).  sms: SMs to plan for (0 = the current
  * device's, 152 without one); max_ctas as in fcc_opts.  Host-only.
  */
 fcc_algo fcc_choose_algo(fcc_op op, int R, int64_t M, int64_t N, int64_t K, int sms,
