@@ -148,6 +148,40 @@ def test_moe_placement_either_side_of_the_one_kernel_limit(T):
         _check(X, logits, W, R, T, H, F, E, topk, cap, out, sample=384)
 
 
+# Rows per expert chosen so that an expert's last unit of at most 128 rows
+# (an M = 128 pair tile: 64 rows from each CTA of the pair) holds rows on one
+# CTA only, on both, or fills it, next to full units, units of 129-255 rows
+# and an expert with no rows.
+SHORT_UNIT_COUNTS = [1, 2, 17, 31, 32, 33, 34, 63, 64, 65, 66, 127, 128, 129, 257, 289, 321,
+                     384, 0, 200]
+
+
+@pytest.mark.parametrize("pair", [1, 2])
+@pytest.mark.parametrize("path", ["workspace", "gather", "unfused_workspace"])
+def test_moe_short_last_units(pair, path):
+    R, H, F, E, topk = 2, 192, 320, len(SHORT_UNIT_COUNTS), 1
+    total = sum(SHORT_UNIT_COUNTS)
+    T = (total + R - 1) // R
+    X, logits, W = synth.moe_inputs(R, T, H, E, F, seed=41)
+    # token i (in (rank, token) order) goes to the expert of its position in
+    # the count list; the padding token, if any, to the last expert
+    owner = np.repeat(np.arange(E), SHORT_UNIT_COUNTS)
+    owner = np.concatenate([owner, np.full(R * T - total, E - 1)])
+    rng = np.random.Generator(np.random.PCG64(43))
+    rng.shuffle(owner)  # interleave the experts over the chunks
+    for s in range(R):
+        logits[s][np.arange(T), owner[s * T:(s + 1) * T]] += 50.0
+    cap = R * T * topk
+    staged, contiguous, algo = PATHS[path]
+    out = _run(X, logits, W, R, T, H, F, E, topk, cap,
+               opts=fcc.make_opts(cta_pair=pair, algo=algo), staged=staged,
+               contiguous=contiguous)
+    counts = out["counts"].cpu().numpy()
+    want = np.bincount(owner, minlength=E)
+    assert np.array_equal(counts, want)
+    _check(X, logits, W, R, T, H, F, E, topk, cap, out)
+
+
 def test_moe_ties_and_f32_output():
     R, T, H, F, E, topk = 2, 128, 64, 64, 8, 2
     X, logits, W = synth.moe_inputs(R, T, H, E, F, seed=5)
