@@ -6,10 +6,12 @@
 
 #include <algorithm>
 #include <atomic>
+#include <chrono>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <random>
 
 #include "fcc.h"
 #include "fcc_internal.h"
@@ -332,22 +334,63 @@ fcc_status gemm_params(GemmParams& p, DeviceState* d, int mode, int R, const voi
   return FCC_OK;
 }
 
+// Clusters (CTAs or CTA pairs) that run tiles at the same time.
+int gemm_slots(const GemmParams& p, DeviceState* d, const fcc_opts* o) {
+  return std::max(1, std::min(grid_for(d, o, INT64_MAX) / p.cg, gemm_max_clusters(p.cg)));
+}
+
+// Tiles of the last round that a fused deterministic RS / AR launch splits
+// in K (0: none): the last round holds at most half a round, after at least
+// one full round, and the K loop has two iterations or more.
+int ksplit_tiles(const GemmParams& p, int slots) {
+  const int rem = p.num_tiles % slots;
+  return (rem > 0 && 2 * rem <= slots && p.num_tiles > slots && p.k_iters >= 2) ? rem : 0;
+}
+
+// Ids of the calls that split tiles in K: unique within the process and, by
+// a random start, across processes that share a caller's workspace.
+std::atomic<unsigned long long> g_call_id{0};
+std::once_flag g_call_id_once;
+unsigned long long next_call_id() {
+  std::call_once(g_call_id_once, [] {
+    std::random_device rd;
+    const unsigned long long salt = (static_cast<unsigned long long>(rd()) << 32) ^ rd() ^
+        static_cast<unsigned long long>(
+            std::chrono::steady_clock::now().time_since_epoch().count());
+    g_call_id.store(salt | 1ull);
+  });
+  return g_call_id.fetch_add(2);  // odd: never the zero of fresh memory
+}
+
 fcc_status run_gemm(const GemmParams& p0, int mode, DeviceState* d, const fcc_opts* o,
                     cudaStream_t st) {
   if (p0.num_tiles <= 0) return FCC_OK;
   GemmParams p = p0;
   // Tiles go round-robin over `slots` CTAs (CTA pairs).  When the last round
   // would hold at most half a round of tiles, each of those tiles runs as two
-  // 128-column halves on two slots, so the round takes half a tile's time.
-  // A half keeps the tile's whole K loop: the results are unchanged.
-  const int slots = std::max(1, std::min(grid_for(d, o, INT64_MAX) / p.cg,
-                                         gemm_max_clusters(p.cg)));
+  // halves on two slots, so the round takes about half a tile's time: for a
+  // fused deterministic RS / AR given split workspace (p.split_ws), K halves
+  // whose partial sums meet in the epilogue (a 128-column half tile costs
+  // 0.81 of a whole one on the tensor cores, a K half 0.5); otherwise
+  // 128-column halves, which keep the tile's whole K loop, so the results
+  // are unchanged.
+  const int slots = gemm_slots(p, d, o);
   const int rem = p.num_tiles % slots;
   p.split_first = p.num_tiles;
+  const int kt = (mode == MODE_RS || mode == MODE_AR) && p.split_ws != nullptr
+                     ? ksplit_tiles(p, slots) : 0;
   if ((mode == MODE_RS || mode == MODE_AR || mode == MODE_AG || mode == MODE_PARTIAL) &&
       rem > 0 && 2 * rem <= slots) {
     p.split_first = p.num_tiles - rem;
     p.num_tiles += rem;
+    if (kt == rem) {
+      p.ksplit = 1;
+      p.k_half = (p.k_iters + 1) / 2;
+      p.split_flags = reinterpret_cast<unsigned long long*>(
+          reinterpret_cast<char*>(p.split_ws) + ksplit_ws_bytes(kt, p.cg) -
+          static_cast<size_t>(kt) * p.cg * 8);
+      p.call_id = next_call_id();
+    }
   }
   // Grid in CTAs: one cluster per slot, at most one per work item.
   const int grid = p.cg * static_cast<int>(std::min<int64_t>(slots, p.num_tiles));
@@ -535,6 +578,18 @@ fcc_status rank_sum_call(int R, const void* const* A, const void* const* B, void
     GemmParams p;
     if ((s = gemm_params(p, d, mode, R, A, B, out, R, M, N, K, Ms, 0, M, out_f32, o)) != FCC_OK)
       return s;
+    // The last round's K halves need room for their partial sums; a caller's
+    // workspace too small for them leaves the column halves instead.
+    const int kt = ksplit_tiles(p, gemm_slots(p, d, o));
+    if (kt > 0) {
+      const size_t sb = ksplit_ws_bytes(kt, p.cg);
+      const bool caller = o != nullptr && o->workspace != nullptr;
+      if (!caller || (o->workspace_bytes >= sb && aligned16(o->workspace))) {
+        void* sws = nullptr;
+        if ((s = get_workspace(d, o, sb, &sws)) != FCC_OK) return s;
+        p.split_ws = static_cast<float*>(sws);
+      }
+    }
     return run_gemm(p, mode, d, o, st);
   }
 
@@ -801,9 +856,26 @@ size_t fcc_workspace_size(fcc_op op, int R, int64_t M, int64_t N, int64_t K,
   if (R < 1 || R > FCC_MAX_RANKS || M <= 0 || N <= 0) return 0;
   switch (op) {
     case FCC_OP_GEMM_RS:
-    case FCC_OP_GEMM_AR:
+    case FCC_OP_GEMM_AR: {
       // bf16 vs f32 output only matters for the push mode; report the larger.
-      return rank_sum_plan(R, M, N, false, opts).total();
+      size_t bytes = rank_sum_plan(R, M, N, false, opts).total();
+      if (algo_of(opts) == FCC_ALGO_FUSED && deterministic_of(opts)) {
+        // The K halves of the last round: at most half a round of tiles.
+        int sms = 0, dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+          sms = 256;
+        int ctas = sms;
+        if (opts != nullptr && opts->max_ctas > 0) ctas = std::min(ctas, opts->max_ctas);
+        const int64_t single = cdiv(M, kBM) * cdiv(N, kGemmBN);
+        const int cg = choose_cg(opts, M, single, ctas);
+        const int64_t tiles = cdiv(M, static_cast<int64_t>(kBM) * cg) * cdiv(N, kGemmBN);
+        const int64_t half_round = std::max(1, ctas / cg) / 2;
+        const int64_t kt = std::min(tiles, half_round);
+        if (kt > 0) bytes += align_up(ksplit_ws_bytes(static_cast<int>(kt), cg));
+      }
+      return bytes;
+    }
     case FCC_OP_GEMV_AR: {
       const bool automatic = opts == nullptr || opts->algo == FCC_ALGO_AUTO;
       fcc_opts plain;

@@ -100,6 +100,8 @@ struct Tile {
   int row0;    // GROUPED: first receive-buffer row of the tile
   int rows;    // GROUPED: valid rows of the tile
   int half;    // -1: the whole 256-column tile; 0 / 1: its first / second 128 columns
+  int kpart;   // -1: the whole K loop; 0 / 1: its first / second half (RS / AR)
+  int slot;    // kpart >= 0: the tile's index among the last round's split tiles
   int m128;    // GROUPED on CTA pairs: 1 = at most 128 rows, run as an M = 128 pair MMA
 };
 
@@ -142,14 +144,24 @@ __device__ __forceinline__ Tile tile_of(const P& p, int t, const int* tab) {
   tl.row0 = 0;
   tl.rows = 0;
   tl.half = -1;
+  tl.kpart = -1;
+  tl.slot = 0;
   tl.m128 = 0;
   if constexpr (MODE == MODE_RS || MODE == MODE_AR || MODE == MODE_AG || MODE == MODE_PARTIAL) {
     // Work items from split_first on are halves of the last round's tiles
-    // (two per tile), so that round takes half a tile's time.
+    // (two per tile), so that round takes about half a tile's time: K halves
+    // (RS / AR with ksplit), else 128-column halves.
     if (t >= p.split_first) {
       const int h = t - p.split_first;
       t = p.split_first + (h >> 1);
-      tl.half = h & 1;
+      bool ks = false;
+      if constexpr (MODE == MODE_RS || MODE == MODE_AR) ks = p.ksplit != 0;
+      if (ks) {
+        tl.kpart = h & 1;
+        tl.slot = h >> 1;
+      } else {
+        tl.half = h & 1;
+      }
     }
   }
   if constexpr (MODE == MODE_GROUPED) {
@@ -330,6 +342,15 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) gemm_kernel(const __gri
   // half of its 256, so the B loads, the MMA width and the epilogue are halved.
   auto narrow = [&](const Tile& tl) { return tl.half >= 0 || p.N - tl.nt * kBN <= kBN / 2; };
   auto col_base = [&](const Tile& tl) { return tl.nt * kBN + (tl.half > 0 ? kBN / 2 : 0); };
+  // The tile's k iterations [it_lo, it_hi).
+  auto k_lo = [&](const Tile& tl) {
+    if constexpr (MODE == MODE_RS || MODE == MODE_AR) return tl.kpart == 1 ? p.k_half : 0;
+    return 0;
+  };
+  auto k_hi = [&](const Tile& tl) {
+    if constexpr (MODE == MODE_RS || MODE == MODE_AR) return tl.kpart == 0 ? p.k_half : k_iters;
+    return k_iters;
+  };
   if (warp == 1) {
     if constexpr (kPair) {
       ptx::tmem_alloc_pair(tmem_slot, kTmemCols);
@@ -472,9 +493,10 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) gemm_kernel(const __gri
             ptx::fence_proxy_async_global();
           }
         }
-        int r = (tl.rank >= 0) ? tl.rank : 0;
-        int kb = 0;
-        for (int it = 0; it < k_iters; ++it) {
+        const int it_lo = k_lo(tl), it_hi = k_hi(tl);
+        int r = ((tl.rank >= 0) ? tl.rank : 0) + it_lo / p.kb_per_rank;
+        int kb = it_lo % p.kb_per_rank;
+        for (int it = it_lo; it < it_hi; ++it) {
           if (!W.wait(&empty[stage], phase ^ 1u)) {
             ok = false;
             break;
@@ -534,7 +556,8 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) gemm_kernel(const __gri
         if (times != nullptr) waited += ptx::globaltimer() - w0;
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * kBN;
-        for (int it = 0; it < k_iters; ++it) {
+        const int it_lo = k_lo(tm_), it_hi = k_hi(tm_);
+        for (int it = it_lo; it < it_hi; ++it) {
           if (!W.wait(&full[stage], phase)) {
             ok = false;
             break;
@@ -549,9 +572,9 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) gemm_kernel(const __gri
             // B: MN-major, advance 16 k-rows (2 KiB); 64-wide n atoms 8 KiB apart.
             const uint64_t bd = ptx::smem_desc_sw128(b_addr + kk * 2048, kBBoxBytes, 1024);
             if constexpr (kPair)
-              ptx::mma_f16_pair(d_tmem, ad, bd, idesc, (it > 0 || kk > 0) ? 1u : 0u);
+              ptx::mma_f16_pair(d_tmem, ad, bd, idesc, (it > it_lo || kk > 0) ? 1u : 0u);
             else
-              ptx::mma_f16(d_tmem, ad, bd, idesc, (it > 0 || kk > 0) ? 1u : 0u);
+              ptx::mma_f16(d_tmem, ad, bd, idesc, (it > it_lo || kk > 0) ? 1u : 0u);
           }
           if constexpr (kPair)
             // Frees the stage in both CTAs of the pair.
@@ -683,6 +706,13 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) gemm_kernel(const __gri
       if constexpr (MODE == MODE_RS_PUSH || MODE == MODE_AR_PUSH) {
         // The four epilogue warps meet at named barriers below: stop together.
         if (ptx::named_barrier_or(1, 128, failed)) break;
+      } else if constexpr (MODE == MODE_RS || MODE == MODE_AR) {
+        // (so do they for a K half of the last round)
+        if (tl.kpart >= 0) {
+          if (ptx::named_barrier_or(1, 128, failed)) break;
+        } else if (failed) {
+          break;
+        }
       } else {
         if (failed) break;
       }
@@ -729,24 +759,20 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) gemm_kernel(const __gri
       // per lane, lanes 64-127 the second half
       const int cend = tl.m128 ? ncols / 2 : ncols;
       const int col0 = col_base(tl) + ((tl.m128 && q >= 2) ? ncols / 2 : 0);
-#pragma unroll 1
-      for (int c = 0; c < cend; c += 32) {
-        uint32_t v[32];
-        ptx::tmem_ld_32x32b_x32(taddr + c, v);
-        ptx::tmem_ld_wait();
-        if (c == cend - 32) {
-          // Accumulator fully read: hand it back to the MMA warp early.
-          ptx::tc_fence_before();
-          __syncwarp();
-          if (lane == 0) {
-            if constexpr (kPair)
-              ptx::mbar_arrive_cluster(tempty_leader0 + acc * 8);
-            else
-              ptx::mbar_arrive(&tempty[acc]);
-          }
+      auto release_acc = [&]() {
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if constexpr (kPair)
+            ptx::mbar_arrive_cluster(tempty_leader0 + acc * 8);
+          else
+            ptx::mbar_arrive(&tempty[acc]);
         }
+      };
+      // Stores accumulator columns [c, c + 32) of this thread's row (v).
+      auto store_cols = [&](int c, const uint32_t (&v)[32]) {
         const int col = col0 + c;
-        if (col >= p.N) continue;
+        if (col >= p.N) return;
         // bf16 results as whole 64-byte row pieces per store: the 8-rank
         // GEMM + AllReduce (eight copies of every tile) went from 2.33 to
         // 2.16 ms, the MoE expert GEMM from 579-584 to 574 us; the RS did
@@ -772,10 +798,10 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) gemm_kernel(const __gri
                                     x.w);
               });
             }
-            continue;
+            return;
           }
         }
-        if (!row_ok) continue;
+        if (!row_ok) return;
         if constexpr (MODE == MODE_AR) {
           for (int r = 0; r < p.R; ++r)
             store_row_chunk(static_cast<char*>(p.out[r]) + grow * p.N * esz, col, p.N, p.out_f32, v);
@@ -793,6 +819,71 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) gemm_kernel(const __gri
         } else {
           store_row_chunk(rowp, col, p.N, p.out_f32, v);
         }
+      };
+
+      bool ksplit_tile = false;
+      if constexpr (MODE == MODE_RS || MODE == MODE_AR) ksplit_tile = tl.kpart >= 0;
+      if (!ksplit_tile) {
+#pragma unroll 1
+        for (int c = 0; c < cend; c += 32) {
+          uint32_t v[32];
+          ptx::tmem_ld_32x32b_x32(taddr + c, v);
+          ptx::tmem_ld_wait();
+          // Accumulator fully read: hand it back to the MMA warp early.
+          if (c == cend - 32) release_acc();
+          store_cols(c, v);
+        }
+      } else if constexpr (MODE == MODE_RS || MODE == MODE_AR) {
+        // A K half of a last-round tile (the only tile of its slot in that
+        // round).  Its partner half runs on another slot at the same time.
+        const int lrow = q * 32 + lane;  // TMEM lane = row of this CTA's 128
+        // The first half's partial of this CTA's 128 rows: block slot * CG + cta.
+        const size_t blk = static_cast<size_t>(tl.slot) * CG + cta;
+        float* const part = p.split_ws + blk * (static_cast<size_t>(kBM) * kBN) +
+                            static_cast<size_t>(lrow) * kBN;
+        unsigned long long* flag = p.split_flags + blk;
+        if (tl.kpart == 0) {
+          // First half: the f32 partial out, then the flag (release).
+          float* dst = part;
+#pragma unroll 1
+          for (int c = 0; c < cend; c += 32) {
+            uint32_t v[32];
+            ptx::tmem_ld_32x32b_x32(taddr + c, v);
+            ptx::tmem_ld_wait();
+#pragma unroll
+            for (int g = 0; g < 8; ++g)
+              ptx::st_global_v4(dst + c + 4 * g, v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
+          }
+          __threadfence();
+          ptx::named_barrier_sync(1, 128);
+          if (threadIdx.x == 64) ptx::st_release_gpu_u64(flag, p.call_id);
+        } else {
+          // Second half: wait for the first half's partial (bounded), add it to
+          // this accumulator and store the sums.  f32 addition is commutative,
+          // so the result does not depend on which half finished first.
+          if (threadIdx.x == 64) *bcast = W.wait_eq(flag, p.call_id) ? 1 : 0;
+          ptx::named_barrier_sync(1, 128);
+          if (*bcast) {
+            const float* src = part;
+#pragma unroll 1
+            for (int c = 0; c < cend; c += 32) {
+              uint32_t v[32];
+              ptx::tmem_ld_32x32b_x32(taddr + c, v);
+              ptx::tmem_ld_wait();
+#pragma unroll
+              for (int g = 0; g < 8; ++g) {
+                const float4 f = __ldcg(reinterpret_cast<const float4*>(src + c + 4 * g));
+                v[4 * g] = __float_as_uint(__uint_as_float(v[4 * g]) + f.x);
+                v[4 * g + 1] = __float_as_uint(__uint_as_float(v[4 * g + 1]) + f.y);
+                v[4 * g + 2] = __float_as_uint(__uint_as_float(v[4 * g + 2]) + f.z);
+                v[4 * g + 3] = __float_as_uint(__uint_as_float(v[4 * g + 3]) + f.w);
+              }
+              store_cols(c, v);
+            }
+          }
+          ptx::named_barrier_sync(1, 128);  // (bcast is read before any reuse)
+        }
+        release_acc();
       }
 
       if constexpr (MODE == MODE_RS_PUSH || MODE == MODE_AR_PUSH) {

@@ -111,7 +111,25 @@ struct GemmParams {
   // 1 = once each CTA's last accumulator is complete (a small next kernel then
   // does not sit resident beside this one for its whole run).
   int trigger_late;
+  // RS / AR, ksplit = 1: the work items from split_first on are the K halves
+  // of the last round's tiles (k iterations [0, k_half) and [k_half, k_iters)),
+  // not column halves.  The first half stores its f32 partial (one 128 x 256
+  // block per CTA of the pair) to split_ws and then sets the tile's flag to
+  // the call's id; the second half waits for the flag, adds the partial to
+  // its own accumulator and stores the result.  A flag left by another call
+  // holds another id, so the flags need no clearing between calls.
+  int ksplit;
+  int k_half;
+  float* split_ws;                    // [split tiles][CG][128][256] f32, then the flags
+  unsigned long long* split_flags;    // [split tiles][CG]
+  unsigned long long call_id;
 };
+
+// Bytes of the K-split workspace for `tiles` split tiles of `cg` CTAs each.
+inline size_t ksplit_ws_bytes(int tiles, int cg) {
+  const size_t part = static_cast<size_t>(tiles) * cg * 128 * 256 * 4;
+  return part + static_cast<size_t>(tiles) * cg * 8;
+}
 
 struct GemvParams {
   CUtensorMap mapA[FCC_MAX_RANKS];  // [M, K], box of 16 rows (rows past M read as zeros)

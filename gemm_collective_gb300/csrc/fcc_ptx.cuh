@@ -66,6 +66,16 @@ __device__ __forceinline__ int ld_acquire_gpu(const int* p) {
   return v;
 }
 
+__device__ __forceinline__ unsigned long long ld_acquire_gpu_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_release_gpu_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.release.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
                "r"(bytes)
@@ -126,6 +136,23 @@ struct Waiter {
     while (true) {
       __nanosleep(64);
       if (ld_acquire_gpu(ctr) >= target) return true;
+      if (*abort_flag) return false;
+      if (globaltimer() - t0 > timeout_ns) {
+        fail();
+        return false;
+      }
+    }
+  }
+
+  // Wait until the global word *flag (written by another CTA with release
+  // semantics) equals `value`; acquire ordering on success.
+  __device__ __forceinline__ bool wait_eq(const unsigned long long* flag,
+                                          unsigned long long value) const {
+    if (ld_acquire_gpu_u64(flag) == value) return true;
+    const uint64_t t0 = globaltimer();
+    while (true) {
+      __nanosleep(32);
+      if (ld_acquire_gpu_u64(flag) == value) return true;
       if (*abort_flag) return false;
       if (globaltimer() - t0 > timeout_ns) {
         fail();

@@ -122,6 +122,14 @@ typedef enum {
  *   out_shard[j][i][n] = sum_{r<R} sum_{k<K} A[r][j*M/R + i][k] * B[r][k][n]
  * R in 1..8; A[r]: [M,K] bf16; B[r]: [K,N] bf16; out_shard[j]: [M/R, N] of
  * dtype `out` (FCC_BF16 or FCC_F32).  M % R == 0, K % 8 == 0, N % 8 == 0.
+ * Deterministic mode: each output tile sums its k terms (rank after rank)
+ * in a fixed order, so results repeat bit for bit and equal fcc_gemm_ar's
+ * rows.  When a launch of several rounds of tiles ends with a round of at
+ * most half the tiles it could hold, each of those tiles runs as two halves
+ * of its k range on two CTA pairs, whose f32 partial sums are then added
+ * (still a fixed order); the partials take workspace (fcc_workspace_size).
+ * A caller workspace too small for them makes those tiles run as column
+ * halves instead, with the tile's whole k range (no error).
  */
 fcc_status fcc_gemm_rs(int R, const void *const *A, const void *const *B,
                        void *const *out_shard, int64_t M, int64_t N, int64_t K,
@@ -131,7 +139,8 @@ fcc_status fcc_gemm_rs(int R, const void *const *A, const void *const *B,
 /*
  * GEMM + AllReduce (mKernel article, fused kernel list).
  *   out[r'] = sum_{r<R} A[r] @ B[r]  for every rank r' (M x N each).
- * Shapes as fcc_gemm_rs (no divisibility of M needed).
+ * Shapes as fcc_gemm_rs (no divisibility of M needed); the same tiling,
+ * summation order and workspace use as fcc_gemm_rs.
  */
 fcc_status fcc_gemm_ar(int R, const void *const *A, const void *const *B, void *const *out,
                        int64_t M, int64_t N, int64_t K, fcc_dtype in, fcc_dtype out_dtype,

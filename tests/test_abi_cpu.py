@@ -117,7 +117,10 @@ def test_interdecom_model(fcc):
 def test_workspace_sizes(fcc):
     o = fcc.make_opts(algo=fcc.FCC_ALGO_UNFUSED)
     assert fcc.fcc_workspace_size(fcc.FCC_OP_GEMM_RS, 8, 8192, 8192, 3584, o) >= 8 * 8192 * 8192 * 4
-    assert fcc.fcc_workspace_size(fcc.FCC_OP_GEMM_RS, 8, 8192, 8192, 3584, None) == 0
+    # fused, deterministic: the K halves of a short last round (at most half
+    # a round of 256 x 256 tiles, f32 partials) and their flags
+    fused = fcc.fcc_workspace_size(fcc.FCC_OP_GEMM_RS, 8, 8192, 8192, 3584, None)
+    assert 0 < fused <= 128 * 2 * 128 * 256 * 4 + 4096
     o = fcc.make_opts(algo=fcc.FCC_ALGO_CE)
     assert fcc.fcc_workspace_size(fcc.FCC_OP_GEMM_RS, 2, 256, 256, 128, o) >= 2 * 2 * 256 * 256 * 4
     assert fcc.fcc_workspace_size(fcc.FCC_OP_AG_GEMM, 8, 8192, 3584, 8192, None) == 0

@@ -150,6 +150,59 @@ def test_last_round_half_tiles_bit_identical(op, pair, N, split_ctas, whole_ctas
         assert np.array_equal(to_f64(split[j]), ref), f"buffer {j} vs oracle"
 
 
+# (pair, max_ctas, N): launches of more than one round whose last round holds
+# at most half a round of tiles, which then run as two K halves each:
+# 16 pair tiles on 5 pairs (one split tile), 32 single-CTA tiles on 10 CTAs
+# (two), a narrow last column tile (N % 256 = 128) and a ragged one (136).
+KSPLIT_CASES = [(2, 10, 1024), (1, 10, 1024), (1, 10, 896), (2, 10, 904)]
+
+
+@pytest.mark.parametrize("pair,ctas,N", KSPLIT_CASES)
+@pytest.mark.parametrize("out_dtype", [fcc.FCC_BF16, fcc.FCC_F32])
+def test_last_round_k_halves(pair, ctas, N, out_dtype):
+    """Float inputs: the K-split last round matches the oracle within the
+    tolerance, repeats bit for bit, gives the AllReduce the reduce-scatter's
+    rows bit for bit, and agrees with the column-halves form (a caller
+    workspace too small for the partial sums) within the tolerance."""
+    R, M, K = 4, 1024, 256
+    A, B = synth.gemm_inputs(R, M, N, K, 1.0, 1.0, seed=N + pair)
+    dA, dB = _upload(A, B)
+    o = fcc.make_opts(cta_pair=pair, max_ctas=ctas)
+    rs = _rs(R, dA, dB, M, N, K, out_dtype, o)
+    again = _rs(R, dA, dB, M, N, K, out_dtype, o)
+    ar = _ar(R, dA, dB, M, N, K, out_dtype, o)
+    ws = torch.empty(256, dtype=torch.uint8, device="cuda")
+    halves = _rs(R, dA, dB, M, N, K, out_dtype,
+                 fcc.make_opts(cta_pair=pair, max_ctas=ctas, workspace=ws, workspace_bytes=256))
+    Ms = M // R
+    for j in range(R):
+        ref = oracle.gemm_rs(A, B, j)
+        assert_close(to_f64(rs[j]), ref, f"shard {j}")
+        assert_close(to_f64(halves[j]), ref, f"column halves, shard {j}")
+        assert np.array_equal(bits(rs[j]), bits(again[j])), "not bitwise repeatable"
+        assert np.array_equal(bits(rs[j]), bits(ar[0])[j * Ms:(j + 1) * Ms]), "RS != AR rows"
+    for r in range(1, R):
+        assert np.array_equal(bits(ar[r]), bits(ar[0]))
+
+
+def test_last_round_k_halves_caller_workspace():
+    """The size query covers the K halves' partial sums: a caller workspace of
+    that size gives the same bits as the library's own pool."""
+    R, M, N, K = 2, 1024, 1024, 128
+    A, B = synth.gemm_inputs(R, M, N, K, 1.0, 1.0, seed=77)
+    dA, dB = _upload(A, B)
+    o = fcc.make_opts(cta_pair=2, max_ctas=10)
+    need = fcc.fcc_workspace_size(fcc.FCC_OP_GEMM_RS, R, M, N, K, o)
+    assert need > 0
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    own = _rs(R, dA, dB, M, N, K, fcc.FCC_F32, o)
+    given = _rs(R, dA, dB, M, N, K, fcc.FCC_F32,
+                fcc.make_opts(cta_pair=2, max_ctas=10, workspace=ws, workspace_bytes=need))
+    for j in range(R):
+        assert np.array_equal(bits(own[j]), bits(given[j]))
+        assert_close(to_f64(given[j]), oracle.gemm_rs(A, B, j))
+
+
 @pytest.mark.parametrize("R,M,N,K", [(2, 1024, 136, 64), (4, 512, 128, 192), (2, 2048, 264, 64)])
 def test_single_ctas_match_pairs_bitwise(R, M, N, K):
     """One CTA per 128-row tile against a CTA pair per 256-row tile: the same K
