@@ -87,23 +87,33 @@ struct AttnParams {
 // The key blocks a CTA visits, in ring order: block i of the walk is block
 // i % kvb of shard (r + i / kvb) % R.  Tile t sees block i unless the tile
 // lies past the shard's end or, with the causal mask, the block's first
-// position lies past the tile's last query (every role applies the same
-// test, so the barrier counts agree).
+// position lies past the tile's last query.  In ring order those blocks form
+// two runs: the own shard's first blocks (walk indices [0, own_end[t]), up to
+// the tile's diagonal) and, from walk index other_begin on, the shards before
+// this one (causal: shards 0 .. r-1, at walk indices [(R - r) kvb, R kvb);
+// without the mask every block, other_begin = kvb).  Every role walks only
+// those runs and applies the same test, so the barrier counts agree; the
+// blocks in between (the shards past this one) cost nothing.
 struct Walk {
   int r, kvb, R, S, causal;
   bool valid[2];                     // the tile holds rows of the shard
   long long q_last[2];               // global position of the tile's last query row
+  int own_end[2];                    // own-shard blocks [0, own_end[t]) are visible to tile t
+  int other_begin;                   // walk indices from here on are visible to valid tiles
   __device__ __forceinline__ int total() const { return R * kvb; }
   __device__ __forceinline__ int shard(int i) const { return (r + i / kvb) % R; }
   __device__ __forceinline__ int row0(int i) const { return (i % kvb) * kBKV; }
-  // Tile t is given by its two fields, so the caller picks them once.
-  __device__ __forceinline__ bool visible(int i, bool tile_valid, long long tile_last) const {
-    if (!tile_valid) return false;
-    if (!causal) return true;
-    return static_cast<long long>(shard(i)) * S + row0(i) <= tile_last;
+  __device__ __forceinline__ bool visible(int i, int t) const {
+    return valid[t] && (i < own_end[t] || i >= other_begin);
   }
-  __device__ __forceinline__ bool visible_a(int i) const { return visible(i, valid[0], q_last[0]); }
-  __device__ __forceinline__ bool visible_b(int i) const { return visible(i, valid[1], q_last[1]); }
+  __device__ __forceinline__ bool visible_a(int i) const { return visible(i, 0); }
+  __device__ __forceinline__ bool visible_b(int i) const { return visible(i, 1); }
+  // The walk index after i among the blocks visible to a tile whose own-shard
+  // run ends at `end` (for both tiles: the larger end).
+  __device__ __forceinline__ int next(int i, int end) const {
+    return (i + 1 == end && end < other_begin) ? other_begin : i + 1;
+  }
+  __device__ __forceinline__ int first(int end) const { return end > 0 ? 0 : other_begin; }
 };
 
 // K-major SW128 operand of 128 rows x 128 elements (two 64-element atoms):
@@ -152,10 +162,14 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attention_kernel(const __gri
   walk.causal = p.causal;
   for (int t = 0; t < 2; ++t) {
     const int qt = 2 * qp + t;
+    const int last_local = min(p.S, (qt + 1) * kBQ) - 1;  // the tile's last query row
     walk.valid[t] = qt < p.qtiles;
-    walk.q_last[t] = static_cast<long long>(r) * p.S + min(p.S, (qt + 1) * kBQ) - 1;
+    walk.q_last[t] = static_cast<long long>(r) * p.S + last_local;
+    walk.own_end[t] = !walk.valid[t] ? 0 : (p.causal ? min(p.kvb, last_local / kBKV + 1) : p.kvb);
   }
+  walk.other_begin = p.causal ? (p.R - r) * p.kvb : p.kvb;
   const int nwalk = walk.total();
+  const int own_end_u = max(walk.own_end[0], walk.own_end[1]);  // either tile's run
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(q_full, 1);
@@ -213,7 +227,7 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attention_kernel(const __gri
         ++u;
         return true;
       };
-      for (int i = 0; i < nwalk && ok; ++i) {
+      for (int i = walk.first(own_end_u); i < nwalk && ok; i = walk.next(i, own_end_u)) {
         if (!walk.visible_a(i) && !walk.visible_b(i)) continue;
         const int sh = walk.shard(i);
         const int y = walk.row0(i);
@@ -260,7 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attention_kernel(const __gri
         return true;
       };
       int j = 0;                                // walk ordinal of the blocks either tile sees
-      for (int i = 0; i < nwalk && ok; ++i) {
+      for (int i = walk.first(own_end_u); i < nwalk && ok; i = walk.next(i, own_end_u)) {
         const bool vis_a = walk.visible_a(i), vis_b = walk.visible_b(i);
         if (!vis_a && !vis_b) continue;
         const int pos = 2 * j;
@@ -307,7 +321,7 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attention_kernel(const __gri
     const uint32_t s_addr = lane_addr + t * kBKV;          // S_t, and P_t over its first 64
     const uint32_t o_addr = lane_addr + kColO + t * kD;    // O_t
     const bool t_valid = t == 0 ? walk.valid[0] : walk.valid[1];
-    const long long t_last = t == 0 ? walk.q_last[0] : walk.q_last[1];
+    const int t_end = t == 0 ? walk.own_end[0] : walk.own_end[1];
     // Lane 0 waits, the warp follows (the warp stops as one).
     auto wait_warp = [&](uint64_t* bar, uint32_t parity) -> bool {
       int good = 1;
@@ -316,11 +330,12 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attention_kernel(const __gri
     };
     // The last valid column of block i for this row (keys past the shard's
     // end, and with the mask past the row's own position, are out).
-    auto last_col = [&](int i) -> int {
-      const int r0 = walk.row0(i);
+    // The last valid column of the block at row r0 of shard sh (keys past the
+    // shard's end, and with the mask past the row's own position, are out).
+    auto last_col = [&](int sh, int r0) -> int {
       int c = min(kBKV, p.S - r0) - 1;
       if (p.causal) {
-        const long long lim = qpos - (static_cast<long long>(walk.shard(i)) * p.S + r0);
+        const long long lim = qpos - (static_cast<long long>(sh) * p.S + r0);
         c = static_cast<int>(min(static_cast<long long>(c), lim));
       }
       return c;                                 // -1: nothing valid
@@ -329,15 +344,18 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attention_kernel(const __gri
     int n = 0;                                  // blocks of this tile done
     float m_used = -INFINITY;                   // the maximum p is taken against
     float l = 0.f;                              // the row's sum of p
-    for (int i = 0; i < nwalk; ++i) {
-      if (!walk.visible(i, t_valid, t_last)) continue;
+    // The walk visits only this tile's visible blocks (next() skips the
+    // rest); the block's shard and row follow the walk index step by step.
+    const int i0 = t_valid ? walk.first(t_end) : nwalk;
+    int sh = i0 < nwalk ? walk.shard(i0) : 0, r0 = i0 < nwalk ? walk.row0(i0) : 0;
+    for (int i = i0; i < nwalk; ) {
       // A failed wait ends this warp's walk; the others' waits then end on
       // the abort flag or their own limit (no barrier inside the walk).
       if (!wait_warp(&s_full[t], n & 1u)) {
         ok = false;
         break;
       }
-      const int cmax = last_col(i);
+      const int cmax = last_col(sh, r0);
       uint32_t v[kBKV];
       ptx::tc_fence_after();
 #pragma unroll
@@ -427,6 +445,18 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attention_kernel(const __gri
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&p_full[t]);
       ++n;
+      const int i_next = walk.next(i, t_end);
+      if (i_next == i + 1) {
+        r0 += kBKV;
+        if (r0 >= walk.kvb * kBKV) {
+          r0 = 0;
+          sh = sh + 1 == p.R ? 0 : sh + 1;
+        }
+      } else if (i_next < nwalk) {
+        sh = walk.shard(i_next);
+        r0 = walk.row0(i_next);
+      }
+      i = i_next;
     }
     // Output: the row of O_t / l, for rows inside the shard.
     if (ok && t_valid && wait_warp(o_full, 0)) {

@@ -34,7 +34,8 @@ def _run(Q, K, V, causal, out_dtype=fcc.FCC_BF16):
 
 # S = 40 and 64: the second half of every key block is past the shard's end.
 @pytest.mark.parametrize("R,S,H", [(2, 128, 1), (2, 200, 2), (3, 256, 2), (1, 300, 1),
-                                   (4, 96, 3), (2, 513, 1), (2, 40, 2), (3, 64, 1)])
+                                   (4, 96, 3), (2, 513, 1), (2, 40, 2), (3, 64, 1),
+                                   (8, 130, 1), (8, 384, 1)])
 @pytest.mark.parametrize("causal", [False, True])
 def test_ring_attention_small(R, S, H, causal):
     Q, K, V = synth.attention_inputs(R, S, H, 128, seed=R * 1000 + S + H)
