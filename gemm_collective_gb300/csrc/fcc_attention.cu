@@ -328,8 +328,6 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attention_kernel(const __gri
       if (lane == 0) good = W.wait(bar, parity) ? 1 : 0;
       return __shfl_sync(0xffffffffu, good, 0) != 0;
     };
-    // The last valid column of block i for this row (keys past the shard's
-    // end, and with the mask past the row's own position, are out).
     // The last valid column of the block at row r0 of shard sh (keys past the
     // shard's end, and with the mask past the row's own position, are out).
     auto last_col = [&](int sh, int r0) -> int {
