@@ -116,6 +116,44 @@ __device__ __forceinline__ void pool_bag(const EmbArgs& a, int t, long long g, c
     atomicCAS(a.status, 0, static_cast<int>(FCC_ERR_INVALID));
 }
 
+// A walk over (table t, sample g = r * Bl + b) in steps of a fixed number of
+// items, table-major, without a division per step: the step is split once
+// into whole tables, whole ranks and samples, and each step adds those with
+// carries (fused form 1284-1297 -> 1246-1262 us at 8 x 64 tables of 65536 x
+// 128, against two 64-bit divisions per bag).
+struct ItemWalk {
+  int t, r, b;                 // current item
+  int st, sr, sb;              // the step in tables, ranks and samples
+  int R, Bl;
+  __device__ __forceinline__ void init(long long it, long long step, int R_, int Bl_) {
+    R = R_;
+    Bl = Bl_;
+    const long long nsamp = static_cast<long long>(R) * Bl;
+    t = static_cast<int>(it / nsamp);
+    const long long g = it - static_cast<long long>(t) * nsamp;
+    r = static_cast<int>(g / Bl);
+    b = static_cast<int>(g - static_cast<long long>(r) * Bl);
+    st = static_cast<int>(step / nsamp);
+    const long long sg = step - static_cast<long long>(st) * nsamp;
+    sr = static_cast<int>(sg / Bl);
+    sb = static_cast<int>(sg - static_cast<long long>(sr) * Bl);
+  }
+  __device__ __forceinline__ void advance() {
+    b += sb;                   // < 2 Bl
+    r += sr;
+    t += st;
+    if (b >= Bl) {
+      b -= Bl;
+      ++r;
+    }
+    if (r >= R) {              // r < 2 R
+      r -= R;
+      ++t;
+    }
+  }
+  __device__ __forceinline__ long long g() const { return static_cast<long long>(r) * Bl + b; }
+};
+
 // STAGED = false: bag (t, g) -> out[g / Bl][g % Bl][t] (the fused all-to-all);
 // STAGED = true: -> pooled[t][g] (each owner's local result).
 template <bool STAGED>
@@ -125,24 +163,25 @@ __global__ void __launch_bounds__(256) embedding_kernel(const EmbArgs a) {
   const long long items = nsamp * a.ntables;
   const long long nwarps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
   const long long esz = a.out_f32 ? 4 : 2;
-  for (long long it = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
-       it < items; it += nwarps) {
+  long long it = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (it >= items) return;
+  ItemWalk w;
+  w.init(it, nwarps, a.R, a.Bl);
+  for (; it < items; it += nwarps, w.advance()) {
     // Table-major order: the warps running at once gather from one table,
     // which stays in L2 while its bags are pooled (random indices reuse its
     // rows many times), whichever buffer the vectors go to.  (Interleaving
     // 4, 8 or 16 tables, so that consecutive bags fill adjacent output rows,
     // measured slower: the larger live set costs L2 hits.)
-    const int t = static_cast<int>(it / nsamp);
-    const long long g = it - static_cast<long long>(t) * nsamp;
+    const long long g = w.g();
     char* dst;
     if constexpr (STAGED) {
-      dst = static_cast<char*>(a.pooled) + (static_cast<long long>(t) * nsamp + g) * a.D * esz;
+      dst = static_cast<char*>(a.pooled) + (static_cast<long long>(w.t) * nsamp + g) * a.D * esz;
     } else {
-      const int r = static_cast<int>(g / a.Bl);
-      const long long b = g - static_cast<long long>(r) * a.Bl;
-      dst = static_cast<char*>(a.out[r]) + (b * a.ntables + t) * a.D * esz;
+      dst = static_cast<char*>(a.out[w.r]) +
+            (static_cast<long long>(w.b) * a.ntables + w.t) * a.D * esz;
     }
-    pool_bag(a, t, g, dst, lane);
+    pool_bag(a, w.t, g, dst, lane);
   }
 }
 
