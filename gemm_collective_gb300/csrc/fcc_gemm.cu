@@ -70,13 +70,20 @@ constexpr int threads_of() {
 
 // CG = CTAs per cluster: 1 (one CTA per 128x256 tile) or 2 (a CTA pair per
 // 256x256 tile).  Every TMA load goes to the issuing CTA's own shared memory.
-template <int CG>
+// Ring depth on CTA pairs: five stages for the ordered RS and AR (8-rank
+// RS 1.98-2.09 ms against 2.01-2.09 with seven, on three boxes, with lower
+// DRAM reads, 4.6 against 5.4 GB; AR 2.05-2.08 against 2.05-2.13; four or
+// three stages were slower), seven for the others: the AllGather + GEMM
+// (1.99-2.01 against 1.99-2.02 ms with five) and the MoE expert GEMM, whose
+// 64-deep K loops and in-kernel row copy want the deeper ring (561 us
+// against 566 with six and 585 with five).
+template <int CG, bool kShallow = false>
 struct Cfg {
   static_assert(CG == 1 || CG == 2, "one CTA or a CTA pair per tile");
   static constexpr int kPairCtas = CG;                      // CTAs of one MMA
   static constexpr int kTileM = kBM * kPairCtas;            // rows of one (pair) tile
   static constexpr int kBNcta = kBN / kPairCtas;            // B columns this CTA holds
-  static constexpr int kStages = CG >= 2 ? 7 : 4;
+  static constexpr int kStages = CG >= 2 ? (kShallow ? 5 : 7) : 4;
   static constexpr uint32_t kBBytes = kBK * kBNcta * 2;     // 32 or 16 KiB
   static constexpr uint32_t kStageBytes = kABytes + kBBytes;
   static constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(kTileM, kBN, false, true);
@@ -285,7 +292,7 @@ __device__ __forceinline__ void red_row_chunk(float* row_ptr, int col, int N,
 
 template <int MODE, int CG, class P>
 __global__ void __launch_bounds__(threads_of<MODE>(), 1) gemm_kernel(const __grid_constant__ P p) {
-  using C = Cfg<CG>;
+  using C = Cfg<CG, MODE == MODE_RS || MODE == MODE_AR>;
   constexpr int kStages = C::kStages;
   constexpr int TM = C::kTileM;
   extern __shared__ uint8_t smem_raw[];
@@ -969,10 +976,11 @@ template <int MODE, int CG, class P>
 cudaError_t launch_mode(const P& p, int grid, cudaStream_t st) {
   auto kern = gemm_kernel<MODE, CG, P>;
   static bool attr_set[64] = {};
-  const cudaError_t e = smem_attr_once(attr_set, kern, Cfg<CG>::kSmem);
+  constexpr int kSmem = Cfg<CG, MODE == MODE_RS || MODE == MODE_AR>::kSmem;
+  const cudaError_t e = smem_attr_once(attr_set, kern, kSmem);
   if (e != cudaSuccess) return e;
   // CTA pairs launch as clusters of two; a single CTA is its own cluster.
-  return launch_pdl(kern, dim3(grid, 1, 1), dim3(threads_of<MODE>(), 1, 1), Cfg<CG>::kSmem, st,
+  return launch_pdl(kern, dim3(grid, 1, 1), dim3(threads_of<MODE>(), 1, 1), kSmem, st,
                     CG == 2 ? 2u : 1u, p);
 }
 
@@ -991,13 +999,11 @@ cudaError_t launch_cg(const GemmParams& p, int mode, int grid, cudaStream_t st) 
 
 }  // namespace
 
-int gemm_smem_bytes(int cg) { return cg == 2 ? Cfg<2>::kSmem : Cfg<1>::kSmem; }
-
 namespace {
 template <int CG>
 int query_max_clusters() {
   auto kern = gemm_kernel<MODE_RS, CG, GemmParams>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<CG>::kSmem) !=
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<CG, true>::kSmem) !=
       cudaSuccess)
     return 0;
   int sms = 0, dev = 0;
@@ -1006,7 +1012,7 @@ int query_max_clusters() {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(std::max(CG, (sms / CG) * CG)), 1, 1);
   cfg.blockDim = dim3(kGemmThreads, 1, 1);
-  cfg.dynamicSmemBytes = Cfg<CG>::kSmem;
+  cfg.dynamicSmemBytes = Cfg<CG, true>::kSmem;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = CG;

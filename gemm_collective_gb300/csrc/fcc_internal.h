@@ -196,7 +196,6 @@ struct GroupedParams {
 // 256 x 256 tile.  grid is in CTAs (a multiple of cg).
 cudaError_t launch_gemm(const GemmParams& p, int mode, int cg, int grid, cudaStream_t st);
 cudaError_t launch_grouped_gemm(const GroupedParams& p, int cg, int grid, cudaStream_t st);
-int gemm_smem_bytes(int cg);
 // Clusters of cg CTAs of the GEMM kernel that fit on the current device at once.
 int gemm_max_clusters(int cg);
 cudaError_t launch_gemv(const GemvParams& p, int grid, cudaStream_t st);
