@@ -14,8 +14,8 @@
 // token t's row.  The MMA's A operand is 128 rows, of which only the first 16
 // are loaded: rows 16-127 read whatever shared memory follows (later stages),
 // and each output row depends on its own A row only, so those lanes hold
-// values nobody reads.  The stage thus costs 34 KiB instead of 48, and six
-// stages (204 KiB of B in flight) fit where four did.
+// values nobody reads.  The stage thus costs 34 KiB instead of 48; five
+// stages (160 KiB of B in flight) measured faster than six.
 //
 // Cross-CTA sum: each CTA writes its f32 partial rows for the group to its
 // own workspace slot and takes the group's ticket; the last to arrive adds the
@@ -40,7 +40,9 @@ constexpr int kStageCols = 256;                 // columns per pipeline stage (U
 constexpr int kTok = kGemvTok;                  // token rows loaded per stage (M <= 16)
 constexpr int kTokStep = 8;                     // tokens per step of the final sum
 constexpr int kMaxClusterSplits = 16;           // splits a column group's cluster may hold
-constexpr int kStages = 6;
+// Five stages: 76.2 us at the 8-rank decode workload against 77.9 with six
+// (four: 76.1).
+constexpr int kStages = 5;
 constexpr uint32_t kBBox = kBK * 64 * 2;        // [64 k][64 n] bf16 = 8 KiB
 constexpr uint32_t kBStage = 4 * kBBox;         // 32 KiB: [64 k][256 n]
 constexpr uint32_t kAStage = kTok * kBK * 2;    // 2 KiB: [16 rows][64 k], rows >= M zero
