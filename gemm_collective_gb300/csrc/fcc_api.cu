@@ -180,13 +180,13 @@ fcc_algo choose_algo(fcc_op op, int R, int64_t M, int64_t N, int64_t K, int sms,
     gemv_shape(N, R, K, sms, max_ctas, &groups, &splits);
     return splits >= 16 ? FCC_ALGO_UNFUSED : FCC_ALGO_FUSED;
   }
-  //  * Embedding + All-to-All: pooling table by table into a staging buffer,
-  //    then the exchange kernel.  Over the nine recorded runs on GB300s (8
-  //    ranks x 64 tables of 65536 x 128, 2048 samples a rank, bags of 32) it
-  //    took 1154-1418 us, median 1261, and the fused store of each pooled
-  //    row to its sample's rank 1184-1339 us, median 1317; the staged form
-  //    was the faster in five of the nine.
-  if (op == FCC_OP_EMBEDDING_A2A) return FCC_ALGO_UNFUSED;
+  //  * Embedding + All-to-All: the fused kernel (each pooled row stored
+  //    straight into its sample's rank).  With eight rows in flight a warp it
+  //    took 1133-1140 us at 8 ranks x 64 tables of 65536 x 128, 2048 samples
+  //    a rank, bags of 32, against 1304-1308 us for pooling into a staging
+  //    buffer and the exchange kernel (two boxes).  (With four rows in
+  //    flight the two forms were within the box-to-box spread, and the
+  //    staged one was kept.)
   return FCC_ALGO_FUSED;
 }
 

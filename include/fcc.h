@@ -293,8 +293,8 @@ fcc_status fcc_moe_combine(int R, const void *const *recv_y, int64_t cap, int64_
  * tables[t]: [V, D] bf16; offsets[t]: [R*Bl + 1] int32, non-decreasing;
  * indices[t]: [offsets[t][R*Bl]] int32 in [0, V); out[r]: [Bl, ntables, D]
  * (bf16 or f32).  R <= 8, ntables % R == 0, ntables <= FCC_MAX_TABLES,
- * D % 8 == 0.  opts->algo: FUSED = one kernel pools each bag and stores
- * it straight into its sample's rank buffer; UNFUSED (AUTO) = each table's
+ * D % 8 == 0.  opts->algo: FUSED (AUTO) = one kernel pools each bag and
+ * stores it straight into its sample's rank buffer; UNFUSED = each table's
  * pooled vectors into a [ntables, R*Bl, D] workspace, then a kernel moves
  * them to the sample ranks; CE = the same workspace moved by copy-engine 2-D
  * copies (one per table and rank).  A negative offset step or an index
@@ -354,12 +354,11 @@ const char *fcc_status_string(fcc_status s);
  * would split the rank-and-K range 16 or more ways (few 512-column groups:
  * its final serial sum of the splits then costs more than the plain GEMM +
  * reduce), else FCC_ALGO_FUSED; for the embedding + All-to-All,
- * FCC_ALGO_UNFUSED (pooling table by table into a staging buffer, then the
- * exchange: median 1261 us over nine runs on 8 ranks x 64 tables of 65536 x
- * 128, 2048 samples a rank, bags of 32, against 1317 us for storing each
- * pooled row straight to its sample's rank; the staged form was the faster
- * in five of the nine).  sms: SMs to plan for (0 = the current
- * device's, 152 without one); max_ctas as in fcc_opts.  Host-only.
+ * FCC_ALGO_FUSED (1133-1140 us on 8 ranks x 64 tables of 65536 x 128, 2048
+ * samples a rank, bags of 32, against 1304-1308 us for pooling table by table
+ * into a staging buffer and then the exchange).  sms: SMs to plan for (0 =
+ * the current device's, 152 without one); max_ctas as in fcc_opts.
+ * Host-only.
  */
 fcc_algo fcc_choose_algo(fcc_op op, int R, int64_t M, int64_t N, int64_t K, int sms,
                          int max_ctas);

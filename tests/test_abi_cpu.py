@@ -148,5 +148,5 @@ def test_strategy_selector(fcc):
     assert fcc.fcc_choose_algo(gemv, 8, 8, 1024, 3584, 152, 64) == U
     # few K blocks bound the splits: 2 ranks x 1 block of 64 -> 2 splits
     assert fcc.fcc_choose_algo(gemv, 2, 8, 512, 64, 152) == F
-    # embedding + all-to-all: pooling per table, then the exchange
-    assert fcc.fcc_choose_algo(fcc.FCC_OP_EMBEDDING_A2A, 8, 0, 0, 0, 152) == U
+    # embedding + all-to-all: the fused pooling + exchange
+    assert fcc.fcc_choose_algo(fcc.FCC_OP_EMBEDDING_A2A, 8, 0, 0, 0, 152) == F
