@@ -932,8 +932,10 @@ def run_fcc(args, world, rank, local, pg):
     sustained = timed_s >= 0.5
     peak = pk["bf16_tflops_sustained"] if sustained else pk["bf16_tflops"]
     achieved = flops / (ms_local * 1e-3) / 1e12
+    # (the kernel sources and the host code that sets its raster and splits)
     traffic = kernel_traffic("gemm_rs_fused", ["gemm_collective_gb300/csrc/fcc_gemm.cu",
-                                                "gemm_collective_gb300/csrc/fcc_ptx.cuh"])
+                                                "gemm_collective_gb300/csrc/fcc_ptx.cuh",
+                                                "gemm_collective_gb300/csrc/fcc_api.cu"])
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "traffic": traffic,
                 "peak_source": f"{pk_src} {'sustained' if sustained else 'burst'} bf16",

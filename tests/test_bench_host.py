@@ -13,7 +13,8 @@ sys.path.insert(0, ROOT)
 
 import bench  # noqa: E402
 
-SOURCES = ["gemm_collective_gb300/csrc/fcc_gemm.cu", "gemm_collective_gb300/csrc/fcc_ptx.cuh"]
+SOURCES = ["gemm_collective_gb300/csrc/fcc_gemm.cu", "gemm_collective_gb300/csrc/fcc_ptx.cuh",
+           "gemm_collective_gb300/csrc/fcc_api.cu"]
 
 
 def _write_capture(root, sha, total=123456789):
