@@ -676,7 +676,7 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) gemm_kernel(const __gri
 #pragma unroll
               for (int j = 0; j < kV; ++j) {
                 const int v = v0 + 32 * j + lane;
-                if (v < vec) x[j] = __ldcs(sp + v);
+                if (v < vec) x[j] = __ldg(sp + v);  // (read-only path: 602.6 against 608.3 us)
               }
 #pragma unroll
               for (int j = 0; j < kV; ++j) {
