@@ -112,6 +112,7 @@ _launches = _sig("fcc_launch_count", ctypes.c_uint64, [])
 _version = _sig("fcc_version", ctypes.c_char_p, [])
 _wait_timeout = _sig("fcc_test_wait_timeout", _I, [_I64, _P])
 _grouped_wait_timeout = _sig("fcc_test_grouped_wait_timeout", _I, [_I64, _P])
+_ksplit_wait_timeout = _sig("fcc_test_ksplit_wait_timeout", _I, [_I64, _P])
 
 
 # ---------------------------------------------------------------- marshalling
@@ -273,6 +274,10 @@ def fcc_test_wait_timeout(timeout_ns: int, stream=None):
 
 def fcc_test_grouped_wait_timeout(timeout_ns: int, stream=None):
     _check(_grouped_wait_timeout(timeout_ns, _stream(stream)), "fcc_test_grouped_wait_timeout")
+
+
+def fcc_test_ksplit_wait_timeout(timeout_ns: int, stream=None):
+    _check(_ksplit_wait_timeout(timeout_ns, _stream(stream)), "fcc_test_ksplit_wait_timeout")
 
 
 def raw_status(fn_name: str, *args) -> int:

@@ -980,6 +980,44 @@ fcc_status fcc_test_wait_timeout(int64_t timeout_ns, fcc_stream_t stream) {
                                      reinterpret_cast<cudaStream_t>(stream)));
 }
 
+// Test support: a 1-rank 384 x 256 x 128 reduce-scatter (zeros) on two single
+// CTAs, so its three 128-row tiles take a round of two and a last tile split
+// in K; the second K half waits for a call id the first half never writes,
+// so its bounded wait runs out after timeout_ns.
+fcc_status fcc_test_ksplit_wait_timeout(int64_t timeout_ns, fcc_stream_t stream) {
+  if (timeout_ns <= 0) return FCC_ERR_INVALID;
+  DeviceState* d = nullptr;
+  fcc_status s = device_state(&d);
+  if (s != FCC_OK) return s;
+  constexpr int64_t kM = 384, kN = 256, kK = 128;
+  const size_t a_bytes = static_cast<size_t>(kM) * kK * 2, b_bytes = static_cast<size_t>(kK) * kN * 2,
+               o_bytes = static_cast<size_t>(kM) * kN * 4, w_bytes = ksplit_ws_bytes(1, 1);
+  const size_t total = align_up(a_bytes) + align_up(b_bytes) + align_up(o_bytes) + align_up(w_bytes);
+  fcc_opts o;
+  std::memset(&o, 0, sizeof(o));
+  o.algo = FCC_ALGO_FUSED;
+  o.deterministic = 1;
+  o.max_ctas = 2;
+  o.cta_pair = 1;
+  o.timeout_ns = timeout_ns;
+  void* ws = nullptr;
+  if ((s = get_workspace(d, nullptr, total, &ws)) != FCC_OK) return s;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(ws, 0, total, st) != cudaSuccess) return FCC_ERR_CUDA;
+  char* base = static_cast<char*>(ws);
+  const void* A[1] = {base};
+  const void* B[1] = {base + align_up(a_bytes)};
+  void* out[1] = {base + align_up(a_bytes) + align_up(b_bytes)};
+  GemmParams p;
+  if ((s = gemm_params(p, d, MODE_RS, 1, A, B, out, 1, kM, kN, kK, kM, 0, kM, 1, &o)) != FCC_OK)
+    return s;
+  if (p.cg != 1 || ksplit_tiles(p, gemm_slots(p, d, &o)) != 1) return FCC_ERR_UNSUPPORTED;
+  p.split_ws = reinterpret_cast<float*>(base + align_up(a_bytes) + align_up(b_bytes) +
+                                        align_up(o_bytes));
+  p.flag_skew = 2;  // (call ids are odd: the skewed one is never written)
+  return run_gemm(p, MODE_RS, d, &o, st);
+}
+
 }  // extern "C"
 
 // ------------------------------------------------------------------------

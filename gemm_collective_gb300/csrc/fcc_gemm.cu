@@ -868,7 +868,7 @@ __global__ void __launch_bounds__(threads_of<MODE>(), 1) gemm_kernel(const __gri
           // Second half: wait for the first half's partial (bounded), add it to
           // this accumulator and store the sums.  f32 addition is commutative,
           // so the result does not depend on which half finished first.
-          if (threadIdx.x == 64) *bcast = W.wait_eq(flag, p.call_id) ? 1 : 0;
+          if (threadIdx.x == 64) *bcast = W.wait_eq(flag, p.call_id + p.flag_skew) ? 1 : 0;
           ptx::named_barrier_sync(1, 128);
           if (*bcast) {
             const float* src = part;

@@ -123,6 +123,7 @@ struct GemmParams {
   float* split_ws;                    // [split tiles][CG][128][256] f32, then the flags
   unsigned long long* split_flags;    // [split tiles][CG]
   unsigned long long call_id;
+  unsigned long long flag_skew;       // test support: the second half waits for call_id + this
 };
 
 // Bytes of the K-split workspace for `tiles` split tiles of `cg` CTAs each.

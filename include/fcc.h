@@ -393,6 +393,16 @@ fcc_status fcc_test_wait_timeout(int64_t timeout_ns, fcc_stream_t stream);
  */
 fcc_status fcc_test_grouped_wait_timeout(int64_t timeout_ns, fcc_stream_t stream);
 
+/*
+ * Test support: launches the fused GEMM + ReduceScatter kernel on a small
+ * problem (1 rank, 384 x 256 x 128, on two single CTAs) whose short last
+ * round runs as two K halves, with the second half waiting for a flag value
+ * the first never writes, so that bounded wait runs out after timeout_ns;
+ * the kernel records FCC_ERR_TIMEOUT, stores nothing for that tile and
+ * returns, leaving the context usable.  Uses the internal workspace pool.
+ */
+fcc_status fcc_test_ksplit_wait_timeout(int64_t timeout_ns, fcc_stream_t stream);
+
 /* Number of kernels this library has launched in this process (all devices). */
 uint64_t fcc_launch_count(void);
 

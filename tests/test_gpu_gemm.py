@@ -435,6 +435,21 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     assert np.array_equal(to_f64(outs[1]), oracle.gemm_rs(A, B, 1))
 
 
+def test_k_half_wait_reports_timeout_and_context_survives():
+    """The second K half of a short last round waits (bounded) for the first
+    half's partial: with the flag value it waits for never written, the wait
+    runs out, the status word says so and clears, and the same split launch
+    afterwards is exact."""
+    fcc.fcc_test_ksplit_wait_timeout(2_000_000)  # 2 ms
+    assert fcc.fcc_stream_status() == fcc.FCC_ERR_TIMEOUT
+    assert fcc.fcc_stream_status() == fcc.FCC_OK
+    R, M, N, K = 1, 384, 256, 128  # three 128-row tiles on two CTAs: the last in K halves
+    A, B = synth.integer_gemm_inputs(R, M, N, K, -3, 3, seed=8)
+    dA, dB = _upload(A, B)
+    outs = _rs(R, dA, dB, M, N, K, fcc.FCC_F32, fcc.make_opts(cta_pair=1, max_ctas=2))
+    assert np.array_equal(to_f64(outs[0]), oracle.gemm_rs(A, B, 0))
+
+
 def test_invalid_arguments_rejected_before_launch():
     R, M, N, K = 2, 256, 256, 128
     A, B = synth.gemm_inputs(R, M, N, K, 1.0, 1.0)
