@@ -6,12 +6,15 @@
 
 #include <algorithm>
 #include <atomic>
+#include <cctype>
 #include <chrono>
 #include <cmath>
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <random>
+#include <string>
 
 #include "fcc.h"
 #include "fcc_internal.h"
@@ -152,13 +155,23 @@ bool ptrs_ok(const void* const* arr, int n) {
 }
 
 unsigned long long timeout_of(const fcc_opts* o) {
-  return (o != nullptr && o->timeout_ns > 0) ? static_cast<unsigned long long>(o->timeout_ns)
-                                              : kDefaultTimeoutNs;
+  if (o != nullptr && o->timeout_ns > 0) return static_cast<unsigned long long>(o->timeout_ns);
+  const int64_t env = env_defaults().timeout_ns;
+  return env > 0 ? static_cast<unsigned long long>(env) : kDefaultTimeoutNs;
 }
 
 fcc_algo algo_of(const fcc_opts* o) {
-  if (o == nullptr || o->algo == FCC_ALGO_AUTO) return FCC_ALGO_FUSED;
+  if (o == nullptr || o->algo == FCC_ALGO_AUTO) {
+    const fcc_algo env = env_defaults().algo;
+    return env != FCC_ALGO_AUTO ? env : FCC_ALGO_FUSED;
+  }
   return o->algo;
+}
+
+// opts->chunks, else FCC_CHUNKS, else 0 (the cost model decides).
+int chunks_of(const fcc_opts* o) {
+  if (o != nullptr && o->chunks > 0) return o->chunks;
+  return env_defaults().chunks;
 }
 
 }  // namespace
@@ -175,6 +188,8 @@ fcc_algo algo_of(const fcc_opts* o) {
 //    against 45.5 us.  So the plain form is chosen from 16 splits on.
 fcc_algo choose_algo(fcc_op op, int R, int64_t M, int64_t N, int64_t K, int sms, int max_ctas) {
   (void)M;
+  // FCC_ALGO in the environment replaces the rule below.
+  if (env_defaults().algo != FCC_ALGO_AUTO) return env_defaults().algo;
   if (op == FCC_OP_GEMV_AR) {
     int groups = 0, splits = 0;
     gemv_shape(N, R, K, sms, max_ctas, &groups, &splits);
@@ -192,7 +207,10 @@ fcc_algo choose_algo(fcc_op op, int R, int64_t M, int64_t N, int64_t K, int sms,
 
 namespace {
 
-bool deterministic_of(const fcc_opts* o) { return o == nullptr || o->deterministic != 0; }
+bool deterministic_of(const fcc_opts* o) {
+  if (o != nullptr) return o->deterministic != 0;
+  return env_defaults().deterministic != 0;  // (-1, unset: deterministic)
+}
 
 // Tensor-core tile shape (CTAs per cluster): a CTA pair per 256-row tile
 // unless the rows are few (one CTA per 128-row tile), or the caller's shape.
@@ -526,8 +544,7 @@ fcc_status rank_sum_unfused(int R, const void* const* A, const void* const* B, v
 
   // INTERDECOM: GEMM of row chunk i on the caller stream overlaps the reduce
   // of chunk i-1 on a side stream.
-  int chunks = (o != nullptr && o->chunks > 0) ? o->chunks
-                                               : model_chunks(R, M, N, K, out_f32 ? 4 : 2);
+  int chunks = chunks_of(o) > 0 ? chunks_of(o) : model_chunks(R, M, N, K, out_f32 ? 4 : 2);
   chunks = std::max(1, std::min(chunks, kMaxChunks));
   const int64_t rows = chunk_rows(M, chunks);
   cudaStream_t side = d->side[0];
@@ -642,6 +659,35 @@ GemvPlan gemv_plan(int R, int64_t M, int64_t N, int64_t K, int sms, const fcc_op
 }
 
 }  // namespace
+
+const EnvDefaults& env_defaults() {
+  static EnvDefaults e;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    auto integer = [](const char* name, long long lo, long long hi, long long* out) {
+      const char* v = std::getenv(name);
+      if (v == nullptr || *v == 0) return false;
+      char* end = nullptr;
+      const long long n = std::strtoll(v, &end, 10);
+      if (end == nullptr || *end != 0 || n < lo || n > hi) return false;
+      *out = n;
+      return true;
+    };
+    if (const char* v = std::getenv("FCC_ALGO")) {
+      std::string a(v);
+      for (char& c : a) c = static_cast<char>(std::tolower(static_cast<unsigned char>(c)));
+      if (a == "fused") e.algo = FCC_ALGO_FUSED;
+      else if (a == "unfused") e.algo = FCC_ALGO_UNFUSED;
+      else if (a == "interdecom") e.algo = FCC_ALGO_INTERDECOM;
+      else if (a == "ce") e.algo = FCC_ALGO_CE;
+    }
+    long long n = 0;
+    if (integer("FCC_DETERMINISTIC", 0, 1, &n)) e.deterministic = static_cast<int>(n);
+    if (integer("FCC_CHUNKS", 1, kMaxChunks, &n)) e.chunks = static_cast<int>(n);
+    if (integer("FCC_TIMEOUT_MS", 1, 3600 * 1000, &n)) e.timeout_ns = n * 1000 * 1000;
+  });
+  return e;
+}
 
 int* device_status_ptr() {
   DeviceState* d = nullptr;
@@ -805,8 +851,7 @@ fcc_status fcc_ag_gemm(int R, const void* const* X_shard, const void* const* B, 
     // stream at once, and the GEMM of chunk i (rows [m0, m1) of every rank's
     // output) runs on the caller's stream after chunk i's gather, so chunk
     // i+1's gather overlaps chunk i's GEMM.  Chunks are whole 256-row tiles.
-    int chunks = (opts != nullptr && opts->chunks > 0) ? opts->chunks
-                                                       : ag_model_chunks(R, M, N, K);
+    int chunks = chunks_of(opts) > 0 ? chunks_of(opts) : ag_model_chunks(R, M, N, K);
     chunks = std::max(1, std::min(chunks, kMaxChunks));
     const int64_t rows = chunk_rows(M, chunks, 2 * kBM);
     cudaStream_t side = d->side[0];

@@ -262,4 +262,15 @@ fcc_status internal_streams_events(cudaStream_t* side, int nside, cudaEvent_t* e
 fcc_status internal_host_buffer(size_t bytes, void** out);
 // The algorithm FCC_ALGO_AUTO runs (the strategy selector, fcc_api.cu).
 fcc_algo choose_algo(fcc_op op, int R, int64_t M, int64_t N, int64_t K, int sms, int max_ctas);
+// Defaults from the environment, read once (fcc.h, fcc_opts): the algorithm
+// that replaces FCC_ALGO_AUTO (FCC_ALGO_AUTO when unset), the deterministic
+// setting of calls without opts (-1 when unset), the InterDecom chunk count
+// (0 when unset) and the device wait limit (0 when unset).
+struct EnvDefaults {
+  fcc_algo algo = FCC_ALGO_AUTO;
+  int deterministic = -1;
+  int chunks = 0;
+  int64_t timeout_ns = 0;
+};
+const EnvDefaults& env_defaults();
 }  // namespace fcc

@@ -766,7 +766,8 @@ fcc_status fcc_moe_dispatch_gemm(int R, const void* const* X, const float* const
   fcc_status s = check_moe(R, X, logits, W, T, H, F, E, topk, recv_x, recv_y, cap, topk_idx,
                            topk_gate, expert_counts, send_counts, recv_src, in, out_dtype, opts);
   if (s != FCC_OK) return s;
-  const fcc_algo algo = opts != nullptr ? opts->algo : FCC_ALGO_AUTO;
+  fcc_algo algo = opts != nullptr ? opts->algo : FCC_ALGO_AUTO;
+  if (algo == FCC_ALGO_AUTO) algo = env_defaults().algo;  // (FCC_ALGO; AUTO when unset)
   const bool gather = moe_gathers(opts, R, X, T, H);
   const bool interdecom = algo == FCC_ALGO_INTERDECOM;
   const bool ce = algo == FCC_ALGO_CE;
@@ -902,7 +903,8 @@ fcc_status fcc_moe_dispatch_gemm(int R, const void* const* X, const float* const
     // caller's stream after range i's copy, so range i+1's copy overlaps
     // range i's GEMM.  c from opts->chunks or the chunk model.
     int chunks = (opts != nullptr && opts->chunks > 0) ? opts->chunks
-                                                       : moe_model_chunks(R, T, H, F, E, topk);
+                 : (env_defaults().chunks > 0 ? env_defaults().chunks
+                                              : moe_model_chunks(R, T, H, F, E, topk));
     chunks = std::max(1, std::min(chunks, E));
     cudaStream_t side = nullptr;
     cudaEvent_t ev[FCC_MAX_EXPERTS + 1];

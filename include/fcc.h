@@ -36,6 +36,15 @@
  *  - Not thread-safe for concurrent calls on the same stream; calls on
  *    different streams share the internal pool and must not overlap unless
  *    each passes its own workspace.
+ *  - Environment defaults, read once when the library first needs one:
+ *    FCC_ALGO=fused|unfused|interdecom|ce replaces FCC_ALGO_AUTO (also in
+ *    fcc_choose_algo) for the operators with several forms (a form an
+ *    operator lacks gives FCC_ERR_UNSUPPORTED; the attention and the MoE
+ *    combine have one form and ignore it); FCC_DETERMINISTIC=0|1 is the
+ *    summation mode of calls with opts == NULL; FCC_CHUNKS=n (1..64) the
+ *    InterDecom chunk count where opts->chunks is 0; FCC_TIMEOUT_MS=n the
+ *    device wait limit where opts->timeout_ns is 0.  Unset or unparsable
+ *    values leave the built-in defaults.
  */
 #ifndef FCC_H_
 #define FCC_H_

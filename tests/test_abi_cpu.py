@@ -150,3 +150,41 @@ def test_strategy_selector(fcc):
     assert fcc.fcc_choose_algo(gemv, 2, 8, 512, 64, 152) == F
     # embedding + all-to-all: the fused pooling + exchange
     assert fcc.fcc_choose_algo(fcc.FCC_OP_EMBEDDING_A2A, 8, 0, 0, 0, 152) == F
+
+
+def _in_subprocess(env_extra, code):
+    """Runs `code` with the library loaded in a fresh process whose environment
+    adds env_extra (the environment defaults are read once per process)."""
+    import subprocess
+    import sys
+    env = dict(os.environ)
+    env.update(env_extra)
+    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env, capture_output=True,
+                       text=True, timeout=120)
+    assert r.returncode == 0, r.stderr
+    return r.stdout.strip()
+
+
+def test_environment_algorithm_default():
+    """FCC_ALGO replaces the AUTO rule (here in fcc_choose_algo, which the calls
+    use); an unknown value leaves the rule."""
+    code = ("import gemm_collective_gb300 as f; "
+            "print(f.fcc_choose_algo(f.FCC_OP_GEMM_RS, 8, 8192, 8192, 3584, 152), "
+            "f.fcc_choose_algo(f.FCC_OP_EMBEDDING_A2A, 8, 0, 0, 0, 152))")
+    import gemm_collective_gb300 as f
+    U, C, F = f.FCC_ALGO_UNFUSED, f.FCC_ALGO_CE, f.FCC_ALGO_FUSED
+    assert _in_subprocess({"FCC_ALGO": "unfused"}, code) == f"{U} {U}"
+    assert _in_subprocess({"FCC_ALGO": "CE"}, code) == f"{C} {C}"
+    assert _in_subprocess({"FCC_ALGO": "bogus"}, code) == f"{F} {F}"
+
+
+def test_environment_deterministic_default_sizes_workspace():
+    """FCC_DETERMINISTIC=0 makes calls without opts use the push mode, whose
+    bf16 form needs an f32 accumulator: the size query with opts == NULL
+    reports it."""
+    code = ("import gemm_collective_gb300 as f; "
+            "print(f.fcc_workspace_size(f.FCC_OP_GEMM_RS, 8, 8192, 8192, 3584, None))")
+    push = int(_in_subprocess({"FCC_DETERMINISTIC": "0"}, code))
+    ordered = int(_in_subprocess({"FCC_DETERMINISTIC": "1"}, code))
+    assert push >= 8192 * 8192 * 4 > ordered
+
