@@ -17,6 +17,10 @@
 //   accumulator (in TMEM) and its sum l by 2^(m_old c - m_new c);
 //   P (bf16) is written into TMEM over the first 64 columns of S_t and is the
 //   A operand of O_t += P V (tcgen05, A from TMEM); at the end O_t / l.
+// Past a tile's first block, a whole (unmasked) block is exponentiated
+// against the current maximum 32 columns at a time while the next 32 come
+// from TMEM, its maximum taken along the way; only a block whose maximum
+// calls for a raise starts over from S (still in TMEM) in the general form.
 // One softmax thread owns one query row and all 128 columns of a block, so
 // no two threads share a row's maximum or sum.  The two tiles take turns on
 // the tensor core: while tile A's softmax runs, the tensor core computes tile
@@ -125,6 +129,21 @@ __device__ __forceinline__ uint64_t desc_kmajor(uint32_t base, int kk) {
 // apart): descriptor of the 16-key K step kk.
 __device__ __forceinline__ uint64_t desc_mnmajor(uint32_t base, int kk) {
   return ptx::smem_desc_sw128(base + kk * 2048, kAtom, 1024);
+}
+
+// tcgen05.wait::ld tied to the 32 registers one 32x32b.x32 load filled, so
+// the compiler keeps every use of them after the wait while arithmetic on
+// other registers may run between the load and the wait.
+__device__ __forceinline__ void tmem_ld_wait_regs(uint32_t (&v)[32]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(v[0]), "+r"(v[1]), "+r"(v[2]), "+r"(v[3]), "+r"(v[4]), "+r"(v[5]),
+                 "+r"(v[6]), "+r"(v[7]), "+r"(v[8]), "+r"(v[9]), "+r"(v[10]), "+r"(v[11]),
+                 "+r"(v[12]), "+r"(v[13]), "+r"(v[14]), "+r"(v[15]), "+r"(v[16]), "+r"(v[17]),
+                 "+r"(v[18]), "+r"(v[19]), "+r"(v[20]), "+r"(v[21]), "+r"(v[22]), "+r"(v[23]),
+                 "+r"(v[24]), "+r"(v[25]), "+r"(v[26]), "+r"(v[27]), "+r"(v[28]), "+r"(v[29]),
+                 "+r"(v[30]), "+r"(v[31])
+               :
+               : "memory");
 }
 
 __global__ void __launch_bounds__(kThreads, 1) ring_attention_kernel(const __grid_constant__ AttnParams p) {
@@ -354,88 +373,151 @@ __global__ void __launch_bounds__(kThreads, 1) ring_attention_kernel(const __gri
         break;
       }
       const int cmax = last_col(sh, r0);
-      uint32_t v[kBKV];
+      uint32_t vb[2][32];                       // two 32-column chunks of S in flight
+      bool done = false;
       ptx::tc_fence_after();
+      // The form is chosen for the whole warp (the TMEM loads and stores
+      // and the vote below are warp-collective): with the mask, cmax differs
+      // from row to row on a diagonal block.
+      if (n > 0 && __all_sync(0xffffffffu, cmax >= kBKV - 1)) {
+        // Speculative form, for a whole block once the row has a maximum:
+        // each 32-column chunk of S is exponentiated against the current
+        // maximum while the next chunk is still coming from TMEM, and the
+        // block's maximum is taken along the way.  P is stored only if no
+        // row's block maximum exceeds its current one by more than kRaise
+        // (rare past a tile's first block); otherwise the general form below
+        // starts over from S, still intact in TMEM, with the same result.
+        const float msc = m_used * p.scale_log2;
+        const uint64_t c2 = ptx::f32x2_pack(p.scale_log2, p.scale_log2);
+        const uint64_t n2 = ptx::f32x2_pack(-msc, -msc);
+        uint64_t s2[4] = {0, 0, 0, 0};          // four chains of packed partial sums (a half)
+        float ls[4] = {0.f, 0.f, 0.f, 0.f};     // the halves' sums, as the general form adds them
+        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        uint32_t pk[64];                        // bf16 pairs of p, the whole block
+        ptx::tmem_ld_32x32b_x32(s_addr, vb[0]);
+        tmem_ld_wait_regs(vb[0]);
 #pragma unroll
-      for (int k = 0; k < kBKV; k += 32)
-        ptx::tmem_ld_32x32b_x32(s_addr + k, *reinterpret_cast<uint32_t(*)[32]>(v + k));
-      ptx::tmem_ld_wait();
-      float bm = -INFINITY;
-      if (cmax >= kBKV - 1) {
-        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};  // four short chains
+        for (int c = 0; c < 4; ++c) {
+          if (c < 3) ptx::tmem_ld_32x32b_x32(s_addr + 32 * (c + 1), vb[(c + 1) & 1]);
 #pragma unroll
-        for (int k = 0; k < kBKV; k += 2)
-          mx[(k / 2) & 3] = ptx::max3(mx[(k / 2) & 3], __uint_as_float(v[k]),
-                                      __uint_as_float(v[k + 1]));
-        bm = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-      } else {
-#pragma unroll
-        for (int k = 0; k < kBKV; ++k)
-          if (k <= cmax) bm = fmaxf(bm, __uint_as_float(v[k]));
-      }
-      // Raise the maximum when this block's exceeds it by more than kRaise.
-      const bool raise = bm * p.scale_log2 > m_used * p.scale_log2 + kRaise;
-      const float m_new = raise ? bm : m_used;
-      const float corr = ptx::ex2_approx((m_used - m_new) * p.scale_log2);  // 0 at the start
-      if (raise) l *= (m_used == -INFINITY) ? 0.f : corr;
-      m_used = m_new;
-      const float msc = m_used * p.scale_log2;
-      float ls[4] = {0.f, 0.f, 0.f, 0.f};       // four partial sums of this block's p
-      // Two halves of 64 scores; each half's 32 bf16 pairs of p go to TMEM
-      // over columns its scores came from (read above) as soon as they exist.
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        uint32_t pk[32];                        // bf16 pairs of p
-        if (cmax >= kBKV - 1) {
-          const uint64_t c2 = ptx::f32x2_pack(p.scale_log2, p.scale_log2);
-          const uint64_t n2 = ptx::f32x2_pack(-msc, -msc);
-          uint64_t s2[4] = {0, 0, 0, 0};        // four chains of packed partial sums
-#pragma unroll
-          for (int k = 0; k < 64; k += 2) {
-            const int kv = 64 * hf + k;
+          for (int k = 0; k < 32; k += 2) {
+            const float x0 = __uint_as_float(vb[c & 1][k]), x1 = __uint_as_float(vb[c & 1][k + 1]);
+            mx[(k / 2) & 3] = ptx::max3(mx[(k / 2) & 3], x0, x1);
             float y0, y1;
-            const uint64_t x2 = ptx::f32x2_pack(__uint_as_float(v[kv]), __uint_as_float(v[kv + 1]));
-            ptx::f32x2_unpack(ptx::f32x2_fma(x2, c2, n2), y0, y1);   // s c - m c, two at once
+            ptx::f32x2_unpack(ptx::f32x2_fma(ptx::f32x2_pack(x0, x1), c2, n2), y0, y1);
             const float p0 = ptx::ex2_approx(y0);
             const float p1 = ptx::ex2_approx(y1);
             s2[(k / 2) & 3] = ptx::f32x2_add(s2[(k / 2) & 3], ptx::f32x2_pack(p0, p1));
-            pk[k / 2] = ptx::pack_bf16x2(p0, p1);
+            pk[16 * c + k / 2] = ptx::pack_bf16x2(p0, p1);
           }
+          if (c & 1) {
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            float a0, a1;
-            ptx::f32x2_unpack(s2[j], a0, a1);
-            ls[j] += a0 + a1;
+            for (int j = 0; j < 4; ++j) {
+              float a0, a1;
+              ptx::f32x2_unpack(s2[j], a0, a1);
+              ls[j] += a0 + a1;
+              s2[j] = 0;
+            }
           }
-        } else {
+          if (c < 3) tmem_ld_wait_regs(vb[(c + 1) & 1]);
+        }
+        const float bm = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+        if (!__any_sync(0xffffffffu, bm * p.scale_log2 > msc + kRaise)) {
+          ptx::tmem_st_32x32b_x32(s_addr, *reinterpret_cast<uint32_t(*)[32]>(pk));
+          ptx::tmem_st_32x32b_x32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(pk + 32));
+          l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+          done = true;
+        }
+      }
+      if (!done) {  // warp-uniform: decided by __any_sync
+        // General form: the block's maximum over the valid columns, then the
+        // exponentials, in two passes over S in TMEM (a chunk at a time).
+        float bm = -INFINITY;
 #pragma unroll
-          for (int k = 0; k < 64; k += 2) {
-            const int kv = 64 * hf + k;
-            float p0 = ptx::ex2_approx(fmaf(__uint_as_float(v[kv]), p.scale_log2, -msc));
-            float p1 = ptx::ex2_approx(fmaf(__uint_as_float(v[kv + 1]), p.scale_log2, -msc));
-            if (kv > cmax) p0 = 0.f;
-            if (kv + 1 > cmax) p1 = 0.f;
-            ls[(k / 2) & 3] += p0 + p1;
-            pk[k / 2] = ptx::pack_bf16x2(p0, p1);
+        for (int c = 0; c < 4; ++c) {
+          ptx::tmem_ld_32x32b_x32(s_addr + 32 * c, vb[c & 1]);
+          tmem_ld_wait_regs(vb[c & 1]);
+          if (cmax >= kBKV - 1) {
+            float mx[4] = {bm, -INFINITY, -INFINITY, -INFINITY};  // four short chains
+#pragma unroll
+            for (int k = 0; k < 32; k += 2)
+              mx[(k / 2) & 3] = ptx::max3(mx[(k / 2) & 3], __uint_as_float(vb[c & 1][k]),
+                                          __uint_as_float(vb[c & 1][k + 1]));
+            bm = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+          } else {
+#pragma unroll
+            for (int k = 0; k < 32; ++k)
+              if (32 * c + k <= cmax) bm = fmaxf(bm, __uint_as_float(vb[c & 1][k]));
           }
         }
-        ptx::tmem_st_32x32b_x32(s_addr + 32 * hf, pk);
-      }
-      l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-      // Rows whose maximum was raised rescale their O_t (after the first
-      // block, when it holds earlier blocks' sums), here where the scores
-      // are no longer held.  S_t of this block was issued after the last
-      // P_t V, so O_t has no product in flight until P_t is signalled.
-      if (n > 0 && __any_sync(0xffffffffu, raise)) {
-        const float f = raise ? corr : 1.f;
-#pragma unroll 1
-        for (int c = 0; c < kD; c += 32) {
-          uint32_t o[32];
-          ptx::tmem_ld_32x32b_x32(o_addr + c, o);
-          ptx::tmem_ld_wait();
+        // Raise the maximum when this block's exceeds it by more than kRaise.
+        const bool raise = bm * p.scale_log2 > m_used * p.scale_log2 + kRaise;
+        const float m_new = raise ? bm : m_used;
+        const float corr = ptx::ex2_approx((m_used - m_new) * p.scale_log2);  // 0 at the start
+        if (raise) l *= (m_used == -INFINITY) ? 0.f : corr;
+        m_used = m_new;
+        const float msc = m_used * p.scale_log2;
+        float ls[4] = {0.f, 0.f, 0.f, 0.f};     // four partial sums of this block's p
+        // Two halves of 64 scores; each half's 32 bf16 pairs of p go to TMEM
+        // over columns its scores came from (read just before).
 #pragma unroll
-          for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * f);
-          ptx::tmem_st_32x32b_x32(o_addr + c, o);
+        for (int hf = 0; hf < 2; ++hf) {
+          ptx::tmem_ld_32x32b_x32(s_addr + 64 * hf, vb[0]);
+          ptx::tmem_ld_32x32b_x32(s_addr + 64 * hf + 32, vb[1]);
+          tmem_ld_wait_regs(vb[0]);
+          tmem_ld_wait_regs(vb[1]);
+          uint32_t pk[32];                      // bf16 pairs of p
+          if (cmax >= kBKV - 1) {
+            const uint64_t c2 = ptx::f32x2_pack(p.scale_log2, p.scale_log2);
+            const uint64_t n2 = ptx::f32x2_pack(-msc, -msc);
+            uint64_t s2[4] = {0, 0, 0, 0};      // four chains of packed partial sums
+#pragma unroll
+            for (int k = 0; k < 64; k += 2) {
+              float y0, y1;
+              const uint64_t x2 = ptx::f32x2_pack(__uint_as_float(vb[k >> 5][k & 31]),
+                                                  __uint_as_float(vb[k >> 5][(k & 31) + 1]));
+              ptx::f32x2_unpack(ptx::f32x2_fma(x2, c2, n2), y0, y1);   // s c - m c, two at once
+              const float p0 = ptx::ex2_approx(y0);
+              const float p1 = ptx::ex2_approx(y1);
+              s2[(k / 2) & 3] = ptx::f32x2_add(s2[(k / 2) & 3], ptx::f32x2_pack(p0, p1));
+              pk[k / 2] = ptx::pack_bf16x2(p0, p1);
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              float a0, a1;
+              ptx::f32x2_unpack(s2[j], a0, a1);
+              ls[j] += a0 + a1;
+            }
+          } else {
+#pragma unroll
+            for (int k = 0; k < 64; k += 2) {
+              const int kv = 64 * hf + k;
+              float p0 = ptx::ex2_approx(fmaf(__uint_as_float(vb[k >> 5][k & 31]), p.scale_log2, -msc));
+              float p1 = ptx::ex2_approx(fmaf(__uint_as_float(vb[k >> 5][(k & 31) + 1]), p.scale_log2, -msc));
+              if (kv > cmax) p0 = 0.f;
+              if (kv + 1 > cmax) p1 = 0.f;
+              ls[(k / 2) & 3] += p0 + p1;
+              pk[k / 2] = ptx::pack_bf16x2(p0, p1);
+            }
+          }
+          ptx::tmem_st_32x32b_x32(s_addr + 32 * hf, pk);
+        }
+        l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+        // Rows whose maximum was raised rescale their O_t (after the first
+        // block, when it holds earlier blocks' sums).  S_t of this block was
+        // issued after the last P_t V, so O_t has no product in flight until
+        // P_t is signalled.
+        if (n > 0 && __any_sync(0xffffffffu, raise)) {
+          const float f = raise ? corr : 1.f;
+#pragma unroll 1
+          for (int c = 0; c < kD; c += 32) {
+            uint32_t o[32];
+            ptx::tmem_ld_32x32b_x32(o_addr + c, o);
+            ptx::tmem_ld_wait();
+#pragma unroll
+            for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * f);
+            ptx::tmem_st_32x32b_x32(o_addr + c, o);
+          }
         }
       }
       ptx::tmem_st_wait();                      // P_t (and a rescaled O_t) in place
