@@ -111,3 +111,24 @@ def test_ring_attention_growing_scores_rescale(causal):
     ref = oracle.ring_attention(Q, K, V, causal)
     for r in range(R):
         assert_close(to_f64(O[r]).reshape(-1, d), ref[r].reshape(-1, d), f"rank {r}")
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_ring_attention_mixed_rescale_within_a_warp(causal):
+    """The same growing keys, but query row i is (0, 1/2, 1 or 2 by i mod 4)
+    times ones: neighbouring rows of one warp raise their maximum every
+    block, every second or fourth block, or never, so blocks where only some
+    rows of a warp need a raise are redone while the others keep theirs."""
+    R, S, H, d = 2, 640, 2, 128
+    _, _, V = synth.attention_inputs(R, S, H, d, seed=13)
+    gain = np.array([0.0, 0.5, 1.0, 2.0], np.float32)[np.arange(S) % 4]
+    Q = [synth.f32_to_bf16_bits(np.broadcast_to(gain[:, None, None], (S, H, d)).astype(np.float32))
+         for _ in range(R)]
+    K = []
+    for r in range(R):
+        j = (r * S + np.arange(S, dtype=np.float32))[:, None, None]
+        K.append(synth.f32_to_bf16_bits(np.broadcast_to(0.002 * j, (S, H, d)).astype(np.float32)))
+    O = _run(Q, K, V, causal, fcc.FCC_F32)
+    ref = oracle.ring_attention(Q, K, V, causal)
+    for r in range(R):
+        assert_close(to_f64(O[r]).reshape(-1, d), ref[r].reshape(-1, d), f"rank {r}")
